@@ -1,0 +1,373 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Nothing here calls the CUDA library.  The oracle is checked against
+hand-worked examples (tests/golden), an independent brute-force formulation
+(tests/bruteforce.py), closed forms and invariants.
+"""
+import json
+import os
+import random
+from fractions import Fraction
+
+import numpy as np
+import pytest
+
+from bruteforce import brute_propose, brute_suffix_array
+
+GOLDEN = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "worked_examples.json")))
+
+
+def _params(orc, case, corpus=False):
+    pr = dict(S=1000, V=100, k=8, D=24, R=64, factor=(1, 1), offset=0, min_prob=(1, 10),
+              depth_sum_cap=False)
+    for key, val in case.get("params", {}).items():
+        pr[key] = tuple(val) if isinstance(val, list) else val
+    return orc.Params(**pr), pr
+
+
+@pytest.mark.parametrize("case", GOLDEN["cases"], ids=lambda c: c["name"])
+def test_worked_example(orc, case):
+    p, pr = _params(orc, case)
+    t = case["t"]
+    X = case.get("X")
+    r = orc.propose_row(p, t, len(t), X=X, active=case.get("active", True))
+    exp = case["expect"]
+    L = len(exp["drafts"])
+    assert r.num_valid == L
+    assert r.drafts[:L].tolist() == exp["drafts"]
+    assert (r.drafts[L:] == -1).all()
+    assert r.match_info.tolist() == [exp["M"], exp["source"]]
+    want_score = np.float32(Fraction(*exp["score"]))
+    assert np.float32(r.score) == want_score
+    for d, (a, b) in enumerate(exp["probs"]):
+        assert r.probs[d] == np.float32(Fraction(a, b))
+    assert (r.probs[L:] == 0).all()
+
+
+@pytest.mark.parametrize("case", GOLDEN["suffix_arrays"], ids=lambda c: c["name"])
+def test_suffix_array_examples(orc, case):
+    assert orc.suffix_array(case["X"]).tolist() == case["SA"]
+    assert orc.check_suffix_array(case["X"], case["SA"]) == 0
+
+
+@pytest.mark.parametrize("case", GOLDEN["updates"], ids=lambda c: c["name"])
+def test_update_examples(orc, case):
+    row = np.array([case["row"]], dtype=np.int32)
+    n = np.array([case["n"]], dtype=np.int32)
+    f = orc.update_state(row, n, np.array([case["sampled"]], dtype=np.int32), case["V"])
+    assert row[0].tolist() == case["expect_row"]
+    assert int(n[0]) == case["expect_n"]
+    assert f == case["expect_flags"]
+
+
+@pytest.mark.parametrize("case", GOLDEN["rings"], ids=lambda c: c["name"])
+def test_ring_examples(orc, case):
+    docs = case["docs"]
+    width = max(1, max(len(d) for d in docs))
+    buf = np.full((len(docs), width), -1, dtype=np.int32)
+    for i, d in enumerate(docs):
+        buf[i, :len(d)] = d
+    ring = orc.Ring(case["C"], case["max_docs"], case["V"])
+    f = ring.ingest(buf, np.arange(len(docs)), np.zeros(len(docs)), [len(d) for d in docs])
+    assert f == case["expect_flags"]
+    assert ring.live == case["expect_live"]
+    assert ring.snapshot().tolist() == case["expect_snapshot"]
+
+
+# --------------------------------------------------------------------------
+# brute force over every suffix length and every occurrence
+
+def _rand_params(rng):
+    k = rng.randint(1, 10)
+    D = rng.randint(1, 9)
+    factor = rng.choice([(1, 1), (2, 1), (1, 2), (3, 2), (0, 1)])
+    offset = rng.choice([0, 0, 1, 2])
+    min_prob = rng.choice([(0, 1), (1, 10), (1, 4), (1, 3), (1, 2), (2, 3), (1, 1)])
+    return k, D, factor, offset, min_prob
+
+
+def _compare(orc, t, n, S, V, k, D, R, factor, offset, min_prob, X=None, dsc=False):
+    p = orc.Params(S=S, V=V, k=k, D=D, R=R if R is not None else 4096, factor=factor,
+                   offset=offset, min_prob=min_prob, depth_sum_cap=dsc)
+    r = orc.propose_row(p, np.asarray(t, dtype=np.int32), n, X=X)
+    b = brute_propose(t, n, k, D, R, S, factor, offset, min_prob, X=X, Z=V, depth_sum_cap=dsc)
+    ctx = dict(t=list(t[:n]), X=None if X is None else list(X), k=k, D=D, R=R, S=S,
+               factor=factor, offset=offset, min_prob=min_prob)
+    assert r.match_info.tolist() == [b.M, b.source], ctx
+    assert r.num_valid == len(b.drafts), ctx
+    assert r.drafts[:r.num_valid].tolist() == b.drafts, ctx
+    assert (r.drafts[r.num_valid:] == -1).all()
+    assert np.float32(r.score) == np.float32(b.score), ctx
+    for d, pr in enumerate(b.probs):
+        assert r.probs[d] == np.float32(pr), ctx
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_self_vs_bruteforce_unbounded(orc, seed):
+    rng = random.Random(1000 + seed)
+    for _ in range(150):
+        V = rng.choice([2, 3, 4])
+        n = rng.randint(0, 48)
+        S = n + rng.choice([0, 1, 2, 5, 40])
+        t = [rng.randrange(V) for _ in range(n)]
+        k, D, factor, offset, min_prob = _rand_params(rng)
+        _compare(orc, t, n, S, V, k, D, None, factor, offset, min_prob,
+                 dsc=rng.random() < 0.2)
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_self_vs_bruteforce_budget(orc, seed):
+    rng = random.Random(2000 + seed)
+    for _ in range(150):
+        V = rng.choice([2, 3])
+        n = rng.randint(2, 48)
+        S = n + 40
+        t = [rng.randrange(V) for _ in range(n)]
+        k, D, factor, offset, min_prob = _rand_params(rng)
+        R = rng.randint(1, 4)
+        _compare(orc, t, n, S, V, k, D, R, factor, offset, min_prob)
+
+
+def _rand_corpus(rng, V, ndocs, maxlen):
+    X = []
+    for _ in range(ndocs):
+        L = rng.randint(1, maxlen)
+        X += [rng.randrange(V) for _ in range(L)] + [V]
+    return X
+
+
+@pytest.mark.parametrize("seed", range(4))
+def test_corpus_vs_bruteforce(orc, seed):
+    rng = random.Random(3000 + seed)
+    for _ in range(120):
+        V = rng.choice([2, 3, 4])
+        n = rng.randint(0, 24)
+        S = n + rng.choice([1, 3, 40])
+        t = [rng.randrange(V) for _ in range(n)]
+        X = _rand_corpus(rng, V, rng.randint(1, 6), 12)
+        k, D, factor, offset, min_prob = _rand_params(rng)
+        R = rng.choice([None, None, 1, 2, 3])
+        _compare(orc, t, n, S, V, k, D, R, factor, offset, min_prob, X=X)
+
+
+def test_corpus_match_scan_vs_substrings(orc):
+    """Mc and its occurrence set against a naive search over all lengths."""
+    rng = random.Random(77)
+    from bruteforce import ends_of
+    for _ in range(400):
+        V = rng.choice([2, 3])
+        X = _rand_corpus(rng, V, rng.randint(1, 5), 10)
+        n = rng.randint(0, 12)
+        t = [rng.randrange(V) for _ in range(n)]
+        D = rng.randint(1, 8)
+        R = rng.randint(1, 6)
+        M, occ = orc.corpus_match(X, V, t, n, D, R)
+        best = 0
+        ends = []
+        if D >= 2 and n >= 2:
+            for l in range(min(D, n), 1, -1):
+                es = [e for e in ends_of(X, t[n - l:]) if e + 1 < len(X) and X[e + 1] != V]
+                if es:
+                    best, ends = l, sorted(es, reverse=True)[:R]
+                    break
+        assert M == best
+        assert occ.tolist() == ends
+
+
+def test_self_match_occurrences_vs_substrings(orc):
+    rng = random.Random(78)
+    from bruteforce import ends_of
+    for _ in range(400):
+        V = rng.choice([2, 3])
+        n = rng.randint(0, 30)
+        t = [rng.randrange(V) for _ in range(n)]
+        D = rng.randint(1, 10)
+        R = rng.randint(1, 6)
+        M, occ = orc.self_match(t, n, D, R)
+        best, ends = 0, []
+        for l in range(min(D, n - 1), 0, -1):
+            es = [e for e in ends_of(t, t[n - l:]) if e <= n - 2]
+            if es:
+                best, ends = l, sorted(es, reverse=True)[:R]
+                break
+        assert M == best
+        assert occ.tolist() == ends
+
+
+# --------------------------------------------------------------------------
+# closed forms
+
+@pytest.mark.parametrize("p,n,D,k", [(3, 40, 8, 8), (2, 31, 6, 10), (5, 64, 7, 16),
+                                     (4, 9, 8, 8), (7, 10, 24, 16), (1, 20, 5, 8)])
+def test_periodic_closed_form(orc, p, n, D, k):
+    """A period-p text: if n - p >= D then M = D, the draft continues the period,
+    and depth d keeps c0 - floor(d / p) survivors (occurrences run off the end
+    one period at a time); otherwise M = n - p with one occurrence."""
+    base = list(range(10, 10 + p))
+    t = [base[i % p] for i in range(n)]
+    S = 10 * n
+    prm = orc.Params(S=S, V=100, k=k, D=D, R=4096, factor=(100, 1), offset=0, min_prob=(0, 1))
+    r = orc.propose_row(prm, t, n)
+    if n - p >= D:
+        M = D
+        # ends j <= n-2 with j = n-1 (mod p) and j >= D-1
+        occ = [j for j in range(D - 1, n - 1) if (j - (n - 1)) % p == 0]
+        c0 = len(occ)
+        L = k
+        exp_probs = [Fraction(c0 - d // p, c0) for d in range(L)]
+        assert r.match_info.tolist() == [M, 1]
+        assert r.num_valid == L
+        assert r.drafts.tolist() == [t[(n + d) % p] if False else base[(n + d) % p] for d in range(L)]
+        for d in range(L):
+            assert r.probs[d] == np.float32(exp_probs[d])
+    else:
+        M = n - p
+        assert r.match_info.tolist() == [M, 1 if M > 0 else 0]
+        if M > 0:
+            L = min(k, p, S - n - 1)
+            assert r.num_valid == L
+            assert r.drafts[:L].tolist() == [base[(n + d) % p] for d in range(L)]
+
+
+def test_all_distinct_and_short(orc):
+    prm = orc.Params(S=100, V=1000, k=8, D=24, R=64)
+    r = orc.propose_row(prm, list(range(50)), 50)
+    assert r.num_valid == 0 and r.match_info.tolist() == [0, 0]
+    for n in (0, 1):
+        r = orc.propose_row(prm, [3, 3], n)
+        assert r.num_valid == 0
+
+
+def test_no_room_near_capacity(orc):
+    t = [1, 2] * 10
+    for S, want in ((20, 0), (21, 0), (22, 1), (23, 2)):
+        prm = orc.Params(S=S, V=10, k=8, D=24, R=64, factor=(10, 1))
+        r = orc.propose_row(prm, t, 20)
+        assert r.num_valid == want
+
+
+# --------------------------------------------------------------------------
+# suffix array
+
+def test_suffix_array_vs_python_sort(orc):
+    rng = random.Random(5)
+    for _ in range(300):
+        N = rng.randint(0, 60)
+        V = rng.choice([1, 2, 3, 50])
+        X = [rng.randrange(V) - (1 if rng.random() < 0.1 else 0) for _ in range(N)]
+        sa = orc.suffix_array(X)
+        assert sa.tolist() == brute_suffix_array(X)
+        assert orc.check_suffix_array(X, sa) == 0
+
+
+def test_suffix_array_checker_rejects(orc):
+    X = [3, 1, 2, 1, 2, 100]
+    good = brute_suffix_array(X)
+    assert orc.check_suffix_array(X, good) == 0
+    bad = list(good)
+    bad[1], bad[2] = bad[2], bad[1]
+    assert orc.check_suffix_array(X, bad) != 0
+    dup = list(good)
+    dup[0] = dup[1]
+    assert orc.check_suffix_array(X, dup) != 0
+
+
+def test_suffix_array_large_sorted(orc):
+    rng = np.random.default_rng(3)
+    X = rng.integers(0, 4, size=20000).astype(np.int32)
+    X[rng.integers(0, 20000, size=200)] = 4
+    X[-1] = 4
+    sa = orc.suffix_array(X)
+    assert orc.check_suffix_array(X, sa) == 0
+
+
+# --------------------------------------------------------------------------
+# ring and update
+
+def test_ring_vs_fifo_model(orc):
+    """The ring holds the newest docs whose tokens + sentinels fit in C."""
+    rng = random.Random(9)
+    for _ in range(50):
+        C = rng.randint(5, 60)
+        max_docs = rng.randint(1, 8)
+        ring = orc.Ring(C, max_docs, 50)
+        model = []
+        for _step in range(20):
+            m = rng.randint(0, 4)
+            docs = [[rng.randrange(50) for _ in range(rng.randint(0, 15))] for _ in range(m)]
+            if m == 0:
+                continue
+            width = max(1, max(len(d) for d in docs))
+            buf = np.full((m, width), -1, dtype=np.int32)
+            for i, d in enumerate(docs):
+                buf[i, :len(d)] = d
+            ring.ingest(buf, np.arange(m), np.zeros(m), [len(d) for d in docs])
+            for d in docs:
+                if len(d) == 0 or len(d) + 1 > C:
+                    continue
+                model.append(d)
+                while sum(len(x) + 1 for x in model) > C or len(model) > max_docs:
+                    model.pop(0)
+            snap = []
+            for d in model:
+                snap += d + [50]
+            assert ring.snapshot().tolist() == snap
+            assert ring.live == len(snap) <= C
+            assert ring.ndocs == len(model)
+
+
+def test_ring_rejects_bad_args(orc):
+    ring = orc.Ring(100, 8, 50)
+    buf = np.array([[1, 2, 3, 4]], dtype=np.int32)
+    assert ring.ingest(buf, [1], [0], [2]) == orc.ERR_DOC_ARGS        # row out of range
+    assert ring.ingest(buf, [0], [3], [2]) == orc.ERR_DOC_ARGS        # past the row
+    assert ring.ingest(buf, [0], [-1], [2]) == orc.ERR_DOC_ARGS
+    assert ring.ingest(buf, [0], [0], [3], num_tokens=[2]) == orc.ERR_DOC_ARGS
+    assert ring.live == 0
+    assert ring.ingest(buf, [0], [1], [2], num_tokens=[4]) == 0
+    assert ring.snapshot().tolist() == [2, 3, 50]
+
+
+def test_update_batch(orc):
+    rng = np.random.default_rng(1)
+    B, S, T, V = 8, 32, 5, 20
+    tok = np.full((B, S), -1, dtype=np.int32)
+    n = rng.integers(0, S + 1, size=B).astype(np.int32)
+    for b in range(B):
+        tok[b, :n[b]] = rng.integers(0, V, size=n[b])
+    sampled = rng.integers(-1, V, size=(B, T)).astype(np.int32)
+    tok0, n0 = tok.copy(), n.copy()
+    orc.update_state(tok, n, sampled, V)
+    for b in range(B):
+        c = 0
+        while c < T and 0 <= sampled[b, c] < V:
+            c += 1
+        assert n[b] == min(S, n0[b] + c)
+        assert tok[b, :n0[b]].tolist() == tok0[b, :n0[b]].tolist()
+        assert tok[b, n0[b]:n[b]].tolist() == sampled[b, :n[b] - n0[b]].tolist()
+        assert (tok[b, n[b]:] == tok0[b, n[b]:]).all()
+
+
+def test_invariants_random_rows(orc):
+    """num_valid <= cap, -1 padding, non-increasing probs >= min_prob, score = sum."""
+    rng = np.random.default_rng(11)
+    for _ in range(200):
+        V = int(rng.integers(2, 6))
+        n = int(rng.integers(0, 80))
+        t = rng.integers(0, V, size=n).astype(np.int32)
+        k = int(rng.integers(1, 12))
+        prm = orc.Params(S=n + 30, V=V, k=k, D=int(rng.integers(1, 12)), R=int(rng.integers(1, 9)),
+                         min_prob=(1, 5))
+        r = orc.propose_row(prm, t, n)
+        L = r.num_valid
+        assert 0 <= L <= k
+        assert (r.drafts[L:] == -1).all() and (r.drafts[:L] >= 0).all()
+        pr = r.probs[:L]
+        assert (np.diff(pr) <= 0).all()
+        assert (pr >= np.float32(0.2) - 1e-7).all()
+        assert abs(float(r.score) - float(pr.astype(np.float64).sum())) < 1e-5
+        if L:
+            M = r.match_info[0]
+            W = list(t[n - M:]) + r.drafts[:L].tolist()
+            s = "," + ",".join(map(str, t.tolist())) + ","
+            assert ("," + ",".join(map(str, W)) + ",") in s
