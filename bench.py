@@ -1,0 +1,461 @@
+#!/usr/bin/env python
+"""Benchmark of the GPU-resident suffix-decoding drafter.
+
+Metric: propose steps/s and us/step at B=256, S=4096 (one step = the whole
+drafting path on one batch: update + self match + corpus probe + expansion,
+the ingest of the rows that finish in that step, the background suffix-array
+rebuild policy and the swap poll), plus suffix-array build Mtok/s and the HBM
+GB/s of the dominant kernel against the measured copy bandwidth.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Under torchrun every rank runs an independent replica of the workload on its
+own GPU (rows shard across GPUs; there is no data-path collective); rank 0
+prints one JSON line.  `--impl reference` times the CPU oracle instead.
+"""
+from __future__ import annotations
+
+import argparse
+import dataclasses
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "propose steps/s & µs/step at B=256,S=4096; SA build Mtok/s; HBM GB/s"
+WORKLOAD = ("c3 serving loop: B=256 rows, S=4096 int32, vocab 151936 (Zipf 1.1 fresh tokens, "
+            "p=0.5 repeats from 256 spans of 16-128), num_tokens U[1024,4096], k=16, "
+            "max_tree_depth=24, max_occurrences=64, T=17 sampled ids (U[1,17] accepted), "
+            "1M-token corpus ring prefilled with 64-512-token responses; per step 5% of rows "
+            "finish and are ingested, a side-stream rebuild starts once 2^16 tokens arrived")
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ---------------------------------------------------------------------------
+class Clocks:
+    """nvidia-smi samples of SM clocks and throttle reasons during a region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        os.unlink(self.path)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------
+def make_steps(cfg, seed, n_steps):
+    from model_free_suffix_gb300 import workload as W
+    tr = W.ServingTrace(cfg, seed=seed, steps=n_steps)
+    tok, n = tr.initial()
+    steps = [tr.next_step() for _ in range(n_steps)]
+    return tr, tok, n, steps
+
+
+def algorithmic_bytes_propose(sum_n, B, T, k, N):
+    """Bytes one propose_with_update launch must touch (lower bound):
+    every valid token of every row once, the sampled ids, the outputs, and the
+    sectors of two suffix-array binary searches per row."""
+    probe = 0 if N <= 0 else B * 2 * int(np.ceil(np.log2(N + 1))) * 2 * 32
+    return 4 * sum_n + 4 * B * T + B * (8 * k + 16) + probe
+
+
+def run_ours(args, rank, world):
+    import torch
+    from model_free_suffix_gb300 import SuffixDrafter
+    from model_free_suffix_gb300 import workload as W
+
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+    cfg = W.CONFIGS[args.config]
+    K, Wm = args.steps, args.warmup
+    n_steps = K + Wm
+    tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=2 * n_steps)
+    dr = SuffixDrafter(max_batch=cfg.B, seq_capacity=cfg.S, vocab_size=cfg.V, k=cfg.k,
+                       max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
+                       max_spec_factor=cfg.factor, max_spec_offset=cfg.offset,
+                       min_token_prob=cfg.min_prob, corpus_capacity=cfg.corpus_tokens,
+                       device=dev.index)
+    stream = torch.cuda.current_stream(dev)
+    side = torch.cuda.Stream(device=dev, priority=0)
+    # corpus prefill (setup, untimed)
+    docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
+    for s0 in range(0, docs.shape[0], 2048):
+        d = docs[s0:s0 + 2048]
+        m = d.shape[0]
+        buf = torch.full((m, cfg.S), -1, dtype=torch.int32, device=dev)
+        buf[:, :d.shape[1]] = torch.from_numpy(d).to(dev)
+        dr.ingest(buf, torch.arange(m, dtype=torch.int32, device=dev),
+                  torch.zeros(m, dtype=torch.int32, device=dev),
+                  torch.from_numpy(np.ascontiguousarray(lens[s0:s0 + 2048])).to(dev))
+    dr.build_sa(side)
+    assert dr.poll(wait=True)[0] == 1
+
+    g_tok = torch.from_numpy(tok).to(dev)
+    g_n = torch.from_numpy(n).to(dev)
+    out = dr.new_outputs(cfg.B)
+    samp = [torch.from_numpy(s.sampled).to(dev) for s in steps]
+    fin = [(torch.from_numpy(s.finished).to(dev), torch.from_numpy(s.ingest_starts).to(dev),
+            torch.from_numpy(s.ingest_lengths).to(dev), int(s.ingest_lengths.sum()),
+            torch.from_numpy(s.finished.astype(np.int64)).to(dev),
+            torch.from_numpy(s.reset_tokens).to(dev), torch.from_numpy(s.reset_n).to(dev))
+           for s in steps]
+    props = torch.cuda.get_device_properties(dev)
+    l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
+    flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
+    state = {"pending": False, "ingested": 0, "swaps": 0, "builds": 0}
+
+    def one_step(i, ev=None):
+        if i > 0:  # the previous step's finished rows restart (workload bookkeeping)
+            _, _, _, _, idx, rt, rn = fin[i - 1]
+            if idx.numel():
+                g_tok[idx] = rt
+                g_n[idx] = rn
+        flush.fill_(i)
+        if ev:
+            ev[0].record(stream)
+        dr.propose_with_update(g_tok, g_n, samp[i], out=out)
+        if ev:
+            ev[1].record(stream)
+        rows, st_, ln, tot, _, _, _ = fin[i]
+        if rows.numel():
+            dr.ingest(g_tok, rows, st_, ln, num_tokens=g_n)
+            state["ingested"] += tot
+        if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
+            dr.build_sa(side)
+            state["pending"] = True
+            state["ingested"] = 0
+            state["builds"] += 1
+        st, _ = dr.poll(wait=False)
+        if st == 1:
+            state["pending"] = False
+            state["swaps"] += 1
+        if ev:
+            ev[2].record(stream)
+
+    for i in range(Wm):
+        one_step(i)
+    torch.cuda.synchronize()
+    barrier(world)
+    torch.cuda.synchronize()
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    sum_n = []
+    l0 = dr.launch_count()
+    clk = Clocks(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
+    clk.start()
+    b0 = state["builds"]
+    t_wall = time.perf_counter()
+    for j in range(K):
+        one_step(Wm + j, evs[j])
+    torch.cuda.synchronize()
+    t_wall = time.perf_counter() - t_wall
+    clocks = clk.stop()
+    barrier(world)
+    torch.cuda.synchronize()
+    launches = dr.launch_count() - l0
+    step_ms = [e[0].elapsed_time(e[2]) for e in evs]
+    prop_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    total_ms = float(np.sum(step_ms))
+    total_ms_max = allreduce_max(total_ms, world)
+    builds_in_region = state["builds"] - b0
+    # final num_tokens -> algorithmic bytes of a propose launch (mean over the region)
+    n_final = int(g_n.sum().item())
+    sum_n_est = n_final
+    # e2e: host buffers through the public API, copies inside the timed region
+    e2e = e2e_leg(args, dr, cfg, steps, Wm + K, K, g_tok, g_n, out, flush, side, state, dev)
+    # suffix-array builds, standalone (C4 workload)
+    sa = sa_build_leg(args, dev)
+    peak, peak_kind = peaks()
+    byts = algorithmic_bytes_propose(sum_n_est, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens)
+    prop_avg_s = float(np.mean(prop_ms)) / 1e3
+    ach = byts / prop_avg_s / 1e9
+    rl_prop = {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 2),
+               "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": None,
+               "bytes_per_launch": int(byts), "avg_launch_us": round(prop_avg_s * 1e6, 2),
+               "peak_kind": peak_kind}
+    dr.close()
+    value = world * K / (total_ms_max / 1e3)
+    res = {
+        "metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world,
+        "steps": K, "warmup": Wm, "ms_per_step": round(total_ms_max / K, 5),
+        "us_per_step": round(1e3 * total_ms_max / K, 2),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD, "B": cfg.B, "S": cfg.S, "k": cfg.k, "D": cfg.D,
+                   "R": cfg.R, "T": cfg.T, "corpus_tokens": cfg.corpus_tokens,
+                   "rebuild_tokens": cfg.rebuild_tokens,
+                   "l2": "flushed before every timed step (%d MiB write)" % (flush.numel() * 4 >> 20),
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "roofline": rl_prop,
+        "propose_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
+                       "median": round(1e3 * float(np.median(prop_ms)), 2)},
+        "builds_in_timed_region": builds_in_region, "swaps": state["swaps"],
+        "wall_s_timed_region": round(t_wall, 4),
+        "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks, "sa_build": sa,
+    }
+    return res
+
+
+def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state, dev):
+    """Same steps through the public API with pinned host buffers: each step
+    copies its sampled ids (and ingest arguments) host->device and reads the
+    drafts and valid counts back, all inside the timed region."""
+    import torch
+    n_avail = len(steps) - first
+    K = min(K, n_avail)
+    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
+    h_samp = [pin(steps[first + j].sampled) for j in range(K)]
+    h_fin = [(pin(steps[first + j].finished), pin(steps[first + j].ingest_starts),
+              pin(steps[first + j].ingest_lengths)) for j in range(K)]
+    d_samp = torch.empty((cfg.B, cfg.T), dtype=torch.int32, device=dev)
+    m_max = max(1, max(x[0].numel() for x in h_fin))
+    d_rows = torch.empty(m_max, dtype=torch.int32, device=dev)
+    d_st = torch.empty(m_max, dtype=torch.int32, device=dev)
+    d_ln = torch.empty(m_max, dtype=torch.int32, device=dev)
+    h_drafts = torch.empty((cfg.B, cfg.k), dtype=torch.int32).pin_memory()
+    h_nv = torch.empty(cfg.B, dtype=torch.int32).pin_memory()
+    stream = torch.cuda.current_stream(dev)
+    times = []
+    bi = bo = 0
+    for j in range(K):
+        s = steps[first + j]
+        if first + j > 0:
+            p = steps[first + j - 1]
+            if p.finished.shape[0]:
+                idx = torch.from_numpy(p.finished.astype(np.int64)).to(dev)
+                g_tok[idx] = torch.from_numpy(p.reset_tokens).to(dev)
+                g_n[idx] = torch.from_numpy(p.reset_n).to(dev)
+        flush.fill_(j)
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        d_samp.copy_(h_samp[j], non_blocking=True)
+        m = h_fin[j][0].numel()
+        if m:
+            d_rows[:m].copy_(h_fin[j][0], non_blocking=True)
+            d_st[:m].copy_(h_fin[j][1], non_blocking=True)
+            d_ln[:m].copy_(h_fin[j][2], non_blocking=True)
+        dr.propose_with_update(g_tok, g_n, d_samp, out=out)
+        if m:
+            dr.ingest(g_tok, d_rows[:m], d_st[:m], d_ln[:m], num_tokens=g_n)
+            state["ingested"] += int(s.ingest_lengths.sum())
+        if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
+            dr.build_sa(side)
+            state["pending"] = True
+            state["ingested"] = 0
+        st, _ = dr.poll(wait=False)
+        if st == 1:
+            state["pending"] = False
+        h_drafts.copy_(out.drafts, non_blocking=True)
+        h_nv.copy_(out.num_valid, non_blocking=True)
+        stream.synchronize()
+        times.append(time.perf_counter() - t0)
+        bi = h_samp[j].numel() * 4 + 3 * m * 4
+        bo = h_drafts.numel() * 4 + h_nv.numel() * 4
+    if state["pending"]:
+        dr.poll(wait=True)
+        state["pending"] = False
+    tot = float(np.sum(times))
+    return {"value": round(K / tot, 2), "unit": "steps/s", "h2d_bytes_per_step": int(bi),
+            "d2h_bytes_per_step": int(bo), "us_per_step": round(1e6 * tot / K, 2), "steps": K}
+
+
+def sa_build_leg(args, dev):
+    """Standalone suffix-array builds of the suffix-array workload (1M and 16M)."""
+    import torch
+    from model_free_suffix_gb300 import SuffixDrafter
+    from model_free_suffix_gb300 import workload as W
+    peak, peak_kind = peaks()
+    out = {}
+    sizes = [1 << 20] + ([] if args.no_sa16m else [1 << 24])
+    for N in sizes:
+        X = torch.from_numpy(W.sa_corpus(N, seed=0)).to(dev)
+        dr = SuffixDrafter(max_batch=1, seq_capacity=8, vocab_size=151936, corpus_capacity=N,
+                           device=dev.index)
+        sa = torch.empty(N, dtype=torch.int32, device=dev)
+        runs = []
+        for r in range(3 if N <= 1 << 20 else 2):
+            dr.suffix_array(X, out=sa)
+            runs.append(dr.build_stats())
+        best = min(runs, key=lambda s: s["ms"])
+        pass_bytes = 24 * best["pass_elems"]
+        r_pass = pass_bytes / (best["pass_ms"] / 1e3) / 1e9 if best["pass_ms"] > 0 else None
+        r_all = best["model_bytes"] / (best["ms"] / 1e3) / 1e9
+        out["%dM" % (N >> 20)] = {
+            "n": N, "ms": round(best["ms"], 3), "mtok_s": round(N / best["ms"] / 1e3, 1),
+            "rounds": best["rounds"], "passes": best["passes"],
+            "sorted_elems": best["sorted_elems"],
+            "model_gbs": round(r_all, 1), "model_frac": round(r_all / peak, 4),
+            "radix_pass": {"bound": "hbm", "achieved": None if r_pass is None else round(r_pass, 1),
+                           "peak": peak, "unit": "GB/s",
+                           "frac": None if r_pass is None else round(r_pass / peak, 4),
+                           "avg_launch_us": round(1e3 * best["pass_ms"] / max(1, best["passes"]), 2),
+                           "peak_kind": peak_kind},
+        }
+        dr.close()
+        del X, sa
+        torch.cuda.empty_cache()
+    return out
+
+
+# ---------------------------------------------------------------------------
+def cpu_oracle_leg(cfg, seconds, rank=0):
+    """The CPU oracle as it stands, on the same workload, rows spread over all
+    host cores; a bounded sample of steps."""
+    from oracle import oracle as O
+    from model_free_suffix_gb300 import workload as W
+    O.build()
+    threads = os.cpu_count() or 1
+    tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=64)
+    docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
+    ring = O.Ring(cfg.corpus_tokens, 65536, cfg.V)
+    buf = np.full((docs.shape[0], cfg.S), -1, dtype=np.int32)
+    buf[:, :docs.shape[1]] = docs
+    ring.ingest(buf, np.arange(docs.shape[0]), np.zeros(docs.shape[0]), lens)
+    X = ring.snapshot()
+    p = O.Params(S=cfg.S, V=cfg.V, k=cfg.k, D=cfg.D, R=cfg.R, factor=cfg.factor,
+                 offset=cfg.offset, min_prob=cfg.min_prob)
+    done = 0
+    t0 = time.perf_counter()
+    while done < len(steps):
+        s = steps[done]
+        O.update_state(tok, n, s.sampled, cfg.V)
+        O.propose(p, tok, n, X=X, threads=threads)
+        if s.finished.shape[0]:
+            ring.ingest(tok, s.finished, s.ingest_starts, s.ingest_lengths, num_tokens=n)
+            for i, b in enumerate(s.finished):
+                tok[b] = s.reset_tokens[i]
+                n[b] = s.reset_n[i]
+        done += 1
+        if time.perf_counter() - t0 >= seconds:
+            break
+    el = time.perf_counter() - t0
+    return {"value": round(done / el, 3), "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "sample": "%d steps of the same workload (update + propose of all %d rows + ingest; "
+                      "no suffix-array rebuild in the sample), %.1f s" % (done, cfg.B, el)}
+
+
+# ---------------------------------------------------------------------------
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def allreduce_max(x, world):
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64,
+                     device="cuda" if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", default="c3")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--no-sa16m", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        dist.init_process_group(backend="nccl" if torch.cuda.is_available() else "gloo")
+    from model_free_suffix_gb300 import workload as W
+    cfg = W.CONFIGS[args.config]
+    if args.impl == "reference":
+        if rank == 0:
+            cb = cpu_oracle_leg(cfg, args.cpu_seconds)
+            res = {"metric": METRIC, "value": cb["value"], "unit": "steps/s", "n_gpus": world,
+                   "steps": args.steps, "warmup": args.warmup,
+                   "ms_per_step": round(1e3 / cb["value"], 3), "higher_is_better": True,
+                   "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+                   "config": {"workload": WORKLOAD, "B": cfg.B, "S": cfg.S},
+                   "impl": "reference", "cpu_baseline": cb,
+                   "e2e": {"value": cb["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
+                           "d2h_bytes_per_step": 0}}
+            print(json.dumps(res), flush=True)
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return
+    from __graft_entry__ import build
+    build()
+    res = run_ours(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            res["cpu_baseline"] = cpu_oracle_leg(cfg, args.cpu_seconds)
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

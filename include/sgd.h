@@ -1,0 +1,246 @@
+/*
+ * sgd.h -- C ABI of the GPU-resident suffix-decoding drafter (libsgd).
+ *
+ * One library context per GPU.  All drafting work runs in hand-written CUDA
+ * kernels for sm_103a on streams the caller passes; no call on the drafting
+ * path synchronises with the host, allocates memory or changes a device
+ * address, so sgd_update_state / sgd_propose / sgd_propose_with_update /
+ * sgd_ingest can be captured in a CUDA graph.
+ *
+ * Sources (page title, section):
+ *   [RFC]  "Suffix decoding on GPU (suffix_gpu)", vLLM issue: Summary, Design.
+ *   [PYPI] "SuffixGPU" (suffix-gpu 0.1.1 on PyPI): Highlights, Quickstart,
+ *          How it works (steps 1-4), References.
+ *   [DOCS] "Suffix Decoding" (vLLM docs): Model Runner V2.
+ *   [BLOG] "vLLM Suffix Decoding 投机解码实战": section 4 (knob defaults),
+ *          section 5 (proposer flow).
+ *
+ * Conventions for every entry point below:
+ *   - Return value: an SGD_* status.  Negative values are errors detected on
+ *     the host before anything was enqueued (nothing ran), or a CUDA error.
+ *   - Pointers marked DEVICE are caller-owned device memory of the context's
+ *     GPU; the library never frees or keeps them past the call's stream work.
+ *     Token buffers must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ *   - Problems found on the device (bad token ids, out-of-range lengths) are
+ *     never traps: they set bits in a sticky device word (SGD_ERR_*), read by
+ *     sgd_get_error, and the offending id or document is treated as a stop.
+ *   - A context is not thread-safe: call it from one host thread at a time.
+ */
+#ifndef SGD_H
+#define SGD_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------ */
+#define SGD_OK          0   /* done (sgd_poll: nothing new to swap in)          */
+#define SGD_OK_SWAPPED  1   /* sgd_poll: a finished suffix array is now current */
+#define SGD_PENDING     2   /* sgd_poll: a build is still running               */
+#define SGD_EINVAL     -1   /* bad argument (sizes, alignment, NULL)            */
+#define SGD_ECUDA      -2   /* a CUDA runtime call failed                       */
+#define SGD_ENOMEM     -3   /* device or host allocation failed in sgd_create   */
+#define SGD_ETIMEDOUT  -4   /* sgd_poll(wait=1) ran out of time                 */
+#define SGD_EBUSY      -5   /* a build is in flight or not yet swapped in       */
+#define SGD_EBUILD     -6   /* the finished build reported failure; old index kept */
+#define SGD_ENOCORPUS  -7   /* the context was created without a corpus         */
+
+/* ---- sticky device error bits (sgd_get_error) --------------------------- */
+#define SGD_ERR_SAMPLED_TOKEN 0x1u  /* a sampled id >= V ended the accepted prefix    */
+#define SGD_ERR_NUM_TOKENS    0x2u  /* num_tokens outside [0, S]; clamped             */
+#define SGD_ERR_DOC_ARGS      0x4u  /* ingest: bad row/start/length; doc skipped      */
+#define SGD_ERR_DOC_TOKEN     0x8u  /* ingest: token outside [0, V); doc truncated    */
+#define SGD_ERR_DOC_TOO_LONG  0x10u /* ingest: doc + sentinel exceeds the ring; skipped */
+#define SGD_ERR_LOOKBACK      0x20u /* suffix sort: a radix look-back gave up waiting */
+
+typedef struct sgd_ctx sgd_ctx; /* opaque, library-owned */
+
+/* Knobs.  Defaults (sgd_config_default) follow [BLOG] section 4 and
+ * [DOCS] Model Runner V2: max_tree_depth 24, max_spec_factor 1.0,
+ * min_token_prob 0.1, offset 0, corpus of 2^20 tokens; k = 16 and
+ * max_occurrences = 64.  Floating knobs are kept as rationals so that every
+ * stop decision is an integer cross-multiplication. */
+typedef struct {
+  int32_t  max_batch;          /* rows B the context may be called with            */
+  int32_t  seq_capacity;       /* S: row stride of token_ids and max context; S % 4 == 0 */
+  int32_t  vocab_size;         /* V: ids are in [0, V); the corpus sentinel is V   */
+  int32_t  k;                  /* draft width (1..64)                              */
+  int32_t  max_tree_depth;     /* D: longest match considered (1..128)             */
+  int32_t  max_occurrences;    /* R: occurrences voting per row (1..128)           */
+  int32_t  max_sampled;        /* largest T passed to the update (1..1024)         */
+  uint32_t spec_factor_num;    /* max_spec_factor = num / den (den > 0)            */
+  uint32_t spec_factor_den;
+  int32_t  spec_offset;        /* max_spec_offset                                   */
+  uint32_t min_prob_num;       /* min_token_prob = num / den (den > 0, num <= den)  */
+  uint32_t min_prob_den;
+  int32_t  depth_sum_cap;      /* 1: also bound the draft by D - M (CPU-tree style) */
+  int64_t  corpus_capacity;    /* ring tokens incl. sentinels (0: no corpus); <= 2^30 */
+  int32_t  max_docs;           /* documents the ring can hold at once              */
+  int32_t  max_ingest_docs;    /* documents per sgd_ingest call                    */
+  int32_t  corpus_cand_cap;    /* power of two >= R: on-chip candidate buffer of the
+                                  corpus occurrence selection (larger match sets take
+                                  an exact multi-pass path)                        */
+  int32_t  self_warps;         /* warps scanning each row (0: chosen from B and S) */
+} sgd_config;
+
+/* Fills *cfg with the defaults above (max_batch 256, S 4096, V 151936). */
+int sgd_config_default(sgd_config *cfg);
+
+/* Sets max_spec_factor and min_token_prob from floats, as x rounded to a
+ * multiple of 1e-6 (exact for 0.1, 1.0, 2.0, ...).  SGD_EINVAL if negative
+ * or min_token_prob > 1. */
+int sgd_config_set_float(sgd_config *cfg, double max_spec_factor, double min_token_prob);
+
+/* Creates a context on `device` and allocates everything it will ever use:
+ * ring, document FIFO, two suffix-array snapshots, the device descriptor of
+ * the current snapshot, scratch and streams-independent events.
+ * SGD_EINVAL for knobs out of range, SGD_ENOMEM / SGD_ECUDA on failure
+ * (nothing is leaked). */
+int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out);
+
+/* Waits for an in-flight build, then frees everything the context owns. */
+int sgd_destroy(sgd_ctx *ctx);
+
+/* Appends each row's accepted sampled ids ([PYPI] Quickstart: sampled ids
+ * [B, T] are -1 padded; [RFC] Design: the ngram_gpu token bookkeeping).
+ *   token_ids  DEVICE int32 [B, S] row-major, updated in place.
+ *   num_tokens DEVICE int32 [B], updated in place.
+ *   sampled    DEVICE int32 [B, T].
+ * Row b takes the leading run of ids in [0, V) of sampled[b, :]; an id >= V
+ * ends the run and sets SGD_ERR_SAMPLED_TOKEN.  Ids landing at or past S are
+ * dropped; num_tokens saturates at S (values outside [0, S] are clamped and
+ * set SGD_ERR_NUM_TOKENS).  B <= max_batch, 1 <= T <= max_sampled. */
+int sgd_update_state(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_tokens,
+                     const int32_t *sampled, int32_t B, int32_t T, void *stream);
+
+/* Drafts up to k tokens per row ([PYPI] How it works, steps 1-3; [DOCS]
+ * Model Runner V2; [BLOG] sections 4-5):
+ *   1. longest suffix self-match of the row's tail in its own context (length
+ *      <= D; ends j <= n-2), keeping the R most recent ends of that length;
+ *   2. corpus lookup through the current suffix array: the last 4 (else last
+ *      2) tokens are searched and every hit is extended backwards to the
+ *      longest match (length >= 2, <= D; only ends with a continuation), the
+ *      R most recent ends kept;
+ *   3. the longer match wins (equal lengths: the row itself);
+ *   4. cap = min(k, floor(factor * M) + offset, S - n - 1) [, D - M];
+ *   5. depth by depth the surviving occurrences vote on their next token
+ *      (ties: smallest id); the winner is emitted while |survivors| / c0 >=
+ *      min_token_prob (integer cross-multiplication).
+ *   token_ids  DEVICE int32 [B, S];  num_tokens DEVICE int32 [B] (clamped to [0, S]).
+ *   active     DEVICE uint8 [B] or NULL (all rows); a 0 row drafts nothing.
+ *   drafts     DEVICE int32 [B, k]: draft ids, then -1.
+ *   num_valid  DEVICE int32 [B].
+ *   score      DEVICE float [B] or NULL: sum of the emitted chain probabilities,
+ *              float(integer sum / c0) rounded from double.
+ *   probs      DEVICE float [B, k] or NULL: chain probability per emitted slot, 0 after.
+ *   match_info DEVICE int32 [B, 2] or NULL: {M, source} with source 0 = no
+ *              match, 1 = the row itself, 2 = corpus.
+ * One kernel launch on `stream`; reads the snapshot current at launch time. */
+int sgd_propose(sgd_ctx *ctx, const int32_t *token_ids, const int32_t *num_tokens,
+                const uint8_t *active, int32_t B, int32_t *drafts, int32_t *num_valid,
+                float *score, float *probs, int32_t *match_info, void *stream);
+
+/* sgd_update_state followed by sgd_propose, fused into one kernel launch
+ * ([PYPI] Quickstart: propose_with_update).  The update applies to every row;
+ * `active` masks only the drafting. */
+int sgd_propose_with_update(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_tokens,
+                            const int32_t *sampled, int32_t T, const uint8_t *active,
+                            int32_t B, int32_t *drafts, int32_t *num_valid, float *score,
+                            float *probs, int32_t *match_info, void *stream);
+
+/* Appends finished responses to the corpus ring ([PYPI] Quickstart:
+ * harvest_finished; How it works, step 4: oldest documents are evicted when
+ * the ring is full; [DOCS] Model Runner V2: oldest first out).
+ *   token_ids  DEVICE int32 [B, S];  num_tokens DEVICE int32 [B] or NULL.
+ *   rows, starts, lengths  DEVICE int32 [n_docs]: doc i is
+ *              token_ids[rows[i], starts[i] : starts[i] + lengths[i]].
+ * Docs are appended in order, each followed by the sentinel V; before each,
+ * the oldest docs are evicted while the ring would exceed corpus_capacity or
+ * hold max_docs docs.  Bad (row, start, length) -> skipped, SGD_ERR_DOC_ARGS;
+ * an id outside [0, V) truncates the doc there (SGD_ERR_DOC_TOKEN); a doc
+ * longer than the ring is skipped (SGD_ERR_DOC_TOO_LONG).  New docs become
+ * visible to drafting only after the next build is swapped in.
+ * n_docs <= max_ingest_docs.  SGD_ENOCORPUS without a corpus. */
+int sgd_ingest(sgd_ctx *ctx, const int32_t *token_ids, const int32_t *num_tokens,
+               int32_t B, const int32_t *rows, const int32_t *starts,
+               const int32_t *lengths, int32_t n_docs, void *stream);
+
+/* Starts a background suffix-array build ([PYPI] How it works, step 4 and
+ * Highlights: rebuilt on a side CUDA stream, double-buffered, swapped in
+ * place).  The live ring is copied (oldest doc first) into the spare
+ * snapshot buffer on `stream` -- so it reflects every ingest enqueued there
+ * before -- and the suffix array is then built by prefix doubling on
+ * `side_stream`, driven by a library-owned host thread.  Returns at once.
+ * `stream` must also be ordered after every propose that may still read the
+ * spare buffer (a propose enqueued before the previous swap).
+ * SGD_EBUSY while an earlier build is running or not yet swapped in. */
+int sgd_build_sa(sgd_ctx *ctx, void *stream, void *side_stream);
+
+/* Swaps in a finished build ([PYPI] Quickstart: poll).  If the build is done
+ * and succeeded, a 32-byte descriptor write is enqueued on `stream`, so every
+ * later propose on `stream` (including replays of graphs captured earlier)
+ * reads the new snapshot; returns SGD_OK_SWAPPED.  SGD_PENDING while running
+ * (wait = 0); with wait = 1 blocks up to timeout_us (< 0: forever), then
+ * SGD_ETIMEDOUT.  SGD_OK if no build was started.  SGD_EBUILD if the build
+ * failed (the previous snapshot stays current).  *generation (may be NULL)
+ * receives the number of swaps so far. */
+int sgd_poll(sgd_ctx *ctx, int wait, int64_t timeout_us, void *stream, uint64_t *generation);
+
+/* Suffix array of a caller text, with the context's scratch, blocking the
+ * host until done ([PYPI] References: Manber & Myers prefix doubling).
+ *   text DEVICE int32 [n], any int32 values; sa DEVICE int32 [n] output.
+ * Order: token by token as signed int32, a proper prefix first.
+ * n <= corpus_capacity.  SGD_EBUSY while a background build runs;
+ * SGD_EBUILD if the sort reported a failure. */
+int sgd_suffix_array(sgd_ctx *ctx, const int32_t *text, int64_t n, int32_t *sa, void *stream);
+
+/* Reads (and with clear = 1 resets) the sticky device error word; this
+ * synchronises the device and is not meant for the drafting path. */
+int sgd_get_error(sgd_ctx *ctx, uint32_t *flags, int clear);
+
+/* Copies the current snapshot (text and suffix array) into caller DEVICE
+ * buffers of `capacity` elements and returns its length and generation.
+ * Synchronises the device.  SGD_EINVAL if capacity is too small. */
+int sgd_export_snapshot(sgd_ctx *ctx, int32_t *text, int32_t *sa, int64_t capacity,
+                        int64_t *n, uint64_t *generation);
+
+/* Live ring tokens (incl. sentinels) and documents.  Synchronises the device. */
+int sgd_corpus_stats(sgd_ctx *ctx, int64_t *live_tokens, int32_t *ndocs);
+
+/* Figures of the last finished suffix-array build. */
+typedef struct {
+  int64_t n;              /* tokens sorted                                        */
+  int32_t rounds;         /* prefix-doubling rounds, the initial sort included     */
+  int32_t passes;         /* radix passes run                                      */
+  int64_t sorted_elems;   /* sum over rounds of the suffixes still unresolved      */
+  int64_t pass_elems;     /* sum over passes of the elements moved                 */
+  int64_t model_bytes;    /* algorithmic bytes of the build (see the design notes) */
+  double  ms;             /* device time of the whole build (events, side stream)  */
+  double  pass_ms;        /* device time inside the radix-pass kernels             */
+  int32_t status;         /* SGD_OK or SGD_EBUILD                                  */
+} sgd_build_info;
+int sgd_build_stats(sgd_ctx *ctx, sgd_build_info *info);
+
+/* Host-side fault injection for tests (no GPU fault is ever provoked):
+ *   SGD_INJECT_NONE        clear;
+ *   SGD_INJECT_BUILD_FAIL  the next build reports failure;
+ *   SGD_INJECT_BUILD_HANG  the next build never reports completion (its
+ *                          kernels still run; sgd_poll stays pending). */
+#define SGD_INJECT_NONE       0
+#define SGD_INJECT_BUILD_FAIL 1
+#define SGD_INJECT_BUILD_HANG 2
+int sgd_debug_inject(sgd_ctx *ctx, int what);
+
+/* Kernel launches the context made since creation (every library kernel). */
+int sgd_launch_count(sgd_ctx *ctx, uint64_t *count);
+
+const char *sgd_strerror(int status);
+int sgd_version(void); /* major * 10000 + minor * 100 + patch */
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* SGD_H */

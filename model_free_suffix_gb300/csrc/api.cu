@@ -1,0 +1,598 @@
+// api.cu -- host side of libsgd: the context, argument checks, launches on
+// the caller's streams and the background suffix-array build.
+//
+// The build of a new suffix array is driven by one host thread per context
+// (its prefix-doubling rounds read small counts back to size the next round),
+// while drafting keeps running on the caller's stream; sgd_poll swaps the
+// finished snapshot in with a 32-byte device write ("SuffixGPU", PyPI: How it
+// works, step 4 -- rebuilt on a side stream, double-buffered, swapped in
+// place so captured CUDA graphs keep working).
+#include <atomic>
+#include <chrono>
+#include <condition_variable>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <thread>
+
+#include "sgd_internal.h"
+
+using namespace sgd;
+
+namespace {
+
+enum BuildState { B_IDLE = 0, B_RUNNING = 1, B_DONE = 2, B_HUNG = 3 };
+
+}  // namespace
+
+struct sgd_ctx {
+  sgd_config cfg;
+  int device = 0;
+  int nself = 1;
+  size_t smem = 0;
+  bool corpus = false;
+  // device state
+  uint32_t *d_err = nullptr;        // sticky error bits of drafting and ingest
+  uint32_t *d_build_err = nullptr;  // error bits of the build in progress
+  int32_t *d_ring = nullptr;
+  RingState *d_rs = nullptr;
+  int64_t *d_doc_start = nullptr;
+  int32_t *d_doc_len = nullptr;
+  int32_t *d_text[2] = {nullptr, nullptr};
+  int32_t *d_sa[2] = {nullptr, nullptr};
+  CorpusDesc *d_desc = nullptr;
+  IngestScratch ing{};
+  SaScratch sa{};
+  int64_t *h_n = nullptr;      // pinned
+  uint32_t *h_err = nullptr;   // pinned
+  cudaEvent_t ev_lin = nullptr, ev_b0 = nullptr, ev_b1 = nullptr;
+  // snapshots
+  int front = 0;
+  int64_t front_n = 0;
+  uint64_t gen = 0;
+  // build worker
+  std::thread worker;
+  std::mutex mu;
+  std::condition_variable cv;
+  bool quit = false;
+  bool job_ready = false;
+  int job_back = 1;
+  cudaStream_t job_side = nullptr;
+  int bstate = B_IDLE;
+  int bstatus = SGD_OK;
+  int64_t built_n = 0;
+  int inject = SGD_INJECT_NONE;
+  int job_inject = SGD_INJECT_NONE;
+  sgd_build_info last{};
+  std::atomic<uint64_t> launches{0};
+};
+
+namespace {
+
+bool is_pow2(int x) { return x > 0 && (x & (x - 1)) == 0; }
+
+int check_cuda(cudaError_t e) { return e == cudaSuccess ? SGD_OK : SGD_ECUDA; }
+
+bool aligned16(const void *p) { return ((uintptr_t)p & 15u) == 0; }
+
+int validate(const sgd_config &c) {
+  if (c.max_batch < 1 || c.seq_capacity < 4 || c.seq_capacity % 4 != 0) return SGD_EINVAL;
+  if (c.vocab_size < 1 || c.vocab_size == 0x7fffffff) return SGD_EINVAL;
+  if (c.k < 1 || c.k > MAX_K) return SGD_EINVAL;
+  if (c.max_tree_depth < 1 || c.max_tree_depth > MAX_D) return SGD_EINVAL;
+  if (c.max_occurrences < 1 || c.max_occurrences > MAX_R) return SGD_EINVAL;
+  if (c.max_sampled < 1 || c.max_sampled > 1024) return SGD_EINVAL;
+  if (c.spec_factor_den == 0 || c.min_prob_den == 0 || c.min_prob_num > c.min_prob_den)
+    return SGD_EINVAL;
+  if (c.spec_offset < 0) return SGD_EINVAL;
+  if (c.corpus_capacity < 0 || c.corpus_capacity > (1LL << 30)) return SGD_EINVAL;
+  if (c.corpus_capacity > 0 && (c.max_docs < 1 || c.max_ingest_docs < 1)) return SGD_EINVAL;
+  if (!is_pow2(c.corpus_cand_cap) || c.corpus_cand_cap < c.max_occurrences ||
+      c.corpus_cand_cap > 16384)
+    return SGD_EINVAL;
+  if (c.self_warps < 0 || c.self_warps > MAX_SELF_WARPS) return SGD_EINVAL;
+  return SGD_OK;
+}
+
+int choose_self_warps(const sgd_config &c) {
+  if (c.self_warps > 0) return c.self_warps;
+  int w = c.seq_capacity / 512;
+  if (w < 1) w = 1;
+  const int cap = c.max_batch <= 76 ? 16 : 8;
+  if (w > cap) w = cap;
+  return w;
+}
+
+void free_ctx(sgd_ctx *x) {
+  cudaFree(x->d_err);
+  cudaFree(x->d_build_err);
+  cudaFree(x->d_ring);
+  cudaFree(x->d_rs);
+  cudaFree(x->d_doc_start);
+  cudaFree(x->d_doc_len);
+  for (int i = 0; i < 2; ++i) {
+    cudaFree(x->d_text[i]);
+    cudaFree(x->d_sa[i]);
+  }
+  cudaFree(x->d_desc);
+  cudaFree(x->ing.eff);
+  cudaFree(x->ing.dest);
+  cudaFree(x->ing.order);
+  if (x->sa.keyA) sa_scratch_free(&x->sa);
+  if (x->h_n) cudaFreeHost(x->h_n);
+  if (x->h_err) cudaFreeHost(x->h_err);
+  if (x->ev_lin) cudaEventDestroy(x->ev_lin);
+  if (x->ev_b0) cudaEventDestroy(x->ev_b0);
+  if (x->ev_b1) cudaEventDestroy(x->ev_b1);
+}
+
+// One background build: wait for the snapshot copy, sort, report.
+void worker_main(sgd_ctx *x) {
+  cudaSetDevice(x->device);
+  std::unique_lock<std::mutex> lk(x->mu);
+  for (;;) {
+    x->cv.wait(lk, [&] { return x->quit || x->job_ready; });
+    if (x->quit) return;
+    x->job_ready = false;
+    const int back = x->job_back;
+    cudaStream_t side = x->job_side;
+    const int inj = x->job_inject;
+    lk.unlock();
+
+    int status = SGD_OK;
+    int64_t n = 0;
+    SaStats st;
+    int launches = 0;
+    float ms = 0.f;
+    cudaError_t e = cudaStreamWaitEvent(side, x->ev_lin, 0);
+    if (e == cudaSuccess) e = cudaMemsetAsync(x->d_build_err, 0, 4, side);
+    if (e == cudaSuccess) e = cudaEventRecord(x->ev_b0, side);
+    if (e == cudaSuccess)
+      e = cudaMemcpyAsync(x->h_n, &x->d_rs->snap_n, 8, cudaMemcpyDeviceToHost, side);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(side);
+    if (e == cudaSuccess) {
+      n = *x->h_n;
+      const int r = sa_build(x->sa, x->d_text[back], n, x->d_sa[back], x->d_build_err, side, &st,
+                             true, &launches);
+      if (r != 0) status = SGD_EBUILD;
+      e = cudaEventRecord(x->ev_b1, side);
+      if (e == cudaSuccess)
+        e = cudaMemcpyAsync(x->h_err, x->d_build_err, 4, cudaMemcpyDeviceToHost, side);
+      if (e == cudaSuccess) e = cudaStreamSynchronize(side);
+      if (e == cudaSuccess) cudaEventElapsedTime(&ms, x->ev_b0, x->ev_b1);
+      if (e == cudaSuccess && *x->h_err != 0) status = SGD_EBUILD;
+    }
+    if (e != cudaSuccess) status = SGD_EBUILD;
+    if (inj == SGD_INJECT_BUILD_FAIL) status = SGD_EBUILD;
+    x->launches += (uint64_t)launches + 1;
+
+    lk.lock();
+    x->built_n = n;
+    x->bstatus = status;
+    x->last.n = n;
+    x->last.rounds = st.rounds;
+    x->last.passes = st.passes;
+    x->last.sorted_elems = st.sorted_elems;
+    x->last.pass_elems = st.pass_elems;
+    x->last.model_bytes = st.model_bytes;
+    x->last.ms = ms;
+    x->last.pass_ms = st.pass_ms;
+    x->last.status = status;
+    x->bstate = inj == SGD_INJECT_BUILD_HANG ? B_HUNG : B_DONE;
+    x->cv.notify_all();
+  }
+}
+
+}  // namespace
+
+extern "C" {
+
+int sgd_version(void) { return 100; }
+
+const char *sgd_strerror(int s) {
+  switch (s) {
+    case SGD_OK: return "ok";
+    case SGD_OK_SWAPPED: return "ok: new suffix array swapped in";
+    case SGD_PENDING: return "build pending";
+    case SGD_EINVAL: return "invalid argument";
+    case SGD_ECUDA: return "CUDA error";
+    case SGD_ENOMEM: return "out of memory";
+    case SGD_ETIMEDOUT: return "timed out";
+    case SGD_EBUSY: return "a suffix-array build is in flight";
+    case SGD_EBUILD: return "suffix-array build failed";
+    case SGD_ENOCORPUS: return "context has no corpus";
+    default: return "unknown status";
+  }
+}
+
+int sgd_config_default(sgd_config *c) {
+  if (!c) return SGD_EINVAL;
+  std::memset(c, 0, sizeof(*c));
+  c->max_batch = 256;
+  c->seq_capacity = 4096;
+  c->vocab_size = 151936;
+  c->k = 16;
+  c->max_tree_depth = 24;
+  c->max_occurrences = 64;
+  c->max_sampled = 64;
+  c->spec_factor_num = 1;
+  c->spec_factor_den = 1;
+  c->spec_offset = 0;
+  c->min_prob_num = 1;
+  c->min_prob_den = 10;
+  c->depth_sum_cap = 0;
+  c->corpus_capacity = 1LL << 20;
+  c->max_docs = 65536;
+  c->max_ingest_docs = 4096;
+  c->corpus_cand_cap = 2048;
+  c->self_warps = 0;
+  return SGD_OK;
+}
+
+static void to_rational(double x, uint32_t *num, uint32_t *den) {
+  long long n = (long long)(x * 1e6 + 0.5);
+  long long d = 1000000;
+  long long a = n, b = d;
+  while (b) {
+    const long long t = a % b;
+    a = b;
+    b = t;
+  }
+  if (a == 0) a = 1;
+  *num = (uint32_t)(n / a);
+  *den = (uint32_t)(d / a);
+}
+
+int sgd_config_set_float(sgd_config *c, double factor, double min_prob) {
+  if (!c || !(factor >= 0) || !(min_prob >= 0) || min_prob > 1 || factor > 4000) return SGD_EINVAL;
+  to_rational(factor, &c->spec_factor_num, &c->spec_factor_den);
+  to_rational(min_prob, &c->min_prob_num, &c->min_prob_den);
+  return SGD_OK;
+}
+
+int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
+  if (!cfg || !out) return SGD_EINVAL;
+  *out = nullptr;
+  int v = validate(*cfg);
+  if (v != SGD_OK) return v;
+  if (cudaSetDevice(device) != cudaSuccess) return SGD_ECUDA;
+  sgd_ctx *x = new (std::nothrow) sgd_ctx;
+  if (!x) return SGD_ENOMEM;
+  x->cfg = *cfg;
+  x->device = device;
+  x->nself = choose_self_warps(*cfg);
+  x->corpus = cfg->corpus_capacity > 0;
+  x->smem = propose_smem_bytes(x->nself, cfg->max_occurrences, cfg->k, cfg->corpus_cand_cap);
+  cudaError_t e = cudaSuccess;
+  auto al = [&](void **p, size_t bytes) {
+    if (e == cudaSuccess) e = cudaMalloc(p, bytes);
+  };
+  al((void **)&x->d_err, 4);
+  al((void **)&x->d_build_err, 4);
+  if (e == cudaSuccess) e = cudaMemset(x->d_err, 0, 4);
+  if (e == cudaSuccess) e = cudaMemset(x->d_build_err, 0, 4);
+  if (x->corpus) {
+    const int64_t C = cfg->corpus_capacity;
+    al((void **)&x->d_ring, (size_t)C * 4);
+    al((void **)&x->d_rs, sizeof(RingState));
+    al((void **)&x->d_doc_start, (size_t)cfg->max_docs * 8);
+    al((void **)&x->d_doc_len, (size_t)cfg->max_docs * 4);
+    for (int i = 0; i < 2; ++i) {
+      al((void **)&x->d_text[i], (size_t)C * 4);
+      al((void **)&x->d_sa[i], (size_t)C * 4);
+    }
+    al((void **)&x->d_desc, sizeof(CorpusDesc));
+    al((void **)&x->ing.eff, (size_t)cfg->max_ingest_docs * 4);
+    al((void **)&x->ing.dest, (size_t)cfg->max_ingest_docs * 8);
+    al((void **)&x->ing.order, (size_t)cfg->max_ingest_docs * 4);
+    if (e == cudaSuccess) e = sa_scratch_alloc(&x->sa, C);
+    if (e == cudaSuccess) e = cudaMemset(x->d_rs, 0, sizeof(RingState));
+    if (e == cudaSuccess) e = cudaMemset(x->d_doc_start, 0, (size_t)cfg->max_docs * 8);
+    if (e == cudaSuccess) e = cudaMemset(x->d_doc_len, 0, (size_t)cfg->max_docs * 4);
+    if (e == cudaSuccess) {
+      CorpusDesc d0{x->d_text[0], x->d_sa[0], 0, 0};
+      e = cudaMemcpy(x->d_desc, &d0, sizeof(d0), cudaMemcpyHostToDevice);
+    }
+    if (e == cudaSuccess) e = cudaMallocHost((void **)&x->h_n, 8);
+    if (e == cudaSuccess) e = cudaMallocHost((void **)&x->h_err, 4);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&x->ev_lin, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventCreate(&x->ev_b0);
+    if (e == cudaSuccess) e = cudaEventCreate(&x->ev_b1);
+  }
+  if (e == cudaSuccess && x->smem > 48 * 1024) e = propose_set_smem_limit(x->smem);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    const bool oom = e == cudaErrorMemoryAllocation;
+    free_ctx(x);
+    delete x;
+    cudaGetLastError();
+    return oom ? SGD_ENOMEM : SGD_ECUDA;
+  }
+  if (x->corpus) {
+    try {
+      x->worker = std::thread(worker_main, x);
+    } catch (...) {
+      free_ctx(x);
+      delete x;
+      return SGD_ENOMEM;
+    }
+  }
+  *out = x;
+  return SGD_OK;
+}
+
+int sgd_destroy(sgd_ctx *x) {
+  if (!x) return SGD_EINVAL;
+  cudaSetDevice(x->device);
+  if (x->worker.joinable()) {
+    {
+      std::unique_lock<std::mutex> lk(x->mu);
+      x->cv.wait(lk, [&] { return x->bstate != B_RUNNING && !x->job_ready; });
+      x->quit = true;
+      x->cv.notify_all();
+    }
+    x->worker.join();
+  }
+  cudaDeviceSynchronize();
+  free_ctx(x);
+  delete x;
+  return SGD_OK;
+}
+
+static ProposeArgs base_args(sgd_ctx *x) {
+  ProposeArgs a{};
+  const sgd_config &c = x->cfg;
+  a.S = c.seq_capacity;
+  a.V = c.vocab_size;
+  a.k = c.k;
+  a.D = c.max_tree_depth;
+  a.R = c.max_occurrences;
+  a.fN = c.spec_factor_num;
+  a.fD = c.spec_factor_den;
+  a.offset = c.spec_offset;
+  a.pN = c.min_prob_num;
+  a.pD = c.min_prob_den;
+  a.depth_sum_cap = c.depth_sum_cap;
+  a.desc = x->corpus ? x->d_desc : nullptr;
+  a.err = x->d_err;
+  a.nself = x->nself;
+  a.cand_cap = c.corpus_cand_cap;
+  return a;
+}
+
+int sgd_update_state(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int32_t *sampled,
+                     int32_t B, int32_t T, void *stream) {
+  if (!x || B < 0 || B > x->cfg.max_batch || T < 1 || T > x->cfg.max_sampled) return SGD_EINVAL;
+  if (B == 0) return SGD_OK;
+  if (!token_ids || !num_tokens || !sampled) return SGD_EINVAL;
+  if (!aligned16(token_ids)) return SGD_EINVAL;
+  x->launches++;
+  return check_cuda(launch_update(token_ids, num_tokens, sampled, B, T, x->cfg.seq_capacity,
+                                  x->cfg.vocab_size, x->d_err, (cudaStream_t)stream));
+}
+
+static int propose_impl(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int32_t *sampled,
+                        int32_t T, const uint8_t *active, int32_t B, int32_t *drafts,
+                        int32_t *num_valid, float *score, float *probs, int32_t *match_info,
+                        void *stream) {
+  if (!x || B < 0 || B > x->cfg.max_batch) return SGD_EINVAL;
+  if (sampled && (T < 1 || T > x->cfg.max_sampled)) return SGD_EINVAL;
+  if (B == 0) return SGD_OK;
+  if (!token_ids || !num_tokens || !drafts || !num_valid) return SGD_EINVAL;
+  if (!aligned16(token_ids)) return SGD_EINVAL;
+  ProposeArgs a = base_args(x);
+  a.tok = token_ids;
+  a.ntok = num_tokens;
+  a.sampled = sampled;
+  a.T = sampled ? T : 0;
+  a.do_update = sampled != nullptr;
+  a.active = active;
+  a.B = B;
+  a.drafts = drafts;
+  a.num_valid = num_valid;
+  a.score = score;
+  a.probs = probs;
+  a.match_info = match_info;
+  x->launches++;
+  return check_cuda(launch_propose(a, (cudaStream_t)stream));
+}
+
+int sgd_propose(sgd_ctx *x, const int32_t *token_ids, const int32_t *num_tokens,
+                const uint8_t *active, int32_t B, int32_t *drafts, int32_t *num_valid, float *score,
+                float *probs, int32_t *match_info, void *stream) {
+  return propose_impl(x, const_cast<int32_t *>(token_ids), const_cast<int32_t *>(num_tokens),
+                      nullptr, 0, active, B, drafts, num_valid, score, probs, match_info, stream);
+}
+
+int sgd_propose_with_update(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens,
+                            const int32_t *sampled, int32_t T, const uint8_t *active, int32_t B,
+                            int32_t *drafts, int32_t *num_valid, float *score, float *probs,
+                            int32_t *match_info, void *stream) {
+  if (!sampled && B != 0) return SGD_EINVAL;
+  return propose_impl(x, token_ids, num_tokens, sampled, T, active, B, drafts, num_valid, score,
+                      probs, match_info, stream);
+}
+
+int sgd_ingest(sgd_ctx *x, const int32_t *token_ids, const int32_t *num_tokens, int32_t B,
+               const int32_t *rows, const int32_t *starts, const int32_t *lengths, int32_t n_docs,
+               void *stream) {
+  if (!x) return SGD_EINVAL;
+  if (!x->corpus) return SGD_ENOCORPUS;
+  if (n_docs < 0 || n_docs > x->cfg.max_ingest_docs || B < 0) return SGD_EINVAL;
+  if (n_docs == 0) return SGD_OK;
+  if (!token_ids || !rows || !starts || !lengths) return SGD_EINVAL;
+  int launches = 0;
+  const cudaError_t e =
+      launch_ingest(token_ids, num_tokens, B, x->cfg.seq_capacity, x->cfg.vocab_size, rows, starts,
+                    lengths, n_docs, x->d_ring, x->cfg.corpus_capacity, x->d_rs, x->d_doc_start,
+                    x->d_doc_len, x->cfg.max_docs, x->ing, x->d_err, (cudaStream_t)stream, &launches);
+  x->launches += launches;
+  return check_cuda(e);
+}
+
+int sgd_build_sa(sgd_ctx *x, void *stream, void *side_stream) {
+  if (!x) return SGD_EINVAL;
+  if (!x->corpus) return SGD_ENOCORPUS;
+  std::unique_lock<std::mutex> lk(x->mu);
+  if (x->bstate != B_IDLE || x->job_ready) return SGD_EBUSY;
+  const int back = 1 - x->front;
+  int launches = 0;
+  cudaError_t e = launch_linearize(x->d_ring, x->cfg.corpus_capacity, x->d_rs, x->d_doc_start,
+                                   x->cfg.max_docs, x->d_text[back], (cudaStream_t)stream, &launches);
+  x->launches += launches;
+  if (e == cudaSuccess) e = cudaEventRecord(x->ev_lin, (cudaStream_t)stream);
+  if (e != cudaSuccess) return SGD_ECUDA;
+  x->job_back = back;
+  x->job_side = (cudaStream_t)side_stream;
+  x->job_inject = x->inject;
+  x->inject = SGD_INJECT_NONE;
+  x->job_ready = true;
+  x->bstate = B_RUNNING;
+  x->cv.notify_all();
+  return SGD_OK;
+}
+
+int sgd_poll(sgd_ctx *x, int wait, int64_t timeout_us, void *stream, uint64_t *generation) {
+  if (!x) return SGD_EINVAL;
+  if (!x->corpus) return SGD_ENOCORPUS;
+  std::unique_lock<std::mutex> lk(x->mu);
+  if (x->bstate == B_IDLE) {
+    if (generation) *generation = x->gen;
+    return SGD_OK;
+  }
+  if (x->bstate != B_DONE) {
+    if (!wait) {
+      if (generation) *generation = x->gen;
+      return SGD_PENDING;
+    }
+    auto ready = [&] { return x->bstate == B_DONE; };
+    if (timeout_us < 0) {
+      x->cv.wait(lk, ready);
+    } else if (!x->cv.wait_for(lk, std::chrono::microseconds(timeout_us), ready)) {
+      if (generation) *generation = x->gen;
+      return SGD_ETIMEDOUT;
+    }
+  }
+  x->bstate = B_IDLE;
+  if (x->bstatus != SGD_OK) {
+    if (generation) *generation = x->gen;
+    return SGD_EBUILD;
+  }
+  const int back = 1 - x->front;
+  const cudaError_t e = launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->built_n,
+                                    x->gen + 1, (cudaStream_t)stream);
+  if (e != cudaSuccess) return SGD_ECUDA;
+  x->launches++;
+  x->front = back;
+  x->front_n = x->built_n;
+  x->gen++;
+  if (generation) *generation = x->gen;
+  return SGD_OK_SWAPPED;
+}
+
+int sgd_suffix_array(sgd_ctx *x, const int32_t *text, int64_t n, int32_t *sa, void *stream) {
+  if (!x) return SGD_EINVAL;
+  if (!x->corpus) return SGD_ENOCORPUS;
+  if (n < 0 || n > x->cfg.corpus_capacity || (n > 0 && (!text || !sa))) return SGD_EINVAL;
+  std::unique_lock<std::mutex> lk(x->mu);
+  if (x->bstate != B_IDLE || x->job_ready) return SGD_EBUSY;
+  cudaStream_t st = (cudaStream_t)stream;
+  SaStats stats;
+  int launches = 0;
+  if (cudaMemsetAsync(x->d_build_err, 0, 4, st) != cudaSuccess) return SGD_ECUDA;
+  if (cudaEventRecord(x->ev_b0, st) != cudaSuccess) return SGD_ECUDA;
+  const int r = sa_build(x->sa, text, n, sa, x->d_build_err, st, &stats, true, &launches);
+  x->launches += launches;
+  if (r < 0) return SGD_ECUDA;
+  float ms = 0.f;
+  if (cudaEventRecord(x->ev_b1, st) != cudaSuccess) return SGD_ECUDA;
+  if (cudaMemcpyAsync(x->h_err, x->d_build_err, 4, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return SGD_ECUDA;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SGD_ECUDA;
+  cudaEventElapsedTime(&ms, x->ev_b0, x->ev_b1);
+  const int status = (r != 0 || *x->h_err != 0) ? SGD_EBUILD : SGD_OK;
+  x->last.n = n;
+  x->last.rounds = stats.rounds;
+  x->last.passes = stats.passes;
+  x->last.sorted_elems = stats.sorted_elems;
+  x->last.pass_elems = stats.pass_elems;
+  x->last.model_bytes = stats.model_bytes;
+  x->last.ms = ms;
+  x->last.pass_ms = stats.pass_ms;
+  x->last.status = status;
+  return status;
+}
+
+int sgd_get_error(sgd_ctx *x, uint32_t *flags, int clear) {
+  if (!x || !flags) return SGD_EINVAL;
+  if (cudaSetDevice(x->device) != cudaSuccess) return SGD_ECUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SGD_ECUDA;
+  uint32_t a = 0, b = 0;
+  if (cudaMemcpy(&a, x->d_err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return SGD_ECUDA;
+  if (cudaMemcpy(&b, x->d_build_err, 4, cudaMemcpyDeviceToHost) != cudaSuccess) return SGD_ECUDA;
+  *flags = a | b;
+  if (clear) {
+    if (cudaMemset(x->d_err, 0, 4) != cudaSuccess) return SGD_ECUDA;
+    std::unique_lock<std::mutex> lk(x->mu);
+    if (x->bstate == B_IDLE && cudaMemset(x->d_build_err, 0, 4) != cudaSuccess) return SGD_ECUDA;
+  }
+  return SGD_OK;
+}
+
+int sgd_export_snapshot(sgd_ctx *x, int32_t *text, int32_t *sa, int64_t capacity, int64_t *n,
+                        uint64_t *generation) {
+  if (!x || !n) return SGD_EINVAL;
+  if (!x->corpus) return SGD_ENOCORPUS;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SGD_ECUDA;
+  *n = x->front_n;
+  if (generation) *generation = x->gen;
+  if (x->front_n > capacity) return SGD_EINVAL;
+  if (x->front_n > 0) {
+    if (!text || !sa) return SGD_EINVAL;
+    if (cudaMemcpy(text, x->d_text[x->front], (size_t)x->front_n * 4, cudaMemcpyDeviceToDevice) !=
+            cudaSuccess ||
+        cudaMemcpy(sa, x->d_sa[x->front], (size_t)x->front_n * 4, cudaMemcpyDeviceToDevice) !=
+            cudaSuccess)
+      return SGD_ECUDA;
+  }
+  return SGD_OK;
+}
+
+int sgd_corpus_stats(sgd_ctx *x, int64_t *live_tokens, int32_t *ndocs) {
+  if (!x) return SGD_EINVAL;
+  if (!x->corpus) return SGD_ENOCORPUS;
+  if (cudaDeviceSynchronize() != cudaSuccess) return SGD_ECUDA;
+  RingState r;
+  if (cudaMemcpy(&r, x->d_rs, sizeof(r), cudaMemcpyDeviceToHost) != cudaSuccess) return SGD_ECUDA;
+  if (live_tokens) *live_tokens = r.live;
+  if (ndocs) *ndocs = r.ndocs;
+  return SGD_OK;
+}
+
+int sgd_build_stats(sgd_ctx *x, sgd_build_info *info) {
+  if (!x || !info) return SGD_EINVAL;
+  std::unique_lock<std::mutex> lk(x->mu);
+  *info = x->last;
+  return SGD_OK;
+}
+
+int sgd_debug_inject(sgd_ctx *x, int what) {
+  if (!x) return SGD_EINVAL;
+  if (what < SGD_INJECT_NONE || what > SGD_INJECT_BUILD_HANG) return SGD_EINVAL;
+  std::unique_lock<std::mutex> lk(x->mu);
+  x->inject = what;
+  if (what == SGD_INJECT_NONE && x->bstate == B_HUNG) {
+    x->bstate = B_DONE;
+    x->cv.notify_all();
+  }
+  return SGD_OK;
+}
+
+int sgd_launch_count(sgd_ctx *x, uint64_t *count) {
+  if (!x || !count) return SGD_EINVAL;
+  *count = x->launches.load();
+  return SGD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,162 @@
+// corpus.cu -- the ring of finished responses: ingest (scatter_append),
+// linearisation of the live docs into a snapshot, and the descriptor swap.
+//
+// Sources (page title, section):
+//   "SuffixGPU" (suffix-gpu 0.1.1, PyPI): Quickstart (harvest_finished, poll);
+//     How it works, step 4 (new documents append; oldest documents are
+//     evicted when the ring is full; the suffix array is swapped in place).
+//   "Suffix Decoding" (vLLM docs): Model Runner V2 (a token budget, oldest
+//     first out).
+//
+// Layout: ring[C] int32 holds the live docs back to back (circularly), each
+// followed by the sentinel Z = V.  Because docs are appended at the write
+// offset and evicted from the oldest end, the live tokens always form one
+// circular run starting at the oldest doc: doc_start[head] + live == wp (mod C).
+#include "sgd_internal.h"
+
+namespace sgd {
+
+namespace {
+
+// Per doc: check (row, start, length) and find the first id outside [0, V).
+__global__ void __launch_bounds__(256) ingest_measure(const int32_t *tok, const int32_t *ntok, int B,
+                                                      int S, int V, const int32_t *rows,
+                                                      const int32_t *starts, const int32_t *lengths,
+                                                      int m, int32_t *eff, uint32_t *err) {
+  const int i = blockIdx.x;
+  if (i >= m) return;
+  __shared__ int s_first;
+  const int row = rows[i], st = starts[i], ln = lengths[i];
+  const bool ok = row >= 0 && row < B && st >= 0 && ln >= 0 && (long long)st + ln <= S &&
+                  (ntok == nullptr || (long long)st + ln <= (long long)ntok[row]);
+  if (!ok) {
+    if (threadIdx.x == 0) {
+      eff[i] = -1;
+      atomicOr(err, SGD_ERR_DOC_ARGS);
+    }
+    return;
+  }
+  if (threadIdx.x == 0) s_first = ln;
+  __syncthreads();
+  const int32_t *src = tok + (size_t)row * S + st;
+  for (int u = threadIdx.x; u < ln; u += blockDim.x) {
+    const int v = src[u];
+    if (v < 0 || v >= V) atomicMin(&s_first, u);
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    eff[i] = s_first;
+    if (s_first < ln) atomicOr(err, SGD_ERR_DOC_TOKEN);
+  }
+}
+
+// Sequential placement, in call order: evict the oldest docs while the new
+// doc would not fit (or the FIFO is full), then append at the write offset.
+// A doc pushed by this call and evicted by a later doc of the same call is
+// not copied.
+__global__ void ingest_plan(const int32_t *eff, int m, long long C, RingState *rs, int64_t *doc_start,
+                            int32_t *doc_len, int max_docs, int64_t *dest, int32_t *order,
+                            uint32_t *err) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  RingState r = *rs;
+  int old_remaining = r.ndocs;
+  int pushed = 0, ev = 0;
+  uint32_t fl = 0;
+  for (int i = 0; i < m; ++i) {
+    dest[i] = -1;
+    const int L = eff[i];
+    if (L <= 0) continue;
+    const long long s = (long long)L + 1;
+    if (s > C) { fl |= SGD_ERR_DOC_TOO_LONG; continue; }
+    while (r.ndocs > 0 && (r.live + s > C || r.ndocs == max_docs)) {
+      r.live -= (long long)doc_len[r.head] + 1;
+      r.head = (r.head + 1) % max_docs;
+      r.ndocs--;
+      if (old_remaining > 0) old_remaining--;
+      else dest[order[ev++]] = -1;
+    }
+    const int slot = (r.head + r.ndocs) % max_docs;
+    doc_start[slot] = r.wp;
+    doc_len[slot] = L;
+    dest[i] = r.wp;
+    order[pushed++] = i;
+    r.wp = (r.wp + s) % C;
+    r.live += s;
+    r.ndocs++;
+  }
+  *rs = r;
+  if (fl) atomicOr(err, fl);
+}
+
+__global__ void __launch_bounds__(256) ingest_copy(const int32_t *tok, int S, const int32_t *rows,
+                                                   const int32_t *starts, const int32_t *eff,
+                                                   const int64_t *dest, int m, int32_t *ring,
+                                                   long long C, int Z) {
+  const int i = blockIdx.x;
+  if (i >= m) return;
+  const long long d0 = dest[i];
+  if (d0 < 0) return;
+  const int L = eff[i];
+  const int32_t *src = tok + (size_t)rows[i] * S + starts[i];
+  for (int u = threadIdx.x; u <= L; u += blockDim.x) {
+    long long pos = d0 + u;
+    if (pos >= C) pos -= C;
+    ring[pos] = u < L ? src[u] : Z;
+  }
+}
+
+__global__ void __launch_bounds__(256) linearize_kernel(const int32_t *ring, long long C,
+                                                        RingState *rs, const int64_t *doc_start,
+                                                        int32_t *out) {
+  const long long live = rs->live;
+  const long long start = rs->ndocs > 0 ? doc_start[rs->head] : 0;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < live; i += stride) {
+    long long p = start + i;
+    if (p >= C) p -= C;
+    out[i] = ring[p];
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) rs->snap_n = live;
+}
+
+__global__ void swap_kernel(CorpusDesc *desc, const int32_t *text, const int32_t *sa, long long n,
+                            uint64_t gen) {
+  desc->text = text;
+  desc->sa = sa;
+  desc->n = n;
+  desc->gen = gen;
+}
+
+}  // namespace
+
+cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S, int V,
+                          const int32_t *rows, const int32_t *starts, const int32_t *lengths, int m,
+                          int32_t *ring, int64_t C, RingState *rs, int64_t *doc_start,
+                          int32_t *doc_len, int max_docs, const IngestScratch &sc, uint32_t *err,
+                          cudaStream_t st, int *launches) {
+  if (m <= 0) return cudaSuccess;
+  ingest_measure<<<m, 256, 0, st>>>(tok, ntok, B, S, V, rows, starts, lengths, m, sc.eff, err);
+  ingest_plan<<<1, 32, 0, st>>>(sc.eff, m, C, rs, doc_start, doc_len, max_docs, sc.dest, sc.order, err);
+  ingest_copy<<<m, 256, 0, st>>>(tok, S, rows, starts, sc.eff, sc.dest, m, ring, C, V);
+  *launches += 3;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs, const int64_t *doc_start,
+                             int max_docs, int32_t *out, cudaStream_t st, int *launches) {
+  (void)max_docs;
+  long long blocks = (C + 1023) / 1024;
+  if (blocks > 152 * 8) blocks = 152 * 8;
+  if (blocks < 1) blocks = 1;
+  linearize_kernel<<<(int)blocks, 256, 0, st>>>(ring, C, rs, doc_start, out);
+  *launches += 1;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, int64_t n,
+                        uint64_t gen, cudaStream_t st) {
+  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, n, gen);
+  return cudaGetLastError();
+}
+
+}  // namespace sgd

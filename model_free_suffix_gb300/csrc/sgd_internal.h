@@ -1,0 +1,116 @@
+// sgd_internal.h -- shared declarations of the libsgd CUDA sources.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "sgd.h"
+
+namespace sgd {
+
+constexpr unsigned FULL = 0xffffffffu;
+constexpr int WIN = 128;        // tokens per warp window: 32 lanes x int4
+constexpr int MAX_D = 128;      // the halo of one window covers D - 1 <= 127
+constexpr int MAX_R = 128;      // up to 4 occurrences per lane in the vote warp
+constexpr int MAX_K = 64;
+constexpr int MAX_SELF_WARPS = 16;
+constexpr int NPROBE = 4;       // probe warps: {P4, P2} x {lower, upper bound}
+
+// Descriptor of the suffix-array snapshot drafting reads.  It lives in device
+// memory at a fixed address, so graphs captured before a swap see the new
+// snapshot after it.
+struct CorpusDesc {
+  const int32_t *text;  // X[0..n): live docs oldest first, each followed by Z
+  const int32_t *sa;    // suffix array of X
+  int64_t n;
+  uint64_t gen;
+};
+
+// Ring bookkeeping, device resident.  The doc FIFO lives in two arrays of
+// max_docs entries indexed (head + i) % max_docs.
+struct RingState {
+  int64_t wp;      // next write offset in [0, C)
+  int64_t live;    // tokens of live docs, sentinels included
+  int32_t head;    // FIFO index of the oldest doc
+  int32_t ndocs;
+  int64_t snap_n;  // length of the last linearised snapshot
+};
+
+struct ProposeArgs {
+  int32_t *tok;            // [B, S]
+  int32_t *ntok;           // [B]
+  const int32_t *sampled;  // [B, T] or null
+  int T;
+  int do_update;
+  const uint8_t *active;   // [B] or null
+  int B, S, V, k, D, R;
+  long long fN, fD, offset, pN, pD;
+  int depth_sum_cap;
+  const CorpusDesc *desc;  // null when the context has no corpus
+  int32_t *drafts;         // [B, k]
+  int32_t *num_valid;      // [B]
+  float *score;            // [B] or null
+  float *probs;            // [B, k] or null
+  int32_t *match_info;     // [B, 2] or null
+  uint32_t *err;
+  int nself;               // self-scan warps per row
+  int cand_cap;            // corpus candidate buffer (power of two >= R)
+};
+
+// propose.cu
+size_t propose_smem_bytes(int nself, int R, int k, int cand_cap);
+cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st);
+cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, int B,
+                          int T, int S, int V, uint32_t *err, cudaStream_t st);
+cudaError_t propose_set_smem_limit(size_t bytes);
+
+// corpus.cu
+struct IngestScratch {
+  int32_t *eff;     // [max_ingest_docs] effective doc length (-1: skip)
+  int64_t *dest;    // [max_ingest_docs] ring offset or -1
+  int32_t *order;   // [max_ingest_docs] docs pushed by this call, push order
+};
+cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S, int V,
+                          const int32_t *rows, const int32_t *starts, const int32_t *lengths,
+                          int m, int32_t *ring, int64_t C, RingState *rs, int64_t *doc_start,
+                          int32_t *doc_len, int max_docs, const IngestScratch &sc,
+                          uint32_t *err, cudaStream_t st, int *launches);
+cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs,
+                             const int64_t *doc_start, int max_docs, int32_t *out,
+                             cudaStream_t st, int *launches);
+cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, int64_t n,
+                        uint64_t gen, cudaStream_t st);
+
+// sa_build.cu
+struct SaScratch {
+  int64_t cap;          // elements the scratch can sort
+  uint64_t *keyA, *keyB;
+  int32_t *valA, *valB;
+  int32_t *rank;        // head-position ranks
+  int32_t *act, *act2;  // SA positions of unresolved suffixes
+  int32_t *tmp;         // head positions, then ranks
+  int32_t *head;        // 1 at the first member of each group
+  int32_t *tile_sums;
+  uint32_t *hist;       // [8][256] digit histograms
+  uint32_t *status;     // look-back words, [tiles][256]
+  uint32_t *counter;    // tile ticket + small device counters
+  int32_t *h_pinned;    // pinned host words for counts read back by the driver
+  uint32_t *h_hist;     // pinned [8][256]
+  int64_t status_words;
+};
+struct SaStats {
+  int rounds = 0, passes = 0;
+  long long sorted_elems = 0, pass_elems = 0, model_bytes = 0;
+  double pass_ms = 0;
+};
+size_t sa_scratch_bytes(int64_t cap);
+cudaError_t sa_scratch_alloc(SaScratch *s, int64_t cap);
+void sa_scratch_free(SaScratch *s);
+// Builds the suffix array of text[0..n) into sa; host-driven rounds on `st`
+// (blocks the calling thread).  Returns 0 on success, else SGD_ERR_* bits
+// (through *dev_flags as well) or -1 on a CUDA error.
+int sa_build(const SaScratch &s, const int32_t *text, int64_t n, int32_t *sa,
+             uint32_t *err, cudaStream_t st, SaStats *stats, bool time_passes,
+             int *launches);
+
+}  // namespace sgd

@@ -1,0 +1,77 @@
+"""The C-ABI library builds, loads and exports every symbol include/sgd.h declares.
+
+No compute call is made here (there may be no GPU).
+"""
+import ctypes
+
+import pytest
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from model_free_suffix_gb300 import build as B
+    B.build()
+    from model_free_suffix_gb300 import _lib as L
+    return L
+
+
+def test_exports_every_declared_function(lib):
+    L = lib.load()
+    names = lib.header_functions()
+    assert len(names) >= 15
+    missing = [n for n in names if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_config_defaults(lib):
+    L = lib.load()
+    c = lib.SgdConfig()
+    assert L.sgd_config_default(ctypes.byref(c)) == 0
+    assert (c.k, c.max_tree_depth, c.max_occurrences) == (16, 24, 64)
+    assert (c.spec_factor_num, c.spec_factor_den) == (1, 1)
+    assert (c.min_prob_num, c.min_prob_den) == (1, 10)
+    assert c.corpus_capacity == 1 << 20
+
+
+def test_config_set_float_rationals(lib):
+    L = lib.load()
+    c = lib.SgdConfig()
+    L.sgd_config_default(ctypes.byref(c))
+    assert L.sgd_config_set_float(ctypes.byref(c), 2.0, 0.1) == 0
+    assert (c.spec_factor_num, c.spec_factor_den) == (2, 1)
+    assert (c.min_prob_num, c.min_prob_den) == (1, 10)
+    assert L.sgd_config_set_float(ctypes.byref(c), 1.5, 0.25) == 0
+    assert (c.spec_factor_num, c.spec_factor_den) == (3, 2)
+    assert (c.min_prob_num, c.min_prob_den) == (1, 4)
+    assert L.sgd_config_set_float(ctypes.byref(c), -1.0, 0.1) == lib.SGD_EINVAL
+    assert L.sgd_config_set_float(ctypes.byref(c), 1.0, 1.5) == lib.SGD_EINVAL
+
+
+def test_strerror_and_null_args(lib):
+    L = lib.load()
+    assert L.sgd_strerror(lib.SGD_EBUSY).decode().startswith("a suffix-array build")
+    assert L.sgd_destroy(None) == lib.SGD_EINVAL
+    assert L.sgd_propose(None, None, None, None, 0, None, None, None, None, None, None) == lib.SGD_EINVAL
+    h = ctypes.c_void_p()
+    assert L.sgd_create(None, 0, ctypes.byref(h)) == lib.SGD_EINVAL
+
+
+def test_create_rejects_bad_knobs_before_touching_the_gpu(lib):
+    L = lib.load()
+    bad = [("seq_capacity", 4098), ("k", 0), ("k", 65), ("max_tree_depth", 129),
+           ("max_occurrences", 0), ("corpus_cand_cap", 100), ("corpus_cand_cap", 32),
+           ("min_prob_den", 0), ("self_warps", 17)]
+    for field, val in bad:
+        c = lib.SgdConfig()
+        L.sgd_config_default(ctypes.byref(c))
+        setattr(c, field, val)
+        h = ctypes.c_void_p()
+        assert L.sgd_create(ctypes.byref(c), 0, ctypes.byref(h)) == lib.SGD_EINVAL, field
+
+
+def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):
+    from model_free_suffix_gb300 import _lib as L
+    monkeypatch.setattr(L, "_lib", None)
+    monkeypatch.setattr(L, "LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        L.load()
