@@ -66,7 +66,7 @@ class Clocks:
             os.close(fd)
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.idx), "--query-gpu=" + self.Q,
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "10"],
                 stdout=open(self.path, "w"), stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -125,67 +125,103 @@ def run_ours(args, rank, world):
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.config]
     K, Wm = args.steps, args.warmup
-    n_steps = K + Wm
-    tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=2 * n_steps)
+    K_e2e = min(K, args.e2e_steps)
+    tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=Wm + K + K_e2e)
     dr = SuffixDrafter(max_batch=cfg.B, seq_capacity=cfg.S, vocab_size=cfg.V, k=cfg.k,
                        max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
                        max_spec_factor=cfg.factor, max_spec_offset=cfg.offset,
                        min_token_prob=cfg.min_prob, corpus_capacity=cfg.corpus_tokens,
                        device=dev.index)
-    stream = torch.cuda.current_stream(dev)
-    side = torch.cuda.Stream(device=dev, priority=0)
+    stream = torch.cuda.Stream(device=dev)
+    side = torch.cuda.Stream(device=dev)
+    torch.cuda.set_stream(stream)
     # corpus prefill (setup, untimed)
-    docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
-    for s0 in range(0, docs.shape[0], 2048):
-        d = docs[s0:s0 + 2048]
-        m = d.shape[0]
-        buf = torch.full((m, cfg.S), -1, dtype=torch.int32, device=dev)
-        buf[:, :d.shape[1]] = torch.from_numpy(d).to(dev)
-        dr.ingest(buf, torch.arange(m, dtype=torch.int32, device=dev),
-                  torch.zeros(m, dtype=torch.int32, device=dev),
-                  torch.from_numpy(np.ascontiguousarray(lens[s0:s0 + 2048])).to(dev))
-    dr.build_sa(side)
-    assert dr.poll(wait=True)[0] == 1
+    if cfg.corpus_tokens:
+        docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
+        for s0 in range(0, docs.shape[0], 2048):
+            d = docs[s0:s0 + 2048]
+            m = d.shape[0]
+            buf = torch.full((m, cfg.S), -1, dtype=torch.int32, device=dev)
+            buf[:, :d.shape[1]] = torch.from_numpy(d).to(dev)
+            dr.ingest(buf, torch.arange(m, dtype=torch.int32, device=dev),
+                      torch.zeros(m, dtype=torch.int32, device=dev),
+                      torch.from_numpy(np.ascontiguousarray(lens[s0:s0 + 2048])).to(dev))
+        dr.build_sa(side)
+        assert dr.poll(wait=True)[0] == 1
 
     g_tok = torch.from_numpy(tok).to(dev)
     g_n = torch.from_numpy(n).to(dev)
     out = dr.new_outputs(cfg.B)
+    m_fin = int(np.floor(cfg.finish_frac * cfg.B))
+    # fixed device inputs of one step; each step's values are staged into them
+    d_samp = torch.full((cfg.B, cfg.T), -1, dtype=torch.int32, device=dev)
+    d_rows = torch.zeros(max(1, m_fin), dtype=torch.int32, device=dev)
+    d_st = torch.zeros(max(1, m_fin), dtype=torch.int32, device=dev)
+    d_ln = torch.zeros(max(1, m_fin), dtype=torch.int32, device=dev)
     samp = [torch.from_numpy(s.sampled).to(dev) for s in steps]
     fin = [(torch.from_numpy(s.finished).to(dev), torch.from_numpy(s.ingest_starts).to(dev),
             torch.from_numpy(s.ingest_lengths).to(dev), int(s.ingest_lengths.sum()),
             torch.from_numpy(s.finished.astype(np.int64)).to(dev),
-            torch.from_numpy(s.reset_tokens).to(dev), torch.from_numpy(s.reset_n).to(dev))
-           for s in steps]
+            None if s.reset_tokens is None else torch.from_numpy(s.reset_tokens).to(dev),
+            torch.from_numpy(s.reset_n).to(dev)) for s in steps]
+    # the step's kernels, captured once: propose_with_update, then the ingest
+    g_prop, g_ing = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    dr.propose_with_update(g_tok, g_n, d_samp, out=out)  # warm the launch path
+    torch.cuda.synchronize()
+    with torch.cuda.graph(g_prop, stream=stream):
+        dr.propose_with_update(g_tok, g_n, d_samp, out=out, stream=stream)
+    if m_fin and cfg.corpus_tokens:
+        with torch.cuda.graph(g_ing, stream=stream):
+            dr.ingest(g_tok, d_rows, d_st, d_ln, num_tokens=g_n, stream=stream)
+    g_tok.copy_(torch.from_numpy(tok))   # undo the warm-up update
+    g_n.copy_(torch.from_numpy(n))
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
-    state = {"pending": False, "ingested": 0, "swaps": 0, "builds": 0}
+    state = {"pending": False, "ingested": 0, "swaps": 0, "builds": 0, "build_stats": []}
 
-    def one_step(i, ev=None):
-        if i > 0:  # the previous step's finished rows restart (workload bookkeeping)
+    def stage(i):
+        """Outside the timed region: the previous step's finished rows restart
+        (workload bookkeeping), this step's inputs land in the fixed buffers,
+        and L2 is flushed."""
+        if i > 0:
             _, _, _, _, idx, rt, rn = fin[i - 1]
             if idx.numel():
                 g_tok[idx] = rt
                 g_n[idx] = rn
+        d_samp.copy_(samp[i])
+        rows, st_, ln, _, _, _, _ = fin[i]
+        if rows.numel():
+            d_rows.copy_(rows)
+            d_st.copy_(st_)
+            d_ln.copy_(ln)
         flush.fill_(i)
+
+    def policy(i):
+        """Host side of the step: rebuild policy and the swap poll."""
+        state["ingested"] += fin[i][3]
+        if cfg.corpus_tokens:
+            if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
+                dr.build_sa(side, stream=stream)
+                state["pending"] = True
+                state["ingested"] = 0
+                state["builds"] += 1
+            st, _ = dr.poll(wait=False, stream=stream)
+            if st == 1:
+                state["pending"] = False
+                state["swaps"] += 1
+                state["build_stats"].append(dr.build_stats())
+
+    def one_step(i, ev=None):
+        stage(i)
         if ev:
             ev[0].record(stream)
-        dr.propose_with_update(g_tok, g_n, samp[i], out=out)
+        g_prop.replay()
         if ev:
             ev[1].record(stream)
-        rows, st_, ln, tot, _, _, _ = fin[i]
-        if rows.numel():
-            dr.ingest(g_tok, rows, st_, ln, num_tokens=g_n)
-            state["ingested"] += tot
-        if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
-            dr.build_sa(side)
-            state["pending"] = True
-            state["ingested"] = 0
-            state["builds"] += 1
-        st, _ = dr.poll(wait=False)
-        if st == 1:
-            state["pending"] = False
-            state["swaps"] += 1
+        if m_fin and cfg.corpus_tokens:
+            g_ing.replay()
+        policy(i)
         if ev:
             ev[2].record(stream)
 
@@ -195,10 +231,11 @@ def run_ours(args, rank, world):
     barrier(world)
     torch.cuda.synchronize()
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
-    sum_n = []
     l0 = dr.launch_count()
+    nb0 = len(state["build_stats"])
     clk = Clocks(dev.index if "CUDA_VISIBLE_DEVICES" not in os.environ else 0)
     clk.start()
+    time.sleep(0.05)
     b0 = state["builds"]
     t_wall = time.perf_counter()
     for j in range(K):
@@ -208,28 +245,45 @@ def run_ours(args, rank, world):
     clocks = clk.stop()
     barrier(world)
     torch.cuda.synchronize()
-    launches = dr.launch_count() - l0
+    graph_kernels = 1 + (3 if (m_fin and cfg.corpus_tokens) else 0)
+    launches = dr.launch_count() - l0 + graph_kernels * K
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     prop_ms = [e[0].elapsed_time(e[1]) for e in evs]
     total_ms = float(np.sum(step_ms))
     total_ms_max = allreduce_max(total_ms, world)
     builds_in_region = state["builds"] - b0
-    # final num_tokens -> algorithmic bytes of a propose launch (mean over the region)
-    n_final = int(g_n.sum().item())
-    sum_n_est = n_final
+    region_builds = state["build_stats"][nb0:]
+    n_sum = int(g_n.sum().item())
     # e2e: host buffers through the public API, copies inside the timed region
-    e2e = e2e_leg(args, dr, cfg, steps, Wm + K, K, g_tok, g_n, out, flush, side, state, dev)
-    # suffix-array builds, standalone (C4 workload)
+    if state["pending"]:
+        dr.poll(wait=True, stream=stream)
+        state["pending"] = False
+    e2e = e2e_leg(args, dr, cfg, steps, Wm + K, K_e2e, g_tok, g_n, out, flush, side, state, dev,
+                  stream)
+    dr.close()
+    # suffix-array builds, standalone (the suffix-array workload)
     sa = sa_build_leg(args, dev)
     peak, peak_kind = peaks()
-    byts = algorithmic_bytes_propose(sum_n_est, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens)
+    byts = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens)
     prop_avg_s = float(np.mean(prop_ms)) / 1e3
     ach = byts / prop_avg_s / 1e9
     rl_prop = {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 2),
                "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": None,
                "bytes_per_launch": int(byts), "avg_launch_us": round(prop_avg_s * 1e6, 2),
                "peak_kind": peak_kind}
-    dr.close()
+    # GPU time of the background builds that finished inside the region
+    pass_ms = float(sum(b["pass_ms"] for b in region_builds))
+    pass_elems = int(sum(b["pass_elems"] for b in region_builds))
+    n_passes = int(sum(b["passes"] for b in region_builds))
+    kernels = {"propose_kernel": {"launches": K, "total_ms": round(float(np.sum(prop_ms)), 3)},
+               "k_onesweep (side stream)": {"launches": n_passes, "total_ms": round(pass_ms, 3)}}
+    rl = rl_prop
+    if pass_ms > float(np.sum(prop_ms)) and n_passes:
+        ach_p = 24.0 * pass_elems / (pass_ms / 1e3) / 1e9
+        rl = {"bound": "hbm", "kernel": "k_onesweep", "achieved": round(ach_p, 2), "peak": peak,
+              "unit": "GB/s", "frac": round(ach_p / peak, 4), "traffic": None,
+              "bytes_per_launch": int(24 * pass_elems / n_passes),
+              "avg_launch_us": round(1e3 * pass_ms / n_passes, 2), "peak_kind": peak_kind}
     value = world * K / (total_ms_max / 1e3)
     res = {
         "metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world,
@@ -241,18 +295,20 @@ def run_ours(args, rank, world):
                    "R": cfg.R, "T": cfg.T, "corpus_tokens": cfg.corpus_tokens,
                    "rebuild_tokens": cfg.rebuild_tokens,
                    "l2": "flushed before every timed step (%d MiB write)" % (flush.numel() * 4 >> 20),
+                   "launch": "each step replays CUDA graphs of the library's kernels",
                    "parallelism": "replicas" if world > 1 else "single"},
-        "roofline": rl_prop,
+        "roofline": rl, "roofline_propose": rl_prop, "kernels": kernels,
         "propose_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
-                       "median": round(1e3 * float(np.median(prop_ms)), 2)},
-        "builds_in_timed_region": builds_in_region, "swaps": state["swaps"],
+                       "median": round(1e3 * float(np.median(prop_ms)), 2),
+                       "p90": round(1e3 * float(np.percentile(prop_ms, 90)), 2)},
+        "builds_in_timed_region": builds_in_region,
         "wall_s_timed_region": round(t_wall, 4),
         "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks, "sa_build": sa,
     }
     return res
 
 
-def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state, dev):
+def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state, dev, stream):
     """Same steps through the public API with pinned host buffers: each step
     copies its sampled ids (and ingest arguments) host->device and reads the
     drafts and valid counts back, all inside the timed region."""
@@ -270,7 +326,6 @@ def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state,
     d_ln = torch.empty(m_max, dtype=torch.int32, device=dev)
     h_drafts = torch.empty((cfg.B, cfg.k), dtype=torch.int32).pin_memory()
     h_nv = torch.empty(cfg.B, dtype=torch.int32).pin_memory()
-    stream = torch.cuda.current_stream(dev)
     times = []
     bi = bo = 0
     for j in range(K):
@@ -291,16 +346,17 @@ def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state,
             d_st[:m].copy_(h_fin[j][1], non_blocking=True)
             d_ln[:m].copy_(h_fin[j][2], non_blocking=True)
         dr.propose_with_update(g_tok, g_n, d_samp, out=out)
-        if m:
+        if m and cfg.corpus_tokens:
             dr.ingest(g_tok, d_rows[:m], d_st[:m], d_ln[:m], num_tokens=g_n)
             state["ingested"] += int(s.ingest_lengths.sum())
-        if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
-            dr.build_sa(side)
-            state["pending"] = True
-            state["ingested"] = 0
-        st, _ = dr.poll(wait=False)
-        if st == 1:
-            state["pending"] = False
+        if cfg.corpus_tokens:
+            if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
+                dr.build_sa(side)
+                state["pending"] = True
+                state["ingested"] = 0
+            st, _ = dr.poll(wait=False)
+            if st == 1:
+                state["pending"] = False
         h_drafts.copy_(out.drafts, non_blocking=True)
         h_nv.copy_(out.num_valid, non_blocking=True)
         stream.synchronize()
@@ -361,13 +417,15 @@ def cpu_oracle_leg(cfg, seconds, rank=0):
     from model_free_suffix_gb300 import workload as W
     O.build()
     threads = os.cpu_count() or 1
-    tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=64)
-    docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
-    ring = O.Ring(cfg.corpus_tokens, 65536, cfg.V)
-    buf = np.full((docs.shape[0], cfg.S), -1, dtype=np.int32)
-    buf[:, :docs.shape[1]] = docs
-    ring.ingest(buf, np.arange(docs.shape[0]), np.zeros(docs.shape[0]), lens)
-    X = ring.snapshot()
+    tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=400)
+    ring, X = None, None
+    if cfg.corpus_tokens:
+        docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
+        ring = O.Ring(cfg.corpus_tokens, 65536, cfg.V)
+        buf = np.full((docs.shape[0], cfg.S), -1, dtype=np.int32)
+        buf[:, :docs.shape[1]] = docs
+        ring.ingest(buf, np.arange(docs.shape[0]), np.zeros(docs.shape[0]), lens)
+        X = ring.snapshot()
     p = O.Params(S=cfg.S, V=cfg.V, k=cfg.k, D=cfg.D, R=cfg.R, factor=cfg.factor,
                  offset=cfg.offset, min_prob=cfg.min_prob)
     done = 0
@@ -377,7 +435,8 @@ def cpu_oracle_leg(cfg, seconds, rank=0):
         O.update_state(tok, n, s.sampled, cfg.V)
         O.propose(p, tok, n, X=X, threads=threads)
         if s.finished.shape[0]:
-            ring.ingest(tok, s.finished, s.ingest_starts, s.ingest_lengths, num_tokens=n)
+            if ring is not None:
+                ring.ingest(tok, s.finished, s.ingest_starts, s.ingest_lengths, num_tokens=n)
             for i, b in enumerate(s.finished):
                 tok[b] = s.reset_tokens[i]
                 n[b] = s.reset_n[i]
@@ -411,7 +470,8 @@ def allreduce_max(x, world):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--steps", type=int, default=512)
+    ap.add_argument("--e2e-steps", type=int, default=256)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c3")

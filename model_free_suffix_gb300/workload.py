@@ -154,10 +154,13 @@ class ServingTrace:
 
     Each row owns one token stream: its first n tokens fill the buffer, the rest
     is the continuation that later steps' sampled ids reveal (a uniform 1..T
-    accepted prefix per step, the remainder -1).  When rows finish, their
+    accepted prefix per step, the remainder -1).  Continuations are generated
+    on demand, in blocks, from the same mixed process.  When rows finish, their
     response (the tokens appended since the row started) is handed to the
     corpus and the row restarts with a fresh stream.
     """
+
+    BLOCK = 256
 
     def __init__(self, cfg: Config, seed: int = 0, steps: Optional[int] = None,
                  finish_frac: Optional[float] = None, B: Optional[int] = None):
@@ -187,8 +190,15 @@ class ServingTrace:
     def _new_row(self, rng: np.random.Generator) -> Tuple[np.ndarray, int]:
         cfg = self.cfg
         n = int(rng.integers(cfg.n_lo, cfg.n_hi + 1))
-        total = n + self.steps * cfg.T
-        return mixed_sequence(rng, total, cfg.p_repeat, self.pool, self.fresh), n
+        return mixed_sequence(rng, n + self.BLOCK, cfg.p_repeat, self.pool, self.fresh), n
+
+    def _continuation(self, b: int, need: int, rng: np.random.Generator) -> np.ndarray:
+        p = int(self.pos[b])
+        while self.stream[b].shape[0] < p + need:
+            ext = mixed_sequence(rng, max(self.BLOCK, need), self.cfg.p_repeat, self.pool,
+                                 self.fresh)
+            self.stream[b] = np.concatenate([self.stream[b], ext])
+        return self.stream[b][p:p + need]
 
     def initial(self) -> Tuple[np.ndarray, np.ndarray]:
         return self.tokens.copy(), self.n0.copy()
@@ -199,9 +209,8 @@ class ServingTrace:
         a = rng.integers(1, T + 1, size=B)
         sampled = np.full((B, T), -1, dtype=np.int32)
         for b in range(B):
-            p = int(self.pos[b])
-            sampled[b, :a[b]] = self.stream[b][p:p + a[b]]
-            self.pos[b] = p + a[b]
+            sampled[b, :a[b]] = self._continuation(b, int(a[b]), self._rows_rng)
+            self.pos[b] += a[b]
         m = int(np.floor(self.finish_frac * B))
         if m > 0:
             fin = np.sort(self._fin_rng.choice(B, size=m, replace=False)).astype(np.int32)
