@@ -50,42 +50,130 @@ __global__ void __launch_bounds__(256) ingest_measure(const int32_t *tok, const 
   }
 }
 
+constexpr int PLAN_THREADS = 1024;
+constexpr int PLAN_CHUNK = 4096;   // docs whose lengths are staged per round
+constexpr int PLAN_WINDOW = 1024;  // oldest FIFO lengths staged for evictions
+constexpr int SMALL_DOCS = 32;     // calls up to this size run as one CTA
+
 // Sequential placement, in call order: evict the oldest docs while the new
 // doc would not fit (or the FIFO is full), then append at the write offset.
 // A doc pushed by this call and evicted by a later doc of the same call is
-// not copied.
-__global__ void ingest_plan(const int32_t *eff, int m, long long C, RingState *rs, int64_t *doc_start,
-                            int32_t *doc_len, int max_docs, int64_t *dest, int32_t *order,
-                            uint32_t *err) {
-  if (threadIdx.x != 0 || blockIdx.x != 0) return;
-  RingState r = *rs;
-  int old_remaining = r.ndocs;
-  int pushed = 0, ev = 0;
+// not copied.  Thread 0 walks the docs; every value it reads (effective doc
+// lengths, lengths of the oldest FIFO docs) is staged in shared memory by
+// the whole CTA first, so the walk never waits on global memory.
+__device__ void plan_docs(const int32_t *eff_g, const int32_t *eff_s, int m, long long C,
+                          RingState *rs, int64_t *doc_start, int32_t *doc_len, int max_docs,
+                          int64_t *dest, int32_t *order, uint32_t *err, int *s_eff, int *s_dl,
+                          RingState *s_rs) {
+  const int tid = threadIdx.x;
+  if (tid == 0) *s_rs = *rs;
+  __syncthreads();
+  const RingState r0 = *s_rs;
+  const int win = min(r0.ndocs, PLAN_WINDOW);
+  for (int j = tid; j < win; j += blockDim.x) s_dl[j] = doc_len[(r0.head + j) % max_docs];
+  RingState r = r0;
+  int evicted = 0, pushed = 0, ev_call = 0;
   uint32_t fl = 0;
-  for (int i = 0; i < m; ++i) {
-    dest[i] = -1;
-    const int L = eff[i];
-    if (L <= 0) continue;
-    const long long s = (long long)L + 1;
-    if (s > C) { fl |= SGD_ERR_DOC_TOO_LONG; continue; }
-    while (r.ndocs > 0 && (r.live + s > C || r.ndocs == max_docs)) {
-      r.live -= (long long)doc_len[r.head] + 1;
-      r.head = (r.head + 1) % max_docs;
-      r.ndocs--;
-      if (old_remaining > 0) old_remaining--;
-      else dest[order[ev++]] = -1;
+  for (int c0 = 0; c0 < m; c0 += PLAN_CHUNK) {
+    const int cn = min(PLAN_CHUNK, m - c0);
+    if (eff_s == nullptr)
+      for (int j = tid; j < cn; j += blockDim.x) s_eff[j] = eff_g[c0 + j];
+    __syncthreads();
+    if (tid == 0) {
+      const int *ef = eff_s ? eff_s + c0 : s_eff;
+      for (int j = 0; j < cn; ++j) {
+        const int i = c0 + j;
+        dest[i] = -1;
+        const int L = ef[j];
+        if (L <= 0) continue;
+        const long long s = (long long)L + 1;
+        if (s > C) { fl |= SGD_ERR_DOC_TOO_LONG; continue; }
+        while (r.ndocs > 0 && (r.live + s > C || r.ndocs == max_docs)) {
+          const int len = evicted < win ? s_dl[evicted] : doc_len[r.head];
+          r.live -= (long long)len + 1;
+          r.head = (r.head + 1) % max_docs;
+          r.ndocs--;
+          if (evicted >= r0.ndocs) dest[order[ev_call++]] = -1;  // pushed by this call
+          ++evicted;
+        }
+        const int slot = (r.head + r.ndocs) % max_docs;
+        doc_start[slot] = r.wp;
+        doc_len[slot] = L;
+        dest[i] = r.wp;
+        order[pushed++] = i;
+        r.wp = (r.wp + s) % C;
+        r.live += s;
+        r.ndocs++;
+      }
     }
-    const int slot = (r.head + r.ndocs) % max_docs;
-    doc_start[slot] = r.wp;
-    doc_len[slot] = L;
-    dest[i] = r.wp;
-    order[pushed++] = i;
-    r.wp = (r.wp + s) % C;
-    r.live += s;
-    r.ndocs++;
+    __syncthreads();
   }
-  *rs = r;
-  if (fl) atomicOr(err, fl);
+  if (tid == 0) {
+    *rs = r;
+    if (fl) atomicOr(err, fl);
+  }
+}
+
+__global__ void __launch_bounds__(PLAN_THREADS) ingest_plan(const int32_t *eff, int m, long long C,
+                                                            RingState *rs, int64_t *doc_start,
+                                                            int32_t *doc_len, int max_docs,
+                                                            int64_t *dest, int32_t *order,
+                                                            uint32_t *err) {
+  __shared__ int s_eff[PLAN_CHUNK];
+  __shared__ int s_dl[PLAN_WINDOW];
+  __shared__ RingState s_rs;
+  plan_docs(eff, nullptr, m, C, rs, doc_start, doc_len, max_docs, dest, order, err, s_eff, s_dl,
+            &s_rs);
+}
+
+// A small call in one CTA: measure (one warp per doc), plan, copy.
+__global__ void __launch_bounds__(PLAN_THREADS) ingest_small(
+    const int32_t *tok, const int32_t *ntok, int B, int S, int V, const int32_t *rows,
+    const int32_t *starts, const int32_t *lengths, int m, int32_t *ring, long long C, RingState *rs,
+    int64_t *doc_start, int32_t *doc_len, int max_docs, int64_t *dest, int32_t *order,
+    uint32_t *err) {
+  __shared__ int s_eff[SMALL_DOCS];
+  __shared__ int s_dl[PLAN_WINDOW];
+  __shared__ RingState s_rs;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int i = warp; i < m; i += nw) {
+    const int row = rows[i], st = starts[i], ln = lengths[i];
+    const bool ok = row >= 0 && row < B && st >= 0 && ln >= 0 && (long long)st + ln <= S &&
+                    (ntok == nullptr || (long long)st + ln <= (long long)ntok[row]);
+    if (!ok) {
+      if (lane == 0) {
+        s_eff[i] = -1;
+        atomicOr(err, SGD_ERR_DOC_ARGS);
+      }
+      continue;
+    }
+    const int32_t *src = tok + (size_t)row * S + st;
+    int first = ln;
+    for (int u0 = 0; u0 < ln; u0 += 32) {
+      const int u = u0 + lane;
+      const int v = u < ln ? src[u] : 0;
+      const unsigned bad = __ballot_sync(FULL, u < ln && (v < 0 || v >= V));
+      if (bad) { first = u0 + __ffs(bad) - 1; break; }
+    }
+    if (lane == 0) {
+      s_eff[i] = first;
+      if (first < ln) atomicOr(err, SGD_ERR_DOC_TOKEN);
+    }
+  }
+  __syncthreads();
+  plan_docs(nullptr, s_eff, m, C, rs, doc_start, doc_len, max_docs, dest, order, err, nullptr, s_dl,
+            &s_rs);
+  for (int i = 0; i < m; ++i) {
+    const long long d0 = dest[i];
+    if (d0 < 0) continue;
+    const int L = s_eff[i];
+    const int32_t *src = tok + (size_t)rows[i] * S + starts[i];
+    for (int u = threadIdx.x; u <= L; u += blockDim.x) {
+      long long pos = d0 + u;
+      if (pos >= C) pos -= C;
+      ring[pos] = u < L ? src[u] : V;
+    }
+  }
 }
 
 __global__ void __launch_bounds__(256) ingest_copy(const int32_t *tok, int S, const int32_t *rows,
@@ -135,8 +223,15 @@ cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S,
                           int32_t *doc_len, int max_docs, const IngestScratch &sc, uint32_t *err,
                           cudaStream_t st, int *launches) {
   if (m <= 0) return cudaSuccess;
+  if (m <= SMALL_DOCS) {
+    ingest_small<<<1, PLAN_THREADS, 0, st>>>(tok, ntok, B, S, V, rows, starts, lengths, m, ring, C, rs,
+                                             doc_start, doc_len, max_docs, sc.dest, sc.order, err);
+    *launches += 1;
+    return cudaGetLastError();
+  }
   ingest_measure<<<m, 256, 0, st>>>(tok, ntok, B, S, V, rows, starts, lengths, m, sc.eff, err);
-  ingest_plan<<<1, 32, 0, st>>>(sc.eff, m, C, rs, doc_start, doc_len, max_docs, sc.dest, sc.order, err);
+  ingest_plan<<<1, PLAN_THREADS, 0, st>>>(sc.eff, m, C, rs, doc_start, doc_len, max_docs, sc.dest,
+                                          sc.order, err);
   ingest_copy<<<m, 256, 0, st>>>(tok, S, rows, starts, sc.eff, sc.dest, m, ring, C, V);
   *launches += 3;
   return cudaGetLastError();

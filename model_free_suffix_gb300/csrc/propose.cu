@@ -10,11 +10,11 @@
 //     min_token_prob), section 5 (max_model_len - num_tokens - 1).
 //
 // CTA layout: `nself` warps scan the row for the self match (warp-per-segment,
-// int4 loads, ballot early-outs), and, when a corpus exists, 4 more warps run
-// the suffix-array probes concurrently (32-ary search) and the first pass
-// over the probe interval.  Warp 0 finally runs the depth-wise vote.  All
-// decisions are integer; the only floating-point values are the reported
-// probabilities and score.
+// int4 loads, ballot early-outs) while, when a corpus exists, 4 more warps
+// run the suffix-array probes (32-ary searches).  The whole CTA then scans
+// the probe interval with batched loads, and warp 0 runs the depth-wise
+// vote.  All decisions are integer; the only floating-point values are the
+// reported probabilities and score.
 #include <climits>
 
 #include "sgd_internal.h"
@@ -22,6 +22,8 @@
 namespace sgd {
 
 namespace {
+
+constexpr int LCAP = 16384;  // interval entries whose match length is cached on chip
 
 __device__ __forceinline__ int4 load_win(const int32_t *row, int widx, int lane, int S) {
   const int p = widx * WIN + 4 * lane;
@@ -198,7 +200,61 @@ __device__ __forceinline__ int corpus_entry(const int32_t *SA, const int32_t *X,
   return extend(X, e, lvl, s_tail, n, D);
 }
 
-__device__ __forceinline__ void named_sync_probe() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Match length of every end in the SA interval [lo, hi) of a pattern of
+// length lvl, by the whole CTA.  Each thread takes 4 entries per round and
+// issues their loads together (SA entries, then the continuation token and
+// the first token before the pattern), so a long interval costs a few
+// dependent round trips per round rather than one chain per entry.  The
+// length of entry lo + i (0 for an end without continuation) is kept in
+// s_L[i] for i < lcap; s_lhist[L] counts the valid ends of each length.
+__device__ void scan_interval(const int32_t *SA, const int32_t *X, long long N, int Z, long long lo,
+                              long long hi, int lvl, const int *s_tail, int n, int D,
+                              unsigned char *s_L, int lcap, int *s_lhist, int tid, int nthr) {
+  const long long dn = min(D, n);
+  for (long long base = lo + tid; base < hi; base += 4LL * nthr) {
+    long long e[4];
+    int x1[4], x0[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long long p = base + (long long)u * nthr;
+      e[u] = p < hi ? (long long)__ldg(SA + p) + lvl - 1 : -1;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const bool ok = e[u] >= 0 && e[u] + 1 < N;
+      x1[u] = ok ? __ldg(X + e[u] + 1) : Z;
+      x0[u] = ok && lvl < min(dn, e[u] + 1) ? __ldg(X + e[u] - lvl) : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const long long p = base + (long long)u * nthr;
+      if (p >= hi) continue;
+      int L = 0;
+      if (x1[u] != Z) {
+        const long long lim = min(dn, e[u] + 1);
+        L = lvl;
+        if (L < lim && x0[u] == s_tail[L]) {
+          ++L;
+          while (L < lim && __ldg(X + e[u] - L) == s_tail[L]) ++L;
+        }
+        atomicAdd(&s_lhist[L], 1);
+      }
+      if (p - lo < lcap) s_L[p - lo] = (unsigned char)L;
+    }
+  }
+}
+
+// Match length of SA entry p during selection: from the cache when scanned
+// into it, else recomputed.
+__device__ __forceinline__ int entry_len(const int32_t *SA, const int32_t *X, long long N, int Z,
+                                         long long p, long long lo, int lvl, const int *s_tail, int n,
+                                         int D, const unsigned char *s_L, int lcap, long long &e) {
+  if (p - lo < lcap) {
+    e = (long long)__ldg(SA + p) + lvl - 1;
+    return s_L[p - lo];
+  }
+  return corpus_entry(SA, X, N, Z, p, lvl, s_tail, n, D, e);
+}
 
 // Descending bitonic sort of s[0..P2) (P2 a power of two), whole CTA.
 __device__ void bitonic_desc(int *s, int P2, int tid, int nthr) {
@@ -256,13 +312,13 @@ __global__ void __launch_bounds__(128) update_kernel(int32_t *tok, int32_t *ntok
   }
 }
 
-__global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
+__device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   extern __shared__ __align__(16) int dsm[];
   __shared__ int s_wM[MAX_SELF_WARPS], s_wcnt[MAX_SELF_WARPS];
   __shared__ int s_hist[256];
   __shared__ long long s_bound[NPROBE];
-  __shared__ int s_pmax[NPROBE], s_pvalid[NPROBE];
-  __shared__ int s_n, s_Ms, s_cs, s_Mc, s_lvl, s_c0, s_q, s_sel, s_need, s_corpus_ok;
+  __shared__ int s_lhist[MAX_D + 1];
+  __shared__ int s_n, s_Ms, s_cs, s_c0, s_q, s_sel, s_need, s_corpus_ok;
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
@@ -273,6 +329,7 @@ __global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
   int *s_occ = s_wlist + a.nself * R;  // R
   int *s_run = s_occ + R;              // R
   int *s_big = s_run + R;              // max(cand_cap, R * k)
+  unsigned char *s_L = reinterpret_cast<unsigned char *>(s_big + max(a.cand_cap, R * k));  // LCAP
 
   // ---- the row's length, and the update when fused ----
   if (warp == 0) {
@@ -309,8 +366,6 @@ __global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
   for (int i = tid; i < dl; i += nthr) s_tail[i] = row[n - 1 - i];
   if (tid == 0) {
     s_corpus_ok = a.desc != nullptr && D >= 2 && n >= 2 && a.desc->n >= 2;
-    s_Mc = 0;
-    s_lvl = 2;
   }
   __syncthreads();
 
@@ -323,14 +378,13 @@ __global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
     N = a.desc->n;
   }
 
-  // ---- self match (nself warps) || corpus probes (4 warps) ----
+  // ---- self match (nself warps) || suffix-array probes (4 warps) ----
   if (warp < a.nself) {
     int Mw, cnt;
     self_scan(row, n, S, D, R, s_tail, s_wlist + warp * R, warp, a.nself, lane, Mw, cnt);
     if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; }
   } else if (s_corpus_ok) {
     const int pw = warp - a.nself;
-    const int ptid = tid - a.nself * 32;
     const bool use4 = D >= 4 && n >= 4;
     const int m = pw < 2 ? 4 : 2;
     if (pw >= 2 || use4) {
@@ -341,42 +395,6 @@ __global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
       if (lane == 0) s_bound[pw] = r;
     } else if (lane == 0) {
       s_bound[pw] = 0;
-    }
-    named_sync_probe();
-    // first pass: longest corpus match among the P4 hits, else the P2 hits
-    int lvl = 4;
-    int best = 0, nvalid = 0;
-    if (use4) {
-      for (long long p = s_bound[0] + ptid; p < s_bound[1]; p += 128) {
-        long long e;
-        const int L = corpus_entry(SA, X, N, Z, p, 4, s_tail, n, D, e);
-        if (L) { ++nvalid; best = max(best, L); }
-      }
-    }
-    best = (int)__reduce_max_sync(FULL, (unsigned)best);
-    nvalid = (int)__reduce_add_sync(FULL, (unsigned)nvalid);
-    if (lane == 0) { s_pmax[pw] = best; s_pvalid[pw] = nvalid; }
-    named_sync_probe();
-    int tb = max(max(s_pmax[0], s_pmax[1]), max(s_pmax[2], s_pmax[3]));
-    int tv = s_pvalid[0] + s_pvalid[1] + s_pvalid[2] + s_pvalid[3];
-    if (tv == 0) {
-      named_sync_probe();  // everyone has read the P4 totals
-      lvl = 2;
-      best = 0;
-      nvalid = 0;
-      for (long long p = s_bound[2] + ptid; p < s_bound[3]; p += 128) {
-        long long e;
-        const int L = corpus_entry(SA, X, N, Z, p, 2, s_tail, n, D, e);
-        if (L) { ++nvalid; best = max(best, L); }
-      }
-      best = (int)__reduce_max_sync(FULL, (unsigned)best);
-      if (lane == 0) s_pmax[pw] = best;
-      named_sync_probe();
-      tb = max(max(s_pmax[0], s_pmax[1]), max(s_pmax[2], s_pmax[3]));
-    }
-    if (ptid == 0) {
-      s_Mc = tb >= 2 ? tb : 0;
-      s_lvl = lvl;
     }
   }
   __syncthreads();
@@ -397,33 +415,61 @@ __global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
     if (lane == 0) { s_Ms = Ms; s_cs = c; }
   }
   __syncthreads();
+  const int Ms = s_Ms;
 
-  // ---- the longer match wins (equal lengths: the row itself) ----
-  const int Ms = s_Ms, Mc = s_Mc;
+  // ---- corpus: longest match among the probe hits, where it can still win ----
+  // Ends with a match >= 4 are exactly the P4 hits; if none of them has a
+  // continuation, valid matches of 2 or 3 are exactly the valid P2 hits.  A
+  // level is scanned only if its longest possible match exceeds Ms, which
+  // leaves the chosen source and its occurrences unchanged.
+  int Mc = 0, lvl = 4;
+  long long lo = 0, hi = 0;
+  if (s_corpus_ok) {
+    const int dn = min(D, n);
+    const bool use4 = D >= 4 && n >= 4;
+    bool have4 = false;
+    for (int pass = 0; pass < 2; ++pass) {
+      const int L_hi = pass == 0 ? dn : min(3, dn);
+      if (pass == 0 && !use4) continue;
+      if (pass == 1 && have4) break;
+      if (Ms >= L_hi) break;
+      const int lv = pass == 0 ? 4 : 2;
+      const long long l0 = pass == 0 ? s_bound[0] : s_bound[2];
+      const long long h0 = pass == 0 ? s_bound[1] : s_bound[3];
+      if (h0 <= l0) continue;
+      __syncthreads();  // the previous pass's histogram has been read
+      for (int i = tid; i <= MAX_D; i += nthr) s_lhist[i] = 0;
+      __syncthreads();
+      scan_interval(SA, X, N, Z, l0, h0, lv, s_tail, n, D, s_L, LCAP, s_lhist, tid, nthr);
+      __syncthreads();
+      int best = 0;
+      for (int L = dn; L >= 1; --L)
+        if (s_lhist[L] > 0) { best = L; break; }
+      if (best > 0) {
+        if (pass == 0) have4 = true;
+        if (best >= 2) { Mc = best; lvl = lv; lo = l0; hi = h0; }
+      }
+    }
+  }
   int src, M;
   if (Mc > Ms) { src = 2; M = Mc; }
   else { src = Ms > 0 ? 1 : 0; M = Ms; }
 
   if (src == 2) {
-    // second pass over the winning interval: the R largest ends with L == Mc
-    const int lvl = s_lvl;
-    const long long lo = lvl == 4 ? s_bound[0] : s_bound[2];
-    const long long hi = lvl == 4 ? s_bound[1] : s_bound[3];
+    // the R largest ends with length Mc (cached lengths; no second random pass)
     int *cand = s_big;
-    if (tid == 0) s_q = 0;
-    __syncthreads();
-    for (long long p = lo + tid; p < hi; p += nthr) {
-      long long e;
-      if (corpus_entry(SA, X, N, Z, p, lvl, s_tail, n, D, e) == Mc) {
-        const int slot = atomicAdd(&s_q, 1);
-        if (slot < a.cand_cap) cand[slot] = (int)e;
+    const int Q = s_lhist[Mc];
+    if (Q <= a.cand_cap) {
+      if (tid == 0) s_q = 0;
+      __syncthreads();
+      for (long long p = lo + tid; p < hi; p += nthr) {
+        long long e;
+        if (entry_len(SA, X, N, Z, p, lo, lvl, s_tail, n, D, s_L, LCAP, e) == Mc)
+          cand[atomicAdd(&s_q, 1)] = (int)e;
       }
-    }
-    __syncthreads();
-    int Q = s_q;
-    if (Q > a.cand_cap) {
+    } else {
       // more candidates than fit on chip: radix-select the R-th largest end
-      // byte by byte over the interval, then collect the R ends above it
+      // byte by byte, then collect the R ends at or above it
       unsigned prefix = 0, mask = 0;
       int need = R;
       for (int shift = 24; shift >= 0; shift -= 8) {
@@ -431,7 +477,7 @@ __global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
         __syncthreads();
         for (long long p = lo + tid; p < hi; p += nthr) {
           long long e;
-          if (corpus_entry(SA, X, N, Z, p, lvl, s_tail, n, D, e) == Mc &&
+          if (entry_len(SA, X, N, Z, p, lo, lvl, s_tail, n, D, s_L, LCAP, e) == Mc &&
               ((unsigned)e & mask) == prefix)
             atomicAdd(&s_hist[((unsigned)e >> shift) & 255u], 1);
         }
@@ -452,20 +498,21 @@ __global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
       __syncthreads();
       for (long long p = lo + tid; p < hi; p += nthr) {
         long long e;
-        if (corpus_entry(SA, X, N, Z, p, lvl, s_tail, n, D, e) == Mc && (unsigned)e >= prefix) {
+        if (entry_len(SA, X, N, Z, p, lo, lvl, s_tail, n, D, s_L, LCAP, e) == Mc &&
+            (unsigned)e >= prefix) {
           const int slot = atomicAdd(&s_q, 1);
           if (slot < a.cand_cap) cand[slot] = (int)e;
         }
       }
-      __syncthreads();
-      Q = min(s_q, a.cand_cap);
     }
+    __syncthreads();
+    const int Qc = min(s_q, a.cand_cap);
     int P2 = 1;
-    while (P2 < Q) P2 <<= 1;
-    for (int i = Q + tid; i < P2; i += nthr) cand[i] = -1;
+    while (P2 < Qc) P2 <<= 1;
+    for (int i = Qc + tid; i < P2; i += nthr) cand[i] = -1;
     __syncthreads();
     bitonic_desc(cand, P2, tid, nthr);
-    const int c0 = min(Q, R);
+    const int c0 = min(Qc, R);
     for (int i = tid; i < c0; i += nthr) s_occ[i] = cand[i];
     if (tid == 0) s_c0 = c0;
   } else if (tid == 0) {
@@ -578,18 +625,28 @@ __global__ void __launch_bounds__(640) propose_kernel(const ProposeArgs a) {
   }
 }
 
+// Two instantiations: up to 12 warps with room for two CTAs per SM, and up
+// to 20 warps with one.
+template <int MAXT, int MINB>
+__global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a) {
+  propose_body(a);
+}
+
 }  // namespace
 
 size_t propose_smem_bytes(int nself, int R, int k, int cand_cap) {
   const size_t big = (size_t)max(cand_cap, R * k);
-  return sizeof(int) * ((size_t)MAX_D + (size_t)nself * R + 2 * (size_t)R + big);
+  return sizeof(int) * ((size_t)MAX_D + (size_t)nself * R + 2 * (size_t)R + big) + LCAP;
 }
 
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   if (a.B <= 0) return cudaSuccess;
   const int warps = a.nself + (a.desc ? NPROBE : 0);
   const size_t smem = propose_smem_bytes(a.nself, a.R, a.k, a.cand_cap);
-  propose_kernel<<<a.B, 32 * warps, smem, st>>>(a);
+  if (warps <= 12)
+    propose_kernel<384, 2><<<a.B, 32 * warps, smem, st>>>(a);
+  else
+    propose_kernel<640, 1><<<a.B, 32 * warps, smem, st>>>(a);
   return cudaGetLastError();
 }
 
@@ -601,7 +658,11 @@ cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, i
 }
 
 cudaError_t propose_set_smem_limit(size_t bytes) {
-  return cudaFuncSetAttribute(propose_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  cudaError_t e = cudaFuncSetAttribute(propose_kernel<384, 2>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(propose_kernel<640, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)bytes);
 }
 
 }  // namespace sgd

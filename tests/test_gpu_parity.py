@@ -277,16 +277,18 @@ def test_empty_batch_and_small_rows():
 
 
 # ---------------------------------------------------------------------------
-def test_ring_and_snapshot_match_oracle():
+@pytest.mark.parametrize("max_m", [8, 64])
+def test_ring_and_snapshot_match_oracle(max_m):
+    """Small calls run as one CTA, larger ones as measure/plan/copy kernels."""
     SuffixDrafter, W, O, H = _mods()
-    rng = np.random.default_rng(8)
-    V, S, C, MD = 50, 64, 500, 12
+    rng = np.random.default_rng(8 + max_m)
+    V, S, C, MD = 50, 64, 500 if max_m == 8 else 2000, 12 if max_m == 8 else 40
     dr = SuffixDrafter(max_batch=16, seq_capacity=S, vocab_size=V, k=4, corpus_capacity=C,
-                       max_docs=MD, max_ingest_docs=16)
+                       max_docs=MD, max_ingest_docs=max_m)
     ring = O.Ring(C, MD, V)
     side = torch.cuda.Stream()
     for it in range(40):
-        m = int(rng.integers(1, 9))
+        m = int(rng.integers(1, max_m + 1))
         buf = rng.integers(0, V, size=(m, S)).astype(np.int32)
         buf[rng.random((m, S)) < 0.01] = V + 3          # occasional bad id -> truncation
         rows = np.arange(m, dtype=np.int32)
@@ -295,7 +297,7 @@ def test_ring_and_snapshot_match_oracle():
         lens[0] = min(lens[0], S - starts[0])
         if it % 7 == 3:
             rows[-1] = 99                                 # bad row -> skipped
-        num = np.full(16, S, dtype=np.int32)
+        num = np.full(max_m, S, dtype=np.int32)
         dr.ingest(_dev(buf), _dev(rows), _dev(starts), _dev(lens), num_tokens=_dev(num[:m]))
         f_orc = ring.ingest(buf, rows, starts, lens, num_tokens=num[:m])
         assert dr.get_error(clear=True) == f_orc
