@@ -41,6 +41,7 @@ struct sgd_ctx {
   int32_t *d_doc_len = nullptr;
   int32_t *d_text[2] = {nullptr, nullptr};
   int32_t *d_sa[2] = {nullptr, nullptr};
+  int4 *d_keys[2] = {nullptr, nullptr};
   CorpusDesc *d_desc = nullptr;
   IngestScratch ing{};
   SaScratch sa{};
@@ -114,6 +115,7 @@ void free_ctx(sgd_ctx *x) {
   for (int i = 0; i < 2; ++i) {
     cudaFree(x->d_text[i]);
     cudaFree(x->d_sa[i]);
+    cudaFree(x->d_keys[i]);
   }
   cudaFree(x->d_desc);
   cudaFree(x->ing.eff);
@@ -156,6 +158,10 @@ void worker_main(sgd_ctx *x) {
       const int r = sa_build(x->sa, x->d_text[back], n, x->d_sa[back], x->d_build_err, side, &st,
                              true, &launches);
       if (r != 0) status = SGD_EBUILD;
+      if (r == 0 && launch_suffix_keys(x->d_text[back], x->d_sa[back], n, x->d_keys[back], side) !=
+                        cudaSuccess)
+        status = SGD_EBUILD;
+      ++launches;
       e = cudaEventRecord(x->ev_b1, side);
       if (e == cudaSuccess)
         e = cudaMemcpyAsync(x->h_err, x->d_build_err, 4, cudaMemcpyDeviceToHost, side);
@@ -281,6 +287,7 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
     for (int i = 0; i < 2; ++i) {
       al((void **)&x->d_text[i], (size_t)C * 4);
       al((void **)&x->d_sa[i], (size_t)C * 4);
+      al((void **)&x->d_keys[i], (size_t)C * 16);
     }
     al((void **)&x->d_desc, sizeof(CorpusDesc));
     al((void **)&x->ing.eff, (size_t)cfg->max_ingest_docs * 4);
@@ -291,7 +298,7 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_start, 0, (size_t)cfg->max_docs * 8);
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_len, 0, (size_t)cfg->max_docs * 4);
     if (e == cudaSuccess) {
-      CorpusDesc d0{x->d_text[0], x->d_sa[0], 0, 0};
+      CorpusDesc d0{x->d_text[0], x->d_sa[0], x->d_keys[0], 0, 0, 0};
       e = cudaMemcpy(x->d_desc, &d0, sizeof(d0), cudaMemcpyHostToDevice);
     }
     if (e == cudaSuccess) e = cudaMallocHost((void **)&x->h_n, 8);
@@ -480,8 +487,8 @@ int sgd_poll(sgd_ctx *x, int wait, int64_t timeout_us, void *stream, uint64_t *g
     return SGD_EBUILD;
   }
   const int back = 1 - x->front;
-  const cudaError_t e = launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->built_n,
-                                    x->gen + 1, (cudaStream_t)stream);
+  const cudaError_t e = launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->d_keys[back],
+                                    x->built_n, x->gen + 1, (cudaStream_t)stream);
   if (e != cudaSuccess) return SGD_ECUDA;
   x->launches++;
   x->front = back;

@@ -207,12 +207,30 @@ __global__ void __launch_bounds__(256) linearize_kernel(const int32_t *ring, lon
   if (blockIdx.x == 0 && threadIdx.x == 0) rs->snap_n = live;
 }
 
-__global__ void swap_kernel(CorpusDesc *desc, const int32_t *text, const int32_t *sa, long long n,
-                            uint64_t gen) {
+__global__ void swap_kernel(CorpusDesc *desc, const int32_t *text, const int32_t *sa,
+                            const int4 *keys, long long n, uint64_t gen) {
   desc->text = text;
   desc->sa = sa;
+  desc->keys = keys;
   desc->n = n;
   desc->gen = gen;
+}
+
+// The first four tokens of every suffix, in suffix-array order.  Corpus
+// tokens are in [0, V], so KEY_END (INT_MIN) marks the end of the text and
+// sorts below every token, as the end of the text does in the suffix order.
+__global__ void __launch_bounds__(256) suffix_keys_kernel(const int32_t *text, const int32_t *sa,
+                                                          long long n, int4 *keys) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x; p < n; p += stride) {
+    const long long i = sa[p];
+    int4 k;
+    k.x = i < n ? text[i] : KEY_END;
+    k.y = i + 1 < n ? text[i + 1] : KEY_END;
+    k.z = i + 2 < n ? text[i + 2] : KEY_END;
+    k.w = i + 3 < n ? text[i + 3] : KEY_END;
+    keys[p] = k;
+  }
 }
 
 }  // namespace
@@ -248,9 +266,18 @@ cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs, cons
   return cudaGetLastError();
 }
 
-cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, int64_t n,
-                        uint64_t gen, cudaStream_t st) {
-  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, n, gen);
+cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
+                        int64_t n, uint64_t gen, cudaStream_t st) {
+  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, n, gen);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_suffix_keys(const int32_t *text, const int32_t *sa, int64_t n, int4 *keys,
+                               cudaStream_t st) {
+  if (n <= 0) return cudaSuccess;
+  long long blocks = (n + 1023) / 1024;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  suffix_keys_kernel<<<(int)blocks, 256, 0, st>>>(text, sa, n, keys);
   return cudaGetLastError();
 }
 

@@ -10,11 +10,20 @@
 //     min_token_prob), section 5 (max_model_len - num_tokens - 1).
 //
 // CTA layout: `nself` warps scan the row for the self match (warp-per-segment,
-// int4 loads, ballot early-outs) while, when a corpus exists, 4 more warps
-// run the suffix-array probes (32-ary searches).  The whole CTA then scans
-// the probe interval with batched loads, and warp 0 runs the depth-wise
-// vote.  All decisions are integer; the only floating-point values are the
-// reported probabilities and score.
+// int4 loads, ballot early-outs) while, when a corpus exists, 3 more warps
+// find the suffix-array intervals of the last 4, 3 and 2 tokens by a 32-ary
+// descent of the suffix-key array.  The whole CTA then evaluates the hits of
+// the longest useful interval, and warp 0 runs the depth-wise vote.  All
+// decisions are integer; the only floating-point values are the reported
+// probabilities and score.
+//
+// Corpus levels.  An end e matches >= 4 tokens iff the suffix starting at
+// e-3 begins with the last 4 tokens (the P4 interval), and likewise for 3 and
+// 2.  If no P4 hit has a continuation, every valid end matching >= 3 tokens
+// matches exactly 3, so the valid P3 hits (read from the key array alone)
+// are the answer; if there are none, the valid P2 hits are.  A level is
+// evaluated only when its longest possible match exceeds the row's own
+// match, which leaves the chosen source and its occurrences unchanged.
 #include <climits>
 
 #include "sgd_internal.h"
@@ -23,7 +32,10 @@ namespace sgd {
 
 namespace {
 
-constexpr int LCAP = 16384;  // interval entries whose match length is cached on chip
+constexpr int LCAP = 16384;    // P4 hits whose match length is cached on chip
+constexpr int NPROBE3 = 3;     // probe warps: P4, P3, P2
+constexpr int TOP_KEYS = 32;   // staged keys of the top level of the descent
+constexpr int MID_KEYS = 1024; // staged keys of the level below it
 
 __device__ __forceinline__ int4 load_win(const int32_t *row, int widx, int lane, int S) {
   const int p = widx * WIN + 4 * lane;
@@ -108,77 +120,127 @@ __device__ __forceinline__ void self_window(int wi, const int4 &cur, const int4 
   }
 }
 
-// Warp w scans windows [wlo, whi] from the top down (most recent first).
-__device__ void self_scan(const int32_t *row, int n, int S, int D, int R, const int *s_tail, int *list,
-                          int w, int nself, int lane, int &Mw, int &cnt) {
-  Mw = 0;
-  cnt = 0;
+// The windows of warp w: [wlo, whi], scanned from the top down (most recent
+// first).  The first five are loaded before the tail is known (their loads
+// overlap the tail's), the rest five ahead of use.
+struct SelfScan {
+  int wlo, whi;
+  int4 b0, b1, b2, b3, b4;
+};
+
+__device__ __forceinline__ void self_prefetch(const int32_t *row, int n, int S, int w, int nself,
+                                              int lane, SelfScan &sc) {
   const int J = n - 1;
+  sc.wlo = 0;
+  sc.whi = -1;
+  const int4 z = make_int4(0, 0, 0, 0);
+  sc.b0 = sc.b1 = sc.b2 = sc.b3 = sc.b4 = z;
   if (J <= 0) return;
   const int nwin = (J + WIN - 1) / WIN;
   const int per = (nwin + nself - 1) / nself;
-  const int wlo = w * per;
-  const int whi = min(nwin, wlo + per) - 1;
-  if (whi < wlo) return;
+  sc.wlo = w * per;
+  sc.whi = min(nwin, sc.wlo + per) - 1;
+  if (sc.whi < sc.wlo) return;
+  sc.b0 = load_win(row, sc.whi, lane, S);
+  sc.b1 = load_win(row, sc.whi - 1, lane, S);
+  if (sc.whi - 2 >= sc.wlo - 1) sc.b2 = load_win(row, sc.whi - 2, lane, S);
+  if (sc.whi - 3 >= sc.wlo - 1) sc.b3 = load_win(row, sc.whi - 3, lane, S);
+  if (sc.whi - 4 >= sc.wlo - 1) sc.b4 = load_win(row, sc.whi - 4, lane, S);
+}
+
+__device__ void self_process(const int32_t *row, int n, int S, int D, int R, const int *s_tail,
+                             int *list, int lane, SelfScan &sc, int &Mw, int &cnt) {
+  Mw = 0;
+  cnt = 0;
+  if (sc.whi < sc.wlo) return;
+  const int J = n - 1;
   const int t0 = s_tail[0];
   const int4 z = make_int4(0, 0, 0, 0);
-  int4 b0 = load_win(row, whi, lane, S);
-  int4 b1 = load_win(row, whi - 1, lane, S);
-  int4 b2 = whi - 2 >= wlo - 1 ? load_win(row, whi - 2, lane, S) : z;
-  int4 b3 = whi - 3 >= wlo - 1 ? load_win(row, whi - 3, lane, S) : z;
-  int4 b4 = whi - 4 >= wlo - 1 ? load_win(row, whi - 4, lane, S) : z;
-  for (int wi = whi; wi >= wlo; --wi) {
+  for (int wi = sc.whi; wi >= sc.wlo; --wi) {
     const int nx = wi - 5;
-    const int4 nb = nx >= wlo - 1 ? load_win(row, nx, lane, S) : z;
-    self_window(wi, b0, b1, lane, J, D, s_tail, t0, R, list, Mw, cnt);
-    b0 = b1; b1 = b2; b2 = b3; b3 = b4; b4 = nb;
+    const int4 nb = nx >= sc.wlo - 1 ? load_win(row, nx, lane, S) : z;
+    self_window(wi, sc.b0, sc.b1, lane, J, D, s_tail, t0, R, list, Mw, cnt);
+    sc.b0 = sc.b1; sc.b1 = sc.b2; sc.b2 = sc.b3; sc.b3 = sc.b4; sc.b4 = nb;
   }
 }
 
-// Three-way compare of the suffix starting at SA[q] with pattern P[0..m):
-// token by token as signed int32; running off the text sorts first.
-__device__ __forceinline__ int cmp_suffix(const int32_t *SA, const int32_t *X, long long N, long long q,
-                                          const int *P, int m) {
-  const long long i = __ldg(SA + q);
-#pragma unroll
-  for (int u = 0; u < 4; ++u) {
-    if (u >= m) break;
-    if (i + u >= N) return -1;
-    const int x = __ldg(X + i + u);
-    if (x != P[u]) return x < P[u] ? -1 : 1;
-  }
+// ---------------------------------------------------------------------------
+// corpus: key-array descent
+
+// First m tokens of a suffix key against the pattern P (signed order).
+__device__ __forceinline__ int key_cmp(const int4 &k, const int4 &P, int m) {
+  if (k.x != P.x) return k.x < P.x ? -1 : 1;
+  if (m < 2) return 0;
+  if (k.y != P.y) return k.y < P.y ? -1 : 1;
+  if (m < 3) return 0;
+  if (k.z != P.z) return k.z < P.z ? -1 : 1;
+  if (m < 4) return 0;
+  if (k.w != P.w) return k.w < P.w ? -1 : 1;
   return 0;
 }
 
-// First q in [0, N) whose suffix compares >= P (upper = false) or > P
-// (upper = true) on its first m tokens; N if none.  A warp probes 32 evenly
-// spaced positions per step, narrowing the range 33-fold.
-__device__ long long kary_search(const int32_t *SA, const int32_t *X, long long N, const int *P, int m,
-                                 bool upper, int lane) {
-  long long lo = 0, hi = N;
-  while (lo < hi) {
-    const long long len = hi - lo;
-    const bool small = len <= 32;
-    const long long q = small ? lo + lane : lo + (len * (lane + 1)) / 33;
-    bool pr = false;
-    if (!small || lane < len) {
-      const int c = cmp_suffix(SA, X, N, q, P, m);
-      pr = upper ? (c > 0) : (c >= 0);
-    }
-    const unsigned bal = __ballot_sync(FULL, pr);
-    if (small) return bal ? lo + (__ffs(bal) - 1) : hi;
-    if (bal == 0) {
-      lo = __shfl_sync(FULL, q, 31) + 1;
-    } else {
-      const int f = __ffs(bal) - 1;
-      const long long qf = __shfl_sync(FULL, q, f);
-      const long long qp = __shfl_sync(FULL, q, f > 0 ? f - 1 : 0);
-      hi = qf;
-      if (f > 0) lo = qp + 1;
-    }
-  }
-  return lo;
+// Smallest level l whose samples (positions multiple of 32^l) number <= 32.
+__device__ __forceinline__ int top_level(long long N) {
+  int l = 0;
+  while (((N + (1LL << (5 * l)) - 1) >> (5 * l)) > 32) ++l;
+  return l;
 }
+
+struct Corpus {
+  const int32_t *X;
+  const int32_t *SA;
+  const int4 *K;
+  long long N;
+  int Lmax;
+  const int4 *s_top;  // K[j * 32^Lmax]
+  const int4 *s_mid;  // K[j * 32^(Lmax-1)]
+};
+
+__device__ __forceinline__ int4 key_at(const Corpus &c, int l, long long q) {
+  if (l == c.Lmax) return c.s_top[q >> (5 * l)];
+  if (l == c.Lmax - 1) return c.s_mid[q >> (5 * l)];
+  return __ldg(c.K + q);
+}
+
+__device__ __forceinline__ void narrow(long long &a, long long &b, long long q, bool v, bool pr) {
+  const unsigned bp = __ballot_sync(FULL, pr);
+  const unsigned bv = __ballot_sync(FULL, v);
+  if (bp) {
+    const int f = __ffs(bp) - 1;
+    const long long qf = __shfl_sync(FULL, q, f);
+    const long long qp = __shfl_sync(FULL, q, f > 0 ? f - 1 : 0);
+    b = qf;
+    if (f > 0) a = qp;
+  } else if (bv) {
+    a = __shfl_sync(FULL, q, 31 - __clz((int)bv));
+  }
+}
+
+// [lo, hi): the suffixes whose first m tokens equal P, by one warp.  Both
+// bounds descend together: at level l the answer lies in (a, b], and the at
+// most 32 positions strictly inside that are multiples of 32^l are probed;
+// the first probe at or above P (lower) / above P (upper) narrows it.  At
+// level 0 every position of the bracket has been probed.
+__device__ void probe_bounds(const Corpus &c, const int4 &P, int m, int lane, long long &lo,
+                             long long &hi) {
+  long long aL = -1, bL = c.N, aU = -1, bU = c.N;
+  for (int l = c.Lmax; l >= 0; --l) {
+    const long long st = 1LL << (5 * l);
+    const long long qL = (aL < 0 ? 0 : aL + st) + (long long)lane * st;
+    const long long qU = (aU < 0 ? 0 : aU + st) + (long long)lane * st;
+    const bool vL = qL < bL, vU = qU < bU;
+    bool pL = false, pU = false;
+    if (vL) pL = key_cmp(key_at(c, l, qL), P, m) >= 0;
+    if (vU) pU = key_cmp(key_at(c, l, qU), P, m) > 0;
+    narrow(aL, bL, qL, vL, pL);
+    narrow(aU, bU, qU, vU, pU);
+  }
+  lo = bL;
+  hi = bU;
+}
+
+// ---------------------------------------------------------------------------
+// corpus: the P4 level (random access into the text)
 
 // Backward extension of a corpus end e already known to match l0 tokens.
 __device__ __forceinline__ int extend(const int32_t *X, long long e, int l0, const int *s_tail, int n,
@@ -189,27 +251,22 @@ __device__ __forceinline__ int extend(const int32_t *X, long long e, int l0, con
   return L;
 }
 
-// Corpus end behind SA entry p for a pattern of length lvl, if it has a
-// continuation (X[e+1] != Z); returns its match length, or 0.
-__device__ __forceinline__ int corpus_entry(const int32_t *SA, const int32_t *X, long long N, int Z,
-                                            long long p, int lvl, const int *s_tail, int n, int D,
-                                            long long &e) {
-  e = (long long)__ldg(SA + p) + lvl - 1;
-  if (e + 1 >= N) return 0;
-  if (__ldg(X + e + 1) == Z) return 0;
-  return extend(X, e, lvl, s_tail, n, D);
+// Match length of the end behind P4 hit p, 0 without a continuation.
+__device__ __forceinline__ int p4_entry(const Corpus &c, int Z, long long p, const int *s_tail, int n,
+                                        int D, long long &e) {
+  e = (long long)__ldg(c.SA + p) + 3;
+  if (e + 1 >= c.N) return 0;
+  if (__ldg(c.X + e + 1) == Z) return 0;
+  return extend(c.X, e, 4, s_tail, n, D);
 }
 
-// Match length of every end in the SA interval [lo, hi) of a pattern of
-// length lvl, by the whole CTA.  Each thread takes 4 entries per round and
-// issues their loads together (SA entries, then the continuation token and
-// the first token before the pattern), so a long interval costs a few
-// dependent round trips per round rather than one chain per entry.  The
-// length of entry lo + i (0 for an end without continuation) is kept in
-// s_L[i] for i < lcap; s_lhist[L] counts the valid ends of each length.
-__device__ void scan_interval(const int32_t *SA, const int32_t *X, long long N, int Z, long long lo,
-                              long long hi, int lvl, const int *s_tail, int n, int D,
-                              unsigned char *s_L, int lcap, int *s_lhist, int tid, int nthr) {
+// Match lengths of the P4 hits [lo, hi), by the whole CTA.  Each thread
+// takes 4 hits per round and issues their loads together (SA entries, then
+// the continuation token and the token before the pattern).  The length of
+// hit lo + i (0 without a continuation) is kept in s_L[i] for i < LCAP;
+// s_lhist[L] counts the valid ends of each length.
+__device__ void scan_p4(const Corpus &c, int Z, long long lo, long long hi, const int *s_tail, int n,
+                        int D, unsigned char *s_L, int *s_lhist, int tid, int nthr) {
   const long long dn = min(D, n);
   for (long long base = lo + tid; base < hi; base += 4LL * nthr) {
     long long e[4];
@@ -217,13 +274,13 @@ __device__ void scan_interval(const int32_t *SA, const int32_t *X, long long N, 
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
       const long long p = base + (long long)u * nthr;
-      e[u] = p < hi ? (long long)__ldg(SA + p) + lvl - 1 : -1;
+      e[u] = p < hi ? (long long)__ldg(c.SA + p) + 3 : -1;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
-      const bool ok = e[u] >= 0 && e[u] + 1 < N;
-      x1[u] = ok ? __ldg(X + e[u] + 1) : Z;
-      x0[u] = ok && lvl < min(dn, e[u] + 1) ? __ldg(X + e[u] - lvl) : 0;
+      const bool ok = e[u] >= 0 && e[u] + 1 < c.N;
+      x1[u] = ok ? __ldg(c.X + e[u] + 1) : Z;
+      x0[u] = ok && 4 < min(dn, e[u] + 1) ? __ldg(c.X + e[u] - 4) : 0;
     }
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -232,30 +289,45 @@ __device__ void scan_interval(const int32_t *SA, const int32_t *X, long long N, 
       int L = 0;
       if (x1[u] != Z) {
         const long long lim = min(dn, e[u] + 1);
-        L = lvl;
+        L = 4;
         if (L < lim && x0[u] == s_tail[L]) {
           ++L;
-          while (L < lim && __ldg(X + e[u] - L) == s_tail[L]) ++L;
+          while (L < lim && __ldg(c.X + e[u] - L) == s_tail[L]) ++L;
         }
         atomicAdd(&s_lhist[L], 1);
       }
-      if (p - lo < lcap) s_L[p - lo] = (unsigned char)L;
+      if (p - lo < LCAP) s_L[p - lo] = (unsigned char)L;
     }
   }
 }
 
-// Match length of SA entry p during selection: from the cache when scanned
-// into it, else recomputed.
-__device__ __forceinline__ int entry_len(const int32_t *SA, const int32_t *X, long long N, int Z,
-                                         long long p, long long lo, int lvl, const int *s_tail, int n,
-                                         int D, const unsigned char *s_L, int lcap, long long &e) {
-  if (p - lo < lcap) {
-    e = (long long)__ldg(SA + p) + lvl - 1;
-    return s_L[p - lo];
-  }
-  return corpus_entry(SA, X, N, Z, p, lvl, s_tail, n, D, e);
+// ---------------------------------------------------------------------------
+// corpus: the P3 / P2 levels (key array only)
+
+// A P3 (lvl 3) or P2 (lvl 2) hit is valid when the suffix has a token after
+// the pattern that is not a sentinel; its end is SA[p] + lvl - 1.
+__device__ __forceinline__ bool short_valid(const int4 &k, int lvl, int Z) {
+  const int t = lvl == 2 ? k.z : k.w;
+  return t != Z && t != KEY_END;
 }
 
+// Whether hit p of the chosen level is one of the ends of length Mc.
+__device__ __forceinline__ bool selects(const Corpus &c, int Z, long long p, long long lo, int lvl,
+                                        int Mc, const int *s_tail, int n, int D,
+                                        const unsigned char *s_L, long long &e) {
+  if (lvl == 4) {
+    if (p - lo < LCAP) {
+      e = (long long)__ldg(c.SA + p) + 3;
+      return s_L[p - lo] == Mc;
+    }
+    return p4_entry(c, Z, p, s_tail, n, D, e) == Mc;
+  }
+  const int4 k = __ldg(c.K + p);
+  e = (long long)__ldg(c.SA + p) + lvl - 1;
+  return short_valid(k, lvl, Z);
+}
+
+// ---------------------------------------------------------------------------
 // Descending bitonic sort of s[0..P2) (P2 a power of two), whole CTA.
 __device__ void bitonic_desc(int *s, int P2, int tid, int nthr) {
   for (int k2 = 2; k2 <= P2; k2 <<= 1) {
@@ -312,26 +384,40 @@ __global__ void __launch_bounds__(128) update_kernel(int32_t *tok, int32_t *ntok
   }
 }
 
+// ---------------------------------------------------------------------------
 __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   extern __shared__ __align__(16) int dsm[];
   __shared__ int s_wM[MAX_SELF_WARPS], s_wcnt[MAX_SELF_WARPS];
   __shared__ int s_hist[256];
-  __shared__ long long s_bound[NPROBE];
   __shared__ int s_lhist[MAX_D + 1];
-  __shared__ int s_n, s_Ms, s_cs, s_c0, s_q, s_sel, s_need, s_corpus_ok;
+  __shared__ long long s_bound[2 * NPROBE3];
+  __shared__ int s_n, s_Ms, s_cs, s_c0, s_q, s_sel, s_need, s_have_corpus;
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
-  const int S = a.S, R = a.R, k = a.k, D = a.D;
+  const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
   int32_t *row = a.tok + (size_t)b * S;
+  const int big = max(a.cand_cap, R * k);
   int *s_tail = dsm;                   // MAX_D
   int *s_wlist = s_tail + MAX_D;       // nself * R
   int *s_occ = s_wlist + a.nself * R;  // R
   int *s_run = s_occ + R;              // R
   int *s_big = s_run + R;              // max(cand_cap, R * k)
-  unsigned char *s_L = reinterpret_cast<unsigned char *>(s_big + max(a.cand_cap, R * k));  // LCAP
+  const int koff = (MAX_D + a.nself * R + 2 * R + big + 3) & ~3;
+  int4 *s_top = reinterpret_cast<int4 *>(dsm + koff);                  // TOP_KEYS
+  int4 *s_mid = s_top + TOP_KEYS;                                      // MID_KEYS
+  unsigned char *s_L = reinterpret_cast<unsigned char *>(s_mid + MID_KEYS);  // LCAP
 
-  // ---- the row's length, and the update when fused ----
+  // ---- phase 0: warp 0 updates the row; the others fetch the snapshot
+  // descriptor and stage the top two levels of its key array ----
+  Corpus cp{nullptr, nullptr, nullptr, 0, 0, s_top, s_mid};
+  if (a.desc != nullptr) {
+    cp.X = a.desc->text;
+    cp.SA = a.desc->sa;
+    cp.K = a.desc->keys;
+    cp.N = a.desc->n;
+    cp.Lmax = cp.N >= 2 ? top_level(cp.N) : 0;
+  }
   if (warp == 0) {
     int n = a.ntok[b];
     uint32_t fl = 0;
@@ -342,6 +428,15 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
       if (a.do_update) a.ntok[b] = n;
       if (fl) atomicOr(a.err, fl);
       s_n = n;
+      s_have_corpus = a.desc != nullptr && cp.N >= 2;
+    }
+  } else if (a.desc != nullptr && cp.N >= 2) {
+    const int sh = 5 * cp.Lmax;
+    const long long ntop = (cp.N + (1LL << sh) - 1) >> sh;
+    const long long nmid = cp.Lmax > 0 ? (cp.N + (1LL << (sh - 5)) - 1) >> (sh - 5) : 0;
+    for (long long j = tid - 32; j < ntop + nmid; j += nthr - 32) {
+      if (j < ntop) s_top[j] = __ldg(cp.K + (j << sh));
+      else s_mid[j - ntop] = __ldg(cp.K + ((j - ntop) << (sh - 5)));
     }
   }
   __syncthreads();
@@ -360,42 +455,33 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
     }
     return;
   }
+  const bool corpus_ok = s_have_corpus && D >= 2 && n >= 2;
 
-  // ---- tail[i] = t[n-1-i] ----
+  // ---- phase 1: tail[i] = t[n-1-i]; self warps prefetch their first windows ----
   const int dl = min(D, n);
   for (int i = tid; i < dl; i += nthr) s_tail[i] = row[n - 1 - i];
-  if (tid == 0) {
-    s_corpus_ok = a.desc != nullptr && D >= 2 && n >= 2 && a.desc->n >= 2;
-  }
+  SelfScan sc;
+  if (warp < a.nself) self_prefetch(row, n, S, warp, a.nself, lane, sc);
   __syncthreads();
 
-  const int Z = a.V;
-  const int32_t *X = nullptr, *SA = nullptr;
-  long long N = 0;
-  if (s_corpus_ok) {
-    X = a.desc->text;
-    SA = a.desc->sa;
-    N = a.desc->n;
-  }
-
-  // ---- self match (nself warps) || suffix-array probes (4 warps) ----
+  // ---- phase 2: self match (nself warps) || interval probes (3 warps) ----
   if (warp < a.nself) {
     int Mw, cnt;
-    self_scan(row, n, S, D, R, s_tail, s_wlist + warp * R, warp, a.nself, lane, Mw, cnt);
+    self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, lane, sc, Mw, cnt);
     if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; }
-  } else if (s_corpus_ok) {
-    const int pw = warp - a.nself;
-    const bool use4 = D >= 4 && n >= 4;
-    const int m = pw < 2 ? 4 : 2;
-    if (pw >= 2 || use4) {
-      int P[4];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) P[u] = u < m ? s_tail[m - 1 - u] : 0;
-      const long long r = kary_search(SA, X, N, P, m, (pw & 1) != 0, lane);
-      if (lane == 0) s_bound[pw] = r;
-    } else if (lane == 0) {
-      s_bound[pw] = 0;
+  } else if (corpus_ok) {
+    const int pw = warp - a.nself;  // 0: last 4 tokens, 1: last 3, 2: last 2
+    const int m = 4 - pw;
+    long long lo = 0, hi = 0;
+    if (D >= m && n >= m) {
+      const int4 P = make_int4(s_tail[m - 1], m >= 2 ? s_tail[m - 2] : 0, m >= 3 ? s_tail[m - 3] : 0,
+                               m >= 4 ? s_tail[m - 4] : 0);
+      // a pattern holding KEY_END cannot occur: corpus tokens are in [0, V]
+      const bool endless = P.x != KEY_END && (m < 2 || P.y != KEY_END) &&
+                           (m < 3 || P.z != KEY_END) && (m < 4 || P.w != KEY_END);
+      if (endless) probe_bounds(cp, P, m, lane, lo, hi);
     }
+    if (lane == 0) { s_bound[2 * pw] = lo; s_bound[2 * pw + 1] = hi; }
   }
   __syncthreads();
 
@@ -417,37 +503,56 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   __syncthreads();
   const int Ms = s_Ms;
 
-  // ---- corpus: longest match among the probe hits, where it can still win ----
-  // Ends with a match >= 4 are exactly the P4 hits; if none of them has a
-  // continuation, valid matches of 2 or 3 are exactly the valid P2 hits.  A
-  // level is scanned only if its longest possible match exceeds Ms, which
-  // leaves the chosen source and its occurrences unchanged.
-  int Mc = 0, lvl = 4;
+  // ---- corpus level: the longest match among the hits, where it can win ----
+  int Mc = 0, lvl = 0, Q = 0;
   long long lo = 0, hi = 0;
-  if (s_corpus_ok) {
-    const int dn = min(D, n);
-    const bool use4 = D >= 4 && n >= 4;
-    bool have4 = false;
-    for (int pass = 0; pass < 2; ++pass) {
-      const int L_hi = pass == 0 ? dn : min(3, dn);
-      if (pass == 0 && !use4) continue;
-      if (pass == 1 && have4) break;
-      if (Ms >= L_hi) break;
-      const int lv = pass == 0 ? 4 : 2;
-      const long long l0 = pass == 0 ? s_bound[0] : s_bound[2];
-      const long long h0 = pass == 0 ? s_bound[1] : s_bound[3];
-      if (h0 <= l0) continue;
-      __syncthreads();  // the previous pass's histogram has been read
+  if (corpus_ok && Ms < dl) {
+    bool decided = false;
+    if (D >= 4 && n >= 4 && s_bound[1] > s_bound[0]) {
       for (int i = tid; i <= MAX_D; i += nthr) s_lhist[i] = 0;
       __syncthreads();
-      scan_interval(SA, X, N, Z, l0, h0, lv, s_tail, n, D, s_L, LCAP, s_lhist, tid, nthr);
+      scan_p4(cp, Z, s_bound[0], s_bound[1], s_tail, n, D, s_L, s_lhist, tid, nthr);
       __syncthreads();
-      int best = 0;
-      for (int L = dn; L >= 1; --L)
-        if (s_lhist[L] > 0) { best = L; break; }
-      if (best > 0) {
-        if (pass == 0) have4 = true;
-        if (best >= 2) { Mc = best; lvl = lv; lo = l0; hi = h0; }
+      for (int L = dl; L >= 4; --L)
+        if (s_lhist[L] > 0) {
+          Mc = L;
+          lvl = 4;
+          lo = s_bound[0];
+          hi = s_bound[1];
+          Q = s_lhist[L];
+          decided = true;
+          break;
+        }
+    }
+    for (int lv = 3; lv >= 2 && !decided; --lv) {
+      if (D < lv || n < lv) continue;
+      if (Ms >= lv) break;  // neither this level nor the next can win
+      const long long l0 = s_bound[2 * (4 - lv)], h0 = s_bound[2 * (4 - lv) + 1];
+      if (h0 <= l0) continue;
+      __syncthreads();  // s_q from an earlier level has been read
+      if (tid == 0) s_q = 0;
+      __syncthreads();
+      int cnt = 0;
+      for (long long p = l0 + tid; p < h0; p += 4LL * nthr) {
+        int4 kk[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const long long q = p + (long long)u * nthr;
+          kk[u] = q < h0 ? __ldg(cp.K + q) : make_int4(Z, Z, Z, Z);
+        }
+#pragma unroll
+        for (int u = 0; u < 4; ++u) cnt += short_valid(kk[u], lv, Z);
+      }
+      cnt = (int)__reduce_add_sync(FULL, (unsigned)cnt);
+      if (lane == 0 && cnt) atomicAdd(&s_q, cnt);
+      __syncthreads();
+      if (s_q > 0) {
+        Mc = lv;
+        lvl = lv;
+        lo = l0;
+        hi = h0;
+        Q = s_q;
+        decided = true;
       }
     }
   }
@@ -456,16 +561,15 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   else { src = Ms > 0 ? 1 : 0; M = Ms; }
 
   if (src == 2) {
-    // the R largest ends with length Mc (cached lengths; no second random pass)
+    // the R largest ends among the Q of length Mc
     int *cand = s_big;
-    const int Q = s_lhist[Mc];
+    __syncthreads();
     if (Q <= a.cand_cap) {
       if (tid == 0) s_q = 0;
       __syncthreads();
       for (long long p = lo + tid; p < hi; p += nthr) {
         long long e;
-        if (entry_len(SA, X, N, Z, p, lo, lvl, s_tail, n, D, s_L, LCAP, e) == Mc)
-          cand[atomicAdd(&s_q, 1)] = (int)e;
+        if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e)) cand[atomicAdd(&s_q, 1)] = (int)e;
       }
     } else {
       // more candidates than fit on chip: radix-select the R-th largest end
@@ -477,8 +581,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
         __syncthreads();
         for (long long p = lo + tid; p < hi; p += nthr) {
           long long e;
-          if (entry_len(SA, X, N, Z, p, lo, lvl, s_tail, n, D, s_L, LCAP, e) == Mc &&
-              ((unsigned)e & mask) == prefix)
+          if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e) && ((unsigned)e & mask) == prefix)
             atomicAdd(&s_hist[((unsigned)e >> shift) & 255u], 1);
         }
         __syncthreads();
@@ -498,8 +601,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
       __syncthreads();
       for (long long p = lo + tid; p < hi; p += nthr) {
         long long e;
-        if (entry_len(SA, X, N, Z, p, lo, lvl, s_tail, n, D, s_L, LCAP, e) == Mc &&
-            (unsigned)e >= prefix) {
+        if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e) && (unsigned)e >= prefix) {
           const int slot = atomicAdd(&s_q, 1);
           if (slot < a.cand_cap) cand[slot] = (int)e;
         }
@@ -540,7 +642,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
       const long long pos = (long long)s_occ[o] + 1 + d;
       int v;
       if (src == 1) v = pos <= n - 1 ? row[pos] : 0;
-      else v = pos < N ? __ldg(X + pos) : Z;
+      else v = pos < cp.N ? __ldg(cp.X + pos) : Z;
       cont[idx] = v;
     }
     __syncthreads();
@@ -636,12 +738,13 @@ __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a
 
 size_t propose_smem_bytes(int nself, int R, int k, int cand_cap) {
   const size_t big = (size_t)max(cand_cap, R * k);
-  return sizeof(int) * ((size_t)MAX_D + (size_t)nself * R + 2 * (size_t)R + big) + LCAP;
+  const size_t ints = ((size_t)MAX_D + (size_t)nself * R + 2 * (size_t)R + big + 3) & ~(size_t)3;
+  return sizeof(int) * ints + sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP;
 }
 
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   if (a.B <= 0) return cudaSuccess;
-  const int warps = a.nself + (a.desc ? NPROBE : 0);
+  const int warps = a.nself + (a.desc ? NPROBE3 : 0);
   const size_t smem = propose_smem_bytes(a.nself, a.R, a.k, a.cand_cap);
   if (warps <= 12)
     propose_kernel<384, 2><<<a.B, 32 * warps, smem, st>>>(a);

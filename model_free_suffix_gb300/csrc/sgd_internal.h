@@ -14,7 +14,7 @@ constexpr int MAX_D = 128;      // the halo of one window covers D - 1 <= 127
 constexpr int MAX_R = 128;      // up to 4 occurrences per lane in the vote warp
 constexpr int MAX_K = 64;
 constexpr int MAX_SELF_WARPS = 16;
-constexpr int NPROBE = 4;       // probe warps: {P4, P2} x {lower, upper bound}
+constexpr int MAX_PROPOSE_THREADS = 640;
 
 // Descriptor of the suffix-array snapshot drafting reads.  It lives in device
 // memory at a fixed address, so graphs captured before a swap see the new
@@ -22,9 +22,12 @@ constexpr int NPROBE = 4;       // probe warps: {P4, P2} x {lower, upper bound}
 struct CorpusDesc {
   const int32_t *text;  // X[0..n): live docs oldest first, each followed by Z
   const int32_t *sa;    // suffix array of X
+  const int4 *keys;     // keys[p] = X[sa[p] .. sa[p]+3], KEY_END past the text
   int64_t n;
   uint64_t gen;
+  int64_t pad;
 };
+constexpr int KEY_END = (int)0x80000000;  // below every id: the text ran out
 
 // Ring bookkeeping, device resident.  The doc FIFO lives in two arrays of
 // max_docs entries indexed (head + i) % max_docs.
@@ -78,8 +81,11 @@ cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S,
 cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs,
                              const int64_t *doc_start, int max_docs, int32_t *out,
                              cudaStream_t st, int *launches);
-cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, int64_t n,
-                        uint64_t gen, cudaStream_t st);
+cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
+                        int64_t n, uint64_t gen, cudaStream_t st);
+// keys[p] = text[sa[p] .. sa[p]+3] (KEY_END past n), on `st`
+cudaError_t launch_suffix_keys(const int32_t *text, const int32_t *sa, int64_t n, int4 *keys,
+                               cudaStream_t st);
 
 // sa_build.cu
 struct SaScratch {
