@@ -243,12 +243,28 @@ __device__ void probe_bounds(const Corpus &c, const int4 &P, int m, int lane, lo
 // corpus: the P4 level (random access into the text)
 
 // Backward extension of a corpus end e already known to match l0 tokens.
+// Tokens are compared 8 at a time, their loads issued together.
+__device__ __forceinline__ int extend_from(const int32_t *X, long long e, int L, long long lim,
+                                           const int *s_tail) {
+  while (L < lim) {
+    const int cn = (int)min(8LL, lim - L);
+    int v[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) v[j] = j < cn ? __ldg(X + e - L - j) : 0;
+    int j = cn;  // first mismatch in the chunk
+#pragma unroll
+    for (int t = 0; t < 8; ++t)
+      if (t < j && v[t] != s_tail[L + t]) j = t;
+    L += j;
+    if (j < cn) break;
+  }
+  return L;
+}
+
 __device__ __forceinline__ int extend(const int32_t *X, long long e, int l0, const int *s_tail, int n,
                                       int D) {
   const long long lim = min((long long)min(D, n), e + 1);
-  int L = l0;
-  while (L < lim && __ldg(X + e - L) == s_tail[L]) ++L;
-  return L;
+  return extend_from(X, e, l0, lim, s_tail);
 }
 
 // Match length of the end behind P4 hit p, 0 without a continuation.
@@ -290,10 +306,7 @@ __device__ void scan_p4(const Corpus &c, int Z, long long lo, long long hi, cons
       if (x1[u] != Z) {
         const long long lim = min(dn, e[u] + 1);
         L = 4;
-        if (L < lim && x0[u] == s_tail[L]) {
-          ++L;
-          while (L < lim && __ldg(c.X + e[u] - L) == s_tail[L]) ++L;
-        }
+        if (L < lim && x0[u] == s_tail[L]) L = extend_from(c.X, e[u], L + 1, lim, s_tail);
         atomicAdd(&s_lhist[L], 1);
       }
       if (p - lo < LCAP) s_L[p - lo] = (unsigned char)L;
@@ -328,21 +341,46 @@ __device__ __forceinline__ bool selects(const Corpus &c, int Z, long long p, lon
 }
 
 // ---------------------------------------------------------------------------
-// Descending bitonic sort of s[0..P2) (P2 a power of two), whole CTA.
-__device__ void bitonic_desc(int *s, int P2, int tid, int nthr) {
-  for (int k2 = 2; k2 <= P2; k2 <<= 1) {
-    for (int j = k2 >> 1; j > 0; j >>= 1) {
-      for (int i = tid; i < P2; i += nthr) {
-        const int ixj = i ^ j;
-        if (ixj > i) {
-          const int x = s[i], y = s[ixj];
-          const bool first_half = (i & k2) == 0;
-          if (first_half ? (x < y) : (x > y)) { s[i] = y; s[ixj] = x; }
-        }
+// Radix selection step, one warp: walking the 256 bins from the top, the bin
+// where the running count first reaches `need`, and what is still needed
+// inside it.  The caller guarantees the bins hold at least `need`.
+__device__ void pick_bin(const int *hist, int need, int lane, int *s_sel, int *s_need) {
+  int h[8];
+  int tot = 0;
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    h[j] = hist[255 - (lane * 8 + j)];
+    tot += h[j];
+  }
+  int x = tot;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_up_sync(FULL, x, off);
+    if (lane >= off) x += y;
+  }
+  const unsigned m = __ballot_sync(FULL, x >= need);
+  if (lane == __ffs(m) - 1) {
+    int acc = x - tot;
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+      if (acc + h[j] >= need) {
+        *s_sel = 255 - (lane * 8 + j);
+        *s_need = need - acc;
+        break;
       }
-      __syncthreads();
+      acc += h[j];
     }
   }
+}
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 
 __device__ int update_row_warp(int32_t *row, int n, const int32_t *sp, int T, int S, int V, int lane,
@@ -390,6 +428,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   __shared__ int s_wM[MAX_SELF_WARPS], s_wcnt[MAX_SELF_WARPS];
   __shared__ int s_hist[256];
   __shared__ int s_lhist[MAX_D + 1];
+  __shared__ int s_vv[MAX_R];
   __shared__ long long s_bound[2 * NPROBE3];
   __shared__ int s_n, s_Ms, s_cs, s_c0, s_q, s_sel, s_need, s_have_corpus;
 
@@ -435,9 +474,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
     const long long ntop = (cp.N + (1LL << sh) - 1) >> sh;
     const long long nmid = cp.Lmax > 0 ? (cp.N + (1LL << (sh - 5)) - 1) >> (sh - 5) : 0;
     for (long long j = tid - 32; j < ntop + nmid; j += nthr - 32) {
-      if (j < ntop) s_top[j] = __ldg(cp.K + (j << sh));
-      else s_mid[j - ntop] = __ldg(cp.K + ((j - ntop) << (sh - 5)));
+      if (j < ntop) cp_async16(&s_top[j], cp.K + (j << sh));
+      else cp_async16(&s_mid[j - ntop], cp.K + ((j - ntop) << (sh - 5)));
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
   }
   __syncthreads();
   const int n = s_n;
@@ -462,6 +502,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   for (int i = tid; i < dl; i += nthr) s_tail[i] = row[n - 1 - i];
   SelfScan sc;
   if (warp < a.nself) self_prefetch(row, n, S, warp, a.nself, lane, sc);
+  asm volatile("cp.async.wait_all;" ::: "memory");  // staged keys landed (no-op if none)
   __syncthreads();
 
   // ---- phase 2: self match (nself warps) || interval probes (3 warps) ----
@@ -513,16 +554,18 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
       __syncthreads();
       scan_p4(cp, Z, s_bound[0], s_bound[1], s_tail, n, D, s_L, s_lhist, tid, nthr);
       __syncthreads();
-      for (int L = dl; L >= 4; --L)
-        if (s_lhist[L] > 0) {
-          Mc = L;
-          lvl = 4;
-          lo = s_bound[0];
-          hi = s_bound[1];
-          Q = s_lhist[L];
-          decided = true;
-          break;
-        }
+      int lbest = 0;
+      for (int L = 4 + lane; L <= dl; L += 32)
+        if (s_lhist[L] > 0) lbest = L;
+      lbest = (int)__reduce_max_sync(FULL, (unsigned)lbest);
+      if (lbest > 0) {
+        Mc = lbest;
+        lvl = 4;
+        lo = s_bound[0];
+        hi = s_bound[1];
+        Q = s_lhist[lbest];
+        decided = true;
+      }
     }
     for (int lv = 3; lv >= 2 && !decided; --lv) {
       if (D < lv || n < lv) continue;
@@ -560,21 +603,33 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   if (Mc > Ms) { src = 2; M = Mc; }
   else { src = Ms > 0 ? 1 : 0; M = Ms; }
 
+  // draft length bound: min(k, floor(factor * M) + offset, S - n - 1) [, D - M]
+  long long capl = 0;
+  if (M > 0) {
+    capl = min((long long)k, a.fN * M / a.fD + a.offset);
+    long long room = (long long)S - n - 1;
+    if (room < 0) room = 0;
+    capl = min(capl, room);
+    if (a.depth_sum_cap) capl = min(capl, (long long)D - M);
+    if (capl < 0) capl = 0;
+  }
+  const int cap = (int)capl;
+  int *cont = s_big;
+  // with at most R candidates every one is kept: their continuations are
+  // requested while they are collected
+  const bool prefetch = src == 2 && Q <= R;
+
   if (src == 2) {
-    // the R largest ends among the Q of length Mc
+    // The R largest ends among the Q of length Mc.  O_0 is a set (the vote
+    // does not depend on its order), so nothing is sorted.
     int *cand = s_big;
     __syncthreads();
-    if (Q <= a.cand_cap) {
-      if (tid == 0) s_q = 0;
-      __syncthreads();
-      for (long long p = lo + tid; p < hi; p += nthr) {
-        long long e;
-        if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e)) cand[atomicAdd(&s_q, 1)] = (int)e;
-      }
-    } else {
-      // more candidates than fit on chip: radix-select the R-th largest end
-      // byte by byte, then collect the R ends at or above it
-      unsigned prefix = 0, mask = 0;
+    if (tid == 0) s_q = 0;
+    unsigned prefix = 0;
+    if (Q > a.cand_cap) {
+      // more than fit on chip: radix-select the R-th largest end over the
+      // interval, byte by byte; the R ends at or above it are collected below
+      unsigned mask = 0;
       int need = R;
       for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = tid; i < 256; i += nthr) s_hist[i] = 0;
@@ -585,37 +640,60 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
             atomicAdd(&s_hist[((unsigned)e >> shift) & 255u], 1);
         }
         __syncthreads();
-        if (tid == 0) {
-          int acc = 0;
-          for (int v = 255; v >= 0; --v) {
-            if (acc + s_hist[v] >= need) { s_sel = v; s_need = need - acc; break; }
-            acc += s_hist[v];
-          }
-        }
+        if (warp == 0) pick_bin(s_hist, need, lane, &s_sel, &s_need);
         __syncthreads();
         prefix |= (unsigned)s_sel << shift;
         mask |= 255u << shift;
         need = s_need;
       }
-      if (tid == 0) s_q = 0;
-      __syncthreads();
-      for (long long p = lo + tid; p < hi; p += nthr) {
-        long long e;
-        if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e) && (unsigned)e >= prefix) {
-          const int slot = atomicAdd(&s_q, 1);
-          if (slot < a.cand_cap) cand[slot] = (int)e;
+    }
+    __syncthreads();
+    for (long long p = lo + tid; p < hi; p += nthr) {
+      long long e;
+      if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e) && (unsigned)e >= prefix) {
+        const int slot = atomicAdd(&s_q, 1);
+        if (prefetch) {
+          s_occ[slot] = (int)e;
+          for (int d = 0; d < cap; ++d) {
+            const long long pos = e + 1 + d;
+            if (pos < cp.N) cp_async4(&cont[slot * cap + d], cp.X + pos);
+            else cont[slot * cap + d] = Z;
+          }
+        } else if (slot < a.cand_cap) {
+          cand[slot] = (int)e;
         }
       }
     }
+    asm volatile("cp.async.commit_group;" ::: "memory");
     __syncthreads();
     const int Qc = min(s_q, a.cand_cap);
-    int P2 = 1;
-    while (P2 < Qc) P2 <<= 1;
-    for (int i = Qc + tid; i < P2; i += nthr) cand[i] = -1;
-    __syncthreads();
-    bitonic_desc(cand, P2, tid, nthr);
-    const int c0 = min(Qc, R);
-    for (int i = tid; i < c0; i += nthr) s_occ[i] = cand[i];
+    int c0;
+    if (Qc > R) {
+      // radix-select the R largest among the on-chip candidates
+      unsigned pf = 0, mk = 0;
+      int need = R;
+      for (int shift = 24; shift >= 0; shift -= 8) {
+        for (int i = tid; i < 256; i += nthr) s_hist[i] = 0;
+        __syncthreads();
+        for (int i = tid; i < Qc; i += nthr)
+          if (((unsigned)cand[i] & mk) == pf) atomicAdd(&s_hist[((unsigned)cand[i] >> shift) & 255u], 1);
+        __syncthreads();
+        if (warp == 0) pick_bin(s_hist, need, lane, &s_sel, &s_need);
+        __syncthreads();
+        pf |= (unsigned)s_sel << shift;
+        mk |= 255u << shift;
+        need = s_need;
+      }
+      if (tid == 0) s_q = 0;
+      __syncthreads();
+      for (int i = tid; i < Qc; i += nthr)
+        if ((unsigned)cand[i] >= pf) s_occ[atomicAdd(&s_q, 1)] = cand[i];
+      c0 = R;
+    } else {
+      if (!prefetch)
+        for (int i = tid; i < Qc; i += nthr) s_occ[i] = cand[i];
+      c0 = Qc;
+    }
     if (tid == 0) s_c0 = c0;
   } else if (tid == 0) {
     s_c0 = s_cs;
@@ -624,19 +702,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
 
   // ---- length cap and the continuation matrix ----
   const int c0 = s_c0;
-  long long capl = 0;
-  if (M > 0 && c0 > 0) {
-    capl = min((long long)k, a.fN * M / a.fD + a.offset);
-    long long room = (long long)S - n - 1;
-    if (room < 0) room = 0;
-    capl = min(capl, room);
-    if (a.depth_sum_cap) capl = min(capl, (long long)D - M);
-    if (capl < 0) capl = 0;
-  }
-  const int cap = (int)capl;
-  int *cont = s_big;
-  if (cap > 0) {
-    const int tot = c0 * cap;
+  if (prefetch) asm volatile("cp.async.wait_all;" ::: "memory");
+  if (cap > 0 && c0 > 0) {
+    const int tot = prefetch ? 0 : c0 * cap;
     for (int idx = tid; idx < tot; idx += nthr) {
       const int o = idx / cap, d = idx - o * cap;
       const long long pos = (long long)s_occ[o] + 1 + d;
@@ -661,59 +729,151 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   if (warp != 0) return;
 
   // ---- depth-wise majority vote (one warp, up to 4 occurrences per lane) ----
+  // With a reference survivor chosen at depth d, let diff(o) be the first
+  // depth >= d where survivor o disagrees with the reference or runs out.
+  // Then at depth x the survivors are {diff >= x}, the participants are those
+  // not running out at x, and the reference's token is continued by
+  // c(x) = #{diff > x}.  While the reference takes part and c(x) is a strict
+  // majority of the participants, the reference's token wins with count
+  // c(x): two histograms of diff give every c(x) at once, so a whole run of
+  // depths is decided in one warp scan.  Where the majority fails, all
+  // participants' tokens are counted (most frequent wins, ties to the
+  // smallest id) and a new reference is taken among the winners.
   int len = 0;
   long long sum = 0;
   if (cap > 0) {
     bool alive[4];
 #pragma unroll
     for (int s = 0; s < 4; ++s) alive[s] = lane + 32 * s < c0;
-    for (int d = 0; d < cap; ++d) {
-      int val[4];
+    const unsigned lt = (1u << lane) - 1u;
+    int *H = s_hist, *HR = s_hist + 128;  // diff histogram; run-outs among them
+    int d = 0;
+    while (d < cap) {
+      unsigned am[4];
+      int nalive = 0;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        am[s] = __ballot_sync(FULL, alive[s]);
+        nalive += __popc(am[s]);
+      }
+      if (nalive == 0) break;
+      const int ss = am[0] ? 0 : (am[1] ? 1 : (am[2] ? 2 : 3));
+      const unsigned mm = am[0] ? am[0] : (am[1] ? am[1] : (am[2] ? am[2] : am[3]));
+      const int ref = (__ffs(mm) - 1) + 32 * ss;
+      const int run_ref = min(s_run[ref], cap);
+      for (int i = lane; i <= cap; i += 32) { H[i] = 0; HR[i] = 0; }
+      __syncwarp();
+      int diff[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        diff[s] = cap;
+        if (!alive[s]) continue;
+        const int o = lane + 32 * s;
+        const int r = min(s_run[o], cap);
+        int dd = d;
+        while (dd < r && cont[o * cap + dd] == cont[ref * cap + dd]) ++dd;
+        diff[s] = dd;
+        atomicAdd(&H[dd], 1);
+        if (dd == r && r < cap) atomicAdd(&HR[dd], 1);
+      }
+      __syncwarp();
+      // c(x) = nalive - #{diff <= x}, for x = d + lane and x = d + 32 + lane
+      const int x1 = d + lane, x2 = d + 32 + lane;
+      const int h1 = x1 <= cap ? H[x1] : 0, h2 = x2 <= cap ? H[x2] : 0;
+      int p1 = h1, p2 = h2;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y1 = __shfl_up_sync(FULL, p1, off), y2 = __shfl_up_sync(FULL, p2, off);
+        if (lane >= off) { p1 += y1; p2 += y2; }
+      }
+      p2 += __shfl_sync(FULL, p1, 31);
+      const int c1 = nalive - p1, c2 = nalive - p2;
+      const int part1 = c1 + h1 - (x1 <= cap ? HR[x1] : 0);
+      const int part2 = c2 + h2 - (x2 <= cap ? HR[x2] : 0);
+      const bool maj1 = x1 < run_ref && 2 * c1 > part1, maj2 = x2 < run_ref && 2 * c2 > part2;
+      const bool ok1 = maj1 && (long long)c1 * a.pD >= a.pN * (long long)c0;
+      const bool ok2 = maj2 && (long long)c2 * a.pD >= a.pN * (long long)c0;
+      const unsigned bad1 = __ballot_sync(FULL, x1 < cap && !ok1);
+      const unsigned bad2 = __ballot_sync(FULL, x2 < cap && !ok2);
+      const int F = bad1 ? d + __ffs(bad1) - 1 : (bad2 ? d + 32 + __ffs(bad2) - 1 : cap);
+      // emit depths [d, F): the reference's tokens
+      long long part_sum = 0;
+      if (x1 < F) {
+        dr[x1] = cont[ref * cap + x1];
+        if (pr) pr[x1] = (float)((double)c1 / (double)c0);
+        part_sum += c1;
+      }
+      if (x2 < F) {
+        dr[x2] = cont[ref * cap + x2];
+        if (pr) pr[x2] = (float)((double)c2 / (double)c0);
+        part_sum += c2;
+      }
+      for (int off = 16; off > 0; off >>= 1) part_sum += __shfl_xor_sync(FULL, part_sum, off);
+      sum += part_sum;
+      len += F - d;
+      if (F >= cap) break;
+      // depth F: stop if the reference's majority only missed the threshold
+      const bool majF = __shfl_sync(FULL, F - d < 32 ? maj1 : maj2, (F - d) & 31);
+      if (majF) break;
+      d = F;
+      // full count among the participants at depth d
       bool part[4];
+      unsigned pm[4];
       int npart = 0;
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        const int o = lane + 32 * s;
-        part[s] = alive[s] && d < s_run[o];
-        val[s] = part[s] ? cont[o * cap + d] : 0;
-        npart += __popc(__ballot_sync(FULL, part[s]));
+        alive[s] = alive[s] && diff[s] >= d;
+        part[s] = alive[s] && d < s_run[lane + 32 * s];
+        pm[s] = __ballot_sync(FULL, part[s]);
+        npart += __popc(pm[s]);
       }
       if (npart == 0) break;
-      bool pend[4] = {part[0], part[1], part[2], part[3]};
-      int remaining = npart, best_cnt = 0, best_tok = 0;
-      while (remaining > 0) {
-        const unsigned m0 = __ballot_sync(FULL, pend[0]);
-        const unsigned m1 = __ballot_sync(FULL, pend[1]);
-        const unsigned m2 = __ballot_sync(FULL, pend[2]);
-        const unsigned m3 = __ballot_sync(FULL, pend[3]);
-        const int ss = m0 ? 0 : (m1 ? 1 : (m2 ? 2 : 3));
-        const unsigned mm = m0 ? m0 : (m1 ? m1 : (m2 ? m2 : m3));
-        const int ll = __ffs(mm) - 1;
-        const int x0 = __shfl_sync(FULL, val[0], ll);
-        const int x1 = __shfl_sync(FULL, val[1], ll);
-        const int x2 = __shfl_sync(FULL, val[2], ll);
-        const int x3 = __shfl_sync(FULL, val[3], ll);
-        const int v = ss == 0 ? x0 : (ss == 1 ? x1 : (ss == 2 ? x2 : x3));
-        int cnt = 0;
+      int val[4];
+      int base = 0;
 #pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          const bool e = pend[s] && val[s] == v;
-          cnt += __popc(__ballot_sync(FULL, e));
-          pend[s] = pend[s] && !e;
+      for (int s = 0; s < 4; ++s) {
+        val[s] = part[s] ? cont[(lane + 32 * s) * cap + d] : 0;
+        if (part[s]) s_vv[base + __popc(pm[s] & lt)] = val[s];
+        base += __popc(pm[s]);
+      }
+      __syncwarp();
+      unsigned mycnt = 0, myv = 0xffffffffu;
+      int cnt;
+      if (npart <= 32) {
+        const unsigned vm = npart == 32 ? FULL : ((1u << npart) - 1u);
+        const int v = lane < npart ? s_vv[lane] : 0;
+        if (lane < npart) mycnt = __popc(__match_any_sync(vm, v));
+        const unsigned maxc = __reduce_max_sync(FULL, mycnt);
+        if (lane < npart && mycnt == maxc) myv = (unsigned)v ^ 0x80000000u;
+        cnt = (int)maxc;
+      } else {
+        int c4[4] = {0, 0, 0, 0};
+        for (int q = 0; q < npart; ++q) {
+          const int vq = s_vv[q];
+#pragma unroll
+          for (int s = 0; s < 4; ++s) c4[s] += vq == val[s];
         }
-        if (cnt > best_cnt || (cnt == best_cnt && v < best_tok)) { best_cnt = cnt; best_tok = v; }
-        remaining -= cnt;
-        if (best_cnt > remaining) break;
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (part[s]) mycnt = max(mycnt, (unsigned)c4[s]);
+        const unsigned maxc = __reduce_max_sync(FULL, mycnt);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (part[s] && (unsigned)c4[s] == maxc) myv = min(myv, (unsigned)val[s] ^ 0x80000000u);
+        cnt = (int)maxc;
       }
-      if ((long long)best_cnt * a.pD < a.pN * (long long)c0) break;
+      const int tau = (int)(__reduce_min_sync(FULL, myv) ^ 0x80000000u);
+      __syncwarp();
+      if ((long long)cnt * a.pD < a.pN * (long long)c0) break;
       if (lane == 0) {
-        dr[d] = best_tok;
-        if (pr) pr[d] = (float)((double)best_cnt / (double)c0);
+        dr[d] = tau;
+        if (pr) pr[d] = (float)((double)cnt / (double)c0);
       }
-      sum += best_cnt;
+      sum += cnt;
       ++len;
 #pragma unroll
-      for (int s = 0; s < 4; ++s) alive[s] = part[s] && val[s] == best_tok;
+      for (int s = 0; s < 4; ++s) alive[s] = part[s] && val[s] == tau;
+      ++d;
     }
   }
   for (int d = len + lane; d < k; d += 32) {
