@@ -47,6 +47,7 @@ extern "C" {
 #define SGD_EBUSY      -5   /* a build is in flight or not yet swapped in       */
 #define SGD_EBUILD     -6   /* the finished build reported failure; old index kept */
 #define SGD_ENOCORPUS  -7   /* the context was created without a corpus         */
+#define SGD_ETOOLARGE  -8   /* longer than the fixed scratch of sgd_suffix_array_noalloc */
 
 /* ---- sticky device error bits (sgd_get_error) --------------------------- */
 #define SGD_ERR_SAMPLED_TOKEN 0x1u  /* a sampled id >= V ended the accepted prefix    */
@@ -196,6 +197,28 @@ int sgd_poll(sgd_ctx *ctx, int wait, int64_t timeout_us, void *stream, uint64_t 
  * n <= corpus_capacity.  SGD_EBUSY while a background build runs;
  * SGD_EBUILD if the sort reported a failure. */
 int sgd_suffix_array(sgd_ctx *ctx, const int32_t *text, int64_t n, int32_t *sa, void *stream);
+
+/* Suffix array of a caller text without allocating anything: no device,
+ * pinned-host or library allocation happens in the call.  This is for
+ * callers that cannot call cudaMalloc where they need the array -- a server
+ * whose own caching allocator owns the device memory, code running under
+ * another framework's memory budget, or code that must not risk an
+ * out-of-memory error or the device-wide synchronisation of cudaMalloc /
+ * cudaFree mid-work.  (The pages describe no such entry point; it has no
+ * counterpart there.)
+ *   text DEVICE int32 [n] (any values), sa DEVICE int32 [n] output, both
+ *   caller-owned; same order as sgd_suffix_array; no context is needed.
+ * The working memory is one fixed device array of the library, sized for
+ * SGD_NOALLOC_MAX_TOKENS tokens (about 3 MB, held on every GPU that loads the
+ * library until the process exits); longer texts return SGD_ETOOLARGE.  The
+ * first call on a device (with that device current) looks the array up on
+ * that device; make that first call before any stream capture.  All calls
+ * share the array and it keeps the previous call's contents: calls whose GPU
+ * work overlaps (two streams, two threads, two processes' graphs) race;
+ * host threads are serialised inside the call.  Blocks the host until the
+ * array is written.  SGD_EBUILD if the sort reported a failure. */
+#define SGD_NOALLOC_MAX_TOKENS 65536
+int sgd_suffix_array_noalloc(const int32_t *text, int64_t n, int32_t *sa, void *stream);
 
 /* Reads (and with clear = 1 resets) the sticky device error word; this
  * synchronises the device and is not meant for the drafting path. */

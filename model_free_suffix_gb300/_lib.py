@@ -19,6 +19,8 @@ SGD_ETIMEDOUT = -4
 SGD_EBUSY = -5
 SGD_EBUILD = -6
 SGD_ENOCORPUS = -7
+SGD_ETOOLARGE = -8
+NOALLOC_MAX_TOKENS = 65536
 
 ERR_SAMPLED_TOKEN = 0x1
 ERR_NUM_TOKENS = 0x2
@@ -103,6 +105,7 @@ def load() -> ctypes.CDLL:
         "sgd_build_sa": (ctypes.c_int, [P, P, P]),
         "sgd_poll": (ctypes.c_int, [P, ctypes.c_int, i64, P, u64p]),
         "sgd_suffix_array": (ctypes.c_int, [P, P, i64, P, P]),
+        "sgd_suffix_array_noalloc": (ctypes.c_int, [P, i64, P, P]),
         "sgd_get_error": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
         "sgd_export_snapshot": (ctypes.c_int, [P, P, P, i64, ctypes.POINTER(ctypes.c_int64), u64p]),
         "sgd_corpus_stats": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_int64),

@@ -208,6 +208,7 @@ const char *sgd_strerror(int s) {
     case SGD_EBUSY: return "a suffix-array build is in flight";
     case SGD_EBUILD: return "suffix-array build failed";
     case SGD_ENOCORPUS: return "context has no corpus";
+    case SGD_ETOOLARGE: return "text longer than the fixed no-allocation scratch";
     default: return "unknown status";
   }
 }

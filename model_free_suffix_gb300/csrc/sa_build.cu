@@ -401,6 +401,36 @@ cudaError_t sa_scratch_alloc(SaScratch *s, int64_t cap) {
   return e;
 }
 
+size_t sa_scratch_carve(SaScratch *s, unsigned char *base, size_t bytes, int64_t cap) {
+  *s = SaScratch{};
+  const long long c = cap > 0 ? cap : 1;
+  const long long os_tiles = (c + OS_TILE - 1) / OS_TILE;
+  const long long sc_tiles = (c + SC_TILE - 1) / SC_TILE;
+  size_t off = 0;
+  auto take = [&](size_t n) {
+    unsigned char *p = base + off;
+    off += (n + 255) & ~(size_t)255;
+    return p;
+  };
+  s->cap = cap;
+  s->status_words = os_tiles * RADIX;
+  s->keyA = (uint64_t *)take(c * 8);
+  s->keyB = (uint64_t *)take(c * 8);
+  s->valA = (int32_t *)take(c * 4);
+  s->valB = (int32_t *)take(c * 4);
+  s->rank = (int32_t *)take(c * 4);
+  s->act = (int32_t *)take(c * 4);
+  s->act2 = (int32_t *)take(c * 4);
+  s->tmp = (int32_t *)take(c * 4);
+  s->head = (int32_t *)take(c * 4);
+  s->tile_sums = (int32_t *)take((sc_tiles + 1) * 4);
+  s->hist = (uint32_t *)take(8 * RADIX * 4);
+  s->status = (uint32_t *)take(s->status_words * 4);
+  s->counter = (uint32_t *)take(64);
+  if (off > bytes) *s = SaScratch{};
+  return off;
+}
+
 void sa_scratch_free(SaScratch *s) {
   cudaFree(s->keyA); cudaFree(s->keyB); cudaFree(s->valA); cudaFree(s->valB);
   cudaFree(s->rank); cudaFree(s->act); cudaFree(s->act2); cudaFree(s->tmp); cudaFree(s->head);

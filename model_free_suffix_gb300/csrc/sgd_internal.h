@@ -112,6 +112,11 @@ struct SaStats {
 size_t sa_scratch_bytes(int64_t cap);
 cudaError_t sa_scratch_alloc(SaScratch *s, int64_t cap);
 void sa_scratch_free(SaScratch *s);
+// Lays the device buffers of a scratch for `cap` elements out in
+// [base, base + bytes) (256-byte aligned pieces, no allocation); returns the
+// bytes needed, and leaves *s empty if they exceed `bytes`.  Host words
+// (h_pinned, h_hist) are left to the caller.
+size_t sa_scratch_carve(SaScratch *s, unsigned char *base, size_t bytes, int64_t cap);
 // Builds the suffix array of text[0..n) into sa; host-driven rounds on `st`
 // (blocks the calling thread).  Returns 0 on success, else SGD_ERR_* bits
 // (through *dev_flags as well) or -1 on a CUDA error.
