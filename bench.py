@@ -39,6 +39,20 @@ WORKLOAD = ("c3 serving loop: B=256 rows, S=4096 int32, vocab 151936 (Zipf 1.1 f
             "finish and are ingested, a side-stream rebuild starts once 2^16 tokens arrived")
 
 
+def kernel_traffic(kernel):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the kernel's current source (else None)."""
+    import hashlib
+    try:
+        rec = json.load(open(os.path.join(ROOT, "profiles", "traffic.json")))[kernel]
+        src = open(os.path.join(ROOT, rec["source"]), "rb").read()
+        if hashlib.sha256(src).hexdigest() != rec["sha256"]:
+            return None
+        return int(rec["bytes_per_launch"])
+    except Exception:
+        return None
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -268,7 +282,8 @@ def run_ours(args, rank, world):
     prop_avg_s = float(np.mean(prop_ms)) / 1e3
     ach = byts / prop_avg_s / 1e9
     rl_prop = {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 2),
-               "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4), "traffic": None,
+               "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+               "traffic": kernel_traffic("propose_kernel"),
                "bytes_per_launch": int(byts), "avg_launch_us": round(prop_avg_s * 1e6, 2),
                "peak_kind": peak_kind}
     # GPU time of the background builds that finished inside the region
@@ -281,7 +296,7 @@ def run_ours(args, rank, world):
     if pass_ms > float(np.sum(prop_ms)) and n_passes:
         ach_p = 24.0 * pass_elems / (pass_ms / 1e3) / 1e9
         rl = {"bound": "hbm", "kernel": "k_onesweep", "achieved": round(ach_p, 2), "peak": peak,
-              "unit": "GB/s", "frac": round(ach_p / peak, 4), "traffic": None,
+              "unit": "GB/s", "frac": round(ach_p / peak, 4), "traffic": kernel_traffic("k_onesweep"),
               "bytes_per_launch": int(24 * pass_elems / n_passes),
               "avg_launch_us": round(1e3 * pass_ms / n_passes, 2), "peak_kind": peak_kind}
     value = world * K / (total_ms_max / 1e3)
@@ -371,14 +386,15 @@ def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state,
             "d2h_bytes_per_step": int(bo), "us_per_step": round(1e6 * tot / K, 2), "steps": K}
 
 
-def sa_build_leg(args, dev):
+def sa_build_leg(args, dev, sizes=None):
     """Standalone suffix-array builds of the suffix-array workload (1M and 16M)."""
     import torch
     from model_free_suffix_gb300 import SuffixDrafter
     from model_free_suffix_gb300 import workload as W
     peak, peak_kind = peaks()
     out = {}
-    sizes = [1 << 20] + ([] if args.no_sa16m else [1 << 24])
+    if sizes is None:
+        sizes = [1 << 20] + ([] if args.no_sa16m else [1 << 24])
     for N in sizes:
         X = torch.from_numpy(W.sa_corpus(N, seed=0)).to(dev)
         dr = SuffixDrafter(max_batch=1, seq_capacity=8, vocab_size=151936, corpus_capacity=N,
@@ -398,7 +414,7 @@ def sa_build_leg(args, dev):
             "sorted_elems": best["sorted_elems"],
             "model_gbs": round(r_all, 1), "model_frac": round(r_all / peak, 4),
             "radix_pass": {"bound": "hbm", "achieved": None if r_pass is None else round(r_pass, 1),
-                           "peak": peak, "unit": "GB/s",
+                           "peak": peak, "unit": "GB/s", "traffic": kernel_traffic("k_onesweep"),
                            "frac": None if r_pass is None else round(r_pass / peak, 4),
                            "avg_launch_us": round(1e3 * best["pass_ms"] / max(1, best["passes"]), 2),
                            "peak_kind": peak_kind},
@@ -478,6 +494,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-sa16m", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--sa-only", type=int, default=0,
+                    help="only time suffix-array builds of this many tokens and print them")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -507,6 +525,13 @@ def main():
         return
     from __graft_entry__ import build
     build()
+    if args.sa_only:
+        import torch
+        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+        torch.cuda.set_device(dev)
+        if rank == 0:
+            print(json.dumps(sa_build_leg(args, dev, sizes=[args.sa_only])), flush=True)
+        return
     res = run_ours(args, rank, world)
     if rank == 0:
         if not args.no_cpu_baseline:
