@@ -323,6 +323,68 @@ def run_ours(args, rank, world):
     return res
 
 
+def long_context_leg(args, rank):
+    """Propose steps of the long-context workload (B=1024, S=32768, 4M-token
+    corpus, k=32, D=32): the per-row scans dominate, so this is where the
+    propose kernel meets the HBM roofline.  Each step: L2 flush (untimed),
+    propose_with_update timed with CUDA events."""
+    import torch
+    from model_free_suffix_gb300 import SuffixDrafter
+    from model_free_suffix_gb300 import workload as W
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    cfg = W.CONFIGS["c5"]
+    K, Wm = args.long_context_steps, 3
+    tr = W.ServingTrace(cfg, seed=rank, steps=K + Wm, finish_frac=0.0)
+    tok, n = tr.initial()
+    steps = [tr.next_step() for _ in range(K + Wm)]
+    dr = SuffixDrafter(max_batch=cfg.B, seq_capacity=cfg.S, vocab_size=cfg.V, k=cfg.k,
+                       max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
+                       corpus_capacity=cfg.corpus_tokens, device=dev.index)
+    docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
+    chunk = 512
+    for s0 in range(0, docs.shape[0], chunk):
+        d = docs[s0:s0 + chunk]
+        m = d.shape[0]
+        buf = torch.full((m, cfg.S), -1, dtype=torch.int32, device=dev)
+        buf[:, :d.shape[1]] = torch.from_numpy(d).to(dev)
+        dr.ingest(buf, torch.arange(m, dtype=torch.int32, device=dev),
+                  torch.zeros(m, dtype=torch.int32, device=dev),
+                  torch.from_numpy(np.ascontiguousarray(lens[s0:s0 + chunk])).to(dev))
+        del buf
+    side = torch.cuda.Stream(device=dev)
+    dr.build_sa(side)
+    assert dr.poll(wait=True)[0] == 1
+    g_tok = torch.from_numpy(tok).to(dev)
+    g_n = torch.from_numpy(n).to(dev)
+    out = dr.new_outputs(cfg.B)
+    samp = [torch.from_numpy(s.sampled).to(dev) for s in steps]
+    flush = torch.empty(256 << 20 >> 2, dtype=torch.int32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    ms, sum_n = [], []
+    for i in range(K + Wm):
+        flush.fill_(i)
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        dr.propose_with_update(g_tok, g_n, samp[i], out=out)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        if i >= Wm:
+            ms.append(e0.elapsed_time(e1))
+            sum_n.append(int(g_n.sum().item()))
+    dr.close()
+    peak, peak_kind = peaks()
+    byts = algorithmic_bytes_propose(int(np.mean(sum_n)), cfg.B, cfg.T, cfg.k, cfg.corpus_tokens)
+    avg = float(np.mean(ms)) / 1e3
+    ach = byts / avg / 1e9
+    return {"workload": "c5: B=1024, S=32768, num_tokens U[8192,32768], Zipf(1.1) over 151936, "
+                        "p=0.8 repeats of 1024 spans 32-512, k=32, D=32, R=64, T=33, 4M-token corpus",
+            "steps": K, "propose_us": round(avg * 1e6, 2), "steps_per_s": round(1.0 / avg, 2),
+            "roofline": {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 1),
+                         "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                         "bytes_per_launch": int(byts), "peak_kind": peak_kind},
+            "l2": "flushed before every timed step"}
+
+
 def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state, dev, stream):
     """Same steps through the public API with pinned host buffers: each step
     copies its sampled ids (and ingest arguments) host->device and reads the
@@ -494,6 +556,8 @@ def main():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--no-sa16m", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--long-context-steps", type=int, default=16,
+                    help="steps of the long-context workload timed as a secondary line (0: skip)")
     ap.add_argument("--sa-only", type=int, default=0,
                     help="only time suffix-array builds of this many tokens and print them")
     args = ap.parse_args()
@@ -533,6 +597,8 @@ def main():
             print(json.dumps(sa_build_leg(args, dev, sizes=[args.sa_only])), flush=True)
         return
     res = run_ours(args, rank, world)
+    if args.long_context_steps > 0 and args.config == "c3":
+        res["long_context"] = long_context_leg(args, rank)
     if rank == 0:
         if not args.no_cpu_baseline:
             res["cpu_baseline"] = cpu_oracle_leg(cfg, args.cpu_seconds)

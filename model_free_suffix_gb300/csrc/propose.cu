@@ -36,6 +36,7 @@ constexpr int LCAP = 16384;    // P4 hits whose match length is cached on chip
 constexpr int NPROBE3 = 3;     // probe warps: P4, P3, P2
 constexpr int TOP_KEYS = 32;   // staged keys of the top level of the descent
 constexpr int MID_KEYS = 1024; // staged keys of the level below it
+constexpr long long BIG_INTERVAL = 4096;  // probe hits worth waiting for the self match
 
 __device__ __forceinline__ int4 load_win(const int32_t *row, int widx, int lane, int S) {
   const int p = widx * WIN + 4 * lane;
@@ -373,6 +374,19 @@ __device__ void pick_bin(const int *hist, int need, int lane, int *s_sel, int *s
   }
 }
 
+// barrier of the three probe warps only
+__device__ __forceinline__ void probe_sync() { asm volatile("bar.sync 1, 96;" ::: "memory"); }
+
+// draft length bound: min(k, floor(factor * M) + offset, S - n - 1) [, D - M]
+__device__ __forceinline__ int draft_cap(const ProposeArgs &a, int M, int n) {
+  long long c = min((long long)a.k, a.fN * M / a.fD + a.offset);
+  long long room = (long long)a.S - n - 1;
+  if (room < 0) room = 0;
+  c = min(c, room);
+  if (a.depth_sum_cap) c = min(c, (long long)a.D - M);
+  return c < 0 ? 0 : (int)c;
+}
+
 __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
@@ -430,7 +444,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   __shared__ int s_lhist[MAX_D + 1];
   __shared__ int s_vv[MAX_R];
   __shared__ long long s_bound[2 * NPROBE3];
-  __shared__ int s_n, s_Ms, s_cs, s_c0, s_q, s_sel, s_need, s_have_corpus;
+  __shared__ int s_n, s_Ms, s_cs, s_q, s_sel, s_need, s_have_corpus;
+  __shared__ int s_self_done, s_ms_ready, s_pms, s_Mc, s_c0c, s_cpf;
 
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
@@ -441,8 +456,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   int *s_wlist = s_tail + MAX_D;       // nself * R
   int *s_occ = s_wlist + a.nself * R;  // R
   int *s_run = s_occ + R;              // R
-  int *s_big = s_run + R;              // max(cand_cap, R * k)
-  const int koff = (MAX_D + a.nself * R + 2 * R + big + 3) & ~3;
+  int *s_occc = s_run + R;             // R (corpus ends)
+  int *s_big = s_occc + R;             // max(cand_cap, R * k)
+  const int koff = (MAX_D + a.nself * R + 3 * R + big + 3) & ~3;
   int4 *s_top = reinterpret_cast<int4 *>(dsm + koff);                  // TOP_KEYS
   int4 *s_mid = s_top + TOP_KEYS;                                      // MID_KEYS
   unsigned char *s_L = reinterpret_cast<unsigned char *>(s_mid + MID_KEYS);  // LCAP
@@ -468,6 +484,13 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
       if (fl) atomicOr(a.err, fl);
       s_n = n;
       s_have_corpus = a.desc != nullptr && cp.N >= 2;
+      s_self_done = 0;
+      s_ms_ready = 0;
+      s_Ms = 0;
+      s_cs = 0;
+      s_Mc = 0;
+      s_c0c = 0;
+      s_cpf = 0;
     }
   } else if (a.desc != nullptr && cp.N >= 2) {
     const int sh = 5 * cp.Lmax;
@@ -505,209 +528,244 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   asm volatile("cp.async.wait_all;" ::: "memory");  // staged keys landed (no-op if none)
   __syncthreads();
 
-  // ---- phase 2: self match (nself warps) || interval probes (3 warps) ----
+  // ---- phase 2: self match (nself warps) || corpus chain (3 probe warps) ----
+  // The corpus side does not need the row's own match: while the self warps
+  // scan, the probe warps find the intervals, evaluate the winning corpus
+  // level and collect its R most recent ends, requesting their continuation
+  // tokens.  The last self warp to finish merges the self result and
+  // publishes it through a shared flag; the probe warps read it at their
+  // decision points to skip levels that cannot win, which only saves work.
   if (warp < a.nself) {
     int Mw, cnt;
     self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, lane, sc, Mw, cnt);
     if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; }
+    __threadfence_block();
+    __syncwarp();
+    int last = 0;
+    if (lane == 0) last = atomicAdd(&s_self_done, 1) == a.nself - 1;
+    last = __shfl_sync(FULL, last, 0);
+    if (last) {
+      __threadfence_block();
+      int Ms = 0;
+      for (int w = 0; w < a.nself; ++w) Ms = max(Ms, s_wM[w]);
+      int c = 0;
+      if (Ms > 0) {
+        for (int w = a.nself - 1; w >= 0 && c < R; --w) {
+          if (s_wM[w] != Ms) continue;
+          const int mm = min(s_wcnt[w], R - c);
+          for (int i = lane; i < mm; i += 32) s_occ[c + i] = s_wlist[w * R + i];
+          c += mm;
+        }
+      }
+      if (lane == 0) {
+        s_Ms = Ms;
+        s_cs = c;
+        __threadfence_block();
+        *(volatile int *)&s_ms_ready = 1;
+      }
+    }
   } else if (corpus_ok) {
     const int pw = warp - a.nself;  // 0: last 4 tokens, 1: last 3, 2: last 2
-    const int m = 4 - pw;
+    const int ptid = tid - 32 * a.nself, pthr = 32 * NPROBE3;
+    {
+      const int m = 4 - pw;
+      long long plo = 0, phi = 0;
+      if (D >= m && n >= m) {
+        const int4 P = make_int4(s_tail[m - 1], m >= 2 ? s_tail[m - 2] : 0,
+                                 m >= 3 ? s_tail[m - 3] : 0, m >= 4 ? s_tail[m - 4] : 0);
+        // a pattern holding KEY_END cannot occur: corpus tokens are in [0, V]
+        const bool endless = P.x != KEY_END && (m < 2 || P.y != KEY_END) &&
+                             (m < 3 || P.z != KEY_END) && (m < 4 || P.w != KEY_END);
+        if (endless) probe_bounds(cp, P, m, lane, plo, phi);
+      }
+      if (lane == 0) { s_bound[2 * pw] = plo; s_bound[2 * pw + 1] = phi; }
+    }
+    probe_sync();
+    // The row's own match length, -1 while the self warps still scan.  Before
+    // a large piece of work the probe warps wait for it (bounded; on time-out
+    // they go on without pruning, which only costs time).
+    auto self_len = [&](bool wait) {
+      if (ptid == 0) {
+        unsigned spins = 0;
+        while (wait && *(volatile int *)&s_ms_ready == 0 && ++spins < (1u << 22)) __nanosleep(64);
+        const int ready = *(volatile int *)&s_ms_ready;
+        __threadfence_block();
+        s_pms = ready ? *(volatile int *)&s_Ms : -1;
+      }
+      probe_sync();
+      return s_pms;
+    };
+    int pms = self_len(false);
+    int Mc = 0, lvl = 0, Q = 0;
     long long lo = 0, hi = 0;
-    if (D >= m && n >= m) {
-      const int4 P = make_int4(s_tail[m - 1], m >= 2 ? s_tail[m - 2] : 0, m >= 3 ? s_tail[m - 3] : 0,
-                               m >= 4 ? s_tail[m - 4] : 0);
-      // a pattern holding KEY_END cannot occur: corpus tokens are in [0, V]
-      const bool endless = P.x != KEY_END && (m < 2 || P.y != KEY_END) &&
-                           (m < 3 || P.z != KEY_END) && (m < 4 || P.w != KEY_END);
-      if (endless) probe_bounds(cp, P, m, lane, lo, hi);
-    }
-    if (lane == 0) { s_bound[2 * pw] = lo; s_bound[2 * pw + 1] = hi; }
-  }
-  __syncthreads();
-
-  // ---- merge the self scans: max length, most recent ends first ----
-  if (warp == 0) {
-    int Ms = 0;
-    for (int w = 0; w < a.nself; ++w) Ms = max(Ms, s_wM[w]);
-    int c = 0;
-    if (Ms > 0) {
-      for (int w = a.nself - 1; w >= 0 && c < R; --w) {
-        if (s_wM[w] != Ms) continue;
-        const int mm = min(s_wcnt[w], R - c);
-        for (int i = lane; i < mm; i += 32) s_occ[c + i] = s_wlist[w * R + i];
-        c += mm;
+    if (pms < dl) {
+      bool decided = false;
+      if (D >= 4 && n >= 4 && s_bound[1] > s_bound[0]) {
+        if (pms < 0 && s_bound[1] - s_bound[0] > BIG_INTERVAL) pms = self_len(true);
       }
-    }
-    if (lane == 0) { s_Ms = Ms; s_cs = c; }
-  }
-  __syncthreads();
-  const int Ms = s_Ms;
-
-  // ---- corpus level: the longest match among the hits, where it can win ----
-  int Mc = 0, lvl = 0, Q = 0;
-  long long lo = 0, hi = 0;
-  if (corpus_ok && Ms < dl) {
-    bool decided = false;
-    if (D >= 4 && n >= 4 && s_bound[1] > s_bound[0]) {
-      for (int i = tid; i <= MAX_D; i += nthr) s_lhist[i] = 0;
-      __syncthreads();
-      scan_p4(cp, Z, s_bound[0], s_bound[1], s_tail, n, D, s_L, s_lhist, tid, nthr);
-      __syncthreads();
-      int lbest = 0;
-      for (int L = 4 + lane; L <= dl; L += 32)
-        if (s_lhist[L] > 0) lbest = L;
-      lbest = (int)__reduce_max_sync(FULL, (unsigned)lbest);
-      if (lbest > 0) {
-        Mc = lbest;
-        lvl = 4;
-        lo = s_bound[0];
-        hi = s_bound[1];
-        Q = s_lhist[lbest];
-        decided = true;
-      }
-    }
-    for (int lv = 3; lv >= 2 && !decided; --lv) {
-      if (D < lv || n < lv) continue;
-      if (Ms >= lv) break;  // neither this level nor the next can win
-      const long long l0 = s_bound[2 * (4 - lv)], h0 = s_bound[2 * (4 - lv) + 1];
-      if (h0 <= l0) continue;
-      __syncthreads();  // s_q from an earlier level has been read
-      if (tid == 0) s_q = 0;
-      __syncthreads();
-      int cnt = 0;
-      for (long long p = l0 + tid; p < h0; p += 4LL * nthr) {
-        int4 kk[4];
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const long long q = p + (long long)u * nthr;
-          kk[u] = q < h0 ? __ldg(cp.K + q) : make_int4(Z, Z, Z, Z);
+      if (D >= 4 && n >= 4 && s_bound[1] > s_bound[0] && pms < dl) {
+        for (int i = ptid; i <= MAX_D; i += pthr) s_lhist[i] = 0;
+        probe_sync();
+        scan_p4(cp, Z, s_bound[0], s_bound[1], s_tail, n, D, s_L, s_lhist, ptid, pthr);
+        probe_sync();
+        int lbest = 0;
+        for (int L = 4 + lane; L <= dl; L += 32)
+          if (s_lhist[L] > 0) lbest = L;
+        lbest = (int)__reduce_max_sync(FULL, (unsigned)lbest);
+        if (lbest > 0) {
+          Mc = lbest;
+          lvl = 4;
+          lo = s_bound[0];
+          hi = s_bound[1];
+          Q = s_lhist[lbest];
+          decided = true;
         }
-#pragma unroll
-        for (int u = 0; u < 4; ++u) cnt += short_valid(kk[u], lv, Z);
       }
-      cnt = (int)__reduce_add_sync(FULL, (unsigned)cnt);
-      if (lane == 0 && cnt) atomicAdd(&s_q, cnt);
-      __syncthreads();
-      if (s_q > 0) {
-        Mc = lv;
-        lvl = lv;
-        lo = l0;
-        hi = h0;
-        Q = s_q;
-        decided = true;
+      for (int lv = 3; lv >= 2 && !decided; --lv) {
+        if (D < lv || n < lv) continue;
+        if (pms >= lv) break;  // neither this level nor the next can win
+        const long long l0 = s_bound[2 * (4 - lv)], h0 = s_bound[2 * (4 - lv) + 1];
+        if (h0 <= l0) continue;
+        if (pms < 0 && h0 - l0 > BIG_INTERVAL) {
+          pms = self_len(true);
+          if (pms >= lv) break;
+        }
+        probe_sync();  // s_q from an earlier level has been read
+        if (ptid == 0) s_q = 0;
+        probe_sync();
+        int cnt = 0;
+        for (long long p = l0 + ptid; p < h0; p += 4LL * pthr) {
+          int4 kk[4];
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const long long q = p + (long long)u * pthr;
+            kk[u] = q < h0 ? __ldg(cp.K + q) : make_int4(Z, Z, Z, Z);
+          }
+#pragma unroll
+          for (int u = 0; u < 4; ++u) cnt += short_valid(kk[u], lv, Z);
+        }
+        cnt = (int)__reduce_add_sync(FULL, (unsigned)cnt);
+        if (lane == 0 && cnt) atomicAdd(&s_q, cnt);
+        probe_sync();
+        if (s_q > 0) {
+          Mc = lv;
+          lvl = lv;
+          lo = l0;
+          hi = h0;
+          Q = s_q;
+          decided = true;
+        }
       }
     }
+    if (Mc > 0 && pms < 0 && Q > R) pms = self_len(true);
+    if (Mc > 0 && Mc > pms) {
+      // The R largest ends among the Q of length Mc.  O_0 is a set (the vote
+      // does not depend on its order), so nothing is sorted.  With at most R
+      // of them, all are kept and their continuations requested right away.
+      const int capc = draft_cap(a, Mc, n);
+      const bool pf = Q <= R;
+      int *cand = s_big;
+      probe_sync();
+      if (ptid == 0) s_q = 0;
+      unsigned prefix = 0;
+      if (Q > a.cand_cap) {
+        // more than fit on chip: radix-select the R-th largest end over the
+        // interval, byte by byte; the R ends at or above it are collected below
+        unsigned mask = 0;
+        int need = R;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+          for (int i = ptid; i < 256; i += pthr) s_hist[i] = 0;
+          probe_sync();
+          for (long long p0 = lo + ptid; p0 < hi; p0 += 4LL * pthr) {
+            long long e[4];
+            bool q[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const long long p = p0 + (long long)u * pthr;
+              q[u] = p < hi && selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              if (q[u] && ((unsigned)e[u] & mask) == prefix)
+                atomicAdd(&s_hist[((unsigned)e[u] >> shift) & 255u], 1);
+          }
+          probe_sync();
+          if (pw == 0) pick_bin(s_hist, need, lane, &s_sel, &s_need);
+          probe_sync();
+          prefix |= (unsigned)s_sel << shift;
+          mask |= 255u << shift;
+          need = s_need;
+        }
+      }
+      probe_sync();
+      for (long long p = lo + ptid; p < hi; p += pthr) {
+        long long e;
+        if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e) && (unsigned)e >= prefix) {
+          const int slot = atomicAdd(&s_q, 1);
+          if (pf) {
+            s_occc[slot] = (int)e;
+            for (int d = 0; d < capc; ++d) {
+              const long long pos = e + 1 + d;
+              if (pos < cp.N) cp_async4(&s_big[slot * capc + d], cp.X + pos);
+              else s_big[slot * capc + d] = Z;
+            }
+          } else if (slot < a.cand_cap) {
+            cand[slot] = (int)e;
+          }
+        }
+      }
+      asm volatile("cp.async.commit_group;" ::: "memory");
+      probe_sync();
+      const int Qc = min(s_q, a.cand_cap);
+      int c0c;
+      if (Qc > R) {
+        // radix-select the R largest among the on-chip candidates
+        unsigned pf2 = 0, mk = 0;
+        int need = R;
+        for (int shift = 24; shift >= 0; shift -= 8) {
+          for (int i = ptid; i < 256; i += pthr) s_hist[i] = 0;
+          probe_sync();
+          for (int i = ptid; i < Qc; i += pthr)
+            if (((unsigned)cand[i] & mk) == pf2) atomicAdd(&s_hist[((unsigned)cand[i] >> shift) & 255u], 1);
+          probe_sync();
+          if (pw == 0) pick_bin(s_hist, need, lane, &s_sel, &s_need);
+          probe_sync();
+          pf2 |= (unsigned)s_sel << shift;
+          mk |= 255u << shift;
+          need = s_need;
+        }
+        if (ptid == 0) s_q = 0;
+        probe_sync();
+        for (int i = ptid; i < Qc; i += pthr)
+          if ((unsigned)cand[i] >= pf2) s_occc[atomicAdd(&s_q, 1)] = cand[i];
+        c0c = R;
+      } else {
+        if (!pf)
+          for (int i = ptid; i < Qc; i += pthr) s_occc[i] = cand[i];
+        c0c = Qc;
+      }
+      asm volatile("cp.async.wait_all;" ::: "memory");
+      if (ptid == 0) { s_Mc = Mc; s_c0c = c0c; s_cpf = pf; }
+    } else if (ptid == 0) {
+      s_Mc = 0;
+    }
   }
+  __syncthreads();
+
+  // ---- the longer match wins (equal lengths: the row itself) ----
+  const int Ms = s_Ms, Mc = corpus_ok ? s_Mc : 0;
   int src, M;
   if (Mc > Ms) { src = 2; M = Mc; }
   else { src = Ms > 0 ? 1 : 0; M = Ms; }
-
-  // draft length bound: min(k, floor(factor * M) + offset, S - n - 1) [, D - M]
-  long long capl = 0;
-  if (M > 0) {
-    capl = min((long long)k, a.fN * M / a.fD + a.offset);
-    long long room = (long long)S - n - 1;
-    if (room < 0) room = 0;
-    capl = min(capl, room);
-    if (a.depth_sum_cap) capl = min(capl, (long long)D - M);
-    if (capl < 0) capl = 0;
-  }
-  const int cap = (int)capl;
+  const int cap = M > 0 ? draft_cap(a, M, n) : 0;
+  const int c0 = src == 2 ? s_c0c : s_cs;
+  const int *occ = src == 2 ? s_occc : s_occ;
   int *cont = s_big;
-  // with at most R candidates every one is kept: their continuations are
-  // requested while they are collected
-  const bool prefetch = src == 2 && Q <= R;
-
-  if (src == 2) {
-    // The R largest ends among the Q of length Mc.  O_0 is a set (the vote
-    // does not depend on its order), so nothing is sorted.
-    int *cand = s_big;
-    __syncthreads();
-    if (tid == 0) s_q = 0;
-    unsigned prefix = 0;
-    if (Q > a.cand_cap) {
-      // more than fit on chip: radix-select the R-th largest end over the
-      // interval, byte by byte; the R ends at or above it are collected below
-      unsigned mask = 0;
-      int need = R;
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += nthr) s_hist[i] = 0;
-        __syncthreads();
-        for (long long p = lo + tid; p < hi; p += nthr) {
-          long long e;
-          if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e) && ((unsigned)e & mask) == prefix)
-            atomicAdd(&s_hist[((unsigned)e >> shift) & 255u], 1);
-        }
-        __syncthreads();
-        if (warp == 0) pick_bin(s_hist, need, lane, &s_sel, &s_need);
-        __syncthreads();
-        prefix |= (unsigned)s_sel << shift;
-        mask |= 255u << shift;
-        need = s_need;
-      }
-    }
-    __syncthreads();
-    for (long long p = lo + tid; p < hi; p += nthr) {
-      long long e;
-      if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e) && (unsigned)e >= prefix) {
-        const int slot = atomicAdd(&s_q, 1);
-        if (prefetch) {
-          s_occ[slot] = (int)e;
-          for (int d = 0; d < cap; ++d) {
-            const long long pos = e + 1 + d;
-            if (pos < cp.N) cp_async4(&cont[slot * cap + d], cp.X + pos);
-            else cont[slot * cap + d] = Z;
-          }
-        } else if (slot < a.cand_cap) {
-          cand[slot] = (int)e;
-        }
-      }
-    }
-    asm volatile("cp.async.commit_group;" ::: "memory");
-    __syncthreads();
-    const int Qc = min(s_q, a.cand_cap);
-    int c0;
-    if (Qc > R) {
-      // radix-select the R largest among the on-chip candidates
-      unsigned pf = 0, mk = 0;
-      int need = R;
-      for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += nthr) s_hist[i] = 0;
-        __syncthreads();
-        for (int i = tid; i < Qc; i += nthr)
-          if (((unsigned)cand[i] & mk) == pf) atomicAdd(&s_hist[((unsigned)cand[i] >> shift) & 255u], 1);
-        __syncthreads();
-        if (warp == 0) pick_bin(s_hist, need, lane, &s_sel, &s_need);
-        __syncthreads();
-        pf |= (unsigned)s_sel << shift;
-        mk |= 255u << shift;
-        need = s_need;
-      }
-      if (tid == 0) s_q = 0;
-      __syncthreads();
-      for (int i = tid; i < Qc; i += nthr)
-        if ((unsigned)cand[i] >= pf) s_occ[atomicAdd(&s_q, 1)] = cand[i];
-      c0 = R;
-    } else {
-      if (!prefetch)
-        for (int i = tid; i < Qc; i += nthr) s_occ[i] = cand[i];
-      c0 = Qc;
-    }
-    if (tid == 0) s_c0 = c0;
-  } else if (tid == 0) {
-    s_c0 = s_cs;
-  }
-  __syncthreads();
-
-  // ---- length cap and the continuation matrix ----
-  const int c0 = s_c0;
-  if (prefetch) asm volatile("cp.async.wait_all;" ::: "memory");
   if (cap > 0 && c0 > 0) {
-    const int tot = prefetch ? 0 : c0 * cap;
+    const int tot = (src == 2 && s_cpf) ? 0 : c0 * cap;  // prefetched by the probe warps
     for (int idx = tid; idx < tot; idx += nthr) {
       const int o = idx / cap, d = idx - o * cap;
-      const long long pos = (long long)s_occ[o] + 1 + d;
+      const long long pos = (long long)occ[o] + 1 + d;
       int v;
       if (src == 1) v = pos <= n - 1 ? row[pos] : 0;
       else v = pos < cp.N ? __ldg(cp.X + pos) : Z;
@@ -717,7 +775,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
     for (int o = tid; o < c0; o += nthr) {
       int r;
       if (src == 1) {
-        r = min(cap, n - 1 - s_occ[o]);
+        r = min(cap, n - 1 - occ[o]);
       } else {
         r = 0;
         while (r < cap && cont[o * cap + r] != Z) ++r;
@@ -898,7 +956,7 @@ __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a
 
 size_t propose_smem_bytes(int nself, int R, int k, int cand_cap) {
   const size_t big = (size_t)max(cand_cap, R * k);
-  const size_t ints = ((size_t)MAX_D + (size_t)nself * R + 2 * (size_t)R + big + 3) & ~(size_t)3;
+  const size_t ints = ((size_t)MAX_D + (size_t)nself * R + 3 * (size_t)R + big + 3) & ~(size_t)3;
   return sizeof(int) * ints + sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP;
 }
 
