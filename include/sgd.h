@@ -209,7 +209,7 @@ int sgd_suffix_array(sgd_ctx *ctx, const int32_t *text, int64_t n, int32_t *sa, 
  *   text DEVICE int32 [n] (any values), sa DEVICE int32 [n] output, both
  *   caller-owned; same order as sgd_suffix_array; no context is needed.
  * The working memory is one fixed device array of the library, sized for
- * SGD_NOALLOC_MAX_TOKENS tokens (about 3 MB, held on every GPU that loads the
+ * SGD_NOALLOC_MAX_TOKENS tokens (about 2.5 MB, held on every GPU that loads the
  * library until the process exits); longer texts return SGD_ETOOLARGE.  The
  * first call on a device (with that device current) looks the array up on
  * that device; make that first call before any stream capture.  All calls

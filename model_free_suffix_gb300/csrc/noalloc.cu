@@ -23,9 +23,9 @@ namespace {
 constexpr long long kMax = SGD_NOALLOC_MAX_TOKENS;
 constexpr long long kTiles = (kMax + 2047) / 2048 + 1;
 // bytes of the pieces laid out by sa_scratch_carve for kMax elements, each
-// rounded up to 256, plus the error word; checked against the carve at setup
-constexpr size_t kBytes = 2 * kMax * 8 + 7 * kMax * 4 + kTiles * 4 + 8 * 256 * 4 + kTiles * 256 * 4 +
-                          64 + 16 * 256;
+// rounded up to 256, plus the error word; checked against the carve per call
+constexpr size_t kBytes = 2 * kMax * 8 + 5 * kMax * 4 + kTiles * 256 * 8 + kTiles * 8 +
+                          8 * 256 * 4 + 1024 + 16 * 256;
 
 // The fixed working memory.  From host code its name is only a stand-in:
 // the device address is obtained with cudaGetSymbolAddress, per device.

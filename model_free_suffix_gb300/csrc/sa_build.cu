@@ -10,12 +10,20 @@
 // suffix the SA position of the first member of its group ("head rank"),
 // then for h = 1, 2, 4, ... re-sort only the suffixes whose group has more
 // than one member by the pair (rank[i], rank[i + h]) (rank -1 past the end),
-// until every group is a singleton.  Each sort is an LSD radix sort over
-// 8-bit digits with one onesweep pass per digit: one kernel per pass that
-// ranks each tile's items, publishes the tile's per-digit counts and looks
-// back over earlier tiles' published counts (decoupled look-back, with a
-// bounded wait) to place its items.  Digit places whose 256 buckets hold
-// everything in one bucket are skipped.
+// until every group is a singleton.
+//
+// Per round: one kernel builds the keys of the unresolved suffixes and all
+// digit histograms; the host reads the round's size and histograms back
+// (the one synchronisation of a round) and runs one onesweep LSD radix pass
+// per digit place that is not constant; one more kernel writes the sorted
+// suffixes back, finds the new groups (a max-scan of group heads) and lists
+// the suffixes still unresolved (a sum-scan), both in a single pass.
+//
+// The passes and the post-processing are single-pass chained scans: a tile
+// publishes its aggregate, then looks back over earlier tiles' published
+// values.  Tiles take tickets in launch order, so an earlier tile is already
+// running; every wait is bounded (after SPIN_LIMIT polls SGD_ERR_LOOKBACK is
+// set, the build reports failure and the previous snapshot stays current).
 #include <algorithm>
 #include <climits>
 #include <vector>
@@ -30,86 +38,97 @@ constexpr int OS_THREADS = 256;
 constexpr int OS_ITEMS = 8;
 constexpr int OS_TILE = OS_THREADS * OS_ITEMS;  // 2048 items per tile
 constexpr int RADIX = 256;
-constexpr uint32_t FLAG_AGG = 1u << 30;
-constexpr uint32_t FLAG_INC = 2u << 30;
-constexpr uint32_t VALUE_MASK = (1u << 30) - 1;
 constexpr unsigned SPIN_LIMIT = 1u << 18;  // ~0.1 s of polling; a normal wait is microseconds
+constexpr int MAX_PASSES = 250;            // ticket counters per build
 
-constexpr int SC_THREADS = 256;
-constexpr int SC_ITEMS = 8;
-constexpr int SC_TILE = SC_THREADS * SC_ITEMS;
+// counter layout (uint32 words): [0] active count written by the post pass,
+// [1] post ticket, [2..] radix-pass tickets
+constexpr int CNT_ACTIVE = 0, CNT_POST = 1, CNT_PASS = 2;
 
-__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t *p) {
-  uint32_t v;
-  asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long *p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_relaxed(uint32_t *p, uint32_t v) {
-  asm volatile("st.relaxed.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+__device__ __forceinline__ void st_relaxed64(unsigned long long *p, unsigned long long v) {
+  asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 
-// ---------------------------------------------------------------------------
-// round 0 keys: the token itself, order-preserving for signed int32
-__global__ void k_init0(const int32_t *text, long long n, uint64_t *key, int32_t *val) {
+// Histograms of the digit places [0, ndig) of the keys this CTA produced,
+// accumulated in shared memory and added to the global ones.
+__device__ __forceinline__ void hist_flush(uint32_t *s, int ndig, uint32_t *hist) {
+  __syncthreads();
+  for (int i = threadIdx.x; i < ndig * RADIX; i += blockDim.x)
+    if (s[i]) atomicAdd(&hist[i], s[i]);
+}
+
+// round 0: key = the token, order-preserving for signed int32; all digit
+// histograms in the same pass
+__global__ void __launch_bounds__(256) k_init_keys(const int32_t *text, long long n, uint64_t *key,
+                                                   int32_t *val, uint32_t *hist) {
+  __shared__ uint32_t s[4 * RADIX];
+  for (int i = threadIdx.x; i < 4 * RADIX; i += blockDim.x) s[i] = 0;
+  __syncthreads();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    key[i] = (uint64_t)((uint32_t)text[i] ^ 0x80000000u);
+    const uint32_t k = (uint32_t)text[i] ^ 0x80000000u;
+    key[i] = k;
     val[i] = (int32_t)i;
+#pragma unroll
+    for (int d = 0; d < 4; ++d) atomicAdd(&s[d * RADIX + ((k >> (8 * d)) & 255u)], 1u);
   }
+  hist_flush(s, 4, hist);
 }
 
-// doubling-round keys: (head rank of i, 1 + head rank of i + h, or 0 past the end)
-__global__ void k_keys(const int32_t *act, long long na, const int32_t *SA, const int32_t *rank,
-                       long long h, long long n, uint64_t *key, int32_t *val) {
+// doubling round: (head rank of i, 1 + head rank of i + h, or 0 past the end)
+// for the na unresolved suffixes (na read on the device), with histograms
+__global__ void __launch_bounds__(256) k_round_keys(const int32_t *act, const uint32_t *count,
+                                                    const int32_t *SA, const int32_t *rank, long long h,
+                                                    long long n, int ndig, uint64_t *key, int32_t *val,
+                                                    uint32_t *hist) {
+  __shared__ uint32_t s[8 * RADIX];
+  for (int i = threadIdx.x; i < ndig * RADIX; i += blockDim.x) s[i] = 0;
+  __syncthreads();
+  const long long na = count[CNT_ACTIVE];
   const long long stride = (long long)gridDim.x * blockDim.x;
   const uint64_t base = (uint64_t)n + 1;
   for (long long a = (long long)blockIdx.x * blockDim.x + threadIdx.x; a < na; a += stride) {
     const int32_t i = SA[act[a]];
     const uint64_t r1 = (uint64_t)rank[i];
     const uint64_t r2 = (long long)i + h < n ? (uint64_t)rank[i + h] + 1 : 0;
-    key[a] = r1 * base + r2;
+    const uint64_t k = r1 * base + r2;
+    key[a] = k;
     val[a] = i;
-  }
-}
-
-// all digit-place histograms in one read of the keys
-__global__ void __launch_bounds__(256) k_hist(const uint64_t *key, long long n, int ndig,
-                                              uint32_t *hist) {
-  __shared__ uint32_t s[8 * RADIX];
-  for (int i = threadIdx.x; i < ndig * RADIX; i += blockDim.x) s[i] = 0;
-  __syncthreads();
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    const uint64_t k = key[i];
     for (int d = 0; d < ndig; ++d) atomicAdd(&s[d * RADIX + ((k >> (8 * d)) & 255u)], 1u);
   }
-  __syncthreads();
-  for (int i = threadIdx.x; i < ndig * RADIX; i += blockDim.x)
-    if (s[i]) atomicAdd(&hist[i], s[i]);
+  hist_flush(s, ndig, hist);
 }
 
-// One LSD pass over the digit at `shift`.  Tiles take tickets in launch
-// order; tile t waits only for tiles < t, which hold earlier tickets and so
-// are already running, and every tile publishes its own counts before it
-// waits.  A wait longer than SPIN_LIMIT polls sets SGD_ERR_LOOKBACK (the
-// build is then reported failed) instead of hanging.
+// One LSD pass over the digit at `shift`.  A tile ranks its items stably
+// (items in (warp, item, lane) order are the input order), publishes its
+// per-digit counts, looks back for the counts of earlier tiles, then stages
+// its items in shared memory in digit order so that consecutive threads
+// write consecutive outputs.  Look-back words: epoch (bits 63..34, the
+// build's pass number), flag (33..32: 1 aggregate, 2 inclusive), count.
 __global__ void __launch_bounds__(OS_THREADS) k_onesweep(const uint64_t *kin, const int32_t *vin,
                                                          uint64_t *kout, int32_t *vout, long long n,
                                                          int shift, const uint32_t *hist_d,
-                                                         uint32_t *status, uint32_t *ticket,
-                                                         uint32_t *err) {
+                                                         unsigned long long *status, uint32_t *ticket,
+                                                         unsigned long long epoch, uint32_t *err) {
   constexpr int NW = OS_THREADS / 32;
   __shared__ uint32_t s_whist[NW][RADIX];
-  __shared__ uint32_t s_base[RADIX];
-  __shared__ uint32_t s_excl[RADIX];
+  __shared__ uint32_t s_base[RADIX];    // global start of each digit
+  __shared__ uint32_t s_tstart[RADIX];  // start of each digit inside this tile
+  __shared__ uint32_t s_excl[RADIX];    // items of each digit in earlier tiles
   __shared__ uint32_t s_wsum[NW];
+  __shared__ uint64_t s_k[OS_TILE];
+  __shared__ int32_t s_v[OS_TILE];
   __shared__ int s_tile;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (tid == 0) s_tile = (int)atomicAdd(ticket, 1u);
   for (int i = tid; i < NW * RADIX; i += OS_THREADS) (&s_whist[0][0])[i] = 0;
-  // global start of every digit: exclusive scan of this digit place's histogram
   {
-    uint32_t c = hist_d[tid];
+    const uint32_t c = hist_d[tid];
     uint32_t x = c;
 #pragma unroll
     for (int off = 1; off < 32; off <<= 1) {
@@ -136,7 +155,6 @@ __global__ void __launch_bounds__(OS_THREADS) k_onesweep(const uint64_t *kin, co
     key[it] = valid ? kin[idx] : 0;
     val[it] = valid ? vin[idx] : 0;
   }
-  // stable ranks inside the warp: items in (item, lane) order = input order
 #pragma unroll
   for (int it = 0; it < OS_ITEMS; ++it) {
     const long long idx = tbase + it * 32 + lane;
@@ -155,7 +173,7 @@ __global__ void __launch_bounds__(OS_THREADS) k_onesweep(const uint64_t *kin, co
     rk[it] = before + __popc(peers & lt);
   }
   __syncthreads();
-  // per digit: warp-exclusive offsets and the tile count
+  // per digit d: warp-exclusive offsets, the tile count, its start in the tile
   const int d = tid;
   uint32_t cnt = 0;
 #pragma unroll
@@ -164,176 +182,172 @@ __global__ void __launch_bounds__(OS_THREADS) k_onesweep(const uint64_t *kin, co
     s_whist[w][d] = cnt;
     cnt += c;
   }
+  {
+    uint32_t x = cnt;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const uint32_t y = __shfl_up_sync(FULL, x, off);
+      if (lane >= off) x += y;
+    }
+    __syncthreads();  // s_wsum reuse
+    if (lane == 31) s_wsum[warp] = x;
+    __syncthreads();
+    uint32_t pre = 0;
+    for (int w = 0; w < warp; ++w) pre += s_wsum[w];
+    s_tstart[d] = pre + x - cnt;
+  }
   // decoupled look-back for digit d
-  uint32_t *my = status + (size_t)tile * RADIX + d;
+  unsigned long long *my = status + (size_t)tile * RADIX + d;
+  const unsigned long long tag = epoch << 34;
   uint32_t excl = 0;
   if (tile == 0) {
-    st_relaxed(my, FLAG_INC | cnt);
+    st_relaxed64(my, tag | (2ull << 32) | cnt);
   } else {
-    st_relaxed(my, FLAG_AGG | cnt);
+    st_relaxed64(my, tag | (1ull << 32) | cnt);
     long long t = tile - 1;
     unsigned spins = 0;
     bool failed = false;
     while (t >= 0) {
-      const uint32_t s = ld_relaxed(status + (size_t)t * RADIX + d);
-      const uint32_t fl = s & ~VALUE_MASK;
-      if (fl == 0) {
+      const unsigned long long w = ld_relaxed64(status + (size_t)t * RADIX + d);
+      if ((w >> 34) != epoch) {
         if (++spins > SPIN_LIMIT) { failed = true; break; }
         if (spins > 64) __nanosleep(32);
         continue;
       }
-      excl += s & VALUE_MASK;
-      if (fl == FLAG_INC) break;
+      excl += (uint32_t)w;
+      if (((w >> 32) & 3ull) == 2ull) break;
       --t;
     }
     if (failed) atomicOr(err, SGD_ERR_LOOKBACK);
-    st_relaxed(my, FLAG_INC | ((excl + cnt) & VALUE_MASK));
+    st_relaxed64(my, tag | (2ull << 32) | (uint32_t)(excl + cnt));
   }
   s_excl[d] = excl;
   __syncthreads();
+  // stage the tile in digit order
 #pragma unroll
   for (int it = 0; it < OS_ITEMS; ++it) {
     const long long idx = tbase + it * 32 + lane;
     if (idx < n) {
       const uint32_t dg = (uint32_t)(key[it] >> shift) & 255u;
-      const uint32_t dst = s_base[dg] + s_excl[dg] + s_whist[warp][dg] + rk[it];
-      if (dst < n) {  // always true unless a look-back gave up (the build then fails)
-        kout[dst] = key[it];
-        vout[dst] = val[it];
-      }
+      const uint32_t lp = s_tstart[dg] + s_whist[warp][dg] + rk[it];
+      s_k[lp] = key[it];
+      s_v[lp] = val[it];
+    }
+  }
+  __syncthreads();
+  const long long tn = min((long long)OS_TILE, n - tile * OS_TILE);
+  for (int i = tid; i < tn; i += OS_THREADS) {
+    const uint64_t k = s_k[i];
+    const uint32_t dg = (uint32_t)(k >> shift) & 255u;
+    const uint64_t dst = (uint64_t)s_base[dg] + s_excl[dg] + (i - s_tstart[dg]);
+    if (dst < (uint64_t)n) {  // always true unless a look-back gave up (the build then fails)
+      kout[dst] = k;
+      vout[dst] = s_v[i];
     }
   }
 }
 
-// After a round's sort: write the suffixes back to their SA slots, mark the
-// first member of every new group and give it its SA position.
-__global__ void k_post(const int32_t *act, long long na, const uint64_t *key, const int32_t *val,
-                       int32_t *SA, int32_t *headpos, int32_t *head) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long a = (long long)blockIdx.x * blockDim.x + threadIdx.x; a < na; a += stride) {
-    const int32_t p = act ? act[a] : (int32_t)a;
-    SA[p] = val[a];
-    const int h = a == 0 || key[a] != key[a - 1];
-    head[a] = h;
-    headpos[a] = h ? p : -1;
+// After a round's sort (na sorted keys/values; act maps them to SA slots, or
+// is the identity in round 0): write each suffix to its slot, give it the SA
+// position of the first member of its new group (a running max of the
+// positions of group heads), and list the suffixes whose group still has
+// another member (a running count of them gives their place in act2).  Both
+// scans run in one pass; look-back words pack flag (bits 63..62), the max
+// head position + 1 (61..31) and the count (30..0).
+__global__ void __launch_bounds__(OS_THREADS) k_post(const int32_t *act, long long na,
+                                                     const uint64_t *key, const int32_t *val,
+                                                     int32_t *SA, int32_t *rank, int32_t *act2,
+                                                     unsigned long long *pstatus, uint32_t *counter,
+                                                     uint32_t *err) {
+  constexpr int NW = OS_THREADS / 32;
+  __shared__ uint32_t s_wmax[NW], s_wsum[NW];
+  __shared__ uint32_t s_emax, s_esum;
+  __shared__ int s_tile;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) s_tile = (int)atomicAdd(&counter[CNT_POST], 1u);
+  __syncthreads();
+  const long long tile = s_tile;
+  const long long base = tile * OS_TILE + (long long)tid * OS_ITEMS;
+  uint32_t hp[OS_ITEMS];  // head position + 1, or 0
+  uint32_t keep = 0;      // bit i: item i stays unresolved
+  uint32_t tmax = 0, tsum = 0;
+#pragma unroll
+  for (int i = 0; i < OS_ITEMS; ++i) {
+    const long long a = base + i;
+    hp[i] = 0;
+    if (a < na) {
+      const uint64_t k = key[a];
+      const bool head = a == 0 || key[a - 1] != k;
+      const bool last = a == na - 1 || key[a + 1] != k;
+      const int32_t p = act ? act[a] : (int32_t)a;
+      if (head) hp[i] = (uint32_t)p + 1;
+      if (!(head && last)) { keep |= 1u << i; ++tsum; }
+      tmax = max(tmax, hp[i]);
+    }
   }
-}
-
-// rank[i] = head position of i's group; flag suffixes whose group has >= 2 members
-__global__ void k_rank(long long na, const int32_t *val, const int32_t *newrank, const int32_t *head,
-                       int32_t *rank, int32_t *keep) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long a = (long long)blockIdx.x * blockDim.x + threadIdx.x; a < na; a += stride) {
-    rank[val[a]] = newrank[a];
-    const bool single = head[a] && (a == na - 1 || head[a + 1]);
-    keep[a] = single ? 0 : 1;
-  }
-}
-
-__global__ void k_compact(long long na, const int32_t *act, const int32_t *head, const int32_t *pos,
-                          int32_t *act2, int32_t *count) {
-  const long long stride = (long long)gridDim.x * blockDim.x;
-  for (long long a = (long long)blockIdx.x * blockDim.x + threadIdx.x; a < na; a += stride) {
-    const bool single = head[a] && (a == na - 1 || head[a + 1]);
-    if (!single) act2[pos[a]] = act ? act[a] : (int32_t)a;
-    if (a == na - 1) *count = pos[a] + (single ? 0 : 1);
-  }
-}
-
-// ---------------------------------------------------------------------------
-// device-wide scans (sum or max) in three steps: tile totals, a scan of the
-// totals in one CTA, and the per-tile scan with its offset.
-template <bool MAX>
-__device__ __forceinline__ int sop(int a, int b) { return MAX ? max(a, b) : a + b; }
-template <bool MAX>
-__device__ __forceinline__ int sid() { return MAX ? INT_MIN : 0; }
-
-// Block-wide scan of one value per thread: inclusive and exclusive prefixes
-// and the block total.
-template <bool MAX>
-__device__ void block_scan(int v, int &incl, int &excl, int &total) {
-  constexpr int NW = SC_THREADS / 32;
-  __shared__ int s_w[NW];
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  int x = v;
+  // block-exclusive (max, sum) over threads
+  uint32_t xm = tmax, xs = tsum;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(FULL, x, off);
-    if (lane >= off) x = sop<MAX>(x, y);
+    const uint32_t ym = __shfl_up_sync(FULL, xm, off), ys = __shfl_up_sync(FULL, xs, off);
+    if (lane >= off) { xm = max(xm, ym); xs += ys; }
   }
-  int wex = __shfl_up_sync(FULL, x, 1);
-  if (lane == 0) wex = sid<MAX>();
-  if (lane == 31) s_w[warp] = x;
+  if (lane == 31) { s_wmax[warp] = xm; s_wsum[warp] = xs; }
   __syncthreads();
-  if (warp == 0) {
-    int w = lane < NW ? s_w[lane] : sid<MAX>();
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_up_sync(FULL, w, off);
-      if (lane >= off) w = sop<MAX>(w, y);
-    }
-    if (lane < NW) s_w[lane] = w;
+  uint32_t pm = 0, ps = 0, Tm = 0, Ts = 0;
+  for (int w = 0; w < NW; ++w) {
+    if (w < warp) { pm = max(pm, s_wmax[w]); ps += s_wsum[w]; }
+    Tm = max(Tm, s_wmax[w]);
+    Ts += s_wsum[w];
   }
-  __syncthreads();
-  const int pre = warp > 0 ? s_w[warp - 1] : sid<MAX>();
-  incl = sop<MAX>(pre, x);
-  excl = sop<MAX>(pre, wex);
-  total = s_w[NW - 1];
-  __syncthreads();
-}
-
-template <bool MAX>
-__global__ void __launch_bounds__(SC_THREADS) k_scan_reduce(const int32_t *in, long long n,
-                                                            int32_t *tile_sums) {
-  const long long base = (long long)blockIdx.x * SC_TILE + (long long)threadIdx.x * SC_ITEMS;
-  int acc = sid<MAX>();
-#pragma unroll
-  for (int i = 0; i < SC_ITEMS; ++i)
-    if (base + i < n) acc = sop<MAX>(acc, in[base + i]);
-  int incl, excl, total;
-  block_scan<MAX>(acc, incl, excl, total);
-  if (threadIdx.x == 0) tile_sums[blockIdx.x] = total;
-}
-
-// exclusive scan of the tile totals, in place, one CTA
-template <bool MAX>
-__global__ void __launch_bounds__(SC_THREADS) k_scan_tiles(int32_t *tile_sums, long long ntiles) {
-  int carry = sid<MAX>();
-  for (long long base = 0; base < ntiles; base += SC_THREADS) {
-    const long long i = base + threadIdx.x;
-    const int v = i < ntiles ? tile_sums[i] : sid<MAX>();
-    int incl, excl, total;
-    block_scan<MAX>(v, incl, excl, total);
-    if (i < ntiles) tile_sums[i] = sop<MAX>(carry, excl);
-    carry = sop<MAX>(carry, total);
-  }
-}
-
-template <bool MAX, bool INCLUSIVE>
-__global__ void __launch_bounds__(SC_THREADS) k_scan_apply(const int32_t *in, int32_t *out, long long n,
-                                                           const int32_t *tile_sums) {
-  const long long base = (long long)blockIdx.x * SC_TILE + (long long)threadIdx.x * SC_ITEMS;
-  int v[SC_ITEMS];
-  int acc = sid<MAX>();
-#pragma unroll
-  for (int i = 0; i < SC_ITEMS; ++i) {
-    v[i] = base + i < n ? in[base + i] : sid<MAX>();
-    acc = sop<MAX>(acc, v[i]);
-  }
-  int incl, excl, total;
-  block_scan<MAX>(acc, incl, excl, total);
-  int run = sop<MAX>(tile_sums[blockIdx.x], excl);
-#pragma unroll
-  for (int i = 0; i < SC_ITEMS; ++i) {
-    if (base + i < n) {
-      if (INCLUSIVE) {
-        run = sop<MAX>(run, v[i]);
-        out[base + i] = run;
-      } else {
-        out[base + i] = run;
-        run = sop<MAX>(run, v[i]);
+  uint32_t em = max(pm, __shfl_up_sync(FULL, xm, 1)), es = ps + __shfl_up_sync(FULL, xs, 1);
+  if (lane == 0) { em = pm; es = ps; }
+  // tile look-back (thread 0)
+  if (tid == 0) {
+    unsigned long long *my = pstatus + tile;
+    uint32_t bm = 0, bs = 0;
+    auto pack = [](unsigned long long flag, uint32_t m, uint32_t s) {
+      return (flag << 62) | ((unsigned long long)m << 31) | (unsigned long long)s;
+    };
+    if (tile == 0) {
+      st_relaxed64(my, pack(2, Tm, Ts));
+    } else {
+      st_relaxed64(my, pack(1, Tm, Ts));
+      long long t = tile - 1;
+      unsigned spins = 0;
+      bool failed = false;
+      while (t >= 0) {
+        const unsigned long long w = ld_relaxed64(pstatus + t);
+        const unsigned long long fl = w >> 62;
+        if (fl == 0) {
+          if (++spins > SPIN_LIMIT) { failed = true; break; }
+          if (spins > 64) __nanosleep(32);
+          continue;
+        }
+        bm = max(bm, (uint32_t)((w >> 31) & 0x7fffffffull));
+        bs += (uint32_t)(w & 0x7fffffffull);
+        if (fl == 2) break;
+        --t;
       }
+      if (failed) atomicOr(err, SGD_ERR_LOOKBACK);
+      st_relaxed64(my, pack(2, max(bm, Tm), bs + Ts));
     }
+    s_emax = bm;
+    s_esum = bs;
+    if ((tile + 1) * (long long)OS_TILE >= na) counter[CNT_ACTIVE] = bs + Ts;  // the last tile
+  }
+  __syncthreads();
+  uint32_t rm = max(s_emax, em), rs = s_esum + es;
+#pragma unroll
+  for (int i = 0; i < OS_ITEMS; ++i) {
+    const long long a = base + i;
+    if (a >= na) break;
+    rm = max(rm, hp[i]);
+    const int32_t p = act ? act[a] : (int32_t)a;
+    const int32_t v = val[a];
+    SA[p] = v;
+    rank[v] = (int32_t)rm - 1;
+    if (keep & (1u << i)) act2[rs++] = p;
   }
 }
 
@@ -342,17 +356,6 @@ int grid_for(long long n, int per_block) {
   if (g > 152 * 16) g = 152 * 16;
   if (g < 1) g = 1;
   return (int)g;
-}
-
-template <bool MAX, bool INCLUSIVE>
-cudaError_t device_scan(const int32_t *in, int32_t *out, long long n, int32_t *tile_sums,
-                        cudaStream_t st, int *launches) {
-  const long long tiles = (n + SC_TILE - 1) / SC_TILE;
-  k_scan_reduce<MAX><<<(unsigned)tiles, SC_THREADS, 0, st>>>(in, n, tile_sums);
-  k_scan_tiles<MAX><<<1, SC_THREADS, 0, st>>>(tile_sums, tiles);
-  k_scan_apply<MAX, INCLUSIVE><<<(unsigned)tiles, SC_THREADS, 0, st>>>(in, out, n, tile_sums);
-  *launches += 3;
-  return cudaGetLastError();
 }
 
 int bits_of(unsigned long long x) {
@@ -365,47 +368,15 @@ int bits_of(unsigned long long x) {
 
 size_t sa_scratch_bytes(int64_t cap) {
   const long long c = cap > 0 ? cap : 1;
-  const long long os_tiles = (c + OS_TILE - 1) / OS_TILE;
-  const long long sc_tiles = (c + SC_TILE - 1) / SC_TILE;
-  return (size_t)c * (8 + 8 + 4 + 4 + 4 + 4 + 4 + 4 + 4) + (size_t)sc_tiles * 4 + 8 * RADIX * 4 +
-         (size_t)os_tiles * RADIX * 4 + 64;
-}
-
-cudaError_t sa_scratch_alloc(SaScratch *s, int64_t cap) {
-  *s = SaScratch{};
-  const long long c = cap > 0 ? cap : 1;
-  s->cap = cap;
-  const long long os_tiles = (c + OS_TILE - 1) / OS_TILE;
-  const long long sc_tiles = (c + SC_TILE - 1) / SC_TILE;
-  s->status_words = os_tiles * RADIX;
-  cudaError_t e = cudaSuccess;
-  auto al = [&](void **p, size_t bytes) {
-    if (e == cudaSuccess) e = cudaMalloc(p, bytes);
-  };
-  al((void **)&s->keyA, c * 8);
-  al((void **)&s->keyB, c * 8);
-  al((void **)&s->valA, c * 4);
-  al((void **)&s->valB, c * 4);
-  al((void **)&s->rank, c * 4);
-  al((void **)&s->act, c * 4);
-  al((void **)&s->act2, c * 4);
-  al((void **)&s->tmp, c * 4);
-  al((void **)&s->head, c * 4);
-  al((void **)&s->tile_sums, (sc_tiles + 1) * 4);
-  al((void **)&s->hist, 8 * RADIX * 4);
-  al((void **)&s->status, s->status_words * 4);
-  al((void **)&s->counter, 64);
-  if (e == cudaSuccess) e = cudaMallocHost((void **)&s->h_pinned, 64);
-  if (e == cudaSuccess) e = cudaMallocHost((void **)&s->h_hist, 8 * RADIX * 4);
-  if (e != cudaSuccess) sa_scratch_free(s);
-  return e;
+  const long long tiles = (c + OS_TILE - 1) / OS_TILE;
+  return (size_t)c * (8 + 8 + 4 * 5) + (size_t)tiles * RADIX * 8 + (size_t)tiles * 8 +
+         8 * RADIX * 4 + 1024 + 16 * 256;
 }
 
 size_t sa_scratch_carve(SaScratch *s, unsigned char *base, size_t bytes, int64_t cap) {
   *s = SaScratch{};
   const long long c = cap > 0 ? cap : 1;
-  const long long os_tiles = (c + OS_TILE - 1) / OS_TILE;
-  const long long sc_tiles = (c + SC_TILE - 1) / SC_TILE;
+  const long long tiles = (c + OS_TILE - 1) / OS_TILE;
   size_t off = 0;
   auto take = [&](size_t n) {
     unsigned char *p = base + off;
@@ -413,7 +384,7 @@ size_t sa_scratch_carve(SaScratch *s, unsigned char *base, size_t bytes, int64_t
     return p;
   };
   s->cap = cap;
-  s->status_words = os_tiles * RADIX;
+  s->status_words = tiles * RADIX;
   s->keyA = (uint64_t *)take(c * 8);
   s->keyB = (uint64_t *)take(c * 8);
   s->valA = (int32_t *)take(c * 4);
@@ -421,87 +392,34 @@ size_t sa_scratch_carve(SaScratch *s, unsigned char *base, size_t bytes, int64_t
   s->rank = (int32_t *)take(c * 4);
   s->act = (int32_t *)take(c * 4);
   s->act2 = (int32_t *)take(c * 4);
-  s->tmp = (int32_t *)take(c * 4);
-  s->head = (int32_t *)take(c * 4);
-  s->tile_sums = (int32_t *)take((sc_tiles + 1) * 4);
+  s->status = (unsigned long long *)take(s->status_words * 8);
+  s->pstatus = (unsigned long long *)take(tiles * 8);
   s->hist = (uint32_t *)take(8 * RADIX * 4);
-  s->status = (uint32_t *)take(s->status_words * 4);
-  s->counter = (uint32_t *)take(64);
+  s->counter = (uint32_t *)take(1024);
   if (off > bytes) *s = SaScratch{};
   return off;
 }
 
+cudaError_t sa_scratch_alloc(SaScratch *s, int64_t cap) {
+  *s = SaScratch{};
+  const size_t bytes = sa_scratch_bytes(cap);
+  unsigned char *base = nullptr;
+  cudaError_t e = cudaMalloc((void **)&base, bytes);
+  if (e != cudaSuccess) return e;
+  sa_scratch_carve(s, base, bytes, cap);
+  s->owned = base;
+  e = cudaMallocHost((void **)&s->h_pinned, 64);
+  if (e == cudaSuccess) e = cudaMallocHost((void **)&s->h_hist, 8 * RADIX * 4);
+  if (e != cudaSuccess) sa_scratch_free(s);
+  return e;
+}
+
 void sa_scratch_free(SaScratch *s) {
-  cudaFree(s->keyA); cudaFree(s->keyB); cudaFree(s->valA); cudaFree(s->valB);
-  cudaFree(s->rank); cudaFree(s->act); cudaFree(s->act2); cudaFree(s->tmp); cudaFree(s->head);
-  cudaFree(s->tile_sums); cudaFree(s->hist); cudaFree(s->status); cudaFree(s->counter);
+  if (s->owned) cudaFree(s->owned);
   if (s->h_pinned) cudaFreeHost(s->h_pinned);
   if (s->h_hist) cudaFreeHost(s->h_hist);
   *s = SaScratch{};
 }
-
-namespace {
-
-struct Sorter {
-  const SaScratch &s;
-  cudaStream_t st;
-  uint32_t *err;
-  SaStats *stats;
-  bool time_passes;
-  int *launches;
-  std::vector<cudaEvent_t> evs;
-
-  // Sorts (keyA, valA)[0..n) by the low `bits` of the key.  Returns the
-  // buffers holding the result through kres / vres.
-  cudaError_t sort(long long n, int bits, uint64_t *&kres, int32_t *&vres) {
-    uint64_t *kin = s.keyA, *kout = s.keyB;
-    int32_t *vin = s.valA, *vout = s.valB;
-    const int ndig = std::max(1, (bits + 7) / 8);
-    cudaError_t e = cudaMemsetAsync(s.hist, 0, 8 * RADIX * 4, st);
-    if (e != cudaSuccess) return e;
-    k_hist<<<grid_for(n, 256 * 8), 256, 0, st>>>(kin, n, ndig, s.hist);
-    ++*launches;
-    e = cudaMemcpyAsync(s.h_hist, s.hist, (size_t)ndig * RADIX * 4, cudaMemcpyDeviceToHost, st);
-    if (e != cudaSuccess) return e;
-    e = cudaStreamSynchronize(st);
-    if (e != cudaSuccess) return e;
-    const long long tiles = (n + OS_TILE - 1) / OS_TILE;
-    for (int d = 0; d < ndig; ++d) {
-      bool trivial = false;
-      for (int v = 0; v < RADIX; ++v)
-        if ((long long)s.h_hist[d * RADIX + v] == n) trivial = true;
-      if (trivial) continue;
-      e = cudaMemsetAsync(s.status, 0, (size_t)tiles * RADIX * 4, st);
-      if (e == cudaSuccess) e = cudaMemsetAsync(s.counter, 0, 4, st);
-      if (e != cudaSuccess) return e;
-      cudaEvent_t e0 = nullptr, e1 = nullptr;
-      if (time_passes) {
-        cudaEventCreate(&e0);
-        cudaEventCreate(&e1);
-        cudaEventRecord(e0, st);
-      }
-      k_onesweep<<<(unsigned)tiles, OS_THREADS, 0, st>>>(kin, vin, kout, vout, n, 8 * d,
-                                                         s.hist + d * RADIX, s.status, s.counter, err);
-      ++*launches;
-      if (time_passes) {
-        cudaEventRecord(e1, st);
-        evs.push_back(e0);
-        evs.push_back(e1);
-      }
-      e = cudaGetLastError();
-      if (e != cudaSuccess) return e;
-      stats->passes++;
-      stats->pass_elems += n;
-      std::swap(kin, kout);
-      std::swap(vin, vout);
-    }
-    kres = kin;
-    vres = vin;
-    return cudaSuccess;
-  }
-};
-
-}  // namespace
 
 int sa_build(const SaScratch &s, const int32_t *text, int64_t n, int32_t *sa, uint32_t *err,
              cudaStream_t st, SaStats *stats, bool time_passes, int *launches) {
@@ -509,73 +427,108 @@ int sa_build(const SaScratch &s, const int32_t *text, int64_t n, int32_t *sa, ui
   if (!stats) stats = &local;
   *stats = SaStats{};
   if (n <= 0) return 0;
-  if (n > s.cap) return -1;
-  if (n == 1) {
-    if (cudaMemsetAsync(sa, 0, 4, st) != cudaSuccess) return -1;
-    return 0;
-  }
-  Sorter so{s, st, err, stats, time_passes, launches, {}};
-  cudaError_t e = cudaSuccess;
-  const int G = grid_for(n, 256 * 4);
+  if (n > s.cap || s.keyA == nullptr) return -1;
+  if (n == 1) return cudaMemsetAsync(sa, 0, 4, st) == cudaSuccess ? 0 : -1;
+  const long long tiles_max = (n + OS_TILE - 1) / OS_TILE;
+  std::vector<cudaEvent_t> evs;
+  unsigned long long epoch = 0;
+  int pass_idx = 0;
+  uint64_t *kin = s.keyA, *kout = s.keyB;
+  int32_t *vin = s.valA, *vout = s.valB;
+  auto ok = [](cudaError_t e) { return e == cudaSuccess; };
+  if (!ok(cudaMemsetAsync(s.status, 0, (size_t)tiles_max * RADIX * 8, st))) return -1;
+  if (!ok(cudaMemsetAsync(s.counter, 0, 1024, st))) return -1;
+
+  // LSD passes over the non-constant digit places of (kin, vin)[0..na)
+  auto passes = [&](long long na, int ndig) -> bool {
+    const long long tiles = (na + OS_TILE - 1) / OS_TILE;
+    kin = s.keyA; vin = s.valA; kout = s.keyB; vout = s.valB;
+    for (int d = 0; d < ndig; ++d) {
+      bool trivial = false;
+      for (int v = 0; v < RADIX; ++v)
+        if ((long long)s.h_hist[d * RADIX + v] == na) trivial = true;
+      if (trivial) continue;
+      if (pass_idx >= MAX_PASSES) return false;
+      cudaEvent_t e0 = nullptr, e1 = nullptr;
+      if (time_passes) {
+        cudaEventCreate(&e0);
+        cudaEventCreate(&e1);
+        cudaEventRecord(e0, st);
+      }
+      k_onesweep<<<(unsigned)tiles, OS_THREADS, 0, st>>>(kin, vin, kout, vout, na, 8 * d,
+                                                         s.hist + d * RADIX, s.status,
+                                                         s.counter + CNT_PASS + pass_idx, ++epoch, err);
+      ++pass_idx;
+      ++*launches;
+      if (time_passes) {
+        cudaEventRecord(e1, st);
+        evs.push_back(e0);
+        evs.push_back(e1);
+      }
+      if (!ok(cudaGetLastError())) return false;
+      stats->passes++;
+      stats->pass_elems += na;
+      std::swap(kin, kout);
+      std::swap(vin, vout);
+    }
+    return true;
+  };
+  auto read_back = [&](int ndig) -> bool {
+    if (!ok(cudaMemcpyAsync(s.h_pinned, s.counter + CNT_ACTIVE, 4, cudaMemcpyDeviceToHost, st)))
+      return false;
+    if (!ok(cudaMemcpyAsync(s.h_hist, s.hist, (size_t)ndig * RADIX * 4, cudaMemcpyDeviceToHost, st)))
+      return false;
+    return ok(cudaStreamSynchronize(st));
+  };
+
   // round 0: sort by the first token
-  k_init0<<<G, 256, 0, st>>>(text, n, s.keyA, s.valA);
+  if (!ok(cudaMemsetAsync(s.hist, 0, 8 * RADIX * 4, st))) return -1;
+  k_init_keys<<<grid_for(n, 256 * 4), 256, 0, st>>>(text, n, s.keyA, s.valA, s.hist);
   ++*launches;
-  uint64_t *kr;
-  int32_t *vr;
-  e = so.sort(n, 32, kr, vr);
-  if (e != cudaSuccess) return -1;
+  if (!read_back(4)) return -1;
+  if (!passes(n, 4)) return -1;
   long long na = n;
   const int32_t *act = nullptr;
   int32_t *act_next = s.act;
   long long h = 1;
-  const int round_bits = bits_of((unsigned long long)(n - 1) * (unsigned long long)(n + 1) +
-                                 (unsigned long long)n);
+  const int ndig = (bits_of((unsigned long long)(n - 1) * (unsigned long long)(n + 1) +
+                            (unsigned long long)n) + 7) / 8;
   for (;;) {
     stats->rounds++;
     stats->sorted_elems += na;
-    stats->model_bytes += na * (16 + 12);
-    // write back, new heads, ranks, and the suffixes still unresolved
-    int32_t *spare = (vr == s.valA) ? s.valB : s.valA;  // free int32 buffer of this round
-    k_post<<<grid_for(na, 256 * 4), 256, 0, st>>>(act, na, kr, vr, sa, s.tmp, s.head);
+    const long long tiles = (na + OS_TILE - 1) / OS_TILE;
+    if (!ok(cudaMemsetAsync(s.pstatus, 0, (size_t)tiles * 8, st))) return -1;
+    if (!ok(cudaMemsetAsync(s.counter + CNT_POST, 0, 4, st))) return -1;
+    k_post<<<(unsigned)tiles, OS_THREADS, 0, st>>>(act, na, kin, vin, sa, s.rank, act_next, s.pstatus,
+                                                   s.counter, err);
     ++*launches;
-    e = device_scan<true, true>(s.tmp, s.tmp, na, s.tile_sums, st, launches);
-    if (e != cudaSuccess) return -1;
-    k_rank<<<grid_for(na, 256 * 4), 256, 0, st>>>(na, vr, s.tmp, s.head, s.rank, spare);
-    ++*launches;
-    e = device_scan<false, false>(spare, spare, na, s.tile_sums, st, launches);
-    if (e != cudaSuccess) return -1;
-    k_compact<<<grid_for(na, 256 * 4), 256, 0, st>>>(na, act, s.head, spare, act_next,
-                                                      (int32_t *)s.counter + 1);
-    ++*launches;
-    e = cudaMemcpyAsync(s.h_pinned, (int32_t *)s.counter + 1, 4, cudaMemcpyDeviceToHost, st);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(st);
-    if (e != cudaSuccess) return -1;
-    const long long next = s.h_pinned[0];
-    if (next == 0) break;
     if (h >= n) break;  // cannot happen for a valid order; guards the loop
-    // next round over the unresolved suffixes
+    // next round's keys over the unresolved suffixes (their number is read on
+    // the device), then its size and histograms in one read-back
+    if (!ok(cudaMemsetAsync(s.hist, 0, 8 * RADIX * 4, st))) return -1;
+    k_round_keys<<<grid_for(na, 256 * 4), 256, 0, st>>>(act_next, s.counter, sa, s.rank, h, n, ndig,
+                                                        s.keyA, s.valA, s.hist);
+    ++*launches;
+    if (!read_back(ndig)) return -1;
+    const long long next = s.h_pinned[0];
+    stats->model_bytes += na * (16 + 12);
+    if (next == 0) break;
     act = act_next;
     act_next = (act_next == s.act) ? s.act2 : s.act;
     na = next;
-    k_keys<<<grid_for(na, 256 * 4), 256, 0, st>>>(act, na, sa, s.rank, h, n, s.keyA, s.valA);
-    ++*launches;
     const int passes_before = stats->passes;
-    e = so.sort(na, round_bits, kr, vr);
-    if (e != cudaSuccess) return -1;
+    if (!passes(na, ndig)) return -1;
     stats->model_bytes += na * 24LL * (stats->passes - passes_before);
     h *= 2;
   }
   stats->model_bytes += 8LL * n;
-  e = cudaStreamSynchronize(st);
-  if (e != cudaSuccess) return -1;
-  if (time_passes) {
-    for (size_t i = 0; i + 1 < so.evs.size(); i += 2) {
-      float ms = 0;
-      cudaEventElapsedTime(&ms, so.evs[i], so.evs[i + 1]);
-      stats->pass_ms += ms;
-      cudaEventDestroy(so.evs[i]);
-      cudaEventDestroy(so.evs[i + 1]);
-    }
+  if (!ok(cudaStreamSynchronize(st))) return -1;
+  for (size_t i = 0; i + 1 < evs.size(); i += 2) {
+    float ms = 0;
+    cudaEventElapsedTime(&ms, evs[i], evs[i + 1]);
+    stats->pass_ms += ms;
+    cudaEventDestroy(evs[i]);
+    cudaEventDestroy(evs[i + 1]);
   }
   return 0;
 }

@@ -89,20 +89,19 @@ cudaError_t launch_suffix_keys(const int32_t *text, const int32_t *sa, int64_t n
 
 // sa_build.cu
 struct SaScratch {
-  int64_t cap;          // elements the scratch can sort
+  int64_t cap;                  // elements the scratch can sort
   uint64_t *keyA, *keyB;
   int32_t *valA, *valB;
-  int32_t *rank;        // head-position ranks
-  int32_t *act, *act2;  // SA positions of unresolved suffixes
-  int32_t *tmp;         // head positions, then ranks
-  int32_t *head;        // 1 at the first member of each group
-  int32_t *tile_sums;
-  uint32_t *hist;       // [8][256] digit histograms
-  uint32_t *status;     // look-back words, [tiles][256]
-  uint32_t *counter;    // tile ticket + small device counters
-  int32_t *h_pinned;    // pinned host words for counts read back by the driver
-  uint32_t *h_hist;     // pinned [8][256]
+  int32_t *rank;                // head-position ranks
+  int32_t *act, *act2;          // SA positions of unresolved suffixes
+  unsigned long long *status;   // radix look-back words, [tiles][256]
+  unsigned long long *pstatus;  // post-pass look-back words, [tiles]
+  uint32_t *hist;               // [8][256] digit histograms
+  uint32_t *counter;            // active count, tickets
+  int32_t *h_pinned;            // host words for counts read back by the driver
+  uint32_t *h_hist;             // host [8][256]
   int64_t status_words;
+  unsigned char *owned;         // device block owned by this scratch (alloc), else null
 };
 struct SaStats {
   int rounds = 0, passes = 0;
