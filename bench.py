@@ -122,12 +122,13 @@ def make_steps(cfg, seed, n_steps):
     return tr, tok, n, steps
 
 
-def algorithmic_bytes_propose(sum_n, B, T, k, N):
-    """Bytes one propose_with_update launch must touch (lower bound):
-    every valid token of every row once, the sampled ids, the outputs, and the
-    sectors of two suffix-array binary searches per row."""
+def algorithmic_bytes_propose(sum_n, B, T, k, N, ingest_tokens=0):
+    """Bytes one step launch must touch (lower bound): every valid token of
+    every row once, the sampled ids, the outputs, the sectors of two
+    suffix-array binary searches per row, and the ingested docs (read once,
+    written once into the ring)."""
     probe = 0 if N <= 0 else B * 2 * int(np.ceil(np.log2(N + 1))) * 2 * 32
-    return 4 * sum_n + 4 * B * T + B * (8 * k + 16) + probe
+    return 4 * sum_n + 4 * B * T + B * (8 * k + 16) + probe + 8 * ingest_tokens
 
 
 def run_ours(args, rank, world):
@@ -178,15 +179,17 @@ def run_ours(args, rank, world):
             torch.from_numpy(s.finished.astype(np.int64)).to(dev),
             None if s.reset_tokens is None else torch.from_numpy(s.reset_tokens).to(dev),
             torch.from_numpy(s.reset_n).to(dev)) for s in steps]
-    # the step's kernels, captured once: propose_with_update, then the ingest
-    g_prop, g_ing = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    # the step, captured once: update + propose + ingest of the finished rows
+    # (one fused launch; the two calls when there is nothing to ingest)
+    fused = bool(m_fin and cfg.corpus_tokens)
+    g_step = torch.cuda.CUDAGraph()
     dr.propose_with_update(g_tok, g_n, d_samp, out=out)  # warm the launch path
     torch.cuda.synchronize()
-    with torch.cuda.graph(g_prop, stream=stream):
-        dr.propose_with_update(g_tok, g_n, d_samp, out=out, stream=stream)
-    if m_fin and cfg.corpus_tokens:
-        with torch.cuda.graph(g_ing, stream=stream):
-            dr.ingest(g_tok, d_rows, d_st, d_ln, num_tokens=g_n, stream=stream)
+    with torch.cuda.graph(g_step, stream=stream):
+        if fused:
+            dr.step(g_tok, g_n, d_samp, d_rows, d_st, d_ln, out=out, stream=stream)
+        else:
+            dr.propose_with_update(g_tok, g_n, d_samp, out=out, stream=stream)
     g_tok.copy_(torch.from_numpy(tok))   # undo the warm-up update
     g_n.copy_(torch.from_numpy(n))
     props = torch.cuda.get_device_properties(dev)
@@ -230,11 +233,9 @@ def run_ours(args, rank, world):
         stage(i)
         if ev:
             ev[0].record(stream)
-        g_prop.replay()
+        g_step.replay()
         if ev:
             ev[1].record(stream)
-        if m_fin and cfg.corpus_tokens:
-            g_ing.replay()
         policy(i)
         if ev:
             ev[2].record(stream)
@@ -259,7 +260,7 @@ def run_ours(args, rank, world):
     clocks = clk.stop()
     barrier(world)
     torch.cuda.synchronize()
-    graph_kernels = 1 + (3 if (m_fin and cfg.corpus_tokens) else 0)
+    graph_kernels = 1
     launches = dr.launch_count() - l0 + graph_kernels * K
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     prop_ms = [e[0].elapsed_time(e[1]) for e in evs]
@@ -278,7 +279,8 @@ def run_ours(args, rank, world):
     # suffix-array builds, standalone (the suffix-array workload)
     sa = sa_build_leg(args, dev)
     peak, peak_kind = peaks()
-    byts = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens)
+    ing_tok = float(np.mean([fin[Wm + j][3] for j in range(K)])) if fused else 0.0
+    byts = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens, ing_tok)
     prop_avg_s = float(np.mean(prop_ms)) / 1e3
     ach = byts / prop_avg_s / 1e9
     rl_prop = {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 2),
@@ -310,7 +312,8 @@ def run_ours(args, rank, world):
                    "R": cfg.R, "T": cfg.T, "corpus_tokens": cfg.corpus_tokens,
                    "rebuild_tokens": cfg.rebuild_tokens,
                    "l2": "flushed before every timed step (%d MiB write)" % (flush.numel() * 4 >> 20),
-                   "launch": "each step replays CUDA graphs of the library's kernels",
+                   "launch": "each step replays one CUDA graph: the fused sgd_step launch "
+                             "(update + propose + ingest); rebuilds on a side stream",
                    "parallelism": "replicas" if world > 1 else "single"},
         "roofline": rl, "roofline_propose": rl_prop, "kernels": kernels,
         "propose_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
@@ -422,10 +425,11 @@ def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state,
             d_rows[:m].copy_(h_fin[j][0], non_blocking=True)
             d_st[:m].copy_(h_fin[j][1], non_blocking=True)
             d_ln[:m].copy_(h_fin[j][2], non_blocking=True)
-        dr.propose_with_update(g_tok, g_n, d_samp, out=out)
         if m and cfg.corpus_tokens:
-            dr.ingest(g_tok, d_rows[:m], d_st[:m], d_ln[:m], num_tokens=g_n)
+            dr.step(g_tok, g_n, d_samp, d_rows[:m], d_st[:m], d_ln[:m], out=out)
             state["ingested"] += int(s.ingest_lengths.sum())
+        else:
+            dr.propose_with_update(g_tok, g_n, d_samp, out=out)
         if cfg.corpus_tokens:
             if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
                 dr.build_sa(side)

@@ -5,7 +5,7 @@
  * kernels for sm_103a on streams the caller passes; no call on the drafting
  * path synchronises with the host, allocates memory or changes a device
  * address, so sgd_update_state / sgd_propose / sgd_propose_with_update /
- * sgd_ingest can be captured in a CUDA graph.
+ * sgd_ingest / sgd_step can be captured in a CUDA graph.
  *
  * Sources (page title, section):
  *   [RFC]  "Suffix decoding on GPU (suffix_gpu)", vLLM issue: Summary, Design.
@@ -56,6 +56,7 @@ extern "C" {
 #define SGD_ERR_DOC_TOKEN     0x8u  /* ingest: token outside [0, V); doc truncated    */
 #define SGD_ERR_DOC_TOO_LONG  0x10u /* ingest: doc + sentinel exceeds the ring; skipped */
 #define SGD_ERR_LOOKBACK      0x20u /* suffix sort: a radix look-back gave up waiting */
+#define SGD_ERR_INGEST_WAIT   0x40u /* sgd_step: a doc's row update never showed; doc skipped */
 
 typedef struct sgd_ctx sgd_ctx; /* opaque, library-owned */
 
@@ -151,6 +152,21 @@ int sgd_propose_with_update(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_token
                             const int32_t *sampled, int32_t T, const uint8_t *active,
                             int32_t B, int32_t *drafts, int32_t *num_valid, float *score,
                             float *probs, int32_t *match_info, void *stream);
+
+/* One decoding step: sgd_propose_with_update, then sgd_ingest of n_docs docs
+ * read from the rows after their update ([PYPI] Quickstart: the serving loop
+ * calls propose_with_update and harvest_finished every step).  Results equal
+ * those of the two calls made in that order on `stream` (num_tokens, after
+ * the update, bounds the docs).  With 1 <= n_docs <= 32 everything runs in
+ * ONE kernel launch: one extra CTA appends the docs while the row CTAs
+ * draft, after waiting (bounded, ~0.1 s) for each doc's row to be updated; a
+ * wait that runs out skips that doc and sets SGD_ERR_INGEST_WAIT.  Larger
+ * n_docs run as the two calls.  Steps of one context must not overlap (one
+ * stream at a time).  SGD_ENOCORPUS if n_docs > 0 without a corpus. */
+int sgd_step(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_tokens, const int32_t *sampled,
+             int32_t T, const uint8_t *active, int32_t B, int32_t *drafts, int32_t *num_valid,
+             float *score, float *probs, int32_t *match_info, const int32_t *rows,
+             const int32_t *starts, const int32_t *lengths, int32_t n_docs, void *stream);
 
 /* Appends finished responses to the corpus ring ([PYPI] Quickstart:
  * harvest_finished; How it works, step 4: oldest documents are evicted when
@@ -251,10 +267,15 @@ int sgd_build_stats(sgd_ctx *ctx, sgd_build_info *info);
  *   SGD_INJECT_NONE        clear;
  *   SGD_INJECT_BUILD_FAIL  the next build reports failure;
  *   SGD_INJECT_BUILD_HANG  the next build never reports completion (its
- *                          kernels still run; sgd_poll stays pending). */
+ *                          kernels still run; sgd_poll stays pending);
+ *   SGD_INJECT_STEP_WAIT   the ingest CTA of the next fused sgd_step waits for
+ *                          a row signal that no CTA sends: its bounded wait
+ *                          (~0.1 s) runs out, the docs are skipped and
+ *                          SGD_ERR_INGEST_WAIT is set; drafting is unaffected. */
 #define SGD_INJECT_NONE       0
 #define SGD_INJECT_BUILD_FAIL 1
 #define SGD_INJECT_BUILD_HANG 2
+#define SGD_INJECT_STEP_WAIT  3
 int sgd_debug_inject(sgd_ctx *ctx, int what);
 
 /* Kernel launches the context made since creation (every library kernel). */

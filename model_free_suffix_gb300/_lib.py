@@ -28,10 +28,12 @@ ERR_DOC_ARGS = 0x4
 ERR_DOC_TOKEN = 0x8
 ERR_DOC_TOO_LONG = 0x10
 ERR_LOOKBACK = 0x20
+ERR_INGEST_WAIT = 0x40
 
 INJECT_NONE = 0
 INJECT_BUILD_FAIL = 1
 INJECT_BUILD_HANG = 2
+INJECT_STEP_WAIT = 3
 
 
 class SgdConfig(ctypes.Structure):
@@ -102,6 +104,7 @@ def load() -> ctypes.CDLL:
         "sgd_propose": (ctypes.c_int, [P, P, P, P, i32, P, P, P, P, P, P]),
         "sgd_propose_with_update": (ctypes.c_int, [P, P, P, P, i32, P, i32, P, P, P, P, P, P]),
         "sgd_ingest": (ctypes.c_int, [P, P, P, i32, P, P, P, i32, P]),
+        "sgd_step": (ctypes.c_int, [P, P, P, P, i32, P, i32, P, P, P, P, P, P, P, P, i32, P]),
         "sgd_build_sa": (ctypes.c_int, [P, P, P]),
         "sgd_poll": (ctypes.c_int, [P, ctypes.c_int, i64, P, u64p]),
         "sgd_suffix_array": (ctypes.c_int, [P, P, i64, P, P]),

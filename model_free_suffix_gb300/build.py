@@ -32,7 +32,7 @@ def nvcc() -> str:
 
 def _headers():
     hs = [os.path.join(INCLUDE, "sgd.h")]
-    hs += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith(".h")]
+    hs += [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".h", ".cuh"))]
     return hs
 
 

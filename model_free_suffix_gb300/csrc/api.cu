@@ -35,6 +35,8 @@ struct sgd_ctx {
   // device state
   uint32_t *d_err = nullptr;        // sticky error bits of drafting and ingest
   uint32_t *d_build_err = nullptr;  // error bits of the build in progress
+  uint32_t *d_step_ready = nullptr; // [max_batch] fused step: per-row update epoch
+  uint32_t *d_step_sync = nullptr;  // fused step: epoch, arrivals
   int32_t *d_ring = nullptr;
   RingState *d_rs = nullptr;
   int64_t *d_doc_start = nullptr;
@@ -107,6 +109,8 @@ int choose_self_warps(const sgd_config &c) {
 
 void free_ctx(sgd_ctx *x) {
   cudaFree(x->d_err);
+  cudaFree(x->d_step_ready);
+  cudaFree(x->d_step_sync);
   cudaFree(x->d_build_err);
   cudaFree(x->d_ring);
   cudaFree(x->d_rs);
@@ -291,6 +295,10 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
       al((void **)&x->d_keys[i], (size_t)C * 16);
     }
     al((void **)&x->d_desc, sizeof(CorpusDesc));
+    al((void **)&x->d_step_ready, (size_t)cfg->max_batch * 4);
+    al((void **)&x->d_step_sync, 8);
+    if (e == cudaSuccess) e = cudaMemset(x->d_step_ready, 0, (size_t)cfg->max_batch * 4);
+    if (e == cudaSuccess) e = cudaMemset(x->d_step_sync, 0, 8);
     al((void **)&x->ing.eff, (size_t)cfg->max_ingest_docs * 4);
     al((void **)&x->ing.dest, (size_t)cfg->max_ingest_docs * 8);
     al((void **)&x->ing.order, (size_t)cfg->max_ingest_docs * 4);
@@ -422,6 +430,60 @@ int sgd_propose_with_update(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens,
                       probs, match_info, stream);
 }
 
+int sgd_step(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int32_t *sampled, int32_t T,
+             const uint8_t *active, int32_t B, int32_t *drafts, int32_t *num_valid, float *score,
+             float *probs, int32_t *match_info, const int32_t *rows, const int32_t *starts,
+             const int32_t *lengths, int32_t n_docs, void *stream) {
+  if (!x) return SGD_EINVAL;
+  if (n_docs < 0 || n_docs > x->cfg.max_ingest_docs) return SGD_EINVAL;
+  if (n_docs > 0 && !x->corpus) return SGD_ENOCORPUS;
+  if (n_docs > 0 && (!rows || !starts || !lengths)) return SGD_EINVAL;
+  if (n_docs == 0 || n_docs > propose_step_max_docs() || B == 0) {
+    int r = sgd_propose_with_update(x, token_ids, num_tokens, sampled, T, active, B, drafts,
+                                    num_valid, score, probs, match_info, stream);
+    if (r != SGD_OK || n_docs == 0) return r;
+    return sgd_ingest(x, token_ids, num_tokens, B, rows, starts, lengths, n_docs, stream);
+  }
+  if (B < 0 || B > x->cfg.max_batch || !sampled || T < 1 || T > x->cfg.max_sampled)
+    return SGD_EINVAL;
+  if (!token_ids || !num_tokens || !drafts || !num_valid) return SGD_EINVAL;
+  if (!aligned16(token_ids)) return SGD_EINVAL;
+  ProposeArgs a = base_args(x);
+  a.tok = token_ids;
+  a.ntok = num_tokens;
+  a.sampled = sampled;
+  a.T = T;
+  a.do_update = 1;
+  a.active = active;
+  a.B = B;
+  a.drafts = drafts;
+  a.num_valid = num_valid;
+  a.score = score;
+  a.probs = probs;
+  a.match_info = match_info;
+  a.ing_m = n_docs;
+  a.ing_rows = rows;
+  a.ing_starts = starts;
+  a.ing_lengths = lengths;
+  a.ring = x->d_ring;
+  a.C = x->cfg.corpus_capacity;
+  a.rs = x->d_rs;
+  a.doc_start = x->d_doc_start;
+  a.doc_len = x->d_doc_len;
+  a.max_docs = x->cfg.max_docs;
+  a.step_ready = x->d_step_ready;
+  a.step_sync = x->d_step_sync;
+  {
+    std::unique_lock<std::mutex> lk(x->mu);
+    if (x->inject == SGD_INJECT_STEP_WAIT) {
+      a.ing_skew = 1;
+      x->inject = SGD_INJECT_NONE;
+    }
+  }
+  x->launches++;
+  return check_cuda(launch_propose(a, (cudaStream_t)stream));
+}
+
 int sgd_ingest(sgd_ctx *x, const int32_t *token_ids, const int32_t *num_tokens, int32_t B,
                const int32_t *rows, const int32_t *starts, const int32_t *lengths, int32_t n_docs,
                void *stream) {
@@ -453,8 +515,8 @@ int sgd_build_sa(sgd_ctx *x, void *stream, void *side_stream) {
   if (e != cudaSuccess) return SGD_ECUDA;
   x->job_back = back;
   x->job_side = (cudaStream_t)side_stream;
-  x->job_inject = x->inject;
-  x->inject = SGD_INJECT_NONE;
+  x->job_inject = x->inject == SGD_INJECT_STEP_WAIT ? SGD_INJECT_NONE : x->inject;
+  if (x->inject != SGD_INJECT_STEP_WAIT) x->inject = SGD_INJECT_NONE;
   x->job_ready = true;
   x->bstate = B_RUNNING;
   x->cv.notify_all();
@@ -587,7 +649,7 @@ int sgd_build_stats(sgd_ctx *x, sgd_build_info *info) {
 
 int sgd_debug_inject(sgd_ctx *x, int what) {
   if (!x) return SGD_EINVAL;
-  if (what < SGD_INJECT_NONE || what > SGD_INJECT_BUILD_HANG) return SGD_EINVAL;
+  if (what < SGD_INJECT_NONE || what > SGD_INJECT_STEP_WAIT) return SGD_EINVAL;
   std::unique_lock<std::mutex> lk(x->mu);
   x->inject = what;
   if (what == SGD_INJECT_NONE && x->bstate == B_HUNG) {

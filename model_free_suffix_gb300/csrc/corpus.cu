@@ -12,7 +12,7 @@
 // followed by the sentinel Z = V.  Because docs are appended at the write
 // offset and evicted from the oldest end, the live tokens always form one
 // circular run starting at the oldest doc: doc_start[head] + live == wp (mod C).
-#include "sgd_internal.h"
+#include "ingest_cta.cuh"
 
 namespace sgd {
 
@@ -52,67 +52,6 @@ __global__ void __launch_bounds__(256) ingest_measure(const int32_t *tok, const 
 
 constexpr int PLAN_THREADS = 1024;
 constexpr int PLAN_CHUNK = 4096;   // docs whose lengths are staged per round
-constexpr int PLAN_WINDOW = 1024;  // oldest FIFO lengths staged for evictions
-constexpr int SMALL_DOCS = 32;     // calls up to this size run as one CTA
-
-// Sequential placement, in call order: evict the oldest docs while the new
-// doc would not fit (or the FIFO is full), then append at the write offset.
-// A doc pushed by this call and evicted by a later doc of the same call is
-// not copied.  Thread 0 walks the docs; every value it reads (effective doc
-// lengths, lengths of the oldest FIFO docs) is staged in shared memory by
-// the whole CTA first, so the walk never waits on global memory.
-__device__ void plan_docs(const int32_t *eff_g, const int32_t *eff_s, int m, long long C,
-                          RingState *rs, int64_t *doc_start, int32_t *doc_len, int max_docs,
-                          int64_t *dest, int32_t *order, uint32_t *err, int *s_eff, int *s_dl,
-                          RingState *s_rs) {
-  const int tid = threadIdx.x;
-  if (tid == 0) *s_rs = *rs;
-  __syncthreads();
-  const RingState r0 = *s_rs;
-  const int win = min(r0.ndocs, PLAN_WINDOW);
-  for (int j = tid; j < win; j += blockDim.x) s_dl[j] = doc_len[(r0.head + j) % max_docs];
-  RingState r = r0;
-  int evicted = 0, pushed = 0, ev_call = 0;
-  uint32_t fl = 0;
-  for (int c0 = 0; c0 < m; c0 += PLAN_CHUNK) {
-    const int cn = min(PLAN_CHUNK, m - c0);
-    if (eff_s == nullptr)
-      for (int j = tid; j < cn; j += blockDim.x) s_eff[j] = eff_g[c0 + j];
-    __syncthreads();
-    if (tid == 0) {
-      const int *ef = eff_s ? eff_s + c0 : s_eff;
-      for (int j = 0; j < cn; ++j) {
-        const int i = c0 + j;
-        dest[i] = -1;
-        const int L = ef[j];
-        if (L <= 0) continue;
-        const long long s = (long long)L + 1;
-        if (s > C) { fl |= SGD_ERR_DOC_TOO_LONG; continue; }
-        while (r.ndocs > 0 && (r.live + s > C || r.ndocs == max_docs)) {
-          const int len = evicted < win ? s_dl[evicted] : doc_len[r.head];
-          r.live -= (long long)len + 1;
-          r.head = (r.head + 1) % max_docs;
-          r.ndocs--;
-          if (evicted >= r0.ndocs) dest[order[ev_call++]] = -1;  // pushed by this call
-          ++evicted;
-        }
-        const int slot = (r.head + r.ndocs) % max_docs;
-        doc_start[slot] = r.wp;
-        doc_len[slot] = L;
-        dest[i] = r.wp;
-        order[pushed++] = i;
-        r.wp = (r.wp + s) % C;
-        r.live += s;
-        r.ndocs++;
-      }
-    }
-    __syncthreads();
-  }
-  if (tid == 0) {
-    *rs = r;
-    if (fl) atomicOr(err, fl);
-  }
-}
 
 __global__ void __launch_bounds__(PLAN_THREADS) ingest_plan(const int32_t *eff, int m, long long C,
                                                             RingState *rs, int64_t *doc_start,
@@ -122,58 +61,30 @@ __global__ void __launch_bounds__(PLAN_THREADS) ingest_plan(const int32_t *eff, 
   __shared__ int s_eff[PLAN_CHUNK];
   __shared__ int s_dl[PLAN_WINDOW];
   __shared__ RingState s_rs;
-  plan_docs(eff, nullptr, m, C, rs, doc_start, doc_len, max_docs, dest, order, err, s_eff, s_dl,
-            &s_rs);
+  const int tid = threadIdx.x;
+  if (tid == 0) s_rs = *rs;
+  __syncthreads();
+  PlanWalk w{s_rs, s_rs.ndocs, min(s_rs.ndocs, PLAN_WINDOW), 0, 0, 0, 0u};
+  for (int j = tid; j < w.win; j += blockDim.x) s_dl[j] = doc_len[(w.r.head + j) % max_docs];
+  for (int c0 = 0; c0 < m; c0 += PLAN_CHUNK) {
+    const int cn = min(PLAN_CHUNK, m - c0);
+    for (int j = tid; j < cn; j += blockDim.x) s_eff[j] = eff[c0 + j];
+    __syncthreads();
+    if (tid == 0)
+      for (int j = 0; j < cn; ++j)
+        place_doc(w, c0 + j, s_eff[j], C, s_dl, doc_start, doc_len, max_docs, dest, order);
+    __syncthreads();
+  }
+  if (tid == 0) {
+    *rs = w.r;
+    if (w.fl) atomicOr(err, w.fl);
+  }
 }
 
-// A small call in one CTA: measure (one warp per doc), plan, copy.
-__global__ void __launch_bounds__(PLAN_THREADS) ingest_small(
-    const int32_t *tok, const int32_t *ntok, int B, int S, int V, const int32_t *rows,
-    const int32_t *starts, const int32_t *lengths, int m, int32_t *ring, long long C, RingState *rs,
-    int64_t *doc_start, int32_t *doc_len, int max_docs, int64_t *dest, int32_t *order,
-    uint32_t *err) {
-  __shared__ int s_eff[SMALL_DOCS];
-  __shared__ int s_dl[PLAN_WINDOW];
-  __shared__ RingState s_rs;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nw = blockDim.x >> 5;
-  for (int i = warp; i < m; i += nw) {
-    const int row = rows[i], st = starts[i], ln = lengths[i];
-    const bool ok = row >= 0 && row < B && st >= 0 && ln >= 0 && (long long)st + ln <= S &&
-                    (ntok == nullptr || (long long)st + ln <= (long long)ntok[row]);
-    if (!ok) {
-      if (lane == 0) {
-        s_eff[i] = -1;
-        atomicOr(err, SGD_ERR_DOC_ARGS);
-      }
-      continue;
-    }
-    const int32_t *src = tok + (size_t)row * S + st;
-    int first = ln;
-    for (int u0 = 0; u0 < ln; u0 += 32) {
-      const int u = u0 + lane;
-      const int v = u < ln ? src[u] : 0;
-      const unsigned bad = __ballot_sync(FULL, u < ln && (v < 0 || v >= V));
-      if (bad) { first = u0 + __ffs(bad) - 1; break; }
-    }
-    if (lane == 0) {
-      s_eff[i] = first;
-      if (first < ln) atomicOr(err, SGD_ERR_DOC_TOKEN);
-    }
-  }
-  __syncthreads();
-  plan_docs(nullptr, s_eff, m, C, rs, doc_start, doc_len, max_docs, dest, order, err, nullptr, s_dl,
-            &s_rs);
-  for (int i = 0; i < m; ++i) {
-    const long long d0 = dest[i];
-    if (d0 < 0) continue;
-    const int L = s_eff[i];
-    const int32_t *src = tok + (size_t)rows[i] * S + starts[i];
-    for (int u = threadIdx.x; u <= L; u += blockDim.x) {
-      long long pos = d0 + u;
-      if (pos >= C) pos -= C;
-      ring[pos] = u < L ? src[u] : V;
-    }
-  }
+// A call of up to SMALL_DOCS docs as one CTA.
+__global__ void __launch_bounds__(PLAN_THREADS) ingest_small(SmallIngest g) {
+  __shared__ SmallIngestSmem s;
+  ingest_small_cta(g, s);
 }
 
 __global__ void __launch_bounds__(256) ingest_copy(const int32_t *tok, int S, const int32_t *rows,
@@ -242,8 +153,9 @@ cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S,
                           cudaStream_t st, int *launches) {
   if (m <= 0) return cudaSuccess;
   if (m <= SMALL_DOCS) {
-    ingest_small<<<1, PLAN_THREADS, 0, st>>>(tok, ntok, B, S, V, rows, starts, lengths, m, ring, C, rs,
-                                             doc_start, doc_len, max_docs, sc.dest, sc.order, err);
+    const SmallIngest g{tok, ntok, B, S, V, rows, starts, lengths, m, ring, C, rs,
+                        doc_start, doc_len, max_docs, err, nullptr, 0u};
+    ingest_small<<<1, PLAN_THREADS, 0, st>>>(g);
     *launches += 1;
     return cudaGetLastError();
   }

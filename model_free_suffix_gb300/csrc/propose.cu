@@ -26,7 +26,7 @@
 // match, which leaves the chosen source and its occurrences unchanged.
 #include <climits>
 
-#include "sgd_internal.h"
+#include "ingest_cta.cuh"
 
 namespace sgd {
 
@@ -437,7 +437,42 @@ __global__ void __launch_bounds__(128) update_kernel(int32_t *tok, int32_t *ntok
 }
 
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void propose_body(const ProposeArgs &a) {
+// Fused step: every CTA of the launch reads the step epoch E, then counts
+// itself in; the last one to arrive resets the count and advances E (all
+// CTAs have read it by then), so each launch has its own epoch.
+__device__ __forceinline__ void step_arrive(uint32_t *sync, uint32_t e0) {
+  __threadfence();
+  if (atomicAdd(&sync[1], 1u) == gridDim.x - 1) {
+    sync[1] = 0;
+    atomicExch(&sync[0], e0 + 1);
+  }
+}
+
+__device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t *p) {
+  return *reinterpret_cast<const volatile uint32_t *>(p);
+}
+
+__device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// CTA 0 of a fused step: the ingest of the step's finished docs.
+__device__ __forceinline__ void step_ingest(const ProposeArgs &a) {
+  extern __shared__ __align__(16) int dsm[];
+  __shared__ uint32_t s_e0;
+  if (threadIdx.x == 0) {
+    const uint32_t e0 = ld_volatile_u32(&a.step_sync[0]);
+    s_e0 = e0;
+    step_arrive(a.step_sync, e0);
+  }
+  __syncthreads();
+  const SmallIngest g{a.tok, a.ntok, a.B, a.S, a.V, a.ing_rows, a.ing_starts, a.ing_lengths,
+                      a.ing_m, a.ring, a.C, a.rs, a.doc_start, a.doc_len, a.max_docs, a.err,
+                      a.step_ready, s_e0 + 1 + a.ing_skew};
+  ingest_small_cta(g, *reinterpret_cast<SmallIngestSmem *>(dsm));
+}
+
+__device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) {
   extern __shared__ __align__(16) int dsm[];
   __shared__ int s_wM[MAX_SELF_WARPS], s_wcnt[MAX_SELF_WARPS];
   __shared__ int s_hist[256];
@@ -447,7 +482,6 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
   __shared__ int s_n, s_Ms, s_cs, s_q, s_sel, s_need, s_have_corpus;
   __shared__ int s_self_done, s_ms_ready, s_pms, s_Mc, s_c0c, s_cpf;
 
-  const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
   const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
   int32_t *row = a.tok + (size_t)b * S;
@@ -474,13 +508,22 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
     cp.Lmax = cp.N >= 2 ? top_level(cp.N) : 0;
   }
   if (warp == 0) {
+    const uint32_t e0 = a.ing_m > 0 && lane == 0 ? ld_volatile_u32(&a.step_sync[0]) : 0u;
     int n = a.ntok[b];
     uint32_t fl = 0;
     if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
     if (n > S) { n = S; fl |= SGD_ERR_NUM_TOKENS; }
     if (a.do_update) n = update_row_warp(row, n, a.sampled + (size_t)b * a.T, a.T, S, a.V, lane, fl);
+    if (lane == 0 && a.do_update) a.ntok[b] = n;
+    if (a.ing_m > 0) {  // publish the updated row to the ingest CTA
+      __threadfence();
+      __syncwarp();
+      if (lane == 0) {
+        st_release_u32(&a.step_ready[b], e0 + 1);
+        step_arrive(a.step_sync, e0);
+      }
+    }
     if (lane == 0) {
-      if (a.do_update) a.ntok[b] = n;
       if (fl) atomicOr(a.err, fl);
       s_n = n;
       s_have_corpus = a.desc != nullptr && cp.N >= 2;
@@ -949,7 +992,12 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a) {
 // to 20 warps with one.
 template <int MAXT, int MINB>
 __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a) {
-  propose_body(a);
+  if (a.ing_m > 0) {
+    if (blockIdx.x == 0) step_ingest(a);
+    else propose_body(a, blockIdx.x - 1);
+  } else {
+    propose_body(a, blockIdx.x);
+  }
 }
 
 }  // namespace
@@ -957,17 +1005,21 @@ __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a
 size_t propose_smem_bytes(int nself, int R, int k, int cand_cap) {
   const size_t big = (size_t)max(cand_cap, R * k);
   const size_t ints = ((size_t)MAX_D + (size_t)nself * R + 3 * (size_t)R + big + 3) & ~(size_t)3;
-  return sizeof(int) * ints + sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP;
+  const size_t bytes = sizeof(int) * ints + sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP;
+  return bytes > sizeof(SmallIngestSmem) ? bytes : sizeof(SmallIngestSmem);
 }
+
+int propose_step_max_docs() { return SMALL_DOCS; }
 
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   if (a.B <= 0) return cudaSuccess;
   const int warps = a.nself + (a.desc ? NPROBE3 : 0);
   const size_t smem = propose_smem_bytes(a.nself, a.R, a.k, a.cand_cap);
+  const int grid = a.B + (a.ing_m > 0 ? 1 : 0);
   if (warps <= 12)
-    propose_kernel<384, 2><<<a.B, 32 * warps, smem, st>>>(a);
+    propose_kernel<384, 2><<<grid, 32 * warps, smem, st>>>(a);
   else
-    propose_kernel<640, 1><<<a.B, 32 * warps, smem, st>>>(a);
+    propose_kernel<640, 1><<<grid, 32 * warps, smem, st>>>(a);
   return cudaGetLastError();
 }
 

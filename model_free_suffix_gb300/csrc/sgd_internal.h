@@ -58,10 +58,24 @@ struct ProposeArgs {
   uint32_t *err;
   int nself;               // self-scan warps per row
   int cand_cap;            // corpus candidate buffer (power of two >= R)
+  // fused step: ing_m > 0 adds CTA 0, which appends ing_m docs to the ring
+  // once their rows are updated (the row CTAs are 1..B)
+  int ing_m;
+  const int32_t *ing_rows, *ing_starts, *ing_lengths;
+  int32_t *ring;
+  long long C;
+  RingState *rs;
+  int64_t *doc_start;
+  int32_t *doc_len;
+  int max_docs;
+  uint32_t *step_ready;  // [max_batch] per row: the step epoch once updated
+  uint32_t *step_sync;   // [0] step epoch, [1] CTAs arrived in this launch
+  uint32_t ing_skew;     // added to the awaited epoch (0; 1 only under test injection)
 };
 
 // propose.cu
 size_t propose_smem_bytes(int nself, int R, int k, int cand_cap);
+int propose_step_max_docs();  // largest doc count a fused step ingests in-kernel
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st);
 cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, int B,
                           int T, int S, int V, uint32_t *err, cudaStream_t st);

@@ -146,6 +146,24 @@ class SuffixDrafter:
             "sgd_propose_with_update")
         return out
 
+    def step(self, token_ids: torch.Tensor, num_tokens: torch.Tensor, sampled: torch.Tensor,
+             rows: torch.Tensor, starts: torch.Tensor, lengths: torch.Tensor,
+             active: Optional[torch.Tensor] = None, out: Optional[Proposal] = None,
+             stream=None) -> Proposal:
+        """propose_with_update, then ingest of the docs (rows, starts, lengths)
+        read after the update: one kernel launch for up to 32 docs."""
+        B, T = sampled.shape
+        m = rows.shape[0]
+        out = out or self.new_outputs(B)
+        self._check(self._lib.sgd_step(
+            self._h, self._t(token_ids, name="token_ids"), self._t(num_tokens, name="num_tokens"),
+            self._t(sampled, name="sampled"), T, self._t(active, torch.uint8, "active"), B,
+            self._t(out.drafts), self._t(out.num_valid), self._t(out.score, torch.float32),
+            self._t(out.probs, torch.float32), self._t(out.match_info),
+            self._t(rows, name="rows"), self._t(starts, name="starts"),
+            self._t(lengths, name="lengths"), m, _stream_handle(stream)), "sgd_step")
+        return out
+
     # -- corpus ---------------------------------------------------------------
     def ingest(self, token_ids: torch.Tensor, rows: torch.Tensor, starts: torch.Tensor,
                lengths: torch.Tensor, num_tokens: Optional[torch.Tensor] = None, stream=None) -> None:

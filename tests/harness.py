@@ -85,8 +85,9 @@ class Lockstep:
     def __init__(self, cfg: W.Config, seed: int = 0, B: Optional[int] = None,
                  steps: Optional[int] = None, finish_frac: Optional[float] = None,
                  corpus: Optional[int] = None, drafter_over: Optional[dict] = None,
-                 param_over: Optional[dict] = None):
+                 param_over: Optional[dict] = None, fused: bool = False):
         self.cfg = cfg
+        self.fused = fused  # drive each step through sgd_step (update + propose + ingest)
         self.trace = W.ServingTrace(cfg, seed=seed, steps=steps, finish_frac=finish_frac, B=B)
         self.B = self.trace.B
         self.corpus = cfg.corpus_tokens if corpus is None else corpus
@@ -152,7 +153,14 @@ class Lockstep:
             self.swap()
         dev = self.dr.device
         sampled = torch.from_numpy(sd.sampled).to(dev)
-        self.dr.propose_with_update(self.tok, self.n, sampled, out=self.out)
+        m = sd.finished.shape[0]
+        fused = self.fused and self.ring is not None
+        if fused:
+            self.dr.step(self.tok, self.n, sampled, torch.from_numpy(sd.finished).to(dev),
+                         torch.from_numpy(sd.ingest_starts).to(dev),
+                         torch.from_numpy(sd.ingest_lengths).to(dev), out=self.out)
+        else:
+            self.dr.propose_with_update(self.tok, self.n, sampled, out=self.out)
         O.update_state(self.o_tok, self.o_n, sd.sampled, self.cfg.V)
         if check:
             orc = O.propose(self.p, self.o_tok, self.o_n, X=self.X, rows=check_rows, threads=THREADS)
@@ -161,12 +169,12 @@ class Lockstep:
         if check_state:
             assert np.array_equal(to_np(self.n), self.o_n)
             assert np.array_equal(to_np(self.tok), self.o_tok)
-        m = sd.finished.shape[0]
         if m:
             if self.ring is not None:
-                rows_t = torch.from_numpy(sd.finished).to(dev)
-                self.dr.ingest(self.tok, rows_t, torch.from_numpy(sd.ingest_starts).to(dev),
-                               torch.from_numpy(sd.ingest_lengths).to(dev), num_tokens=self.n)
+                if not fused:
+                    rows_t = torch.from_numpy(sd.finished).to(dev)
+                    self.dr.ingest(self.tok, rows_t, torch.from_numpy(sd.ingest_starts).to(dev),
+                                   torch.from_numpy(sd.ingest_lengths).to(dev), num_tokens=self.n)
                 self.ring.ingest(self.o_tok, sd.finished, sd.ingest_starts, sd.ingest_lengths,
                                  num_tokens=self.o_n)
                 self.ingested_since_build += int(sd.ingest_lengths.sum())

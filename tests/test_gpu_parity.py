@@ -297,7 +297,7 @@ def test_ring_and_snapshot_match_oracle(max_m):
         lens[0] = min(lens[0], S - starts[0])
         if it % 7 == 3:
             rows[-1] = 99                                 # bad row -> skipped
-        num = np.full(max_m, S, dtype=np.int32)
+        num = rng.integers(S // 2, S + 1, size=max_m).astype(np.int32)  # some docs end past it
         dr.ingest(_dev(buf), _dev(rows), _dev(starts), _dev(lens), num_tokens=_dev(num[:m]))
         f_orc = ring.ingest(buf, rows, starts, lens, num_tokens=num[:m])
         assert dr.get_error(clear=True) == f_orc
