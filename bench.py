@@ -138,6 +138,13 @@ def algorithmic_bytes_propose(sum_n, B, T, k, N, ingest_tokens=0):
     return 4 * sum_n + 4 * B * T + B * (8 * k + 16) + probe + 8 * ingest_tokens
 
 
+def workload_config(cfg, world):
+    """The workload both arms run, by what it is and its sizes."""
+    return {"workload": WORKLOAD, "B": cfg.B, "S": cfg.S, "k": cfg.k, "D": cfg.D, "R": cfg.R,
+            "T": cfg.T, "corpus_tokens": cfg.corpus_tokens, "rebuild_tokens": cfg.rebuild_tokens,
+            "parallelism": "replicas" if world > 1 else "single"}
+
+
 def run_ours(args, rank, world):
     import torch
     from model_free_suffix_gb300 import SuffixDrafter
@@ -316,13 +323,10 @@ def run_ours(args, rank, world):
         "us_per_step": round(1e3 * total_ms_max / K, 2),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD, "B": cfg.B, "S": cfg.S, "k": cfg.k, "D": cfg.D,
-                   "R": cfg.R, "T": cfg.T, "corpus_tokens": cfg.corpus_tokens,
-                   "rebuild_tokens": cfg.rebuild_tokens,
-                   "l2": "flushed before every timed step (%d MiB write)" % (flush.numel() * 4 >> 20),
-                   "launch": "each step replays one CUDA graph: the fused sgd_step launch "
-                             "(update + propose + ingest); rebuilds on a side stream",
-                   "parallelism": "replicas" if world > 1 else "single"},
+        "config": dict(workload_config(cfg, world),
+                   l2="flushed before every timed step (%d MiB write)" % (flush.numel() * 4 >> 20),
+                   launch="each step replays one CUDA graph: the fused sgd_step launch "
+                          "(update + propose + ingest); rebuilds on a side stream"),
         "roofline": rl, "roofline_propose": rl_prop, "kernels": kernels,
         "propose_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
                        "median": round(1e3 * float(np.median(prop_ms)), 2),
@@ -577,6 +581,8 @@ def main():
                     help="steps of the long-context workload timed as a secondary line (0: skip)")
     ap.add_argument("--sa-only", type=int, default=0,
                     help="only time suffix-array builds of this many tokens and print them")
+    ap.add_argument("--long-only", action="store_true",
+                    help="only time the long-context workload and print its line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -595,7 +601,7 @@ def main():
                    "steps": args.steps, "warmup": args.warmup,
                    "ms_per_step": round(1e3 / cb["value"], 3), "higher_is_better": True,
                    "scaling": "weak", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
-                   "config": {"workload": WORKLOAD, "B": cfg.B, "S": cfg.S},
+                   "config": workload_config(cfg, world),
                    "impl": "reference", "cpu_baseline": cb,
                    "e2e": {"value": cb["value"], "unit": "steps/s", "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}}
@@ -612,6 +618,10 @@ def main():
         torch.cuda.set_device(dev)
         if rank == 0:
             print(json.dumps(sa_build_leg(args, dev, sizes=[args.sa_only])), flush=True)
+        return
+    if args.long_only:
+        if rank == 0:
+            print(json.dumps(long_context_leg(args, rank)), flush=True)
         return
     res = run_ours(args, rank, world)
     if args.long_context_steps > 0 and args.config == "c3":

@@ -6,11 +6,12 @@
 //     How it works, step 4 (built on a side CUDA stream).
 //
 // Order: suffixes compare token by token as signed int32, a proper prefix
-// first.  Construction (Manber & Myers): sort by the first token, give every
-// suffix the SA position of the first member of its group ("head rank"),
-// then for h = 1, 2, 4, ... re-sort only the suffixes whose group has more
-// than one member by the pair (rank[i], rank[i + h]) (rank -1 past the end),
-// until every group is a singleton.
+// first.  Construction (Manber & Myers): sort by the first h0 tokens (h0
+// tokens packed into one 64-bit key: as many as fit at the text's token
+// range, at most 4), give every suffix the SA position of the first member of
+// its group ("head rank"), then for h = h0, 2h0, 4h0, ... re-sort only the
+// suffixes whose group has more than one member by the pair (rank[i],
+// rank[i + h]) (rank -1 past the end), until every group is a singleton.
 //
 // Per round: one kernel builds the keys of the unresolved suffixes and all
 // digit histograms; the host reads the round's size and histograms back
@@ -40,10 +41,13 @@ constexpr int OS_TILE = OS_THREADS * OS_ITEMS;  // 2048 items per tile
 constexpr int RADIX = 256;
 constexpr unsigned SPIN_LIMIT = 1u << 18;  // ~0.1 s of polling; a normal wait is microseconds
 constexpr int MAX_PASSES = 250;            // ticket counters per build
+constexpr int LB = 8;                      // look-back words a thread reads per round trip
 
 // counter layout (uint32 words): [0] active count written by the post pass,
-// [1] post ticket, [2..] radix-pass tickets
-constexpr int CNT_ACTIVE = 0, CNT_POST = 1, CNT_PASS = 2;
+// [1] [2] smallest and largest token (order-preserving unsigned codes), [3]
+// post ticket, [4..] radix-pass tickets
+constexpr int CNT_ACTIVE = 0, CNT_MIN = 1, CNT_MAX = 2, CNT_POST = 3, CNT_PASS = 4;
+static_assert(CNT_PASS + 250 <= 256, "ticket block is 1 KB");
 
 __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long *p) {
   unsigned long long v;
@@ -62,22 +66,69 @@ __device__ __forceinline__ void hist_flush(uint32_t *s, int ndig, uint32_t *hist
     if (s[i]) atomicAdd(&hist[i], s[i]);
 }
 
-// round 0: key = the token, order-preserving for signed int32; all digit
-// histograms in the same pass
-__global__ void __launch_bounds__(256) k_init_keys(const int32_t *text, long long n, uint64_t *key,
+__host__ __device__ inline int bits_of(unsigned long long x) {
+  int b = 0;
+  while (x) { ++b; x >>= 1; }
+  return b;
+}
+
+// Round 0 sorts by the first h0 tokens of every suffix at once: token t is
+// coded as t - min + 1 in b bits (0 past the end of the text, which sorts a
+// proper prefix first), h0 codes packed into one 64-bit key.  Sorting by h0
+// tokens before doubling skips the most expensive early rounds.
+__host__ __device__ inline void pack_params(uint32_t lo, uint32_t hi, int &h0, int &b) {
+  b = bits_of((unsigned long long)(hi - lo) + 1);
+  h0 = 64 / b;
+  if (h0 > 4) h0 = 4;
+  if (h0 < 1) h0 = 1;
+}
+
+// smallest and largest token, as order-preserving unsigned codes
+__global__ void __launch_bounds__(256) k_minmax(const int32_t *text, long long n, uint32_t *counter) {
+  __shared__ uint32_t s_lo[8], s_hi[8];
+  uint32_t lo = 0xffffffffu, hi = 0u;
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
+    const uint32_t u = (uint32_t)text[i] ^ 0x80000000u;
+    lo = min(lo, u);
+    hi = max(hi, u);
+  }
+  lo = __reduce_min_sync(FULL, lo);
+  hi = __reduce_max_sync(FULL, hi);
+  const int warp = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) { s_lo[warp] = lo; s_hi[warp] = hi; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    for (int w = 1; w < (int)(blockDim.x >> 5); ++w) { lo = min(lo, s_lo[w]); hi = max(hi, s_hi[w]); }
+    atomicMin(&counter[CNT_MIN], lo);
+    atomicMax(&counter[CNT_MAX], hi);
+  }
+}
+
+// round 0 keys (h0 packed tokens) and the histograms of their digit places
+__global__ void __launch_bounds__(256) k_init_keys(const int32_t *text, long long n,
+                                                   const uint32_t *counter, uint64_t *key,
                                                    int32_t *val, uint32_t *hist) {
-  __shared__ uint32_t s[4 * RADIX];
-  for (int i = threadIdx.x; i < 4 * RADIX; i += blockDim.x) s[i] = 0;
+  __shared__ uint32_t s[8 * RADIX];
+  const uint32_t lo = counter[CNT_MIN], hi = counter[CNT_MAX];
+  int h0, b;
+  pack_params(lo, hi, h0, b);
+  const int nd = (h0 * b + 7) / 8;
+  for (int i = threadIdx.x; i < nd * RADIX; i += blockDim.x) s[i] = 0;
   __syncthreads();
   const long long stride = (long long)gridDim.x * blockDim.x;
   for (long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += stride) {
-    const uint32_t k = (uint32_t)text[i] ^ 0x80000000u;
+    uint64_t k = 0;
+    for (int t = 0; t < h0; ++t) {
+      const long long j = i + t;
+      const uint64_t c = j < n ? (uint64_t)(((uint32_t)text[j] ^ 0x80000000u) - lo) + 1 : 0;
+      k = (k << b) | c;
+    }
     key[i] = k;
     val[i] = (int32_t)i;
-#pragma unroll
-    for (int d = 0; d < 4; ++d) atomicAdd(&s[d * RADIX + ((k >> (8 * d)) & 255u)], 1u);
+    for (int d = 0; d < nd; ++d) atomicAdd(&s[d * RADIX + ((k >> (8 * d)) & 255u)], 1u);
   }
-  hist_flush(s, 4, hist);
+  hist_flush(s, nd, hist);
 }
 
 // doubling round: (head rank of i, 1 + head rank of i + h, or 0 past the end)
@@ -204,19 +255,31 @@ __global__ void __launch_bounds__(OS_THREADS) k_onesweep(const uint64_t *kin, co
     st_relaxed64(my, tag | (2ull << 32) | cnt);
   } else {
     st_relaxed64(my, tag | (1ull << 32) | cnt);
+    // LB predecessors per round trip; consume them nearest first and stop at
+    // the first inclusive word (done) or the first one not yet published
     long long t = tile - 1;
     unsigned spins = 0;
     bool failed = false;
-    while (t >= 0) {
-      const unsigned long long w = ld_relaxed64(status + (size_t)t * RADIX + d);
-      if ((w >> 34) != epoch) {
+    for (;;) {
+      unsigned long long w[LB];
+#pragma unroll
+      for (int j = 0; j < LB; ++j)
+        w[j] = t - j >= 0 ? ld_relaxed64(status + (size_t)(t - j) * RADIX + d) : 0ull;
+      int used = 0;
+      bool done = false;
+#pragma unroll
+      for (int j = 0; j < LB; ++j) {
+        if (done || used != j || (w[j] >> 34) != epoch) continue;
+        excl += (uint32_t)w[j];
+        used = j + 1;
+        done = ((w[j] >> 32) & 3ull) == 2ull;
+      }
+      if (done) break;
+      t -= used;
+      if (used == 0) {
         if (++spins > SPIN_LIMIT) { failed = true; break; }
         if (spins > 64) __nanosleep(32);
-        continue;
       }
-      excl += (uint32_t)w;
-      if (((w >> 32) & 3ull) == 2ull) break;
-      --t;
     }
     if (failed) atomicOr(err, SGD_ERR_LOOKBACK);
     st_relaxed64(my, tag | (2ull << 32) | (uint32_t)(excl + cnt));
@@ -302,39 +365,51 @@ __global__ void __launch_bounds__(OS_THREADS) k_post(const int32_t *act, long lo
   }
   uint32_t em = max(pm, __shfl_up_sync(FULL, xm, 1)), es = ps + __shfl_up_sync(FULL, xs, 1);
   if (lane == 0) { em = pm; es = ps; }
-  // tile look-back (thread 0)
-  if (tid == 0) {
+  // tile look-back (warp 0): lane i reads the word of tile t - i, 32 tiles
+  // per round trip, consumed nearest first up to the first inclusive word or
+  // the first word not yet published
+  if (warp == 0) {
     unsigned long long *my = pstatus + tile;
     uint32_t bm = 0, bs = 0;
     auto pack = [](unsigned long long flag, uint32_t m, uint32_t s) {
       return (flag << 62) | ((unsigned long long)m << 31) | (unsigned long long)s;
     };
     if (tile == 0) {
-      st_relaxed64(my, pack(2, Tm, Ts));
+      if (lane == 0) st_relaxed64(my, pack(2, Tm, Ts));
     } else {
-      st_relaxed64(my, pack(1, Tm, Ts));
+      if (lane == 0) st_relaxed64(my, pack(1, Tm, Ts));
       long long t = tile - 1;
       unsigned spins = 0;
       bool failed = false;
-      while (t >= 0) {
-        const unsigned long long w = ld_relaxed64(pstatus + t);
-        const unsigned long long fl = w >> 62;
-        if (fl == 0) {
+      for (;;) {
+        const unsigned long long w = t - lane >= 0 ? ld_relaxed64(pstatus + (t - lane)) : 0ull;
+        const unsigned fl = (unsigned)(w >> 62);
+        const unsigned inc = __ballot_sync(FULL, fl == 2), unp = __ballot_sync(FULL, fl == 0);
+        const int first_inc = inc ? __ffs(inc) - 1 : 32, first_unp = unp ? __ffs(unp) - 1 : 32;
+        const bool done = first_inc < first_unp;
+        const int used = done ? first_inc + 1 : first_unp;  // lanes [0, used) are consumed
+        const bool take = lane < used;
+        const uint32_t m = take ? (uint32_t)((w >> 31) & 0x7fffffffull) : 0u;
+        const uint32_t c = take ? (uint32_t)(w & 0x7fffffffull) : 0u;
+        bm = max(bm, __reduce_max_sync(FULL, m));
+        bs += __reduce_add_sync(FULL, c);
+        if (done) break;
+        t -= used;
+        if (used == 0) {
           if (++spins > SPIN_LIMIT) { failed = true; break; }
           if (spins > 64) __nanosleep(32);
-          continue;
         }
-        bm = max(bm, (uint32_t)((w >> 31) & 0x7fffffffull));
-        bs += (uint32_t)(w & 0x7fffffffull);
-        if (fl == 2) break;
-        --t;
       }
-      if (failed) atomicOr(err, SGD_ERR_LOOKBACK);
-      st_relaxed64(my, pack(2, max(bm, Tm), bs + Ts));
+      if (lane == 0) {
+        if (failed) atomicOr(err, SGD_ERR_LOOKBACK);
+        st_relaxed64(my, pack(2, max(bm, Tm), bs + Ts));
+      }
     }
-    s_emax = bm;
-    s_esum = bs;
-    if ((tile + 1) * (long long)OS_TILE >= na) counter[CNT_ACTIVE] = bs + Ts;  // the last tile
+    if (lane == 0) {
+      s_emax = bm;
+      s_esum = bs;
+      if ((tile + 1) * (long long)OS_TILE >= na) counter[CNT_ACTIVE] = bs + Ts;  // the last tile
+    }
   }
   __syncthreads();
   uint32_t rm = max(s_emax, em), rs = s_esum + es;
@@ -358,11 +433,6 @@ int grid_for(long long n, int per_block) {
   return (int)g;
 }
 
-int bits_of(unsigned long long x) {
-  int b = 0;
-  while (x) { ++b; x >>= 1; }
-  return b;
-}
 
 }  // namespace
 
@@ -438,6 +508,7 @@ int sa_build(const SaScratch &s, const int32_t *text, int64_t n, int32_t *sa, ui
   auto ok = [](cudaError_t e) { return e == cudaSuccess; };
   if (!ok(cudaMemsetAsync(s.status, 0, (size_t)tiles_max * RADIX * 8, st))) return -1;
   if (!ok(cudaMemsetAsync(s.counter, 0, 1024, st))) return -1;
+  if (!ok(cudaMemsetAsync(s.counter + CNT_MIN, 0xff, 4, st))) return -1;
 
   // LSD passes over the non-constant digit places of (kin, vin)[0..na)
   auto passes = [&](long long na, int ndig) -> bool {
@@ -474,23 +545,26 @@ int sa_build(const SaScratch &s, const int32_t *text, int64_t n, int32_t *sa, ui
     return true;
   };
   auto read_back = [&](int ndig) -> bool {
-    if (!ok(cudaMemcpyAsync(s.h_pinned, s.counter + CNT_ACTIVE, 4, cudaMemcpyDeviceToHost, st)))
+    if (!ok(cudaMemcpyAsync(s.h_pinned, s.counter + CNT_ACTIVE, 12, cudaMemcpyDeviceToHost, st)))
       return false;
     if (!ok(cudaMemcpyAsync(s.h_hist, s.hist, (size_t)ndig * RADIX * 4, cudaMemcpyDeviceToHost, st)))
       return false;
     return ok(cudaStreamSynchronize(st));
   };
 
-  // round 0: sort by the first token
+  // round 0: sort by the first h0 tokens
   if (!ok(cudaMemsetAsync(s.hist, 0, 8 * RADIX * 4, st))) return -1;
-  k_init_keys<<<grid_for(n, 256 * 4), 256, 0, st>>>(text, n, s.keyA, s.valA, s.hist);
-  ++*launches;
-  if (!read_back(4)) return -1;
-  if (!passes(n, 4)) return -1;
+  k_minmax<<<grid_for(n, 256 * 8), 256, 0, st>>>(text, n, s.counter);
+  k_init_keys<<<grid_for(n, 256 * 4), 256, 0, st>>>(text, n, s.counter, s.keyA, s.valA, s.hist);
+  *launches += 2;
+  if (!read_back(8)) return -1;
+  int h0 = 1, b0 = 32;
+  pack_params((uint32_t)s.h_pinned[1], (uint32_t)s.h_pinned[2], h0, b0);
+  if (!passes(n, (h0 * b0 + 7) / 8)) return -1;
   long long na = n;
   const int32_t *act = nullptr;
   int32_t *act_next = s.act;
-  long long h = 1;
+  long long h = h0;
   const int ndig = (bits_of((unsigned long long)(n - 1) * (unsigned long long)(n + 1) +
                             (unsigned long long)n) + 7) / 8;
   for (;;) {

@@ -459,6 +459,27 @@ def test_c4_suffix_array(N):
     dr.close()
 
 
+@pytest.mark.parametrize("lo,hi", [(0, 1), (0, (1 << 16) - 2), (0, 151936), (-5, (1 << 21) - 6),
+                                   (-(1 << 31), (1 << 31) - 1)])
+def test_suffix_array_token_ranges(lo, hi):
+    """Round 0 packs as many tokens per key as the text's token range allows
+    (4, 4, 3, 2 and 1 token here); every range must give the oracle's array."""
+    SuffixDrafter, W, O, H = _mods()
+    rng = np.random.default_rng(hi & 0xffff)
+    n = 30000
+    X = rng.integers(lo, hi, size=n, endpoint=True, dtype=np.int64)
+    span = rng.integers(lo, hi, size=300, endpoint=True, dtype=np.int64)
+    for s0 in range(0, n - 300, 3000):  # long repeats force many doubling rounds
+        X[s0:s0 + 300] = span
+    X[0], X[-1] = lo, hi
+    X = X.astype(np.int32)
+    dr = SuffixDrafter(max_batch=1, seq_capacity=8, vocab_size=16, corpus_capacity=n)
+    sa = dr.suffix_array(_dev(X)).cpu().numpy()
+    assert np.array_equal(sa, O.suffix_array(X))
+    assert dr.build_stats()["status"] == 0
+    dr.close()
+
+
 def test_c4_background_build_while_proposing():
     """The 1M corpus built on a side stream while proposes run; a graph
     captured before the swap reads the new index after it."""
