@@ -86,7 +86,17 @@ typedef struct {
                                   corpus occurrence selection (larger match sets take
                                   an exact multi-pass path)                        */
   int32_t  self_warps;         /* warps scanning each row (0: chosen from B and S) */
+  int32_t  corpus_records;     /* 1 (default): each snapshot also holds, per suffix-array
+                                  position, the suffix's position, the D-4 tokens before
+                                  it and the k tokens after its first four, so that a
+                                  small 4-token interval is evaluated from one read;
+                                  4*roundup4(1+max(D-4,0)+k) bytes per corpus token per
+                                  snapshot, used only while both snapshots' records fit
+                                  in SGD_RECORD_BUDGET bytes.  0: off.  Drafts are the
+                                  same either way. */
 } sgd_config;
+
+#define SGD_RECORD_BUDGET (8ull << 30)
 
 /* Fills *cfg with the defaults above (max_batch 256, S 4096, V 151936). */
 int sgd_config_default(sgd_config *cfg);

@@ -56,6 +56,7 @@ class SgdConfig(ctypes.Structure):
         ("max_ingest_docs", ctypes.c_int32),
         ("corpus_cand_cap", ctypes.c_int32),
         ("self_warps", ctypes.c_int32),
+        ("corpus_records", ctypes.c_int32),
     ]
 
 

@@ -44,6 +44,8 @@ struct sgd_ctx {
   int32_t *d_text[2] = {nullptr, nullptr};
   int32_t *d_sa[2] = {nullptr, nullptr};
   int4 *d_keys[2] = {nullptr, nullptr};
+  int32_t *d_rec[2] = {nullptr, nullptr};  // per-position records, or null (off / over budget)
+  RecShape rsh{};
   CorpusDesc *d_desc = nullptr;
   IngestScratch ing{};
   SaScratch sa{};
@@ -95,6 +97,7 @@ int validate(const sgd_config &c) {
       c.corpus_cand_cap > 16384)
     return SGD_EINVAL;
   if (c.self_warps < 0 || c.self_warps > MAX_SELF_WARPS) return SGD_EINVAL;
+  if (c.corpus_records != 0 && c.corpus_records != 1) return SGD_EINVAL;
   return SGD_OK;
 }
 
@@ -110,6 +113,8 @@ int choose_self_warps(const sgd_config &c) {
 void free_ctx(sgd_ctx *x) {
   cudaFree(x->d_err);
   cudaFree(x->d_step_ready);
+  cudaFree(x->d_rec[0]);
+  cudaFree(x->d_rec[1]);
   cudaFree(x->d_step_sync);
   cudaFree(x->d_build_err);
   cudaFree(x->d_ring);
@@ -166,6 +171,12 @@ void worker_main(sgd_ctx *x) {
                         cudaSuccess)
         status = SGD_EBUILD;
       ++launches;
+      if (r == 0 && x->d_rec[back] != nullptr) {
+        if (launch_records(x->d_text[back], x->d_sa[back], n, x->rsh, x->cfg.vocab_size,
+                           x->d_rec[back], side) != cudaSuccess)
+          status = SGD_EBUILD;
+        ++launches;
+      }
       e = cudaEventRecord(x->ev_b1, side);
       if (e == cudaSuccess)
         e = cudaMemcpyAsync(x->h_err, x->d_build_err, 4, cudaMemcpyDeviceToHost, side);
@@ -237,6 +248,7 @@ int sgd_config_default(sgd_config *c) {
   c->max_docs = 65536;
   c->max_ingest_docs = 4096;
   c->corpus_cand_cap = 2048;
+  c->corpus_records = 1;
   c->self_warps = 0;
   return SGD_OK;
 }
@@ -295,6 +307,12 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
       al((void **)&x->d_keys[i], (size_t)C * 16);
     }
     al((void **)&x->d_desc, sizeof(CorpusDesc));
+    x->rsh = rec_shape(cfg->max_tree_depth, cfg->k);
+    if (cfg->corpus_records &&
+        2ull * (unsigned long long)C * (unsigned long long)x->rsh.ri * 4ull <= SGD_RECORD_BUDGET) {
+      al((void **)&x->d_rec[0], (size_t)C * x->rsh.ri * 4);
+      al((void **)&x->d_rec[1], (size_t)C * x->rsh.ri * 4);
+    }
     al((void **)&x->d_step_ready, (size_t)cfg->max_batch * 4);
     al((void **)&x->d_step_sync, 8);
     if (e == cudaSuccess) e = cudaMemset(x->d_step_ready, 0, (size_t)cfg->max_batch * 4);
@@ -307,7 +325,7 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_start, 0, (size_t)cfg->max_docs * 8);
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_len, 0, (size_t)cfg->max_docs * 4);
     if (e == cudaSuccess) {
-      CorpusDesc d0{x->d_text[0], x->d_sa[0], x->d_keys[0], 0, 0, 0};
+      CorpusDesc d0{x->d_text[0], x->d_sa[0], x->d_keys[0], 0, 0, x->d_rec[0]};
       e = cudaMemcpy(x->d_desc, &d0, sizeof(d0), cudaMemcpyHostToDevice);
     }
     if (e == cudaSuccess) e = cudaMallocHost((void **)&x->h_n, 8);
@@ -374,6 +392,7 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.err = x->d_err;
   a.nself = x->nself;
   a.cand_cap = c.corpus_cand_cap;
+  a.rsh = x->rsh;
   return a;
 }
 
@@ -551,7 +570,7 @@ int sgd_poll(sgd_ctx *x, int wait, int64_t timeout_us, void *stream, uint64_t *g
   }
   const int back = 1 - x->front;
   const cudaError_t e = launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->d_keys[back],
-                                    x->built_n, x->gen + 1, (cudaStream_t)stream);
+                                    x->d_rec[back], x->built_n, x->gen + 1, (cudaStream_t)stream);
   if (e != cudaSuccess) return SGD_ECUDA;
   x->launches++;
   x->front = back;

@@ -119,12 +119,40 @@ __global__ void __launch_bounds__(256) linearize_kernel(const int32_t *ring, lon
 }
 
 __global__ void swap_kernel(CorpusDesc *desc, const int32_t *text, const int32_t *sa,
-                            const int4 *keys, long long n, uint64_t gen) {
+                            const int4 *keys, const int32_t *rec, long long n, uint64_t gen) {
   desc->text = text;
   desc->sa = sa;
   desc->keys = keys;
+  desc->rec = rec;
   desc->n = n;
   desc->gen = gen;
+}
+
+// The record of every suffix-array position, one warp per record: lane f
+// writes int f (RecShape: position, tokens before, tokens after the first
+// four).  The text around a suffix is contiguous, so a warp's reads fall in
+// a few sectors.
+__global__ void __launch_bounds__(256) records_kernel(const int32_t *text, const int32_t *sa,
+                                                      long long n, RecShape sh, int Z, int32_t *rec) {
+  const int lane = threadIdx.x & 31;
+  const long long nw = (long long)gridDim.x * (blockDim.x >> 5);
+  for (long long p = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); p < n; p += nw) {
+    const long long i = sa[p];
+    int32_t *r = rec + (size_t)p * sh.ri;
+    for (int f = lane; f < sh.ri; f += 32) {
+      int v = 0;
+      if (f == 0) {
+        v = (int)i;
+      } else if (f <= sh.bk) {
+        const long long q = i - f;
+        v = q >= 0 ? text[q] : KEY_END;
+      } else if (f <= sh.bk + sh.kc) {
+        const long long q = i + 4 + (f - 1 - sh.bk);
+        v = q < n ? text[q] : Z;
+      }
+      r[f] = v;
+    }
+  }
 }
 
 // The first four tokens of every suffix, in suffix-array order.  Corpus
@@ -179,8 +207,17 @@ cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs, cons
 }
 
 cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
-                        int64_t n, uint64_t gen, cudaStream_t st) {
-  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, n, gen);
+                        const int32_t *rec, int64_t n, uint64_t gen, cudaStream_t st) {
+  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, rec, n, gen);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_records(const int32_t *text, const int32_t *sa, int64_t n, RecShape shape, int Z,
+                           int32_t *rec, cudaStream_t st) {
+  if (n <= 0 || rec == nullptr) return cudaSuccess;
+  long long blocks = (n + 7) / 8;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  records_kernel<<<(int)blocks, 256, 0, st>>>(text, sa, n, shape, Z, rec);
   return cudaGetLastError();
 }
 

@@ -32,11 +32,29 @@ namespace sgd {
 
 namespace {
 
-constexpr int LCAP = 16384;    // P4 hits whose match length is cached on chip
+constexpr int LCAP = 65536;    // P4 hits whose match length is cached on chip
+// A small P4 interval is evaluated from one round trip of context: for each
+// hit, its k continuation tokens and the tokens before the pattern, fetched
+// with cp.async into the L-cache area (lengths, then ends, then contexts).
+constexpr int P4C_MAX = 512;                                   // hits
+constexpr int P4C_CTX = (LCAP - P4C_MAX - 4 * P4C_MAX) / 4;    // context ints
 constexpr int NPROBE3 = 3;     // probe warps: P4, P3, P2
 constexpr int TOP_KEYS = 32;   // staged keys of the top level of the descent
 constexpr int MID_KEYS = 1024; // staged keys of the level below it
 constexpr long long BIG_INTERVAL = 4096;  // probe hits worth waiting for the self match
+
+// barrier of the three probe warps only
+__device__ __forceinline__ void probe_sync() { asm volatile("bar.sync 1, 96;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
+}
+
+__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
+}
 
 __device__ __forceinline__ int4 load_win(const int32_t *row, int widx, int lane, int S) {
   const int p = widx * WIN + 4 * lane;
@@ -191,6 +209,8 @@ struct Corpus {
   const int32_t *X;
   const int32_t *SA;
   const int4 *K;
+  const int32_t *Rec;  // per-position records, or null
+  RecShape rs;
   long long N;
   int Lmax;
   const int4 *s_top;  // K[j * 32^Lmax]
@@ -315,30 +335,119 @@ __device__ void scan_p4(const Corpus &c, int Z, long long lo, long long hi, cons
   }
 }
 
+// Whether the P4 interval [lo, hi) is small enough for scan_p4_ctx.
+__device__ __forceinline__ bool p4_ctx_fits(long long cnt, int W) {
+  return cnt <= P4C_MAX && cnt * W <= P4C_CTX;
+}
+
+// Match lengths of a small P4 interval: the ends (SA entries) in one round
+// trip, then every hit's context in a second one, all on chip afterwards.
+// Context of hit i, W = kc + dl - 4 ints at s_ctx[i * W]: X[e+1 .. e+kc]
+// (Z past the end of the text), then X[e-4-j] for j < dl - 4.  Lengths go to
+// s_L[i] (0 without a continuation), ends to s_e[i], counts to s_lhist.
+__device__ void scan_p4_ctx(const Corpus &c, int Z, long long lo, long long hi, const int *s_tail,
+                            int n, int D, int kc, unsigned char *s_L, int *s_e, int *s_ctx,
+                            int *s_lhist, int tid, int nthr) {
+  const int cnt = (int)(hi - lo);
+  const int dl = min(D, n);
+  if (c.Rec != nullptr) {
+    // the snapshot's records hold all of it: one round trip of 16-byte copies
+    const int ri = c.rs.ri, bk = c.rs.bk, q4 = ri >> 2;
+    for (int f = tid; f < cnt * q4; f += nthr) {
+      const int i = f / q4, j = f - i * q4;
+      cp_async16(&s_ctx[i * ri + 4 * j], c.Rec + (size_t)(lo + i) * ri + 4 * j);
+    }
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+    probe_sync();
+    for (int i = tid; i < cnt; i += nthr) {
+      const int *x = s_ctx + (size_t)i * ri;
+      const long long e = (long long)x[0] + 3;
+      s_e[i] = (int)e;
+      int L = 0;
+      if (x[1 + bk] != Z) {
+        const long long lim = min((long long)dl, e + 1);
+        L = 4;
+        while (L < lim && x[1 + L - 4] == s_tail[L]) ++L;
+        atomicAdd(&s_lhist[L], 1);
+      }
+      s_L[i] = (unsigned char)L;
+    }
+    return;
+  }
+  const int W = kc + dl - 4;
+  for (int i = tid; i < cnt; i += nthr) s_e[i] = __ldg(c.SA + lo + i) + 3;
+  probe_sync();
+  for (int f = tid; f < cnt * W; f += nthr) {
+    const int i = f / W, j = f - i * W;
+    const long long e = s_e[i];
+    const long long pos = j < kc ? e + 1 + j : e - 4 - (j - kc);
+    if (pos >= 0 && pos < c.N) cp_async4(&s_ctx[f], c.X + pos);
+    else s_ctx[f] = Z;  // past the end (continuation) or before the start (never compared)
+  }
+  asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+  probe_sync();
+  for (int i = tid; i < cnt; i += nthr) {
+    const int *x = s_ctx + (size_t)i * W;
+    const long long e = s_e[i];
+    int L = 0;
+    if (x[0] != Z) {
+      const long long lim = min((long long)dl, e + 1);
+      L = 4;
+      while (L < lim && x[kc + L - 4] == s_tail[L]) ++L;
+      atomicAdd(&s_lhist[L], 1);
+    }
+    s_L[i] = (unsigned char)L;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // corpus: the P3 / P2 levels (key array only)
 
 // A P3 (lvl 3) or P2 (lvl 2) hit is valid when the suffix has a token after
-// the pattern that is not a sentinel; its end is SA[p] + lvl - 1.
-__device__ __forceinline__ bool short_valid(const int4 &k, int lvl, int Z) {
-  const int t = lvl == 2 ? k.z : k.w;
-  return t != Z && t != KEY_END;
+// the pattern that is not a sentinel (nor the end of the text); its end is
+// SA[p] + lvl - 1.
+// The token after the pattern of a P3 / P2 hit, from the key array.
+__device__ __forceinline__ int short_token(const Corpus &c, long long p, int lvl) {
+  const int *k = reinterpret_cast<const int *>(c.K + p);
+  return __ldg(k + (lvl == 2 ? 2 : 3));
 }
 
-// Whether hit p of the chosen level is one of the ends of length Mc.
-__device__ __forceinline__ bool selects(const Corpus &c, int Z, long long p, long long lo, int lvl,
-                                        int Mc, const int *s_tail, int n, int D,
-                                        const unsigned char *s_L, long long &e) {
-  if (lvl == 4) {
-    if (p - lo < LCAP) {
-      e = (long long)__ldg(c.SA + p) + 3;
-      return s_L[p - lo] == Mc;
+// Hits p0 + u * stride (u < SB) of the chosen level: q[u] whether the hit is
+// an end of length Mc, e[u] its end.  All loads of the batch are issued
+// before any is used (one round trip per batch).
+constexpr int SB = 8;
+__device__ __forceinline__ void select_batch(const Corpus &c, int Z, long long p0, int stride,
+                                             long long lo, long long hi, int lvl, int Mc,
+                                             const int *s_tail, int n, int D,
+                                             const unsigned char *s_L, int *e, bool *q) {
+  if (lvl != 4) {
+    int t[SB];
+#pragma unroll
+    for (int u = 0; u < SB; ++u) {
+      const long long p = p0 + (long long)u * stride;
+      const bool in = p < hi;
+      t[u] = in ? short_token(c, p, lvl) : Z;
+      e[u] = in ? __ldg(c.SA + p) + lvl - 1 : 0;
     }
-    return p4_entry(c, Z, p, s_tail, n, D, e) == Mc;
+#pragma unroll
+    for (int u = 0; u < SB; ++u) q[u] = t[u] != Z && t[u] != KEY_END;
+    return;
   }
-  const int4 k = __ldg(c.K + p);
-  e = (long long)__ldg(c.SA + p) + lvl - 1;
-  return short_valid(k, lvl, Z);
+#pragma unroll
+  for (int u = 0; u < SB; ++u) {
+    const long long p = p0 + (long long)u * stride;
+    q[u] = p < hi && p - lo < LCAP && s_L[p - lo] == Mc;
+    e[u] = q[u] ? __ldg(c.SA + p) + 3 : 0;
+  }
+#pragma unroll
+  for (int u = 0; u < SB; ++u) {
+    const long long p = p0 + (long long)u * stride;
+    if (p < hi && p - lo >= LCAP) {  // beyond the length cache: evaluate again
+      long long ee;
+      q[u] = p4_entry(c, Z, p, s_tail, n, D, ee) == Mc;
+      e[u] = (int)ee;
+    }
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -374,8 +483,6 @@ __device__ void pick_bin(const int *hist, int need, int lane, int *s_sel, int *s
   }
 }
 
-// barrier of the three probe warps only
-__device__ __forceinline__ void probe_sync() { asm volatile("bar.sync 1, 96;" ::: "memory"); }
 
 // draft length bound: min(k, floor(factor * M) + offset, S - n - 1) [, D - M]
 __device__ __forceinline__ int draft_cap(const ProposeArgs &a, int M, int n) {
@@ -385,16 +492,6 @@ __device__ __forceinline__ int draft_cap(const ProposeArgs &a, int M, int n) {
   c = min(c, room);
   if (a.depth_sum_cap) c = min(c, (long long)a.D - M);
   return c < 0 ? 0 : (int)c;
-}
-
-__device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(sa), "l"(gmem) : "memory");
-}
-
-__device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 
 __device__ int update_row_warp(int32_t *row, int n, const int32_t *sp, int T, int S, int V, int lane,
@@ -499,11 +596,12 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
 
   // ---- phase 0: warp 0 updates the row; the others fetch the snapshot
   // descriptor and stage the top two levels of its key array ----
-  Corpus cp{nullptr, nullptr, nullptr, 0, 0, s_top, s_mid};
+  Corpus cp{nullptr, nullptr, nullptr, nullptr, a.rsh, 0, 0, s_top, s_mid};
   if (a.desc != nullptr) {
     cp.X = a.desc->text;
     cp.SA = a.desc->sa;
     cp.K = a.desc->keys;
+    cp.Rec = a.desc->rec;
     cp.N = a.desc->n;
     cp.Lmax = cp.N >= 2 ? top_level(cp.N) : 0;
   }
@@ -640,6 +738,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     };
     int pms = self_len(false);
     int Mc = 0, lvl = 0, Q = 0;
+    bool p4ctx = false;   // the P4 interval was evaluated on chip (scan_p4_ctx)
+    bool oncand = false;  // a short level's ends are all in s_big already
+    int *s_e4 = reinterpret_cast<int *>(s_L + P4C_MAX);  // small-P4 ends, then contexts
+    int *s_ctx = s_e4 + P4C_MAX;
     long long lo = 0, hi = 0;
     if (pms < dl) {
       bool decided = false;
@@ -649,7 +751,12 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       if (D >= 4 && n >= 4 && s_bound[1] > s_bound[0] && pms < dl) {
         for (int i = ptid; i <= MAX_D; i += pthr) s_lhist[i] = 0;
         probe_sync();
-        scan_p4(cp, Z, s_bound[0], s_bound[1], s_tail, n, D, s_L, s_lhist, ptid, pthr);
+        p4ctx = p4_ctx_fits(s_bound[1] - s_bound[0], cp.Rec ? cp.rs.ri : k + dl - 4);
+        if (p4ctx)
+          scan_p4_ctx(cp, Z, s_bound[0], s_bound[1], s_tail, n, D, k, s_L, s_e4, s_ctx, s_lhist,
+                      ptid, pthr);
+        else
+          scan_p4(cp, Z, s_bound[0], s_bound[1], s_tail, n, D, s_L, s_lhist, ptid, pthr);
         probe_sync();
         int lbest = 0;
         for (int L = 4 + lane; L <= dl; L += 32)
@@ -676,19 +783,28 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         probe_sync();  // s_q from an earlier level has been read
         if (ptid == 0) s_q = 0;
         probe_sync();
-        int cnt = 0;
-        for (long long p = l0 + ptid; p < h0; p += 4LL * pthr) {
-          int4 kk[4];
+        // one pass: count the valid hits and keep their ends on chip (while
+        // they fit); a warp takes its slots with one shared atomic per batch
+        const unsigned lt = (1u << lane) - 1u;
+        for (long long p0 = l0 + 32 * pw; p0 < h0; p0 += (long long)SB * pthr) {
+          int t[SB], eb[SB];
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const long long q = p + (long long)u * pthr;
-            kk[u] = q < h0 ? __ldg(cp.K + q) : make_int4(Z, Z, Z, Z);
+          for (int u = 0; u < SB; ++u) {
+            const long long q = p0 + lane + (long long)u * pthr;
+            t[u] = q < h0 ? short_token(cp, q, lv) : Z;
+            eb[u] = q < h0 ? __ldg(cp.SA + q) + lv - 1 : 0;
           }
 #pragma unroll
-          for (int u = 0; u < 4; ++u) cnt += short_valid(kk[u], lv, Z);
+          for (int u = 0; u < SB; ++u) {
+            const bool v = t[u] != Z && t[u] != KEY_END;
+            const unsigned m = __ballot_sync(FULL, v);
+            int base = 0;
+            if (lane == 0 && m) base = atomicAdd(&s_q, __popc(m));
+            base = __shfl_sync(FULL, base, 0);
+            const int slot = base + __popc(m & lt);
+            if (v && slot < a.cand_cap) s_big[slot] = eb[u];
+          }
         }
-        cnt = (int)__reduce_add_sync(FULL, (unsigned)cnt);
-        if (lane == 0 && cnt) atomicAdd(&s_q, cnt);
         probe_sync();
         if (s_q > 0) {
           Mc = lv;
@@ -696,68 +812,118 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
           lo = l0;
           hi = h0;
           Q = s_q;
+          oncand = Q <= a.cand_cap;
           decided = true;
         }
       }
     }
     if (Mc > 0 && pms < 0 && Q > R) pms = self_len(true);
-    if (Mc > 0 && Mc > pms) {
-      // The R largest ends among the Q of length Mc.  O_0 is a set (the vote
-      // does not depend on its order), so nothing is sorted.  With at most R
-      // of them, all are kept and their continuations requested right away.
+    if (Mc > 0 && Mc > pms && lvl == 4 && p4ctx) {
+      // A small P4 interval: ends, lengths and continuations are on chip.
+      // The R largest ends of length Mc (a radix select over the ends when
+      // there are more), their continuations copied for the vote.
       const int capc = draft_cap(a, Mc, n);
-      const bool pf = Q <= R;
-      int *cand = s_big;
+      const int cnt = (int)(hi - lo);
+      const int W = cp.Rec ? cp.rs.ri : k + dl - 4;      // context stride
+      const int co = cp.Rec ? 1 + cp.rs.bk : 0;          // where the continuation starts
       probe_sync();
       if (ptid == 0) s_q = 0;
-      unsigned prefix = 0;
-      if (Q > a.cand_cap) {
-        // more than fit on chip: radix-select the R-th largest end over the
-        // interval, byte by byte; the R ends at or above it are collected below
-        unsigned mask = 0;
+      unsigned thr = 0;
+      if (Q > R) {
+        unsigned mk = 0;
         int need = R;
         for (int shift = 24; shift >= 0; shift -= 8) {
           for (int i = ptid; i < 256; i += pthr) s_hist[i] = 0;
           probe_sync();
-          for (long long p0 = lo + ptid; p0 < hi; p0 += 4LL * pthr) {
-            long long e[4];
-            bool q[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const long long p = p0 + (long long)u * pthr;
-              q[u] = p < hi && selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-              if (q[u] && ((unsigned)e[u] & mask) == prefix)
-                atomicAdd(&s_hist[((unsigned)e[u] >> shift) & 255u], 1);
+          for (int i = ptid; i < cnt; i += pthr) {
+            const unsigned e = (unsigned)s_e4[i];
+            if (s_L[i] == Mc && (e & mk) == thr) atomicAdd(&s_hist[(e >> shift) & 255u], 1);
           }
           probe_sync();
           if (pw == 0) pick_bin(s_hist, need, lane, &s_sel, &s_need);
           probe_sync();
-          prefix |= (unsigned)s_sel << shift;
-          mask |= 255u << shift;
+          thr |= (unsigned)s_sel << shift;
+          mk |= 255u << shift;
           need = s_need;
         }
       }
       probe_sync();
-      for (long long p = lo + ptid; p < hi; p += pthr) {
-        long long e;
-        if (selects(cp, Z, p, lo, lvl, Mc, s_tail, n, D, s_L, e) && (unsigned)e >= prefix) {
+      for (int i = ptid; i < cnt; i += pthr) {
+        const unsigned e = (unsigned)s_e4[i];
+        if (s_L[i] == Mc && e >= thr) {
           const int slot = atomicAdd(&s_q, 1);
-          if (pf) {
-            s_occc[slot] = (int)e;
-            for (int d = 0; d < capc; ++d) {
-              const long long pos = e + 1 + d;
-              if (pos < cp.N) cp_async4(&s_big[slot * capc + d], cp.X + pos);
-              else s_big[slot * capc + d] = Z;
-            }
-          } else if (slot < a.cand_cap) {
-            cand[slot] = (int)e;
-          }
+          s_occc[slot] = (int)e;
+          const int *x = s_ctx + (size_t)i * W + co;
+          for (int d = 0; d < capc; ++d) s_big[slot * capc + d] = x[d];
         }
       }
-      asm volatile("cp.async.commit_group;" ::: "memory");
+      if (ptid == 0) { s_Mc = Mc; s_c0c = min(Q, R); s_cpf = 1; }
+    } else if (Mc > 0 && Mc > pms) {
+      // The R largest ends among the Q of length Mc.  O_0 is a set (the vote
+      // does not depend on its order), so nothing is sorted.  With at most R
+      // of them, all are kept and their continuations requested right away.
+      const int capc = draft_cap(a, Mc, n);
+      const bool pf = Q <= R && !oncand;
+      int *cand = s_big;
+      probe_sync();
+      if (!oncand) {
+        if (ptid == 0) s_q = 0;
+        unsigned prefix = 0;
+        if (Q > a.cand_cap) {
+          // more than fit on chip: radix-select the R-th largest end over the
+          // interval, byte by byte; the R ends at or above it are collected below
+          unsigned mask = 0;
+          int need = R;
+          for (int shift = 24; shift >= 0; shift -= 8) {
+            for (int i = ptid; i < 256; i += pthr) s_hist[i] = 0;
+            probe_sync();
+            for (long long p0 = lo + ptid; p0 < hi; p0 += (long long)SB * pthr) {
+              int e[SB];
+              bool q[SB];
+              select_batch(cp, Z, p0, pthr, lo, hi, lvl, Mc, s_tail, n, D, s_L, e, q);
+  #pragma unroll
+              for (int u = 0; u < SB; ++u)
+                if (q[u] && ((unsigned)e[u] & mask) == prefix)
+                  atomicAdd(&s_hist[((unsigned)e[u] >> shift) & 255u], 1);
+            }
+            probe_sync();
+            if (pw == 0) pick_bin(s_hist, need, lane, &s_sel, &s_need);
+            probe_sync();
+            prefix |= (unsigned)s_sel << shift;
+            mask |= 255u << shift;
+            need = s_need;
+          }
+        }
+        probe_sync();
+        const unsigned lt = (1u << lane) - 1u;
+        for (long long p0 = lo + 32 * pw; p0 < hi; p0 += (long long)SB * pthr) {
+          int eb[SB];
+          bool qb[SB];
+          select_batch(cp, Z, p0 + lane, pthr, lo, hi, lvl, Mc, s_tail, n, D, s_L, eb, qb);
+  #pragma unroll
+          for (int u = 0; u < SB; ++u) {
+            const bool v = qb[u] && (unsigned)eb[u] >= prefix;
+            const unsigned m = __ballot_sync(FULL, v);
+            int base = 0;
+            if (lane == 0 && m) base = atomicAdd(&s_q, __popc(m));
+            base = __shfl_sync(FULL, base, 0);
+            if (!v) continue;
+            const int e = eb[u];
+            const int slot = base + __popc(m & lt);
+            if (pf) {
+              s_occc[slot] = e;
+              for (int d = 0; d < capc; ++d) {
+                const long long pos = (long long)e + 1 + d;
+                if (pos < cp.N) cp_async4(&s_big[slot * capc + d], cp.X + pos);
+                else s_big[slot * capc + d] = Z;
+              }
+            } else if (slot < a.cand_cap) {
+              cand[slot] = e;
+            }
+          }
+        }
+        asm volatile("cp.async.commit_group;" ::: "memory");
+      }
       probe_sync();
       const int Qc = min(s_q, a.cand_cap);
       int c0c;

@@ -25,8 +25,22 @@ struct CorpusDesc {
   const int4 *keys;     // keys[p] = X[sa[p] .. sa[p]+3], KEY_END past the text
   int64_t n;
   uint64_t gen;
-  int64_t pad;
+  const int32_t *rec;   // per-position records (RecShape), or null
 };
+
+// Record of suffix-array position p (i = sa[p]), ri ints: [0] i; [1, 1+bk)
+// the tokens before the suffix, X[i-1-j] (KEY_END before the text); then kc
+// tokens after its first four, X[i+4+j] (Z past the end); zero padding.
+struct RecShape {
+  int ri, bk, kc;
+};
+inline RecShape rec_shape(int D, int k) {
+  RecShape r;
+  r.bk = D > 4 ? D - 4 : 0;
+  r.kc = k;
+  r.ri = (1 + r.bk + r.kc + 3) & ~3;
+  return r;
+}
 constexpr int KEY_END = (int)0x80000000;  // below every id: the text ran out
 
 // Ring bookkeeping, device resident.  The doc FIFO lives in two arrays of
@@ -58,6 +72,7 @@ struct ProposeArgs {
   uint32_t *err;
   int nself;               // self-scan warps per row
   int cand_cap;            // corpus candidate buffer (power of two >= R)
+  RecShape rsh;            // layout of the snapshot's records (desc->rec)
   // fused step: ing_m > 0 adds CTA 0, which appends ing_m docs to the ring
   // once their rows are updated (the row CTAs are 1..B)
   int ing_m;
@@ -95,7 +110,10 @@ cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S,
 cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs,
                              const int64_t *doc_start, int max_docs, int32_t *out,
                              cudaStream_t st, int *launches);
+cudaError_t launch_records(const int32_t *text, const int32_t *sa, int64_t n, RecShape shape, int Z,
+                           int32_t *rec, cudaStream_t st);
 cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
+                        const int32_t *rec,
                         int64_t n, uint64_t gen, cudaStream_t st);
 // keys[p] = text[sa[p] .. sa[p]+3] (KEY_END past n), on `st`
 cudaError_t launch_suffix_keys(const int32_t *text, const int32_t *sa, int64_t n, int4 *keys,

@@ -55,7 +55,8 @@ class SuffixDrafter:
                  max_spec_factor: Rational = 1.0, max_spec_offset: int = 0,
                  min_token_prob: Rational = 0.1, depth_sum_cap: bool = False,
                  corpus_capacity: int = 0, max_docs: int = 65536, max_ingest_docs: int = 4096,
-                 corpus_cand_cap: int = 2048, self_warps: int = 0, device: int = 0):
+                 corpus_cand_cap: int = 2048, self_warps: int = 0, corpus_records: int = 1,
+                 device: int = 0):
         self._lib = L.load()
         cfg = L.SgdConfig()
         self._check(self._lib.sgd_config_default(ctypes.byref(cfg)), "sgd_config_default")
@@ -75,6 +76,7 @@ class SuffixDrafter:
         cfg.max_ingest_docs = max_ingest_docs
         cfg.corpus_cand_cap = corpus_cand_cap
         cfg.self_warps = self_warps
+        cfg.corpus_records = corpus_records
         self.cfg = cfg
         self.device = torch.device("cuda", device)
         torch.cuda.init()

@@ -154,8 +154,9 @@ CORPUS_GRID = [
 ]
 
 
+@pytest.mark.parametrize("records", [1, 0], ids=["records", "text"])
 @pytest.mark.parametrize("grid", CORPUS_GRID, ids=lambda g: "V%d_D%d_R%d_cap%d" % (g[0], g[1], g[2], g[4]))
-def test_fuzz_corpus(grid):
+def test_fuzz_corpus(grid, records):
     SuffixDrafter, W, O, H = _mods()
     V, D, R, k, cc, nd, dl = grid
     rng = np.random.default_rng(sum(grid))
@@ -179,7 +180,7 @@ def test_fuzz_corpus(grid):
         n[b] = nb
     dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=D,
                        max_occurrences=R, corpus_capacity=max(1024, len(X)), corpus_cand_cap=cc,
-                       max_spec_factor=(2, 1), min_token_prob=(1, 8))
+                       max_spec_factor=(2, 1), min_token_prob=(1, 8), corpus_records=records)
     _ingest_text(dr, X, V, S)
     dr.build_sa(torch.cuda.Stream())
     assert dr.poll(wait=True)[0] == 1
@@ -223,6 +224,41 @@ def test_large_match_set_multi_pass_selection():
         H.compare(out, orc, ctx="cand_cap %d R %d" % (cc, R))
         assert (orc.match_info[:, 1] == 2).all()
         dr.close()
+
+
+@pytest.mark.parametrize("records", [1, 0], ids=["records", "text"])
+@pytest.mark.parametrize("R", [16, 128])
+def test_small_p4_interval_long_matches(R, records):
+    """A 4-token pattern with ~100 hits whose matches run back 10 tokens: the
+    small-interval path evaluates them from one round of on-chip context and
+    selects the R most recent (on-chip radix select when R < hits)."""
+    SuffixDrafter, W, O, H = _mods()
+    rng = np.random.default_rng(77 + R)
+    V, S = 1000, 128
+    A = rng.integers(0, V, size=30).tolist()
+    X = []
+    for i in range(110):
+        L = int(rng.integers(10, 31))
+        X += rng.integers(0, V, size=5).tolist() + A[:L] + rng.integers(0, V, size=3).tolist() + [V]
+    X += A[:10] + [V]                       # a hit whose continuation is the sentinel
+    X = np.asarray(X, dtype=np.int32)
+    tok = np.full((3, S), -1, dtype=np.int32)
+    tok[0, :12] = [3, 4] + A[:10]            # M_c = 10 (the prefix breaks the match)
+    tok[1, :10] = A[:10]                     # match bounded by the row start
+    tok[2, :26] = [5] + A[:25]               # long match, capped by D
+    n = np.array([12, 10, 26], dtype=np.int32)
+    dr = SuffixDrafter(max_batch=3, seq_capacity=S, vocab_size=V, k=8, max_tree_depth=24,
+                       max_occurrences=R, corpus_capacity=len(X), min_token_prob=(1, 20),
+                       max_docs=4096, corpus_records=records)
+    _ingest_text(dr, X, V, S)
+    dr.build_sa(torch.cuda.Stream())
+    assert dr.poll(wait=True)[0] == 1
+    out = dr.propose(_dev(tok), _dev(n))
+    p = O.Params(S=S, V=V, k=8, D=24, R=R, min_prob=(1, 20))
+    orc = O.propose(p, tok, n, X=X)
+    H.compare(out, orc, ctx="R %d" % R)
+    assert (orc.match_info[:, 1] == 2).all()
+    dr.close()
 
 
 def test_update_and_error_flags():
