@@ -582,14 +582,16 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
   const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
   int32_t *row = a.tok + (size_t)b * S;
-  const int big = max(a.cand_cap, R * k);
+  const int big = max(a.cand_cap, R * ((k + 3) & ~3));
   int *s_tail = dsm;                   // MAX_D
   int *s_wlist = s_tail + MAX_D;       // nself * R
   int *s_occ = s_wlist + a.nself * R;  // R
   int *s_run = s_occ + R;              // R
   int *s_occc = s_run + R;             // R (corpus ends)
-  int *s_big = s_occc + R;             // max(cand_cap, R * k)
-  const int koff = (MAX_D + a.nself * R + 3 * R + big + 3) & ~3;
+  // s_big and everything after it start on 16-byte boundaries (int4 access)
+  const int boff = (MAX_D + a.nself * R + 3 * R + 3) & ~3;
+  int *s_big = dsm + boff;             // max(cand_cap, R * roundup4(k))
+  const int koff = (boff + big + 3) & ~3;
   int4 *s_top = reinterpret_cast<int4 *>(dsm + koff);                  // TOP_KEYS
   int4 *s_mid = s_top + TOP_KEYS;                                      // MID_KEYS
   unsigned char *s_L = reinterpret_cast<unsigned char *>(s_mid + MID_KEYS);  // LCAP
@@ -822,7 +824,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       // A small P4 interval: ends, lengths and continuations are on chip.
       // The R largest ends of length Mc (a radix select over the ends when
       // there are more), their continuations copied for the vote.
-      const int capc = draft_cap(a, Mc, n);
+      const int capc = draft_cap(a, Mc, n), capp = (capc + 3) & ~3;  // row stride 16-B aligned
       const int cnt = (int)(hi - lo);
       const int W = cp.Rec ? cp.rs.ri : k + dl - 4;      // context stride
       const int co = cp.Rec ? 1 + cp.rs.bk : 0;          // where the continuation starts
@@ -854,7 +856,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
           const int slot = atomicAdd(&s_q, 1);
           s_occc[slot] = (int)e;
           const int *x = s_ctx + (size_t)i * W + co;
-          for (int d = 0; d < capc; ++d) s_big[slot * capc + d] = x[d];
+          for (int d = 0; d < capc; ++d) s_big[slot * capp + d] = x[d];
         }
       }
       if (ptid == 0) { s_Mc = Mc; s_c0c = min(Q, R); s_cpf = 1; }
@@ -862,7 +864,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       // The R largest ends among the Q of length Mc.  O_0 is a set (the vote
       // does not depend on its order), so nothing is sorted.  With at most R
       // of them, all are kept and their continuations requested right away.
-      const int capc = draft_cap(a, Mc, n);
+      const int capc = draft_cap(a, Mc, n), capp = (capc + 3) & ~3;
       const bool pf = Q <= R && !oncand;
       int *cand = s_big;
       probe_sync();
@@ -914,8 +916,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
               s_occc[slot] = e;
               for (int d = 0; d < capc; ++d) {
                 const long long pos = (long long)e + 1 + d;
-                if (pos < cp.N) cp_async4(&s_big[slot * capc + d], cp.X + pos);
-                else s_big[slot * capc + d] = Z;
+                if (pos < cp.N) cp_async4(&s_big[slot * capp + d], cp.X + pos);
+                else s_big[slot * capp + d] = Z;
               }
             } else if (slot < a.cand_cap) {
               cand[slot] = e;
@@ -969,7 +971,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int cap = M > 0 ? draft_cap(a, M, n) : 0;
   const int c0 = src == 2 ? s_c0c : s_cs;
   const int *occ = src == 2 ? s_occc : s_occ;
-  int *cont = s_big;
+  int *cont = s_big;                  // cont[o * capp + d]: rows 16-byte aligned
+  const int capp = (cap + 3) & ~3;
   if (cap > 0 && c0 > 0) {
     const int tot = (src == 2 && s_cpf) ? 0 : c0 * cap;  // prefetched by the probe warps
     for (int idx = tid; idx < tot; idx += nthr) {
@@ -978,7 +981,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       int v;
       if (src == 1) v = pos <= n - 1 ? row[pos] : 0;
       else v = pos < cp.N ? __ldg(cp.X + pos) : Z;
-      cont[idx] = v;
+      cont[o * capp + d] = v;
     }
     __syncthreads();
     for (int o = tid; o < c0; o += nthr) {
@@ -987,7 +990,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         r = min(cap, n - 1 - occ[o]);
       } else {
         r = 0;
-        while (r < cap && cont[o * cap + r] != Z) ++r;
+        while (r < cap && cont[o * capp + r] != Z) ++r;
       }
       s_run[o] = r;
     }
@@ -1006,6 +1009,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // depths is decided in one warp scan.  Where the majority fails, all
   // participants' tokens are counted (most frequent wins, ties to the
   // smallest id) and a new reference is taken among the winners.
+  // Probabilities are quotients c / c0 of integers with c <= 64 * c0 and
+  // c0 <= 128: both are exact floats, and a correctly rounded single
+  // division gives the same float as rounding the double quotient (checked
+  // over that whole range by the test suite), so no double arithmetic.
   int len = 0;
   long long sum = 0;
   if (cap > 0) {
@@ -1037,8 +1044,21 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         if (!alive[s]) continue;
         const int o = lane + 32 * s;
         const int r = min(s_run[o], cap);
-        int dd = d;
-        while (dd < r && cont[o * cap + dd] == cont[ref * cap + dd]) ++dd;
+        // first depth in [d, r) where o disagrees with the reference, else r;
+        // four depths per 16-byte load of each row
+        const int4 *ro = reinterpret_cast<const int4 *>(cont + o * capp);
+        const int4 *rr = reinterpret_cast<const int4 *>(cont + ref * capp);
+        int dd = r;
+        for (int q = d >> 2; (q << 2) < r; ++q) {
+          const int4 x = ro[q], y = rr[q];
+          const int b = q << 2;
+          int f = -1;
+          if (b + 3 >= d && b + 3 < r && x.w != y.w) f = b + 3;
+          if (b + 2 >= d && b + 2 < r && x.z != y.z) f = b + 2;
+          if (b + 1 >= d && b + 1 < r && x.y != y.y) f = b + 1;
+          if (b >= d && b < r && x.x != y.x) f = b;
+          if (f >= 0) { dd = f; break; }
+        }
         diff[s] = dd;
         atomicAdd(&H[dd], 1);
         if (dd == r && r < cap) atomicAdd(&HR[dd], 1);
@@ -1066,13 +1086,13 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       // emit depths [d, F): the reference's tokens
       long long part_sum = 0;
       if (x1 < F) {
-        dr[x1] = cont[ref * cap + x1];
-        if (pr) pr[x1] = (float)((double)c1 / (double)c0);
+        dr[x1] = cont[ref * capp + x1];
+        if (pr) pr[x1] = (float)c1 / (float)c0;
         part_sum += c1;
       }
       if (x2 < F) {
-        dr[x2] = cont[ref * cap + x2];
-        if (pr) pr[x2] = (float)((double)c2 / (double)c0);
+        dr[x2] = cont[ref * capp + x2];
+        if (pr) pr[x2] = (float)c2 / (float)c0;
         part_sum += c2;
       }
       for (int off = 16; off > 0; off >>= 1) part_sum += __shfl_xor_sync(FULL, part_sum, off);
@@ -1099,7 +1119,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       int base = 0;
 #pragma unroll
       for (int s = 0; s < 4; ++s) {
-        val[s] = part[s] ? cont[(lane + 32 * s) * cap + d] : 0;
+        val[s] = part[s] ? cont[(lane + 32 * s) * capp + d] : 0;
         if (part[s]) s_vv[base + __popc(pm[s] & lt)] = val[s];
         base += __popc(pm[s]);
       }
@@ -1134,7 +1154,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       if ((long long)cnt * a.pD < a.pN * (long long)c0) break;
       if (lane == 0) {
         dr[d] = tau;
-        if (pr) pr[d] = (float)((double)cnt / (double)c0);
+        if (pr) pr[d] = (float)cnt / (float)c0;
       }
       sum += cnt;
       ++len;
@@ -1149,7 +1169,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   }
   if (lane == 0) {
     a.num_valid[b] = len;
-    if (a.score) a.score[b] = c0 > 0 ? (float)((double)sum / (double)c0) : 0.f;
+    if (a.score) a.score[b] = c0 > 0 ? (float)sum / (float)c0 : 0.f;
     if (a.match_info) { a.match_info[2 * b] = M; a.match_info[2 * b + 1] = src; }
   }
 }
@@ -1169,8 +1189,9 @@ __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a
 }  // namespace
 
 size_t propose_smem_bytes(int nself, int R, int k, int cand_cap) {
-  const size_t big = (size_t)max(cand_cap, R * k);
-  const size_t ints = ((size_t)MAX_D + (size_t)nself * R + 3 * (size_t)R + big + 3) & ~(size_t)3;
+  const size_t big = (size_t)max(cand_cap, R * ((k + 3) & ~3));
+  const size_t boff = ((size_t)MAX_D + (size_t)nself * R + 3 * (size_t)R + 3) & ~(size_t)3;
+  const size_t ints = (boff + big + 3) & ~(size_t)3;
   const size_t bytes = sizeof(int) * ints + sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP;
   return bytes > sizeof(SmallIngestSmem) ? bytes : sizeof(SmallIngestSmem);
 }
