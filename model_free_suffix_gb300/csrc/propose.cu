@@ -32,7 +32,7 @@ namespace sgd {
 
 namespace {
 
-constexpr int LCAP = 65536;    // P4 hits whose match length is cached on chip
+constexpr int LCAP = 40960;    // P4 hits whose match length is cached on chip
 // A small P4 interval is evaluated from one round trip of context: for each
 // hit, its k continuation tokens and the tokens before the pattern, fetched
 // with cp.async into the L-cache area (lengths, then ends, then contexts).
@@ -54,12 +54,6 @@ __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
 __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
-}
-
-__device__ __forceinline__ int4 load_win(const int32_t *row, int widx, int lane, int S) {
-  const int p = widx * WIN + 4 * lane;
-  if (widx < 0 || p >= S) return make_int4(0, 0, 0, 0);
-  return *reinterpret_cast<const int4 *>(row + p);
 }
 
 // value of component `vc`/`vp` held by lane `src` of the current window, or
@@ -140,31 +134,50 @@ __device__ __forceinline__ void self_window(int wi, const int4 &cur, const int4 
 }
 
 // The windows of warp w: [wlo, whi], scanned from the top down (most recent
-// first).  The first five are loaded before the tail is known (their loads
-// overlap the tail's), the rest five ahead of use.
+// first).  They stream through a per-warp ring of SR 512-byte slots in shared
+// memory, filled with cp.async: each lane copies (and later reads) only its
+// own 16 bytes of every window, so the ring needs no synchronisation beyond
+// the lane's own cp.async groups.  Window s of the sequence (whi - s; the
+// window below wlo is fetched too, as the last window's predecessor) uses
+// slot s % SR; SPF windows are in flight while one is scanned.
+constexpr int SPF = 8;            // windows in flight per self warp
+constexpr int SR = SPF + 2;       // ring slots: the window scanned, its predecessor, SPF ahead
+
 struct SelfScan {
   int wlo, whi;
-  int4 b0, b1, b2, b3, b4;
+  int4 *ring;  // this warp's SR slots; lane l owns ring[slot * 32 + l]
 };
 
-__device__ __forceinline__ void self_prefetch(const int32_t *row, int n, int S, int w, int nself,
-                                              int lane, SelfScan &sc) {
+// Copy window widx (zeros outside [0, S)) into ring slot `slot`, one group.
+__device__ __forceinline__ void self_fetch(const int32_t *row, int widx, int lane, int S, int4 *ring,
+                                           int slot) {
+  const int p = widx * WIN + 4 * lane;
+  const bool in = widx >= 0 && p < S;
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(ring + slot * 32 + lane);
+  const int32_t *src = in ? row + p : row;
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n\tcp.async.commit_group;" ::"r"(sa),
+               "l"(src), "r"(in ? 16 : 0)
+               : "memory");
+}
+
+// Returns whether the warp has windows (and so committed SPF + 1 groups).
+__device__ __forceinline__ bool self_prefetch(const int32_t *row, int n, int S, int w, int nself,
+                                              int lane, int4 *ring, SelfScan &sc) {
   const int J = n - 1;
   sc.wlo = 0;
   sc.whi = -1;
-  const int4 z = make_int4(0, 0, 0, 0);
-  sc.b0 = sc.b1 = sc.b2 = sc.b3 = sc.b4 = z;
-  if (J <= 0) return;
+  sc.ring = ring;
+  if (J <= 0) return false;
   const int nwin = (J + WIN - 1) / WIN;
   const int per = (nwin + nself - 1) / nself;
   sc.wlo = w * per;
   sc.whi = min(nwin, sc.wlo + per) - 1;
-  if (sc.whi < sc.wlo) return;
-  sc.b0 = load_win(row, sc.whi, lane, S);
-  sc.b1 = load_win(row, sc.whi - 1, lane, S);
-  if (sc.whi - 2 >= sc.wlo - 1) sc.b2 = load_win(row, sc.whi - 2, lane, S);
-  if (sc.whi - 3 >= sc.wlo - 1) sc.b3 = load_win(row, sc.whi - 3, lane, S);
-  if (sc.whi - 4 >= sc.wlo - 1) sc.b4 = load_win(row, sc.whi - 4, lane, S);
+  if (sc.whi < sc.wlo) return false;
+  // windows 0 .. SPF of the sequence (the last of them may lie below wlo - 1:
+  // those slots are never read)
+#pragma unroll
+  for (int q = 0; q <= SPF; ++q) self_fetch(row, sc.whi - q, lane, S, ring, q);
+  return true;
 }
 
 __device__ void self_process(const int32_t *row, int n, int S, int D, int R, const int *s_tail,
@@ -174,13 +187,15 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
   if (sc.whi < sc.wlo) return;
   const int J = n - 1;
   const int t0 = s_tail[0];
-  const int4 z = make_int4(0, 0, 0, 0);
-  for (int wi = sc.whi; wi >= sc.wlo; --wi) {
-    const int nx = wi - 5;
-    const int4 nb = nx >= sc.wlo - 1 ? load_win(row, nx, lane, S) : z;
-    self_window(wi, sc.b0, sc.b1, lane, J, D, s_tail, t0, R, list, Mw, cnt);
-    sc.b0 = sc.b1; sc.b1 = sc.b2; sc.b2 = sc.b3; sc.b3 = sc.b4; sc.b4 = nb;
+  for (int wi = sc.whi, q = 0; wi >= sc.wlo; --wi, ++q) {
+    // keep SPF windows in flight; then windows q and q + 1 must have landed
+    self_fetch(row, wi - SPF - 1, lane, S, sc.ring, (q + SPF + 1) % SR);
+    asm volatile("cp.async.wait_group %0;" ::"n"(SPF) : "memory");
+    const int4 cur = sc.ring[(q % SR) * 32 + lane];
+    const int4 prv = sc.ring[((q + 1) % SR) * 32 + lane];
+    self_window(wi, cur, prv, lane, J, D, s_tail, t0, R, list, Mw, cnt);
   }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of the ring left in flight
 }
 
 // ---------------------------------------------------------------------------
@@ -595,6 +610,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   int4 *s_top = reinterpret_cast<int4 *>(dsm + koff);                  // TOP_KEYS
   int4 *s_mid = s_top + TOP_KEYS;                                      // MID_KEYS
   unsigned char *s_L = reinterpret_cast<unsigned char *>(s_mid + MID_KEYS);  // LCAP
+  int4 *s_ring = reinterpret_cast<int4 *>(s_L + LCAP);                // nself * SR windows
 
   // ---- phase 0: warp 0 updates the row; the others fetch the snapshot
   // descriptor and stage the top two levels of its key array ----
@@ -667,8 +683,12 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int dl = min(D, n);
   for (int i = tid; i < dl; i += nthr) s_tail[i] = row[n - 1 - i];
   SelfScan sc;
-  if (warp < a.nself) self_prefetch(row, n, S, warp, a.nself, lane, sc);
-  asm volatile("cp.async.wait_all;" ::: "memory");  // staged keys landed (no-op if none)
+  // staged keys landed (no-op without any); a self warp's window groups,
+  // committed after them, stay in flight
+  if (warp < a.nself && self_prefetch(row, n, S, warp, a.nself, lane, s_ring + warp * (SR * 32), sc))
+    asm volatile("cp.async.wait_group %0;" ::"n"(SPF + 1) : "memory");
+  else
+    asm volatile("cp.async.wait_all;" ::: "memory");
   __syncthreads();
 
   // ---- phase 2: self match (nself warps) || corpus chain (3 probe warps) ----
@@ -1192,7 +1212,8 @@ size_t propose_smem_bytes(int nself, int R, int k, int cand_cap) {
   const size_t big = (size_t)max(cand_cap, R * ((k + 3) & ~3));
   const size_t boff = ((size_t)MAX_D + (size_t)nself * R + 3 * (size_t)R + 3) & ~(size_t)3;
   const size_t ints = (boff + big + 3) & ~(size_t)3;
-  const size_t bytes = sizeof(int) * ints + sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP;
+  const size_t bytes = sizeof(int) * ints + sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP +
+                       (size_t)nself * SR * 32 * sizeof(int4);
   return bytes > sizeof(SmallIngestSmem) ? bytes : sizeof(SmallIngestSmem);
 }
 
