@@ -94,6 +94,14 @@ typedef struct {
                                   snapshot, used only while both snapshots' records fit
                                   in SGD_RECORD_BUDGET bytes.  0: off.  Drafts are the
                                   same either way. */
+  int32_t  corpus_gram_index;  /* 1 (default): each snapshot also holds a hash table from
+                                  every distinct 2-, 3- and 4-gram that begins a suffix
+                                  to its suffix-array interval, so that the probe finds
+                                  an interval in one read instead of a descent;
+                                  128 * next_pow2(corpus_capacity) bytes per snapshot,
+                                  used only while both snapshots' tables fit in
+                                  SGD_RECORD_BUDGET bytes.  0: off (descent of the key
+                                  array).  Drafts are the same either way. */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)

@@ -57,6 +57,7 @@ class SgdConfig(ctypes.Structure):
         ("corpus_cand_cap", ctypes.c_int32),
         ("self_warps", ctypes.c_int32),
         ("corpus_records", ctypes.c_int32),
+        ("corpus_gram_index", ctypes.c_int32),
     ]
 
 

@@ -46,6 +46,8 @@ struct sgd_ctx {
   int4 *d_keys[2] = {nullptr, nullptr};
   int32_t *d_rec[2] = {nullptr, nullptr};  // per-position records, or null (off / over budget)
   RecShape rsh{};
+  int32_t *d_gt[2] = {nullptr, nullptr};   // n-gram tables, or null (off / over budget)
+  uint64_t gt_mask = 0;
   CorpusDesc *d_desc = nullptr;
   IngestScratch ing{};
   SaScratch sa{};
@@ -98,6 +100,7 @@ int validate(const sgd_config &c) {
     return SGD_EINVAL;
   if (c.self_warps < 0 || c.self_warps > MAX_SELF_WARPS) return SGD_EINVAL;
   if (c.corpus_records != 0 && c.corpus_records != 1) return SGD_EINVAL;
+  if (c.corpus_gram_index != 0 && c.corpus_gram_index != 1) return SGD_EINVAL;
   return SGD_OK;
 }
 
@@ -115,6 +118,8 @@ void free_ctx(sgd_ctx *x) {
   cudaFree(x->d_step_ready);
   cudaFree(x->d_rec[0]);
   cudaFree(x->d_rec[1]);
+  cudaFree(x->d_gt[0]);
+  cudaFree(x->d_gt[1]);
   cudaFree(x->d_step_sync);
   cudaFree(x->d_build_err);
   cudaFree(x->d_ring);
@@ -171,6 +176,11 @@ void worker_main(sgd_ctx *x) {
                         cudaSuccess)
         status = SGD_EBUILD;
       ++launches;
+      if (r == 0 && x->d_gt[back] != nullptr) {
+        if (launch_gram_table(x->d_keys[back], n, x->d_gt[back], x->gt_mask, side) != cudaSuccess)
+          status = SGD_EBUILD;
+        launches += 2;
+      }
       if (r == 0 && x->d_rec[back] != nullptr) {
         if (launch_records(x->d_text[back], x->d_sa[back], n, x->rsh, x->cfg.vocab_size,
                            x->d_rec[back], side) != cudaSuccess)
@@ -249,6 +259,7 @@ int sgd_config_default(sgd_config *c) {
   c->max_ingest_docs = 4096;
   c->corpus_cand_cap = 2048;
   c->corpus_records = 1;
+  c->corpus_gram_index = 1;
   c->self_warps = 0;
   return SGD_OK;
 }
@@ -313,6 +324,18 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
       al((void **)&x->d_rec[0], (size_t)C * x->rsh.ri * 4);
       al((void **)&x->d_rec[1], (size_t)C * x->rsh.ri * 4);
     }
+    {
+      // buckets: next power of two >= C, so 3 C grams fill at most 3/4 of the entries
+      unsigned long long nb = 1;
+      while (nb < (unsigned long long)C) nb <<= 1;
+      const unsigned long long bytes = nb * GT_BUCKET * GT_ENTRY * 4ull;
+      if (cfg->corpus_gram_index && 2ull * bytes <= SGD_RECORD_BUDGET) {
+        x->gt_mask = nb - 1;
+        al((void **)&x->d_gt[0], (size_t)bytes);
+        al((void **)&x->d_gt[1], (size_t)bytes);
+        if (e == cudaSuccess) e = cudaMemset(x->d_gt[0], 0, (size_t)bytes);
+      }
+    }
     al((void **)&x->d_step_ready, (size_t)cfg->max_batch * 4);
     al((void **)&x->d_step_sync, 8);
     if (e == cudaSuccess) e = cudaMemset(x->d_step_ready, 0, (size_t)cfg->max_batch * 4);
@@ -325,7 +348,7 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_start, 0, (size_t)cfg->max_docs * 8);
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_len, 0, (size_t)cfg->max_docs * 4);
     if (e == cudaSuccess) {
-      CorpusDesc d0{x->d_text[0], x->d_sa[0], x->d_keys[0], 0, 0, x->d_rec[0]};
+      CorpusDesc d0{x->d_text[0], x->d_sa[0], x->d_keys[0], 0, 0, x->d_rec[0], x->d_gt[0], x->gt_mask};
       e = cudaMemcpy(x->d_desc, &d0, sizeof(d0), cudaMemcpyHostToDevice);
     }
     if (e == cudaSuccess) e = cudaMallocHost((void **)&x->h_n, 8);
@@ -570,7 +593,8 @@ int sgd_poll(sgd_ctx *x, int wait, int64_t timeout_us, void *stream, uint64_t *g
   }
   const int back = 1 - x->front;
   const cudaError_t e = launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->d_keys[back],
-                                    x->d_rec[back], x->built_n, x->gen + 1, (cudaStream_t)stream);
+                                    x->d_rec[back], x->d_gt[back], x->gt_mask, x->built_n, x->gen + 1,
+                                    (cudaStream_t)stream);
   if (e != cudaSuccess) return SGD_ECUDA;
   x->launches++;
   x->front = back;

@@ -119,13 +119,81 @@ __global__ void __launch_bounds__(256) linearize_kernel(const int32_t *ring, lon
 }
 
 __global__ void swap_kernel(CorpusDesc *desc, const int32_t *text, const int32_t *sa,
-                            const int4 *keys, const int32_t *rec, long long n, uint64_t gen) {
+                            const int4 *keys, const int32_t *rec, const int32_t *gt,
+                            uint64_t gt_mask, long long n, uint64_t gen) {
   desc->text = text;
   desc->sa = sa;
   desc->keys = keys;
   desc->rec = rec;
+  desc->gt = gt;
+  desc->gt_mask = gt_mask;
   desc->n = n;
   desc->gen = gen;
+}
+
+// The first m tokens of a key (the rest KEY_END), and whether they exist.
+__device__ __forceinline__ bool gram_of(const int4 &k, int m, int4 &g) {
+  g = make_int4(k.x, m >= 2 ? k.y : KEY_END, m >= 3 ? k.z : KEY_END, m >= 4 ? k.w : KEY_END);
+  return k.x != KEY_END && (m < 2 || k.y != KEY_END) && (m < 3 || k.z != KEY_END) &&
+         (m < 4 || k.w != KEY_END);
+}
+
+__device__ __forceinline__ bool same_gram(const int4 &a, const int4 &b, int m) {
+  return a.x == b.x && (m < 2 || a.y == b.y) && (m < 3 || a.z == b.z) && (m < 4 || a.w == b.w);
+}
+
+// n-gram table, pass 1: the first suffix of every run of equal m-grams
+// inserts the gram with lo = its position (each gram once, so claims by
+// compare-and-swap on the m word are the only contention).
+__global__ void __launch_bounds__(256) gram_insert_kernel(const int4 *K, long long n, int32_t *gt,
+                                                          uint64_t mask) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x; p < n; p += stride) {
+    const int4 k = K[p];
+    const int4 kp = p > 0 ? K[p - 1] : make_int4(KEY_END, KEY_END, KEY_END, KEY_END);
+    for (int m = 2; m <= 4; ++m) {
+      int4 g;
+      if (!gram_of(k, m, g)) break;  // shorter than m tokens, so also than m + 1
+      if (p > 0 && same_gram(kp, k, m)) continue;
+      uint64_t b = gram_hash(m, g.x, g.y, g.z, g.w) & mask;
+      for (uint64_t step = 0; step <= mask; ++step, b = (b + 1) & mask) {
+        int32_t *e = gt + (size_t)b * GT_BUCKET * GT_ENTRY;
+        int j = 0;
+        for (; j < GT_BUCKET; ++j, e += GT_ENTRY)
+          if (atomicCAS(e, 0, m) == 0) break;
+        if (j == GT_BUCKET) continue;
+        e[1] = g.x; e[2] = g.y; e[3] = g.z; e[4] = g.w;
+        e[5] = (int32_t)p;
+        break;
+      }
+    }
+  }
+}
+
+// pass 2: the last suffix of every run finds its gram and writes hi.
+__global__ void __launch_bounds__(256) gram_hi_kernel(const int4 *K, long long n, int32_t *gt,
+                                                      uint64_t mask) {
+  const long long stride = (long long)gridDim.x * blockDim.x;
+  for (long long p = (long long)blockIdx.x * blockDim.x + threadIdx.x; p < n; p += stride) {
+    const int4 k = K[p];
+    const int4 kn = p + 1 < n ? K[p + 1] : make_int4(KEY_END, KEY_END, KEY_END, KEY_END);
+    for (int m = 2; m <= 4; ++m) {
+      int4 g;
+      if (!gram_of(k, m, g)) break;
+      if (p + 1 < n && same_gram(kn, k, m)) continue;
+      uint64_t b = gram_hash(m, g.x, g.y, g.z, g.w) & mask;
+      for (uint64_t step = 0; step <= mask; ++step, b = (b + 1) & mask) {
+        int32_t *e = gt + (size_t)b * GT_BUCKET * GT_ENTRY;
+        bool done = false;
+        for (int j = 0; j < GT_BUCKET && !done; ++j, e += GT_ENTRY)
+          if (e[0] == m && e[1] == g.x && e[2] == g.y && e[3] == g.z && e[4] == g.w) {
+            e[6] = (int32_t)(p + 1);
+            done = true;
+          }
+        if (done) break;
+      }
+    }
+  }
 }
 
 // The record of every suffix-array position, one warp per record: lane f
@@ -207,8 +275,21 @@ cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs, cons
 }
 
 cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
-                        const int32_t *rec, int64_t n, uint64_t gen, cudaStream_t st) {
-  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, rec, n, gen);
+                        const int32_t *rec, const int32_t *gt, uint64_t gt_mask, int64_t n,
+                        uint64_t gen, cudaStream_t st) {
+  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, rec, gt, gt_mask, n, gen);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gram_table(const int4 *keys, int64_t n, int32_t *gt, uint64_t mask,
+                              cudaStream_t st) {
+  if (gt == nullptr) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(gt, 0, (size_t)(mask + 1) * GT_BUCKET * GT_ENTRY * 4, st);
+  if (e != cudaSuccess || n <= 0) return e;
+  long long blocks = (n + 1023) / 1024;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  gram_insert_kernel<<<(int)blocks, 256, 0, st>>>(keys, n, gt, mask);
+  gram_hi_kernel<<<(int)blocks, 256, 0, st>>>(keys, n, gt, mask);
   return cudaGetLastError();
 }
 

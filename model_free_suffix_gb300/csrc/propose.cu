@@ -226,6 +226,8 @@ struct Corpus {
   const int4 *K;
   const int32_t *Rec;  // per-position records, or null
   RecShape rs;
+  const int32_t *GT;   // n-gram table, or null
+  uint64_t gtm;        // its buckets - 1
   long long N;
   int Lmax;
   const int4 *s_top;  // K[j * 32^Lmax]
@@ -273,6 +275,34 @@ __device__ void probe_bounds(const Corpus &c, const int4 &P, int m, int lane, lo
   }
   lo = bL;
   hi = bU;
+}
+
+// [lo, hi) for the m-gram P from the snapshot's n-gram table, by one warp:
+// lanes 0..7 read a 128-byte bucket (lane 2e and 2e + 1 hold entry e), two
+// ballots find the matching entry; a bucket with an empty entry ends the
+// search (the gram does not begin any suffix).
+__device__ void gram_bounds(const Corpus &c, const int4 &P, int m, int lane, long long &lo,
+                            long long &hi) {
+  const int4 g = make_int4(P.x, m >= 2 ? P.y : KEY_END, m >= 3 ? P.z : KEY_END, m >= 4 ? P.w : KEY_END);
+  uint64_t b = gram_hash(m, g.x, g.y, g.z, g.w) & c.gtm;
+  lo = hi = 0;
+  for (uint64_t step = 0; step <= c.gtm; ++step, b = (b + 1) & c.gtm) {
+    int4 v = make_int4(0, 0, 0, 0);
+    if (lane < 2 * GT_BUCKET)
+      v = __ldg(reinterpret_cast<const int4 *>(c.GT + (size_t)b * GT_BUCKET * GT_ENTRY) + lane);
+    const bool even = (lane & 1) == 0 && lane < 2 * GT_BUCKET;
+    const bool odd = (lane & 1) == 1 && lane < 2 * GT_BUCKET;
+    const unsigned e0 = __ballot_sync(FULL, even && v.x == m && v.y == g.x && v.z == g.y && v.w == g.z);
+    const unsigned e1 = __ballot_sync(FULL, odd && v.x == g.w);
+    const unsigned match = e0 & (e1 >> 1);  // bit 2e: entry e holds the gram
+    if (match) {
+      const int src = __ffs(match);          // lane 2e + 1: (t3, lo, hi, -)
+      lo = __shfl_sync(FULL, v.y, src);
+      hi = __shfl_sync(FULL, v.z, src);
+      return;
+    }
+    if (__ballot_sync(FULL, even && v.x == 0)) return;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -614,12 +644,14 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
 
   // ---- phase 0: warp 0 updates the row; the others fetch the snapshot
   // descriptor and stage the top two levels of its key array ----
-  Corpus cp{nullptr, nullptr, nullptr, nullptr, a.rsh, 0, 0, s_top, s_mid};
+  Corpus cp{nullptr, nullptr, nullptr, nullptr, a.rsh, nullptr, 0, 0, 0, s_top, s_mid};
   if (a.desc != nullptr) {
     cp.X = a.desc->text;
     cp.SA = a.desc->sa;
     cp.K = a.desc->keys;
     cp.Rec = a.desc->rec;
+    cp.GT = a.desc->gt;
+    cp.gtm = a.desc->gt_mask;
     cp.N = a.desc->n;
     cp.Lmax = cp.N >= 2 ? top_level(cp.N) : 0;
   }
@@ -651,7 +683,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_c0c = 0;
       s_cpf = 0;
     }
-  } else if (a.desc != nullptr && cp.N >= 2) {
+  } else if (a.desc != nullptr && cp.N >= 2 && cp.GT == nullptr) {
     const int sh = 5 * cp.Lmax;
     const long long ntop = (cp.N + (1LL << sh) - 1) >> sh;
     const long long nmid = cp.Lmax > 0 ? (cp.N + (1LL << (sh - 5)) - 1) >> (sh - 5) : 0;
@@ -739,7 +771,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         // a pattern holding KEY_END cannot occur: corpus tokens are in [0, V]
         const bool endless = P.x != KEY_END && (m < 2 || P.y != KEY_END) &&
                              (m < 3 || P.z != KEY_END) && (m < 4 || P.w != KEY_END);
-        if (endless) probe_bounds(cp, P, m, lane, plo, phi);
+        if (endless) {
+          if (cp.GT != nullptr) gram_bounds(cp, P, m, lane, plo, phi);
+          else probe_bounds(cp, P, m, lane, plo, phi);
+        }
       }
       if (lane == 0) { s_bound[2 * pw] = plo; s_bound[2 * pw + 1] = phi; }
     }

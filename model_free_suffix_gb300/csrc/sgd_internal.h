@@ -26,7 +26,26 @@ struct CorpusDesc {
   int64_t n;
   uint64_t gen;
   const int32_t *rec;   // per-position records (RecShape), or null
+  const int32_t *gt;    // n-gram table (below), or null
+  uint64_t gt_mask;     // buckets - 1
 };
+
+// n-gram table: for every distinct m-gram (m = 2, 3, 4) that begins a suffix
+// of the snapshot, its suffix-array interval [lo, hi).  Open addressing over
+// buckets of GT_BUCKET entries of GT_ENTRY ints: [0] m (0: empty), [1..4] the
+// tokens (KEY_END past m), [5] lo, [6] hi, [7] unused.  A bucket is 128 bytes.
+constexpr int GT_BUCKET = 4;
+constexpr int GT_ENTRY = 8;
+__host__ __device__ inline uint64_t gram_hash(int m, int t0, int t1, int t2, int t3) {
+  uint64_t h = 0x9E3779B97F4A7C15ull * (uint64_t)(m + 1);
+  const uint32_t t[4] = {(uint32_t)t0, (uint32_t)t1, (uint32_t)t2, (uint32_t)t3};
+  for (int i = 0; i < 4; ++i) {
+    h ^= t[i];
+    h *= 0xff51afd7ed558ccdull;
+    h ^= h >> 32;
+  }
+  return h;
+}
 
 // Record of suffix-array position p (i = sa[p]), ri ints: [0] i; [1, 1+bk)
 // the tokens before the suffix, X[i-1-j] (KEY_END before the text); then kc
@@ -112,8 +131,10 @@ cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs,
                              cudaStream_t st, int *launches);
 cudaError_t launch_records(const int32_t *text, const int32_t *sa, int64_t n, RecShape shape, int Z,
                            int32_t *rec, cudaStream_t st);
+cudaError_t launch_gram_table(const int4 *keys, int64_t n, int32_t *gt, uint64_t mask,
+                              cudaStream_t st);
 cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
-                        const int32_t *rec,
+                        const int32_t *rec, const int32_t *gt, uint64_t gt_mask,
                         int64_t n, uint64_t gen, cudaStream_t st);
 // keys[p] = text[sa[p] .. sa[p]+3] (KEY_END past n), on `st`
 cudaError_t launch_suffix_keys(const int32_t *text, const int32_t *sa, int64_t n, int4 *keys,

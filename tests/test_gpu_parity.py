@@ -154,9 +154,15 @@ CORPUS_GRID = [
 ]
 
 
-@pytest.mark.parametrize("records", [1, 0], ids=["records", "text"])
+# snapshot indexes: (records, n-gram table); drafts must be the same for each
+INDEX_MODES = [(1, 1), (1, 0), (0, 0)]
+INDEX_IDS = ["records+grams", "records+descent", "text+descent"]
+
+
+@pytest.mark.parametrize("mode", INDEX_MODES, ids=INDEX_IDS)
 @pytest.mark.parametrize("grid", CORPUS_GRID, ids=lambda g: "V%d_D%d_R%d_cap%d" % (g[0], g[1], g[2], g[4]))
-def test_fuzz_corpus(grid, records):
+def test_fuzz_corpus(grid, mode):
+    records, grams = mode
     SuffixDrafter, W, O, H = _mods()
     V, D, R, k, cc, nd, dl = grid
     rng = np.random.default_rng(sum(grid))
@@ -180,7 +186,8 @@ def test_fuzz_corpus(grid, records):
         n[b] = nb
     dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=D,
                        max_occurrences=R, corpus_capacity=max(1024, len(X)), corpus_cand_cap=cc,
-                       max_spec_factor=(2, 1), min_token_prob=(1, 8), corpus_records=records)
+                       max_spec_factor=(2, 1), min_token_prob=(1, 8), corpus_records=records,
+                       corpus_gram_index=grams)
     _ingest_text(dr, X, V, S)
     dr.build_sa(torch.cuda.Stream())
     assert dr.poll(wait=True)[0] == 1
@@ -211,10 +218,10 @@ def test_large_match_set_multi_pass_selection():
     tok[2, :4] = [1, 2, 7, 9]
     tok[3, :5] = [9, 3, 9, 7, 9]      # self M=1 (9), corpus 2 wins
     n = np.array([3, 2, 4, 5], dtype=np.int32)
-    for cc, R in ((64, 16), (64, 64), (128, 100), (4096, 64)):
+    for cc, R, grams in ((64, 16, 1), (64, 64, 0), (128, 100, 1), (4096, 64, 0)):
         dr = SuffixDrafter(max_batch=4, seq_capacity=S, vocab_size=V, k=4, max_tree_depth=24,
                            max_occurrences=R, corpus_capacity=len(X), corpus_cand_cap=cc,
-                           min_token_prob=(0, 1), max_docs=4096)
+                           min_token_prob=(0, 1), max_docs=4096, corpus_gram_index=grams)
         _ingest_text(dr, X, V, S)
         dr.build_sa(torch.cuda.Stream())
         assert dr.poll(wait=True)[0] == 1
@@ -226,9 +233,9 @@ def test_large_match_set_multi_pass_selection():
         dr.close()
 
 
-@pytest.mark.parametrize("records", [1, 0], ids=["records", "text"])
+@pytest.mark.parametrize("mode", INDEX_MODES, ids=INDEX_IDS)
 @pytest.mark.parametrize("R", [16, 128])
-def test_small_p4_interval_long_matches(R, records):
+def test_small_p4_interval_long_matches(R, mode):
     """A 4-token pattern with ~100 hits whose matches run back 10 tokens: the
     small-interval path evaluates them from one round of on-chip context and
     selects the R most recent (on-chip radix select when R < hits)."""
@@ -249,7 +256,7 @@ def test_small_p4_interval_long_matches(R, records):
     n = np.array([12, 10, 26], dtype=np.int32)
     dr = SuffixDrafter(max_batch=3, seq_capacity=S, vocab_size=V, k=8, max_tree_depth=24,
                        max_occurrences=R, corpus_capacity=len(X), min_token_prob=(1, 20),
-                       max_docs=4096, corpus_records=records)
+                       max_docs=4096, corpus_records=mode[0], corpus_gram_index=mode[1])
     _ingest_text(dr, X, V, S)
     dr.build_sa(torch.cuda.Stream())
     assert dr.poll(wait=True)[0] == 1
