@@ -211,11 +211,13 @@ __global__ void __launch_bounds__(256) records_kernel(const int32_t *text, const
       int v = 0;
       if (f == 0) {
         v = (int)i;
-      } else if (f <= sh.bk) {
-        const long long q = i - f;
+      } else if (f == 1) {
+        v = i + 4 < n ? text[i + 4] : Z;
+      } else if (f >= 4 && f < 4 + sh.bk) {
+        const long long q = i - 1 - (f - 4);
         v = q >= 0 ? text[q] : KEY_END;
-      } else if (f <= sh.bk + sh.kc) {
-        const long long q = i + 4 + (f - 1 - sh.bk);
+      } else if (f >= sh.co && f < sh.co + sh.kc) {
+        const long long q = i + 4 + (f - sh.co);
         v = q < n ? text[q] : Z;
       }
       r[f] = v;

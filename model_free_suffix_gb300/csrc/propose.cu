@@ -305,6 +305,25 @@ __device__ void gram_bounds(const Corpus &c, const int4 &P, int m, int lane, lon
   }
 }
 
+// The interval of the last m tokens (t[i] = the i-th token from the end),
+// written to bound[0..1] by lane 0; empty when the row is shorter, m > D or
+// the pattern holds KEY_END (corpus tokens are in [0, V], so it cannot occur).
+__device__ void pattern_bounds(const Corpus &c, const int *t, int m, int D, int n, int lane,
+                               long long *bound) {
+  long long plo = 0, phi = 0;
+  if (D >= m && n >= m) {
+    const int4 P = make_int4(t[m - 1], m >= 2 ? t[m - 2] : 0, m >= 3 ? t[m - 3] : 0,
+                             m >= 4 ? t[m - 4] : 0);
+    const bool endless = P.x != KEY_END && (m < 2 || P.y != KEY_END) &&
+                         (m < 3 || P.z != KEY_END) && (m < 4 || P.w != KEY_END);
+    if (endless) {
+      if (c.GT != nullptr) gram_bounds(c, P, m, lane, plo, phi);
+      else probe_bounds(c, P, m, lane, plo, phi);
+    }
+  }
+  if (lane == 0) { bound[0] = plo; bound[1] = phi; }
+}
+
 // ---------------------------------------------------------------------------
 // corpus: the P4 level (random access into the text)
 
@@ -397,7 +416,7 @@ __device__ void scan_p4_ctx(const Corpus &c, int Z, long long lo, long long hi, 
   const int dl = min(D, n);
   if (c.Rec != nullptr) {
     // the snapshot's records hold all of it: one round trip of 16-byte copies
-    const int ri = c.rs.ri, bk = c.rs.bk, q4 = ri >> 2;
+    const int ri = c.rs.ri, q4 = ri >> 2;
     for (int f = tid; f < cnt * q4; f += nthr) {
       const int i = f / q4, j = f - i * q4;
       cp_async16(&s_ctx[i * ri + 4 * j], c.Rec + (size_t)(lo + i) * ri + 4 * j);
@@ -409,10 +428,22 @@ __device__ void scan_p4_ctx(const Corpus &c, int Z, long long lo, long long hi, 
       const long long e = (long long)x[0] + 3;
       s_e[i] = (int)e;
       int L = 0;
-      if (x[1 + bk] != Z) {
-        const long long lim = min((long long)dl, e + 1);
+      if (x[1] != Z) {
+        // back tokens against tail[4..], four per 16-byte load of each
+        const int lim = (int)min((long long)dl, e + 1);
+        const int4 *xb = reinterpret_cast<const int4 *>(x + 4);
+        const int4 *tb = reinterpret_cast<const int4 *>(s_tail + 4);
         L = 4;
-        while (L < lim && x[1 + L - 4] == s_tail[L]) ++L;
+        for (int q = 0; 4 + 4 * q < lim; ++q) {
+          const int4 u = xb[q], v = tb[q];
+          int f = 4;
+          if (u.w != v.w) f = 3;
+          if (u.z != v.z) f = 2;
+          if (u.y != v.y) f = 1;
+          if (u.x != v.x) f = 0;
+          L = min(4 + 4 * q + f, lim);
+          if (f < 4) break;
+        }
         atomicAdd(&s_lhist[L], 1);
       }
       s_L[i] = (unsigned char)L;
@@ -623,6 +654,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ long long s_bound[2 * NPROBE3];
   __shared__ int s_n, s_Ms, s_cs, s_q, s_sel, s_need, s_have_corpus;
   __shared__ int s_self_done, s_ms_ready, s_pms, s_Mc, s_c0c, s_cpf;
+  __shared__ int s_early[4], s_early_ok;  // last four tokens, known from the update
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
   const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
@@ -661,8 +693,13 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     uint32_t fl = 0;
     if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
     if (n > S) { n = S; fl |= SGD_ERR_NUM_TOKENS; }
+    const int n_old = n;
     if (a.do_update) n = update_row_warp(row, n, a.sampled + (size_t)b * a.T, a.T, S, a.V, lane, fl);
     if (lane == 0 && a.do_update) a.ntok[b] = n;
+    // When the update appended >= 4 ids, the last four tokens are those ids:
+    // the probe warps can look the n-grams up before the tail is read back.
+    const bool early = a.do_update && n - n_old >= 4;
+    if (early && lane < 4) s_early[lane] = __ldg(a.sampled + (size_t)b * a.T + (n - n_old) - 1 - lane);
     if (a.ing_m > 0) {  // publish the updated row to the ingest CTA
       __threadfence();
       __syncwarp();
@@ -673,6 +710,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     }
     if (lane == 0) {
       if (fl) atomicOr(a.err, fl);
+      s_early_ok = early;
       s_n = n;
       s_have_corpus = a.desc != nullptr && cp.N >= 2;
       s_self_done = 0;
@@ -714,6 +752,11 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // ---- phase 1: tail[i] = t[n-1-i]; self warps prefetch their first windows ----
   const int dl = min(D, n);
   for (int i = tid; i < dl; i += nthr) s_tail[i] = row[n - 1 - i];
+  // with the last four tokens known from the update and an n-gram table, the
+  // probe warps find their intervals now, while the tail is being read
+  const bool early_bounds = corpus_ok && s_early_ok && cp.GT != nullptr;
+  if (early_bounds && warp >= a.nself)
+    pattern_bounds(cp, s_early, 4 - (warp - a.nself), D, n, lane, &s_bound[2 * (warp - a.nself)]);
   SelfScan sc;
   // staged keys landed (no-op without any); a self warp's window groups,
   // committed after them, stay in flight
@@ -762,22 +805,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   } else if (corpus_ok) {
     const int pw = warp - a.nself;  // 0: last 4 tokens, 1: last 3, 2: last 2
     const int ptid = tid - 32 * a.nself, pthr = 32 * NPROBE3;
-    {
-      const int m = 4 - pw;
-      long long plo = 0, phi = 0;
-      if (D >= m && n >= m) {
-        const int4 P = make_int4(s_tail[m - 1], m >= 2 ? s_tail[m - 2] : 0,
-                                 m >= 3 ? s_tail[m - 3] : 0, m >= 4 ? s_tail[m - 4] : 0);
-        // a pattern holding KEY_END cannot occur: corpus tokens are in [0, V]
-        const bool endless = P.x != KEY_END && (m < 2 || P.y != KEY_END) &&
-                             (m < 3 || P.z != KEY_END) && (m < 4 || P.w != KEY_END);
-        if (endless) {
-          if (cp.GT != nullptr) gram_bounds(cp, P, m, lane, plo, phi);
-          else probe_bounds(cp, P, m, lane, plo, phi);
-        }
-      }
-      if (lane == 0) { s_bound[2 * pw] = plo; s_bound[2 * pw + 1] = phi; }
-    }
+    if (!early_bounds) pattern_bounds(cp, s_tail, 4 - pw, D, n, lane, &s_bound[2 * pw]);
     probe_sync();
     // The row's own match length, -1 while the self warps still scan.  Before
     // a large piece of work the probe warps wait for it (bounded; on time-out
@@ -882,7 +910,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       const int capc = draft_cap(a, Mc, n), capp = (capc + 3) & ~3;  // row stride 16-B aligned
       const int cnt = (int)(hi - lo);
       const int W = cp.Rec ? cp.rs.ri : k + dl - 4;      // context stride
-      const int co = cp.Rec ? 1 + cp.rs.bk : 0;          // where the continuation starts
+      const int co = cp.Rec ? cp.rs.co : 0;              // where the continuation starts
       probe_sync();
       if (ptid == 0) s_q = 0;
       unsigned thr = 0;
@@ -1189,19 +1217,40 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         if (lane < npart && mycnt == maxc) myv = (unsigned)v ^ 0x80000000u;
         cnt = (int)maxc;
       } else {
-        int c4[4] = {0, 0, 0, 0};
-        for (int q = 0; q < npart; ++q) {
-          const int vq = s_vv[q];
+        // more than 32 participants: count every value in a 256-entry open
+        // addressing table in shared memory (the probe's idle length cache);
+        // a key is (1 << 32) | value, so 0 marks a free entry for any value
+        unsigned long long *hk = reinterpret_cast<unsigned long long *>(s_L);
+        unsigned *hc = reinterpret_cast<unsigned *>(s_L + 256 * sizeof(unsigned long long));
+        for (int i = lane; i < 256; i += 32) { hk[i] = 0ull; hc[i] = 0u; }
+        __syncwarp();
+        int hs[4];
 #pragma unroll
-          for (int s = 0; s < 4; ++s) c4[s] += vq == val[s];
+        for (int s = 0; s < 4; ++s) {
+          hs[s] = 0;
+          if (!part[s]) continue;
+          const unsigned long long key = (1ull << 32) | (unsigned)val[s];
+          unsigned h = ((unsigned)val[s] * 0x9E3779B1u) >> 24;
+          for (int t = 0; t < 256; ++t, h = (h + 1) & 255u) {  // <= 128 keys: ends early
+            const unsigned long long old = atomicCAS(&hk[h], 0ull, key);
+            if (old == 0ull || old == key) {
+              atomicAdd(&hc[h], 1u);
+              hs[s] = (int)h;
+              break;
+            }
+          }
         }
+        __syncwarp();
+        unsigned c4[4];
 #pragma unroll
-        for (int s = 0; s < 4; ++s)
-          if (part[s]) mycnt = max(mycnt, (unsigned)c4[s]);
+        for (int s = 0; s < 4; ++s) {
+          c4[s] = part[s] ? hc[hs[s]] : 0u;
+          mycnt = max(mycnt, c4[s]);
+        }
         const unsigned maxc = __reduce_max_sync(FULL, mycnt);
 #pragma unroll
         for (int s = 0; s < 4; ++s)
-          if (part[s] && (unsigned)c4[s] == maxc) myv = min(myv, (unsigned)val[s] ^ 0x80000000u);
+          if (part[s] && c4[s] == maxc) myv = min(myv, (unsigned)val[s] ^ 0x80000000u);
         cnt = (int)maxc;
       }
       const int tau = (int)(__reduce_min_sync(FULL, myv) ^ 0x80000000u);

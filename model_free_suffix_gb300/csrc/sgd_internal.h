@@ -47,17 +47,20 @@ __host__ __device__ inline uint64_t gram_hash(int m, int t0, int t1, int t2, int
   return h;
 }
 
-// Record of suffix-array position p (i = sa[p]), ri ints: [0] i; [1, 1+bk)
-// the tokens before the suffix, X[i-1-j] (KEY_END before the text); then kc
-// tokens after its first four, X[i+4+j] (Z past the end); zero padding.
+// Record of suffix-array position p (i = sa[p]), ri ints, every region on a
+// 16-byte boundary: [0] i, [1] X[i+4] (Z past the end), [2..3] zero;
+// [4, 4+bk) the bk tokens before the suffix, X[i-1-j] (KEY_END before the
+// text); [co, co+kc) the kc tokens after its first four, X[i+4+j] (Z past
+// the end); zero padding.
 struct RecShape {
-  int ri, bk, kc;
+  int ri, bk, kc, co;
 };
 inline RecShape rec_shape(int D, int k) {
   RecShape r;
   r.bk = D > 4 ? D - 4 : 0;
   r.kc = k;
-  r.ri = (1 + r.bk + r.kc + 3) & ~3;
+  r.co = 4 + ((r.bk + 3) & ~3);
+  r.ri = r.co + ((r.kc + 3) & ~3);
   return r;
 }
 constexpr int KEY_END = (int)0x80000000;  // below every id: the text ran out
