@@ -211,8 +211,8 @@ __global__ void __launch_bounds__(256) records_kernel(const int32_t *text, const
       int v = 0;
       if (f == 0) {
         v = (int)i;
-      } else if (f == 1) {
-        v = i + 4 < n ? text[i + 4] : Z;
+      } else if (f <= 3) {
+        v = i + 3 + f < n ? text[i + 3 + f] : Z;
       } else if (f >= 4 && f < 4 + sh.bk) {
         const long long q = i - 1 - (f - 4);
         v = q >= 0 ? text[q] : KEY_END;

@@ -655,6 +655,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ int s_n, s_Ms, s_cs, s_q, s_sel, s_need, s_have_corpus;
   __shared__ int s_self_done, s_ms_ready, s_pms, s_Mc, s_c0c, s_cpf;
   __shared__ int s_early[4], s_early_ok;  // last four tokens, known from the update
+  __shared__ int s_ckey;  // short level whose continuation comes from keys and records, or 0
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
   const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
@@ -720,6 +721,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_Mc = 0;
       s_c0c = 0;
       s_cpf = 0;
+      s_ckey = 0;
     }
   } else if (a.desc != nullptr && cp.N >= 2 && cp.GT == nullptr) {
     const int sh = 5 * cp.Lmax;
@@ -825,6 +827,12 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     int Mc = 0, lvl = 0, Q = 0;
     bool p4ctx = false;   // the P4 interval was evaluated on chip (scan_p4_ctx)
     bool oncand = false;  // a short level's ends are all in s_big already
+    // A short level's candidates also keep their suffix-array positions (in the
+    // idle length-cache area), so that their continuation is read from the key
+    // array (just read, so cached) and the records instead of the text.
+    int *s_candp = reinterpret_cast<int *>(s_L);
+    int *s_occp = s_candp + a.cand_cap;
+    const bool keep_p = (size_t)(a.cand_cap + R) * sizeof(int) <= (size_t)LCAP;
     int *s_e4 = reinterpret_cast<int *>(s_L + P4C_MAX);  // small-P4 ends, then contexts
     int *s_ctx = s_e4 + P4C_MAX;
     long long lo = 0, hi = 0;
@@ -887,7 +895,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
             if (lane == 0 && m) base = atomicAdd(&s_q, __popc(m));
             base = __shfl_sync(FULL, base, 0);
             const int slot = base + __popc(m & lt);
-            if (v && slot < a.cand_cap) s_big[slot] = eb[u];
+            if (v && slot < a.cand_cap) {
+              s_big[slot] = eb[u];
+              if (keep_p) s_candp[slot] = (int)(p0 + lane + (long long)u * pthr);
+            }
           }
         }
         probe_sync();
@@ -1031,15 +1042,27 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         if (ptid == 0) s_q = 0;
         probe_sync();
         for (int i = ptid; i < Qc; i += pthr)
-          if ((unsigned)cand[i] >= pf2) s_occc[atomicAdd(&s_q, 1)] = cand[i];
+          if ((unsigned)cand[i] >= pf2) {
+            const int slot = atomicAdd(&s_q, 1);
+            s_occc[slot] = cand[i];
+            if (oncand && keep_p) s_occp[slot] = s_candp[i];
+          }
         c0c = R;
       } else {
         if (!pf)
-          for (int i = ptid; i < Qc; i += pthr) s_occc[i] = cand[i];
+          for (int i = ptid; i < Qc; i += pthr) {
+            s_occc[i] = cand[i];
+            if (oncand && keep_p) s_occp[i] = s_candp[i];
+          }
         c0c = Qc;
       }
       asm volatile("cp.async.wait_all;" ::: "memory");
-      if (ptid == 0) { s_Mc = Mc; s_c0c = c0c; s_cpf = pf; }
+      if (ptid == 0) {
+        s_Mc = Mc;
+        s_c0c = c0c;
+        s_cpf = pf;
+        s_ckey = oncand && keep_p ? lvl : 0;
+      }
     } else if (ptid == 0) {
       s_Mc = 0;
     }
@@ -1058,12 +1081,23 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int capp = (cap + 3) & ~3;
   if (cap > 0 && c0 > 0) {
     const int tot = (src == 2 && s_cpf) ? 0 : c0 * cap;  // prefetched by the probe warps
+    const int ck = src == 2 ? s_ckey : 0;
+    const int *occp = reinterpret_cast<const int *>(s_L) + a.cand_cap;
     for (int idx = tid; idx < tot; idx += nthr) {
       const int o = idx / cap, d = idx - o * cap;
       const long long pos = (long long)occ[o] + 1 + d;
       int v;
-      if (src == 1) v = pos <= n - 1 ? row[pos] : 0;
-      else v = pos < cp.N ? __ldg(cp.X + pos) : Z;
+      if (src == 1) {
+        v = pos <= n - 1 ? row[pos] : 0;
+      } else if (ck != 0 && ck + d <= 3) {  // inside the hit's suffix key (KEY_END: past the text)
+        const int *kq = reinterpret_cast<const int *>(cp.K + occp[o]);
+        v = __ldg(kq + ck + d);
+        if (v == KEY_END) v = Z;
+      } else if (ck != 0 && cp.Rec != nullptr && ck + d <= 6) {  // the record's first 16 bytes
+        v = __ldg(cp.Rec + (size_t)occp[o] * cp.rs.ri + (ck + d - 3));
+      } else {
+        v = pos < cp.N ? __ldg(cp.X + pos) : Z;
+      }
       cont[o * capp + d] = v;
     }
     __syncthreads();

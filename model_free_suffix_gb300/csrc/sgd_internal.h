@@ -48,7 +48,7 @@ __host__ __device__ inline uint64_t gram_hash(int m, int t0, int t1, int t2, int
 }
 
 // Record of suffix-array position p (i = sa[p]), ri ints, every region on a
-// 16-byte boundary: [0] i, [1] X[i+4] (Z past the end), [2..3] zero;
+// 16-byte boundary: [0] i, [1..3] X[i+4], X[i+5], X[i+6] (Z past the end);
 // [4, 4+bk) the bk tokens before the suffix, X[i-1-j] (KEY_END before the
 // text); [co, co+kc) the kc tokens after its first four, X[i+4+j] (Z past
 // the end); zero padding.
