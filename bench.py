@@ -161,8 +161,10 @@ def run_ours(args, rank, world):
                        max_spec_factor=cfg.factor, max_spec_offset=cfg.offset,
                        min_token_prob=cfg.min_prob, corpus_capacity=cfg.corpus_tokens,
                        device=dev.index)
-    stream = torch.cuda.Stream(device=dev)
-    side = torch.cuda.Stream(device=dev)
+    # drafting at the device's highest stream priority, snapshot builds at the lowest
+    least, greatest = torch.cuda.Stream.priority_range()
+    stream = torch.cuda.Stream(device=dev, priority=greatest)
+    side = torch.cuda.Stream(device=dev, priority=least)
     torch.cuda.set_stream(stream)
     # corpus prefill (setup, untimed)
     if cfg.corpus_tokens:
@@ -326,7 +328,8 @@ def run_ours(args, rank, world):
         "config": dict(workload_config(cfg, world),
                    l2="flushed before every timed step (%d MiB write)" % (flush.numel() * 4 >> 20),
                    launch="each step replays one CUDA graph: the fused sgd_step launch "
-                          "(update + propose + ingest); rebuilds on a side stream"),
+                          "(update + propose + ingest) on a highest-priority stream; "
+                          "rebuilds on a lowest-priority side stream"),
         "roofline": rl, "roofline_propose": rl_prop, "kernels": kernels,
         "propose_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
                        "median": round(1e3 * float(np.median(prop_ms)), 2),
