@@ -404,23 +404,29 @@ def long_context_leg(args, rank):
 
 
 def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state, dev, stream):
-    """Same steps through the public API with pinned host buffers: each step
-    copies its sampled ids (and ingest arguments) host->device and reads the
-    drafts and valid counts back, all inside the timed region."""
+    """Same steps through the public API with pinned host buffers
+    (SuffixDrafter.step_host): each step copies its sampled ids and ingest
+    arguments host->device and reads the drafts and valid counts back, all
+    inside the timed region."""
     import torch
     n_avail = len(steps) - first
     K = min(K, n_avail)
-    pin = lambda a: torch.from_numpy(np.ascontiguousarray(a)).pin_memory()
-    h_samp = [pin(steps[first + j].sampled) for j in range(K)]
-    h_fin = [(pin(steps[first + j].finished), pin(steps[first + j].ingest_starts),
-              pin(steps[first + j].ingest_lengths)) for j in range(K)]
-    d_samp = torch.empty((cfg.B, cfg.T), dtype=torch.int32, device=dev)
-    m_max = max(1, max(x[0].numel() for x in h_fin))
-    d_rows = torch.empty(m_max, dtype=torch.int32, device=dev)
-    d_st = torch.empty(m_max, dtype=torch.int32, device=dev)
-    d_ln = torch.empty(m_max, dtype=torch.int32, device=dev)
-    h_drafts = torch.empty((cfg.B, cfg.k), dtype=torch.int32).pin_memory()
-    h_nv = torch.empty(cfg.B, dtype=torch.int32).pin_memory()
+    # the step's inputs arrive in one fixed pinned block [sampled | rows | starts |
+    # lengths] and the outputs leave through one [drafts | num_valid]: the library
+    # moves each in one copy, and the call is bound to the buffers once
+    BT = cfg.B * cfg.T
+    m = max(s.finished.shape[0] for s in steps[first:first + K]) if cfg.corpus_tokens else 0
+    assert all(s.finished.shape[0] == m for s in steps[first:first + K]) or not cfg.corpus_tokens
+    blocks = [np.concatenate([s.sampled.ravel(), s.finished[:m], s.ingest_starts[:m],
+                              s.ingest_lengths[:m]]).astype(np.int32) for s in steps[first:first + K]]
+    ingested = [int(s.ingest_lengths[:m].sum()) for s in steps[first:first + K]]
+    h_in = torch.empty(BT + 3 * m, dtype=torch.int32).pin_memory()
+    h_in_np = h_in.numpy()
+    h_out = torch.empty(cfg.B * cfg.k + cfg.B, dtype=torch.int32).pin_memory()
+    h_drafts, h_nv = h_out[:cfg.B * cfg.k].view(cfg.B, cfg.k), h_out[cfg.B * cfg.k:]
+    step_host = dr.bind_step_host(g_tok, g_n, h_in[:BT].view(cfg.B, cfg.T), h_in[BT:BT + m],
+                                  h_in[BT + m:BT + 2 * m], h_in[BT + 2 * m:], h_drafts, h_nv,
+                                  stream=stream)
     times = []
     bi = bo = 0
     for j in range(K):
@@ -432,19 +438,13 @@ def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state,
                 g_tok[idx] = torch.from_numpy(p.reset_tokens).to(dev)
                 g_n[idx] = torch.from_numpy(p.reset_n).to(dev)
         flush.fill_(j)
+        h_in_np[:] = blocks[j]       # this step's inputs land in pinned host memory
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        d_samp.copy_(h_samp[j], non_blocking=True)
-        m = h_fin[j][0].numel()
-        if m:
-            d_rows[:m].copy_(h_fin[j][0], non_blocking=True)
-            d_st[:m].copy_(h_fin[j][1], non_blocking=True)
-            d_ln[:m].copy_(h_fin[j][2], non_blocking=True)
-        if m and cfg.corpus_tokens:
-            dr.step(g_tok, g_n, d_samp, d_rows[:m], d_st[:m], d_ln[:m], out=out)
-            state["ingested"] += int(s.ingest_lengths.sum())
-        else:
-            dr.propose_with_update(g_tok, g_n, d_samp, out=out)
+        # one library call: host->device copy of the step's inputs, the fused
+        # launch, device->host copy of the drafts and valid counts
+        step_host()
+        state["ingested"] += ingested[j]
         if cfg.corpus_tokens:
             if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
                 dr.build_sa(side)
@@ -453,11 +453,9 @@ def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state,
             st, _ = dr.poll(wait=False)
             if st == 1:
                 state["pending"] = False
-        h_drafts.copy_(out.drafts, non_blocking=True)
-        h_nv.copy_(out.num_valid, non_blocking=True)
         stream.synchronize()
         times.append(time.perf_counter() - t0)
-        bi = h_samp[j].numel() * 4 + 3 * m * 4
+        bi = (BT + 3 * m) * 4
         bo = h_drafts.numel() * 4 + h_nv.numel() * 4
     if state["pending"]:
         dr.poll(wait=True)

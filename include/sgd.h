@@ -186,6 +186,23 @@ int sgd_step(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_tokens, const int32_
              float *score, float *probs, int32_t *match_info, const int32_t *rows,
              const int32_t *starts, const int32_t *lengths, int32_t n_docs, void *stream);
 
+/* sgd_step with the step's inputs and outputs in HOST memory: copies h_sampled
+ * [B, T] (and, with n_docs > 0, h_rows / h_starts / h_lengths [n_docs]) into
+ * library-owned device staging buffers, runs sgd_step on the DEVICE token_ids /
+ * num_tokens (the rows stay resident), and copies drafts [B, k] and num_valid
+ * [B] (and score [B], probs [B, k], match_info [B, 2] where the pointer is not
+ * NULL) back to host memory, all queued on `stream` in that order.  Returns
+ * once queued: the host outputs are valid after the stream is synchronised,
+ * and the host inputs must not change before then.  Host buffers should be
+ * page-locked (cudaHostAlloc / pinned) for the copies to be asynchronous.
+ * All rows are active.  Errors as sgd_step; T <= max_sampled, B <= max_batch,
+ * n_docs <= max_ingest_docs. */
+int sgd_step_host(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_tokens, const int32_t *h_sampled,
+                  int32_t T, int32_t B, const int32_t *h_rows, const int32_t *h_starts,
+                  const int32_t *h_lengths, int32_t n_docs, int32_t *h_drafts,
+                  int32_t *h_num_valid, float *h_score, float *h_probs, int32_t *h_match_info,
+                  void *stream);
+
 /* Appends finished responses to the corpus ring ([PYPI] Quickstart:
  * harvest_finished; How it works, step 4: oldest documents are evicted when
  * the ring is full; [DOCS] Model Runner V2: oldest first out).

@@ -107,6 +107,7 @@ def load() -> ctypes.CDLL:
         "sgd_propose_with_update": (ctypes.c_int, [P, P, P, P, i32, P, i32, P, P, P, P, P, P]),
         "sgd_ingest": (ctypes.c_int, [P, P, P, i32, P, P, P, i32, P]),
         "sgd_step": (ctypes.c_int, [P, P, P, P, i32, P, i32, P, P, P, P, P, P, P, P, i32, P]),
+        "sgd_step_host": (ctypes.c_int, [P, P, P, P, i32, i32, P, P, P, i32, P, P, P, P, P, P]),
         "sgd_build_sa": (ctypes.c_int, [P, P, P]),
         "sgd_poll": (ctypes.c_int, [P, ctypes.c_int, i64, P, u64p]),
         "sgd_suffix_array": (ctypes.c_int, [P, P, i64, P, P]),

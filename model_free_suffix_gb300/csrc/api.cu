@@ -37,6 +37,8 @@ struct sgd_ctx {
   uint32_t *d_build_err = nullptr;  // error bits of the build in progress
   uint32_t *d_step_ready = nullptr; // [max_batch] fused step: per-row update epoch
   uint32_t *d_step_sync = nullptr;  // fused step: epoch, arrivals
+  int32_t *d_hin = nullptr;         // sgd_step_host inputs: sampled, rows, starts, lengths
+  int32_t *d_hout = nullptr;        // sgd_step_host outputs: drafts, num_valid, score, probs, match_info
   int32_t *d_ring = nullptr;
   RingState *d_rs = nullptr;
   int64_t *d_doc_start = nullptr;
@@ -116,6 +118,8 @@ int choose_self_warps(const sgd_config &c) {
 void free_ctx(sgd_ctx *x) {
   cudaFree(x->d_err);
   cudaFree(x->d_step_ready);
+  cudaFree(x->d_hin);
+  cudaFree(x->d_hout);
   cudaFree(x->d_rec[0]);
   cudaFree(x->d_rec[1]);
   cudaFree(x->d_gt[0]);
@@ -304,6 +308,11 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
   };
   al((void **)&x->d_err, 4);
   al((void **)&x->d_build_err, 4);
+  {
+    const size_t Bm = (size_t)cfg->max_batch, kk = (size_t)cfg->k;
+    al((void **)&x->d_hin, 4 * (Bm * (size_t)cfg->max_sampled + 3 * (size_t)cfg->max_ingest_docs));
+    al((void **)&x->d_hout, 4 * (Bm * kk + Bm + Bm + Bm * kk + 2 * Bm));
+  }
   if (e == cudaSuccess) e = cudaMemset(x->d_err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(x->d_build_err, 0, 4);
   if (x->corpus) {
@@ -524,6 +533,71 @@ int sgd_step(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int32_t 
   }
   x->launches++;
   return check_cuda(launch_propose(a, (cudaStream_t)stream));
+}
+
+int sgd_step_host(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int32_t *h_sampled,
+                  int32_t T, int32_t B, const int32_t *h_rows, const int32_t *h_starts,
+                  const int32_t *h_lengths, int32_t n_docs, int32_t *h_drafts, int32_t *h_num_valid,
+                  float *h_score, float *h_probs, int32_t *h_match_info, void *stream) {
+  if (!x) return SGD_EINVAL;
+  if (B < 0 || B > x->cfg.max_batch || T < 1 || T > x->cfg.max_sampled) return SGD_EINVAL;
+  if (n_docs < 0 || n_docs > x->cfg.max_ingest_docs) return SGD_EINVAL;
+  if (B == 0) return SGD_OK;
+  if (!h_sampled || !h_drafts || !h_num_valid) return SGD_EINVAL;
+  if (n_docs > 0 && (!h_rows || !h_starts || !h_lengths)) return SGD_EINVAL;
+  const size_t k = (size_t)x->cfg.k, BT = (size_t)B * T, m = (size_t)n_docs, Bk = (size_t)B * k;
+  // device staging laid out like a host block [sampled | rows | starts | lengths]
+  // and [drafts | num_valid | score | probs | match_info], so that host buffers
+  // that sit back to back move in one copy each way
+  int32_t *d_samp = x->d_hin;
+  int32_t *d_rows = d_samp + BT, *d_starts = d_rows + m, *d_lens = d_starts + m;
+  int32_t *d_drafts = x->d_hout;
+  int32_t *d_nv = d_drafts + Bk;
+  float *d_score = reinterpret_cast<float *>(d_nv + B);
+  float *d_probs = d_score + B;
+  int32_t *d_mi = reinterpret_cast<int32_t *>(d_probs + Bk);
+  cudaStream_t st = (cudaStream_t)stream;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+  cudaError_t e;
+  if (m == 0) {
+    e = cudaMemcpyAsync(d_samp, h_sampled, BT * 4, h2d, st);
+  } else if (h_rows == h_sampled + BT && h_starts == h_rows + m && h_lengths == h_starts + m) {
+    e = cudaMemcpyAsync(d_samp, h_sampled, (BT + 3 * m) * 4, h2d, st);
+  } else {
+    e = cudaMemcpyAsync(d_samp, h_sampled, BT * 4, h2d, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_rows, h_rows, m * 4, h2d, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_starts, h_starts, m * 4, h2d, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(d_lens, h_lengths, m * 4, h2d, st);
+  }
+  if (e != cudaSuccess) return check_cuda(e);
+  const int r = sgd_step(x, token_ids, num_tokens, d_samp, T, nullptr, B, d_drafts, d_nv,
+                         h_score ? d_score : nullptr, h_probs ? d_probs : nullptr,
+                         h_match_info ? d_mi : nullptr, d_rows, d_starts, d_lens, n_docs, stream);
+  if (r != SGD_OK) return r;
+  // outputs: the longest requested run that is contiguous on the host goes in one copy
+  size_t run = Bk + B;
+  const bool nv_next = h_num_valid == h_drafts + Bk;
+  if (nv_next && h_score && (void *)h_score == (void *)(h_num_valid + B)) {
+    run += B;
+    if (h_probs && h_probs == h_score + B) {
+      run += Bk;
+      if (h_match_info && (void *)h_match_info == (void *)(h_probs + Bk)) run += 2 * (size_t)B;
+    }
+  }
+  if (nv_next) {
+    e = cudaMemcpyAsync(h_drafts, d_drafts, run * 4, d2h, st);
+  } else {
+    e = cudaMemcpyAsync(h_drafts, d_drafts, Bk * 4, d2h, st);
+    if (e == cudaSuccess) e = cudaMemcpyAsync(h_num_valid, d_nv, (size_t)B * 4, d2h, st);
+    run = Bk + B;
+  }
+  if (e == cudaSuccess && h_score && run <= Bk + B)
+    e = cudaMemcpyAsync(h_score, d_score, (size_t)B * 4, d2h, st);
+  if (e == cudaSuccess && h_probs && run <= Bk + 2 * (size_t)B)
+    e = cudaMemcpyAsync(h_probs, d_probs, Bk * 4, d2h, st);
+  if (e == cudaSuccess && h_match_info && run <= 2 * Bk + 2 * (size_t)B)
+    e = cudaMemcpyAsync(h_match_info, d_mi, (size_t)B * 8, d2h, st);
+  return check_cuda(e);
 }
 
 int sgd_ingest(sgd_ctx *x, const int32_t *token_ids, const int32_t *num_tokens, int32_t B,

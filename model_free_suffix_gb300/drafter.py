@@ -107,6 +107,17 @@ class SuffixDrafter:
             raise ValueError("%s must be a contiguous %s tensor" % (name, dtype))
         return ctypes.c_void_p(t.data_ptr())
 
+    @staticmethod
+    def _host(t: Optional[torch.Tensor], dtype=torch.int32, name="tensor") -> ctypes.c_void_p:
+        """A host (CPU) tensor's address; pinned memory keeps the copies asynchronous."""
+        if t is None:
+            return ctypes.c_void_p(0)
+        if t.is_cuda:
+            raise ValueError("%s must be a host (CPU) tensor" % name)
+        if t.dtype != dtype or not t.is_contiguous():
+            raise ValueError("%s must be a contiguous %s tensor" % (name, dtype))
+        return ctypes.c_void_p(t.data_ptr())
+
     def new_outputs(self, B: int) -> Proposal:
         d = self.device
         return Proposal(torch.empty((B, self.k), dtype=torch.int32, device=d),
@@ -166,6 +177,52 @@ class SuffixDrafter:
             self._t(rows, name="rows"), self._t(starts, name="starts"),
             self._t(lengths, name="lengths"), m, _stream_handle(stream)), "sgd_step")
         return out
+
+    def step_host(self, token_ids: torch.Tensor, num_tokens: torch.Tensor, h_sampled: torch.Tensor,
+                  h_rows: torch.Tensor, h_starts: torch.Tensor, h_lengths: torch.Tensor,
+                  h_drafts: torch.Tensor, h_num_valid: torch.Tensor,
+                  h_score: Optional[torch.Tensor] = None, h_probs: Optional[torch.Tensor] = None,
+                  h_match_info: Optional[torch.Tensor] = None, stream=None) -> None:
+        """step() with the step's inputs and outputs in host memory (pinned CPU
+        tensors): the copies, the fused launch and the read-back are queued on
+        `stream`; the host outputs are valid once that stream is synchronised."""
+        B, T = h_sampled.shape
+        m = h_rows.shape[0]
+        H = self._host
+        self._check(self._lib.sgd_step_host(
+            self._h, self._t(token_ids, name="token_ids"), self._t(num_tokens, name="num_tokens"),
+            H(h_sampled, name="h_sampled"), T, B, H(h_rows, name="h_rows"),
+            H(h_starts, name="h_starts"), H(h_lengths, name="h_lengths"), m,
+            H(h_drafts, name="h_drafts"), H(h_num_valid, name="h_num_valid"),
+            H(h_score, torch.float32, "h_score"), H(h_probs, torch.float32, "h_probs"),
+            H(h_match_info, name="h_match_info"), _stream_handle(stream)), "sgd_step_host")
+
+    def bind_step_host(self, token_ids: torch.Tensor, num_tokens: torch.Tensor,
+                       h_sampled: torch.Tensor, h_rows: torch.Tensor, h_starts: torch.Tensor,
+                       h_lengths: torch.Tensor, h_drafts: torch.Tensor, h_num_valid: torch.Tensor,
+                       h_score: Optional[torch.Tensor] = None, h_probs: Optional[torch.Tensor] = None,
+                       h_match_info: Optional[torch.Tensor] = None, stream=None):
+        """step_host on fixed buffers, with its arguments checked and marshalled
+        once: the returned function queues one step per call (new inputs are
+        written into the same host buffers between calls)."""
+        B, T = h_sampled.shape
+        H = self._host
+        fn = self._lib.sgd_step_host
+        args = (self._h, self._t(token_ids, name="token_ids"), self._t(num_tokens, name="num_tokens"),
+                H(h_sampled, name="h_sampled"), T, B, H(h_rows, name="h_rows"),
+                H(h_starts, name="h_starts"), H(h_lengths, name="h_lengths"), h_rows.shape[0],
+                H(h_drafts, name="h_drafts"), H(h_num_valid, name="h_num_valid"),
+                H(h_score, torch.float32, "h_score"), H(h_probs, torch.float32, "h_probs"),
+                H(h_match_info, name="h_match_info"), _stream_handle(stream))
+        keep = (token_ids, num_tokens, h_sampled, h_rows, h_starts, h_lengths, h_drafts, h_num_valid,
+                h_score, h_probs, h_match_info)  # the buffers outlive the bound call
+
+        def step_bound(_fn=fn, _args=args, _keep=keep):
+            st = _fn(*_args)
+            if st < 0:
+                raise L.SgdError(st, "sgd_step_host")
+
+        return step_bound
 
     # -- corpus ---------------------------------------------------------------
     def ingest(self, token_ids: torch.Tensor, rows: torch.Tensor, starts: torch.Tensor,

@@ -149,3 +149,102 @@ def test_step_wait_injection_skips_docs_and_recovers():
     assert dr.get_error() == 0
     assert dr.corpus_stats() == (10 + 1 + 12 + 1, 2)
     dr.close()
+
+
+def test_step_host_matches_device_step():
+    """sgd_step_host (host inputs and outputs, library staging) gives exactly
+    what sgd_step gives on device buffers, step after step."""
+    W, O, H = _mods()
+    from model_free_suffix_gb300 import SuffixDrafter
+    V, S, B, T, k = 97, 256, 24, 5, 8
+    rng = np.random.default_rng(21)
+    kw = dict(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=16, max_occurrences=16,
+              max_sampled=T, corpus_capacity=2048, max_docs=256)
+    A, Bd = SuffixDrafter(**kw), SuffixDrafter(**kw)
+    tok = np.zeros((B, S), dtype=np.int32)
+    n = rng.integers(40, 120, size=B).astype(np.int32)
+    base = rng.integers(0, 12, size=64)
+    for b in range(B):
+        tok[b, :n[b]] = np.resize(np.roll(base, b % 5), n[b])
+    ta, na = torch.from_numpy(tok).cuda(), torch.from_numpy(n).cuda()
+    tb, nb = ta.clone(), na.clone()
+    outa = A.new_outputs(B)
+    # outputs as views of one pinned block in the library's order (one copy back)
+    ob = torch.empty(B * k + B + B + B * k + 2 * B, dtype=torch.int32).pin_memory()
+    h_drafts, h_nv = ob[:B * k].view(B, k), ob[B * k:B * k + B]
+    h_score = ob[B * k + B:B * k + 2 * B].view(torch.float32)
+    h_probs = ob[B * k + 2 * B:2 * B * k + 2 * B].view(torch.float32).view(B, k)
+    h_mi = ob[2 * B * k + 2 * B:].view(B, 2)
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    for it in range(8):
+        samp = rng.integers(0, 12, size=(B, T)).astype(np.int32)
+        m = int(rng.integers(0, 6))
+        rows = rng.choice(B, size=m, replace=False).astype(np.int32)
+        # docs: the first 30 tokens of each row, always inside the row after the update;
+        # odd steps pass the inputs as views of one pinned block (copied at once)
+        if it % 2:
+            blk = torch.from_numpy(np.concatenate([samp.ravel(), rows, np.zeros(m, np.int32),
+                                                   np.full(m, 30, np.int32)]).astype(np.int32)).pin_memory()
+            h_samp = blk[:B * T].view(B, T)
+            h_rows, h_st, h_ln = blk[B * T:B * T + m], blk[B * T + m:B * T + 2 * m], blk[B * T + 2 * m:]
+        else:
+            h_samp = torch.from_numpy(samp).pin_memory()
+            h_rows = torch.from_numpy(rows).pin_memory()
+            h_st = torch.zeros(m, dtype=torch.int32).pin_memory()
+            h_ln = torch.full((m,), 30, dtype=torch.int32).pin_memory()
+        A.step(ta, na, h_samp.cuda(), h_rows.cuda(), h_st.cuda(), h_ln.cuda(), out=outa)
+        Bd.step_host(tb, nb, h_samp, h_rows, h_st, h_ln, h_drafts, h_nv, h_score, h_probs, h_mi,
+                     stream=stream)
+        stream.synchronize()
+        assert torch.equal(outa.drafts.cpu(), h_drafts) and torch.equal(outa.num_valid.cpu(), h_nv)
+        assert torch.equal(outa.score.cpu(), h_score) and torch.equal(outa.probs.cpu(), h_probs)
+        assert torch.equal(outa.match_info.cpu(), h_mi)
+        assert torch.equal(ta, tb) and torch.equal(na, nb)
+        assert A.corpus_stats() == Bd.corpus_stats()
+        if it % 3 == 2:
+            for d in (A, Bd):
+                d.build_sa(side)
+                assert d.poll(wait=True)[0] == 1
+    assert A.get_error() == 0 and Bd.get_error() == 0
+    A.close()
+    Bd.close()
+
+
+def test_bound_step_host_reuses_buffers():
+    """bind_step_host: one marshalled call reused over fixed pinned buffers whose
+    contents change between steps gives the same results as step()."""
+    W, O, H = _mods()
+    from model_free_suffix_gb300 import SuffixDrafter
+    V, S, B, T, k, m = 61, 128, 12, 4, 6, 3
+    rng = np.random.default_rng(33)
+    kw = dict(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=12, max_occurrences=8,
+              max_sampled=T, corpus_capacity=1024, max_docs=128)
+    A, Bd = SuffixDrafter(**kw), SuffixDrafter(**kw)
+    tok = rng.integers(0, 7, size=(B, S)).astype(np.int32)
+    n = np.full(B, 40, dtype=np.int32)
+    ta, na = torch.from_numpy(tok).cuda(), torch.from_numpy(n).cuda()
+    tb, nb = ta.clone(), na.clone()
+    outa = A.new_outputs(B)
+    h_in = torch.empty(B * T + 3 * m, dtype=torch.int32).pin_memory()
+    h_out = torch.empty(B * k + B, dtype=torch.int32).pin_memory()
+    h_drafts, h_nv = h_out[:B * k].view(B, k), h_out[B * k:]
+    stream = torch.cuda.current_stream()
+    step = Bd.bind_step_host(tb, nb, h_in[:B * T].view(B, T), h_in[B * T:B * T + m],
+                             h_in[B * T + m:B * T + 2 * m], h_in[B * T + 2 * m:], h_drafts, h_nv,
+                             stream=stream)
+    for it in range(6):
+        samp = rng.integers(0, 7, size=(B, T)).astype(np.int32)
+        rows = rng.choice(B, size=m, replace=False).astype(np.int32)
+        blk = np.concatenate([samp.ravel(), rows, np.zeros(m, np.int32), np.full(m, 20, np.int32)])
+        h_in.numpy()[:] = blk
+        d = torch.from_numpy(blk).cuda()
+        A.step(ta, na, d[:B * T].view(B, T), d[B * T:B * T + m], d[B * T + m:B * T + 2 * m],
+               d[B * T + 2 * m:], out=outa)
+        step()
+        stream.synchronize()
+        assert torch.equal(outa.drafts.cpu(), h_drafts) and torch.equal(outa.num_valid.cpu(), h_nv)
+        assert torch.equal(ta, tb) and torch.equal(na, nb)
+        assert A.corpus_stats() == Bd.corpus_stats()
+    A.close()
+    Bd.close()
