@@ -102,6 +102,12 @@ typedef struct {
                                   used only while both snapshots' tables fit in
                                   SGD_RECORD_BUDGET bytes.  0: off (descent of the key
                                   array).  Drafts are the same either way. */
+  int32_t  propose_mode;       /* 0 (default) or 1: each propose is one kernel launch
+                                  (a CTA per row scans its row while probing the
+                                  corpus).  2: two launches, the update and self match
+                                  in small CTAs (more per SM), then the corpus chain and
+                                  vote.  Drafts are the same either way; on the long-
+                                  context workload mode 1 is currently the faster. */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)

@@ -58,6 +58,7 @@ class SgdConfig(ctypes.Structure):
         ("self_warps", ctypes.c_int32),
         ("corpus_records", ctypes.c_int32),
         ("corpus_gram_index", ctypes.c_int32),
+        ("propose_mode", ctypes.c_int32),
     ]
 
 

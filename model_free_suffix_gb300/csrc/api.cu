@@ -7,6 +7,7 @@
 // finished snapshot in with a 32-byte device write ("SuffixGPU", PyPI: How it
 // works, step 4 -- rebuilt on a side stream, double-buffered, swapped in
 // place so captured CUDA graphs keep working).
+#include <algorithm>
 #include <atomic>
 #include <chrono>
 #include <condition_variable>
@@ -39,6 +40,8 @@ struct sgd_ctx {
   uint32_t *d_step_sync = nullptr;  // fused step: epoch, arrivals
   int32_t *d_hin = nullptr;         // sgd_step_host inputs: sampled, rows, starts, lengths
   int32_t *d_hout = nullptr;        // sgd_step_host outputs: drafts, num_valid, score, probs, match_info
+  int32_t *d_self_res = nullptr;    // two-launch propose: per-row self results
+  int split = 0;
   int32_t *d_ring = nullptr;
   RingState *d_rs = nullptr;
   int64_t *d_doc_start = nullptr;
@@ -103,6 +106,7 @@ int validate(const sgd_config &c) {
   if (c.self_warps < 0 || c.self_warps > MAX_SELF_WARPS) return SGD_EINVAL;
   if (c.corpus_records != 0 && c.corpus_records != 1) return SGD_EINVAL;
   if (c.corpus_gram_index != 0 && c.corpus_gram_index != 1) return SGD_EINVAL;
+  if (c.propose_mode < 0 || c.propose_mode > 2) return SGD_EINVAL;
   return SGD_OK;
 }
 
@@ -119,6 +123,7 @@ void free_ctx(sgd_ctx *x) {
   cudaFree(x->d_err);
   cudaFree(x->d_step_ready);
   cudaFree(x->d_hin);
+  cudaFree(x->d_self_res);
   cudaFree(x->d_hout);
   cudaFree(x->d_rec[0]);
   cudaFree(x->d_rec[1]);
@@ -264,6 +269,7 @@ int sgd_config_default(sgd_config *c) {
   c->corpus_cand_cap = 2048;
   c->corpus_records = 1;
   c->corpus_gram_index = 1;
+  c->propose_mode = 0;
   c->self_warps = 0;
   return SGD_OK;
 }
@@ -301,13 +307,21 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
   x->device = device;
   x->nself = choose_self_warps(*cfg);
   x->corpus = cfg->corpus_capacity > 0;
-  x->smem = propose_smem_bytes(x->nself, cfg->max_occurrences, cfg->k, cfg->corpus_cand_cap);
+  x->split = cfg->propose_mode == 2;
+  {
+    const int R = cfg->max_occurrences, k = cfg->k, cc = cfg->corpus_cand_cap;
+    x->smem = x->split ? std::max(propose_smem_bytes(1, x->nself, R, k, cc),
+                                  propose_smem_bytes(2, 1, R, k, cc))
+                       : propose_smem_bytes(0, x->nself, R, k, cc);
+  }
   cudaError_t e = cudaSuccess;
   auto al = [&](void **p, size_t bytes) {
     if (e == cudaSuccess) e = cudaMalloc(p, bytes);
   };
   al((void **)&x->d_err, 4);
   al((void **)&x->d_build_err, 4);
+  if (x->split)
+    al((void **)&x->d_self_res, (size_t)cfg->max_batch * (cfg->max_occurrences + 6) * 4);
   {
     const size_t Bm = (size_t)cfg->max_batch, kk = (size_t)cfg->k;
     al((void **)&x->d_hin, 4 * (Bm * (size_t)cfg->max_sampled + 3 * (size_t)cfg->max_ingest_docs));
@@ -425,6 +439,8 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.nself = x->nself;
   a.cand_cap = c.corpus_cand_cap;
   a.rsh = x->rsh;
+  a.split = x->split;
+  a.self_res = x->d_self_res;
   return a;
 }
 

@@ -633,7 +633,7 @@ __device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
 __device__ __forceinline__ void step_ingest(const ProposeArgs &a) {
   extern __shared__ __align__(16) int dsm[];
   __shared__ uint32_t s_e0;
-  if (threadIdx.x == 0) {
+  if (threadIdx.x == 0 && a.step_ready != nullptr) {
     const uint32_t e0 = ld_volatile_u32(&a.step_sync[0]);
     s_e0 = e0;
     step_arrive(a.step_sync, e0);
@@ -645,7 +645,13 @@ __device__ __forceinline__ void step_ingest(const ProposeArgs &a) {
   ingest_small_cta(g, *reinterpret_cast<SmallIngestSmem *>(dsm));
 }
 
+// MODE 0: the whole step in one kernel.  MODE 1 (long rows, first launch):
+// the update and the self scan only; the row's self result is written to
+// a.self_res.  MODE 2 (second launch): one warp reads that result back in
+// place of the scan, the probe warps and the vote run as in MODE 0.
+template <int MODE>
 __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) {
+  constexpr bool SELF_ONLY = MODE == 1, FROM_RES = MODE == 2;
   extern __shared__ __align__(16) int dsm[];
   __shared__ int s_wM[MAX_SELF_WARPS], s_wcnt[MAX_SELF_WARPS];
   __shared__ int s_hist[256];
@@ -660,7 +666,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
   const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
   int32_t *row = a.tok + (size_t)b * S;
-  const int big = max(a.cand_cap, R * ((k + 3) & ~3));
+  const int big = SELF_ONLY ? 0 : max(a.cand_cap, R * ((k + 3) & ~3));
   int *s_tail = dsm;                   // MAX_D
   int *s_wlist = s_tail + MAX_D;       // nself * R
   int *s_occ = s_wlist + a.nself * R;  // R
@@ -673,12 +679,13 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   int4 *s_top = reinterpret_cast<int4 *>(dsm + koff);                  // TOP_KEYS
   int4 *s_mid = s_top + TOP_KEYS;                                      // MID_KEYS
   unsigned char *s_L = reinterpret_cast<unsigned char *>(s_mid + MID_KEYS);  // LCAP
-  int4 *s_ring = reinterpret_cast<int4 *>(s_L + LCAP);                // nself * SR windows
+  // nself * SR windows; the self-only launch has no corpus areas before them
+  int4 *s_ring = SELF_ONLY ? s_top : reinterpret_cast<int4 *>(s_L + LCAP);
 
   // ---- phase 0: warp 0 updates the row; the others fetch the snapshot
   // descriptor and stage the top two levels of its key array ----
   Corpus cp{nullptr, nullptr, nullptr, nullptr, a.rsh, nullptr, 0, 0, 0, s_top, s_mid};
-  if (a.desc != nullptr) {
+  if (!SELF_ONLY && a.desc != nullptr) {
     cp.X = a.desc->text;
     cp.SA = a.desc->sa;
     cp.K = a.desc->keys;
@@ -689,7 +696,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     cp.Lmax = cp.N >= 2 ? top_level(cp.N) : 0;
   }
   if (warp == 0) {
-    const uint32_t e0 = a.ing_m > 0 && lane == 0 ? ld_volatile_u32(&a.step_sync[0]) : 0u;
+    const bool signal = a.ing_m > 0 && a.step_ready != nullptr;
+    const uint32_t e0 = signal && lane == 0 ? ld_volatile_u32(&a.step_sync[0]) : 0u;
     int n = a.ntok[b];
     uint32_t fl = 0;
     if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
@@ -699,9 +707,17 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     if (lane == 0 && a.do_update) a.ntok[b] = n;
     // When the update appended >= 4 ids, the last four tokens are those ids:
     // the probe warps can look the n-grams up before the tail is read back.
-    const bool early = a.do_update && n - n_old >= 4;
+    bool early = a.do_update && n - n_old >= 4;
     if (early && lane < 4) s_early[lane] = __ldg(a.sampled + (size_t)b * a.T + (n - n_old) - 1 - lane);
-    if (a.ing_m > 0) {  // publish the updated row to the ingest CTA
+    if (FROM_RES) {  // the first launch's result: Ms, cs, the last four tokens
+      const int32_t *res = a.self_res + (size_t)b * (R + 6);
+      const int v = lane < 6 ? __ldg(res + lane) : 0;
+      if (lane >= 2 && lane < 6) s_early[lane - 2] = v;
+      early = n >= 4;
+      const int Ms = __shfl_sync(FULL, v, 0), cs = __shfl_sync(FULL, v, 1);
+      if (lane == 0) { s_Ms = Ms; s_cs = cs; }
+    }
+    if (signal) {  // publish the updated row to the ingest CTA
       __threadfence();
       __syncwarp();
       if (lane == 0) {
@@ -716,14 +732,16 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_have_corpus = a.desc != nullptr && cp.N >= 2;
       s_self_done = 0;
       s_ms_ready = 0;
-      s_Ms = 0;
-      s_cs = 0;
+      if (!FROM_RES) {
+        s_Ms = 0;
+        s_cs = 0;
+      }
       s_Mc = 0;
       s_c0c = 0;
       s_cpf = 0;
       s_ckey = 0;
     }
-  } else if (a.desc != nullptr && cp.N >= 2 && cp.GT == nullptr) {
+  } else if (!SELF_ONLY && a.desc != nullptr && cp.N >= 2 && cp.GT == nullptr) {
     const int sh = 5 * cp.Lmax;
     const long long ntop = (cp.N + (1LL << sh) - 1) >> sh;
     const long long nmid = cp.Lmax > 0 ? (cp.N + (1LL << (sh - 5)) - 1) >> (sh - 5) : 0;
@@ -738,14 +756,16 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   int32_t *dr = a.drafts + (size_t)b * k;
   float *pr = a.probs ? a.probs + (size_t)b * k : nullptr;
   if (!((a.active == nullptr || a.active[b] != 0) && n > 0)) {
-    for (int d = tid; d < k; d += nthr) {
-      dr[d] = -1;
-      if (pr) pr[d] = 0.f;
-    }
-    if (tid == 0) {
-      a.num_valid[b] = 0;
-      if (a.score) a.score[b] = 0.f;
-      if (a.match_info) { a.match_info[2 * b] = 0; a.match_info[2 * b + 1] = 0; }
+    if constexpr (!SELF_ONLY) {  // (the self-only launch leaves the outputs to the second)
+      for (int d = tid; d < k; d += nthr) {
+        dr[d] = -1;
+        if (pr) pr[d] = 0.f;
+      }
+      if (tid == 0) {
+        a.num_valid[b] = 0;
+        if (a.score) a.score[b] = 0.f;
+        if (a.match_info) { a.match_info[2 * b] = 0; a.match_info[2 * b + 1] = 0; }
+      }
     }
     return;
   }
@@ -762,7 +782,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   SelfScan sc;
   // staged keys landed (no-op without any); a self warp's window groups,
   // committed after them, stay in flight
-  if (warp < a.nself && self_prefetch(row, n, S, warp, a.nself, lane, s_ring + warp * (SR * 32), sc))
+  if (!FROM_RES && warp < a.nself &&
+      self_prefetch(row, n, S, warp, a.nself, lane, s_ring + warp * (SR * 32), sc))
     asm volatile("cp.async.wait_group %0;" ::"n"(SPF + 1) : "memory");
   else
     asm volatile("cp.async.wait_all;" ::: "memory");
@@ -775,7 +796,17 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // tokens.  The last self warp to finish merges the self result and
   // publishes it through a shared flag; the probe warps read it at their
   // decision points to skip levels that cannot win, which only saves work.
-  if (warp < a.nself) {
+  if (FROM_RES && warp == 0) {
+    // the self result of the first launch: the most recent ends of length Ms
+    const int32_t *res = a.self_res + (size_t)b * (R + 6);
+    const int c = s_cs;
+    for (int i = lane; i < c; i += 32) s_occ[i] = __ldg(res + 6 + i);
+    __syncwarp();
+    if (lane == 0) {
+      __threadfence_block();
+      *(volatile int *)&s_ms_ready = 1;
+    }
+  } else if (!FROM_RES && warp < a.nself) {
     int Mw, cnt;
     self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, lane, sc, Mw, cnt);
     if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; }
@@ -802,6 +833,16 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         s_cs = c;
         __threadfence_block();
         *(volatile int *)&s_ms_ready = 1;
+      }
+      if (SELF_ONLY) {  // the row's self result for the second launch
+        __syncwarp();
+        int32_t *res = a.self_res + (size_t)b * (R + 6);
+        for (int i = lane; i < c; i += 32) res[6 + i] = s_occ[i];
+        if (lane < 4) res[2 + lane] = lane < dl ? s_tail[lane] : 0;
+        if (lane == 0) {
+          res[0] = Ms;
+          res[1] = c;
+        }
       }
     }
   } else if (corpus_ok) {
@@ -1067,6 +1108,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_Mc = 0;
     }
   }
+  if (SELF_ONLY) return;
   __syncthreads();
 
   // ---- the longer match wins (equal lengths: the row itself) ----
@@ -1312,26 +1354,30 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   }
 }
 
-// Two instantiations: up to 12 warps with room for two CTAs per SM, and up
-// to 20 warps with one.
-template <int MAXT, int MINB>
+// Instantiations.  One kernel per step: up to 12 warps with room for two CTAs
+// per SM, and up to 20 warps with one.  Long rows, two launches: the update
+// and self scan (self warps only, small footprint, many CTAs per SM), then
+// the corpus chain and vote (one warp + the probe warps).
+template <int MAXT, int MINB, int MODE>
 __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a) {
-  if (a.ing_m > 0) {
+  if (MODE != 1 && a.ing_m > 0) {
     if (blockIdx.x == 0) step_ingest(a);
-    else propose_body(a, blockIdx.x - 1);
+    else propose_body<MODE>(a, blockIdx.x - 1);
   } else {
-    propose_body(a, blockIdx.x);
+    propose_body<MODE>(a, blockIdx.x);
   }
 }
 
 }  // namespace
 
-size_t propose_smem_bytes(int nself, int R, int k, int cand_cap) {
-  const size_t big = (size_t)max(cand_cap, R * ((k + 3) & ~3));
+size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap) {
+  const size_t big = mode == 1 ? 0 : (size_t)max(cand_cap, R * ((k + 3) & ~3));
   const size_t boff = ((size_t)MAX_D + (size_t)nself * R + 3 * (size_t)R + 3) & ~(size_t)3;
   const size_t ints = (boff + big + 3) & ~(size_t)3;
-  const size_t bytes = sizeof(int) * ints + sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP +
-                       (size_t)nself * SR * 32 * sizeof(int4);
+  const size_t ring = (size_t)nself * SR * 32 * sizeof(int4);
+  size_t bytes = sizeof(int) * ints;
+  if (mode == 1) return bytes + ring;
+  bytes += sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP + (mode == 0 ? ring : 0);
   return bytes > sizeof(SmallIngestSmem) ? bytes : sizeof(SmallIngestSmem);
 }
 
@@ -1339,13 +1385,38 @@ int propose_step_max_docs() { return SMALL_DOCS; }
 
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   if (a.B <= 0) return cudaSuccess;
-  const int warps = a.nself + (a.desc ? NPROBE3 : 0);
-  const size_t smem = propose_smem_bytes(a.nself, a.R, a.k, a.cand_cap);
-  const int grid = a.B + (a.ing_m > 0 ? 1 : 0);
-  if (warps <= 12)
-    propose_kernel<384, 2><<<grid, 32 * warps, smem, st>>>(a);
+  const int probe = a.desc ? NPROBE3 : 0;
+  if (!a.split) {
+    const int warps = a.nself + probe;
+    const size_t smem = propose_smem_bytes(0, a.nself, a.R, a.k, a.cand_cap);
+    const int grid = a.B + (a.ing_m > 0 ? 1 : 0);
+    if (warps <= 12)
+      propose_kernel<384, 2, 0><<<grid, 32 * warps, smem, st>>>(a);
+    else
+      propose_kernel<640, 1, 0><<<grid, 32 * warps, smem, st>>>(a);
+    return cudaGetLastError();
+  }
+  // first launch: update + self scan of every row (no corpus, no ingest)
+  ProposeArgs a1 = a;
+  a1.desc = nullptr;
+  a1.ing_m = 0;
+  const size_t smem1 = propose_smem_bytes(1, a.nself, a.R, a.k, a.cand_cap);
+  if (a.nself <= 8)
+    propose_kernel<256, 3, 1><<<a.B, 32 * a.nself, smem1, st>>>(a1);
   else
-    propose_kernel<640, 1><<<grid, 32 * warps, smem, st>>>(a);
+    propose_kernel<512, 1, 1><<<a.B, 32 * a.nself, smem1, st>>>(a1);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // second launch: corpus chain and vote; the rows are updated already, so the
+  // ingest CTA needs no signal from them
+  ProposeArgs a2 = a;
+  a2.do_update = 0;
+  a2.nself = 1;
+  a2.step_ready = nullptr;
+  a2.step_sync = nullptr;
+  const size_t smem2 = propose_smem_bytes(2, 1, a.R, a.k, a.cand_cap);
+  const int grid2 = a.B + (a.ing_m > 0 ? 1 : 0);
+  propose_kernel<128, 3, 2><<<grid2, 32 * (1 + probe), smem2, st>>>(a2);
   return cudaGetLastError();
 }
 
@@ -1357,11 +1428,15 @@ cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, i
 }
 
 cudaError_t propose_set_smem_limit(size_t bytes) {
-  cudaError_t e = cudaFuncSetAttribute(propose_kernel<384, 2>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
-  if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(propose_kernel<640, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              (int)bytes);
+  // every instantiation may be launched with up to `bytes` of dynamic shared memory
+  const void *fns[] = {(const void *)propose_kernel<384, 2, 0>, (const void *)propose_kernel<640, 1, 0>,
+                       (const void *)propose_kernel<256, 3, 1>, (const void *)propose_kernel<512, 1, 1>,
+                       (const void *)propose_kernel<128, 3, 2>};
+  for (const void *f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace sgd

@@ -108,10 +108,15 @@ struct ProposeArgs {
   uint32_t *step_ready;  // [max_batch] per row: the step epoch once updated
   uint32_t *step_sync;   // [0] step epoch, [1] CTAs arrived in this launch
   uint32_t ing_skew;     // added to the awaited epoch (0; 1 only under test injection)
+  // split launch (long rows): the self kernel writes per row, at self_res + b *
+  // (R + 6): Ms, cs, the last four tokens, then the cs most recent ends; the
+  // corpus kernel reads them back instead of scanning
+  int32_t *self_res;
+  int split;             // 0: one fused kernel; 1: self kernel + corpus kernel
 };
 
 // propose.cu
-size_t propose_smem_bytes(int nself, int R, int k, int cand_cap);
+size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap);  // mode as the kernel's
 int propose_step_max_docs();  // largest doc count a fused step ingests in-kernel
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st);
 cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, int B,

@@ -112,8 +112,9 @@ SELF_GRID = [
 ]
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["one-launch", "two-launch"])
 @pytest.mark.parametrize("grid", SELF_GRID, ids=lambda g: "V%d_S%d_k%d_D%d_R%d" % g[:5])
-def test_fuzz_self(grid):
+def test_fuzz_self(grid, mode):
     SuffixDrafter, W, O, H = _mods()
     V, S, k, D, R, f, off, mp, dsc, sw = grid
     rng = np.random.default_rng(hash(grid) & 0xffff)
@@ -134,7 +135,7 @@ def test_fuzz_self(grid):
         n[b] = nb
     dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=D,
                        max_occurrences=R, max_spec_factor=f, max_spec_offset=off, min_token_prob=mp,
-                       depth_sum_cap=dsc, self_warps=sw)
+                       depth_sum_cap=dsc, self_warps=sw, propose_mode=mode)
     active = (rng.random(B) < 0.9).astype(np.uint8)
     out = dr.propose(_dev(tok), _dev(n), active=_dev(active, torch.uint8))
     p = O.Params(S=S, V=V, k=k, D=D, R=R, factor=f, offset=off, min_prob=mp, depth_sum_cap=dsc)
@@ -155,14 +156,15 @@ CORPUS_GRID = [
 
 
 # snapshot indexes: (records, n-gram table); drafts must be the same for each
-INDEX_MODES = [(1, 1), (1, 0), (0, 0)]
-INDEX_IDS = ["records+grams", "records+descent", "text+descent"]
+INDEX_MODES = [(1, 1, 1), (1, 0, 1), (0, 0, 1), (1, 1, 2), (0, 0, 2)]
+INDEX_IDS = ["records+grams", "records+descent", "text+descent", "records+grams-2launch",
+             "text+descent-2launch"]
 
 
 @pytest.mark.parametrize("mode", INDEX_MODES, ids=INDEX_IDS)
 @pytest.mark.parametrize("grid", CORPUS_GRID, ids=lambda g: "V%d_D%d_R%d_cap%d" % (g[0], g[1], g[2], g[4]))
 def test_fuzz_corpus(grid, mode):
-    records, grams = mode
+    records, grams, launches = mode
     SuffixDrafter, W, O, H = _mods()
     V, D, R, k, cc, nd, dl = grid
     rng = np.random.default_rng(sum(grid))
@@ -187,7 +189,7 @@ def test_fuzz_corpus(grid, mode):
     dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=D,
                        max_occurrences=R, corpus_capacity=max(1024, len(X)), corpus_cand_cap=cc,
                        max_spec_factor=(2, 1), min_token_prob=(1, 8), corpus_records=records,
-                       corpus_gram_index=grams)
+                       corpus_gram_index=grams, propose_mode=launches)
     _ingest_text(dr, X, V, S)
     dr.build_sa(torch.cuda.Stream())
     assert dr.poll(wait=True)[0] == 1
@@ -256,7 +258,8 @@ def test_small_p4_interval_long_matches(R, mode):
     n = np.array([12, 10, 26], dtype=np.int32)
     dr = SuffixDrafter(max_batch=3, seq_capacity=S, vocab_size=V, k=8, max_tree_depth=24,
                        max_occurrences=R, corpus_capacity=len(X), min_token_prob=(1, 20),
-                       max_docs=4096, corpus_records=mode[0], corpus_gram_index=mode[1])
+                       max_docs=4096, corpus_records=mode[0], corpus_gram_index=mode[1],
+                       propose_mode=mode[2])
     _ingest_text(dr, X, V, S)
     dr.build_sa(torch.cuda.Stream())
     assert dr.poll(wait=True)[0] == 1

@@ -31,12 +31,14 @@ def _ring_matches(ls):
     assert (live, nd) == (ls.ring.live, ls.ring.ndocs)
 
 
+@pytest.mark.parametrize("mode", [1, 2], ids=["one-launch", "two-launch"])
 @pytest.mark.parametrize("finish_frac", [0.1, 0.6])
-def test_fused_step_matches_oracle(finish_frac):
+def test_fused_step_matches_oracle(finish_frac, mode):
     """0.1: a few docs per step (in-kernel ingest); 0.6: more than 32 docs (two calls)."""
     W, O, H = _mods()
     cfg = dataclasses.replace(W.CONFIGS["c3"], rebuild_tokens=2048)
-    ls = H.Lockstep(cfg, seed=3, B=64, steps=14, finish_frac=finish_frac, corpus=1 << 16, fused=True)
+    ls = H.Lockstep(cfg, seed=3, B=64, steps=14, finish_frac=finish_frac, corpus=1 << 16, fused=True,
+                    drafter_over=dict(propose_mode=mode))
     ls.prefill(seed=3)
     docs = 0
     for _ in range(14):
@@ -52,7 +54,8 @@ def test_fused_step_matches_oracle(finish_frac):
     ls.close()
 
 
-def test_fused_step_graph_replays():
+@pytest.mark.parametrize("mode", [1, 2], ids=["one-launch", "two-launch"])
+def test_fused_step_graph_replays(mode):
     """One captured sgd_step replayed with new inputs staged into its buffers:
     every replay must wait for its own rows' updates (fresh epoch per launch)."""
     W, O, H = _mods()
@@ -61,7 +64,8 @@ def test_fused_step_graph_replays():
     rng = np.random.default_rng(11)
     C = 2048
     dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=8, max_tree_depth=16,
-                       max_occurrences=16, max_sampled=T, corpus_capacity=C, max_docs=256)
+                       max_occurrences=16, max_sampled=T, corpus_capacity=C, max_docs=256,
+                       propose_mode=mode)
     ring = O.Ring(C, 256, V)
     p = O.Params(S=S, V=V, k=8, D=16, R=16)
     tok = np.zeros((B, S), dtype=np.int32)
