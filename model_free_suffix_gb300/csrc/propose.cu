@@ -56,83 +56,6 @@ __device__ __forceinline__ void cp_async16(void *smem, const void *gmem) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa), "l"(gmem) : "memory");
 }
 
-// value of component `vc`/`vp` held by lane `src` of the current window, or
-// of the window below it when src < 0 (src >= -32)
-__device__ __forceinline__ int pick(int vc, int vp, int src) {
-  const int a = __shfl_sync(FULL, vc, src & 31);
-  const int b = __shfl_sync(FULL, vp, src & 31);
-  return src >= 0 ? a : b;
-}
-
-// Tokens at positions (4*lane + c) - i, c = 0..3, relative to the window
-// start, for 1 <= i <= 127.
-__device__ __forceinline__ void shifted(const int4 &c, const int4 &p, int lane, int i, int &v0,
-                                        int &v1, int &v2, int &v3) {
-  const int q = i >> 2;
-  const int sA = lane - q, sB = lane - q - 1;
-  switch (i & 3) {
-    case 0:
-      v0 = pick(c.x, p.x, sA); v1 = pick(c.y, p.y, sA); v2 = pick(c.z, p.z, sA); v3 = pick(c.w, p.w, sA);
-      break;
-    case 1:
-      v0 = pick(c.w, p.w, sB); v1 = pick(c.x, p.x, sA); v2 = pick(c.y, p.y, sA); v3 = pick(c.z, p.z, sA);
-      break;
-    case 2:
-      v0 = pick(c.z, p.z, sB); v1 = pick(c.w, p.w, sB); v2 = pick(c.x, p.x, sA); v3 = pick(c.y, p.y, sA);
-      break;
-    default:
-      v0 = pick(c.y, p.y, sB); v1 = pick(c.z, p.z, sB); v2 = pick(c.w, p.w, sB); v3 = pick(c.x, p.x, sA);
-      break;
-  }
-}
-
-// One 128-token window of the self match.  L(j) for the 4 ends j this lane
-// holds: the length of the common run of t[j-i] and tail[i] = t[n-1-i],
-// bounded by D and by j + 1; ends j >= J = n - 1 do not count.  Keeps the
-// warp's running maximum Mw and its most recent ends (descending) in `list`.
-__device__ __forceinline__ void self_window(int wi, const int4 &cur, const int4 &prv, int lane,
-                                            int J, int D, const int *s_tail, int t0, int R,
-                                            int *list, int &Mw, int &cnt) {
-  const int base = wi * WIN + 4 * lane;
-  bool a0 = cur.x == t0 && base + 0 < J;
-  bool a1 = cur.y == t0 && base + 1 < J;
-  bool a2 = cur.z == t0 && base + 2 < J;
-  bool a3 = cur.w == t0 && base + 3 < J;
-  if (!__any_sync(FULL, a0 | a1 | a2 | a3)) return;
-  int L0 = a0, L1 = a1, L2 = a2, L3 = a3;
-  for (int i = 1; i < D; ++i) {
-    const int ti = s_tail[i];
-    int v0, v1, v2, v3;
-    shifted(cur, prv, lane, i, v0, v1, v2, v3);
-    a0 = a0 && base + 0 >= i && v0 == ti;
-    a1 = a1 && base + 1 >= i && v1 == ti;
-    a2 = a2 && base + 2 >= i && v2 == ti;
-    a3 = a3 && base + 3 >= i && v3 == ti;
-    L0 += a0; L1 += a1; L2 += a2; L3 += a3;
-    if (!__any_sync(FULL, a0 | a1 | a2 | a3)) break;
-  }
-  const int lm = max(max(L0, L1), max(L2, L3));
-  const int wm = (int)__reduce_max_sync(FULL, (unsigned)lm);
-  if (wm > Mw) { Mw = wm; cnt = 0; }
-  if (wm == Mw && cnt < R) {
-    const int f0 = L0 == wm, f1 = L1 == wm, f2 = L2 == wm, f3 = L3 == wm;
-    const int q = f0 + f1 + f2 + f3;
-    int x = q;  // inclusive suffix sum over lanes >= lane
-#pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const int y = __shfl_down_sync(FULL, x, off);
-      if (lane + off < 32) x += y;
-    }
-    const int total = __shfl_sync(FULL, x, 0);
-    int slot = cnt + (x - q);
-    if (f3) { if (slot < R) list[slot] = base + 3; ++slot; }
-    if (f2) { if (slot < R) list[slot] = base + 2; ++slot; }
-    if (f1) { if (slot < R) list[slot] = base + 1; ++slot; }
-    if (f0) { if (slot < R) list[slot] = base + 0; ++slot; }
-    cnt = min(R, cnt + total);
-  }
-}
-
 // The windows of warp w: [wlo, whi], scanned from the top down (most recent
 // first).  They stream through a per-warp ring of SR 512-byte slots in shared
 // memory, filled with cp.async: each lane copies (and later reads) only its
@@ -180,20 +103,112 @@ __device__ __forceinline__ bool self_prefetch(const int32_t *row, int n, int S, 
   return true;
 }
 
+// L(j) for an end j whose last two tokens already match (t[j] = tail[0],
+// t[j-1] = tail[1]): lane i compares t[j-1-i] with tail[1+i], 32 depths per
+// round, from the window pair [prv | cur] in the ring (the comparisons reach
+// back at most 127 positions, never past prv).  tail1 = tail[1 + lane].
+__device__ __forceinline__ int self_extend(int j, int base, const int *cw, const int *pw, int D,
+                                          const int *s_tail, int tail1, int lane) {
+  int L = 1;
+  for (int r = 0; r < 4; ++r) {
+    const int i = 32 * r + lane;
+    const int p = j - 1 - i;
+    bool ok = false;
+    if (i + 1 < D && p >= 0) {
+      const int rel = p - (base - WIN);
+      const int v = rel >= WIN ? cw[rel - WIN] : pw[rel];
+      ok = v == (r == 0 ? tail1 : s_tail[1 + i]);
+    }
+    const unsigned mis = __ballot_sync(FULL, !ok);
+    if (mis) return L + __ffs(mis) - 1;
+    L += 32;
+  }
+  return L;
+}
+
+// The warp's windows, most recent first.  Ends with L >= 1 are exactly the
+// positions holding tail[0] = t0; those with L >= 2 also hold tail[1] just
+// before.  Each lane holds four consecutive tokens of a window (its own 16
+// bytes of the ring slot), so a window without t0 costs one load, four
+// compares and a vote.  Otherwise the R most recent t0 positions are kept
+// (list1: the answer when no end matches two tokens) and every (t1, t0)
+// position, most recent first, is extended by self_extend into (Mw, list).
 __device__ void self_process(const int32_t *row, int n, int S, int D, int R, const int *s_tail,
-                             int *list, int lane, SelfScan &sc, int &Mw, int &cnt) {
+                             int *list, int *list1, int lane, SelfScan &sc, int &Mw, int &cnt,
+                             int &cnt1) {
   Mw = 0;
   cnt = 0;
+  cnt1 = 0;
   if (sc.whi < sc.wlo) return;
   const int J = n - 1;
   const int t0 = s_tail[0];
+  const bool two = D >= 2 && n >= 2;
+  const int t1 = two ? s_tail[1] : 0;
+  const int tail1 = lane + 1 < min(D, n) ? s_tail[1 + lane] : 0;
   for (int wi = sc.whi, q = 0; wi >= sc.wlo; --wi, ++q) {
     // keep SPF windows in flight; then windows q and q + 1 must have landed
     self_fetch(row, wi - SPF - 1, lane, S, sc.ring, (q + SPF + 1) % SR);
     asm volatile("cp.async.wait_group %0;" ::"n"(SPF) : "memory");
     const int4 cur = sc.ring[(q % SR) * 32 + lane];
-    const int4 prv = sc.ring[((q + 1) % SR) * 32 + lane];
-    self_window(wi, cur, prv, lane, J, D, s_tail, t0, R, list, Mw, cnt);
+    const int base = wi * WIN, p0 = base + 4 * lane;
+    const bool a0 = cur.x == t0 && p0 < J, a1 = cur.y == t0 && p0 + 1 < J;
+    const bool a2 = cur.z == t0 && p0 + 2 < J, a3 = cur.w == t0 && p0 + 3 < J;
+    if (__any_sync(FULL, a0 | a1 | a2 | a3)) {
+      // t0 positions, most recent first: higher lanes, then higher components
+      if (cnt1 < R) {
+        const int mine = (int)a0 + (int)a1 + (int)a2 + (int)a3;
+        int x = mine;  // over lanes >= this one
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+          const int y = __shfl_down_sync(FULL, x, off);
+          if (lane + off < 32) x += y;
+        }
+        const int total = __shfl_sync(FULL, x, 0);
+        int slot = cnt1 + x - mine;
+        if (a3) { if (slot < R) list1[slot] = p0 + 3; ++slot; }
+        if (a2) { if (slot < R) list1[slot] = p0 + 2; ++slot; }
+        if (a1) { if (slot < R) list1[slot] = p0 + 1; ++slot; }
+        if (a0) { if (slot < R) list1[slot] = p0; }
+        cnt1 = min(R, cnt1 + total);
+      }
+      // (t1, t0) positions: the token before position p0 is the previous
+      // lane's last one, or the last token of the window below for lane 0
+      const int4 prv = sc.ring[((q + 1) % SR) * 32 + lane];
+      const int up = __shfl_up_sync(FULL, cur.w, 1);
+      const int below = __shfl_sync(FULL, prv.w, 31);
+      const int before0 = lane == 0 ? below : up;
+      unsigned m0 = __ballot_sync(FULL, a0 && two && p0 >= 1 && before0 == t1);
+      unsigned m1 = __ballot_sync(FULL, a1 && two && cur.x == t1);
+      unsigned m2 = __ballot_sync(FULL, a2 && two && cur.y == t1);
+      unsigned m3 = __ballot_sync(FULL, a3 && two && cur.z == t1);
+      if (m0 | m1 | m2 | m3) {
+        __syncwarp();  // every lane's copies visible to the warp (self_extend reads across lanes)
+        const int *cw = reinterpret_cast<const int *>(sc.ring + (q % SR) * 32);
+        const int *pw = reinterpret_cast<const int *>(sc.ring + ((q + 1) % SR) * 32);
+        for (;;) {  // candidates in descending position 4 * lane + c
+          int best = -1;
+          if (m0) best = 4 * (31 - __clz(m0));
+          if (m1) best = max(best, 4 * (31 - __clz(m1)) + 1);
+          if (m2) best = max(best, 4 * (31 - __clz(m2)) + 2);
+          if (m3) best = max(best, 4 * (31 - __clz(m3)) + 3);
+          if (best < 0) break;
+          const unsigned keep = ~(1u << (best >> 2));
+          const int bc = best & 3;
+          m0 = bc == 0 ? m0 & keep : m0;
+          m1 = bc == 1 ? m1 & keep : m1;
+          m2 = bc == 2 ? m2 & keep : m2;
+          m3 = bc == 3 ? m3 & keep : m3;
+          const int jj = base + best;
+          const int L = self_extend(jj, base, cw, pw, D, s_tail, tail1, lane);
+          if (L > Mw) { Mw = L; cnt = 0; }
+          if (L == Mw && cnt < R) {
+            if (lane == 0) list[cnt] = jj;
+            ++cnt;
+          }
+        }
+        __syncwarp();  // cross-lane reads of the slot done before it is refilled
+      }
+    }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of the ring left in flight
 }
@@ -653,7 +668,7 @@ template <int MODE>
 __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) {
   constexpr bool SELF_ONLY = MODE == 1, FROM_RES = MODE == 2;
   extern __shared__ __align__(16) int dsm[];
-  __shared__ int s_wM[MAX_SELF_WARPS], s_wcnt[MAX_SELF_WARPS];
+  __shared__ int s_wM[MAX_SELF_WARPS], s_wcnt[MAX_SELF_WARPS], s_wcnt1[MAX_SELF_WARPS];
   __shared__ int s_hist[256];
   __shared__ int s_lhist[MAX_D + 1];
   __shared__ int s_vv[MAX_R];
@@ -668,12 +683,13 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   int32_t *row = a.tok + (size_t)b * S;
   const int big = SELF_ONLY ? 0 : max(a.cand_cap, R * ((k + 3) & ~3));
   int *s_tail = dsm;                   // MAX_D
-  int *s_wlist = s_tail + MAX_D;       // nself * R
-  int *s_occ = s_wlist + a.nself * R;  // R
+  int *s_wlist = s_tail + MAX_D;       // nself * R: per warp, ends matching >= 2 tokens
+  int *s_wlist1 = s_wlist + a.nself * R;  // nself * R: per warp, the t0 positions
+  int *s_occ = s_wlist1 + a.nself * R; // R
   int *s_run = s_occ + R;              // R
   int *s_occc = s_run + R;             // R (corpus ends)
   // s_big and everything after it start on 16-byte boundaries (int4 access)
-  const int boff = (MAX_D + a.nself * R + 3 * R + 3) & ~3;
+  const int boff = (MAX_D + 2 * a.nself * R + 3 * R + 3) & ~3;
   int *s_big = dsm + boff;             // max(cand_cap, R * roundup4(k))
   const int koff = (boff + big + 3) & ~3;
   int4 *s_top = reinterpret_cast<int4 *>(dsm + koff);                  // TOP_KEYS
@@ -807,9 +823,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       *(volatile int *)&s_ms_ready = 1;
     }
   } else if (!FROM_RES && warp < a.nself) {
-    int Mw, cnt;
-    self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, lane, sc, Mw, cnt);
-    if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; }
+    int Mw, cnt, cnt1;
+    self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, s_wlist1 + warp * R, lane, sc, Mw, cnt,
+                 cnt1);
+    if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; s_wcnt1[warp] = cnt1; }
     __threadfence_block();
     __syncwarp();
     int last = 0;
@@ -827,6 +844,13 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
           for (int i = lane; i < mm; i += 32) s_occ[c + i] = s_wlist[w * R + i];
           c += mm;
         }
+      } else {  // no end matches two tokens: the ends are the t0 positions (L = 1)
+        for (int w = a.nself - 1; w >= 0 && c < R; --w) {
+          const int mm = min(s_wcnt1[w], R - c);
+          for (int i = lane; i < mm; i += 32) s_occ[c + i] = s_wlist1[w * R + i];
+          c += mm;
+        }
+        if (c > 0) Ms = 1;
       }
       if (lane == 0) {
         s_Ms = Ms;
@@ -1372,7 +1396,7 @@ __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a
 
 size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap) {
   const size_t big = mode == 1 ? 0 : (size_t)max(cand_cap, R * ((k + 3) & ~3));
-  const size_t boff = ((size_t)MAX_D + (size_t)nself * R + 3 * (size_t)R + 3) & ~(size_t)3;
+  const size_t boff = ((size_t)MAX_D + 2 * (size_t)nself * R + 3 * (size_t)R + 3) & ~(size_t)3;
   const size_t ints = (boff + big + 3) & ~(size_t)3;
   const size_t ring = (size_t)nself * SR * 32 * sizeof(int4);
   size_t bytes = sizeof(int) * ints;
