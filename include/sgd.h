@@ -199,9 +199,11 @@ int sgd_step(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_tokens, const int32_
  * [B] (and score [B], probs [B, k], match_info [B, 2] where the pointer is not
  * NULL) back to host memory, all queued on `stream` in that order.  Returns
  * once queued: the host outputs are valid after the stream is synchronised,
- * and the host inputs must not change before then.  Host buffers should be
- * page-locked (cudaHostAlloc / pinned) for the copies to be asynchronous.
- * All rows are active.  Errors as sgd_step; T <= max_sampled, B <= max_batch,
+ * and the host inputs must not change before then.  When every given host
+ * buffer is page-locked and mapped (cudaHostAlloc / pinned memory on a
+ * unified-address system) no staging copy is made: the kernel reads the inputs
+ * and writes the outputs in host memory in place.  Otherwise (e.g. pageable
+ * memory) the copies go through the device staging buffers.  All rows are active.  Errors as sgd_step; T <= max_sampled, B <= max_batch,
  * n_docs <= max_ingest_docs. */
 int sgd_step_host(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_tokens, const int32_t *h_sampled,
                   int32_t T, int32_t B, const int32_t *h_rows, const int32_t *h_starts,

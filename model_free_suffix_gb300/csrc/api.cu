@@ -41,6 +41,10 @@ struct sgd_ctx {
   int32_t *d_hin = nullptr;         // sgd_step_host inputs: sampled, rows, starts, lengths
   int32_t *d_hout = nullptr;        // sgd_step_host outputs: drafts, num_valid, score, probs, match_info
   int32_t *d_self_res = nullptr;    // two-launch propose: per-row self results
+  // sgd_step_host: the last set of host buffers checked for in-place access
+  const void *zc_key[9] = {};
+  void *zc_dev[9] = {};
+  bool zc_ok = false;
   int split = 0;
   int32_t *d_ring = nullptr;
   RingState *d_rs = nullptr;
@@ -562,6 +566,40 @@ int sgd_step_host(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int
   if (!h_sampled || !h_drafts || !h_num_valid) return SGD_EINVAL;
   if (n_docs > 0 && (!h_rows || !h_starts || !h_lengths)) return SGD_EINVAL;
   const size_t k = (size_t)x->cfg.k, BT = (size_t)B * T, m = (size_t)n_docs, Bk = (size_t)B * k;
+  // In place: when every host buffer is page-locked and mapped into the GPU's
+  // address space (cudaHostAlloc, pinned torch tensors), the kernel reads the
+  // step's inputs and writes its outputs in host memory directly, over the
+  // GPU's coherent link to it; no staging copies.  Checked once per set of
+  // buffers.
+  {
+    const void *key[9] = {h_sampled, h_rows, h_starts, h_lengths, h_drafts, h_num_valid, h_score,
+                          h_probs, h_match_info};
+    bool same = true;
+    for (int i = 0; i < 9; ++i) same = same && key[i] == x->zc_key[i];
+    if (!same) {
+      bool ok = true;
+      for (int i = 0; i < 9; ++i) {
+        x->zc_key[i] = key[i];
+        x->zc_dev[i] = nullptr;
+        if (key[i] == nullptr) continue;
+        cudaPointerAttributes at{};
+        if (cudaPointerGetAttributes(&at, key[i]) != cudaSuccess || at.type != cudaMemoryTypeHost ||
+            at.devicePointer == nullptr) {
+          cudaGetLastError();
+          ok = false;
+          continue;
+        }
+        x->zc_dev[i] = at.devicePointer;
+      }
+      x->zc_ok = ok;
+    }
+    if (x->zc_ok) {
+      void **d = x->zc_dev;
+      return sgd_step(x, token_ids, num_tokens, (const int32_t *)d[0], T, nullptr, B, (int32_t *)d[4],
+                      (int32_t *)d[5], (float *)d[6], (float *)d[7], (int32_t *)d[8],
+                      (const int32_t *)d[1], (const int32_t *)d[2], (const int32_t *)d[3], n_docs, stream);
+    }
+  }
   // device staging laid out like a host block [sampled | rows | starts | lengths]
   // and [drafts | num_valid | score | probs | match_info], so that host buffers
   // that sit back to back move in one copy each way

@@ -724,7 +724,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     // When the update appended >= 4 ids, the last four tokens are those ids:
     // the probe warps can look the n-grams up before the tail is read back.
     bool early = a.do_update && n - n_old >= 4;
-    if (early && lane < 4) s_early[lane] = __ldg(a.sampled + (size_t)b * a.T + (n - n_old) - 1 - lane);
+    // (plain loads: `sampled` may be page-locked host memory read in place)
+    if (early && lane < 4) s_early[lane] = a.sampled[(size_t)b * a.T + (n - n_old) - 1 - lane];
     if (FROM_RES) {  // the first launch's result: Ms, cs, the last four tokens
       const int32_t *res = a.self_res + (size_t)b * (R + 6);
       const int v = lane < 6 ? __ldg(res + lane) : 0;

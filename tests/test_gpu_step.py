@@ -155,11 +155,14 @@ def test_step_wait_injection_skips_docs_and_recovers():
     dr.close()
 
 
-def test_step_host_matches_device_step():
-    """sgd_step_host (host inputs and outputs, library staging) gives exactly
-    what sgd_step gives on device buffers, step after step."""
+@pytest.mark.parametrize("pinned", [True, False], ids=["pinned-in-place", "pageable-staged"])
+def test_step_host_matches_device_step(pinned):
+    """sgd_step_host gives exactly what sgd_step gives on device buffers, step
+    after step: with page-locked host buffers the kernel reads and writes them
+    in place, with pageable ones the library stages copies."""
     W, O, H = _mods()
     from model_free_suffix_gb300 import SuffixDrafter
+    pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
     V, S, B, T, k = 97, 256, 24, 5, 8
     rng = np.random.default_rng(21)
     kw = dict(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=16, max_occurrences=16,
@@ -173,8 +176,8 @@ def test_step_host_matches_device_step():
     ta, na = torch.from_numpy(tok).cuda(), torch.from_numpy(n).cuda()
     tb, nb = ta.clone(), na.clone()
     outa = A.new_outputs(B)
-    # outputs as views of one pinned block in the library's order (one copy back)
-    ob = torch.empty(B * k + B + B + B * k + 2 * B, dtype=torch.int32).pin_memory()
+    # outputs as views of one host block in the library's order (one copy back when staged)
+    ob = pin(torch.empty(B * k + B + B + B * k + 2 * B, dtype=torch.int32))
     h_drafts, h_nv = ob[:B * k].view(B, k), ob[B * k:B * k + B]
     h_score = ob[B * k + B:B * k + 2 * B].view(torch.float32)
     h_probs = ob[B * k + 2 * B:2 * B * k + 2 * B].view(torch.float32).view(B, k)
@@ -186,17 +189,17 @@ def test_step_host_matches_device_step():
         m = int(rng.integers(0, 6))
         rows = rng.choice(B, size=m, replace=False).astype(np.int32)
         # docs: the first 30 tokens of each row, always inside the row after the update;
-        # odd steps pass the inputs as views of one pinned block (copied at once)
+        # odd steps pass the inputs as views of one host block (moved at once when staged)
         if it % 2:
-            blk = torch.from_numpy(np.concatenate([samp.ravel(), rows, np.zeros(m, np.int32),
-                                                   np.full(m, 30, np.int32)]).astype(np.int32)).pin_memory()
+            blk = pin(torch.from_numpy(np.concatenate([samp.ravel(), rows, np.zeros(m, np.int32),
+                                                       np.full(m, 30, np.int32)]).astype(np.int32)))
             h_samp = blk[:B * T].view(B, T)
             h_rows, h_st, h_ln = blk[B * T:B * T + m], blk[B * T + m:B * T + 2 * m], blk[B * T + 2 * m:]
         else:
-            h_samp = torch.from_numpy(samp).pin_memory()
-            h_rows = torch.from_numpy(rows).pin_memory()
-            h_st = torch.zeros(m, dtype=torch.int32).pin_memory()
-            h_ln = torch.full((m,), 30, dtype=torch.int32).pin_memory()
+            h_samp = pin(torch.from_numpy(samp))
+            h_rows = pin(torch.from_numpy(rows))
+            h_st = pin(torch.zeros(m, dtype=torch.int32))
+            h_ln = pin(torch.full((m,), 30, dtype=torch.int32))
         A.step(ta, na, h_samp.cuda(), h_rows.cuda(), h_st.cuda(), h_ln.cuda(), out=outa)
         Bd.step_host(tb, nb, h_samp, h_rows, h_st, h_ln, h_drafts, h_nv, h_score, h_probs, h_mi,
                      stream=stream)
