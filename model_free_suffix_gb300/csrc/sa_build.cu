@@ -39,7 +39,7 @@ constexpr int OS_THREADS = 256;
 constexpr int OS_ITEMS = 8;
 constexpr int OS_TILE = OS_THREADS * OS_ITEMS;  // 2048 items per tile
 constexpr int RADIX = 256;
-constexpr unsigned SPIN_LIMIT = 1u << 18;  // ~0.1 s of polling; a normal wait is microseconds
+constexpr unsigned SPIN_LIMIT = 1u << 18;  // polls (backing off to 256 ns): ~0.2 s; a normal wait is microseconds
 constexpr int MAX_PASSES = 250;            // ticket counters per build
 constexpr int LB = 8;                      // look-back words a thread reads per round trip
 
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(OS_THREADS) k_onesweep(const uint64_t *kin, co
       t -= used;
       if (used == 0) {
         if (++spins > SPIN_LIMIT) { failed = true; break; }
-        if (spins > 64) __nanosleep(32);
+        if (spins > 2) __nanosleep(spins < 8 ? 64 : 256);  // back off: polls cost issue slots
       }
     }
     if (failed) atomicOr(err, SGD_ERR_LOOKBACK);
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(OS_THREADS) k_post(const int32_t *act, long lo
         t -= used;
         if (used == 0) {
           if (++spins > SPIN_LIMIT) { failed = true; break; }
-          if (spins > 64) __nanosleep(32);
+          if (spins > 2) __nanosleep(spins < 8 ? 64 : 256);  // back off: polls cost issue slots
         }
       }
       if (lane == 0) {
