@@ -86,6 +86,10 @@ def lib():
         _lib.orc_ring_ndocs.argtypes = [P]
         _lib.orc_ring_snapshot.restype = i64
         _lib.orc_ring_snapshot.argtypes = [P, P]
+        _lib.orc_ring_pushed.restype = i64
+        _lib.orc_ring_pushed.argtypes = [P]
+        _lib.orc_ring_delta.restype = i64
+        _lib.orc_ring_delta.argtypes = [P, i64, i64, P]
     return _lib
 
 
@@ -260,3 +264,23 @@ class Ring:
         X = np.zeros(max(self.live, 1), dtype=np.int32)
         n = lib().orc_ring_snapshot(self._h, _p(X))
         return X[:n].copy()
+
+    @property
+    def pushed(self) -> int:
+        return int(lib().orc_ring_pushed(self._h))
+
+    def delta(self, since: int, cap: int) -> np.ndarray:
+        """Docs not yet indexed by a snapshot taken at pushed == since, cut at cap tokens."""
+        Y = np.zeros(max(min(int(cap), self.live), 1), dtype=np.int32)
+        n = lib().orc_ring_delta(self._h, int(since), int(cap), _p(Y))
+        return Y[:n].copy()
+
+
+def corpus_text(X: Optional[np.ndarray], Y: Optional[np.ndarray]) -> Optional[np.ndarray]:
+    """The text a row is matched against: the snapshot, then the not-yet-indexed
+    docs ([PYPI] How it works, step 2: the suffix array plus a brute-force scan
+    of the delta buffer)."""
+    parts = [a for a in (X, Y) if a is not None and a.shape[0] > 0]
+    if not parts:
+        return None
+    return np.concatenate(parts).astype(np.int32)

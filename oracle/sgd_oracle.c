@@ -307,6 +307,8 @@ struct orc_ring {
   int32_t *len;
   int32_t head, ndocs;
   int64_t live;
+  int64_t pushed;  /* docs ever placed; the doc at FIFO index i has sequence
+                      number pushed - ndocs + i */
 };
 
 orc_ring *orc_ring_create(int64_t capacity, int32_t max_docs, int32_t V) {
@@ -364,12 +366,14 @@ uint32_t orc_ring_ingest(orc_ring *r, const int32_t *token_ids,
     r->len[slot] = eff;
     r->ndocs++;
     r->live += (int64_t)eff + 1;
+    r->pushed++;
   }
   return flags;
 }
 
 int64_t orc_ring_live(const orc_ring *r) { return r->live; }
 int32_t orc_ring_ndocs(const orc_ring *r) { return r->ndocs; }
+int64_t orc_ring_pushed(const orc_ring *r) { return r->pushed; }
 
 int64_t orc_ring_snapshot(const orc_ring *r, int32_t *X) {
   int64_t pos = 0;
@@ -378,6 +382,27 @@ int64_t orc_ring_snapshot(const orc_ring *r, int32_t *X) {
     memcpy(X + pos, r->doc[slot], sizeof(int32_t) * (size_t)r->len[slot]);
     pos += r->len[slot];
     X[pos++] = r->V;
+  }
+  return pos;
+}
+
+/* ------------------------------------------------------------------------ */
+/* Delta: [PYPI] How it works, step 2 (global matching also scans, by brute
+ * force, the buffer of documents not yet in the suffix array) and step 4 (new
+ * documents append to that buffer until a rebuild indexes them).  The docs
+ * not yet indexed by a snapshot are those placed after it was taken: the live
+ * docs whose sequence number is >= `since` (the ring's pushed count when the
+ * snapshot was linearised), oldest first, each followed by Z.  The buffer
+ * holds at most `cap` tokens: what does not fit waits for the next rebuild,
+ * and a doc cut by the capacity is visible up to the cut.  The corpus a row
+ * is matched against is then the snapshot followed by this text. */
+int64_t orc_ring_delta(const orc_ring *r, int64_t since, int64_t cap, int32_t *Y) {
+  int64_t pos = 0;
+  for (int32_t i = 0; i < r->ndocs && pos < cap; i++) {
+    if (r->pushed - r->ndocs + i < since) continue;
+    int32_t slot = (r->head + i) % r->max_docs;
+    for (int32_t j = 0; j <= r->len[slot] && pos < cap; j++)
+      Y[pos++] = j < r->len[slot] ? r->doc[slot][j] : r->V;
   }
   return pos;
 }

@@ -103,6 +103,13 @@ int64_t orc_ring_live(const orc_ring *r);
 int32_t orc_ring_ndocs(const orc_ring *r);
 /* Writes the live docs, oldest first, each followed by Z; returns the length. */
 int64_t orc_ring_snapshot(const orc_ring *r, int32_t *X);
+/* Docs placed so far (each placed doc, evicted or not, counts once). */
+int64_t orc_ring_pushed(const orc_ring *r);
+/* The docs not yet indexed by a snapshot taken when orc_ring_pushed() was
+ * `since` ([PYPI] How it works, steps 2 and 4): the live docs with sequence
+ * number >= since, oldest first, each followed by Z, cut after `cap` tokens.
+ * Y holds at least min(cap, orc_ring_live(r)) ints; returns the length. */
+int64_t orc_ring_delta(const orc_ring *r, int64_t since, int64_t cap, int32_t *Y);
 
 #ifdef __cplusplus
 }

@@ -371,3 +371,90 @@ def test_invariants_random_rows(orc):
             W = list(t[n - M:]) + r.drafts[:L].tolist()
             s = "," + ",".join(map(str, t.tolist())) + ","
             assert ("," + ",".join(map(str, W)) + ",") in s
+
+
+# --------------------------------------------------------------------------
+# delta (docs placed after the snapshot was taken, not yet indexed)
+
+def _ingest_docs(ring, docs):
+    width = max(1, max(len(d) for d in docs))
+    buf = np.full((len(docs), width), -1, dtype=np.int32)
+    for i, d in enumerate(docs):
+        buf[i, :len(d)] = d
+    ring.ingest(buf, np.arange(len(docs)), np.zeros(len(docs)), [len(d) for d in docs])
+
+
+def test_delta_vs_sequence_model(orc):
+    """The delta of a snapshot taken after `since` placements is the live docs
+    placed after it, oldest first, each followed by the sentinel, cut at cap
+    (checked against a list model that numbers every placed doc)."""
+    rng = random.Random(21)
+    for _ in range(60):
+        C = rng.randint(5, 80)
+        max_docs = rng.randint(1, 9)
+        ring = orc.Ring(C, max_docs, 50)
+        model = []   # (sequence number, tokens) of the live docs, oldest first
+        placed = 0
+        marks = [0]  # pushed counts at which snapshots were "taken"
+        for _step in range(25):
+            m = rng.randint(1, 4)
+            docs = [[rng.randrange(50) for _ in range(rng.randint(0, 15))] for _ in range(m)]
+            _ingest_docs(ring, docs)
+            for d in docs:
+                if len(d) == 0 or len(d) + 1 > C:
+                    continue
+                model.append((placed, d))
+                placed += 1
+                while sum(len(x) + 1 for _, x in model) > C or len(model) > max_docs:
+                    model.pop(0)
+            assert ring.pushed == placed
+            if rng.random() < 0.3:
+                marks.append(placed)
+            for since in marks[-3:] + [placed]:
+                for cap in (0, 1, rng.randint(1, 40), 10 ** 6):
+                    want = []
+                    for sq, d in model:
+                        if sq >= since:
+                            want += d + [50]
+                    assert ring.delta(since, cap).tolist() == want[:cap], (since, cap)
+
+
+def test_delta_completes_the_snapshot(orc):
+    """While nothing has been evicted since a snapshot, that snapshot followed
+    by its full delta is the snapshot the ring would give now; a smaller cap
+    gives a prefix of the full delta."""
+    rng = random.Random(5)
+    for _ in range(40):
+        ring = orc.Ring(10 ** 6, 10 ** 4, 30)
+        _ingest_docs(ring, [[rng.randrange(30) for _ in range(rng.randint(1, 12))]
+                            for _ in range(rng.randint(1, 6))])
+        X0, since = ring.snapshot(), ring.pushed
+        _ingest_docs(ring, [[rng.randrange(30) for _ in range(rng.randint(0, 12))]
+                            for _ in range(rng.randint(1, 6))])
+        full = ring.delta(since, 10 ** 9)
+        assert np.concatenate([X0, full]).tolist() == ring.snapshot().tolist()
+        cap = rng.randint(0, full.shape[0] + 2)
+        assert ring.delta(since, cap).tolist() == full[:cap].tolist()
+        # a ring never snapshotted: every live doc is in the delta
+        assert ring.delta(0, 10 ** 9).tolist() == ring.snapshot().tolist()
+
+
+def test_delta_proposals_equal_the_rebuilt_index(orc):
+    """Matching against snapshot + delta gives the proposals that matching
+    against a snapshot rebuilt over the same docs gives (no evictions)."""
+    rng = np.random.default_rng(17)
+    V, S = 12, 64
+    p = orc.Params(S=S, V=V, k=6, D=8, R=8, min_prob=(1, 10))
+    for trial in range(20):
+        ring = orc.Ring(10 ** 6, 10 ** 4, V)
+        docs = [list(rng.integers(0, V, rng.integers(2, 20))) for _ in range(6)]
+        _ingest_docs(ring, docs[:3])
+        X0, since = ring.snapshot(), ring.pushed
+        _ingest_docs(ring, docs[3:])
+        Xd = orc.corpus_text(X0, ring.delta(since, 10 ** 9))
+        tok = rng.integers(0, V, (8, S)).astype(np.int32)
+        n = rng.integers(2, S - 8, 8).astype(np.int32)
+        a = orc.propose(p, tok, n, X=Xd)
+        b = orc.propose(p, tok, n, X=ring.snapshot())
+        assert np.array_equal(a.drafts, b.drafts) and np.array_equal(a.match_info, b.match_info)
+        assert np.array_equal(a.num_valid, b.num_valid) and np.array_equal(a.score, b.score)
