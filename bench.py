@@ -145,7 +145,10 @@ def workload_config(cfg, world):
             "parallelism": "replicas" if world > 1 else "single"}
 
 
-def run_ours(args, rank, world):
+def run_ours(args, rank, world, delta=0):
+    """The serving loop.  delta > 0: the same loop with the docs ingested since
+    the current snapshot also matched (brute-force scan of up to `delta`
+    tokens), timed as a secondary line (no end-to-end or build legs)."""
     import torch
     from model_free_suffix_gb300 import SuffixDrafter
     from model_free_suffix_gb300 import workload as W
@@ -153,14 +156,14 @@ def run_ours(args, rank, world):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.config]
-    K, Wm = args.steps, args.warmup
-    K_e2e = min(K, args.e2e_steps)
+    K, Wm = (args.delta_steps if delta else args.steps), args.warmup
+    K_e2e = 0 if delta else min(K, args.e2e_steps)
     tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=Wm + K + K_e2e)
     dr = SuffixDrafter(max_batch=cfg.B, seq_capacity=cfg.S, vocab_size=cfg.V, k=cfg.k,
                        max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
                        max_spec_factor=cfg.factor, max_spec_offset=cfg.offset,
                        min_token_prob=cfg.min_prob, corpus_capacity=cfg.corpus_tokens,
-                       device=dev.index)
+                       delta_capacity=delta, device=dev.index)
     # drafting at the device's highest stream priority, snapshot builds at the lowest
     least, greatest = torch.cuda.Stream.priority_range()
     stream = torch.cuda.Stream(device=dev, priority=greatest)
@@ -211,7 +214,11 @@ def run_ours(args, rank, world):
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 0) or (126 << 20)
     flush = torch.empty(max(2 * l2, 256 << 20) // 4, dtype=torch.int32, device=dev)
-    state = {"pending": False, "ingested": 0, "swaps": 0, "builds": 0, "build_stats": []}
+    # ring tokens each step's docs take (a sentinel after each)
+    ring_tok = [int(s.ingest_lengths.sum()) + int((s.ingest_lengths > 0).sum()) for s in steps]
+    state = {"pending": False, "ingested": 0, "swaps": 0, "builds": 0, "build_stats": [],
+             # ring tokens placed since the current / the pending snapshot was linearised
+             "since_front": 0, "since_pending": 0, "delta_tok": []}
 
     def stage(i):
         """Outside the timed region: the previous step's finished rows restart
@@ -232,17 +239,22 @@ def run_ours(args, rank, world):
 
     def policy(i):
         """Host side of the step: rebuild policy and the swap poll."""
+        state["delta_tok"].append(min(delta, state["since_front"]))  # what this step's rows scanned
         state["ingested"] += fin[i][3]
+        state["since_front"] += ring_tok[i]
+        state["since_pending"] += ring_tok[i]
         if cfg.corpus_tokens:
             if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
                 dr.build_sa(side, stream=stream)
                 state["pending"] = True
                 state["ingested"] = 0
+                state["since_pending"] = 0
                 state["builds"] += 1
             st, _ = dr.poll(wait=False, stream=stream)
             if st == 1:
                 state["pending"] = False
                 state["swaps"] += 1
+                state["since_front"] = state["since_pending"]
                 state["build_stats"].append(dr.build_stats())
 
     def one_step(i, ev=None):
@@ -285,6 +297,30 @@ def run_ours(args, rank, world):
     builds_in_region = state["builds"] - b0
     region_builds = state["build_stats"][nb0:]
     n_sum = int(g_n.sum().item())
+    if delta:
+        peak, peak_kind = peaks()
+        ing_tok = float(np.mean([fin[Wm + j][3] for j in range(K)])) if fused else 0.0
+        dv = float(np.mean(state["delta_tok"][Wm:Wm + K]))
+        # the delta is read from HBM once per step (every row then finds it in L2)
+        byts = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens, ing_tok) + 4 * dv
+        prop_avg_s = float(np.mean(prop_ms)) / 1e3
+        ach = byts / prop_avg_s / 1e9
+        if state["pending"]:
+            dr.poll(wait=True, stream=stream)
+        dr.close()
+        return {"workload": "the serving loop above with delta_capacity=%d: the docs ingested "
+                            "since the current snapshot was linearised are matched too, by a "
+                            "brute-force scan of the ring in every row's CTA" % delta,
+                "delta_capacity": delta, "steps": K, "mean_delta_tokens": round(dv, 1),
+                "us_per_step": round(1e3 * total_ms_max / K, 2),
+                "steps_per_s": round(world * K / (total_ms_max / 1e3), 2),
+                "propose_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
+                               "median": round(1e3 * float(np.median(prop_ms)), 2),
+                               "p90": round(1e3 * float(np.percentile(prop_ms, 90)), 2)},
+                "roofline": {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 2),
+                             "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
+                             "bytes_per_launch": int(byts), "peak_kind": peak_kind},
+                "builds_in_timed_region": builds_in_region, "clocks": clocks}
     # e2e: host buffers through the public API, copies inside the timed region
     if state["pending"]:
         dr.poll(wait=True, stream=stream)
@@ -582,6 +618,8 @@ def main():
                     help="steps of the long-context workload timed as a secondary line (0: skip)")
     ap.add_argument("--sa-only", type=int, default=0,
                     help="only time suffix-array builds of this many tokens and print them")
+    ap.add_argument("--delta-steps", type=int, default=256,
+                    help="steps of the serving loop with the delta scan on, a secondary line (0: skip)")
     ap.add_argument("--long-only", action="store_true",
                     help="only time the long-context workload and print its line")
     args = ap.parse_args()
@@ -625,6 +663,8 @@ def main():
             print(json.dumps(long_context_leg(args, rank)), flush=True)
         return
     res = run_ours(args, rank, world)
+    if args.delta_steps > 0 and args.config == "c3":
+        res["delta"] = run_ours(args, rank, world, delta=cfg.rebuild_tokens)
     if args.long_context_steps > 0 and args.config == "c3":
         res["long_context"] = long_context_leg(args, rank)
     if rank == 0:

@@ -108,6 +108,18 @@ typedef struct {
                                   in small CTAs (more per SM), then the corpus chain and
                                   vote.  Drafts are the same either way; on the long-
                                   context workload mode 1 is currently the faster. */
+  int64_t  delta_capacity;     /* 0 (default): a doc becomes matchable once a suffix array
+                                  built after its ingest is swapped in.  > 0: the docs
+                                  placed since the current snapshot was linearised (the
+                                  delta, [PYPI] How it works, steps 2 and 4) are matched
+                                  too, by a brute-force scan of up to delta_capacity of
+                                  their tokens (sentinels included), oldest first; a doc
+                                  cut by the capacity is visible up to the cut and the
+                                  rest waits for the next swap.  The corpus a row matches
+                                  is then the snapshot followed by that text; delta ends
+                                  count as more recent than snapshot ends.  Requires
+                                  corpus_capacity to be a multiple of 128;
+                                  <= corpus_capacity. */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)

@@ -59,6 +59,7 @@ class SgdConfig(ctypes.Structure):
         ("corpus_records", ctypes.c_int32),
         ("corpus_gram_index", ctypes.c_int32),
         ("propose_mode", ctypes.c_int32),
+        ("delta_capacity", ctypes.c_int64),
     ]
 
 

@@ -111,6 +111,8 @@ int validate(const sgd_config &c) {
   if (c.corpus_records != 0 && c.corpus_records != 1) return SGD_EINVAL;
   if (c.corpus_gram_index != 0 && c.corpus_gram_index != 1) return SGD_EINVAL;
   if (c.propose_mode < 0 || c.propose_mode > 2) return SGD_EINVAL;
+  if (c.delta_capacity < 0 || c.delta_capacity > c.corpus_capacity) return SGD_EINVAL;
+  if (c.delta_capacity > 0 && c.corpus_capacity % WIN != 0) return SGD_EINVAL;
   return SGD_OK;
 }
 
@@ -274,6 +276,7 @@ int sgd_config_default(sgd_config *c) {
   c->corpus_records = 1;
   c->corpus_gram_index = 1;
   c->propose_mode = 0;
+  c->delta_capacity = 0;
   c->self_warps = 0;
   return SGD_OK;
 }
@@ -325,7 +328,7 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
   al((void **)&x->d_err, 4);
   al((void **)&x->d_build_err, 4);
   if (x->split)
-    al((void **)&x->d_self_res, (size_t)cfg->max_batch * (cfg->max_occurrences + 6) * 4);
+    al((void **)&x->d_self_res, (size_t)cfg->max_batch * self_res_ints(cfg->max_occurrences) * 4);
   {
     const size_t Bm = (size_t)cfg->max_batch, kk = (size_t)cfg->k;
     al((void **)&x->d_hin, 4 * (Bm * (size_t)cfg->max_sampled + 3 * (size_t)cfg->max_ingest_docs));
@@ -364,9 +367,9 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
       }
     }
     al((void **)&x->d_step_ready, (size_t)cfg->max_batch * 4);
-    al((void **)&x->d_step_sync, 8);
+    al((void **)&x->d_step_sync, 16);
     if (e == cudaSuccess) e = cudaMemset(x->d_step_ready, 0, (size_t)cfg->max_batch * 4);
-    if (e == cudaSuccess) e = cudaMemset(x->d_step_sync, 0, 8);
+    if (e == cudaSuccess) e = cudaMemset(x->d_step_sync, 0, 16);
     al((void **)&x->ing.eff, (size_t)cfg->max_ingest_docs * 4);
     al((void **)&x->ing.dest, (size_t)cfg->max_ingest_docs * 8);
     al((void **)&x->ing.order, (size_t)cfg->max_ingest_docs * 4);
@@ -445,6 +448,13 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.rsh = x->rsh;
   a.split = x->split;
   a.self_res = x->d_self_res;
+  if (x->corpus && c.delta_capacity > 0) {  // the delta is read from the ring in place
+    a.dcap = c.delta_capacity;
+    a.ring = x->d_ring;
+    a.C = c.corpus_capacity;
+    a.rs = x->d_rs;
+    a.doc_start = x->d_doc_start;
+  }
   return a;
 }
 
@@ -509,7 +519,10 @@ int sgd_step(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int32_t 
   if (n_docs < 0 || n_docs > x->cfg.max_ingest_docs) return SGD_EINVAL;
   if (n_docs > 0 && !x->corpus) return SGD_ENOCORPUS;
   if (n_docs > 0 && (!rows || !starts || !lengths)) return SGD_EINVAL;
-  if (n_docs == 0 || n_docs > propose_step_max_docs() || B == 0) {
+  // (two launches for the long-row mode with a delta: its second kernel must
+  // not append to the ring while its rows read delta continuations)
+  if (n_docs == 0 || n_docs > propose_step_max_docs() || B == 0 ||
+      (x->split && x->cfg.delta_capacity > 0)) {
     int r = sgd_propose_with_update(x, token_ids, num_tokens, sampled, T, active, B, drafts,
                                     num_valid, score, probs, match_info, stream);
     if (r != SGD_OK || n_docs == 0) return r;
@@ -722,7 +735,7 @@ int sgd_poll(sgd_ctx *x, int wait, int64_t timeout_us, void *stream, uint64_t *g
   const int back = 1 - x->front;
   const cudaError_t e = launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->d_keys[back],
                                     x->d_rec[back], x->d_gt[back], x->gt_mask, x->built_n, x->gen + 1,
-                                    (cudaStream_t)stream);
+                                    x->d_rs, (cudaStream_t)stream);
   if (e != cudaSuccess) return SGD_ECUDA;
   x->launches++;
   x->front = back;

@@ -115,12 +115,21 @@ __global__ void __launch_bounds__(256) linearize_kernel(const int32_t *ring, lon
     if (p >= C) p -= C;
     out[i] = ring[p];
   }
-  if (blockIdx.x == 0 && threadIdx.x == 0) rs->snap_n = live;
+  if (blockIdx.x == 0 && threadIdx.x == 0) {
+    rs->snap_n = live;
+    rs->snap_pushed = rs->pushed;  // docs placed after this point form the delta
+    rs->snap_wp = rs->wp;
+  }
 }
 
+// The new snapshot becomes current; its delta starts where its linearisation
+// stopped (the last linearisation is the one this snapshot was built from:
+// no other starts while a build is outstanding).
 __global__ void swap_kernel(CorpusDesc *desc, const int32_t *text, const int32_t *sa,
                             const int4 *keys, const int32_t *rec, const int32_t *gt,
-                            uint64_t gt_mask, long long n, uint64_t gen) {
+                            uint64_t gt_mask, long long n, uint64_t gen, const RingState *rs) {
+  desc->lin_pushed = rs->snap_pushed;
+  desc->lin_wp = rs->snap_wp;
   desc->text = text;
   desc->sa = sa;
   desc->keys = keys;
@@ -252,7 +261,7 @@ cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S,
   if (m <= 0) return cudaSuccess;
   if (m <= SMALL_DOCS) {
     const SmallIngest g{tok, ntok, B, S, V, rows, starts, lengths, m, ring, C, rs,
-                        doc_start, doc_len, max_docs, err, nullptr, 0u};
+                        doc_start, doc_len, max_docs, err, nullptr, 0u, nullptr, nullptr, 0};
     ingest_small<<<1, PLAN_THREADS, 0, st>>>(g);
     *launches += 1;
     return cudaGetLastError();
@@ -278,8 +287,8 @@ cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs, cons
 
 cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
                         const int32_t *rec, const int32_t *gt, uint64_t gt_mask, int64_t n,
-                        uint64_t gen, cudaStream_t st) {
-  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, rec, gt, gt_mask, n, gen);
+                        uint64_t gen, const RingState *rs, cudaStream_t st) {
+  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, rec, gt, gt_mask, n, gen, rs);
   return cudaGetLastError();
 }
 

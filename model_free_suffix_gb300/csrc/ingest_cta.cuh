@@ -64,6 +64,7 @@ __device__ inline void place_doc(PlanWalk &w, int i, int L, long long C, const i
   r.wp = (r.wp + s) % C;
   r.live += s;
   r.ndocs++;
+  r.pushed++;
 }
 
 // Warp 0: inclusive prefix sums of c over the 32 lanes into s_cum[1..32].
@@ -100,6 +101,7 @@ struct SmallIngestSmem {
   int cum[SMALL_DOCS + 1];
   int dl[PLAN_WINDOW];
   RingState rs;
+  int stop;  // a wait gave up: no doc of the call is placed
 };
 
 struct SmallIngest {
@@ -117,7 +119,24 @@ struct SmallIngest {
   uint32_t *err;
   const uint32_t *ready;  // per row: == expect once the row's update is written; or null
   uint32_t expect;
+  // Fused step whose rows also read the delta from the ring (dcap > 0): the
+  // ring state is changed only once every row CTA has read it (sync[0], the
+  // step epoch, == expect), and if the new docs' tokens could land on the
+  // rows' visible delta, only once every row CTA is done (sync[3] == expect).
+  const uint32_t *sync;
+  const CorpusDesc *desc;
+  long long dcap;
 };
+
+// Bounded wait for *f == expect; false if it gave up.
+__device__ inline bool wait_flag(const uint32_t *f, uint32_t expect) {
+  unsigned spins = 0;
+  while (ld_acquire_u32(f) != expect) {
+    if (++spins > STEP_SPIN_LIMIT) return false;
+    if (spins > 16) __nanosleep(64);
+  }
+  return true;
+}
 
 // The whole call in one CTA (any block size that is a multiple of 32).  Each
 // phase issues all of its loads at once over the docs' tokens laid end to
@@ -144,21 +163,17 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
     small_cum(ok ? ln : 0, s.cum);
   } else if (tid == 32) {
     s.rs = *g.rs;
+    s.stop = 0;
   }
   __syncthreads();
+  const bool delta = g.ready != nullptr && g.sync != nullptr && g.dcap > 0;
   if (g.ready != nullptr) {
     if (tid < m && s.ln[tid] >= 0) {
-      const uint32_t *f = g.ready + s.row[tid];
-      unsigned spins = 0;
-      while (ld_acquire_u32(f) != g.expect) {
-        if (++spins > STEP_SPIN_LIMIT) {
-          s.ln[tid] = -2;  // give the doc up rather than read a row mid-update
-          break;
-        }
-        if (spins > 16) __nanosleep(64);
-      }
+      // give the doc up rather than read a row mid-update
+      if (!wait_flag(g.ready + s.row[tid], g.expect)) s.ln[tid] = -2;
       __threadfence();
     }
+    if (delta && tid == 32 && !wait_flag(g.sync, g.expect)) s.stop = 1;  // every row CTA counted in
     __syncthreads();
   }
   const RingState r0 = s.rs;
@@ -186,7 +201,7 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
   }
   __syncthreads();
   if (tid < m) {
-    const int ln = s.ln[tid];
+    const int ln = s.stop ? -2 : s.ln[tid];
     if (ln == -2) {
       s.first[tid] = -1;
       atomicOr(g.err, SGD_ERR_INGEST_WAIT);
@@ -199,6 +214,19 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
   }
   __syncthreads();
   if (tid == 0) {
+    if (delta && !s.stop) {
+      // the call writes at most T tokens from the write offset on; the rows'
+      // visible delta ends at the write offset and starts len tokens before it,
+      // so the writes reach it only if T > C - len
+      long long T = 0;
+      for (int i = 0; i < m; ++i)
+        if (s.first[i] > 0) T += s.first[i] + 1;
+      const DeltaView v = delta_view(r0, g.desc->lin_pushed, g.desc->lin_wp, g.C, g.doc_start);
+      if (min(v.len, g.dcap) > 0 && T > g.C - v.len && !wait_flag(g.sync + 3, g.expect)) {
+        for (int i = 0; i < m; ++i) s.first[i] = -1;
+        atomicOr(g.err, SGD_ERR_INGEST_WAIT);
+      }
+    }
     PlanWalk w{r0, r0.ndocs, win, 0, 0, 0, 0u};
     for (int i = 0; i < m; ++i)
       place_doc(w, i, s.first[i], g.C, s.dl, g.doc_start, g.doc_len, g.max_docs, s.dest, s.order);

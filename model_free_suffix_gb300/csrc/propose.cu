@@ -45,6 +45,10 @@ constexpr long long BIG_INTERVAL = 4096;  // probe hits worth waiting for the se
 
 // barrier of the three probe warps only
 __device__ __forceinline__ void probe_sync() { asm volatile("bar.sync 1, 96;" ::: "memory"); }
+// the self warps (warps 0 .. nself-1) of a CTA
+__device__ __forceinline__ void self_sync(int nself) {
+  asm volatile("bar.sync 2, %0;" ::"r"(32 * nself) : "memory");
+}
 
 __device__ __forceinline__ void cp_async4(void *smem, const void *gmem) {
   const unsigned sa = (unsigned)__cvta_generic_to_shared(smem);
@@ -103,20 +107,22 @@ __device__ __forceinline__ bool self_prefetch(const int32_t *row, int n, int S, 
   return true;
 }
 
-// L(j) for an end j whose last two tokens already match (t[j] = tail[0],
-// t[j-1] = tail[1]): lane i compares t[j-1-i] with tail[1+i], 32 depths per
-// round, from the window pair [prv | cur] in the ring (the comparisons reach
-// back at most 127 positions, never past prv).  tail1 = tail[1 + lane].
-__device__ __forceinline__ int self_extend(int j, int base, const int *cw, const int *pw, int D,
-                                          const int *s_tail, int tail1, int lane) {
+// The match length of an end whose last two tokens already match the tail
+// (x[jr] = tail[0], x[jr-1] = tail[1]), read from a window pair [pw | cw] in
+// the ring: jr is the end's index in the pair (in [WIN, 2 WIN)), and indices
+// below lo (before the start of the text) hold no token.  Lane i compares
+// x[jr-1-i] with tail[1+i], 32 depths per round, up to depth dlim (the
+// comparisons reach back at most 127 positions, never past pw).
+// tail1 = tail[1 + lane].
+__device__ __forceinline__ int pair_extend(int jr, int lo, const int *cw, const int *pw, int dlim,
+                                           const int *s_tail, int tail1, int lane) {
   int L = 1;
   for (int r = 0; r < 4; ++r) {
     const int i = 32 * r + lane;
-    const int p = j - 1 - i;
+    const int p = jr - 1 - i;
     bool ok = false;
-    if (i + 1 < D && p >= 0) {
-      const int rel = p - (base - WIN);
-      const int v = rel >= WIN ? cw[rel - WIN] : pw[rel];
+    if (i + 1 < dlim && p >= lo) {
+      const int v = p >= WIN ? cw[p - WIN] : pw[p];
       ok = v == (r == 0 ? tail1 : s_tail[1 + i]);
     }
     const unsigned mis = __ballot_sync(FULL, !ok);
@@ -126,16 +132,126 @@ __device__ __forceinline__ int self_extend(int j, int base, const int *cw, const
   return L;
 }
 
+constexpr int LANE_DEPTH = 8;  // depth one lane extends an end to on its own
+
+// One window's ends whose last two tokens match the tail: bit l of mc marks
+// the end at pair index WIN + 4 l + c (lane l's component c), stored as
+// pos0 + c (pos0: lane l's first position).  With more than two of them each
+// lane extends its own ends token by token up to LANE_DEPTH; the ends that
+// may go deeper (and all of them when there are at most two) are extended by
+// the whole warp, one at a time.  Then the warp's longest length Mw and its
+// list of the R most recent ends of that length (positions descending: higher
+// lanes first, then higher components) take in this window's ends.
+__device__ __forceinline__ void window_ends(unsigned m0, unsigned m1, unsigned m2, unsigned m3,
+                                            int pos0, int lo, const int *cw, const int *pw,
+                                            int dlim, const int *s_tail, int tail1, int lane, int R,
+                                            int *list, int &Mw, int &cnt) {
+  const bool b0 = (m0 >> lane) & 1u, b1 = (m1 >> lane) & 1u;
+  const bool b2 = (m2 >> lane) & 1u, b3 = (m3 >> lane) & 1u;
+  int L0 = 0, L1 = 0, L2 = 0, L3 = 0;
+  if (__popc(m0) + __popc(m1) + __popc(m2) + __popc(m3) > 2) {
+    const int jr = WIN + 4 * lane, lim = min(dlim, LANE_DEPTH);
+    auto ext = [&](int j) {  // x[j] = tail[0] and x[j-1] = tail[1] already hold
+      int L = 2;
+      while (L < lim && j - L >= lo) {
+        const int p = j - L;
+        if ((p >= WIN ? cw[p - WIN] : pw[p]) != s_tail[L]) break;
+        ++L;
+      }
+      return L;
+    };
+    if (b0) L0 = ext(jr);
+    if (b1) L1 = ext(jr + 1);
+    if (b2) L2 = ext(jr + 2);
+    if (b3) L3 = ext(jr + 3);
+    const bool deep = lim < dlim;  // (one stopped by lo at exactly lim is redone: same length)
+    m0 = __ballot_sync(FULL, b0 && deep && L0 == lim);
+    m1 = __ballot_sync(FULL, b1 && deep && L1 == lim);
+    m2 = __ballot_sync(FULL, b2 && deep && L2 == lim);
+    m3 = __ballot_sync(FULL, b3 && deep && L3 == lim);
+  }
+  for (;;) {  // warp-wide, in descending position 4 * lane + c
+    int best = -1;
+    if (m0) best = 4 * (31 - __clz(m0));
+    if (m1) best = max(best, 4 * (31 - __clz(m1)) + 1);
+    if (m2) best = max(best, 4 * (31 - __clz(m2)) + 2);
+    if (m3) best = max(best, 4 * (31 - __clz(m3)) + 3);
+    if (best < 0) break;
+    const unsigned keep = ~(1u << (best >> 2));
+    const int bc = best & 3;
+    m0 = bc == 0 ? m0 & keep : m0;
+    m1 = bc == 1 ? m1 & keep : m1;
+    m2 = bc == 2 ? m2 & keep : m2;
+    m3 = bc == 3 ? m3 & keep : m3;
+    const int L = pair_extend(WIN + best, lo, cw, pw, dlim, s_tail, tail1, lane);
+    if (lane == (best >> 2)) {
+      if (bc == 0) L0 = L;
+      else if (bc == 1) L1 = L;
+      else if (bc == 2) L2 = L;
+      else L3 = L;
+    }
+  }
+  const int Lw = (int)__reduce_max_sync(FULL, (unsigned)max(max(L0, L1), max(L2, L3)));
+  if (Lw == 0 || Lw < Mw) return;
+  if (Lw > Mw) { Mw = Lw; cnt = 0; }
+  if (cnt >= R) return;
+  const bool e0 = L0 == Mw, e1 = L1 == Mw, e2 = L2 == Mw, e3 = L3 == Mw;
+  const int mine = (int)e0 + (int)e1 + (int)e2 + (int)e3;
+  int x = mine;  // over lanes >= this one
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int y = __shfl_down_sync(FULL, x, off);
+    if (lane + off < 32) x += y;
+  }
+  const int total = __shfl_sync(FULL, x, 0);
+  int slot = cnt + x - mine;
+  if (e3) { if (slot < R) list[slot] = pos0 + 3; ++slot; }
+  if (e2) { if (slot < R) list[slot] = pos0 + 2; ++slot; }
+  if (e1) { if (slot < R) list[slot] = pos0 + 1; ++slot; }
+  if (e0) { if (slot < R) list[slot] = pos0; }
+  cnt = min(R, cnt + total);
+}
+
+// The ends of a window worth extending: lane l's component c (position 4l + c)
+// where ok_c holds and the last k tokens (2 <= k <= 4) are tail[k-1 .. 0]
+// (tk = tail[k], tail[2] and tail[3] only read when k says so).  An end that
+// matches fewer than k tokens cannot reach the CTA's longest length so far,
+// so it cannot be among the ends that vote.  prv is the window below (the
+// tokens before lane 0's first).
+__device__ __forceinline__ void kgram_ballots(const int4 &cur, const int4 &prv, int lane, int k, int t0,
+                                              int t1, int t2, int t3, bool ok0, bool ok1, bool ok2,
+                                              bool ok3, unsigned &m0, unsigned &m1, unsigned &m2,
+                                              unsigned &m3) {
+  int py = __shfl_up_sync(FULL, cur.y, 1), pz = __shfl_up_sync(FULL, cur.z, 1);
+  int pw = __shfl_up_sync(FULL, cur.w, 1);
+  const int by = __shfl_sync(FULL, prv.y, 31), bz = __shfl_sync(FULL, prv.z, 31);
+  const int bw = __shfl_sync(FULL, prv.w, 31);
+  if (lane == 0) { py = by; pz = bz; pw = bw; }
+  const bool g3 = k >= 3, g4 = k >= 4;
+  m3 = __ballot_sync(FULL, ok3 && cur.w == t0 && cur.z == t1 && (!g3 || cur.y == t2) &&
+                               (!g4 || cur.x == t3));
+  m2 = __ballot_sync(FULL, ok2 && cur.z == t0 && cur.y == t1 && (!g3 || cur.x == t2) &&
+                               (!g4 || pw == t3));
+  m1 = __ballot_sync(FULL, ok1 && cur.y == t0 && cur.x == t1 && (!g3 || pw == t2) &&
+                               (!g4 || pz == t3));
+  m0 = __ballot_sync(FULL, ok0 && cur.x == t0 && pw == t1 && (!g3 || pz == t2) && (!g4 || py == t3));
+}
+
+// The CTA's longest length so far (over the warps scanning one text).
+__device__ __forceinline__ int kgram_k(int Mw, const int *s_best) {
+  return min(4, max(2, max(Mw, *(const volatile int *)s_best)));
+}
+
 // The warp's windows, most recent first.  Ends with L >= 1 are exactly the
 // positions holding tail[0] = t0; those with L >= 2 also hold tail[1] just
 // before.  Each lane holds four consecutive tokens of a window (its own 16
 // bytes of the ring slot), so a window without t0 costs one load, four
 // compares and a vote.  Otherwise the R most recent t0 positions are kept
 // (list1: the answer when no end matches two tokens) and every (t1, t0)
-// position, most recent first, is extended by self_extend into (Mw, list).
+// position is extended by window_ends into (Mw, list).
 __device__ void self_process(const int32_t *row, int n, int S, int D, int R, const int *s_tail,
-                             int *list, int *list1, int lane, SelfScan &sc, int &Mw, int &cnt,
-                             int &cnt1) {
+                             int *list, int *list1, int *s_best, int lane, SelfScan &sc, int &Mw,
+                             int &cnt, int &cnt1) {
   Mw = 0;
   cnt = 0;
   cnt1 = 0;
@@ -145,6 +261,7 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
   const bool two = D >= 2 && n >= 2;
   const int t1 = two ? s_tail[1] : 0;
   const int tail1 = lane + 1 < min(D, n) ? s_tail[1 + lane] : 0;
+  const int t2 = min(D, n) >= 3 ? s_tail[2] : 0, t3 = min(D, n) >= 4 ? s_tail[3] : 0;
   for (int wi = sc.whi, q = 0; wi >= sc.wlo; --wi, ++q) {
     // keep SPF windows in flight; then windows q and q + 1 must have landed
     self_fetch(row, wi - SPF - 1, lane, S, sc.ring, (q + SPF + 1) % SR);
@@ -171,44 +288,142 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
         if (a0) { if (slot < R) list1[slot] = p0; }
         cnt1 = min(R, cnt1 + total);
       }
-      // (t1, t0) positions: the token before position p0 is the previous
-      // lane's last one, or the last token of the window below for lane 0
+      // positions matching (t1, t0) -- or more of the tail once the CTA's
+      // longest match is longer -- with the window below for lane 0's past
       const int4 prv = sc.ring[((q + 1) % SR) * 32 + lane];
-      const int up = __shfl_up_sync(FULL, cur.w, 1);
-      const int below = __shfl_sync(FULL, prv.w, 31);
-      const int before0 = lane == 0 ? below : up;
-      unsigned m0 = __ballot_sync(FULL, a0 && two && p0 >= 1 && before0 == t1);
-      unsigned m1 = __ballot_sync(FULL, a1 && two && cur.x == t1);
-      unsigned m2 = __ballot_sync(FULL, a2 && two && cur.y == t1);
-      unsigned m3 = __ballot_sync(FULL, a3 && two && cur.z == t1);
+      unsigned m0, m1, m2, m3;
+      kgram_ballots(cur, prv, lane, kgram_k(Mw, s_best), t0, t1, t2, t3, a0 && two && p0 >= 1,
+                    a1 && two, a2 && two, a3 && two, m0, m1, m2, m3);
       if (m0 | m1 | m2 | m3) {
-        __syncwarp();  // every lane's copies visible to the warp (self_extend reads across lanes)
+        __syncwarp();  // every lane's copies visible to the warp (the extension reads across lanes)
         const int *cw = reinterpret_cast<const int *>(sc.ring + (q % SR) * 32);
         const int *pw = reinterpret_cast<const int *>(sc.ring + ((q + 1) % SR) * 32);
-        for (;;) {  // candidates in descending position 4 * lane + c
-          int best = -1;
-          if (m0) best = 4 * (31 - __clz(m0));
-          if (m1) best = max(best, 4 * (31 - __clz(m1)) + 1);
-          if (m2) best = max(best, 4 * (31 - __clz(m2)) + 2);
-          if (m3) best = max(best, 4 * (31 - __clz(m3)) + 3);
-          if (best < 0) break;
-          const unsigned keep = ~(1u << (best >> 2));
-          const int bc = best & 3;
-          m0 = bc == 0 ? m0 & keep : m0;
-          m1 = bc == 1 ? m1 & keep : m1;
-          m2 = bc == 2 ? m2 & keep : m2;
-          m3 = bc == 3 ? m3 & keep : m3;
-          const int jj = base + best;
-          const int L = self_extend(jj, base, cw, pw, D, s_tail, tail1, lane);
-          if (L > Mw) { Mw = L; cnt = 0; }
-          if (L == Mw && cnt < R) {
-            if (lane == 0) list[cnt] = jj;
-            ++cnt;
-          }
-        }
+        // the row's text starts at position 0: pair index WIN - base
+        const int M0 = Mw;
+        window_ends(m0, m1, m2, m3, p0, WIN - base, cw, pw, D, s_tail, tail1, lane, R, list, Mw,
+                    cnt);
+        if (Mw > M0 && lane == 0) atomicMax(s_best, Mw);
         __syncwarp();  // cross-lane reads of the slot done before it is refilled
       }
     }
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of the ring left in flight
+}
+
+// ---------------------------------------------------------------------------
+// corpus: the delta, scanned by brute force
+//
+// The delta is the text Y[0, dv) of the docs placed after the snapshot was
+// linearised, read in place from the ring: Y[u] = ring[(ds + u) mod C].  The
+// self warps scan it like the row: in windows of WIN aligned ring positions
+// (C is a multiple of WIN), split into contiguous ranges over the warps and
+// streamed through each warp's cp.async ring, the most recent first.  An end
+// u counts when it has a continuation (u + 1 < dv and Y[u+1] is not the
+// sentinel) and matches at least the last two tokens (a corpus match needs
+// two); u >= 1 and positions before ds hold no token.  Each warp keeps its
+// longest length and the R most recent ends of that length.
+
+// Copy ring window rw into slot `slot` of the warp's ring, one group.
+__device__ __forceinline__ void delta_fetch(const int32_t *ring, int rw, int lane, int4 *sring,
+                                            int slot) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(sring + slot * 32 + lane);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(sa),
+               "l"(ring + (size_t)rw * WIN + 4 * lane)
+               : "memory");
+}
+
+// The delta's windows are numbered r = 0 .. nw-1 from the one holding Y[0]:
+// window r starts at Y index r WIN - off (off = ds mod WIN) and is ring
+// window (ds / WIN + r) mod (C / WIN).  All Y indices fit in 32 bits.
+struct DeltaScan {
+  int rlo, rhi;  // this warp's windows
+  int off;       // Y index 0 lies at this offset of window 0
+  int rw;        // ring window of the next fetch
+  int nrw;       // ring windows (C / WIN)
+  int above0;    // Y[first index above window rhi], or Z if that is not visible
+};
+
+// Warp w's windows and the first SPF + 1 fetches; false if it has none.
+__device__ __forceinline__ bool delta_prefetch(const int32_t *ring, long long C, long long ds, int dv,
+                                               int Z, int w, int nself, int lane, int4 *sring,
+                                               DeltaScan &sc) {
+  sc.off = (int)(ds % WIN);
+  const int nw = (sc.off + dv - 1) / WIN + 1;
+  const int per = (nw + nself - 1) / nself;
+  sc.rlo = w * per;
+  sc.rhi = min(nw, sc.rlo + per) - 1;
+  if (sc.rhi < sc.rlo) return false;
+  sc.nrw = (int)(C / WIN);
+  const int rw_top = (int)((ds / WIN + sc.rhi) % sc.nrw);
+  const int ya = (sc.rhi + 1) * WIN - sc.off;  // Y index just above the top window
+  const int rwa = rw_top + 1 == sc.nrw ? 0 : rw_top + 1;
+  sc.above0 = ya < dv ? ring[(size_t)rwa * WIN] : Z;  // (plain load: the ring changes during a fused step)
+  // windows rhi, rhi - 1, ..., rhi - SPF (those below the delta hold other
+  // ring tokens; nothing reads them but the range checks)
+  int rw = rw_top;
+#pragma unroll
+  for (int q = 0; q <= SPF; ++q) {
+    delta_fetch(ring, rw, lane, sring, q);
+    rw = rw == 0 ? sc.nrw - 1 : rw - 1;
+  }
+  sc.rw = rw;
+  return true;
+}
+
+__device__ void delta_process(const int32_t *ring, int dv, int Z, int D, int n, int R,
+                              const int *s_tail, int lane, int4 *sring, DeltaScan &sc, int *list,
+                              int *s_best, int &Mw, int &cnt) {
+  Mw = 0;
+  cnt = 0;
+  const int t0 = s_tail[0], t1 = s_tail[1];
+  const int dlim = min(D, n);
+  const int tail1 = lane + 1 < dlim ? s_tail[1 + lane] : 0;
+  const int t2 = dlim >= 3 ? s_tail[2] : 0, t3 = dlim >= 4 ? s_tail[3] : 0;
+  int above0 = sc.above0, rw = sc.rw;
+  for (int r = sc.rhi, q = 0; r >= sc.rlo; --r, ++q) {
+    delta_fetch(ring, rw, lane, sring, (q + SPF + 1) % SR);
+    rw = rw == 0 ? sc.nrw - 1 : rw - 1;
+    asm volatile("cp.async.wait_group %0;" ::"n"(SPF) : "memory");
+    __syncwarp();  // every lane's copies of this window and the one below visible to the warp
+    const int4 cur = sring[(q % SR) * 32 + lane];
+    const int *cw = reinterpret_cast<const int *>(sring + (q % SR) * 32);
+    const int *pw = reinterpret_cast<const int *>(sring + ((q + 1) % SR) * 32);
+    const int first = __shfl_sync(FULL, cur.x, 0);
+    const int top = above0;  // the token after this window
+    above0 = first;
+    // Positions whose last k tokens match the tail, k = 2, 3 or 4 by the
+    // CTA's longest match so far (a shorter end cannot vote): the three
+    // tokens before each lane's first are the previous lane's last three, or
+    // for lane 0 the window below's.
+    const int4 bl = reinterpret_cast<const int4 *>(pw)[31];  // (one broadcast read)
+    int py = __shfl_up_sync(FULL, cur.y, 1), pz = __shfl_up_sync(FULL, cur.z, 1);
+    int pv = __shfl_up_sync(FULL, cur.w, 1);
+    if (lane == 0) { py = bl.y; pz = bl.z; pv = bl.w; }
+    const int k = kgram_k(Mw, s_best);
+    const bool g3 = k >= 3, g4 = k >= 4;
+    const bool h3 = cur.w == t0 && cur.z == t1 && (!g3 || cur.y == t2) && (!g4 || cur.x == t3);
+    const bool h2 = cur.z == t0 && cur.y == t1 && (!g3 || cur.x == t2) && (!g4 || pv == t3);
+    const bool h1 = cur.y == t0 && cur.x == t1 && (!g3 || pv == t2) && (!g4 || pz == t3);
+    const bool h0 = cur.x == t0 && pv == t1 && (!g3 || pz == t2) && (!g4 || py == t3);
+    if (!__any_sync(FULL, h0 | h1 | h2 | h3)) continue;
+    // ends among them: a continuation, Y index >= 1 (the token after lane
+    // 31's last is the window above's first)
+    const int dn = __shfl_down_sync(FULL, cur.x, 1);
+    const int after3 = lane == 31 ? top : dn;
+    const int yb = r * WIN - sc.off;  // Y index of the window's first token
+    const int u0 = yb + 4 * lane;
+    const unsigned m0 = __ballot_sync(FULL, h0 && cur.y != Z && u0 >= 1 && u0 + 1 < dv);
+    const unsigned m1 = __ballot_sync(FULL, h1 && cur.z != Z && u0 + 1 >= 1 && u0 + 2 < dv);
+    const unsigned m2 = __ballot_sync(FULL, h2 && cur.w != Z && u0 + 2 >= 1 && u0 + 3 < dv);
+    const unsigned m3 = __ballot_sync(FULL, h3 && after3 != Z && u0 + 3 >= 1 && u0 + 4 < dv);
+    if (m0 | m1 | m2 | m3) {
+      // pair index of Y[0] (clamped: below the pair nothing is excluded)
+      const int lo = max(-1, min(2 * WIN, WIN - yb));
+      const int M0 = Mw;
+      window_ends(m0, m1, m2, m3, u0, lo, cw, pw, dlim, s_tail, tail1, lane, R, list, Mw, cnt);
+      if (Mw > M0 && lane == 0) atomicMax(s_best, Mw);
+    }
+    __syncwarp();  // cross-lane reads of the slots done before they are refilled
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of the ring left in flight
 }
@@ -636,6 +851,18 @@ __device__ __forceinline__ void step_arrive(uint32_t *sync, uint32_t e0) {
   }
 }
 
+// Fused step with a delta: each row CTA counts itself out once it no longer
+// reads the ring; the last one publishes the epoch in sync[3] (the ingest CTA
+// waits for it before appending over the rows' visible delta).
+__device__ __forceinline__ void step_done(uint32_t *sync, uint32_t e0) {
+  __threadfence();
+  if (atomicAdd(&sync[2], 1u) == gridDim.x - 2) {  // the row CTAs are all but CTA 0
+    sync[2] = 0;
+    __threadfence();
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(sync + 3), "r"(e0 + 1) : "memory");
+  }
+}
+
 __device__ __forceinline__ uint32_t ld_volatile_u32(const uint32_t *p) {
   return *reinterpret_cast<const volatile uint32_t *>(p);
 }
@@ -656,7 +883,7 @@ __device__ __forceinline__ void step_ingest(const ProposeArgs &a) {
   __syncthreads();
   const SmallIngest g{a.tok, a.ntok, a.B, a.S, a.V, a.ing_rows, a.ing_starts, a.ing_lengths,
                       a.ing_m, a.ring, a.C, a.rs, a.doc_start, a.doc_len, a.max_docs, a.err,
-                      a.step_ready, s_e0 + 1 + a.ing_skew};
+                      a.step_ready, s_e0 + 1 + a.ing_skew, a.step_sync, a.desc, a.dcap};
   ingest_small_cta(g, *reinterpret_cast<SmallIngestSmem *>(dsm));
 }
 
@@ -677,6 +904,12 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ int s_self_done, s_ms_ready, s_pms, s_Mc, s_c0c, s_cpf;
   __shared__ int s_early[4], s_early_ok;  // last four tokens, known from the update
   __shared__ int s_ckey;  // short level whose continuation comes from keys and records, or 0
+  // the delta: ring start, visible tokens, longest match and its ends (their
+  // list is in s_wlist1 once merged); the fused step's epoch
+  __shared__ long long s_ds;
+  __shared__ int s_dv, s_Md, s_cd;
+  __shared__ int s_best_self, s_best_delta;  // longest match so far in the row / the delta
+  __shared__ uint32_t s_ep;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
   const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
@@ -714,6 +947,17 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   if (warp == 0) {
     const bool signal = a.ing_m > 0 && a.step_ready != nullptr;
     const uint32_t e0 = signal && lane == 0 ? ld_volatile_u32(&a.step_sync[0]) : 0u;
+    // Where the delta lies.  In a fused step this is read before the CTA counts
+    // itself in below: the ingest CTA changes the ring state only after every
+    // row CTA has, so all rows see the ring as it was before the step's docs.
+    if (!FROM_RES && a.dcap > 0 && a.desc != nullptr && lane == 0) {
+      const DeltaView v = delta_view(*a.rs, a.desc->lin_pushed, a.desc->lin_wp, a.C, a.doc_start);
+      s_ds = v.start;
+      s_dv = (int)min(v.len, a.dcap);
+    } else if (!FROM_RES && lane == 0) {
+      s_ds = 0;
+      s_dv = 0;
+    }
     int n = a.ntok[b];
     uint32_t fl = 0;
     if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
@@ -726,13 +970,22 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     bool early = a.do_update && n - n_old >= 4;
     // (plain loads: `sampled` may be page-locked host memory read in place)
     if (early && lane < 4) s_early[lane] = a.sampled[(size_t)b * a.T + (n - n_old) - 1 - lane];
-    if (FROM_RES) {  // the first launch's result: Ms, cs, the last four tokens
-      const int32_t *res = a.self_res + (size_t)b * (R + 6);
-      const int v = lane < 6 ? __ldg(res + lane) : 0;
+    if (FROM_RES) {  // the first launch's result: Ms, cs, the last four tokens; the delta's
+      const int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
+      const int v = lane < 6 ? __ldg(res + lane) : (lane < 10 ? __ldg(res + R + lane) : 0);
       if (lane >= 2 && lane < 6) s_early[lane - 2] = v;
       early = n >= 4;
       const int Ms = __shfl_sync(FULL, v, 0), cs = __shfl_sync(FULL, v, 1);
-      if (lane == 0) { s_Ms = Ms; s_cs = cs; }
+      const int Md = __shfl_sync(FULL, v, 6), cd = __shfl_sync(FULL, v, 7);
+      const int ds = __shfl_sync(FULL, v, 8), dv = __shfl_sync(FULL, v, 9);
+      if (lane == 0) {
+        s_Ms = Ms;
+        s_cs = cs;
+        s_Md = Md;
+        s_cd = cd;
+        s_ds = ds;
+        s_dv = dv;
+      }
     }
     if (signal) {  // publish the updated row to the ingest CTA
       __threadfence();
@@ -757,6 +1010,13 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_c0c = 0;
       s_cpf = 0;
       s_ckey = 0;
+      s_ep = e0;
+      s_best_self = 0;
+      s_best_delta = 0;
+      if (!FROM_RES) {
+        s_Md = 0;
+        s_cd = 0;
+      }
     }
   } else if (!SELF_ONLY && a.desc != nullptr && cp.N >= 2 && cp.GT == nullptr) {
     const int sh = 5 * cp.Lmax;
@@ -772,7 +1032,11 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int n = s_n;
   int32_t *dr = a.drafts + (size_t)b * k;
   float *pr = a.probs ? a.probs + (size_t)b * k : nullptr;
+  // fused step with a delta: the ingest CTA may wait for every row CTA to be
+  // done with the ring before appending to it
+  const bool done_signal = MODE == 0 && a.dcap > 0 && a.ing_m > 0 && a.step_ready != nullptr;
   if (!((a.active == nullptr || a.active[b] != 0) && n > 0)) {
+    if (done_signal && tid == 0) step_done(a.step_sync, s_ep);
     if constexpr (!SELF_ONLY) {  // (the self-only launch leaves the outputs to the second)
       for (int d = tid; d < k; d += nthr) {
         dr[d] = -1;
@@ -814,10 +1078,12 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // publishes it through a shared flag; the probe warps read it at their
   // decision points to skip levels that cannot win, which only saves work.
   if (FROM_RES && warp == 0) {
-    // the self result of the first launch: the most recent ends of length Ms
-    const int32_t *res = a.self_res + (size_t)b * (R + 6);
-    const int c = s_cs;
+    // the self result of the first launch: the most recent ends of length Ms;
+    // the delta's most recent ends of length Md
+    const int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
+    const int c = s_cs, cd = s_cd;
     for (int i = lane; i < c; i += 32) s_occ[i] = __ldg(res + 6 + i);
+    for (int i = lane; i < cd; i += 32) s_wlist1[i] = __ldg(res + R + 10 + i);
     __syncwarp();
     if (lane == 0) {
       __threadfence_block();
@@ -825,15 +1091,12 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     }
   } else if (!FROM_RES && warp < a.nself) {
     int Mw, cnt, cnt1;
-    self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, s_wlist1 + warp * R, lane, sc, Mw, cnt,
-                 cnt1);
+    self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, s_wlist1 + warp * R, &s_best_self, lane,
+                 sc, Mw, cnt, cnt1);
     if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; s_wcnt1[warp] = cnt1; }
-    __threadfence_block();
-    __syncwarp();
-    int last = 0;
-    if (lane == 0) last = atomicAdd(&s_self_done, 1) == a.nself - 1;
-    last = __shfl_sync(FULL, last, 0);
-    if (last) {
+    // The self result: the longest length over the warps and its most recent
+    // ends (warps hold ascending ranges); published to the probe warps.
+    auto merge_self = [&]() {
       __threadfence_block();
       int Ms = 0;
       for (int w = 0; w < a.nself; ++w) Ms = max(Ms, s_wM[w]);
@@ -861,13 +1124,70 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       }
       if (SELF_ONLY) {  // the row's self result for the second launch
         __syncwarp();
-        int32_t *res = a.self_res + (size_t)b * (R + 6);
+        int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
         for (int i = lane; i < c; i += 32) res[6 + i] = s_occ[i];
         if (lane < 4) res[2 + lane] = lane < dl ? s_tail[lane] : 0;
         if (lane == 0) {
           res[0] = Ms;
           res[1] = c;
         }
+      }
+    };
+    if (s_dv > 0 && D >= 2 && n >= 2) {
+      // The delta, after the row.  Its first windows are requested before the
+      // self merge (each warp's ring is free again); the per-warp lists are
+      // reused once warp 0 has merged the row's.
+      int4 *sring = s_ring + warp * (SR * 32);
+      DeltaScan dsc;
+      const bool has = delta_prefetch(a.ring, a.C, s_ds, s_dv, Z, warp, a.nself, lane, sring, dsc);
+      self_sync(a.nself);
+      if (warp == 0) merge_self();
+      self_sync(a.nself);
+      int dM = 0, dcnt = 0;
+      if (has)
+        delta_process(a.ring, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, s_wlist + warp * R,
+                      &s_best_delta, dM, dcnt);
+      if (lane == 0) { s_wM[warp] = dM; s_wcnt[warp] = dcnt; }
+      self_sync(a.nself);
+      if (warp == 0) {  // longest delta match; its ends, most recent first, into s_wlist1
+        int Md = 0;
+        for (int w = 0; w < a.nself; ++w) Md = max(Md, s_wM[w]);
+        int c = 0;
+        for (int w = a.nself - 1; w >= 0 && c < R && Md > 0; --w) {
+          if (s_wM[w] != Md) continue;
+          const int mm = min(s_wcnt[w], R - c);
+          for (int i = lane; i < mm; i += 32) s_wlist1[c + i] = s_wlist[w * R + i];
+          c += mm;
+        }
+        if (lane == 0) {
+          s_Md = Md;
+          s_cd = c;
+        }
+        if (SELF_ONLY) {
+          __syncwarp();
+          int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
+          for (int i = lane; i < c; i += 32) res[R + 10 + i] = s_wlist1[i];
+          if (lane == 0) {
+            res[R + 6] = Md;
+            res[R + 7] = c;
+            res[R + 8] = (int)s_ds;
+            res[R + 9] = s_dv;
+          }
+        }
+      }
+    } else {
+      __threadfence_block();
+      __syncwarp();
+      int last = 0;
+      if (lane == 0) last = atomicAdd(&s_self_done, 1) == a.nself - 1;
+      last = __shfl_sync(FULL, last, 0);
+      if (last) merge_self();  // the last self warp to finish
+      if (SELF_ONLY && warp == 0 && lane == 0) {  // no delta for this row
+        int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
+        res[R + 6] = 0;
+        res[R + 7] = 0;
+        res[R + 8] = (int)s_ds;
+        res[R + 9] = 0;
       }
     }
   } else if (corpus_ok) {
@@ -1137,18 +1457,43 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __syncthreads();
 
   // ---- the longer match wins (equal lengths: the row itself) ----
-  const int Ms = s_Ms, Mc = corpus_ok ? s_Mc : 0;
+  // The corpus is the snapshot followed by the delta: its longest match is
+  // the longer of the two, and at equal lengths the delta's ends are the more
+  // recent, so they come first and the snapshot's fill the rest of the R.
+  const int Ms = s_Ms, Mcs = corpus_ok ? s_Mc : 0, Md = s_Md;
+  const int Mc = max(Mcs, Md);
   int src, M;
   if (Mc > Ms) { src = 2; M = Mc; }
   else { src = Ms > 0 ? 1 : 0; M = Ms; }
+  const int nd = src == 2 && Md == Mc ? s_cd : 0;               // delta ends voting
+  const int ns = src == 2 && Mcs == Mc ? min(s_c0c, R - nd) : 0;  // snapshot ends voting
   const int cap = M > 0 ? draft_cap(a, M, n) : 0;
-  const int c0 = src == 2 ? s_c0c : s_cs;
+  const int c0 = src == 2 ? nd + ns : s_cs;
   const int *occ = src == 2 ? s_occc : s_occ;
+  if (nd > 0) {
+    // occurrences: the delta's ends, then the ns most recent of the snapshot's
+    // (ranked by position; they are distinct) -- into s_occ, unused when the
+    // corpus wins
+    const int c0c = Mcs == Mc ? s_c0c : 0;
+    for (int i = tid; i < nd; i += nthr) s_occ[i] = s_wlist1[i];
+    for (int i = tid; i < c0c; i += nthr) {
+      const int e = s_occc[i];
+      int rank = 0;
+      if (ns < c0c)
+        for (int j = 0; j < c0c; ++j) rank += s_occc[j] > e;
+      else
+        rank = i;
+      if (rank < ns) s_occ[nd + rank] = e;
+    }
+    __syncthreads();
+    occ = s_occ;
+  }
   int *cont = s_big;                  // cont[o * capp + d]: rows 16-byte aligned
   const int capp = (cap + 3) & ~3;
   if (cap > 0 && c0 > 0) {
-    const int tot = (src == 2 && s_cpf) ? 0 : c0 * cap;  // prefetched by the probe warps
-    const int ck = src == 2 ? s_ckey : 0;
+    // (prefetched by the probe warps when only the snapshot's ends vote)
+    const int tot = (src == 2 && s_cpf && nd == 0) ? 0 : c0 * cap;
+    const int ck = src == 2 && nd == 0 ? s_ckey : 0;
     const int *occp = reinterpret_cast<const int *>(s_L) + a.cand_cap;
     for (int idx = tid; idx < tot; idx += nthr) {
       const int o = idx / cap, d = idx - o * cap;
@@ -1156,6 +1501,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       int v;
       if (src == 1) {
         v = pos <= n - 1 ? row[pos] : 0;
+      } else if (o < nd) {  // a delta end: Y[pos], the sentinel past the visible part
+        long long q = s_ds + pos;
+        if (q >= a.C) q -= a.C;
+        v = pos < s_dv ? a.ring[q] : Z;
       } else if (ck != 0 && ck + d <= 3) {  // inside the hit's suffix key (KEY_END: past the text)
         const int *kq = reinterpret_cast<const int *>(cp.K + occp[o]);
         v = __ldg(kq + ck + d);
@@ -1180,6 +1529,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     }
     __syncthreads();
   }
+  if (done_signal && tid == 0) step_done(a.step_sync, s_ep);  // the row's ring reads are over
   if (warp != 0) return;
 
   // ---- depth-wise majority vote (one warp, up to 4 occurrences per lane) ----
@@ -1421,9 +1771,10 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
       propose_kernel<640, 1, 0><<<grid, 32 * warps, smem, st>>>(a);
     return cudaGetLastError();
   }
-  // first launch: update + self scan of every row (no corpus, no ingest)
+  // first launch: update + self scan of every row, and of the delta (no
+  // snapshot probe, no ingest; the descriptor only tells where the delta starts)
   ProposeArgs a1 = a;
-  a1.desc = nullptr;
+  if (a.dcap == 0) a1.desc = nullptr;
   a1.ing_m = 0;
   const size_t smem1 = propose_smem_bytes(1, a.nself, a.R, a.k, a.cand_cap);
   if (a.nself <= 8)

@@ -28,6 +28,8 @@ struct CorpusDesc {
   const int32_t *rec;   // per-position records (RecShape), or null
   const int32_t *gt;    // n-gram table (below), or null
   uint64_t gt_mask;     // buckets - 1
+  int64_t lin_pushed;   // the ring's docs placed when X was linearised
+  int64_t lin_wp;       // the ring's write offset then (where the next doc went)
 };
 
 // n-gram table: for every distinct m-gram (m = 2, 3, 4) that begins a suffix
@@ -73,7 +75,35 @@ struct RingState {
   int32_t head;    // FIFO index of the oldest doc
   int32_t ndocs;
   int64_t snap_n;  // length of the last linearised snapshot
+  int64_t pushed;  // docs ever placed; the doc at FIFO index i is number pushed - ndocs + i
+  int64_t snap_pushed, snap_wp;  // pushed and wp when the last snapshot was linearised
 };
+
+// The docs placed after a snapshot was linearised (not in its index yet: the
+// delta), as one circular run of the ring, [start, start + len) mod C, len
+// tokens with the sentinels.  Docs are placed at the write offset in order,
+// so while older docs are still live the first delta doc starts where the
+// write offset was at linearisation; once every live doc is a delta doc, the
+// run is the whole live ring.
+struct DeltaView {
+  long long start, len;
+};
+
+__host__ __device__ inline DeltaView delta_view(const RingState &r, long long since, long long lin_wp,
+                                                long long C, const int64_t *doc_start) {
+  const long long first = since - (r.pushed - r.ndocs);  // FIFO index of the oldest delta doc
+  DeltaView v{0, 0};
+  if (first >= r.ndocs) return v;
+  if (first <= 0) {
+    v.start = doc_start[r.head];
+    v.len = r.live;
+  } else {
+    v.start = lin_wp;
+    v.len = r.wp - lin_wp;
+    if (v.len < 0) v.len += C;
+  }
+  return v;
+}
 
 struct ProposeArgs {
   int32_t *tok;            // [B, S]
@@ -106,14 +136,23 @@ struct ProposeArgs {
   int32_t *doc_len;
   int max_docs;
   uint32_t *step_ready;  // [max_batch] per row: the step epoch once updated
-  uint32_t *step_sync;   // [0] step epoch, [1] CTAs arrived in this launch
+  // [0] step epoch, [1] CTAs arrived in this launch, [2] row CTAs finished,
+  // [3] the epoch whose row CTAs have all finished
+  uint32_t *step_sync;
   uint32_t ing_skew;     // added to the awaited epoch (0; 1 only under test injection)
   // split launch (long rows): the self kernel writes per row, at self_res + b *
-  // (R + 6): Ms, cs, the last four tokens, then the cs most recent ends; the
-  // corpus kernel reads them back instead of scanning
+  // self_res_ints(R): Ms, cs, the last four tokens, the cs most recent ends;
+  // then Md, cd, the delta's start and visible length, the cd most recent
+  // delta ends.  The corpus kernel reads them back instead of scanning.
   int32_t *self_res;
   int split;             // 0: one fused kernel; 1: self kernel + corpus kernel
+  // Delta (docs placed after the snapshot was linearised): searched by brute
+  // force up to dcap tokens, oldest first; 0: not searched.  Needs ring, C
+  // (a multiple of WIN), rs and doc_start.
+  long long dcap;
 };
+
+__host__ __device__ constexpr int self_res_ints(int R) { return 2 * R + 10; }
 
 // propose.cu
 size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap);  // mode as the kernel's
@@ -143,7 +182,7 @@ cudaError_t launch_gram_table(const int4 *keys, int64_t n, int32_t *gt, uint64_t
                               cudaStream_t st);
 cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
                         const int32_t *rec, const int32_t *gt, uint64_t gt_mask,
-                        int64_t n, uint64_t gen, cudaStream_t st);
+                        int64_t n, uint64_t gen, const RingState *rs, cudaStream_t st);
 // keys[p] = text[sa[p] .. sa[p]+3] (KEY_END past n), on `st`
 cudaError_t launch_suffix_keys(const int32_t *text, const int32_t *sa, int64_t n, int4 *keys,
                                cudaStream_t st);

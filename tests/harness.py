@@ -4,7 +4,9 @@ Inputs come from model_free_suffix_gb300.workload; the oracle never sees a
 value produced by the CUDA path.  Build and swap points of the corpus index
 are fixed in advance (a build is started after a step's ingest once enough
 tokens arrived, and swapped in with a blocking poll before the next step),
-so both sides use the same snapshot at every step.
+so both sides use the same snapshot at every step.  With a delta capacity the
+oracle's corpus is that snapshot followed by the docs placed since it was
+linearised (oracle Ring.delta), cut at the capacity.
 """
 from __future__ import annotations
 
@@ -85,13 +87,17 @@ class Lockstep:
     def __init__(self, cfg: W.Config, seed: int = 0, B: Optional[int] = None,
                  steps: Optional[int] = None, finish_frac: Optional[float] = None,
                  corpus: Optional[int] = None, drafter_over: Optional[dict] = None,
-                 param_over: Optional[dict] = None, fused: bool = False):
+                 param_over: Optional[dict] = None, fused: bool = False, delta: int = 0):
         self.cfg = cfg
+        self.delta = delta  # delta capacity in tokens (0: only swapped snapshots are matched)
         self.fused = fused  # drive each step through sgd_step (update + propose + ingest)
         self.trace = W.ServingTrace(cfg, seed=seed, steps=steps, finish_frac=finish_frac, B=B)
         self.B = self.trace.B
         self.corpus = cfg.corpus_tokens if corpus is None else corpus
-        self.dr = drafter_for(cfg, B=self.B, corpus=self.corpus, **(drafter_over or {}))
+        over = dict(drafter_over or {})
+        if delta:
+            over["delta_capacity"] = delta
+        self.dr = drafter_for(cfg, B=self.B, corpus=self.corpus, **over)
         self.p = params_for(cfg, **(param_over or {}))
         tok, n = self.trace.initial()
         self.o_tok, self.o_n = tok.copy(), n.copy()
@@ -101,6 +107,8 @@ class Lockstep:
         self.out = self.dr.new_outputs(self.B)
         self.X = None            # oracle's current snapshot
         self.X_pending = None
+        self.since = 0           # ring docs placed when the current snapshot was linearised
+        self.since_pending = 0
         self.ring = O.Ring(self.corpus, 65536, cfg.V) if self.corpus else None
         self.ingested_since_build = 0
         self.build_pending = False
@@ -132,6 +140,7 @@ class Lockstep:
     def start_build(self):
         self.dr.build_sa(self.side)
         self.X_pending = self.ring.snapshot()
+        self.since_pending = self.ring.pushed
         self.build_pending = True
         self.ingested_since_build = 0
 
@@ -140,11 +149,18 @@ class Lockstep:
         assert st == 1, st
         self.generation = gen
         self.X = self.X_pending
+        self.since = self.since_pending
         self.build_pending = False
 
     def build_and_swap(self):
         self.start_build()
         self.swap()
+
+    def oracle_corpus(self):
+        """The oracle's corpus text for the next propose."""
+        if not self.delta or self.ring is None:
+            return self.X
+        return O.corpus_text(self.X, self.ring.delta(self.since, self.delta))
 
     # steps -------------------------------------------------------------------
     def step(self, check_rows=None, check=True, check_state=False):
@@ -163,7 +179,8 @@ class Lockstep:
             self.dr.propose_with_update(self.tok, self.n, sampled, out=self.out)
         O.update_state(self.o_tok, self.o_n, sd.sampled, self.cfg.V)
         if check:
-            orc = O.propose(self.p, self.o_tok, self.o_n, X=self.X, rows=check_rows, threads=THREADS)
+            orc = O.propose(self.p, self.o_tok, self.o_n, X=self.oracle_corpus(), rows=check_rows,
+                            threads=THREADS)
             compare(self.out, orc, rows=check_rows, ctx="step %d" % self.trace.step_index)
             invariants(self.out, self.cfg.k, self.p.min_prob)
         if check_state:

@@ -31,6 +31,7 @@ def test_config_defaults(lib):
     assert (c.spec_factor_num, c.spec_factor_den) == (1, 1)
     assert (c.min_prob_num, c.min_prob_den) == (1, 10)
     assert c.corpus_capacity == 1 << 20
+    assert c.delta_capacity == 0  # newly ingested docs wait for the next swap
 
 
 def test_config_set_float_rationals(lib):
@@ -67,6 +68,13 @@ def test_create_rejects_bad_knobs_before_touching_the_gpu(lib):
         setattr(c, field, val)
         h = ctypes.c_void_p()
         assert L.sgd_create(ctypes.byref(c), 0, ctypes.byref(h)) == lib.SGD_EINVAL, field
+    # the delta: within the ring, and the ring a whole number of 128-token windows
+    for cap, dcap in [(1 << 20, -1), (1 << 20, (1 << 20) + 1), (1000, 64), (0, 128)]:
+        c = lib.SgdConfig()
+        L.sgd_config_default(ctypes.byref(c))
+        c.corpus_capacity, c.delta_capacity = cap, dcap
+        h = ctypes.c_void_p()
+        assert L.sgd_create(ctypes.byref(c), 0, ctypes.byref(h)) == lib.SGD_EINVAL, (cap, dcap)
 
 
 def test_python_binding_fails_loudly_without_library(tmp_path, monkeypatch):

@@ -54,10 +54,12 @@ def test_fused_step_matches_oracle(finish_frac, mode):
     ls.close()
 
 
+@pytest.mark.parametrize("delta", [0, 2048], ids=["no-delta", "delta"])
 @pytest.mark.parametrize("mode", [1, 2], ids=["one-launch", "two-launch"])
-def test_fused_step_graph_replays(mode):
+def test_fused_step_graph_replays(mode, delta):
     """One captured sgd_step replayed with new inputs staged into its buffers:
-    every replay must wait for its own rows' updates (fresh epoch per launch)."""
+    every replay must wait for its own rows' updates (fresh epoch per launch).
+    With a delta the rows also match the docs ingested since the last swap."""
     W, O, H = _mods()
     from model_free_suffix_gb300 import SuffixDrafter
     V, S, B, T, m = 97, 256, 24, 5, 6
@@ -65,8 +67,9 @@ def test_fused_step_graph_replays(mode):
     C = 2048
     dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=8, max_tree_depth=16,
                        max_occurrences=16, max_sampled=T, corpus_capacity=C, max_docs=256,
-                       propose_mode=mode)
+                       propose_mode=mode, delta_capacity=delta)
     ring = O.Ring(C, 256, V)
+    since = 0
     p = O.Params(S=S, V=V, k=8, D=16, R=16)
     tok = np.zeros((B, S), dtype=np.int32)
     n = rng.integers(40, 120, size=B).astype(np.int32)
@@ -103,7 +106,8 @@ def test_fused_step_graph_replays(mode):
         graph.replay()
         torch.cuda.synchronize()
         n[:] = n_after
-        orc = O.propose(p, tok, n, X=X)
+        Xc = O.corpus_text(X, ring.delta(since, delta)) if delta else X
+        orc = O.propose(p, tok, n, X=Xc)
         H.compare(out, orc, ctx="replay %d" % it)
         assert np.array_equal(g_n.cpu().numpy(), n)
         assert np.array_equal(g_tok.cpu().numpy(), tok)
@@ -113,14 +117,15 @@ def test_fused_step_graph_replays(mode):
         if it % 3 == 2:
             dr.build_sa(side)
             assert dr.poll(wait=True)[0] == 1
-            X = ring.snapshot()
+            X, since = ring.snapshot(), ring.pushed
             text, sa, _ = dr.export_snapshot()
             assert text.cpu().numpy().tolist() == X.tolist()
     assert dr.get_error() == 0
     dr.close()
 
 
-def test_step_wait_injection_skips_docs_and_recovers():
+@pytest.mark.parametrize("delta", [0, 1024], ids=["no-delta", "delta"])
+def test_step_wait_injection_skips_docs_and_recovers(delta):
     """A bounded wait that runs out (test injection: the awaited signal is never
     sent) skips the step's docs with SGD_ERR_INGEST_WAIT; drafting is unaffected
     and the next step ingests normally."""
@@ -128,7 +133,7 @@ def test_step_wait_injection_skips_docs_and_recovers():
     from model_free_suffix_gb300 import SuffixDrafter, _lib as L
     V, S, B, T = 31, 128, 8, 3
     dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=4, max_sampled=T,
-                       corpus_capacity=1024)
+                       corpus_capacity=1024, delta_capacity=delta)
     p = O.Params(S=S, V=V, k=4)
     tok = np.tile(np.arange(20, dtype=np.int32) % 7, (B, 1))
     full = np.zeros((B, S), dtype=np.int32)
@@ -152,6 +157,13 @@ def test_step_wait_injection_skips_docs_and_recovers():
     H.compare(out, O.propose(p, full, n, X=None), ctx="next step")
     assert dr.get_error() == 0
     assert dr.corpus_stats() == (10 + 1 + 12 + 1, 2)
+    if delta:  # the two docs are in the delta: the next step matches them
+        ring = O.Ring(1024, 65536, V)
+        ring.ingest(full, [0, 3], [0, 5], [10, 12], num_tokens=n)  # (tokens the updates left alone)
+        out = dr.step(g_tok, g_n, torch.from_numpy(samp).cuda(), rows[:0], st[:0], ln[:0])
+        torch.cuda.synchronize()
+        O.update_state(full, n, samp, V)
+        H.compare(out, O.propose(p, full, n, X=ring.delta(0, delta)), ctx="delta step")
     dr.close()
 
 
