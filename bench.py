@@ -309,8 +309,9 @@ def run_ours(args, rank, world, delta=0):
             dr.poll(wait=True, stream=stream)
         dr.close()
         return {"workload": "the serving loop above with delta_capacity=%d: the docs ingested "
-                            "since the current snapshot was linearised are matched too, by a "
-                            "brute-force scan of the ring in every row's CTA" % delta,
+                            "since the current snapshot was linearised are matched too (every "
+                            "delta position accounted for; each row reads the ring windows "
+                            "whose gram signature can hold an end that matters)" % delta,
                 "delta_capacity": delta, "steps": K, "mean_delta_tokens": round(dv, 1),
                 "us_per_step": round(1e3 * total_ms_max / K, 2),
                 "steps_per_s": round(world * K / (total_ms_max / 1e3), 2),

@@ -112,14 +112,17 @@ typedef struct {
                                   built after its ingest is swapped in.  > 0: the docs
                                   placed since the current snapshot was linearised (the
                                   delta, [PYPI] How it works, steps 2 and 4) are matched
-                                  too, by a brute-force scan of up to delta_capacity of
-                                  their tokens (sentinels included), oldest first; a doc
-                                  cut by the capacity is visible up to the cut and the
-                                  rest waits for the next swap.  The corpus a row matches
-                                  is then the snapshot followed by that text; delta ends
-                                  count as more recent than snapshot ends.  Requires
-                                  corpus_capacity to be a multiple of 128;
-                                  <= corpus_capacity. */
+                                  too: up to delta_capacity of their tokens (sentinels
+                                  included), oldest first; a doc cut by the capacity is
+                                  visible up to the cut and the rest waits for the next
+                                  swap.  The corpus a row matches is then the snapshot
+                                  followed by that text; delta ends count as more recent
+                                  than snapshot ends.  Every delta position is accounted
+                                  for, as by a brute-force scan, but each row reads only
+                                  the 128-token ring windows whose 2/3/4-gram signature
+                                  (kept with the ring: 8 bytes per ring token) can hold
+                                  an end that matters.  Requires corpus_capacity to be a
+                                  multiple of 128; <= corpus_capacity. */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)

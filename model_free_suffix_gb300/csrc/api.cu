@@ -17,6 +17,7 @@
 #include <new>
 #include <thread>
 
+#include "delta_sig.cuh"
 #include "sgd_internal.h"
 
 using namespace sgd;
@@ -59,6 +60,7 @@ struct sgd_ctx {
   uint64_t gt_mask = 0;
   CorpusDesc *d_desc = nullptr;
   IngestScratch ing{};
+  uint32_t *d_sig = nullptr;        // ring window signatures (with a delta)
   SaScratch sa{};
   int64_t *h_n = nullptr;      // pinned
   uint32_t *h_err = nullptr;   // pinned
@@ -150,6 +152,8 @@ void free_ctx(sgd_ctx *x) {
   cudaFree(x->ing.eff);
   cudaFree(x->ing.dest);
   cudaFree(x->ing.order);
+  cudaFree(x->ing.span);
+  cudaFree(x->d_sig);
   if (x->sa.keyA) sa_scratch_free(&x->sa);
   if (x->h_n) cudaFreeHost(x->h_n);
   if (x->h_err) cudaFreeHost(x->h_err);
@@ -373,6 +377,12 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
     al((void **)&x->ing.eff, (size_t)cfg->max_ingest_docs * 4);
     al((void **)&x->ing.dest, (size_t)cfg->max_ingest_docs * 8);
     al((void **)&x->ing.order, (size_t)cfg->max_ingest_docs * 4);
+    al((void **)&x->ing.span, 16);
+    if (cfg->delta_capacity > 0) {
+      // (C / WIN windows of SIG_WORDS words: 8 bytes per ring token)
+      al((void **)&x->d_sig, (size_t)(C / WIN) * SIG_WORDS * 4);
+      if (e == cudaSuccess) e = cudaMemset(x->d_sig, 0, (size_t)(C / WIN) * SIG_WORDS * 4);
+    }
     if (e == cudaSuccess) e = sa_scratch_alloc(&x->sa, C);
     if (e == cudaSuccess) e = cudaMemset(x->d_rs, 0, sizeof(RingState));
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_start, 0, (size_t)cfg->max_docs * 8);
@@ -454,6 +464,7 @@ static ProposeArgs base_args(sgd_ctx *x) {
     a.C = c.corpus_capacity;
     a.rs = x->d_rs;
     a.doc_start = x->d_doc_start;
+    a.sig = x->d_sig;
   }
   return a;
 }
@@ -679,7 +690,8 @@ int sgd_ingest(sgd_ctx *x, const int32_t *token_ids, const int32_t *num_tokens, 
   const cudaError_t e =
       launch_ingest(token_ids, num_tokens, B, x->cfg.seq_capacity, x->cfg.vocab_size, rows, starts,
                     lengths, n_docs, x->d_ring, x->cfg.corpus_capacity, x->d_rs, x->d_doc_start,
-                    x->d_doc_len, x->cfg.max_docs, x->ing, x->d_err, (cudaStream_t)stream, &launches);
+                    x->d_doc_len, x->cfg.max_docs, x->ing, x->d_sig, x->d_err, (cudaStream_t)stream,
+                    &launches);
   x->launches += launches;
   return check_cuda(e);
 }

@@ -57,14 +57,14 @@ __global__ void __launch_bounds__(PLAN_THREADS) ingest_plan(const int32_t *eff, 
                                                             RingState *rs, int64_t *doc_start,
                                                             int32_t *doc_len, int max_docs,
                                                             int64_t *dest, int32_t *order,
-                                                            uint32_t *err) {
+                                                            int64_t *span, uint32_t *err) {
   __shared__ int s_eff[PLAN_CHUNK];
   __shared__ int s_dl[PLAN_WINDOW];
   __shared__ RingState s_rs;
   const int tid = threadIdx.x;
   if (tid == 0) s_rs = *rs;
   __syncthreads();
-  PlanWalk w{s_rs, s_rs.ndocs, min(s_rs.ndocs, PLAN_WINDOW), 0, 0, 0, 0u};
+  PlanWalk w{s_rs, s_rs.ndocs, min(s_rs.ndocs, PLAN_WINDOW), 0, 0, 0, 0u, 0};
   for (int j = tid; j < w.win; j += blockDim.x) s_dl[j] = doc_len[(w.r.head + j) % max_docs];
   for (int c0 = 0; c0 < m; c0 += PLAN_CHUNK) {
     const int cn = min(PLAN_CHUNK, m - c0);
@@ -77,8 +77,17 @@ __global__ void __launch_bounds__(PLAN_THREADS) ingest_plan(const int32_t *eff, 
   }
   if (tid == 0) {
     *rs = w.r;
+    span[0] = s_rs.wp;
+    span[1] = w.placed;
     if (w.fl) atomicOr(err, w.fl);
   }
+}
+
+// The window signatures after a large call (its span: first position, tokens).
+__global__ void __launch_bounds__(256) sig_kernel(SigBuild g, const int64_t *span) {
+  __shared__ SigBatchSmem s;
+  if (span[1] <= 0) return;
+  sig_update_cta(g, span[0], span[1], s, blockIdx.x, gridDim.x);
 }
 
 // A call of up to SMALL_DOCS docs as one CTA.
@@ -256,21 +265,25 @@ __global__ void __launch_bounds__(256) suffix_keys_kernel(const int32_t *text, c
 cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S, int V,
                           const int32_t *rows, const int32_t *starts, const int32_t *lengths, int m,
                           int32_t *ring, int64_t C, RingState *rs, int64_t *doc_start,
-                          int32_t *doc_len, int max_docs, const IngestScratch &sc, uint32_t *err,
-                          cudaStream_t st, int *launches) {
+                          int32_t *doc_len, int max_docs, const IngestScratch &sc, uint32_t *sig,
+                          uint32_t *err, cudaStream_t st, int *launches) {
   if (m <= 0) return cudaSuccess;
   if (m <= SMALL_DOCS) {
     const SmallIngest g{tok, ntok, B, S, V, rows, starts, lengths, m, ring, C, rs,
-                        doc_start, doc_len, max_docs, err, nullptr, 0u, nullptr, nullptr, 0};
+                        doc_start, doc_len, max_docs, err, nullptr, 0u, nullptr, nullptr, 0, sig};
     ingest_small<<<1, PLAN_THREADS, 0, st>>>(g);
     *launches += 1;
     return cudaGetLastError();
   }
   ingest_measure<<<m, 256, 0, st>>>(tok, ntok, B, S, V, rows, starts, lengths, m, sc.eff, err);
   ingest_plan<<<1, PLAN_THREADS, 0, st>>>(sc.eff, m, C, rs, doc_start, doc_len, max_docs, sc.dest,
-                                          sc.order, err);
+                                          sc.order, sc.span, err);
   ingest_copy<<<m, 256, 0, st>>>(tok, S, rows, starts, sc.eff, sc.dest, m, ring, C, V);
   *launches += 3;
+  if (sig != nullptr) {
+    sig_kernel<<<2 * 152, 256, 0, st>>>(SigBuild{ring, C, V, sig, C / WIN}, sc.span);
+    *launches += 1;
+  }
   return cudaGetLastError();
 }
 

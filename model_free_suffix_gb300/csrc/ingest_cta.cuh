@@ -13,6 +13,7 @@
 
 #include <climits>
 
+#include "delta_sig.cuh"
 #include "sgd_internal.h"
 
 namespace sgd {
@@ -35,6 +36,7 @@ struct PlanWalk {
   int win;       // staged oldest lengths
   int evicted, pushed, ev_call;
   uint32_t fl;
+  long long placed;  // ring tokens the call's placements took (from the old write offset on)
 };
 
 __device__ inline void place_doc(PlanWalk &w, int i, int L, long long C, const int *s_dl,
@@ -65,6 +67,7 @@ __device__ inline void place_doc(PlanWalk &w, int i, int L, long long C, const i
   r.live += s;
   r.ndocs++;
   r.pushed++;
+  w.placed += s;
 }
 
 // Warp 0: inclusive prefix sums of c over the 32 lanes into s_cum[1..32].
@@ -102,6 +105,8 @@ struct SmallIngestSmem {
   int dl[PLAN_WINDOW];
   RingState rs;
   int stop;  // a wait gave up: no doc of the call is placed
+  long long placed;
+  SigBatchSmem sig;
 };
 
 struct SmallIngest {
@@ -126,6 +131,7 @@ struct SmallIngest {
   const uint32_t *sync;
   const CorpusDesc *desc;
   long long dcap;
+  uint32_t *sig;  // the ring's window signatures (null: none kept)
 };
 
 // Bounded wait for *f == expect; false if it gave up.
@@ -217,20 +223,23 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
     if (delta && !s.stop) {
       // the call writes at most T tokens from the write offset on; the rows'
       // visible delta ends at the write offset and starts len tokens before it,
-      // so the writes reach it only if T > C - len
+      // so the writes reach it only if T > C - len -- and the rebuilt
+      // signatures of the windows they touch reach its windows only if
+      // T > C - len - 2 WIN
       long long T = 0;
       for (int i = 0; i < m; ++i)
         if (s.first[i] > 0) T += s.first[i] + 1;
       const DeltaView v = delta_view(r0, g.desc->lin_pushed, g.desc->lin_wp, g.C, g.doc_start);
-      if (min(v.len, g.dcap) > 0 && T > g.C - v.len && !wait_flag(g.sync + 3, g.expect)) {
+      if (min(v.len, g.dcap) > 0 && T + 2 * WIN > g.C - v.len && !wait_flag(g.sync + 3, g.expect)) {
         for (int i = 0; i < m; ++i) s.first[i] = -1;
         atomicOr(g.err, SGD_ERR_INGEST_WAIT);
       }
     }
-    PlanWalk w{r0, r0.ndocs, win, 0, 0, 0, 0u};
+    PlanWalk w{r0, r0.ndocs, win, 0, 0, 0, 0u, 0};
     for (int i = 0; i < m; ++i)
       place_doc(w, i, s.first[i], g.C, s.dl, g.doc_start, g.doc_len, g.max_docs, s.dest, s.order);
     *g.rs = w.r;
+    s.placed = w.placed;
     if (w.fl) atomicOr(g.err, w.fl);
   }
   __syncthreads();
@@ -256,6 +265,10 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
 #pragma unroll
     for (int b = 0; b < SMALL_BATCH; ++b)
       if (pos[b] >= 0) g.ring[pos[b]] = v[b];
+  }
+  if (g.sig != nullptr && s.placed > 0) {
+    __syncthreads();  // the docs are in the ring
+    sig_update_cta(SigBuild{g.ring, g.C, g.V, g.sig, g.C / WIN}, r0.wp, s.placed, s.sig);
   }
 }
 

@@ -134,61 +134,90 @@ __device__ __forceinline__ int pair_extend(int jr, int lo, const int *cw, const 
 
 constexpr int LANE_DEPTH = 8;  // depth one lane extends an end to on its own
 
-// One window's ends whose last two tokens match the tail: bit l of mc marks
-// the end at pair index WIN + 4 l + c (lane l's component c), stored as
-// pos0 + c (pos0: lane l's first position).  With more than two of them each
-// lane extends its own ends token by token up to LANE_DEPTH; the ends that
-// may go deeper (and all of them when there are at most two) are extended by
-// the whole warp, one at a time.  Then the warp's longest length Mw and its
-// list of the R most recent ends of that length (positions descending: higher
-// lanes first, then higher components) take in this window's ends.
-__device__ __forceinline__ void window_ends(unsigned m0, unsigned m1, unsigned m2, unsigned m3,
-                                            int pos0, int lo, const int *cw, const int *pw,
-                                            int dlim, const int *s_tail, int tail1, int lane, int R,
-                                            int *list, int &Mw, int &cnt) {
-  const bool b0 = (m0 >> lane) & 1u, b1 = (m1 >> lane) & 1u;
-  const bool b2 = (m2 >> lane) & 1u, b3 = (m3 >> lane) & 1u;
-  int L0 = 0, L1 = 0, L2 = 0, L3 = 0;
-  if (__popc(m0) + __popc(m1) + __popc(m2) + __popc(m3) > 2) {
-    const int jr = WIN + 4 * lane, lim = min(dlim, LANE_DEPTH);
-    auto ext = [&](int j) {  // x[j] = tail[0] and x[j-1] = tail[1] already hold
-      int L = 2;
-      while (L < lim && j - L >= lo) {
-        const int p = j - L;
-        if ((p >= WIN ? cw[p - WIN] : pw[p]) != s_tail[L]) break;
-        ++L;
+// The match depth of a window's ends, from the window's tokens alone: lane l's
+// component c is the end at pair index jr = WIN + 4 l + c (x[jr] = cur.c; the
+// three tokens before lane l's first are the previous lane's last three, or
+// the window below's for lane 0: p1, p2, p3 = x[jr0 - 1 .. jr0 - 3] for
+// jr0 = WIN + 4 l).  L_c = 0 when the end is not wanted (ok_c false) or
+// matches fewer than k (2 <= k <= 4) of the tail's tokens; else its match
+// length when that is below 4 or below dlim; else -4 (at least 4, to be
+// extended).  Pair indices below lo hold no token.
+__device__ __forceinline__ void window_depths(const int4 &cur, int p1, int p2, int p3, int t0, int t1,
+                                              int t2, int t3, int dlim, int k, int lo, int lane,
+                                              bool ok0, bool ok1, bool ok2, bool ok3, int &L0,
+                                              int &L1, int &L2, int &L3) {
+  const int jr0 = WIN + 4 * lane;
+  auto depth = [&](bool ok, int x0, int x1, int x2, int x3, int jr) {
+    if (!ok || x0 != t0 || x1 != t1) return 0;
+    int d = 2;
+    if (dlim > 2 && x2 == t2) {
+      d = 3;
+      if (dlim > 3 && x3 == t3) d = 4;
+    }
+    d = min(d, jr - lo + 1);  // (only tokens at pair index >= lo exist)
+    if (d < k) return 0;
+    return d == 4 && dlim > 4 && jr - lo + 1 > 4 ? -4 : d;
+  };
+  L3 = depth(ok3, cur.w, cur.z, cur.y, cur.x, jr0 + 3);
+  L2 = depth(ok2, cur.z, cur.y, cur.x, p1, jr0 + 2);
+  L1 = depth(ok1, cur.y, cur.x, p1, p2, jr0 + 1);
+  L0 = depth(ok0, cur.x, p1, p2, p3, jr0);
+}
+
+// A window's ends (lengths from window_depths) into the warp's longest length
+// Mw and its list of the R most recent ends of that length, positions
+// descending (higher lanes first, then higher components).  An end of at
+// least 4 is extended here: with more than two of them each lane extends its
+// own token by token up to LANE_DEPTH, and those that may go deeper (all of
+// them when there are at most two) are extended by the whole warp, one at a
+// time.  Lane l's end c is stored as position pos0 + c.
+__device__ __forceinline__ void window_ends(int L0, int L1, int L2, int L3, int pos0, int lo,
+                                            const int *cw, const int *pw, int dlim, const int *s_tail,
+                                            int tail1, int lane, int R, int *list, int &Mw, int &cnt) {
+  unsigned m0 = __ballot_sync(FULL, L0 < 0), m1 = __ballot_sync(FULL, L1 < 0);
+  unsigned m2 = __ballot_sync(FULL, L2 < 0), m3 = __ballot_sync(FULL, L3 < 0);
+  if (m0 | m1 | m2 | m3) {
+    if (__popc(m0) + __popc(m1) + __popc(m2) + __popc(m3) > 2) {
+      const int jr = WIN + 4 * lane, lim = min(dlim, LANE_DEPTH);
+      auto ext = [&](int j) {  // the end at pair index j matches at least 4 tokens
+        int L = 4;
+        while (L < lim && j - L >= lo) {
+          const int p = j - L;
+          if ((p >= WIN ? cw[p - WIN] : pw[p]) != s_tail[L]) break;
+          ++L;
+        }
+        return L;
+      };
+      if (L0 < 0) L0 = ext(jr);
+      if (L1 < 0) L1 = ext(jr + 1);
+      if (L2 < 0) L2 = ext(jr + 2);
+      if (L3 < 0) L3 = ext(jr + 3);
+      const bool deep = lim < dlim;  // (one stopped by lo at exactly lim is redone: same length)
+      m0 = __ballot_sync(FULL, (m0 >> lane & 1u) && deep && L0 == lim);
+      m1 = __ballot_sync(FULL, (m1 >> lane & 1u) && deep && L1 == lim);
+      m2 = __ballot_sync(FULL, (m2 >> lane & 1u) && deep && L2 == lim);
+      m3 = __ballot_sync(FULL, (m3 >> lane & 1u) && deep && L3 == lim);
+    }
+    for (;;) {  // warp-wide, in descending position 4 * lane + c
+      int best = -1;
+      if (m0) best = 4 * (31 - __clz(m0));
+      if (m1) best = max(best, 4 * (31 - __clz(m1)) + 1);
+      if (m2) best = max(best, 4 * (31 - __clz(m2)) + 2);
+      if (m3) best = max(best, 4 * (31 - __clz(m3)) + 3);
+      if (best < 0) break;
+      const unsigned keep = ~(1u << (best >> 2));
+      const int bc = best & 3;
+      m0 = bc == 0 ? m0 & keep : m0;
+      m1 = bc == 1 ? m1 & keep : m1;
+      m2 = bc == 2 ? m2 & keep : m2;
+      m3 = bc == 3 ? m3 & keep : m3;
+      const int L = pair_extend(WIN + best, lo, cw, pw, dlim, s_tail, tail1, lane);
+      if (lane == (best >> 2)) {
+        if (bc == 0) L0 = L;
+        else if (bc == 1) L1 = L;
+        else if (bc == 2) L2 = L;
+        else L3 = L;
       }
-      return L;
-    };
-    if (b0) L0 = ext(jr);
-    if (b1) L1 = ext(jr + 1);
-    if (b2) L2 = ext(jr + 2);
-    if (b3) L3 = ext(jr + 3);
-    const bool deep = lim < dlim;  // (one stopped by lo at exactly lim is redone: same length)
-    m0 = __ballot_sync(FULL, b0 && deep && L0 == lim);
-    m1 = __ballot_sync(FULL, b1 && deep && L1 == lim);
-    m2 = __ballot_sync(FULL, b2 && deep && L2 == lim);
-    m3 = __ballot_sync(FULL, b3 && deep && L3 == lim);
-  }
-  for (;;) {  // warp-wide, in descending position 4 * lane + c
-    int best = -1;
-    if (m0) best = 4 * (31 - __clz(m0));
-    if (m1) best = max(best, 4 * (31 - __clz(m1)) + 1);
-    if (m2) best = max(best, 4 * (31 - __clz(m2)) + 2);
-    if (m3) best = max(best, 4 * (31 - __clz(m3)) + 3);
-    if (best < 0) break;
-    const unsigned keep = ~(1u << (best >> 2));
-    const int bc = best & 3;
-    m0 = bc == 0 ? m0 & keep : m0;
-    m1 = bc == 1 ? m1 & keep : m1;
-    m2 = bc == 2 ? m2 & keep : m2;
-    m3 = bc == 3 ? m3 & keep : m3;
-    const int L = pair_extend(WIN + best, lo, cw, pw, dlim, s_tail, tail1, lane);
-    if (lane == (best >> 2)) {
-      if (bc == 0) L0 = L;
-      else if (bc == 1) L1 = L;
-      else if (bc == 2) L2 = L;
-      else L3 = L;
     }
   }
   const int Lw = (int)__reduce_max_sync(FULL, (unsigned)max(max(L0, L1), max(L2, L3)));
@@ -196,45 +225,15 @@ __device__ __forceinline__ void window_ends(unsigned m0, unsigned m1, unsigned m
   if (Lw > Mw) { Mw = Lw; cnt = 0; }
   if (cnt >= R) return;
   const bool e0 = L0 == Mw, e1 = L1 == Mw, e2 = L2 == Mw, e3 = L3 == Mw;
-  const int mine = (int)e0 + (int)e1 + (int)e2 + (int)e3;
-  int x = mine;  // over lanes >= this one
-#pragma unroll
-  for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_down_sync(FULL, x, off);
-    if (lane + off < 32) x += y;
-  }
-  const int total = __shfl_sync(FULL, x, 0);
-  int slot = cnt + x - mine;
+  const unsigned E0 = __ballot_sync(FULL, e0), E1 = __ballot_sync(FULL, e1);
+  const unsigned E2 = __ballot_sync(FULL, e2), E3 = __ballot_sync(FULL, e3);
+  const unsigned above = lane == 31 ? 0u : (FULL << (lane + 1));  // the more recent lanes
+  int slot = cnt + __popc(E0 & above) + __popc(E1 & above) + __popc(E2 & above) + __popc(E3 & above);
   if (e3) { if (slot < R) list[slot] = pos0 + 3; ++slot; }
   if (e2) { if (slot < R) list[slot] = pos0 + 2; ++slot; }
   if (e1) { if (slot < R) list[slot] = pos0 + 1; ++slot; }
   if (e0) { if (slot < R) list[slot] = pos0; }
-  cnt = min(R, cnt + total);
-}
-
-// The ends of a window worth extending: lane l's component c (position 4l + c)
-// where ok_c holds and the last k tokens (2 <= k <= 4) are tail[k-1 .. 0]
-// (tk = tail[k], tail[2] and tail[3] only read when k says so).  An end that
-// matches fewer than k tokens cannot reach the CTA's longest length so far,
-// so it cannot be among the ends that vote.  prv is the window below (the
-// tokens before lane 0's first).
-__device__ __forceinline__ void kgram_ballots(const int4 &cur, const int4 &prv, int lane, int k, int t0,
-                                              int t1, int t2, int t3, bool ok0, bool ok1, bool ok2,
-                                              bool ok3, unsigned &m0, unsigned &m1, unsigned &m2,
-                                              unsigned &m3) {
-  int py = __shfl_up_sync(FULL, cur.y, 1), pz = __shfl_up_sync(FULL, cur.z, 1);
-  int pw = __shfl_up_sync(FULL, cur.w, 1);
-  const int by = __shfl_sync(FULL, prv.y, 31), bz = __shfl_sync(FULL, prv.z, 31);
-  const int bw = __shfl_sync(FULL, prv.w, 31);
-  if (lane == 0) { py = by; pz = bz; pw = bw; }
-  const bool g3 = k >= 3, g4 = k >= 4;
-  m3 = __ballot_sync(FULL, ok3 && cur.w == t0 && cur.z == t1 && (!g3 || cur.y == t2) &&
-                               (!g4 || cur.x == t3));
-  m2 = __ballot_sync(FULL, ok2 && cur.z == t0 && cur.y == t1 && (!g3 || cur.x == t2) &&
-                               (!g4 || pw == t3));
-  m1 = __ballot_sync(FULL, ok1 && cur.y == t0 && cur.x == t1 && (!g3 || pw == t2) &&
-                               (!g4 || pz == t3));
-  m0 = __ballot_sync(FULL, ok0 && cur.x == t0 && pw == t1 && (!g3 || pz == t2) && (!g4 || py == t3));
+  cnt = min(R, cnt + __popc(E0) + __popc(E1) + __popc(E2) + __popc(E3));
 }
 
 // The CTA's longest length so far (over the warps scanning one text).
@@ -260,8 +259,9 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
   const int t0 = s_tail[0];
   const bool two = D >= 2 && n >= 2;
   const int t1 = two ? s_tail[1] : 0;
-  const int tail1 = lane + 1 < min(D, n) ? s_tail[1 + lane] : 0;
-  const int t2 = min(D, n) >= 3 ? s_tail[2] : 0, t3 = min(D, n) >= 4 ? s_tail[3] : 0;
+  const int dlim = min(D, n);  // (an end j <= n - 2 matches at most j + 1 < n tokens anyway)
+  const int tail1 = lane + 1 < dlim ? s_tail[1 + lane] : 0;
+  const int t2 = dlim >= 3 ? s_tail[2] : 0, t3 = dlim >= 4 ? s_tail[3] : 0;
   for (int wi = sc.whi, q = 0; wi >= sc.wlo; --wi, ++q) {
     // keep SPF windows in flight; then windows q and q + 1 must have landed
     self_fetch(row, wi - SPF - 1, lane, S, sc.ring, (q + SPF + 1) % SR);
@@ -291,16 +291,21 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
       // positions matching (t1, t0) -- or more of the tail once the CTA's
       // longest match is longer -- with the window below for lane 0's past
       const int4 prv = sc.ring[((q + 1) % SR) * 32 + lane];
-      unsigned m0, m1, m2, m3;
-      kgram_ballots(cur, prv, lane, kgram_k(Mw, s_best), t0, t1, t2, t3, a0 && two && p0 >= 1,
-                    a1 && two, a2 && two, a3 && two, m0, m1, m2, m3);
-      if (m0 | m1 | m2 | m3) {
+      int p1 = __shfl_up_sync(FULL, cur.w, 1), p2 = __shfl_up_sync(FULL, cur.z, 1);
+      int p3 = __shfl_up_sync(FULL, cur.y, 1);
+      const int bw = __shfl_sync(FULL, prv.w, 31), bz = __shfl_sync(FULL, prv.z, 31);
+      const int by = __shfl_sync(FULL, prv.y, 31);
+      if (lane == 0) { p1 = bw; p2 = bz; p3 = by; }
+      // the row's text starts at position 0: pair index WIN - base
+      int L0, L1, L2, L3;
+      window_depths(cur, p1, p2, p3, t0, t1, t2, t3, dlim, kgram_k(Mw, s_best), WIN - base, lane,
+                    a0 && two, a1 && two, a2 && two, a3 && two, L0, L1, L2, L3);
+      if (__any_sync(FULL, (L0 | L1 | L2 | L3) != 0)) {
         __syncwarp();  // every lane's copies visible to the warp (the extension reads across lanes)
         const int *cw = reinterpret_cast<const int *>(sc.ring + (q % SR) * 32);
         const int *pw = reinterpret_cast<const int *>(sc.ring + ((q + 1) % SR) * 32);
-        // the row's text starts at position 0: pair index WIN - base
         const int M0 = Mw;
-        window_ends(m0, m1, m2, m3, p0, WIN - base, cw, pw, D, s_tail, tail1, lane, R, list, Mw,
+        window_ends(L0, L1, L2, L3, p0, WIN - base, cw, pw, dlim, s_tail, tail1, lane, R, list, Mw,
                     cnt);
         if (Mw > M0 && lane == 0) atomicMax(s_best, Mw);
         __syncwarp();  // cross-lane reads of the slot done before it is refilled
@@ -311,121 +316,192 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
 }
 
 // ---------------------------------------------------------------------------
-// corpus: the delta, scanned by brute force
+// corpus: the delta
 //
 // The delta is the text Y[0, dv) of the docs placed after the snapshot was
-// linearised, read in place from the ring: Y[u] = ring[(ds + u) mod C].  The
-// self warps scan it like the row: in windows of WIN aligned ring positions
-// (C is a multiple of WIN), split into contiguous ranges over the warps and
-// streamed through each warp's cp.async ring, the most recent first.  An end
-// u counts when it has a continuation (u + 1 < dv and Y[u+1] is not the
+// linearised, read in place from the ring: Y[u] = ring[(ds + u) mod C].  An
+// end u counts when it has a continuation (u + 1 < dv and Y[u+1] is not the
 // sentinel) and matches at least the last two tokens (a corpus match needs
-// two); u >= 1 and positions before ds hold no token.  Each warp keeps its
-// longest length and the R most recent ends of that length.
-
-// Copy ring window rw into slot `slot` of the warp's ring, one group.
-__device__ __forceinline__ void delta_fetch(const int32_t *ring, int rw, int lane, int4 *sring,
-                                            int slot) {
-  const unsigned sa = (unsigned)__cvta_generic_to_shared(sring + slot * 32 + lane);
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n\tcp.async.commit_group;" ::"r"(sa),
-               "l"(ring + (size_t)rw * WIN + 4 * lane)
-               : "memory");
-}
+// two); u >= 1 and positions before ds hold no token.  The self warps share
+// its windows of WIN aligned ring positions (C is a multiple of WIN) in
+// contiguous ranges, each keeping its longest length and the R most recent
+// ends of that length.  Every end is accounted for, as a brute-force scan
+// would, but a window is read only when its gram signature (delta_sig.cuh)
+// says it may hold an end that can still matter: one matching at least
+// `need` tokens, where need is the warp's longest length (one more once R
+// ends of it are kept) and at least the CTA's longest so far.  A window that
+// is read is checked token by token, as the row's own windows are.
 
 // The delta's windows are numbered r = 0 .. nw-1 from the one holding Y[0]:
 // window r starts at Y index r WIN - off (off = ds mod WIN) and is ring
 // window (ds / WIN + r) mod (C / WIN).  All Y indices fit in 32 bits.
+constexpr int DNB = 4;  // windows read per batch: each with the one below (8 slots) + slot 8
+
+// The delta's windows are scanned newest first, in two stages.  Rounds: in
+// round t warp w takes the block of DNB windows that is (t nself + nself-1-w)
+// blocks below the newest, so that all warps work on the most recent windows
+// at once; after each round the warps' ends join one list for the CTA (most
+// recent first).  Rounds go on while they keep finding many ends and the
+// CTA's list holds fewer than R ends of its longest length: rows with a short
+// but frequent match find their R most recent ends this way in few steps.
+// Ranges: the windows below the rounds, split into contiguous ranges (warp
+// nself - 1 the newest).  Everything the rounds covered is more recent than
+// every range.
 struct DeltaScan {
-  int rlo, rhi;  // this warp's windows
-  int off;       // Y index 0 lies at this offset of window 0
-  int rw;        // ring window of the next fetch
-  int nrw;       // ring windows (C / WIN)
-  int above0;    // Y[first index above window rhi], or Z if that is not visible
+  int nw;   // windows
+  int off;  // Y index 0 lies at this offset of window 0
+  int w0;   // ring window of window 0
+  int nrw;  // ring windows (C / WIN)
 };
 
-// Warp w's windows and the first SPF + 1 fetches; false if it has none.
-__device__ __forceinline__ bool delta_prefetch(const int32_t *ring, long long C, long long ds, int dv,
-                                               int Z, int w, int nself, int lane, int4 *sring,
-                                               DeltaScan &sc) {
+__device__ __forceinline__ void delta_windows(long long C, long long ds, int dv, DeltaScan &sc) {
   sc.off = (int)(ds % WIN);
-  const int nw = (sc.off + dv - 1) / WIN + 1;
-  const int per = (nw + nself - 1) / nself;
-  sc.rlo = w * per;
-  sc.rhi = min(nw, sc.rlo + per) - 1;
-  if (sc.rhi < sc.rlo) return false;
+  sc.nw = (sc.off + dv - 1) / WIN + 1;
   sc.nrw = (int)(C / WIN);
-  const int rw_top = (int)((ds / WIN + sc.rhi) % sc.nrw);
-  const int ya = (sc.rhi + 1) * WIN - sc.off;  // Y index just above the top window
-  const int rwa = rw_top + 1 == sc.nrw ? 0 : rw_top + 1;
-  sc.above0 = ya < dv ? ring[(size_t)rwa * WIN] : Z;  // (plain load: the ring changes during a fused step)
-  // windows rhi, rhi - 1, ..., rhi - SPF (those below the delta hold other
-  // ring tokens; nothing reads them but the range checks)
-  int rw = rw_top;
-#pragma unroll
-  for (int q = 0; q <= SPF; ++q) {
-    delta_fetch(ring, rw, lane, sring, q);
-    rw = rw == 0 ? sc.nrw - 1 : rw - 1;
-  }
-  sc.rw = rw;
-  return true;
+  sc.w0 = (int)(ds / WIN);
 }
 
-__device__ void delta_process(const int32_t *ring, int dv, int Z, int D, int n, int R,
-                              const int *s_tail, int lane, int4 *sring, DeltaScan &sc, int *list,
-                              int *s_best, int &Mw, int &cnt) {
+// Copy 16 bytes per lane of ring window rw into ring slot `slot` (no commit).
+__device__ __forceinline__ void ring_copy(const int32_t *ring, int rw, int lane, int4 *sring, int slot) {
+  const unsigned sa = (unsigned)__cvta_generic_to_shared(sring + slot * 32 + lane);
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa),
+               "l"(ring + (size_t)rw * WIN + 4 * lane)
+               : "memory");
+}
+
+// The windows [rlo, rhi] of a warp's block or range into (Mw, cnt, list).
+// s_state[w]: warp w's (longest length << 16 | ends kept) in the same stage,
+// published as one word so that a warp can tell when more recent windows --
+// the CTA's list (cN ends of length cB) and the blocks or ranges of the warps
+// above -- already hold R ends of the CTA's longest length (its own ends of
+// that length then cannot vote).  A stale word only under-counts, which costs
+// reads, never results.
+__device__ void delta_process(const int32_t *ring, const uint32_t *sig, int dv, int Z, int D, int n,
+                              int R, const int *s_tail, int lane, int4 *sring, const DeltaScan &sc,
+                              int rlo, int rhi, int *list, int *s_best, int *s_state, int cB, int cN,
+                              int warp, int nself, int &Mw, int &cnt) {
   Mw = 0;
   cnt = 0;
   const int t0 = s_tail[0], t1 = s_tail[1];
   const int dlim = min(D, n);
   const int tail1 = lane + 1 < dlim ? s_tail[1 + lane] : 0;
   const int t2 = dlim >= 3 ? s_tail[2] : 0, t3 = dlim >= 4 ? s_tail[3] : 0;
-  int above0 = sc.above0, rw = sc.rw;
-  for (int r = sc.rhi, q = 0; r >= sc.rlo; --r, ++q) {
-    delta_fetch(ring, rw, lane, sring, (q + SPF + 1) % SR);
-    rw = rw == 0 ? sc.nrw - 1 : rw - 1;
-    asm volatile("cp.async.wait_group %0;" ::"n"(SPF) : "memory");
-    __syncwarp();  // every lane's copies of this window and the one below visible to the warp
-    const int4 cur = sring[(q % SR) * 32 + lane];
-    const int *cw = reinterpret_cast<const int *>(sring + (q % SR) * 32);
-    const int *pw = reinterpret_cast<const int *>(sring + ((q + 1) % SR) * 32);
-    const int first = __shfl_sync(FULL, cur.x, 0);
-    const int top = above0;  // the token after this window
-    above0 = first;
-    // Positions whose last k tokens match the tail, k = 2, 3 or 4 by the
-    // CTA's longest match so far (a shorter end cannot vote): the three
-    // tokens before each lane's first are the previous lane's last three, or
-    // for lane 0 the window below's.
-    const int4 bl = reinterpret_cast<const int4 *>(pw)[31];  // (one broadcast read)
-    int py = __shfl_up_sync(FULL, cur.y, 1), pz = __shfl_up_sync(FULL, cur.z, 1);
-    int pv = __shfl_up_sync(FULL, cur.w, 1);
-    if (lane == 0) { py = bl.y; pz = bl.z; pv = bl.w; }
-    const int k = kgram_k(Mw, s_best);
-    const bool g3 = k >= 3, g4 = k >= 4;
-    const bool h3 = cur.w == t0 && cur.z == t1 && (!g3 || cur.y == t2) && (!g4 || cur.x == t3);
-    const bool h2 = cur.z == t0 && cur.y == t1 && (!g3 || cur.x == t2) && (!g4 || pv == t3);
-    const bool h1 = cur.y == t0 && cur.x == t1 && (!g3 || pv == t2) && (!g4 || pz == t3);
-    const bool h0 = cur.x == t0 && pv == t1 && (!g3 || pz == t2) && (!g4 || py == t3);
-    if (!__any_sync(FULL, h0 | h1 | h2 | h3)) continue;
-    // ends among them: a continuation, Y index >= 1 (the token after lane
-    // 31's last is the window above's first)
-    const int dn = __shfl_down_sync(FULL, cur.x, 1);
-    const int after3 = lane == 31 ? top : dn;
-    const int yb = r * WIN - sc.off;  // Y index of the window's first token
-    const int u0 = yb + 4 * lane;
-    const unsigned m0 = __ballot_sync(FULL, h0 && cur.y != Z && u0 >= 1 && u0 + 1 < dv);
-    const unsigned m1 = __ballot_sync(FULL, h1 && cur.z != Z && u0 + 1 >= 1 && u0 + 2 < dv);
-    const unsigned m2 = __ballot_sync(FULL, h2 && cur.w != Z && u0 + 2 >= 1 && u0 + 3 < dv);
-    const unsigned m3 = __ballot_sync(FULL, h3 && after3 != Z && u0 + 3 >= 1 && u0 + 4 < dv);
-    if (m0 | m1 | m2 | m3) {
-      // pair index of Y[0] (clamped: below the pair nothing is excluded)
-      const int lo = max(-1, min(2 * WIN, WIN - yb));
-      const int M0 = Mw;
-      window_ends(m0, m1, m2, m3, u0, lo, cw, pw, dlim, s_tail, tail1, lane, R, list, Mw, cnt);
-      if (Mw > M0 && lane == 0) atomicMax(s_best, Mw);
+  const unsigned b2 = sig_bucket(2, t0, t1, 0, 0);
+  const unsigned b3 = dlim >= 3 ? sig_bucket(3, t0, t1, t2, 0) : 0u;
+  const unsigned b4 = dlim >= 4 ? sig_bucket(4, t0, t1, t2, t3) : 0u;
+  const int nrw = sc.nrw;
+  auto rwin = [&](int r) {  // ring window of delta window r (r >= -1)
+    int x = sc.w0 + r;
+    x %= nrw;
+    return x < 0 ? x + nrw : x;
+  };
+  // the shortest end that can still change the result (> dlim: none)
+  auto need = [&]() {
+    const int B = max(*(const volatile int *)s_best, 2);
+    int above = cB == B ? cN : 0;
+    for (int i = warp + 1; i < nself; ++i) {
+      const int st = ((const volatile int *)s_state)[i];
+      if ((st >> 16) == B) above += st & 0xffff;
     }
-    __syncwarp();  // cross-lane reads of the slots done before they are refilled
+    int nd = max(cnt < R ? Mw : Mw + 1, B);
+    if (above >= R && nd <= B) nd = B + 1;
+    return nd;
+  };
+  // windows r - 31 .. r whose signature has the bucket of the `o`-gram (o <= 4): bit i
+  auto candidates = [&](int r, int o, int ilo) {
+    const unsigned bk = o == 2 ? b2 : (o == 3 ? b3 : b4);
+    const int rr = r - lane;
+    bool hit = false;
+    if (lane >= ilo && rr >= rlo)
+      hit = (sig[(size_t)(bk >> 5) * nrw + rwin(rr)] >> (bk & 31)) & 1u;
+    return __ballot_sync(FULL, hit);
+  };
+  bool done = false;
+  for (int r = rhi; r >= rlo && !done; r -= 32) {
+    int nd = need();
+    if (nd > dlim) break;  // no end can matter any more
+    int o = min(nd, 4);
+    unsigned mask = candidates(r, o, 0);
+    while (mask) {
+      // the next DNB windows of the mask (descending), each with the one below
+      // and the first tokens of the one above
+      int wl[DNB];
+      int nb = 0;
+#pragma unroll
+      for (int j = 0; j < DNB; ++j) {
+        wl[j] = -1;
+        if (mask) {
+          const int i = __ffs(mask) - 1;
+          mask &= mask - 1;
+          wl[j] = r - i;
+          nb = j + 1;
+          ring_copy(ring, rwin(r - i), lane, sring, 2 * j);
+          ring_copy(ring, rwin(r - i - 1), lane, sring, 2 * j + 1);
+        }
+      }
+      if (lane < nb) {  // lane j: the first four tokens of the window above wl[j]
+        int wa = wl[0];
+#pragma unroll
+        for (int j = 1; j < DNB; ++j) wa = lane == j ? wl[j] : wa;
+        const unsigned sa = (unsigned)__cvta_generic_to_shared(sring + 8 * 32 + lane);
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(sa),
+                     "l"(ring + (size_t)rwin(wa + 1) * WIN)
+                     : "memory");
+      }
+      asm volatile("cp.async.commit_group;\n\tcp.async.wait_all;" ::: "memory");
+      __syncwarp();  // every lane's copies visible to the warp
+      nd = need();
+#pragma unroll
+      for (int j = 0; j < DNB; ++j) {
+        if (j >= nb || nd > dlim) break;
+        const int rj = wl[j];
+        const int4 cur = sring[(2 * j) * 32 + lane];
+        const int *cw = reinterpret_cast<const int *>(sring + (2 * j) * 32);
+        const int *pw = reinterpret_cast<const int *>(sring + (2 * j + 1) * 32);
+        const int top = reinterpret_cast<const int *>(sring + 8 * 32 + j)[0];  // the token after the window
+        // the depth of the ends matching at least k tokens (k = 2, 3 or 4 by
+        // the shortest end that can still matter); the three tokens before
+        // each lane's first are the previous lane's last three, or the window
+        // below's
+        const int4 bl = reinterpret_cast<const int4 *>(pw)[31];
+        int py = __shfl_up_sync(FULL, cur.y, 1), pz = __shfl_up_sync(FULL, cur.z, 1);
+        int pv = __shfl_up_sync(FULL, cur.w, 1);
+        if (lane == 0) { py = bl.y; pz = bl.z; pv = bl.w; }
+        // ends: a continuation (the token after lane 31's last is the window
+        // above's first), Y index >= 1
+        const int dn = __shfl_down_sync(FULL, cur.x, 1);
+        const int after3 = lane == 31 ? top : dn;
+        const int yb = rj * WIN - sc.off;  // Y index of the window's first token
+        const int u0 = yb + 4 * lane;
+        // pair index of Y[0] (clamped: below the pair nothing is excluded)
+        const int lo = max(-1, min(2 * WIN, WIN - yb));
+        int L0, L1, L2, L3;
+        window_depths(cur, pv, pz, py, t0, t1, t2, t3, dlim, min(nd, 4), lo, lane,
+                      cur.y != Z && u0 >= 1 && u0 + 1 < dv, cur.z != Z && u0 + 1 >= 1 && u0 + 2 < dv,
+                      cur.w != Z && u0 + 2 >= 1 && u0 + 3 < dv,
+                      after3 != Z && u0 + 3 >= 1 && u0 + 4 < dv, L0, L1, L2, L3);
+        if (__any_sync(FULL, (L0 | L1 | L2 | L3) != 0)) {
+          const int M0 = Mw, c0 = cnt;
+          window_ends(L0, L1, L2, L3, u0, lo, cw, pw, dlim, s_tail, tail1, lane, R, list, Mw, cnt);
+          if (Mw > M0 && lane == 0) atomicMax(s_best, Mw);
+          if (Mw != M0 || cnt != c0) nd = need();
+        }
+      }
+      if (lane == 0) *(volatile int *)&s_state[warp] = Mw << 16 | cnt;
+      __syncwarp();  // cross-lane reads of the slots done before they are refilled
+      // fewer windows can matter once longer ends are needed: narrow the rest
+      nd = need();
+      if (nd > dlim) {
+        done = true;
+        break;
+      }
+      if (min(nd, 4) != o && mask) {
+        o = min(nd, 4);
+        const int ilo = 32 - __clz(~mask & (mask - 1u));  // (bits below the lowest set one are done)
+        mask &= candidates(r, o, ilo);
+      }
+    }
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of the ring left in flight
 }
 
 // ---------------------------------------------------------------------------
@@ -883,7 +959,7 @@ __device__ __forceinline__ void step_ingest(const ProposeArgs &a) {
   __syncthreads();
   const SmallIngest g{a.tok, a.ntok, a.B, a.S, a.V, a.ing_rows, a.ing_starts, a.ing_lengths,
                       a.ing_m, a.ring, a.C, a.rs, a.doc_start, a.doc_len, a.max_docs, a.err,
-                      a.step_ready, s_e0 + 1 + a.ing_skew, a.step_sync, a.desc, a.dcap};
+                      a.step_ready, s_e0 + 1 + a.ing_skew, a.step_sync, a.desc, a.dcap, a.sig};
   ingest_small_cta(g, *reinterpret_cast<SmallIngestSmem *>(dsm));
 }
 
@@ -909,6 +985,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ long long s_ds;
   __shared__ int s_dv, s_Md, s_cd;
   __shared__ int s_best_self, s_best_delta;  // longest match so far in the row / the delta
+  __shared__ int s_dstate[MAX_SELF_WARPS];  // per self warp: its delta (length << 16 | ends)
+  __shared__ int s_dcB, s_dcN, s_dmore;     // the CTA's delta list: length, ends; another round
   __shared__ uint32_t s_ep;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
@@ -1013,6 +1091,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_ep = e0;
       s_best_self = 0;
       s_best_delta = 0;
+      for (int w = 0; w < MAX_SELF_WARPS; ++w) s_dstate[w] = 0;
+      s_dcB = 0;
+      s_dcN = 0;
       if (!FROM_RES) {
         s_Md = 0;
         s_cd = 0;
@@ -1139,37 +1220,83 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       // reused once warp 0 has merged the row's.
       int4 *sring = s_ring + warp * (SR * 32);
       DeltaScan dsc;
-      const bool has = delta_prefetch(a.ring, a.C, s_ds, s_dv, Z, warp, a.nself, lane, sring, dsc);
+      delta_windows(a.C, s_ds, s_dv, dsc);
+      const int G = DNB * a.nself;  // windows per round
       self_sync(a.nself);
       if (warp == 0) merge_self();
       self_sync(a.nself);
-      int dM = 0, dcnt = 0;
-      if (has)
-        delta_process(a.ring, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, s_wlist + warp * R,
-                      &s_best_delta, dM, dcnt);
-      if (lane == 0) { s_wM[warp] = dM; s_wcnt[warp] = dcnt; }
-      self_sync(a.nself);
-      if (warp == 0) {  // longest delta match; its ends, most recent first, into s_wlist1
-        int Md = 0;
-        for (int w = 0; w < a.nself; ++w) Md = max(Md, s_wM[w]);
-        int c = 0;
-        for (int w = a.nself - 1; w >= 0 && c < R && Md > 0; --w) {
-          if (s_wM[w] != Md) continue;
-          const int mm = min(s_wcnt[w], R - c);
-          for (int i = lane; i < mm; i += 32) s_wlist1[c + i] = s_wlist[w * R + i];
-          c += mm;
+      // (the row's per-warp lists are free now: s_wlist holds each warp's
+      // ends of a block or range, s_wlist1[0, R) the CTA's list)
+      int *wl = s_wlist + warp * R;
+      int covered = 0;
+      for (int t = 0;; ++t) {
+        const int hi = dsc.nw - 1 - t * G - DNB * (a.nself - 1 - warp);
+        int M = 0, c = 0;
+        delta_process(a.ring, a.sig, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, max(0, hi - DNB + 1),
+                      hi, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp, a.nself, M, c);
+        if (lane == 0) s_dstate[warp] = M << 16 | c;
+        self_sync(a.nself);
+        covered = min(dsc.nw, covered + G);
+        if (warp == 0) {  // the round's ends join the CTA's list (blocks newest first)
+          const int st = lane < a.nself ? s_dstate[lane] : 0;
+          const int Bn = max(s_dcB, (int)__reduce_max_sync(FULL, (unsigned)(st >> 16)));
+          int N = Bn > s_dcB ? 0 : s_dcN;
+          const int N0 = N;
+          if (Bn >= 2)
+            for (int w = a.nself - 1; w >= 0 && N < R; --w) {
+              const int sw = s_dstate[w];
+              if ((sw >> 16) != Bn) continue;
+              const int mm = min(sw & 0xffff, R - N);
+              for (int i = lane; i < mm; i += 32) s_wlist1[N + i] = s_wlist[w * R + i];
+              N += mm;
+            }
+          __syncwarp();
+          if (lane < a.nself) s_dstate[lane] = 0;
+          if (lane == 0) {
+            s_dcB = Bn;
+            s_dcN = N;
+            // another round if windows remain, the list is not full and this
+            // round was dense
+            s_dmore = covered < dsc.nw && N < R && 4 * (N - N0) >= R;
+          }
         }
+        self_sync(a.nself);
+        if (!s_dmore) break;
+      }
+      // the ranges below the rounds
+      const int rest = dsc.nw - covered;
+      const int per = (rest + a.nself - 1) / a.nself;
+      int dM = 0, dcnt = 0;
+      delta_process(a.ring, a.sig, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, warp * per,
+                    min(rest, (warp + 1) * per) - 1, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp,
+                    a.nself, dM, dcnt);
+      if (lane == 0) s_dstate[warp] = dM << 16 | dcnt;
+      self_sync(a.nself);
+      if (warp == 0) {
+        // longest delta match; its ends, most recent first: the CTA's list
+        // (when of that length), then the ranges from the newest warp down
+        const int st = lane < a.nself ? s_dstate[lane] : 0;
+        const int Md = max(s_dcB, (int)__reduce_max_sync(FULL, (unsigned)(st >> 16)));
+        int c = Md >= 2 && s_dcB == Md ? s_dcN : 0;
+        if (Md >= 2)
+          for (int w = a.nself - 1; w >= 0 && c < R; --w) {
+            const int sw = s_dstate[w];
+            if ((sw >> 16) != Md) continue;
+            const int mm = min(sw & 0xffff, R - c);
+            for (int i = lane; i < mm; i += 32) s_wlist1[c + i] = s_wlist[w * R + i];
+            c += mm;
+          }
         if (lane == 0) {
-          s_Md = Md;
-          s_cd = c;
+          s_Md = Md >= 2 ? Md : 0;
+          s_cd = Md >= 2 ? c : 0;
         }
         if (SELF_ONLY) {
           __syncwarp();
           int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
           for (int i = lane; i < c; i += 32) res[R + 10 + i] = s_wlist1[i];
           if (lane == 0) {
-            res[R + 6] = Md;
-            res[R + 7] = c;
+            res[R + 6] = Md >= 2 ? Md : 0;
+            res[R + 7] = Md >= 2 ? c : 0;
             res[R + 8] = (int)s_ds;
             res[R + 9] = s_dv;
           }

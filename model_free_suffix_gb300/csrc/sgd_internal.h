@@ -146,10 +146,11 @@ struct ProposeArgs {
   // delta ends.  The corpus kernel reads them back instead of scanning.
   int32_t *self_res;
   int split;             // 0: one fused kernel; 1: self kernel + corpus kernel
-  // Delta (docs placed after the snapshot was linearised): searched by brute
-  // force up to dcap tokens, oldest first; 0: not searched.  Needs ring, C
-  // (a multiple of WIN), rs and doc_start.
+  // Delta (docs placed after the snapshot was linearised): searched up to
+  // dcap tokens, oldest first; 0: not searched.  Needs ring, C (a multiple of
+  // WIN), rs, doc_start and sig, the ring's window signatures.
   long long dcap;
+  uint32_t *sig;
 };
 
 __host__ __device__ constexpr int self_res_ints(int R) { return 2 * R + 10; }
@@ -167,12 +168,13 @@ struct IngestScratch {
   int32_t *eff;     // [max_ingest_docs] effective doc length (-1: skip)
   int64_t *dest;    // [max_ingest_docs] ring offset or -1
   int32_t *order;   // [max_ingest_docs] docs pushed by this call, push order
+  int64_t *span;    // [2] the call's first ring position and the tokens its placements took
 };
 cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S, int V,
                           const int32_t *rows, const int32_t *starts, const int32_t *lengths,
                           int m, int32_t *ring, int64_t C, RingState *rs, int64_t *doc_start,
                           int32_t *doc_len, int max_docs, const IngestScratch &sc,
-                          uint32_t *err, cudaStream_t st, int *launches);
+                          uint32_t *sig, uint32_t *err, cudaStream_t st, int *launches);
 cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs,
                              const int64_t *doc_start, int max_docs, int32_t *out,
                              cudaStream_t st, int *launches);

@@ -168,16 +168,18 @@ def test_delta_results_equal_the_rebuilt_index():
     ring = O.Ring(1 << 16, 65536, V)
     p = O.Params(S=S, V=V, k=12, D=24, R=32)
     side = torch.cuda.Stream()
-    buf, lens = _docs_rows(rng, V, S, base, 40, 50, 400)
-    rows = torch.arange(40, dtype=torch.int32, device="cuda")
+    # 20 docs indexed, then 40 more in one call (more than the in-CTA ingest
+    # takes: the multi-kernel path, whose signature kernel then runs)
+    buf, lens = _docs_rows(rng, V, S, base, 60, 50, 400)
+    rows = torch.arange(60, dtype=torch.int32, device="cuda")
     g = torch.from_numpy(buf).cuda()
     dr.ingest(g[:20], rows[:20], torch.zeros_like(rows[:20]), torch.from_numpy(lens[:20]).cuda())
     ring.ingest(buf[:20], np.arange(20), np.zeros(20), lens[:20])
     dr.build_sa(side)
     assert dr.poll(wait=True)[0] == 1
     since = ring.pushed
-    dr.ingest(g[20:], rows[:20], torch.zeros_like(rows[:20]), torch.from_numpy(lens[20:]).cuda())
-    ring.ingest(buf[20:], np.arange(20), np.zeros(20), lens[20:])
+    dr.ingest(g[20:], rows[:40], torch.zeros_like(rows[:40]), torch.from_numpy(lens[20:]).cuda())
+    ring.ingest(buf[20:], np.arange(40), np.zeros(40), lens[20:])
     tok = np.zeros((B, S), dtype=np.int32)
     n = rng.integers(16, 400, size=B).astype(np.int32)
     for b in range(B):
