@@ -186,15 +186,21 @@ void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n_in,
   if (Mc > Ms) { source = 2; M = Mc; occ = occ_c; c0 = cc; }
   else { source = Ms > 0 ? 1 : 0; M = Ms; occ = occ_s; c0 = cs; }
   if (match_info) { match_info[0] = M; match_info[1] = source; }
+  /* Model Runner V2 drafts: the slots the vote leaves empty hold the row's
+   * last token, all k of them when there is no match ([DOCS] Model Runner V2) */
+  if (p->fixed_length) {
+    for (int32_t d = 0; d < p->k; d++) drafts[d] = t[n - 1];
+    *num_valid = p->k;
+  }
   if (M == 0 || c0 == 0) { free(occ_s); free(occ_c); return; }
 
-  /* length cap */
+  /* length cap (Model Runner V2: no factor, only k and the context) */
   int64_t cap = p->k;
-  cap = min64(cap, (p->fN * (int64_t)M) / p->fD + p->offset);
+  if (!p->fixed_length) cap = min64(cap, (p->fN * (int64_t)M) / p->fD + p->offset);
   int64_t room = (int64_t)p->S - n - 1;
   if (room < 0) room = 0;
   cap = min64(cap, room);
-  if (p->depth_sum_cap) cap = min64(cap, (int64_t)p->D - M);
+  if (p->depth_sum_cap && !p->fixed_length) cap = min64(cap, (int64_t)p->D - M);
   if (cap < 0) cap = 0;
 
   /* frequency-greedy expansion */
@@ -222,14 +228,14 @@ void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n_in,
         best_tok = val[o];
       }
     }
-    if ((int64_t)best_cnt * p->pD < p->pN * (int64_t)c0) break;
+    if (!p->fixed_length && (int64_t)best_cnt * p->pD < p->pN * (int64_t)c0) break;
     drafts[d] = best_tok;
     if (probs) probs[d] = (float)((double)best_cnt / (double)c0);
     sum += best_cnt;
     len++;
     for (int32_t o = 0; o < c0; o++) alive[o] = has[o] && val[o] == best_tok;
   }
-  *num_valid = len;
+  if (!p->fixed_length) *num_valid = len;
   if (score) *score = (float)((double)sum / (double)c0);
   free(alive); free(val); free(has); free(occ_s); free(occ_c);
 }

@@ -49,6 +49,10 @@ typedef struct {
   int64_t offset;       /* max_spec_offset                                         */
   int64_t pN, pD;       /* min_token_prob = pN / pD                                */
   int32_t depth_sum_cap;/* 1: also bound the draft by D - M                        */
+  int32_t fixed_length; /* 1: Model Runner V2 drafts ([DOCS] Model Runner V2): k
+                           tokens always, slots without a voted continuation hold
+                           the row's last token; factor, offset, min_token_prob
+                           and depth_sum_cap unused                              */
 } orc_params;
 
 /* Append the accepted prefix of one row's sampled ids ([PYPI] Quickstart,

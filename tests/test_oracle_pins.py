@@ -458,3 +458,74 @@ def test_delta_proposals_equal_the_rebuilt_index(orc):
         b = orc.propose(p, tok, n, X=ring.snapshot())
         assert np.array_equal(a.drafts, b.drafts) and np.array_equal(a.match_info, b.match_info)
         assert np.array_equal(a.num_valid, b.num_valid) and np.array_equal(a.score, b.score)
+
+
+# --------------------------------------------------------------------------
+# Model Runner V2 drafts ("Suffix Decoding" (vLLM docs), Model Runner V2: the
+# draft always has k tokens; slots without a match hold the last sampled token;
+# max_spec_factor and min_token_prob are not used)
+
+def _row(orc, p, t, X=None):
+    S = p.S
+    tok = np.zeros((1, S), dtype=np.int32)
+    tok[0, :len(t)] = t
+    return orc.propose(p, tok, np.array([len(t)], dtype=np.int32), X=X)
+
+
+def test_fixed_length_worked_examples(orc):
+    # row 5 6 7 5 6: the tail (5, 6) occurs once before, at 0..1, followed by 7 5 6
+    # and then nothing: the vote gives 7 5 6 (each 1/1), the fourth slot is the last
+    # token 6.  The default rule stops at floor(1.0 * 2) + 0 = 2 tokens instead.
+    p = orc.Params(S=16, V=10, k=4, D=8, R=4, fixed_length=True)
+    r = _row(orc, p, [5, 6, 7, 5, 6])
+    assert r.drafts[0].tolist() == [7, 5, 6, 6] and r.num_valid[0] == 4
+    assert r.probs[0].tolist() == [1.0, 1.0, 1.0, 0.0] and float(r.score[0]) == 3.0
+    assert r.match_info[0].tolist() == [2, 1]
+    r = _row(orc, orc.Params(S=16, V=10, k=4, D=8, R=4), [5, 6, 7, 5, 6])
+    assert r.drafts[0].tolist() == [7, 5, -1, -1] and r.num_valid[0] == 2
+    # no earlier 3 in 1 2 3: every slot is the last token, probability 0
+    r = _row(orc, p, [1, 2, 3])
+    assert r.drafts[0].tolist() == [3, 3, 3, 3] and r.num_valid[0] == 4
+    assert r.probs[0].tolist() == [0.0] * 4 and float(r.score[0]) == 0.0
+    assert r.match_info[0].tolist() == [0, 0]
+    # 9 1 9 2 9 3 9: three ends of length 1 (at 4, 2, 0) continue with 3, 2, 1; the
+    # tie goes to 1 (count 1 of 3), whose end (0) continues 9 2 9.  min_token_prob
+    # 0.5 would stop the default rule before the first token; here it is unused.
+    p = orc.Params(S=16, V=10, k=4, D=8, R=4, min_prob=(1, 2), fixed_length=True)
+    r = _row(orc, p, [9, 1, 9, 2, 9, 3, 9])
+    assert r.drafts[0].tolist() == [1, 9, 2, 9] and r.num_valid[0] == 4
+    assert np.allclose(r.probs[0], [1 / 3] * 4) and abs(float(r.score[0]) - 4 / 3) < 1e-6
+    r = _row(orc, orc.Params(S=16, V=10, k=4, D=8, R=4, min_prob=(1, 2), factor=(100, 1)),
+             [9, 1, 9, 2, 9, 3, 9])
+    assert r.num_valid[0] == 0 and r.drafts[0].tolist() == [-1] * 4
+
+
+def test_fixed_length_is_the_unstopped_vote_then_the_last_token(orc):
+    """On random rows (and a corpus): the voted part of a fixed-length draft is the
+    default draft with no probability floor and no factor cap; the rest is the
+    row's last token; inactive or empty rows stay empty."""
+    rng = np.random.default_rng(8)
+    V, S, k = 7, 96, 6
+    X = np.concatenate([np.append(rng.integers(0, V, rng.integers(5, 40)), V) for _ in range(12)])
+    for trial in range(40):
+        B = 6
+        tok = rng.integers(0, V, (B, S)).astype(np.int32)
+        n = rng.integers(0, S - 2, B).astype(np.int32)
+        n[0] = 0
+        act = np.ones(B, np.uint8)
+        act[1] = 0
+        Xc = X if trial % 2 else None
+        f = orc.propose(orc.Params(S=S, V=V, k=k, D=12, R=8, fixed_length=True), tok, n, X=Xc,
+                        active=act)
+        d = orc.propose(orc.Params(S=S, V=V, k=k, D=12, R=8, min_prob=(0, 1), factor=(10 ** 6, 1)),
+                        tok, n, X=Xc, active=act)
+        for b in range(B):
+            if not act[b] or n[b] == 0:
+                assert f.num_valid[b] == 0 and (f.drafts[b] == -1).all()
+                continue
+            m = d.num_valid[b]
+            assert f.num_valid[b] == k
+            assert f.drafts[b, :m].tolist() == d.drafts[b, :m].tolist()
+            assert (f.drafts[b, m:] == tok[b, n[b] - 1]).all()
+            assert np.array_equal(f.probs[b, :m], d.probs[b, :m]) and (f.probs[b, m:] == 0).all()
+            assert f.score[b] == d.score[b] and np.array_equal(f.match_info[b], d.match_info[b])
