@@ -123,6 +123,16 @@ typedef struct {
                                   (kept with the ring: 8 bytes per ring token) can hold
                                   an end that matters.  Requires corpus_capacity to be a
                                   multiple of 128; <= corpus_capacity. */
+  int32_t  draft_mode;         /* 0 (default): the draft stops where the vote's chain
+                                  probability falls below min_token_prob or at
+                                  floor(max_spec_factor * M) + max_spec_offset tokens;
+                                  -1 padded.  1: Model Runner V2 drafts ([DOCS] Model
+                                  Runner V2): always k tokens -- the vote runs while an
+                                  occurrence continues (within k and the context), the
+                                  slots it leaves hold the row's last token (probability
+                                  0), num_valid = k; max_spec_factor, max_spec_offset,
+                                  min_token_prob and depth_sum_cap are not used.  Rows
+                                  that are inactive or empty stay -1 / 0 either way. */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)

@@ -60,6 +60,7 @@ class SgdConfig(ctypes.Structure):
         ("corpus_gram_index", ctypes.c_int32),
         ("propose_mode", ctypes.c_int32),
         ("delta_capacity", ctypes.c_int64),
+        ("draft_mode", ctypes.c_int32),
     ]
 
 

@@ -115,6 +115,7 @@ int validate(const sgd_config &c) {
   if (c.propose_mode < 0 || c.propose_mode > 2) return SGD_EINVAL;
   if (c.delta_capacity < 0 || c.delta_capacity > c.corpus_capacity) return SGD_EINVAL;
   if (c.delta_capacity > 0 && c.corpus_capacity % WIN != 0) return SGD_EINVAL;
+  if (c.draft_mode != 0 && c.draft_mode != 1) return SGD_EINVAL;
   return SGD_OK;
 }
 
@@ -281,6 +282,7 @@ int sgd_config_default(sgd_config *c) {
   c->corpus_gram_index = 1;
   c->propose_mode = 0;
   c->delta_capacity = 0;
+  c->draft_mode = 0;
   c->self_warps = 0;
   return SGD_OK;
 }
@@ -458,6 +460,11 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.rsh = x->rsh;
   a.split = x->split;
   a.self_res = x->d_self_res;
+  if (c.draft_mode == 1) {  // no probability floor: the vote runs while an occurrence continues
+    a.fixed = 1;
+    a.pN = 0;
+    a.pD = 1;
+  }
   if (x->corpus && c.delta_capacity > 0) {  // the delta is read from the ring in place
     a.dcap = c.delta_capacity;
     a.ring = x->d_ring;

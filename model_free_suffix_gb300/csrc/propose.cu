@@ -867,12 +867,14 @@ __device__ void pick_bin(const int *hist, int need, int lane, int *s_sel, int *s
 
 
 // draft length bound: min(k, floor(factor * M) + offset, S - n - 1) [, D - M]
+// Tokens the vote may emit: k, the factor cap and the context (Model Runner
+// V2 drafts: k and the context only).
 __device__ __forceinline__ int draft_cap(const ProposeArgs &a, int M, int n) {
-  long long c = min((long long)a.k, a.fN * M / a.fD + a.offset);
+  long long c = a.fixed ? (long long)a.k : min((long long)a.k, a.fN * M / a.fD + a.offset);
   long long room = (long long)a.S - n - 1;
   if (room < 0) room = 0;
   c = min(c, room);
-  if (a.depth_sum_cap) c = min(c, (long long)a.D - M);
+  if (a.depth_sum_cap && !a.fixed) c = min(c, (long long)a.D - M);
   return c < 0 ? 0 : (int)c;
 }
 
@@ -1845,12 +1847,14 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       ++d;
     }
   }
+  // the slots the vote left empty: -1, or (Model Runner V2 drafts) the row's last token
+  const int fill = a.fixed ? s_tail[0] : -1;
   for (int d = len + lane; d < k; d += 32) {
-    dr[d] = -1;
+    dr[d] = fill;
     if (pr) pr[d] = 0.f;
   }
   if (lane == 0) {
-    a.num_valid[b] = len;
+    a.num_valid[b] = a.fixed ? k : len;
     if (a.score) a.score[b] = c0 > 0 ? (float)sum / (float)c0 : 0.f;
     if (a.match_info) { a.match_info[2 * b] = M; a.match_info[2 * b + 1] = src; }
   }

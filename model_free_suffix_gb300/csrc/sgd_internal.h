@@ -151,6 +151,10 @@ struct ProposeArgs {
   // WIN), rs, doc_start and sig, the ring's window signatures.
   long long dcap;
   uint32_t *sig;
+  // Model Runner V2 drafts: k tokens always, the vote not stopped by
+  // min_token_prob (pN = 0) nor capped by the factor, empty slots hold the
+  // row's last token
+  int fixed;
 };
 
 __host__ __device__ constexpr int self_res_ints(int R) { return 2 * R + 10; }

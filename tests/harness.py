@@ -81,6 +81,15 @@ def invariants(gpu, k, min_prob=(1, 10)):
     assert np.allclose(s, np.where(valid, p.astype(np.float64), 0).sum(1), rtol=1e-5, atol=1e-5)
 
 
+def invariants_fixed(gpu, k):
+    """Model Runner V2 drafts: k tokens or none, probabilities non-increasing
+    and 0 from the first filled slot on."""
+    d, n, p = to_np(gpu.drafts), to_np(gpu.num_valid), to_np(gpu.probs)
+    assert np.isin(n, [0, k]).all()
+    assert ((d == -1) == (n[:, None] == 0)).all()
+    assert (np.diff(p, axis=1) <= 0).all()
+
+
 class Lockstep:
     """One serving trace run on the GPU and the oracle side by side."""
 
@@ -182,7 +191,10 @@ class Lockstep:
             orc = O.propose(self.p, self.o_tok, self.o_n, X=self.oracle_corpus(), rows=check_rows,
                             threads=THREADS)
             compare(self.out, orc, rows=check_rows, ctx="step %d" % self.trace.step_index)
-            invariants(self.out, self.cfg.k, self.p.min_prob)
+            if self.p.fixed_length:
+                invariants_fixed(self.out, self.cfg.k)
+            else:
+                invariants(self.out, self.cfg.k, self.p.min_prob)
         if check_state:
             assert np.array_equal(to_np(self.n), self.o_n)
             assert np.array_equal(to_np(self.tok), self.o_tok)

@@ -32,6 +32,7 @@ def test_config_defaults(lib):
     assert (c.min_prob_num, c.min_prob_den) == (1, 10)
     assert c.corpus_capacity == 1 << 20
     assert c.delta_capacity == 0  # newly ingested docs wait for the next swap
+    assert c.draft_mode == 0      # drafts stop at the probability floor and the factor cap
 
 
 def test_config_set_float_rationals(lib):
@@ -61,7 +62,7 @@ def test_create_rejects_bad_knobs_before_touching_the_gpu(lib):
     L = lib.load()
     bad = [("seq_capacity", 4098), ("k", 0), ("k", 65), ("max_tree_depth", 129),
            ("max_occurrences", 0), ("corpus_cand_cap", 100), ("corpus_cand_cap", 32),
-           ("min_prob_den", 0), ("self_warps", 17)]
+           ("min_prob_den", 0), ("self_warps", 17), ("draft_mode", 2), ("draft_mode", -1)]
     for field, val in bad:
         c = lib.SgdConfig()
         L.sgd_config_default(ctypes.byref(c))

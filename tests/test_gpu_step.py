@@ -267,3 +267,22 @@ def test_bound_step_host_reuses_buffers():
         assert A.corpus_stats() == Bd.corpus_stats()
     A.close()
     Bd.close()
+
+
+@pytest.mark.parametrize("mode", [1, 2], ids=["one-launch", "two-launch"])
+def test_fixed_length_drafts_lockstep(mode):
+    """Model Runner V2 drafts (draft_mode 1: k tokens, the unstopped vote, the
+    row's last token in the empty slots) through the fused step, with the
+    corpus and rebuilds, against the oracle's fixed_length rule."""
+    W, O, H = _mods()
+    cfg = dataclasses.replace(W.CONFIGS["c3"], rebuild_tokens=4096)
+    ls = H.Lockstep(cfg, seed=9, B=64, steps=10, finish_frac=0.1, corpus=1 << 16, fused=True,
+                    drafter_over=dict(propose_mode=mode, draft_mode=1),
+                    param_over=dict(fixed_length=True))
+    ls.prefill(seed=9)
+    for _ in range(10):
+        ls.step(check_state=True)
+        nv = ls.out.num_valid.cpu().numpy()
+        assert (nv == cfg.k).all()  # every row here is active and non-empty
+    assert ls.dr.get_error() == 0
+    ls.close()
