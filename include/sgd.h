@@ -48,6 +48,7 @@ extern "C" {
 #define SGD_EBUILD     -6   /* the finished build reported failure; old index kept */
 #define SGD_ENOCORPUS  -7   /* the context was created without a corpus         */
 #define SGD_ETOOLARGE  -8   /* longer than the fixed scratch of sgd_suffix_array_noalloc */
+#define SGD_EIO        -9   /* sgd_save / sgd_load: the file could not be written or read */
 
 /* ---- sticky device error bits (sgd_get_error) --------------------------- */
 #define SGD_ERR_SAMPLED_TOKEN 0x1u  /* a sampled id >= V ended the accepted prefix    */
@@ -316,6 +317,26 @@ int sgd_export_snapshot(sgd_ctx *ctx, int32_t *text, int32_t *sa, int64_t capaci
 
 /* Live ring tokens (incl. sentinels) and documents.  Synchronises the device. */
 int sgd_corpus_stats(sgd_ctx *ctx, int64_t *live_tokens, int32_t *ndocs);
+
+/* The cross-request corpus to a file and back ([PYPI] Roadmap: global tree
+ * save & load), so that it survives a restart: the ring (live docs, their
+ * FIFO, docs ever placed), the current snapshot's text and where its delta
+ * starts.  Derived structures (suffix array, keys, records, n-gram table,
+ * delta signatures) are rebuilt by sgd_load, so a file is
+ * 4 C + 12 max_docs + 4 n bytes plus an 88-byte header, in the host's byte
+ * order.  After sgd_load the context drafts exactly as the saved one did and
+ * its generation has advanced by one.
+ *   sgd_save: waits for `stream` (the drafting stream), then writes `path`.
+ *   sgd_load: needs a context of the same vocab_size, corpus_capacity and
+ *   max_docs; reads and checks the whole file (layout, sizes, ids in [0, V],
+ *   the documents back to back ending at the write offset) before changing
+ *   anything, then rebuilds the snapshot's index on `stream` and waits for it.
+ * Both: SGD_EBUSY while a build is in flight or not yet swapped in,
+ * SGD_ENOCORPUS without a corpus, SGD_EIO if the file cannot be written or
+ * read (short file), SGD_EINVAL for a file that is not such a save or does
+ * not fit the context (nothing is changed then). */
+int sgd_save(sgd_ctx *ctx, const char *path, void *stream);
+int sgd_load(sgd_ctx *ctx, const char *path, void *stream);
 
 /* Figures of the last finished suffix-array build. */
 typedef struct {

@@ -20,6 +20,7 @@ SGD_EBUSY = -5
 SGD_EBUILD = -6
 SGD_ENOCORPUS = -7
 SGD_ETOOLARGE = -8
+SGD_EIO = -9
 NOALLOC_MAX_TOKENS = 65536
 
 ERR_SAMPLED_TOKEN = 0x1
@@ -117,6 +118,8 @@ def load() -> ctypes.CDLL:
         "sgd_suffix_array_noalloc": (ctypes.c_int, [P, i64, P, P]),
         "sgd_get_error": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_uint32), ctypes.c_int]),
         "sgd_export_snapshot": (ctypes.c_int, [P, P, P, i64, ctypes.POINTER(ctypes.c_int64), u64p]),
+        "sgd_save": (ctypes.c_int, [P, ctypes.c_char_p, P]),
+        "sgd_load": (ctypes.c_int, [P, ctypes.c_char_p, P]),
         "sgd_corpus_stats": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_int64),
                                             ctypes.POINTER(ctypes.c_int32)]),
         "sgd_build_stats": (ctypes.c_int, [P, ctypes.POINTER(SgdBuildInfo)]),

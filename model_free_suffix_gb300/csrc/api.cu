@@ -11,11 +11,13 @@
 #include <atomic>
 #include <chrono>
 #include <condition_variable>
+#include <cstdio>
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
 #include <new>
 #include <thread>
+#include <vector>
 
 #include "delta_sig.cuh"
 #include "sgd_internal.h"
@@ -830,6 +832,180 @@ int sgd_export_snapshot(sgd_ctx *x, int32_t *text, int32_t *sa, int64_t capacity
       return SGD_ECUDA;
   }
   return SGD_OK;
+}
+
+// ---------------------------------------------------------------------------
+// Save / load of the cross-request corpus ("SuffixGPU" (PyPI), Roadmap: global
+// tree save & load).  File: a header, then the ring [C] int32, the document
+// FIFO's starts [max_docs] int64 and lengths [max_docs] int32, and the current
+// snapshot's text [n] int32, all in the host's byte order.  Loading validates
+// everything it reads before anything on the device changes.
+
+namespace {
+
+struct CorpusFileHeader {
+  char magic[8];       // "SGDCORP1"
+  uint32_t version;    // 1
+  int32_t vocab_size;  // V
+  int64_t capacity;    // C
+  int32_t max_docs;
+  int32_t reserved;
+  int64_t wp, live, pushed;  // ring state
+  int32_t head, ndocs;
+  int64_t snap_n;      // tokens of the snapshot text
+  int64_t lin_pushed;  // the ring's docs placed and write offset when it was linearised
+  int64_t lin_wp;
+};
+
+constexpr char kMagic[8] = {'S', 'G', 'D', 'C', 'O', 'R', 'P', '1'};
+
+struct FileCloser {
+  FILE *f;
+  ~FileCloser() {
+    if (f) fclose(f);
+  }
+};
+
+}  // namespace
+
+int sgd_save(sgd_ctx *x, const char *path, void *stream) {
+  if (!x || !path) return SGD_EINVAL;
+  if (!x->corpus) return SGD_ENOCORPUS;
+  {
+    std::unique_lock<std::mutex> lk(x->mu);
+    if (x->bstate != B_IDLE || x->job_ready) return SGD_EBUSY;
+  }
+  cudaStream_t st = (cudaStream_t)stream;
+  if (cudaStreamSynchronize(st) != cudaSuccess) return SGD_ECUDA;
+  const int64_t C = x->cfg.corpus_capacity;
+  const int md = x->cfg.max_docs;
+  RingState r;
+  CorpusDesc d;
+  if (cudaMemcpy(&r, x->d_rs, sizeof(r), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(&d, x->d_desc, sizeof(d), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return SGD_ECUDA;
+  const int64_t n = x->front_n;
+  std::vector<int32_t> ring((size_t)C), dl((size_t)md), text((size_t)n);
+  std::vector<int64_t> ds((size_t)md);
+  if (cudaMemcpy(ring.data(), x->d_ring, (size_t)C * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(ds.data(), x->d_doc_start, (size_t)md * 8, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemcpy(dl.data(), x->d_doc_len, (size_t)md * 4, cudaMemcpyDeviceToHost) != cudaSuccess ||
+      (n > 0 && cudaMemcpy(text.data(), x->d_text[x->front], (size_t)n * 4,
+                           cudaMemcpyDeviceToHost) != cudaSuccess))
+    return SGD_ECUDA;
+  CorpusFileHeader h{};
+  memcpy(h.magic, kMagic, 8);
+  h.version = 1;
+  h.vocab_size = x->cfg.vocab_size;
+  h.capacity = C;
+  h.max_docs = md;
+  h.wp = r.wp;
+  h.live = r.live;
+  h.pushed = r.pushed;
+  h.head = r.head;
+  h.ndocs = r.ndocs;
+  h.snap_n = n;
+  h.lin_pushed = d.lin_pushed;
+  h.lin_wp = d.lin_wp;
+  FileCloser fc{fopen(path, "wb")};
+  if (!fc.f) return SGD_EIO;
+  bool ok = fwrite(&h, sizeof(h), 1, fc.f) == 1 && fwrite(ring.data(), 4, ring.size(), fc.f) == ring.size() &&
+            fwrite(ds.data(), 8, ds.size(), fc.f) == ds.size() &&
+            fwrite(dl.data(), 4, dl.size(), fc.f) == dl.size() &&
+            fwrite(text.data(), 4, text.size(), fc.f) == text.size();
+  ok = fclose(fc.f) == 0 && ok;
+  fc.f = nullptr;
+  return ok ? SGD_OK : SGD_EIO;
+}
+
+int sgd_load(sgd_ctx *x, const char *path, void *stream) {
+  if (!x || !path) return SGD_EINVAL;
+  if (!x->corpus) return SGD_ENOCORPUS;
+  {
+    std::unique_lock<std::mutex> lk(x->mu);
+    if (x->bstate != B_IDLE || x->job_ready) return SGD_EBUSY;
+  }
+  const int64_t C = x->cfg.corpus_capacity;
+  const int md = x->cfg.max_docs, V = x->cfg.vocab_size;
+  FileCloser fc{fopen(path, "rb")};
+  if (!fc.f) return SGD_EIO;
+  CorpusFileHeader h;
+  if (fread(&h, sizeof(h), 1, fc.f) != 1) return SGD_EIO;
+  // the file must be this layout, for a context of the same shape, and
+  // describe a ring this library could have produced
+  if (memcmp(h.magic, kMagic, 8) != 0 || h.version != 1) return SGD_EINVAL;
+  if (h.vocab_size != V || h.capacity != C || h.max_docs != md) return SGD_EINVAL;
+  if (h.wp < 0 || h.wp >= C || h.live < 0 || h.live > C || h.ndocs < 0 || h.ndocs > md ||
+      h.head < 0 || h.head >= md || h.pushed < h.ndocs || h.snap_n < 0 || h.snap_n > C ||
+      h.lin_pushed < 0 || h.lin_pushed > h.pushed || h.lin_wp < 0 || h.lin_wp >= C)
+    return SGD_EINVAL;
+  std::vector<int32_t> ring((size_t)C), dl((size_t)md), text((size_t)h.snap_n);
+  std::vector<int64_t> ds((size_t)md);
+  if (fread(ring.data(), 4, ring.size(), fc.f) != ring.size() ||
+      fread(ds.data(), 8, ds.size(), fc.f) != ds.size() ||
+      fread(dl.data(), 4, dl.size(), fc.f) != dl.size() ||
+      fread(text.data(), 4, text.size(), fc.f) != text.size())
+    return SGD_EIO;
+  for (int32_t v : ring)
+    if (v < 0 || v > V) return SGD_EINVAL;
+  for (int32_t v : text)
+    if (v < 0 || v > V) return SGD_EINVAL;
+  // the live docs: back to back from the oldest, each followed by the sentinel,
+  // ending at the write offset
+  int64_t pos = h.ndocs > 0 ? ds[(size_t)h.head] : h.wp, tot = 0;
+  for (int32_t i = 0; i < h.ndocs; ++i) {
+    const size_t slot = (size_t)((h.head + i) % md);
+    if (ds[slot] != pos || dl[slot] < 1 || (int64_t)dl[slot] + 1 > C) return SGD_EINVAL;
+    tot += dl[slot] + 1;
+    pos = (pos + dl[slot] + 1) % C;
+  }
+  if (tot != h.live || pos != h.wp) return SGD_EINVAL;
+  cudaStream_t st = (cudaStream_t)stream;
+  RingState r{};
+  r.wp = h.wp;
+  r.live = h.live;
+  r.head = h.head;
+  r.ndocs = h.ndocs;
+  r.pushed = h.pushed;
+  r.snap_n = h.snap_n;  // the snapshot to rebuild, and where its delta starts
+  r.snap_pushed = h.lin_pushed;
+  r.snap_wp = h.lin_wp;
+  const int back = 1 - x->front;
+  if (cudaStreamSynchronize(st) != cudaSuccess ||
+      cudaMemcpy(x->d_ring, ring.data(), (size_t)C * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(x->d_doc_start, ds.data(), (size_t)md * 8, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(x->d_doc_len, dl.data(), (size_t)md * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(x->d_rs, &r, sizeof(r), cudaMemcpyHostToDevice) != cudaSuccess ||
+      (h.snap_n > 0 && cudaMemcpy(x->d_text[back], text.data(), (size_t)h.snap_n * 4,
+                                  cudaMemcpyHostToDevice) != cudaSuccess))
+    return SGD_ECUDA;
+  if (launch_sig_all(x->d_ring, C, V, x->d_sig, st) != cudaSuccess) return SGD_ECUDA;
+  if (h.snap_n == 0) {  // no snapshot: an empty one, the delta from the saved point
+    if (launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->d_keys[back], x->d_rec[back],
+                    x->d_gt[back], x->gt_mask, 0, x->gen + 1, x->d_rs, st) != cudaSuccess ||
+        cudaStreamSynchronize(st) != cudaSuccess)
+      return SGD_ECUDA;
+    std::unique_lock<std::mutex> lk(x->mu);
+    x->front = back;
+    x->front_n = 0;
+    x->gen++;
+    return SGD_OK;
+  }
+  // the snapshot's index is rebuilt by the worker (as after sgd_build_sa) and swapped in
+  if (cudaEventRecord(x->ev_lin, st) != cudaSuccess) return SGD_ECUDA;
+  {
+    std::unique_lock<std::mutex> lk(x->mu);
+    x->job_back = back;
+    x->job_side = st;
+    x->job_inject = SGD_INJECT_NONE;
+    x->job_ready = true;
+    x->bstate = B_RUNNING;
+    x->cv.notify_all();
+  }
+  uint64_t gen = 0;
+  const int pr = sgd_poll(x, 1, -1, stream, &gen);
+  if (pr != SGD_OK_SWAPPED) return pr < 0 ? pr : SGD_ECUDA;
+  return cudaStreamSynchronize(st) == cudaSuccess ? SGD_OK : SGD_ECUDA;
 }
 
 int sgd_corpus_stats(sgd_ctx *x, int64_t *live_tokens, int32_t *ndocs) {

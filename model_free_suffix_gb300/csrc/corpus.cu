@@ -90,6 +90,12 @@ __global__ void __launch_bounds__(256) sig_kernel(SigBuild g, const int64_t *spa
   sig_update_cta(g, span[0], span[1], s, blockIdx.x, gridDim.x);
 }
 
+// Every window's signature, from the ring (a restored ring).
+__global__ void __launch_bounds__(256) sig_all_kernel(SigBuild g) {
+  __shared__ SigBatchSmem s;
+  sig_update_cta(g, 0, g.C, s, blockIdx.x, gridDim.x);
+}
+
 // A call of up to SMALL_DOCS docs as one CTA.
 __global__ void __launch_bounds__(PLAN_THREADS) ingest_small(SmallIngest g) {
   __shared__ SmallIngestSmem s;
@@ -284,6 +290,12 @@ cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S,
     sig_kernel<<<2 * 152, 256, 0, st>>>(SigBuild{ring, C, V, sig, C / WIN}, sc.span);
     *launches += 1;
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sig_all(int32_t *ring, int64_t C, int V, uint32_t *sig, cudaStream_t st) {
+  if (sig == nullptr || C <= 0) return cudaSuccess;
+  sig_all_kernel<<<2 * 152, 256, 0, st>>>(SigBuild{ring, C, V, sig, C / WIN});
   return cudaGetLastError();
 }
 

@@ -179,6 +179,7 @@ cudaError_t launch_ingest(const int32_t *tok, const int32_t *ntok, int B, int S,
                           int m, int32_t *ring, int64_t C, RingState *rs, int64_t *doc_start,
                           int32_t *doc_len, int max_docs, const IngestScratch &sc,
                           uint32_t *sig, uint32_t *err, cudaStream_t st, int *launches);
+cudaError_t launch_sig_all(int32_t *ring, int64_t C, int V, uint32_t *sig, cudaStream_t st);
 cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs,
                              const int64_t *doc_start, int max_docs, int32_t *out,
                              cudaStream_t st, int *launches);

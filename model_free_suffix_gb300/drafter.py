@@ -12,6 +12,7 @@ harvest_finished (here: ingest) and poll.
 from __future__ import annotations
 
 import ctypes
+import os
 from dataclasses import dataclass
 from fractions import Fraction
 from typing import Optional, Tuple, Union
@@ -286,6 +287,18 @@ class SuffixDrafter:
         self._check(self._lib.sgd_corpus_stats(self._h, ctypes.byref(live), ctypes.byref(nd)),
                     "sgd_corpus_stats")
         return int(live.value), int(nd.value)
+
+    def save(self, path: str, stream=None) -> None:
+        """Writes the corpus (ring, document FIFO, current snapshot) to `path`
+        once the work queued on `stream` is done."""
+        self._check(self._lib.sgd_save(self._h, os.fsencode(path), _stream_handle(stream)),
+                    "sgd_save")
+
+    def load(self, path: str, stream=None) -> None:
+        """Replaces the corpus with a saved one and rebuilds its index (on
+        `stream`, waited for): the context then drafts as the saved one did."""
+        self._check(self._lib.sgd_load(self._h, os.fsencode(path), _stream_handle(stream)),
+                    "sgd_load")
 
     def build_stats(self) -> dict:
         info = L.SgdBuildInfo()
