@@ -46,7 +46,8 @@ class _Params(ctypes.Structure):
                 ("D", ctypes.c_int32), ("R", ctypes.c_int32),
                 ("fN", ctypes.c_int64), ("fD", ctypes.c_int64), ("offset", ctypes.c_int64),
                 ("pN", ctypes.c_int64), ("pD", ctypes.c_int64),
-                ("depth_sum_cap", ctypes.c_int32), ("fixed_length", ctypes.c_int32)]
+                ("depth_sum_cap", ctypes.c_int32), ("fixed_length", ctypes.c_int32),
+                ("select_by_score", ctypes.c_int32)]
 
 
 _lib = None
@@ -110,21 +111,23 @@ def rational(x, denom: int = 10 ** 6):
 
 
 class Params:
-    """Drafter knobs (S, V, k, D, R, factor, offset, min_prob, depth_sum_cap, fixed_length)."""
+    """Drafter knobs (S, V, k, D, R, factor, offset, min_prob, depth_sum_cap, fixed_length,
+    select_by_score)."""
 
     def __init__(self, S, V, k=16, D=24, R=64, factor=(1, 1), offset=0,
-                 min_prob=(1, 10), depth_sum_cap=False, fixed_length=False):
+                 min_prob=(1, 10), depth_sum_cap=False, fixed_length=False, select_by_score=False):
         self.S, self.V, self.k, self.D, self.R = int(S), int(V), int(k), int(D), int(R)
         self.factor = rational(factor)
         self.offset = int(offset)
         self.min_prob = rational(min_prob)
         self.depth_sum_cap = bool(depth_sum_cap)
         self.fixed_length = bool(fixed_length)
+        self.select_by_score = bool(select_by_score)
 
     def c(self) -> _Params:
         return _Params(self.S, self.V, self.k, self.D, self.R, self.factor[0], self.factor[1],
                        self.offset, self.min_prob[0], self.min_prob[1], int(self.depth_sum_cap),
-                       int(self.fixed_length))
+                       int(self.fixed_length), int(self.select_by_score))
 
 
 def update_state(token_ids: np.ndarray, num_tokens: np.ndarray, sampled: np.ndarray, V: int) -> int:

@@ -154,46 +154,17 @@ static int32_t cont_of(int32_t source, const int32_t *t, int32_t n,
   return 1;
 }
 
-void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n_in,
-                     const int32_t *X, int64_t N, int32_t active,
-                     int32_t *drafts, int32_t *num_valid, float *score,
-                     float *probs, int32_t *match_info, uint32_t *flags) {
-  for (int32_t d = 0; d < p->k; d++) {
-    drafts[d] = -1;
-    if (probs) probs[d] = 0.0f;
-  }
-  *num_valid = 0;
-  if (score) *score = 0.0f;
-  if (match_info) { match_info[0] = 0; match_info[1] = 0; }
-
-  int32_t n = n_in;
-  if (n < 0) { n = 0; *flags |= ORC_ERR_NUM_TOKENS; }
-  if (n > p->S) { n = p->S; *flags |= ORC_ERR_NUM_TOKENS; }
-  if (!active || n == 0) return;
-
-  const int32_t Z = p->V;
-  int32_t *occ_s = (int32_t *)malloc(sizeof(int32_t) * (size_t)p->R);
-  int32_t *occ_c = (int32_t *)malloc(sizeof(int32_t) * (size_t)p->R);
-  int32_t cs = 0, cc = 0;
-  int32_t Ms = orc_self_match(t, n, p->D, p->R, occ_s, &cs);
-  int32_t Mc = (X != NULL && N > 0)
-                   ? orc_corpus_match(X, N, Z, t, n, p->D, p->R, occ_c, &cc)
-                   : 0;
-
-  /* the longer match wins; equal lengths stay with the request itself */
-  int32_t source, M, c0;
-  const int32_t *occ;
-  if (Mc > Ms) { source = 2; M = Mc; occ = occ_c; c0 = cc; }
-  else { source = Ms > 0 ? 1 : 0; M = Ms; occ = occ_s; c0 = cs; }
-  if (match_info) { match_info[0] = M; match_info[1] = source; }
-  /* Model Runner V2 drafts: the slots the vote leaves empty hold the row's
-   * last token, all k of them when there is no match ([DOCS] Model Runner V2) */
-  if (p->fixed_length) {
-    for (int32_t d = 0; d < p->k; d++) drafts[d] = t[n - 1];
-    *num_valid = p->k;
-  }
-  if (M == 0 || c0 == 0) { free(occ_s); free(occ_c); return; }
-
+/* Frequency-greedy expansion of one candidate (source 1: the row's own ends,
+ * 2: the corpus ends; M its match length, occ its c0 ends): the draft into
+ * drafts / probs (left as they are past the emitted tokens), the number of
+ * tokens emitted and the sum of their vote counts (score = sum / c0). */
+static void expand(const orc_params *p, int32_t source, const int32_t *t, int32_t n,
+                   const int32_t *X, int64_t N, int32_t Z, const int32_t *occ, int32_t c0,
+                   int32_t M, int32_t *drafts, float *probs, int32_t *len_out,
+                   int64_t *sum_out) {
+  *len_out = 0;
+  *sum_out = 0;
+  if (M == 0 || c0 == 0) return;
   /* length cap (Model Runner V2: no factor, only k and the context) */
   int64_t cap = p->k;
   if (!p->fixed_length) cap = min64(cap, (p->fN * (int64_t)M) / p->fD + p->offset);
@@ -203,7 +174,6 @@ void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n_in,
   if (p->depth_sum_cap && !p->fixed_length) cap = min64(cap, (int64_t)p->D - M);
   if (cap < 0) cap = 0;
 
-  /* frequency-greedy expansion */
   uint8_t *alive = (uint8_t *)malloc((size_t)c0);
   int32_t *val = (int32_t *)malloc(sizeof(int32_t) * (size_t)c0);
   uint8_t *has = (uint8_t *)malloc((size_t)c0);
@@ -235,9 +205,74 @@ void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n_in,
     len++;
     for (int32_t o = 0; o < c0; o++) alive[o] = has[o] && val[o] == best_tok;
   }
-  if (!p->fixed_length) *num_valid = len;
-  if (score) *score = (float)((double)sum / (double)c0);
-  free(alive); free(val); free(has); free(occ_s); free(occ_c);
+  free(alive); free(val); free(has);
+  *len_out = len;
+  *sum_out = sum;
+}
+
+void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n_in,
+                     const int32_t *X, int64_t N, int32_t active,
+                     int32_t *drafts, int32_t *num_valid, float *score,
+                     float *probs, int32_t *match_info, uint32_t *flags) {
+  for (int32_t d = 0; d < p->k; d++) {
+    drafts[d] = -1;
+    if (probs) probs[d] = 0.0f;
+  }
+  *num_valid = 0;
+  if (score) *score = 0.0f;
+  if (match_info) { match_info[0] = 0; match_info[1] = 0; }
+
+  int32_t n = n_in;
+  if (n < 0) { n = 0; *flags |= ORC_ERR_NUM_TOKENS; }
+  if (n > p->S) { n = p->S; *flags |= ORC_ERR_NUM_TOKENS; }
+  if (!active || n == 0) return;
+
+  const int32_t Z = p->V;
+  int32_t *occ_s = (int32_t *)malloc(sizeof(int32_t) * (size_t)p->R);
+  int32_t *occ_c = (int32_t *)malloc(sizeof(int32_t) * (size_t)p->R);
+  int32_t cs = 0, cc = 0;
+  int32_t Ms = orc_self_match(t, n, p->D, p->R, occ_s, &cs);
+  int32_t Mc = (X != NULL && N > 0)
+                   ? orc_corpus_match(X, N, Z, t, n, p->D, p->R, occ_c, &cc)
+                   : 0;
+
+  /* Model Runner V2 drafts: the slots the vote leaves empty hold the row's
+   * last token, all k of them when there is no match ([DOCS] Model Runner V2) */
+  if (p->fixed_length)
+    for (int32_t d = 0; d < p->k; d++) drafts[d] = t[n - 1];
+
+  int32_t source, M, c0, len = 0;
+  int64_t sum = 0;
+  if (p->select_by_score && Ms > 0 && Mc > 0) {
+    /* [PYPI] How it works, step 3: both candidates are expanded and the
+     * better score (sum / c0, compared exactly) wins; equal scores go to the
+     * longer match, then to the row itself */
+    int32_t *d2 = (int32_t *)malloc(sizeof(int32_t) * (size_t)p->k);
+    float *p2 = (float *)malloc(sizeof(float) * (size_t)p->k);
+    for (int32_t d = 0; d < p->k; d++) { d2[d] = drafts[d]; p2[d] = probs ? probs[d] : 0.0f; }
+    int32_t len_c;
+    int64_t sum_c;
+    expand(p, 1, t, n, X, N, Z, occ_s, cs, Ms, drafts, probs, &len, &sum);
+    expand(p, 2, t, n, X, N, Z, occ_c, cc, Mc, d2, p2, &len_c, &sum_c);
+    const int64_t lhs = sum_c * cs, rhs = sum * cc;  /* score_c vs score_s */
+    if (lhs > rhs || (lhs == rhs && Mc > Ms)) {
+      source = 2; M = Mc; c0 = cc; len = len_c; sum = sum_c;
+      for (int32_t d = 0; d < p->k; d++) { drafts[d] = d2[d]; if (probs) probs[d] = p2[d]; }
+    } else {
+      source = 1; M = Ms; c0 = cs;
+    }
+    free(d2); free(p2);
+  } else {
+    /* the longer match wins; equal lengths stay with the request itself */
+    const int32_t *occ;
+    if (Mc > Ms) { source = 2; M = Mc; occ = occ_c; c0 = cc; }
+    else { source = Ms > 0 ? 1 : 0; M = Ms; occ = occ_s; c0 = cs; }
+    expand(p, source, t, n, X, N, Z, occ, c0, M, drafts, probs, &len, &sum);
+  }
+  if (match_info) { match_info[0] = M; match_info[1] = source; }
+  *num_valid = p->fixed_length ? p->k : len;
+  if (score && M > 0 && c0 > 0) *score = (float)((double)sum / (double)c0);
+  free(occ_s); free(occ_c);
 }
 
 uint32_t orc_propose(const orc_params *p, const int32_t *token_ids,

@@ -53,6 +53,9 @@ typedef struct {
                            tokens always, slots without a voted continuation hold
                            the row's last token; factor, offset, min_token_prob
                            and depth_sum_cap unused                              */
+  int32_t select_by_score; /* 1: the row's and the corpus's candidates are both
+                           expanded and the better score wins ([PYPI] How it
+                           works, step 3); 0: the longer match wins ([DOCS])    */
 } orc_params;
 
 /* Append the accepted prefix of one row's sampled ids ([PYPI] Quickstart,

@@ -529,3 +529,65 @@ def test_fixed_length_is_the_unstopped_vote_then_the_last_token(orc):
             assert (f.drafts[b, m:] == tok[b, n[b] - 1]).all()
             assert np.array_equal(f.probs[b, :m], d.probs[b, :m]) and (f.probs[b, m:] == 0).all()
             assert f.score[b] == d.score[b] and np.array_equal(f.match_info[b], d.match_info[b])
+
+
+# --------------------------------------------------------------------------
+# score-ranked selection ("SuffixGPU" (PyPI), How it works, step 3: the local
+# and global winners compete by the same score)
+
+def _doc_text(docs, V):
+    out = []
+    for d in docs:
+        out += list(d) + [V]
+    return np.array(out, dtype=np.int32)
+
+
+def test_select_by_score_worked_examples(orc):
+    V = 20
+    row = [1, 2, 9, 8, 7, 1, 2, 9, 8, 7, 5, 1, 2]
+    # the row: (1, 2) occurs at 0..1 and 5..6 (length 2 each, 5 before the tail
+    # breaks the third token), both followed by 9 8: two tokens of 2/2, score 2.
+    # the corpus: (5, 1, 2) three times, followed by 3, 4 and 6: length 3, one
+    # token 3 of 1/3 (the tie goes to the smallest id), then the sentinel.
+    X = _doc_text([[5, 1, 2, 3], [5, 1, 2, 4], [5, 1, 2, 6]], V)
+    base = dict(S=32, V=V, k=4, D=8, R=4)
+    r = _row(orc, orc.Params(**base), row, X=X)          # the longer match wins
+    assert r.match_info[0].tolist() == [3, 2] and r.drafts[0].tolist() == [3, -1, -1, -1]
+    assert abs(float(r.score[0]) - 1 / 3) < 1e-7
+    r = _row(orc, orc.Params(**base, select_by_score=True), row, X=X)  # the better score wins
+    assert r.match_info[0].tolist() == [2, 1] and r.drafts[0].tolist() == [9, 8, -1, -1]
+    assert r.probs[0].tolist() == [1.0, 1.0, 0.0, 0.0] and float(r.score[0]) == 2.0
+    # equal scores: with max_spec_factor 1/2 each side emits one token of 1/1
+    # (the corpus holds (5, 1, 2) once); the longer match, the corpus's, wins
+    X1 = _doc_text([[5, 1, 2, 3]], V)
+    r = _row(orc, orc.Params(**base, factor=(1, 2), select_by_score=True), row, X=X1)
+    assert r.match_info[0].tolist() == [3, 2] and r.drafts[0].tolist() == [3, -1, -1, -1]
+    assert float(r.score[0]) == 1.0
+
+
+def test_select_by_score_picks_the_better_of_the_two(orc):
+    """Where the longer match is the corpus's, its draft is the default rule's
+    and the row's own candidate is the draft without a corpus: the score rule
+    returns the better of those two (ties: the longer match)."""
+    rng = np.random.default_rng(31)
+    V, S, k = 6, 80, 5
+    checked = 0
+    for trial in range(60):
+        X = _doc_text([rng.integers(0, V, rng.integers(4, 30)) for _ in range(15)], V)
+        B = 8
+        tok = rng.integers(0, V, (B, S)).astype(np.int32)
+        n = rng.integers(4, S - 2, B).astype(np.int32)
+        kw = dict(S=S, V=V, k=k, D=10, R=6, min_prob=(1, 5))
+        sc = orc.propose(orc.Params(**kw, select_by_score=True), tok, n, X=X)
+        ln = orc.propose(orc.Params(**kw), tok, n, X=X)
+        own = orc.propose(orc.Params(**kw), tok, n, X=None)
+        for b in range(B):
+            if ln.match_info[b, 1] != 2 or own.match_info[b, 1] != 1:
+                continue
+            checked += 1
+            s_c, s_s = float(ln.score[b]), float(own.score[b])
+            win = ln if s_c >= s_s else own  # (equal: the longer match, the corpus's)
+            assert sc.drafts[b].tolist() == win.drafts[b].tolist(), (trial, b)
+            assert sc.match_info[b].tolist() == win.match_info[b].tolist()
+            assert sc.score[b] == win.score[b] and np.array_equal(sc.probs[b], win.probs[b])
+    assert checked > 20
