@@ -134,6 +134,14 @@ typedef struct {
                                   0), num_valid = k; max_spec_factor, max_spec_offset,
                                   min_token_prob and depth_sum_cap are not used.  Rows
                                   that are inactive or empty stay -1 / 0 either way. */
+  int32_t  select_by_score;    /* 0 (default): the longer match wins, the row's own at
+                                  equal length ([DOCS] Model Runner V2).  1: the row's and
+                                  the corpus's longest-match candidates are both voted
+                                  and the better score (expected accepted tokens, the sum
+                                  of the emitted probabilities) wins; equal scores go to
+                                  the longer match, then to the row ([PYPI] How it works,
+                                  step 3).  The corpus candidate is then always found in
+                                  full (no pruning by the row's match). */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)

@@ -62,6 +62,7 @@ class SgdConfig(ctypes.Structure):
         ("propose_mode", ctypes.c_int32),
         ("delta_capacity", ctypes.c_int64),
         ("draft_mode", ctypes.c_int32),
+        ("select_by_score", ctypes.c_int32),
     ]
 
 

@@ -118,6 +118,7 @@ int validate(const sgd_config &c) {
   if (c.delta_capacity < 0 || c.delta_capacity > c.corpus_capacity) return SGD_EINVAL;
   if (c.delta_capacity > 0 && c.corpus_capacity % WIN != 0) return SGD_EINVAL;
   if (c.draft_mode != 0 && c.draft_mode != 1) return SGD_EINVAL;
+  if (c.select_by_score != 0 && c.select_by_score != 1) return SGD_EINVAL;
   return SGD_OK;
 }
 
@@ -285,6 +286,7 @@ int sgd_config_default(sgd_config *c) {
   c->propose_mode = 0;
   c->delta_capacity = 0;
   c->draft_mode = 0;
+  c->select_by_score = 0;
   c->self_warps = 0;
   return SGD_OK;
 }
@@ -462,6 +464,7 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.rsh = x->rsh;
   a.split = x->split;
   a.self_res = x->d_self_res;
+  a.by_score = c.select_by_score;
   if (c.draft_mode == 1) {  // no probability floor: the vote runs while an occurrence continues
     a.fixed = 1;
     a.pN = 0;

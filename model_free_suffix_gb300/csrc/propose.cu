@@ -965,6 +965,205 @@ __device__ __forceinline__ void step_ingest(const ProposeArgs &a) {
   ingest_small_cta(g, *reinterpret_cast<SmallIngestSmem *>(dsm));
 }
 
+// Depth-wise majority vote of one candidate (one warp, up to 4 occurrences
+// per lane): cont[o * capp + d] is occurrence o's continuation at depth d,
+// run[o] how many of them exist; the emitted tokens and their probabilities
+// go to dr / pr (nothing past them is written), their number to len and the
+// sum of their counts to sum (score = sum / c0).  Scratch: s_hist (256 ints),
+// s_vv (c0 ints), s_hash (256 x 12 bytes).
+//
+// With a reference survivor chosen at depth d, let diff(o) be the first
+// depth >= d where survivor o disagrees with the reference or runs out.
+// Then at depth x the survivors are {diff >= x}, the participants are those
+// not running out at x, and the reference's token is continued by
+// c(x) = #{diff > x}.  While the reference takes part and c(x) is a strict
+// majority of the participants, the reference's token wins with count
+// c(x): two histograms of diff give every c(x) at once, so a whole run of
+// depths is decided in one warp scan.  Where the majority fails, all
+// participants' tokens are counted (most frequent wins, ties to the
+// smallest id) and a new reference is taken among the winners.
+// Probabilities are quotients c / c0 of integers with c <= 64 * c0 and
+// c0 <= 128: both are exact floats, and a correctly rounded single
+// division gives the same float as rounding the double quotient (checked
+// over that whole range by the test suite), so no double arithmetic.
+__device__ void vote_warp(const ProposeArgs &a, const int *cont, int capp, const int *s_run, int c0,
+                          int cap, int *s_hist, int *s_vv, unsigned char *s_hash, int32_t *dr,
+                          float *pr, int &len, long long &sum) {
+  const int lane = threadIdx.x & 31;
+  unsigned char *s_L = s_hash;
+  len = 0;
+  sum = 0;
+  if (cap > 0) {
+    bool alive[4];
+#pragma unroll
+    for (int s = 0; s < 4; ++s) alive[s] = lane + 32 * s < c0;
+    const unsigned lt = (1u << lane) - 1u;
+    int *H = s_hist, *HR = s_hist + 128;  // diff histogram; run-outs among them
+    int d = 0;
+    while (d < cap) {
+      unsigned am[4];
+      int nalive = 0;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        am[s] = __ballot_sync(FULL, alive[s]);
+        nalive += __popc(am[s]);
+      }
+      if (nalive == 0) break;
+      const int ss = am[0] ? 0 : (am[1] ? 1 : (am[2] ? 2 : 3));
+      const unsigned mm = am[0] ? am[0] : (am[1] ? am[1] : (am[2] ? am[2] : am[3]));
+      const int ref = (__ffs(mm) - 1) + 32 * ss;
+      const int run_ref = min(s_run[ref], cap);
+      for (int i = lane; i <= cap; i += 32) { H[i] = 0; HR[i] = 0; }
+      __syncwarp();
+      int diff[4];
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        diff[s] = cap;
+        if (!alive[s]) continue;
+        const int o = lane + 32 * s;
+        const int r = min(s_run[o], cap);
+        // first depth in [d, r) where o disagrees with the reference, else r;
+        // four depths per 16-byte load of each row
+        const int4 *ro = reinterpret_cast<const int4 *>(cont + o * capp);
+        const int4 *rr = reinterpret_cast<const int4 *>(cont + ref * capp);
+        int dd = r;
+        for (int q = d >> 2; (q << 2) < r; ++q) {
+          const int4 x = ro[q], y = rr[q];
+          const int b = q << 2;
+          int f = -1;
+          if (b + 3 >= d && b + 3 < r && x.w != y.w) f = b + 3;
+          if (b + 2 >= d && b + 2 < r && x.z != y.z) f = b + 2;
+          if (b + 1 >= d && b + 1 < r && x.y != y.y) f = b + 1;
+          if (b >= d && b < r && x.x != y.x) f = b;
+          if (f >= 0) { dd = f; break; }
+        }
+        diff[s] = dd;
+        atomicAdd(&H[dd], 1);
+        if (dd == r && r < cap) atomicAdd(&HR[dd], 1);
+      }
+      __syncwarp();
+      // c(x) = nalive - #{diff <= x}, for x = d + lane and x = d + 32 + lane
+      const int x1 = d + lane, x2 = d + 32 + lane;
+      const int h1 = x1 <= cap ? H[x1] : 0, h2 = x2 <= cap ? H[x2] : 0;
+      int p1 = h1, p2 = h2;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y1 = __shfl_up_sync(FULL, p1, off), y2 = __shfl_up_sync(FULL, p2, off);
+        if (lane >= off) { p1 += y1; p2 += y2; }
+      }
+      p2 += __shfl_sync(FULL, p1, 31);
+      const int c1 = nalive - p1, c2 = nalive - p2;
+      const int part1 = c1 + h1 - (x1 <= cap ? HR[x1] : 0);
+      const int part2 = c2 + h2 - (x2 <= cap ? HR[x2] : 0);
+      const bool maj1 = x1 < run_ref && 2 * c1 > part1, maj2 = x2 < run_ref && 2 * c2 > part2;
+      const bool ok1 = maj1 && (long long)c1 * a.pD >= a.pN * (long long)c0;
+      const bool ok2 = maj2 && (long long)c2 * a.pD >= a.pN * (long long)c0;
+      const unsigned bad1 = __ballot_sync(FULL, x1 < cap && !ok1);
+      const unsigned bad2 = __ballot_sync(FULL, x2 < cap && !ok2);
+      const int F = bad1 ? d + __ffs(bad1) - 1 : (bad2 ? d + 32 + __ffs(bad2) - 1 : cap);
+      // emit depths [d, F): the reference's tokens
+      long long part_sum = 0;
+      if (x1 < F) {
+        dr[x1] = cont[ref * capp + x1];
+        if (pr) pr[x1] = (float)c1 / (float)c0;
+        part_sum += c1;
+      }
+      if (x2 < F) {
+        dr[x2] = cont[ref * capp + x2];
+        if (pr) pr[x2] = (float)c2 / (float)c0;
+        part_sum += c2;
+      }
+      for (int off = 16; off > 0; off >>= 1) part_sum += __shfl_xor_sync(FULL, part_sum, off);
+      sum += part_sum;
+      len += F - d;
+      if (F >= cap) break;
+      // depth F: stop if the reference's majority only missed the threshold
+      const bool majF = __shfl_sync(FULL, F - d < 32 ? maj1 : maj2, (F - d) & 31);
+      if (majF) break;
+      d = F;
+      // full count among the participants at depth d
+      bool part[4];
+      unsigned pm[4];
+      int npart = 0;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        alive[s] = alive[s] && diff[s] >= d;
+        part[s] = alive[s] && d < s_run[lane + 32 * s];
+        pm[s] = __ballot_sync(FULL, part[s]);
+        npart += __popc(pm[s]);
+      }
+      if (npart == 0) break;
+      int val[4];
+      int base = 0;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        val[s] = part[s] ? cont[(lane + 32 * s) * capp + d] : 0;
+        if (part[s]) s_vv[base + __popc(pm[s] & lt)] = val[s];
+        base += __popc(pm[s]);
+      }
+      __syncwarp();
+      unsigned mycnt = 0, myv = 0xffffffffu;
+      int cnt;
+      if (npart <= 32) {
+        const unsigned vm = npart == 32 ? FULL : ((1u << npart) - 1u);
+        const int v = lane < npart ? s_vv[lane] : 0;
+        if (lane < npart) mycnt = __popc(__match_any_sync(vm, v));
+        const unsigned maxc = __reduce_max_sync(FULL, mycnt);
+        if (lane < npart && mycnt == maxc) myv = (unsigned)v ^ 0x80000000u;
+        cnt = (int)maxc;
+      } else {
+        // more than 32 participants: count every value in a 256-entry open
+        // addressing table in shared memory (the probe's idle length cache);
+        // a key is (1 << 32) | value, so 0 marks a free entry for any value
+        unsigned long long *hk = reinterpret_cast<unsigned long long *>(s_L);
+        unsigned *hc = reinterpret_cast<unsigned *>(s_L + 256 * sizeof(unsigned long long));
+        for (int i = lane; i < 256; i += 32) { hk[i] = 0ull; hc[i] = 0u; }
+        __syncwarp();
+        int hs[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          hs[s] = 0;
+          if (!part[s]) continue;
+          const unsigned long long key = (1ull << 32) | (unsigned)val[s];
+          unsigned h = ((unsigned)val[s] * 0x9E3779B1u) >> 24;
+          for (int t = 0; t < 256; ++t, h = (h + 1) & 255u) {  // <= 128 keys: ends early
+            const unsigned long long old = atomicCAS(&hk[h], 0ull, key);
+            if (old == 0ull || old == key) {
+              atomicAdd(&hc[h], 1u);
+              hs[s] = (int)h;
+              break;
+            }
+          }
+        }
+        __syncwarp();
+        unsigned c4[4];
+#pragma unroll
+        for (int s = 0; s < 4; ++s) {
+          c4[s] = part[s] ? hc[hs[s]] : 0u;
+          mycnt = max(mycnt, c4[s]);
+        }
+        const unsigned maxc = __reduce_max_sync(FULL, mycnt);
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+          if (part[s] && c4[s] == maxc) myv = min(myv, (unsigned)val[s] ^ 0x80000000u);
+        cnt = (int)maxc;
+      }
+      const int tau = (int)(__reduce_min_sync(FULL, myv) ^ 0x80000000u);
+      __syncwarp();
+      if ((long long)cnt * a.pD < a.pN * (long long)c0) break;
+      if (lane == 0) {
+        dr[d] = tau;
+        if (pr) pr[d] = (float)cnt / (float)c0;
+      }
+      sum += cnt;
+      ++len;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) alive[s] = part[s] && val[s] == tau;
+      ++d;
+    }
+  }
+}
+
 // MODE 0: the whole step in one kernel.  MODE 1 (long rows, first launch):
 // the update and the self scan only; the row's self result is written to
 // a.self_res.  MODE 2 (second launch): one warp reads that result back in
@@ -1327,7 +1526,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     // The row's own match length, -1 while the self warps still scan.  Before
     // a large piece of work the probe warps wait for it (bounded; on time-out
     // they go on without pruning, which only costs time).
+    // (Score-ranked selection: a shorter corpus match may still win, so the
+    // corpus candidate is always found in full.)
     auto self_len = [&](bool wait) {
+      if (a.by_score) return -1;
       if (ptid == 0) {
         unsigned spins = 0;
         while (wait && *(volatile int *)&s_ms_ready == 0 && ++spins < (1u << 22)) __nanosleep(64);
@@ -1591,8 +1793,11 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // recent, so they come first and the snapshot's fill the rest of the R.
   const int Ms = s_Ms, Mcs = corpus_ok ? s_Mc : 0, Md = s_Md;
   const int Mc = max(Mcs, Md);
+  // score-ranked selection with both candidates: the corpus's is prepared as
+  // below, the row's beside it, and the vote decides
+  const bool both = a.by_score && Ms > 0 && Mc > 0;
   int src, M;
-  if (Mc > Ms) { src = 2; M = Mc; }
+  if (Mc > Ms || both) { src = 2; M = Mc; }
   else { src = Ms > 0 ? 1 : 0; M = Ms; }
   const int nd = src == 2 && Md == Mc ? s_cd : 0;               // delta ends voting
   const int ns = src == 2 && Mcs == Mc ? min(s_c0c, R - nd) : 0;  // snapshot ends voting
@@ -1601,10 +1806,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int *occ = src == 2 ? s_occc : s_occ;
   if (nd > 0) {
     // occurrences: the delta's ends, then the ns most recent of the snapshot's
-    // (ranked by position; they are distinct) -- into s_occ, unused when the
-    // corpus wins
+    // (ranked by position; they are distinct) -- into s_wlist, free by now
     const int c0c = Mcs == Mc ? s_c0c : 0;
-    for (int i = tid; i < nd; i += nthr) s_occ[i] = s_wlist1[i];
+    for (int i = tid; i < nd; i += nthr) s_wlist[i] = s_wlist1[i];
     for (int i = tid; i < c0c; i += nthr) {
       const int e = s_occc[i];
       int rank = 0;
@@ -1612,10 +1816,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         for (int j = 0; j < c0c; ++j) rank += s_occc[j] > e;
       else
         rank = i;
-      if (rank < ns) s_occ[nd + rank] = e;
+      if (rank < ns) s_wlist[nd + rank] = e;
     }
     __syncthreads();
-    occ = s_occ;
+    occ = s_wlist;
   }
   int *cont = s_big;                  // cont[o * capp + d]: rows 16-byte aligned
   const int capp = (cap + 3) & ~3;
@@ -1658,195 +1862,53 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     }
     __syncthreads();
   }
+  // the row's candidate beside it (score-ranked selection): its continuations
+  // in the probe's scratch (done with by now), after the vote's hash area
+  int *cont_s = reinterpret_cast<int *>(s_L) + 768;
+  const int cap_s = both ? draft_cap(a, Ms, n) : 0, capp_s = (cap_s + 3) & ~3, cs = s_cs;
+  int *run_s = cont_s + cs * capp_s;
+  if (both && cap_s > 0) {
+    for (int idx = tid; idx < cs * cap_s; idx += nthr) {
+      const int o = idx / cap_s, d = idx - o * cap_s;
+      const int pos = s_occ[o] + 1 + d;
+      cont_s[o * capp_s + d] = pos <= n - 1 ? row[pos] : 0;
+    }
+    for (int o = tid; o < cs; o += nthr) run_s[o] = min(cap_s, n - 1 - s_occ[o]);
+    __syncthreads();
+  }
   if (done_signal && tid == 0) step_done(a.step_sync, s_ep);  // the row's ring reads are over
   if (warp != 0) return;
 
-  // ---- depth-wise majority vote (one warp, up to 4 occurrences per lane) ----
-  // With a reference survivor chosen at depth d, let diff(o) be the first
-  // depth >= d where survivor o disagrees with the reference or runs out.
-  // Then at depth x the survivors are {diff >= x}, the participants are those
-  // not running out at x, and the reference's token is continued by
-  // c(x) = #{diff > x}.  While the reference takes part and c(x) is a strict
-  // majority of the participants, the reference's token wins with count
-  // c(x): two histograms of diff give every c(x) at once, so a whole run of
-  // depths is decided in one warp scan.  Where the majority fails, all
-  // participants' tokens are counted (most frequent wins, ties to the
-  // smallest id) and a new reference is taken among the winners.
-  // Probabilities are quotients c / c0 of integers with c <= 64 * c0 and
-  // c0 <= 128: both are exact floats, and a correctly rounded single
-  // division gives the same float as rounding the double quotient (checked
-  // over that whole range by the test suite), so no double arithmetic.
+  // ---- depth-wise majority vote (one warp) ----
   int len = 0;
   long long sum = 0;
-  if (cap > 0) {
-    bool alive[4];
-#pragma unroll
-    for (int s = 0; s < 4; ++s) alive[s] = lane + 32 * s < c0;
-    const unsigned lt = (1u << lane) - 1u;
-    int *H = s_hist, *HR = s_hist + 128;  // diff histogram; run-outs among them
-    int d = 0;
-    while (d < cap) {
-      unsigned am[4];
-      int nalive = 0;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        am[s] = __ballot_sync(FULL, alive[s]);
-        nalive += __popc(am[s]);
+  vote_warp(a, cont, capp, s_run, c0, cap, s_hist, s_vv, s_L, dr, pr, len, sum);
+  int cw = c0;  // the winner's occurrences
+  if (both) {
+    // the row's draft, staged; it wins unless the corpus's score (sum / c0) is
+    // higher, or equal with the longer match
+    int *stage = run_s + cs;
+    float *pstage = reinterpret_cast<float *>(stage + k);
+    int len_s = 0;
+    long long sum_s = 0;
+    __syncwarp();
+    if (cap_s > 0)
+      vote_warp(a, cont_s, capp_s, run_s, cs, cap_s, s_hist, s_vv, s_L, stage, pstage, len_s, sum_s);
+    __syncwarp();
+    const long long lhs = sum * cs, rhs = sum_s * c0;
+    if (!(lhs > rhs || (lhs == rhs && Mc > Ms))) {
+      for (int d = lane; d < len_s; d += 32) {
+        dr[d] = stage[d];
+        if (pr) pr[d] = pstage[d];
       }
-      if (nalive == 0) break;
-      const int ss = am[0] ? 0 : (am[1] ? 1 : (am[2] ? 2 : 3));
-      const unsigned mm = am[0] ? am[0] : (am[1] ? am[1] : (am[2] ? am[2] : am[3]));
-      const int ref = (__ffs(mm) - 1) + 32 * ss;
-      const int run_ref = min(s_run[ref], cap);
-      for (int i = lane; i <= cap; i += 32) { H[i] = 0; HR[i] = 0; }
-      __syncwarp();
-      int diff[4];
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        diff[s] = cap;
-        if (!alive[s]) continue;
-        const int o = lane + 32 * s;
-        const int r = min(s_run[o], cap);
-        // first depth in [d, r) where o disagrees with the reference, else r;
-        // four depths per 16-byte load of each row
-        const int4 *ro = reinterpret_cast<const int4 *>(cont + o * capp);
-        const int4 *rr = reinterpret_cast<const int4 *>(cont + ref * capp);
-        int dd = r;
-        for (int q = d >> 2; (q << 2) < r; ++q) {
-          const int4 x = ro[q], y = rr[q];
-          const int b = q << 2;
-          int f = -1;
-          if (b + 3 >= d && b + 3 < r && x.w != y.w) f = b + 3;
-          if (b + 2 >= d && b + 2 < r && x.z != y.z) f = b + 2;
-          if (b + 1 >= d && b + 1 < r && x.y != y.y) f = b + 1;
-          if (b >= d && b < r && x.x != y.x) f = b;
-          if (f >= 0) { dd = f; break; }
-        }
-        diff[s] = dd;
-        atomicAdd(&H[dd], 1);
-        if (dd == r && r < cap) atomicAdd(&HR[dd], 1);
-      }
-      __syncwarp();
-      // c(x) = nalive - #{diff <= x}, for x = d + lane and x = d + 32 + lane
-      const int x1 = d + lane, x2 = d + 32 + lane;
-      const int h1 = x1 <= cap ? H[x1] : 0, h2 = x2 <= cap ? H[x2] : 0;
-      int p1 = h1, p2 = h2;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const int y1 = __shfl_up_sync(FULL, p1, off), y2 = __shfl_up_sync(FULL, p2, off);
-        if (lane >= off) { p1 += y1; p2 += y2; }
-      }
-      p2 += __shfl_sync(FULL, p1, 31);
-      const int c1 = nalive - p1, c2 = nalive - p2;
-      const int part1 = c1 + h1 - (x1 <= cap ? HR[x1] : 0);
-      const int part2 = c2 + h2 - (x2 <= cap ? HR[x2] : 0);
-      const bool maj1 = x1 < run_ref && 2 * c1 > part1, maj2 = x2 < run_ref && 2 * c2 > part2;
-      const bool ok1 = maj1 && (long long)c1 * a.pD >= a.pN * (long long)c0;
-      const bool ok2 = maj2 && (long long)c2 * a.pD >= a.pN * (long long)c0;
-      const unsigned bad1 = __ballot_sync(FULL, x1 < cap && !ok1);
-      const unsigned bad2 = __ballot_sync(FULL, x2 < cap && !ok2);
-      const int F = bad1 ? d + __ffs(bad1) - 1 : (bad2 ? d + 32 + __ffs(bad2) - 1 : cap);
-      // emit depths [d, F): the reference's tokens
-      long long part_sum = 0;
-      if (x1 < F) {
-        dr[x1] = cont[ref * capp + x1];
-        if (pr) pr[x1] = (float)c1 / (float)c0;
-        part_sum += c1;
-      }
-      if (x2 < F) {
-        dr[x2] = cont[ref * capp + x2];
-        if (pr) pr[x2] = (float)c2 / (float)c0;
-        part_sum += c2;
-      }
-      for (int off = 16; off > 0; off >>= 1) part_sum += __shfl_xor_sync(FULL, part_sum, off);
-      sum += part_sum;
-      len += F - d;
-      if (F >= cap) break;
-      // depth F: stop if the reference's majority only missed the threshold
-      const bool majF = __shfl_sync(FULL, F - d < 32 ? maj1 : maj2, (F - d) & 31);
-      if (majF) break;
-      d = F;
-      // full count among the participants at depth d
-      bool part[4];
-      unsigned pm[4];
-      int npart = 0;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        alive[s] = alive[s] && diff[s] >= d;
-        part[s] = alive[s] && d < s_run[lane + 32 * s];
-        pm[s] = __ballot_sync(FULL, part[s]);
-        npart += __popc(pm[s]);
-      }
-      if (npart == 0) break;
-      int val[4];
-      int base = 0;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        val[s] = part[s] ? cont[(lane + 32 * s) * capp + d] : 0;
-        if (part[s]) s_vv[base + __popc(pm[s] & lt)] = val[s];
-        base += __popc(pm[s]);
-      }
-      __syncwarp();
-      unsigned mycnt = 0, myv = 0xffffffffu;
-      int cnt;
-      if (npart <= 32) {
-        const unsigned vm = npart == 32 ? FULL : ((1u << npart) - 1u);
-        const int v = lane < npart ? s_vv[lane] : 0;
-        if (lane < npart) mycnt = __popc(__match_any_sync(vm, v));
-        const unsigned maxc = __reduce_max_sync(FULL, mycnt);
-        if (lane < npart && mycnt == maxc) myv = (unsigned)v ^ 0x80000000u;
-        cnt = (int)maxc;
-      } else {
-        // more than 32 participants: count every value in a 256-entry open
-        // addressing table in shared memory (the probe's idle length cache);
-        // a key is (1 << 32) | value, so 0 marks a free entry for any value
-        unsigned long long *hk = reinterpret_cast<unsigned long long *>(s_L);
-        unsigned *hc = reinterpret_cast<unsigned *>(s_L + 256 * sizeof(unsigned long long));
-        for (int i = lane; i < 256; i += 32) { hk[i] = 0ull; hc[i] = 0u; }
-        __syncwarp();
-        int hs[4];
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          hs[s] = 0;
-          if (!part[s]) continue;
-          const unsigned long long key = (1ull << 32) | (unsigned)val[s];
-          unsigned h = ((unsigned)val[s] * 0x9E3779B1u) >> 24;
-          for (int t = 0; t < 256; ++t, h = (h + 1) & 255u) {  // <= 128 keys: ends early
-            const unsigned long long old = atomicCAS(&hk[h], 0ull, key);
-            if (old == 0ull || old == key) {
-              atomicAdd(&hc[h], 1u);
-              hs[s] = (int)h;
-              break;
-            }
-          }
-        }
-        __syncwarp();
-        unsigned c4[4];
-#pragma unroll
-        for (int s = 0; s < 4; ++s) {
-          c4[s] = part[s] ? hc[hs[s]] : 0u;
-          mycnt = max(mycnt, c4[s]);
-        }
-        const unsigned maxc = __reduce_max_sync(FULL, mycnt);
-#pragma unroll
-        for (int s = 0; s < 4; ++s)
-          if (part[s] && c4[s] == maxc) myv = min(myv, (unsigned)val[s] ^ 0x80000000u);
-        cnt = (int)maxc;
-      }
-      const int tau = (int)(__reduce_min_sync(FULL, myv) ^ 0x80000000u);
-      __syncwarp();
-      if ((long long)cnt * a.pD < a.pN * (long long)c0) break;
-      if (lane == 0) {
-        dr[d] = tau;
-        if (pr) pr[d] = (float)cnt / (float)c0;
-      }
-      sum += cnt;
-      ++len;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) alive[s] = part[s] && val[s] == tau;
-      ++d;
+      len = len_s;
+      sum = sum_s;
+      cw = cs;
+      M = Ms;
+      src = 1;
     }
   }
+
   // the slots the vote left empty: -1, or (Model Runner V2 drafts) the row's last token
   const int fill = a.fixed ? s_tail[0] : -1;
   for (int d = len + lane; d < k; d += 32) {
@@ -1855,7 +1917,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   }
   if (lane == 0) {
     a.num_valid[b] = a.fixed ? k : len;
-    if (a.score) a.score[b] = c0 > 0 ? (float)sum / (float)c0 : 0.f;
+    if (a.score) a.score[b] = cw > 0 ? (float)sum / (float)cw : 0.f;
     if (a.match_info) { a.match_info[2 * b] = M; a.match_info[2 * b + 1] = src; }
   }
 }

@@ -155,6 +155,9 @@ struct ProposeArgs {
   // min_token_prob (pN = 0) nor capped by the factor, empty slots hold the
   // row's last token
   int fixed;
+  // score-ranked selection: the row's and the corpus's candidates are both
+  // voted and the better score wins (ties: the longer match, then the row)
+  int by_score;
 };
 
 __host__ __device__ constexpr int self_res_ints(int R) { return 2 * R + 10; }

@@ -62,7 +62,8 @@ def test_create_rejects_bad_knobs_before_touching_the_gpu(lib):
     L = lib.load()
     bad = [("seq_capacity", 4098), ("k", 0), ("k", 65), ("max_tree_depth", 129),
            ("max_occurrences", 0), ("corpus_cand_cap", 100), ("corpus_cand_cap", 32),
-           ("min_prob_den", 0), ("self_warps", 17), ("draft_mode", 2), ("draft_mode", -1)]
+           ("min_prob_den", 0), ("self_warps", 17), ("draft_mode", 2), ("draft_mode", -1),
+           ("select_by_score", 2)]
     for field, val in bad:
         c = lib.SgdConfig()
         L.sgd_config_default(ctypes.byref(c))
