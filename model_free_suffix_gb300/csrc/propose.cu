@@ -236,21 +236,18 @@ __device__ __forceinline__ void window_ends(int L0, int L1, int L2, int L3, int 
   cnt = min(R, cnt + __popc(E0) + __popc(E1) + __popc(E2) + __popc(E3));
 }
 
-// The CTA's longest length so far (over the warps scanning one text).
-__device__ __forceinline__ int kgram_k(int Mw, const int *s_best) {
-  return min(4, max(2, max(Mw, *(const volatile int *)s_best)));
-}
-
 // The warp's windows, most recent first.  Ends with L >= 1 are exactly the
 // positions holding tail[0] = t0; those with L >= 2 also hold tail[1] just
 // before.  Each lane holds four consecutive tokens of a window (its own 16
 // bytes of the ring slot), so a window without t0 costs one load, four
 // compares and a vote.  Otherwise the R most recent t0 positions are kept
 // (list1: the answer when no end matches two tokens) and every (t1, t0)
-// position is extended by window_ends into (Mw, list).
+// position, most recent first, is extended by the whole warp (pair_extend)
+// into (Mw, list).  The row's ends are few per window, so this serial form
+// has the shortest latency per window (the probe warps may wait for it).
 __device__ void self_process(const int32_t *row, int n, int S, int D, int R, const int *s_tail,
-                             int *list, int *list1, int *s_best, int lane, SelfScan &sc, int &Mw,
-                             int &cnt, int &cnt1) {
+                             int *list, int *list1, int lane, SelfScan &sc, int &Mw, int &cnt,
+                             int &cnt1) {
   Mw = 0;
   cnt = 0;
   cnt1 = 0;
@@ -259,9 +256,7 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
   const int t0 = s_tail[0];
   const bool two = D >= 2 && n >= 2;
   const int t1 = two ? s_tail[1] : 0;
-  const int dlim = min(D, n);  // (an end j <= n - 2 matches at most j + 1 < n tokens anyway)
-  const int tail1 = lane + 1 < dlim ? s_tail[1 + lane] : 0;
-  const int t2 = dlim >= 3 ? s_tail[2] : 0, t3 = dlim >= 4 ? s_tail[3] : 0;
+  const int tail1 = lane + 1 < min(D, n) ? s_tail[1 + lane] : 0;
   for (int wi = sc.whi, q = 0; wi >= sc.wlo; --wi, ++q) {
     // keep SPF windows in flight; then windows q and q + 1 must have landed
     self_fetch(row, wi - SPF - 1, lane, S, sc.ring, (q + SPF + 1) % SR);
@@ -288,26 +283,42 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
         if (a0) { if (slot < R) list1[slot] = p0; }
         cnt1 = min(R, cnt1 + total);
       }
-      // positions matching (t1, t0) -- or more of the tail once the CTA's
-      // longest match is longer -- with the window below for lane 0's past
+      // (t1, t0) positions: the token before position p0 is the previous
+      // lane's last one, or the last token of the window below for lane 0
       const int4 prv = sc.ring[((q + 1) % SR) * 32 + lane];
-      int p1 = __shfl_up_sync(FULL, cur.w, 1), p2 = __shfl_up_sync(FULL, cur.z, 1);
-      int p3 = __shfl_up_sync(FULL, cur.y, 1);
-      const int bw = __shfl_sync(FULL, prv.w, 31), bz = __shfl_sync(FULL, prv.z, 31);
-      const int by = __shfl_sync(FULL, prv.y, 31);
-      if (lane == 0) { p1 = bw; p2 = bz; p3 = by; }
-      // the row's text starts at position 0: pair index WIN - base
-      int L0, L1, L2, L3;
-      window_depths(cur, p1, p2, p3, t0, t1, t2, t3, dlim, kgram_k(Mw, s_best), WIN - base, lane,
-                    a0 && two, a1 && two, a2 && two, a3 && two, L0, L1, L2, L3);
-      if (__any_sync(FULL, (L0 | L1 | L2 | L3) != 0)) {
+      const int up = __shfl_up_sync(FULL, cur.w, 1);
+      const int below = __shfl_sync(FULL, prv.w, 31);
+      const int before0 = lane == 0 ? below : up;
+      unsigned m0 = __ballot_sync(FULL, a0 && two && p0 >= 1 && before0 == t1);
+      unsigned m1 = __ballot_sync(FULL, a1 && two && cur.x == t1);
+      unsigned m2 = __ballot_sync(FULL, a2 && two && cur.y == t1);
+      unsigned m3 = __ballot_sync(FULL, a3 && two && cur.z == t1);
+      if (m0 | m1 | m2 | m3) {
         __syncwarp();  // every lane's copies visible to the warp (the extension reads across lanes)
         const int *cw = reinterpret_cast<const int *>(sc.ring + (q % SR) * 32);
         const int *pw = reinterpret_cast<const int *>(sc.ring + ((q + 1) % SR) * 32);
-        const int M0 = Mw;
-        window_ends(L0, L1, L2, L3, p0, WIN - base, cw, pw, dlim, s_tail, tail1, lane, R, list, Mw,
-                    cnt);
-        if (Mw > M0 && lane == 0) atomicMax(s_best, Mw);
+        for (;;) {  // candidates in descending position 4 * lane + c
+          int best = -1;
+          if (m0) best = 4 * (31 - __clz(m0));
+          if (m1) best = max(best, 4 * (31 - __clz(m1)) + 1);
+          if (m2) best = max(best, 4 * (31 - __clz(m2)) + 2);
+          if (m3) best = max(best, 4 * (31 - __clz(m3)) + 3);
+          if (best < 0) break;
+          const unsigned keep = ~(1u << (best >> 2));
+          const int bc = best & 3;
+          m0 = bc == 0 ? m0 & keep : m0;
+          m1 = bc == 1 ? m1 & keep : m1;
+          m2 = bc == 2 ? m2 & keep : m2;
+          m3 = bc == 3 ? m3 & keep : m3;
+          const int jj = base + best;
+          // the row's text starts at position 0: pair index WIN - base
+          const int L = pair_extend(WIN + best, WIN - base, cw, pw, D, s_tail, tail1, lane);
+          if (L > Mw) { Mw = L; cnt = 0; }
+          if (L == Mw && cnt < R) {
+            if (lane == 0) list[cnt] = jj;
+            ++cnt;
+          }
+        }
         __syncwarp();  // cross-lane reads of the slot done before it is refilled
       }
     }
@@ -950,7 +961,7 @@ __device__ __forceinline__ void st_release_u32(uint32_t *p, uint32_t v) {
 }
 
 // CTA 0 of a fused step: the ingest of the step's finished docs.
-__device__ __forceinline__ void step_ingest(const ProposeArgs &a) {
+__device__ __forceinline__ void step_ingest(const ProposeArgs &a, long long dcap) {
   extern __shared__ __align__(16) int dsm[];
   __shared__ uint32_t s_e0;
   if (threadIdx.x == 0 && a.step_ready != nullptr) {
@@ -961,7 +972,7 @@ __device__ __forceinline__ void step_ingest(const ProposeArgs &a) {
   __syncthreads();
   const SmallIngest g{a.tok, a.ntok, a.B, a.S, a.V, a.ing_rows, a.ing_starts, a.ing_lengths,
                       a.ing_m, a.ring, a.C, a.rs, a.doc_start, a.doc_len, a.max_docs, a.err,
-                      a.step_ready, s_e0 + 1 + a.ing_skew, a.step_sync, a.desc, a.dcap, a.sig};
+                      a.step_ready, s_e0 + 1 + a.ing_skew, a.step_sync, a.desc, dcap, a.sig};
   ingest_small_cta(g, *reinterpret_cast<SmallIngestSmem *>(dsm));
 }
 
@@ -1168,7 +1179,7 @@ __device__ void vote_warp(const ProposeArgs &a, const int *cont, int capp, const
 // the update and the self scan only; the row's self result is written to
 // a.self_res.  MODE 2 (second launch): one warp reads that result back in
 // place of the scan, the probe warps and the vote run as in MODE 0.
-template <int MODE>
+template <int MODE, bool EXT>
 __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) {
   constexpr bool SELF_ONLY = MODE == 1, FROM_RES = MODE == 2;
   extern __shared__ __align__(16) int dsm[];
@@ -1185,7 +1196,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // list is in s_wlist1 once merged); the fused step's epoch
   __shared__ long long s_ds;
   __shared__ int s_dv, s_Md, s_cd;
-  __shared__ int s_best_self, s_best_delta;  // longest match so far in the row / the delta
+  __shared__ int s_best_delta;  // longest delta match so far (over the self warps)
   __shared__ int s_dstate[MAX_SELF_WARPS];  // per self warp: its delta (length << 16 | ends)
   __shared__ int s_dcB, s_dcN, s_dmore;     // the CTA's delta list: length, ends; another round
   __shared__ uint32_t s_ep;
@@ -1229,7 +1240,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     // Where the delta lies.  In a fused step this is read before the CTA counts
     // itself in below: the ingest CTA changes the ring state only after every
     // row CTA has, so all rows see the ring as it was before the step's docs.
-    if (!FROM_RES && a.dcap > 0 && a.desc != nullptr && lane == 0) {
+    if (EXT && !FROM_RES && a.dcap > 0 && a.desc != nullptr && lane == 0) {
       const DeltaView v = delta_view(*a.rs, a.desc->lin_pushed, a.desc->lin_wp, a.C, a.doc_start);
       s_ds = v.start;
       s_dv = (int)min(v.len, a.dcap);
@@ -1251,7 +1262,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     if (early && lane < 4) s_early[lane] = a.sampled[(size_t)b * a.T + (n - n_old) - 1 - lane];
     if (FROM_RES) {  // the first launch's result: Ms, cs, the last four tokens; the delta's
       const int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
-      const int v = lane < 6 ? __ldg(res + lane) : (lane < 10 ? __ldg(res + R + lane) : 0);
+      const int v = lane < 6 ? __ldg(res + lane) : (EXT && lane < 10 ? __ldg(res + R + lane) : 0);
       if (lane >= 2 && lane < 6) s_early[lane - 2] = v;
       early = n >= 4;
       const int Ms = __shfl_sync(FULL, v, 0), cs = __shfl_sync(FULL, v, 1);
@@ -1290,7 +1301,6 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_cpf = 0;
       s_ckey = 0;
       s_ep = e0;
-      s_best_self = 0;
       s_best_delta = 0;
       for (int w = 0; w < MAX_SELF_WARPS; ++w) s_dstate[w] = 0;
       s_dcB = 0;
@@ -1316,7 +1326,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   float *pr = a.probs ? a.probs + (size_t)b * k : nullptr;
   // fused step with a delta: the ingest CTA may wait for every row CTA to be
   // done with the ring before appending to it
-  const bool done_signal = MODE == 0 && a.dcap > 0 && a.ing_m > 0 && a.step_ready != nullptr;
+  const bool done_signal = EXT && MODE == 0 && a.dcap > 0 && a.ing_m > 0 && a.step_ready != nullptr;
   if (!((a.active == nullptr || a.active[b] != 0) && n > 0)) {
     if (done_signal && tid == 0) step_done(a.step_sync, s_ep);
     if constexpr (!SELF_ONLY) {  // (the self-only launch leaves the outputs to the second)
@@ -1373,8 +1383,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     }
   } else if (!FROM_RES && warp < a.nself) {
     int Mw, cnt, cnt1;
-    self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, s_wlist1 + warp * R, &s_best_self, lane,
-                 sc, Mw, cnt, cnt1);
+    self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, s_wlist1 + warp * R, lane, sc, Mw, cnt,
+                 cnt1);
     if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; s_wcnt1[warp] = cnt1; }
     // The self result: the longest length over the warps and its most recent
     // ends (warps hold ascending ranges); published to the probe warps.
@@ -1415,7 +1425,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         }
       }
     };
-    if (s_dv > 0 && D >= 2 && n >= 2) {
+    if (EXT && s_dv > 0 && D >= 2 && n >= 2) {
       // The delta, after the row.  Its first windows are requested before the
       // self merge (each warp's ring is free again); the per-warp lists are
       // reused once warp 0 has merged the row's.
@@ -1510,7 +1520,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       if (lane == 0) last = atomicAdd(&s_self_done, 1) == a.nself - 1;
       last = __shfl_sync(FULL, last, 0);
       if (last) merge_self();  // the last self warp to finish
-      if (SELF_ONLY && warp == 0 && lane == 0) {  // no delta for this row
+      if (EXT && SELF_ONLY && warp == 0 && lane == 0) {  // no delta for this row
         int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
         res[R + 6] = 0;
         res[R + 7] = 0;
@@ -1529,7 +1539,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     // (Score-ranked selection: a shorter corpus match may still win, so the
     // corpus candidate is always found in full.)
     auto self_len = [&](bool wait) {
-      if (a.by_score) return -1;
+      if (EXT && a.by_score) return -1;
       if (ptid == 0) {
         unsigned spins = 0;
         while (wait && *(volatile int *)&s_ms_ready == 0 && ++spins < (1u << 22)) __nanosleep(64);
@@ -1791,15 +1801,15 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // The corpus is the snapshot followed by the delta: its longest match is
   // the longer of the two, and at equal lengths the delta's ends are the more
   // recent, so they come first and the snapshot's fill the rest of the R.
-  const int Ms = s_Ms, Mcs = corpus_ok ? s_Mc : 0, Md = s_Md;
+  const int Ms = s_Ms, Mcs = corpus_ok ? s_Mc : 0, Md = EXT ? s_Md : 0;
   const int Mc = max(Mcs, Md);
   // score-ranked selection with both candidates: the corpus's is prepared as
   // below, the row's beside it, and the vote decides
-  const bool both = a.by_score && Ms > 0 && Mc > 0;
+  const bool both = EXT && a.by_score && Ms > 0 && Mc > 0;
   int src, M;
   if (Mc > Ms || both) { src = 2; M = Mc; }
   else { src = Ms > 0 ? 1 : 0; M = Ms; }
-  const int nd = src == 2 && Md == Mc ? s_cd : 0;               // delta ends voting
+  const int nd = EXT && src == 2 && Md == Mc ? s_cd : 0;        // delta ends voting
   const int ns = src == 2 && Mcs == Mc ? min(s_c0c, R - nd) : 0;  // snapshot ends voting
   const int cap = M > 0 ? draft_cap(a, M, n) : 0;
   const int c0 = src == 2 ? nd + ns : s_cs;
@@ -1867,7 +1877,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   int *cont_s = reinterpret_cast<int *>(s_L) + 768;
   const int cap_s = both ? draft_cap(a, Ms, n) : 0, capp_s = (cap_s + 3) & ~3, cs = s_cs;
   int *run_s = cont_s + cs * capp_s;
-  if (both && cap_s > 0) {
+  if constexpr (EXT) if (both && cap_s > 0) {
     for (int idx = tid; idx < cs * cap_s; idx += nthr) {
       const int o = idx / cap_s, d = idx - o * cap_s;
       const int pos = s_occ[o] + 1 + d;
@@ -1926,14 +1936,25 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
 // per SM, and up to 20 warps with one.  Long rows, two launches: the update
 // and self scan (self warps only, small footprint, many CTAs per SM), then
 // the corpus chain and vote (one warp + the probe warps).
-template <int MAXT, int MINB, int MODE>
+// EXT: the kernel also handles the delta and score-ranked selection; the
+// instantiations without them are what a context with neither runs (the
+// extra code costs registers and latency even when unused).
+template <int MAXT, int MINB, int MODE, bool EXT>
 __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a) {
   if (MODE != 1 && a.ing_m > 0) {
-    if (blockIdx.x == 0) step_ingest(a);
-    else propose_body<MODE>(a, blockIdx.x - 1);
+    if (blockIdx.x == 0) step_ingest(a, EXT ? a.dcap : 0);
+    else propose_body<MODE, EXT>(a, blockIdx.x - 1);
   } else {
-    propose_body<MODE>(a, blockIdx.x);
+    propose_body<MODE, EXT>(a, blockIdx.x);
   }
+}
+
+template <int MAXT, int MINB, int MODE>
+void launch_kernel(bool ext, int grid, int threads, size_t smem, cudaStream_t st, const ProposeArgs &a) {
+  if (ext)
+    propose_kernel<MAXT, MINB, MODE, true><<<grid, threads, smem, st>>>(a);
+  else
+    propose_kernel<MAXT, MINB, MODE, false><<<grid, threads, smem, st>>>(a);
 }
 
 }  // namespace
@@ -1954,14 +1975,15 @@ int propose_step_max_docs() { return SMALL_DOCS; }
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   if (a.B <= 0) return cudaSuccess;
   const int probe = a.desc ? NPROBE3 : 0;
+  const bool ext = a.dcap > 0 || a.by_score;
   if (!a.split) {
     const int warps = a.nself + probe;
     const size_t smem = propose_smem_bytes(0, a.nself, a.R, a.k, a.cand_cap);
     const int grid = a.B + (a.ing_m > 0 ? 1 : 0);
     if (warps <= 12)
-      propose_kernel<384, 2, 0><<<grid, 32 * warps, smem, st>>>(a);
+      launch_kernel<384, 2, 0>(ext, grid, 32 * warps, smem, st, a);
     else
-      propose_kernel<640, 1, 0><<<grid, 32 * warps, smem, st>>>(a);
+      launch_kernel<640, 1, 0>(ext, grid, 32 * warps, smem, st, a);
     return cudaGetLastError();
   }
   // first launch: update + self scan of every row, and of the delta (no
@@ -1971,9 +1993,9 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   a1.ing_m = 0;
   const size_t smem1 = propose_smem_bytes(1, a.nself, a.R, a.k, a.cand_cap);
   if (a.nself <= 8)
-    propose_kernel<256, 3, 1><<<a.B, 32 * a.nself, smem1, st>>>(a1);
+    launch_kernel<256, 3, 1>(ext, a.B, 32 * a.nself, smem1, st, a1);
   else
-    propose_kernel<512, 1, 1><<<a.B, 32 * a.nself, smem1, st>>>(a1);
+    launch_kernel<512, 1, 1>(ext, a.B, 32 * a.nself, smem1, st, a1);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   // second launch: corpus chain and vote; the rows are updated already, so the
@@ -1985,7 +2007,7 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   a2.step_sync = nullptr;
   const size_t smem2 = propose_smem_bytes(2, 1, a.R, a.k, a.cand_cap);
   const int grid2 = a.B + (a.ing_m > 0 ? 1 : 0);
-  propose_kernel<128, 3, 2><<<grid2, 32 * (1 + probe), smem2, st>>>(a2);
+  launch_kernel<128, 3, 2>(ext, grid2, 32 * (1 + probe), smem2, st, a2);
   return cudaGetLastError();
 }
 
@@ -1998,9 +2020,12 @@ cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, i
 
 cudaError_t propose_set_smem_limit(size_t bytes) {
   // every instantiation may be launched with up to `bytes` of dynamic shared memory
-  const void *fns[] = {(const void *)propose_kernel<384, 2, 0>, (const void *)propose_kernel<640, 1, 0>,
-                       (const void *)propose_kernel<256, 3, 1>, (const void *)propose_kernel<512, 1, 1>,
-                       (const void *)propose_kernel<128, 3, 2>};
+  const void *fns[] = {
+      (const void *)propose_kernel<384, 2, 0, false>, (const void *)propose_kernel<640, 1, 0, false>,
+      (const void *)propose_kernel<256, 3, 1, false>, (const void *)propose_kernel<512, 1, 1, false>,
+      (const void *)propose_kernel<128, 3, 2, false>, (const void *)propose_kernel<384, 2, 0, true>,
+      (const void *)propose_kernel<640, 1, 0, true>,  (const void *)propose_kernel<256, 3, 1, true>,
+      (const void *)propose_kernel<512, 1, 1, true>,  (const void *)propose_kernel<128, 3, 2, true>};
   for (const void *f : fns) {
     const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes);
     if (e != cudaSuccess) return e;
