@@ -41,7 +41,7 @@ constexpr int OS_TILE = OS_THREADS * OS_ITEMS;  // 2048 items per tile
 constexpr int RADIX = 256;
 constexpr unsigned SPIN_LIMIT = 1u << 18;  // polls (backing off to 256 ns): ~0.2 s; a normal wait is microseconds
 constexpr int MAX_PASSES = 250;            // ticket counters per build
-constexpr int LB = 8;                      // look-back words a thread reads per round trip
+constexpr int LB = 4;                      // look-back words a thread reads per round trip (wider reads more that go unused)
 
 // counter layout (uint32 words): [0] active count written by the post pass,
 // [1] [2] smallest and largest token (order-preserving unsigned codes), [3]
