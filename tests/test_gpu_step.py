@@ -288,17 +288,28 @@ def test_fixed_length_drafts_lockstep(mode):
     ls.close()
 
 
-@pytest.mark.parametrize("mode,delta", [(1, 0), (2, 0), (1, 1 << 16)],
-                         ids=["one-launch", "two-launch", "one-launch+delta"])
-def test_select_by_score_lockstep(mode, delta):
+SCORE_CASES = [
+    (dict(propose_mode=1), {}, 0),
+    (dict(propose_mode=2), {}, 0),
+    (dict(propose_mode=1), {}, 1 << 16),
+    (dict(propose_mode=1, draft_mode=1), dict(fixed_length=True), 0),
+    (dict(propose_mode=1, corpus_records=0, corpus_gram_index=0), {}, 0),
+]
+
+
+@pytest.mark.parametrize("over,pover,delta", SCORE_CASES,
+                         ids=["one-launch", "two-launch", "one-launch+delta", "fixed-length",
+                              "text+descent"])
+def test_select_by_score_lockstep(over, pover, delta):
     """Score-ranked selection (select_by_score 1: the row's and the corpus's
     candidates both voted, the better score wins) through the fused step,
-    with rebuilds (and a delta), against the oracle."""
+    with rebuilds, against the oracle -- in both launch modes, with a delta,
+    with Model Runner V2 drafts and through the text / descent corpus path."""
     W, O, H = _mods()
     cfg = dataclasses.replace(W.CONFIGS["c3"], rebuild_tokens=4096)
     ls = H.Lockstep(cfg, seed=13, B=64, steps=10, finish_frac=0.1, corpus=1 << 16, fused=True,
-                    drafter_over=dict(propose_mode=mode, select_by_score=1),
-                    param_over=dict(select_by_score=True), delta=delta)
+                    drafter_over=dict(over, select_by_score=1),
+                    param_over=dict(pover, select_by_score=True), delta=delta)
     ls.prefill(seed=13)
     switched = 0
     for i in range(10):
@@ -306,7 +317,8 @@ def test_select_by_score_lockstep(mode, delta):
         if i >= 1:  # the rule must change some rows' source for the test to mean anything
             a = O.propose(ls.p, ls.o_tok, ls.o_n, X=ls.oracle_corpus(), threads=H.THREADS)
             p2 = O.Params(**{k: getattr(ls.p, k) for k in ("S", "V", "k", "D", "R", "offset")},
-                          factor=ls.p.factor, min_prob=ls.p.min_prob)
+                          factor=ls.p.factor, min_prob=ls.p.min_prob,
+                          fixed_length=ls.p.fixed_length)
             b2 = O.propose(p2, ls.o_tok, ls.o_n, X=ls.oracle_corpus(), threads=H.THREADS)
             switched += int((a.match_info[:, 1] != b2.match_info[:, 1]).sum())
     assert switched > 0
