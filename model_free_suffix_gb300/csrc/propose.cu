@@ -363,7 +363,35 @@ struct DeltaScan {
   int off;  // Y index 0 lies at this offset of window 0
   int w0;   // ring window of window 0
   int nrw;  // ring windows (C / WIN)
+  __device__ __forceinline__ int rwin(int r) const {  // ring window of delta window r (r >= -1)
+    const int x = (w0 + r) % nrw;
+    return x < 0 ? x + nrw : x;
+  }
 };
+
+// The row's last 2, 3 and 4 tokens as signature buckets.
+struct DeltaGrams {
+  unsigned b2, b3, b4;
+};
+
+// A block's signature words requested ahead of its round (lane i < DNB: the
+// words of window hi - i for the row's 2-, 3- and 4-gram buckets).
+struct SigAhead {
+  uint32_t w2, w3, w4;
+};
+
+__device__ __forceinline__ SigAhead sig_ahead(const uint32_t *sig, const DeltaScan &sc,
+                                              const DeltaGrams &g, int hi, int dlim, int lane) {
+  SigAhead p{0u, 0u, 0u};
+  const int r = hi - lane;
+  if (lane < DNB && r >= 0) {
+    const size_t rw = (size_t)sc.rwin(r);
+    p.w2 = sig[(size_t)(g.b2 >> 5) * sc.nrw + rw];
+    if (dlim >= 3) p.w3 = sig[(size_t)(g.b3 >> 5) * sc.nrw + rw];
+    if (dlim >= 4) p.w4 = sig[(size_t)(g.b4 >> 5) * sc.nrw + rw];
+  }
+  return p;
+}
 
 __device__ __forceinline__ void delta_windows(long long C, long long ds, int dv, DeltaScan &sc) {
   sc.off = (int)(ds % WIN);
@@ -390,22 +418,17 @@ __device__ __forceinline__ void ring_copy(const int32_t *ring, int rw, int lane,
 __device__ void delta_process(const int32_t *ring, const uint32_t *sig, int dv, int Z, int D, int n,
                               int R, const int *s_tail, int lane, int4 *sring, const DeltaScan &sc,
                               int rlo, int rhi, int *list, int *s_best, int *s_state, int cB, int cN,
-                              int warp, int nself, int &Mw, int &cnt) {
+                              int warp, int nself, const DeltaGrams &grams, const SigAhead *ahead,
+                              int &Mw, int &cnt) {
   Mw = 0;
   cnt = 0;
   const int t0 = s_tail[0], t1 = s_tail[1];
   const int dlim = min(D, n);
   const int tail1 = lane + 1 < dlim ? s_tail[1 + lane] : 0;
   const int t2 = dlim >= 3 ? s_tail[2] : 0, t3 = dlim >= 4 ? s_tail[3] : 0;
-  const unsigned b2 = sig_bucket(2, t0, t1, 0, 0);
-  const unsigned b3 = dlim >= 3 ? sig_bucket(3, t0, t1, t2, 0) : 0u;
-  const unsigned b4 = dlim >= 4 ? sig_bucket(4, t0, t1, t2, t3) : 0u;
+  const unsigned b2 = grams.b2, b3 = grams.b3, b4 = grams.b4;
   const int nrw = sc.nrw;
-  auto rwin = [&](int r) {  // ring window of delta window r (r >= -1)
-    int x = sc.w0 + r;
-    x %= nrw;
-    return x < 0 ? x + nrw : x;
-  };
+  auto rwin = [&](int r) { return sc.rwin(r); };
   // the shortest end that can still change the result (> dlim: none)
   auto need = [&]() {
     const int B = max(*(const volatile int *)s_best, 2);
@@ -419,12 +442,16 @@ __device__ void delta_process(const int32_t *ring, const uint32_t *sig, int dv, 
     return nd;
   };
   // windows r - 31 .. r whose signature has the bucket of the `o`-gram (o <= 4): bit i
+  // (ahead: the words of the block [rlo, rhi], at most DNB windows, already read)
   auto candidates = [&](int r, int o, int ilo) {
     const unsigned bk = o == 2 ? b2 : (o == 3 ? b3 : b4);
     const int rr = r - lane;
     bool hit = false;
-    if (lane >= ilo && rr >= rlo)
-      hit = (sig[(size_t)(bk >> 5) * nrw + rwin(rr)] >> (bk & 31)) & 1u;
+    if (lane >= ilo && rr >= rlo) {
+      const uint32_t w = ahead != nullptr ? (o == 2 ? ahead->w2 : (o == 3 ? ahead->w3 : ahead->w4))
+                                          : sig[(size_t)(bk >> 5) * nrw + rwin(rr)];
+      hit = (w >> (bk & 31)) & 1u;
+    }
     return __ballot_sync(FULL, hit);
   };
   bool done = false;
@@ -1433,6 +1460,14 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       DeltaScan dsc;
       delta_windows(a.C, s_ds, s_dv, dsc);
       const int G = DNB * a.nself;  // windows per round
+      const int dlim = min(D, n);
+      const int t2 = dlim >= 3 ? s_tail[2] : 0, t3 = dlim >= 4 ? s_tail[3] : 0;
+      const DeltaGrams grams{sig_bucket(2, s_tail[0], s_tail[1], 0, 0),
+                             dlim >= 3 ? sig_bucket(3, s_tail[0], s_tail[1], t2, 0) : 0u,
+                             dlim >= 4 ? sig_bucket(4, s_tail[0], s_tail[1], t2, t3) : 0u};
+      // the signature words of each round's block are read one round ahead
+      // (round 0's while the row's result is merged)
+      SigAhead ahead = sig_ahead(a.sig, dsc, grams, dsc.nw - 1 - DNB * (a.nself - 1 - warp), dlim, lane);
       self_sync(a.nself);
       if (warp == 0) merge_self();
       self_sync(a.nself);
@@ -1442,9 +1477,11 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       int covered = 0;
       for (int t = 0;; ++t) {
         const int hi = dsc.nw - 1 - t * G - DNB * (a.nself - 1 - warp);
+        const SigAhead cur = ahead;
+        ahead = sig_ahead(a.sig, dsc, grams, hi - G, dlim, lane);  // the next round's
         int M = 0, c = 0;
         delta_process(a.ring, a.sig, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, max(0, hi - DNB + 1),
-                      hi, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp, a.nself, M, c);
+                      hi, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp, a.nself, grams, &cur, M, c);
         if (lane == 0) s_dstate[warp] = M << 16 | c;
         self_sync(a.nself);
         covered = min(dsc.nw, covered + G);
@@ -1480,7 +1517,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       int dM = 0, dcnt = 0;
       delta_process(a.ring, a.sig, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, warp * per,
                     min(rest, (warp + 1) * per) - 1, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp,
-                    a.nself, dM, dcnt);
+                    a.nself, grams, nullptr, dM, dcnt);
       if (lane == 0) s_dstate[warp] = dM << 16 | dcnt;
       self_sync(a.nself);
       if (warp == 0) {
