@@ -47,7 +47,7 @@ class _Params(ctypes.Structure):
                 ("fN", ctypes.c_int64), ("fD", ctypes.c_int64), ("offset", ctypes.c_int64),
                 ("pN", ctypes.c_int64), ("pD", ctypes.c_int64),
                 ("depth_sum_cap", ctypes.c_int32), ("fixed_length", ctypes.c_int32),
-                ("select_by_score", ctypes.c_int32)]
+                ("select_by_score", ctypes.c_int32), ("num_backoff", ctypes.c_int32)]
 
 
 _lib = None
@@ -67,6 +67,8 @@ def lib():
         _lib.orc_self_match.argtypes = [P, i32, i32, i32, P, P]
         _lib.orc_corpus_match.restype = i32
         _lib.orc_corpus_match.argtypes = [P, i64, i32, P, i32, i32, i32, P, P]
+        _lib.orc_backoff_lengths.restype = i32
+        _lib.orc_backoff_lengths.argtypes = [P, i64, i32, i32, P, P]
         _lib.orc_propose_row.restype = None
         _lib.orc_propose_row.argtypes = [P, P, i32, P, i64, i32, P, P, P, P, P, P]
         _lib.orc_propose.restype = u32
@@ -112,10 +114,11 @@ def rational(x, denom: int = 10 ** 6):
 
 class Params:
     """Drafter knobs (S, V, k, D, R, factor, offset, min_prob, depth_sum_cap, fixed_length,
-    select_by_score)."""
+    select_by_score, num_backoff)."""
 
     def __init__(self, S, V, k=16, D=24, R=64, factor=(1, 1), offset=0,
-                 min_prob=(1, 10), depth_sum_cap=False, fixed_length=False, select_by_score=False):
+                 min_prob=(1, 10), depth_sum_cap=False, fixed_length=False, select_by_score=False,
+                 num_backoff=1):
         self.S, self.V, self.k, self.D, self.R = int(S), int(V), int(k), int(D), int(R)
         self.factor = rational(factor)
         self.offset = int(offset)
@@ -123,11 +126,12 @@ class Params:
         self.depth_sum_cap = bool(depth_sum_cap)
         self.fixed_length = bool(fixed_length)
         self.select_by_score = bool(select_by_score)
+        self.num_backoff = int(num_backoff)
 
     def c(self) -> _Params:
         return _Params(self.S, self.V, self.k, self.D, self.R, self.factor[0], self.factor[1],
                        self.offset, self.min_prob[0], self.min_prob[1], int(self.depth_sum_cap),
-                       int(self.fixed_length), int(self.select_by_score))
+                       int(self.fixed_length), int(self.select_by_score), self.num_backoff)
 
 
 def update_state(token_ids: np.ndarray, num_tokens: np.ndarray, sampled: np.ndarray, V: int) -> int:
@@ -161,6 +165,17 @@ class Proposal:
     def __init__(self, drafts, num_valid, score, probs, match_info, flags):
         self.drafts, self.num_valid, self.score = drafts, num_valid, score
         self.probs, self.match_info, self.flags = probs, match_info, flags
+
+
+def backoff_lengths(L, minlen: int, nb: int):
+    """Candidate lengths of multi-length backoff ([PYPI] How it works, step 1):
+    the distinct values among the nb largest match lengths >= minlen, longest
+    first, with the number of ends reaching each."""
+    L = _i32(L)
+    lens = np.zeros(max(nb, 1), dtype=np.int32)
+    sup = np.zeros(max(nb, 1), dtype=np.int64)
+    c = lib().orc_backoff_lengths(_p(L), L.shape[0], minlen, nb, _p(lens), _p(sup))
+    return [(int(lens[i]), int(sup[i])) for i in range(c)]
 
 
 def propose_row(p: Params, t, n: int, X=None, active: bool = True) -> Proposal:

@@ -10,7 +10,9 @@
  * the design notes of the repository):
  *   - an occurrence must have a continuation: self ends j <= n-2, corpus ends
  *     e with X[e+1] != Z;
- *   - only the longest match length votes (no backoff);
+ *   - only the longest match length votes, unless num_backoff > 1: then the
+ *     t-th largest match lengths (t = 1..num_backoff) of each path are
+ *     candidates too, each with its own ends, and the best score wins;
  *   - up to R occurrences are kept, the most recent (largest position) first;
  *   - vote ties go to the smallest token id;
  *   - chain probability P_d = |O_{d+1}| / |O_0|; a token is emitted iff
@@ -210,6 +212,99 @@ static void expand(const orc_params *p, int32_t source, const int32_t *t, int32_
   *sum_out = sum;
 }
 
+/* ------------------------------------------------------------------------ */
+/* Multi-length backoff: [PYPI] Highlights ("Multi-length backoff matching":
+ * the longest suffix plus shorter, better-supported lengths) and How it
+ * works, steps 1-3 (for support threshold t the largest length occurring at
+ * least t times, i.e. the t-th largest match_back value; every candidate is
+ * expanded and scored, the best wins per path and the two winners compete by
+ * the same score).  The thresholds t = 1..nb name at most nb distinct
+ * lengths: each is found by a plain scan for the largest value below the
+ * previous one, until nb ends are covered. */
+int32_t orc_backoff_lengths(const int32_t *L, int64_t nends, int32_t minlen,
+                            int32_t nb, int32_t *len, int64_t *support) {
+  int32_t cnt = 0, prev = INT32_MAX;
+  int64_t covered = 0; /* ends with L >= the last length found: thresholds 1..covered */
+  while (covered < nb) {
+    int32_t best = 0;
+    for (int64_t e = 0; e < nends; e++)
+      if (L[e] >= minlen && L[e] < prev && L[e] > best) best = L[e];
+    if (best == 0) break;
+    int64_t sup = 0;
+    for (int64_t e = 0; e < nends; e++)
+      if (L[e] >= best) sup++;
+    len[cnt] = best;
+    support[cnt] = sup;
+    cnt++;
+    covered = sup;
+    prev = best;
+  }
+  return cnt;
+}
+
+/* Backoff selection for one row (p->num_backoff > 1).  The self lengths L(j)
+ * and corpus lengths Lc(e) are those of orc_self_match / orc_corpus_match
+ * (an end without a continuation has none).  A candidate (path, length l)
+ * votes with the R most recent ends of L >= l, capped as a match of length l.
+ * Best: the higher score sum / c0 (exact), then the longer length, then the
+ * row itself.  Writes the winner's draft, probabilities and (M, source, c0,
+ * len, sum); M = 0 when neither path has a candidate. */
+static void propose_backoff(const orc_params *p, const int32_t *t, int32_t n,
+                            const int32_t *X, int64_t N, int32_t Z, int32_t *drafts,
+                            float *probs, int32_t *M_out, int32_t *source_out,
+                            int32_t *c0_out, int32_t *len_out, int64_t *sum_out) {
+  const int32_t nb = p->num_backoff;
+  const int32_t k = p->k;
+  int32_t *fill = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+  int32_t *d2 = (int32_t *)malloc(sizeof(int32_t) * (size_t)k);
+  float *p2 = (float *)malloc(sizeof(float) * (size_t)k);
+  int32_t *occ = (int32_t *)malloc(sizeof(int32_t) * (size_t)p->R);
+  int32_t *lens = (int32_t *)malloc(sizeof(int32_t) * (size_t)nb);
+  int64_t *sup = (int64_t *)malloc(sizeof(int64_t) * (size_t)nb);
+  for (int32_t d = 0; d < k; d++) fill[d] = drafts[d];
+  *M_out = 0; *source_out = 0; *c0_out = 0; *len_out = 0; *sum_out = 0;
+  for (int32_t source = 1; source <= 2; source++) {
+    int64_t nends = 0;
+    int32_t *L = NULL;
+    if (source == 1 && n >= 2 && p->D >= 1) {
+      nends = n - 1;
+      L = (int32_t *)malloc(sizeof(int32_t) * (size_t)nends);
+      for (int32_t j = 0; j <= n - 2; j++) {
+        int32_t lim = min32(p->D, j + 1), l = 0;
+        while (l < lim && t[j - l] == t[n - 1 - l]) l++;
+        L[j] = l;
+      }
+    } else if (source == 2 && X != NULL && N >= 2 && n >= 2 && p->D >= 2) {
+      nends = N - 1;
+      L = (int32_t *)malloc(sizeof(int32_t) * (size_t)nends);
+      for (int64_t e = 0; e <= N - 2; e++)
+        L[e] = X[e + 1] == Z ? 0 : corpus_L(X, e, t, n, p->D);
+    }
+    if (L == NULL) continue;
+    const int32_t nl = orc_backoff_lengths(L, nends, source == 1 ? 1 : 2, nb, lens, sup);
+    for (int32_t i = 0; i < nl; i++) {
+      int32_t c0 = 0;
+      for (int64_t e = nends - 1; e >= 0 && c0 < p->R; e--)
+        if (L[e] >= lens[i]) occ[c0++] = (int32_t)e;
+      for (int32_t d = 0; d < k; d++) { d2[d] = fill[d]; p2[d] = 0.0f; }
+      int32_t len;
+      int64_t sum;
+      expand(p, source, t, n, X, N, Z, occ, c0, lens[i], d2, p2, &len, &sum);
+      int better = *M_out == 0;
+      if (!better) {
+        const int64_t lhs = sum * *c0_out, rhs = *sum_out * c0;
+        better = lhs > rhs || (lhs == rhs && lens[i] > *M_out);
+      }
+      if (better) {
+        *M_out = lens[i]; *source_out = source; *c0_out = c0; *len_out = len; *sum_out = sum;
+        for (int32_t d = 0; d < k; d++) { drafts[d] = d2[d]; if (probs) probs[d] = p2[d]; }
+      }
+    }
+    free(L);
+  }
+  free(fill); free(d2); free(p2); free(occ); free(lens); free(sup);
+}
+
 void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n_in,
                      const int32_t *X, int64_t N, int32_t active,
                      int32_t *drafts, int32_t *num_valid, float *score,
@@ -243,7 +338,9 @@ void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n_in,
 
   int32_t source, M, c0, len = 0;
   int64_t sum = 0;
-  if (p->select_by_score && Ms > 0 && Mc > 0) {
+  if (p->num_backoff > 1) {
+    propose_backoff(p, t, n, X, N, Z, drafts, probs, &M, &source, &c0, &len, &sum);
+  } else if (p->select_by_score && Ms > 0 && Mc > 0) {
     /* [PYPI] How it works, step 3: both candidates are expanded and the
      * better score (sum / c0, compared exactly) wins; equal scores go to the
      * longer match, then to the row itself */

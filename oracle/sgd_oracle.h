@@ -56,6 +56,10 @@ typedef struct {
   int32_t select_by_score; /* 1: the row's and the corpus's candidates are both
                            expanded and the better score wins ([PYPI] How it
                            works, step 3); 0: the longer match wins ([DOCS])    */
+  int32_t num_backoff;  /* candidate lengths per path ([PYPI] How it works, steps
+                           1-3: for t = 1..num_backoff the t-th largest match
+                           length); > 1 ranks every candidate by score.  0 or 1:
+                           the longest match only                               */
 } orc_params;
 
 /* Append the accepted prefix of one row's sampled ids ([PYPI] Quickstart,
@@ -74,6 +78,14 @@ int32_t orc_self_match(const int32_t *t, int32_t n, int32_t D, int32_t R,
 int32_t orc_corpus_match(const int32_t *X, int64_t N, int32_t Z,
                          const int32_t *t, int32_t n, int32_t D, int32_t R,
                          int32_t *occ, int32_t *count);
+
+/* Multi-length backoff ([PYPI] Highlights, "Multi-length backoff matching";
+ * How it works, step 1): the distinct values among the nb largest entries of
+ * the multiset {L(e)} over the path's ends (self: L >= 1, ends j <= n-2;
+ * corpus: L >= 2, ends with a continuation), longest first.  Returns their
+ * count; len[i] and support[i] (the number of ends with L >= len[i]). */
+int32_t orc_backoff_lengths(const int32_t *L, int64_t nends, int32_t minlen,
+                            int32_t nb, int32_t *len, int64_t *support);
 
 /* One row: match, select, cap, frequency-greedy expansion. */
 void orc_propose_row(const orc_params *p, const int32_t *t, int32_t n,

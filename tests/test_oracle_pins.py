@@ -591,3 +591,155 @@ def test_select_by_score_picks_the_better_of_the_two(orc):
             assert sc.match_info[b].tolist() == win.match_info[b].tolist()
             assert sc.score[b] == win.score[b] and np.array_equal(sc.probs[b], win.probs[b])
     assert checked > 20
+
+
+def test_backoff_lengths_worked_examples(orc):
+    """[PYPI] How it works, step 1: for support threshold t the candidate is the
+    largest length occurring at least t times, the t-th largest match_back
+    value; thresholds 1..nb name the distinct values among the nb largest."""
+    L = [3, 1, 3, 2, 0, 5, 2]  # sorted: 5 3 3 2 2 1 0
+    assert orc.backoff_lengths(L, 1, 1) == [(5, 1)]
+    assert orc.backoff_lengths(L, 1, 2) == [(5, 1), (3, 3)]
+    assert orc.backoff_lengths(L, 1, 3) == [(5, 1), (3, 3)]           # t = 3 is still 3
+    assert orc.backoff_lengths(L, 1, 4) == [(5, 1), (3, 3), (2, 5)]
+    assert orc.backoff_lengths(L, 1, 8) == [(5, 1), (3, 3), (2, 5), (1, 6)]  # no 0: not a match
+    assert orc.backoff_lengths(L, 2, 8) == [(5, 1), (3, 3), (2, 5)]   # the corpus needs >= 2
+    assert orc.backoff_lengths([0, 0, 1], 2, 8) == []
+    assert orc.backoff_lengths([], 1, 4) == []
+
+
+def test_backoff_lengths_are_the_t_th_largest(orc):
+    """The same lengths read off a descending sort: entry t - 1 for t <= nb."""
+    rng = np.random.default_rng(4)
+    for _ in range(200):
+        L = rng.integers(0, 9, rng.integers(0, 40))
+        nb, minlen = int(rng.integers(1, 10)), int(rng.integers(1, 3))
+        srt = sorted([int(x) for x in L if x >= minlen], reverse=True)
+        want = []
+        for t in range(1, nb + 1):
+            if t <= len(srt) and (not want or want[-1][0] != srt[t - 1]):
+                want.append((srt[t - 1], sum(1 for x in srt if x >= srt[t - 1])))
+        assert orc.backoff_lengths(L, minlen, nb) == want
+
+
+def test_backoff_worked_examples(orc):
+    V = 20
+    # Ends of the row's last token 2 (before the tail itself): 2, 7, 12 match
+    # (3, 1, 2), length 3, continued by 7, 9, 11; 17, 22, 27, 32 match (1, 2)
+    # only, length 2, each continued by 5 6.
+    row = [3, 1, 2, 7, 8, 3, 1, 2, 9, 8, 3, 1, 2, 11, 8] + [4, 1, 2, 5, 6] * 4 + [3, 1, 2]
+    base = dict(S=64, V=V, k=4, D=8, R=8, min_prob=(1, 2))
+    # the longest match alone: three ends that disagree, 1/3 < 1/2 stops the vote
+    for nb in (1, 2, 3):
+        r = _row(orc, orc.Params(**base, num_backoff=nb), row)
+        assert r.match_info[0].tolist() == [3, 1] and r.drafts[0].tolist() == [-1] * 4
+        assert int(r.num_valid[0]) == 0 and float(r.score[0]) == 0.0
+    # threshold 4 reaches length 2: all seven ends vote, 5 (4/7) then 6 (4/7),
+    # capped at factor 1 x 2 tokens; score 8/7 beats the empty draft
+    r = _row(orc, orc.Params(**base, num_backoff=4), row)
+    assert r.match_info[0].tolist() == [2, 1] and r.drafts[0].tolist() == [5, 6, -1, -1]
+    assert r.probs[0].tolist() == [np.float32(4 / 7)] * 2 + [0.0, 0.0]
+    assert abs(float(r.score[0]) - 8 / 7) < 1e-6 and int(r.num_valid[0]) == 2
+    # a corpus doc holding (3, 1, 2, 5, 6): corpus length 3, one end, 5 and 6
+    # at 1/1 (then the sentinel): score 2 > 8/7, the corpus wins
+    r = _row(orc, orc.Params(**base, num_backoff=4), row, X=_doc_text([[3, 1, 2, 5, 6]], V))
+    assert r.match_info[0].tolist() == [3, 2] and r.drafts[0].tolist() == [5, 6, -1, -1]
+    assert r.probs[0].tolist() == [1.0, 1.0, 0.0, 0.0] and float(r.score[0]) == 2.0
+    # (3, 1, 2, 5): one token at 1/1, score 1 < 8/7: the row's length 2 wins
+    # although the corpus match is longer
+    r = _row(orc, orc.Params(**base, num_backoff=4), row, X=_doc_text([[3, 1, 2, 5]], V))
+    assert r.match_info[0].tolist() == [2, 1] and r.drafts[0].tolist() == [5, 6, -1, -1]
+    # the corpus's own backoff: (4, 1, 2, 9) x3 and (3, 1, 2, 7), (3, 1, 2, 8):
+    # length 3 has two ends (thresholds 1, 2): 7 at 1/2 (the tie goes to the
+    # smaller id), then the sentinel, score 1/2; threshold 3 reaches length 2:
+    # five ends, 9 at 3/5, then the sentinel, score 3/5.  The row's length 3
+    # covers thresholds 1..3 and drafts nothing, its length 2 needs 4.
+    X = _doc_text([[4, 1, 2, 9]] * 3 + [[3, 1, 2, 7], [3, 1, 2, 8]], V)
+    r = _row(orc, orc.Params(**base, num_backoff=2), row, X=X)
+    assert r.match_info[0].tolist() == [3, 2] and r.drafts[0].tolist() == [7, -1, -1, -1]
+    assert r.probs[0].tolist() == [0.5, 0.0, 0.0, 0.0] and float(r.score[0]) == 0.5
+    r = _row(orc, orc.Params(**base, num_backoff=3), row, X=X)
+    assert r.match_info[0].tolist() == [2, 2] and r.drafts[0].tolist() == [9, -1, -1, -1]
+    assert abs(float(r.score[0]) - 3 / 5) < 1e-6
+    r = _row(orc, orc.Params(**base, num_backoff=4), row, X=X)  # the row's 8/7 wins
+    assert r.match_info[0].tolist() == [2, 1] and r.drafts[0].tolist() == [5, 6, -1, -1]
+
+
+def test_backoff_reduces_to_score_selection(orc):
+    """A row whose ends all match the same length has one candidate per path
+    whatever num_backoff is: the result is score-ranked selection's.  The row
+    repeats a unit of distinct ids and D is at most the unit's length, so
+    every earlier end of its last id matches D tokens; each corpus doc is the
+    unit followed by ids the unit does not hold."""
+    rng = np.random.default_rng(12)
+    V, S = 12, 96
+    for trial in range(40):
+        u = int(rng.integers(3, 7))
+        unit = list(rng.permutation(6)[:u])
+        row = unit * int(rng.integers(2, 8))
+        D = int(rng.integers(2, u + 1))
+        X = _doc_text([unit + list(rng.integers(6, V, rng.integers(0, 5))) for _ in range(4)], V)
+        assert len(set(l for l in _self_lengths(row, D) if l > 0)) == 1
+        assert len(set(l for l in _corpus_lengths(X.tolist(), row, D, V) if l >= 2)) <= 1
+        kw = dict(S=S, V=V, k=6, D=D, R=int(rng.integers(1, 9)), offset=int(rng.integers(0, 3)))
+        one = _row(orc, orc.Params(**kw, select_by_score=True), row, X=X)
+        for nb in (2, 5, 9):
+            r = _row(orc, orc.Params(**kw, num_backoff=nb), row, X=X)
+            assert r.match_info.tolist() == one.match_info.tolist(), trial
+            assert r.drafts.tolist() == one.drafts.tolist() and r.score[0] == one.score[0]
+            assert r.probs.tolist() == one.probs.tolist()
+
+
+def _self_lengths(t, D):
+    n = len(t)
+    out = []
+    for j in range(n - 1):
+        l = 0
+        while l < min(D, j + 1) and t[j - l] == t[n - 1 - l]:
+            l += 1
+        out.append(l)
+    return out
+
+
+def _corpus_lengths(X, t, D, Z):
+    n = len(t)
+    out = []
+    for e in range(len(X) - 1):
+        l = 0
+        if X[e + 1] != Z:
+            while l < min(D, n, e + 1) and X[e - l] == t[n - 1 - l]:
+                l += 1
+        out.append(l)
+    return out
+
+
+def test_backoff_never_scores_below_fewer_candidates(orc):
+    """Thresholds 1..nb name a superset of those of 1..nb-1, and the best score
+    over a superset is no lower: the winner's score never drops as nb grows,
+    and nb = 2 never scores below score-ranked selection over the longest
+    matches.  The winner's length is one of its path's candidate lengths."""
+    rng = np.random.default_rng(23)
+    V, S, B = 3, 72, 8  # few ids and short docs: continuations often run out
+    seen_shorter = 0
+    for trial in range(25):
+        X = _doc_text([rng.integers(0, V, rng.integers(3, 8)) for _ in range(10)], V)
+        tok = rng.integers(0, V, (B, S)).astype(np.int32)
+        n = rng.integers(3, S - 2, B).astype(np.int32)
+        kw = dict(S=S, V=V, k=8, D=9, R=6, offset=1, min_prob=(1, 2))
+        prev = orc.propose(orc.Params(**kw, select_by_score=True), tok, n, X=X)
+        for nb in (2, 3, 5, 8):
+            cur = orc.propose(orc.Params(**kw, num_backoff=nb), tok, n, X=X)
+            for b in range(B):
+                assert cur.score[b] >= prev.score[b], (trial, nb, b)
+                M, src = cur.match_info[b].tolist()
+                t = tok[b, :n[b]].tolist()
+                own = orc.backoff_lengths(_self_lengths(t, 9), 1, nb)
+                other = orc.backoff_lengths(_corpus_lengths(X.tolist(), t, 9, V), 2, nb)
+                if M == 0:
+                    assert own == [] and other == []
+                    continue
+                cands = [l for l, _ in (own if src == 1 else other)]
+                assert M in cands, (trial, nb, b)
+                seen_shorter += int(M != cands[0])
+            prev = cur
+    assert seen_shorter > 10  # shorter lengths do win
