@@ -142,6 +142,21 @@ typedef struct {
                                   the longer match, then to the row ([PYPI] How it works,
                                   step 3).  The corpus candidate is then always found in
                                   full (no pruning by the row's match). */
+  int32_t  num_backoff;        /* 1 (default): one candidate length per path, the longest
+                                  match.  2..8: multi-length backoff ([PYPI] Highlights,
+                                  How it works, steps 1-3): for each support threshold
+                                  t = 1..num_backoff the t-th largest match length of the
+                                  path (the row: lengths >= 1; the corpus, snapshot and
+                                  delta together: >= 2) is a candidate, voted with the R
+                                  most recent ends reaching that length and capped as a
+                                  match of that length; every candidate of both paths is
+                                  ranked by score as with select_by_score = 1 (equal
+                                  scores: the longer length, then the row), whatever
+                                  select_by_score says.  The match lengths are exact
+                                  (every row end, every corpus end matching the last two
+                                  tokens, every delta position), so this mode costs one
+                                  more launch per step and a scan of the whole
+                                  suffix-array interval of the row's last two tokens. */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)

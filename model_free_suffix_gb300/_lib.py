@@ -63,6 +63,7 @@ class SgdConfig(ctypes.Structure):
         ("delta_capacity", ctypes.c_int64),
         ("draft_mode", ctypes.c_int32),
         ("select_by_score", ctypes.c_int32),
+        ("num_backoff", ctypes.c_int32),
     ]
 
 

@@ -16,7 +16,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB_PATH = os.path.join(HERE, "libsgd.so")
-SOURCES = ["propose.cu", "corpus.cu", "sa_build.cu", "api.cu", "noalloc.cu"]
+SOURCES = ["propose.cu", "backoff.cu", "corpus.cu", "sa_build.cu", "api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

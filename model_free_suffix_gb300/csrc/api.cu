@@ -119,6 +119,7 @@ int validate(const sgd_config &c) {
   if (c.delta_capacity > 0 && c.corpus_capacity % WIN != 0) return SGD_EINVAL;
   if (c.draft_mode != 0 && c.draft_mode != 1) return SGD_EINVAL;
   if (c.select_by_score != 0 && c.select_by_score != 1) return SGD_EINVAL;
+  if (c.num_backoff < 1 || c.num_backoff > MAX_BACKOFF) return SGD_EINVAL;
   return SGD_OK;
 }
 
@@ -287,6 +288,7 @@ int sgd_config_default(sgd_config *c) {
   c->delta_capacity = 0;
   c->draft_mode = 0;
   c->select_by_score = 0;
+  c->num_backoff = 1;
   c->self_warps = 0;
   return SGD_OK;
 }
@@ -465,6 +467,7 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.split = x->split;
   a.self_res = x->d_self_res;
   a.by_score = c.select_by_score;
+  a.nb = c.num_backoff;
   if (c.draft_mode == 1) {  // no probability floor: the vote runs while an occurrence continues
     a.fixed = 1;
     a.pN = 0;
@@ -514,6 +517,17 @@ static int propose_impl(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, con
   a.score = score;
   a.probs = probs;
   a.match_info = match_info;
+  if (a.nb > 1) {  // multi-length backoff: the update, then the backoff kernel
+    if (a.do_update) {
+      x->launches++;
+      const int r = check_cuda(launch_update(token_ids, num_tokens, sampled, B, T,
+                                             x->cfg.seq_capacity, x->cfg.vocab_size, x->d_err,
+                                             (cudaStream_t)stream));
+      if (r != SGD_OK) return r;
+    }
+    x->launches++;
+    return check_cuda(launch_backoff(a, (cudaStream_t)stream));
+  }
   x->launches++;
   return check_cuda(launch_propose(a, (cudaStream_t)stream));
 }
@@ -545,7 +559,7 @@ int sgd_step(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int32_t 
   // (two launches for the long-row mode with a delta: its second kernel must
   // not append to the ring while its rows read delta continuations)
   if (n_docs == 0 || n_docs > propose_step_max_docs() || B == 0 ||
-      (x->split && x->cfg.delta_capacity > 0)) {
+      (x->split && x->cfg.delta_capacity > 0) || x->cfg.num_backoff > 1) {
     int r = sgd_propose_with_update(x, token_ids, num_tokens, sampled, T, active, B, drafts,
                                     num_valid, score, probs, match_info, stream);
     if (r != SGD_OK || n_docs == 0) return r;

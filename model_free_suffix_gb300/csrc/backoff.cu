@@ -1,0 +1,494 @@
+// backoff.cu -- multi-length backoff: every row drafts from several candidate
+// match lengths per path and the best-scored candidate wins.
+//
+// Sources (page title, section):
+//   "SuffixGPU" (suffix-gpu 0.1.1, PyPI): Highlights ("Multi-length backoff
+//     matching": the longest suffix plus shorter, better-supported lengths);
+//     How it works, step 1 (for support threshold t, the largest length
+//     occurring at least t times: the t-th largest match_back value), step 2
+//     (the corpus side: the suffix-array interval of the tail plus a
+//     brute-force scan of the not-yet-indexed delta, serving every length),
+//     step 3 (each candidate expanded by majority vote and scored; the best
+//     wins per path and the two winners compete by the same score).
+//
+// One CTA of 256 threads per row.  Match lengths are exact: every end of the
+// row is measured against the tail, and so is every end of the corpus that
+// can match >= 2 tokens -- the hits of the suffix-array interval of the last
+// two tokens, and every position of the delta.  A histogram of the lengths
+// gives the candidate lengths (thresholds 1..nb); one more pass per path
+// collects, for each candidate, its R most recent ends (the row's and the
+// delta's by a backward scan, the snapshot's by a radix selection on the end
+// position over the interval's hits).  Each warp then votes one candidate,
+// and thread 0 picks the winner with exact integer comparisons.
+#include <climits>
+
+#include "sgd_internal.h"
+
+namespace sgd {
+
+namespace {
+
+constexpr int BO_THREADS = 256;
+constexpr int BO_WARPS = BO_THREADS / 32;
+constexpr int BO_CANDS = 2 * MAX_BACKOFF;  // row candidates, then corpus candidates
+constexpr int BO_LCACHE = 8192;            // interval hits whose length is kept on chip
+
+struct BoShared {
+  int tail[MAX_D];
+  int hs[MAX_D + 1];  // row ends by match length
+  int hc[MAX_D + 1];  // corpus ends (snapshot and delta) by match length
+  int hd[MAX_D + 1];  // delta ends by match length
+  int len[BO_CANDS];  // candidate lengths (row: [0, ns), corpus: [MAX_BACKOFF, MAX_BACKOFF + nc))
+  int tot[BO_CANDS];  // ends reaching each length
+  int dtot[BO_CANDS]; // delta ends reaching each length
+  int cnt[BO_CANDS];  // ends collected
+  int occ[BO_CANDS][MAX_R];  // row: position; corpus: snapshot end e >= 0, delta end u as -(u + 1)
+  unsigned wb[MAX_BACKOFF][BO_WARPS];  // per-warp ballots of one chunk
+  int hist[MAX_BACKOFF][256];          // radix selection
+  long long pref[MAX_BACKOFF];
+  int need[MAX_BACKOFF];
+  int mode[MAX_BACKOFF];               // snapshot ends: 0 none, 1 every qualifying end, 2 the need most recent
+  unsigned char lc[BO_LCACHE];         // interval hit lengths (0: no continuation)
+  int vv[BO_WARPS][MAX_R];             // per-warp vote scratch
+  int dtok[BO_CANDS][MAX_K];           // each candidate's voted tokens
+  int dcnt[BO_CANDS][MAX_K];           // and their vote counts
+  int dlen[BO_CANDS];
+  long long dsum[BO_CANDS];
+  long long lo, hi, ds;
+  int n, dv, ns, nc, stop, win;
+};
+
+struct BoRow {
+  const int32_t *row;  // the row's tokens
+  int n, dl;           // tokens; min(D, n)
+  const int32_t *X;    // snapshot text (null: none)
+  const int32_t *SA;
+  const int4 *K;
+  long long N;
+  const int32_t *ring;  // the delta: Y[i] = ring[(ds + i) mod C], i < dv
+  long long C, ds;
+  int dv, Z;
+  const int *tail;
+};
+
+__device__ __forceinline__ int y_at(const BoRow &r, long long i) {
+  return __ldg(r.ring + (r.ds + i) % r.C);
+}
+
+// Row end j (j <= n-2): the longest l <= min(D, j+1) with t[j-i] == t[n-1-i], i < l.
+__device__ __forceinline__ int self_len(const BoRow &r, int j) {
+  const int lim = min(r.dl, j + 1);
+  int l = 0;
+  while (l < lim && __ldg(r.row + j - l) == r.tail[l]) ++l;
+  return l;
+}
+
+// Snapshot end e known to match two tokens, extended (0 without a continuation).
+__device__ __forceinline__ int snap_len(const BoRow &r, long long e) {
+  if (e + 1 >= r.N || __ldg(r.X + e + 1) == r.Z) return 0;
+  const long long lim = min((long long)r.dl, e + 1);
+  int l = 2;
+  while (l < lim && __ldg(r.X + e - l) == r.tail[l]) ++l;
+  return l;
+}
+
+// Delta end u (u <= dv-2): 0 without a continuation, else its match length
+// within the delta (its first token follows the snapshot's final sentinel).
+__device__ __forceinline__ int delta_len(const BoRow &r, long long u) {
+  if (y_at(r, u + 1) == r.Z) return 0;
+  const long long lim = min((long long)r.dl, u + 1);
+  int l = 0;
+  while (l < lim && y_at(r, u - l) == r.tail[l]) ++l;
+  return l;
+}
+
+// First suffix-array index whose key's first two tokens are >= (upper: >) P,
+// by one warp: 32 probes inside the bracket per round, monotone predicate.
+__device__ long long pair_bound(const int4 *K, long long N, int p0, int p1, bool upper, int lane) {
+  long long lo = 0, hi = N;  // the answer lies in [lo, hi]
+  while (hi > lo) {
+    const long long span = hi - lo;
+    const bool dense = span <= 32;
+    const long long q = dense ? lo + lane : lo + (long long)(lane + 1) * span / 33;
+    bool ok = !dense || q < hi;
+    bool pred = true;
+    if (ok) {
+      const int4 k = __ldg(K + q);
+      const int c = k.x != p0 ? (k.x < p0 ? -1 : 1) : (k.y != p1 ? (k.y < p1 ? -1 : 1) : 0);
+      pred = upper ? c > 0 : c >= 0;
+    }
+    const unsigned below = __ballot_sync(FULL, ok && !pred);  // a prefix of the lanes
+    const int f = __popc(below);
+    if (dense) return lo + f;
+    const long long qlo = __shfl_sync(FULL, q, f > 0 ? f - 1 : 0);
+    const long long qhi = __shfl_sync(FULL, q, f < 32 ? f : 31);
+    if (f > 0) lo = qlo + 1;
+    if (f < 32) hi = qhi;
+  }
+  return lo;
+}
+
+// min(k, floor(factor * M) + offset, S - n - 1) [, D - M]; Model Runner V2
+// drafts: k and the context only.
+__device__ __forceinline__ int bo_cap(const ProposeArgs &a, int M, int n) {
+  long long c = a.fixed ? (long long)a.k : min((long long)a.k, a.fN * M / a.fD + a.offset);
+  long long room = (long long)a.S - n - 1;
+  if (room < 0) room = 0;
+  c = min(c, room);
+  if (a.depth_sum_cap && !a.fixed) c = min(c, (long long)a.D - M);
+  return c < 0 ? 0 : (int)c;
+}
+
+// The distinct lengths covering thresholds 1..nb from a length histogram.
+__device__ int pick_lengths(const int *h, int top, int minlen, int nb, int *len, int *tot) {
+  int c = 0, cum = 0;
+  for (int m = top; m >= minlen && cum < nb; --m) {
+    if (h[m] == 0) continue;
+    cum += h[m];
+    len[c] = m;
+    tot[c] = cum;
+    ++c;
+  }
+  return c;
+}
+
+// Continuation token of end o at depth d (-1: none).  src 1: the row; src 2:
+// the corpus (o >= 0 a snapshot end, o < 0 the delta end -(o + 1)).
+__device__ __forceinline__ int bo_cont(const BoRow &r, int src, int o, int d) {
+  if (src == 1) {
+    const int q = o + 1 + d;
+    return q <= r.n - 1 ? __ldg(r.row + q) : -1;
+  }
+  if (o >= 0) {
+    const long long q = (long long)o + 1 + d;
+    if (q >= r.N) return -1;
+    const int v = __ldg(r.X + q);
+    return v == r.Z ? -1 : v;
+  }
+  const long long q = (long long)(-(o + 1)) + 1 + d;
+  if (q >= r.dv) return -1;
+  const int v = y_at(r, q);
+  return v == r.Z ? -1 : v;
+}
+
+// Frequency-greedy expansion of candidate ci by one warp: at each depth the
+// most frequent continuation among the surviving ends (ties: the smallest
+// id), kept while its share of the c0 ends reaches min_token_prob (Model
+// Runner V2 drafts: while any end continues), up to the candidate's cap.
+__device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int ci, int src, int warp,
+                        int lane) {
+  const int c0 = s.cnt[ci], M = s.len[ci];
+  const int cap = bo_cap(a, M, r.n);
+  int *vv = s.vv[warp];
+  bool alive[MAX_R / 32];
+  int v[MAX_R / 32];
+#pragma unroll
+  for (int u = 0; u < MAX_R / 32; ++u) alive[u] = lane + 32 * u < c0;
+  int len = 0;
+  long long sum = 0;
+  for (int d = 0; d < cap; ++d) {
+    bool any = false;
+#pragma unroll
+    for (int u = 0; u < MAX_R / 32; ++u) {
+      const int i = lane + 32 * u;
+      v[u] = -1;
+      if (alive[u]) v[u] = bo_cont(r, src, s.occ[ci][i], d);
+      if (i < c0) vv[i] = v[u];
+      any |= v[u] >= 0;
+    }
+    __syncwarp();
+    if (!__any_sync(FULL, any)) break;
+    int best = 0, cu[MAX_R / 32];
+#pragma unroll
+    for (int u = 0; u < MAX_R / 32; ++u) {
+      cu[u] = 0;
+      if (v[u] < 0) continue;
+      for (int i = 0; i < c0; ++i) cu[u] += vv[i] == v[u];
+      best = max(best, cu[u]);
+    }
+    const int bc = (int)__reduce_max_sync(FULL, (unsigned)best);
+    unsigned mine = UINT_MAX;
+#pragma unroll
+    for (int u = 0; u < MAX_R / 32; ++u)
+      if (v[u] >= 0 && cu[u] == bc) mine = min(mine, (unsigned)v[u]);
+    const int bt = (int)__reduce_min_sync(FULL, mine);
+    __syncwarp();  // every lane done reading vv before the next depth writes it
+    if (!a.fixed && (long long)bc * a.pD < a.pN * (long long)c0) break;
+    if (lane == 0) {
+      s.dtok[ci][d] = bt;
+      s.dcnt[ci][d] = bc;
+    }
+    sum += bc;
+    ++len;
+#pragma unroll
+    for (int u = 0; u < MAX_R / 32; ++u) alive[u] = v[u] == bt;
+  }
+  if (lane == 0) {
+    s.dlen[ci] = len;
+    s.dsum[ci] = sum;
+  }
+}
+
+// One chunk of a backward scan: thread tid holds end `val` with length l
+// (ends in descending recency by tid).  Each candidate c < ncand of list
+// `off` (length s.len[off + c]) appends the chunk's ends reaching its length,
+// in order, up to R; s.stop is set once every list holds min(R, target[c]).
+__device__ void bo_collect(BoShared &s, int off, int ncand, const int *target, int l, int val, int R,
+                           int tid, int warp, int lane) {
+  for (int c = 0; c < ncand; ++c) {
+    const unsigned bal = __ballot_sync(FULL, l >= s.len[off + c]);
+    if (lane == 0) s.wb[c][warp] = bal;
+  }
+  __syncthreads();
+  for (int c = 0; c < ncand; ++c) {
+    if (l < s.len[off + c]) continue;
+    int rank = __popc(s.wb[c][warp] & ((1u << lane) - 1u));
+    for (int w = 0; w < warp; ++w) rank += __popc(s.wb[c][w]);
+    const int slot = s.cnt[off + c] + rank;
+    if (slot < R) s.occ[off + c][slot] = val;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    bool full = true;
+    for (int c = 0; c < ncand; ++c) {
+      int t = 0;
+      for (int w = 0; w < BO_WARPS; ++w) t += __popc(s.wb[c][w]);
+      s.cnt[off + c] = min(R, s.cnt[off + c] + t);
+      full &= s.cnt[off + c] >= min(R, target[c]);
+    }
+    s.stop = full;
+  }
+  __syncthreads();
+}
+
+__global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a) {
+  __shared__ BoShared s;
+  const int b = blockIdx.x;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int S = a.S, D = a.D, R = a.R, k = a.k, nb = a.nb;
+  const int32_t *row = a.tok + (size_t)b * S;
+  const CorpusDesc *cd = a.desc;
+  if (tid == 0) {
+    int n = a.ntok[b];
+    uint32_t fl = 0;
+    if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
+    if (n > S) { n = S; fl |= SGD_ERR_NUM_TOKENS; }
+    if (fl) atomicOr(a.err, fl);
+    s.n = n;
+    s.ds = 0;
+    s.dv = 0;
+    if (a.dcap > 0 && cd != nullptr) {  // the docs placed since the snapshot was linearised
+      const DeltaView v = delta_view(*a.rs, cd->lin_pushed, cd->lin_wp, a.C, a.doc_start);
+      s.ds = v.start;
+      s.dv = (int)min(v.len, a.dcap);
+    }
+    s.lo = 0;
+    s.hi = 0;
+    s.stop = 0;
+    s.win = -1;
+  }
+  for (int i = tid; i <= MAX_D; i += BO_THREADS) {
+    s.hs[i] = 0;
+    s.hc[i] = 0;
+    s.hd[i] = 0;
+  }
+  __syncthreads();
+  const int n = s.n;
+  int32_t *dr = a.drafts + (size_t)b * k;
+  float *pr = a.probs ? a.probs + (size_t)b * k : nullptr;
+  if (!((a.active == nullptr || a.active[b] != 0) && n > 0)) {
+    for (int d = tid; d < k; d += BO_THREADS) {
+      dr[d] = -1;
+      if (pr) pr[d] = 0.f;
+    }
+    if (tid == 0) {
+      a.num_valid[b] = 0;
+      if (a.score) a.score[b] = 0.f;
+      if (a.match_info) { a.match_info[2 * b] = 0; a.match_info[2 * b + 1] = 0; }
+    }
+    return;
+  }
+  const int dl = min(D, n);
+  for (int i = tid; i < dl; i += BO_THREADS) s.tail[i] = __ldg(row + n - 1 - i);
+  BoRow r;
+  r.row = row;
+  r.n = n;
+  r.dl = dl;
+  r.X = cd != nullptr ? cd->text : nullptr;
+  r.SA = cd != nullptr ? cd->sa : nullptr;
+  r.K = cd != nullptr ? cd->keys : nullptr;
+  r.N = cd != nullptr ? cd->n : 0;
+  r.ring = a.ring;
+  r.C = a.C;
+  r.ds = s.ds;
+  r.dv = s.dv;
+  r.Z = a.V;
+  r.tail = s.tail;
+  const bool snap = r.N >= 2 && n >= 2 && D >= 2;
+  const bool delta = r.dv >= 2 && n >= 2 && D >= 2;
+  __syncthreads();
+
+  // ---- match lengths: the row's ends, the interval of the last two tokens, the delta ----
+  if (snap && warp < 2) {
+    const long long q = pair_bound(r.K, r.N, s.tail[1], s.tail[0], warp == 1, lane);
+    if (lane == 0) (warp == 0 ? s.lo : s.hi) = q;
+  }
+  for (int j = tid; j <= n - 2; j += BO_THREADS) {
+    const int l = self_len(r, j);
+    if (l > 0) atomicAdd(&s.hs[l], 1);
+  }
+  if (delta)
+    for (int u = tid; u <= r.dv - 2; u += BO_THREADS) {
+      const int l = delta_len(r, u);
+      if (l >= 2) {
+        atomicAdd(&s.hc[l], 1);
+        atomicAdd(&s.hd[l], 1);
+      }
+    }
+  __syncthreads();
+  const long long lo = s.lo, hi = s.hi;
+  for (long long p = lo + tid; p < hi; p += BO_THREADS) {
+    const int l = snap_len(r, (long long)__ldg(r.SA + p) + 1);
+    if (p - lo < BO_LCACHE) s.lc[p - lo] = (unsigned char)l;
+    if (l > 0) atomicAdd(&s.hc[l], 1);
+  }
+  __syncthreads();
+
+  // ---- candidate lengths: thresholds 1..nb of each path ----
+  if (tid == 0) {
+    s.ns = pick_lengths(s.hs, dl, 1, nb, s.len, s.tot);
+    s.nc = pick_lengths(s.hc, dl, 2, nb, s.len + MAX_BACKOFF, s.tot + MAX_BACKOFF);
+    for (int c = 0; c < BO_CANDS; ++c) s.cnt[c] = 0;
+    for (int c = 0; c < s.nc; ++c) {
+      int t = 0;
+      for (int m = s.len[MAX_BACKOFF + c]; m <= dl; ++m) t += s.hd[m];
+      s.dtot[MAX_BACKOFF + c] = t;
+    }
+    s.stop = 0;
+  }
+  __syncthreads();
+  const int ns = s.ns, nc = s.nc;
+
+  // ---- the row's candidates: their R most recent ends, by a backward scan ----
+  if (ns > 0)
+    for (int base = n - 2; base >= 0; base -= BO_THREADS) {
+      const int j = base - tid;
+      bo_collect(s, 0, ns, s.tot, j >= 0 ? self_len(r, j) : 0, j, R, tid, warp, lane);
+      if (s.stop) break;
+    }
+  // ---- the corpus's: the delta's ends first (the most recent), then the snapshot's ----
+  if (nc > 0 && delta) {
+    if (tid == 0) {
+      bool none = true;
+      for (int c = 0; c < nc; ++c) none &= s.dtot[MAX_BACKOFF + c] == 0;
+      s.stop = none;
+    }
+    __syncthreads();
+    if (!s.stop)
+      for (long long base = r.dv - 2; base >= 0; base -= BO_THREADS) {
+        const long long u = base - tid;
+        bo_collect(s, MAX_BACKOFF, nc, s.dtot + MAX_BACKOFF, u >= 0 ? delta_len(r, u) : 0,
+                   (int)(-(u + 1)), R, tid, warp, lane);
+        if (s.stop) break;
+      }
+  }
+  if (nc > 0 && snap && hi > lo) {
+    if (tid < nc) {
+      const int c = MAX_BACKOFF + tid;
+      const int room = R - s.cnt[c], xq = s.tot[c] - s.dtot[c];
+      s.mode[tid] = room <= 0 || xq <= 0 ? 0 : (xq <= room ? 1 : 2);
+      s.need[tid] = min(room, xq);
+      s.pref[tid] = 0;
+    }
+    __syncthreads();
+    bool radix = false;
+    for (int c = 0; c < nc; ++c) radix |= s.mode[c] == 2;
+    if (radix) {  // the need most recent qualifying ends: MSB-first radix selection on e
+      const int nbits = 64 - __clzll(r.N - 1);
+      for (int sh = ((nbits + 7) / 8 - 1) * 8; sh >= 0; sh -= 8) {
+        for (int i = tid; i < nc * 256; i += BO_THREADS) s.hist[i >> 8][i & 255] = 0;
+        __syncthreads();
+        for (long long p = lo + tid; p < hi; p += BO_THREADS) {
+          const long long e = (long long)__ldg(r.SA + p) + 1;
+          const int l = p - lo < BO_LCACHE ? s.lc[p - lo] : snap_len(r, e);
+          for (int c = 0; c < nc; ++c)
+            if (s.mode[c] == 2 && l >= s.len[MAX_BACKOFF + c] && (e >> (sh + 8)) == (s.pref[c] >> (sh + 8)))
+              atomicAdd(&s.hist[c][(e >> sh) & 255], 1);
+        }
+        __syncthreads();
+        if (tid < nc && s.mode[tid] == 2) {
+          int cum = 0;
+          for (int d = 255; d >= 0; --d) {
+            const int h = s.hist[tid][d];
+            if (cum + h >= s.need[tid]) {
+              s.pref[tid] |= (long long)d << sh;
+              s.need[tid] -= cum;
+              break;
+            }
+            cum += h;
+          }
+        }
+        __syncthreads();
+      }
+    }
+    for (long long p = lo + tid; p < hi; p += BO_THREADS) {
+      const long long e = (long long)__ldg(r.SA + p) + 1;
+      const int l = p - lo < BO_LCACHE ? s.lc[p - lo] : snap_len(r, e);
+      for (int c = 0; c < nc; ++c) {
+        const int m = s.mode[c];
+        if (m == 0 || l < s.len[MAX_BACKOFF + c] || (m == 2 && e < s.pref[c])) continue;
+        const int slot = atomicAdd(&s.cnt[MAX_BACKOFF + c], 1);
+        if (slot < R) s.occ[MAX_BACKOFF + c][slot] = (int)e;
+      }
+    }
+    __syncthreads();
+    if (tid < nc) s.cnt[MAX_BACKOFF + tid] = min(R, s.cnt[MAX_BACKOFF + tid]);  // (exactly room or fewer)
+    __syncthreads();
+  }
+
+  // ---- every candidate voted (one warp each), the best score wins ----
+  for (int q = warp; q < ns + nc; q += BO_WARPS) {
+    const int ci = q < ns ? q : MAX_BACKOFF + (q - ns);
+    bo_vote(a, r, s, ci, q < ns ? 1 : 2, warp, lane);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int w = -1;
+    for (int q = 0; q < ns + nc; ++q) {  // the row's first, longest first
+      const int ci = q < ns ? q : MAX_BACKOFF + (q - ns);
+      if (w < 0) {
+        w = ci;
+        continue;
+      }
+      const long long lhs = s.dsum[ci] * s.cnt[w], rhs = s.dsum[w] * s.cnt[ci];
+      if (lhs > rhs || (lhs == rhs && s.len[ci] > s.len[w])) w = ci;
+    }
+    s.win = w;
+  }
+  __syncthreads();
+  const int w = s.win;
+  const int len = w >= 0 ? s.dlen[w] : 0;
+  const int fill = a.fixed ? s.tail[0] : -1;
+  for (int d = tid; d < k; d += BO_THREADS) {
+    dr[d] = d < len ? s.dtok[w][d] : fill;
+    if (pr) pr[d] = d < len ? (float)((double)s.dcnt[w][d] / (double)s.cnt[w]) : 0.f;
+  }
+  if (tid == 0) {
+    a.num_valid[b] = a.fixed ? k : len;
+    if (a.score) a.score[b] = w >= 0 ? (float)((double)s.dsum[w] / (double)s.cnt[w]) : 0.f;
+    if (a.match_info) {
+      a.match_info[2 * b] = w >= 0 ? s.len[w] : 0;
+      a.match_info[2 * b + 1] = w < 0 ? 0 : (w < MAX_BACKOFF ? 1 : 2);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_backoff(const ProposeArgs &a, cudaStream_t st) {
+  if (a.B <= 0) return cudaSuccess;
+  backoff_kernel<<<a.B, BO_THREADS, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace sgd

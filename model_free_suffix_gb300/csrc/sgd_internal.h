@@ -14,6 +14,7 @@ constexpr int MAX_D = 128;      // the halo of one window covers D - 1 <= 127
 constexpr int MAX_R = 128;      // up to 4 occurrences per lane in the vote warp
 constexpr int MAX_K = 64;
 constexpr int MAX_SELF_WARPS = 16;
+constexpr int MAX_BACKOFF = 8;      // candidate lengths per path
 constexpr int MAX_PROPOSE_THREADS = 640;
 
 // Descriptor of the suffix-array snapshot drafting reads.  It lives in device
@@ -158,6 +159,8 @@ struct ProposeArgs {
   // score-ranked selection: the row's and the corpus's candidates are both
   // voted and the better score wins (ties: the longer match, then the row)
   int by_score;
+  // multi-length backoff: candidate lengths per path (> 1: backoff.cu)
+  int nb;
 };
 
 __host__ __device__ constexpr int self_res_ints(int R) { return 2 * R + 10; }
@@ -169,6 +172,10 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st);
 cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, int B,
                           int T, int S, int V, uint32_t *err, cudaStream_t st);
 cudaError_t propose_set_smem_limit(size_t bytes);
+
+// backoff.cu: multi-length backoff drafting of rows [0, B), one CTA per row
+// (no update: the caller launches it first)
+cudaError_t launch_backoff(const ProposeArgs &a, cudaStream_t st);
 
 // corpus.cu
 struct IngestScratch {

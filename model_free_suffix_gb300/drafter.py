@@ -58,7 +58,8 @@ class SuffixDrafter:
                  corpus_capacity: int = 0, max_docs: int = 65536, max_ingest_docs: int = 4096,
                  corpus_cand_cap: int = 2048, self_warps: int = 0, corpus_records: int = 1,
                  corpus_gram_index: int = 1, propose_mode: int = 0, delta_capacity: int = 0,
-                 draft_mode: int = 0, select_by_score: int = 0, device: int = 0):
+                 draft_mode: int = 0, select_by_score: int = 0, num_backoff: int = 1,
+                 device: int = 0):
         self._lib = L.load()
         cfg = L.SgdConfig()
         self._check(self._lib.sgd_config_default(ctypes.byref(cfg)), "sgd_config_default")
@@ -84,6 +85,7 @@ class SuffixDrafter:
         cfg.delta_capacity = delta_capacity
         cfg.draft_mode = draft_mode
         cfg.select_by_score = select_by_score
+        cfg.num_backoff = num_backoff
         self.cfg = cfg
         self.device = torch.device("cuda", device)
         torch.cuda.init()

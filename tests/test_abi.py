@@ -33,6 +33,7 @@ def test_config_defaults(lib):
     assert c.corpus_capacity == 1 << 20
     assert c.delta_capacity == 0  # newly ingested docs wait for the next swap
     assert c.draft_mode == 0      # drafts stop at the probability floor and the factor cap
+    assert c.num_backoff == 1     # one candidate length per path: the longest match
 
 
 def test_config_set_float_rationals(lib):
@@ -63,7 +64,7 @@ def test_create_rejects_bad_knobs_before_touching_the_gpu(lib):
     bad = [("seq_capacity", 4098), ("k", 0), ("k", 65), ("max_tree_depth", 129),
            ("max_occurrences", 0), ("corpus_cand_cap", 100), ("corpus_cand_cap", 32),
            ("min_prob_den", 0), ("self_warps", 17), ("draft_mode", 2), ("draft_mode", -1),
-           ("select_by_score", 2)]
+           ("select_by_score", 2), ("num_backoff", 0), ("num_backoff", 9)]
     for field, val in bad:
         c = lib.SgdConfig()
         L.sgd_config_default(ctypes.byref(c))
