@@ -145,10 +145,11 @@ def workload_config(cfg, world):
             "parallelism": "replicas" if world > 1 else "single"}
 
 
-def run_ours(args, rank, world, delta=0):
+def run_ours(args, rank, world, delta=0, backoff=1):
     """The serving loop.  delta > 0: the same loop with the docs ingested since
     the current snapshot also matched (brute-force scan of up to `delta`
-    tokens), timed as a secondary line (no end-to-end or build legs)."""
+    tokens); backoff > 1: the same loop drafting with multi-length backoff.
+    Either is timed as a secondary line (no end-to-end or build legs)."""
     import torch
     from model_free_suffix_gb300 import SuffixDrafter
     from model_free_suffix_gb300 import workload as W
@@ -156,14 +157,16 @@ def run_ours(args, rank, world, delta=0):
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
     cfg = W.CONFIGS[args.config]
-    K, Wm = (args.delta_steps if delta else args.steps), args.warmup
-    K_e2e = 0 if delta else min(K, args.e2e_steps)
+    secondary = bool(delta) or backoff > 1
+    K = args.delta_steps if delta else (args.backoff_steps if backoff > 1 else args.steps)
+    Wm = args.warmup
+    K_e2e = 0 if secondary else min(K, args.e2e_steps)
     tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=Wm + K + K_e2e)
     dr = SuffixDrafter(max_batch=cfg.B, seq_capacity=cfg.S, vocab_size=cfg.V, k=cfg.k,
                        max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
                        max_spec_factor=cfg.factor, max_spec_offset=cfg.offset,
                        min_token_prob=cfg.min_prob, corpus_capacity=cfg.corpus_tokens,
-                       delta_capacity=delta, device=dev.index)
+                       delta_capacity=delta, num_backoff=backoff, device=dev.index)
     # drafting at the device's highest stream priority, snapshot builds at the lowest
     least, greatest = torch.cuda.Stream.priority_range()
     stream = torch.cuda.Stream(device=dev, priority=greatest)
@@ -297,6 +300,32 @@ def run_ours(args, rank, world, delta=0):
     builds_in_region = state["builds"] - b0
     region_builds = state["build_stats"][nb0:]
     n_sum = int(g_n.sum().item())
+    if backoff > 1:
+        peak, peak_kind = peaks()
+        ing_tok = float(np.mean([fin[Wm + j][3] for j in range(K)])) if fused else 0.0
+        byts = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens, ing_tok)
+        prop_avg_s = float(np.mean(prop_ms)) / 1e3
+        ach = byts / prop_avg_s / 1e9
+        if state["pending"]:
+            dr.poll(wait=True, stream=stream)
+        dr.close()
+        return {"workload": "the serving loop above with num_backoff=%d: for support thresholds "
+                            "1..%d the t-th largest match length of each path is a candidate, "
+                            "every candidate voted, the best score wins (the update, the "
+                            "backoff kernel and the ingest as separate launches in the graph)"
+                            % (backoff, backoff),
+                "num_backoff": backoff, "steps": K,
+                "us_per_step": round(1e3 * total_ms_max / K, 2),
+                "steps_per_s": round(world * K / (total_ms_max / 1e3), 2),
+                "graph_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
+                             "median": round(1e3 * float(np.median(prop_ms)), 2),
+                             "p90": round(1e3 * float(np.percentile(prop_ms, 90)), 2)},
+                "roofline": {"bound": "hbm", "kernel": "backoff_kernel (with the update and ingest "
+                                                     "launches of the step)",
+                             "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
+                             "frac": round(ach / peak, 4), "bytes_per_launch": int(byts),
+                             "peak_kind": peak_kind},
+                "builds_in_timed_region": builds_in_region, "clocks": clocks}
     if delta:
         peak, peak_kind = peaks()
         ing_tok = float(np.mean([fin[Wm + j][3] for j in range(K)])) if fused else 0.0
@@ -619,6 +648,8 @@ def main():
                     help="steps of the long-context workload timed as a secondary line (0: skip)")
     ap.add_argument("--sa-only", type=int, default=0,
                     help="only time suffix-array builds of this many tokens and print them")
+    ap.add_argument("--backoff-steps", type=int, default=64,
+                    help="steps of the serving loop with num_backoff=8, a secondary line (0: skip)")
     ap.add_argument("--delta-steps", type=int, default=256,
                     help="steps of the serving loop with the delta scan on, a secondary line (0: skip)")
     ap.add_argument("--long-only", action="store_true",
@@ -666,6 +697,8 @@ def main():
     res = run_ours(args, rank, world)
     if args.delta_steps > 0 and args.config == "c3":
         res["delta"] = run_ours(args, rank, world, delta=cfg.rebuild_tokens)
+    if args.backoff_steps > 0 and args.config == "c3":
+        res["backoff"] = run_ours(args, rank, world, backoff=8)
     if args.long_context_steps > 0 and args.config == "c3":
         res["long_context"] = long_context_leg(args, rank)
     if rank == 0:

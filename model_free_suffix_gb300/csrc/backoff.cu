@@ -28,10 +28,10 @@ namespace sgd {
 
 namespace {
 
-constexpr int BO_THREADS = 256;
+constexpr int BO_THREADS = 512;
 constexpr int BO_WARPS = BO_THREADS / 32;
 constexpr int BO_CANDS = 2 * MAX_BACKOFF;  // row candidates, then corpus candidates
-constexpr int BO_LCACHE = 8192;            // interval hits whose length is kept on chip
+constexpr int BO_LCACHE = 16384;           // interval hits whose length is kept on chip
 
 struct BoShared {
   int tail[MAX_D];
@@ -48,8 +48,10 @@ struct BoShared {
   long long pref[MAX_BACKOFF];
   int need[MAX_BACKOFF];
   int mode[MAX_BACKOFF];               // snapshot ends: 0 none, 1 every qualifying end, 2 the need most recent
-  unsigned char lc[BO_LCACHE];         // interval hit lengths (0: no continuation)
-  int vv[BO_WARPS][MAX_R];             // per-warp vote scratch
+  union {
+    unsigned char lc[BO_LCACHE];       // interval hit lengths (0: no continuation), until the votes
+    int vv[BO_WARPS][MAX_R];           // per-warp vote scratch
+  } u;
   int dtok[BO_CANDS][MAX_K];           // each candidate's voted tokens
   int dcnt[BO_CANDS][MAX_K];           // and their vote counts
   int dlen[BO_CANDS];
@@ -90,6 +92,44 @@ __device__ __forceinline__ int snap_len(const BoRow &r, long long e) {
   int l = 2;
   while (l < lim && __ldg(r.X + e - l) == r.tail[l]) ++l;
   return l;
+}
+
+// The lengths of interval hits p0 + j * BO_THREADS (j < 4; l[j] = -1 past hi),
+// their loads issued together: the key gives the continuation X[e+1] (its
+// third token; KEY_END past the text), then the token before the pair for
+// the valid hits; the rare longer matches are extended one token at a time.
+__device__ __forceinline__ void hit_lens(const BoRow &r, long long p0, long long hi, int l[4],
+                                         long long e[4]) {
+  int4 kk[4];
+  int ii[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const long long p = p0 + (long long)j * BO_THREADS;
+    kk[j] = make_int4(0, 0, KEY_END, 0);
+    ii[j] = 0;
+    if (p < hi) {
+      kk[j] = __ldg(r.K + p);
+      ii[j] = __ldg(r.SA + p);
+    }
+  }
+  int xb[4];
+  bool three[4];
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool valid = kk[j].z != KEY_END && kk[j].z != r.Z;
+    three[j] = valid && r.dl >= 3 && ii[j] >= 1;
+    xb[j] = three[j] ? __ldg(r.X + ii[j] - 1) : 0;
+    e[j] = (long long)ii[j] + 1;
+    l[j] = p0 + (long long)j * BO_THREADS < hi ? (valid ? 2 : 0) : -1;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    if (three[j] && xb[j] == r.tail[2]) {
+      const long long lim = min((long long)r.dl, e[j] + 1);
+      int L = 3;
+      while (L < lim && __ldg(r.X + e[j] - L) == r.tail[L]) ++L;
+      l[j] = L;
+    }
 }
 
 // Delta end u (u <= dv-2): 0 without a continuation, else its match length
@@ -179,7 +219,7 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
                         int lane) {
   const int c0 = s.cnt[ci], M = s.len[ci];
   const int cap = bo_cap(a, M, r.n);
-  int *vv = s.vv[warp];
+  int *vv = s.u.vv[warp];
   bool alive[MAX_R / 32];
   int v[MAX_R / 32];
 #pragma unroll
@@ -333,24 +373,56 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     const long long q = pair_bound(r.K, r.N, s.tail[1], s.tail[0], warp == 1, lane);
     if (lane == 0) (warp == 0 ? s.lo : s.hi) = q;
   }
-  for (int j = tid; j <= n - 2; j += BO_THREADS) {
-    const int l = self_len(r, j);
-    if (l > 0) atomicAdd(&s.hs[l], 1);
+  for (int j0 = tid; j0 <= n - 2; j0 += 4 * BO_THREADS) {  // four ends' first tokens at once
+    int x[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q * BO_THREADS;
+      x[q] = j <= n - 2 ? __ldg(row + j) : -1;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      if (x[q] == s.tail[0]) {
+        const int l = self_len(r, j0 + q * BO_THREADS);
+        atomicAdd(&s.hs[l], 1);
+      }
   }
   if (delta)
-    for (int u = tid; u <= r.dv - 2; u += BO_THREADS) {
-      const int l = delta_len(r, u);
-      if (l >= 2) {
-        atomicAdd(&s.hc[l], 1);
-        atomicAdd(&s.hd[l], 1);
+    for (long long u0 = tid; u0 <= r.dv - 2; u0 += 4 * BO_THREADS) {
+      int x[4], c[4];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const long long u = u0 + (long long)q * BO_THREADS;
+        x[q] = -1;
+        c[q] = r.Z;
+        if (u <= r.dv - 2) {
+          x[q] = y_at(r, u);
+          c[q] = y_at(r, u + 1);
+        }
       }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (x[q] == s.tail[0] && c[q] != r.Z) {
+          const int l = delta_len(r, u0 + (long long)q * BO_THREADS);
+          if (l >= 2) {
+            atomicAdd(&s.hc[l], 1);
+            atomicAdd(&s.hd[l], 1);
+          }
+        }
     }
   __syncthreads();
   const long long lo = s.lo, hi = s.hi;
-  for (long long p = lo + tid; p < hi; p += BO_THREADS) {
-    const int l = snap_len(r, (long long)__ldg(r.SA + p) + 1);
-    if (p - lo < BO_LCACHE) s.lc[p - lo] = (unsigned char)l;
-    if (l > 0) atomicAdd(&s.hc[l], 1);
+  for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
+    int l[4];
+    long long e[4];
+    hit_lens(r, p0, hi, l, e);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const long long p = p0 + (long long)j * BO_THREADS;
+      if (l[j] < 0) continue;
+      if (p - lo < BO_LCACHE) s.u.lc[p - lo] = (unsigned char)l[j];
+      if (l[j] > 0) atomicAdd(&s.hc[l[j]], 1);
+    }
   }
   __syncthreads();
 
@@ -410,7 +482,7 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
         __syncthreads();
         for (long long p = lo + tid; p < hi; p += BO_THREADS) {
           const long long e = (long long)__ldg(r.SA + p) + 1;
-          const int l = p - lo < BO_LCACHE ? s.lc[p - lo] : snap_len(r, e);
+          const int l = p - lo < BO_LCACHE ? s.u.lc[p - lo] : snap_len(r, e);
           for (int c = 0; c < nc; ++c)
             if (s.mode[c] == 2 && l >= s.len[MAX_BACKOFF + c] && (e >> (sh + 8)) == (s.pref[c] >> (sh + 8)))
               atomicAdd(&s.hist[c][(e >> sh) & 255], 1);
@@ -433,7 +505,7 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     }
     for (long long p = lo + tid; p < hi; p += BO_THREADS) {
       const long long e = (long long)__ldg(r.SA + p) + 1;
-      const int l = p - lo < BO_LCACHE ? s.lc[p - lo] : snap_len(r, e);
+      const int l = p - lo < BO_LCACHE ? s.u.lc[p - lo] : snap_len(r, e);
       for (int c = 0; c < nc; ++c) {
         const int m = s.mode[c];
         if (m == 0 || l < s.len[MAX_BACKOFF + c] || (m == 2 && e < s.pref[c])) continue;
