@@ -226,13 +226,25 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
   for (int u = 0; u < MAX_R / 32; ++u) alive[u] = lane + 32 * u < c0;
   int len = 0;
   long long sum = 0;
+  int ahead[MAX_R / 32][4];  // continuation tokens of depths d0 .. d0+3, read together
   for (int d = 0; d < cap; ++d) {
+    if ((d & 3) == 0) {
+#pragma unroll
+      for (int u = 0; u < MAX_R / 32; ++u) {
+        const int o = alive[u] ? s.occ[ci][lane + 32 * u] : 0;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          ahead[u][q] = alive[u] && d + q < cap ? bo_cont(r, src, o, d + q) : -1;
+      }
+    }
     bool any = false;
 #pragma unroll
     for (int u = 0; u < MAX_R / 32; ++u) {
       const int i = lane + 32 * u;
       v[u] = -1;
-      if (alive[u]) v[u] = bo_cont(r, src, s.occ[ci][i], d);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if ((d & 3) == q && alive[u]) v[u] = ahead[u][q];
       if (i < c0) vv[i] = v[u];
       any |= v[u] >= 0;
     }
@@ -266,6 +278,23 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
   if (lane == 0) {
     s.dlen[ci] = len;
     s.dsum[ci] = sum;
+  }
+}
+
+// Ends and lengths of interval hits p0 + q * BO_THREADS (q < 4; l = -1 past
+// hi): the suffix-array entries read together, the lengths from the on-chip
+// cache, else evaluated again.
+__device__ __forceinline__ void hit_ends(const BoRow &r, const BoShared &s, long long lo, long long p0,
+                                         long long hi, long long e[4], int l[4]) {
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const long long p = p0 + (long long)q * BO_THREADS;
+    e[q] = p < hi ? (long long)__ldg(r.SA + p) + 1 : -1;
+  }
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    const long long p = p0 + (long long)q * BO_THREADS;
+    l[q] = p >= hi ? -1 : (p - lo < BO_LCACHE ? (int)s.u.lc[p - lo] : snap_len(r, e[q]));
   }
 }
 
@@ -480,12 +509,16 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
       for (int sh = ((nbits + 7) / 8 - 1) * 8; sh >= 0; sh -= 8) {
         for (int i = tid; i < nc * 256; i += BO_THREADS) s.hist[i >> 8][i & 255] = 0;
         __syncthreads();
-        for (long long p = lo + tid; p < hi; p += BO_THREADS) {
-          const long long e = (long long)__ldg(r.SA + p) + 1;
-          const int l = p - lo < BO_LCACHE ? s.u.lc[p - lo] : snap_len(r, e);
-          for (int c = 0; c < nc; ++c)
-            if (s.mode[c] == 2 && l >= s.len[MAX_BACKOFF + c] && (e >> (sh + 8)) == (s.pref[c] >> (sh + 8)))
-              atomicAdd(&s.hist[c][(e >> sh) & 255], 1);
+        for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
+          long long e[4];
+          int l[4];
+          hit_ends(r, s, lo, p0, hi, e, l);
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            for (int c = 0; c < nc; ++c)
+              if (s.mode[c] == 2 && l[q] >= s.len[MAX_BACKOFF + c] &&
+                  (e[q] >> (sh + 8)) == (s.pref[c] >> (sh + 8)))
+                atomicAdd(&s.hist[c][(e[q] >> sh) & 255], 1);
         }
         __syncthreads();
         if (tid < nc && s.mode[tid] == 2) {
@@ -503,15 +536,18 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
         __syncthreads();
       }
     }
-    for (long long p = lo + tid; p < hi; p += BO_THREADS) {
-      const long long e = (long long)__ldg(r.SA + p) + 1;
-      const int l = p - lo < BO_LCACHE ? s.u.lc[p - lo] : snap_len(r, e);
-      for (int c = 0; c < nc; ++c) {
-        const int m = s.mode[c];
-        if (m == 0 || l < s.len[MAX_BACKOFF + c] || (m == 2 && e < s.pref[c])) continue;
-        const int slot = atomicAdd(&s.cnt[MAX_BACKOFF + c], 1);
-        if (slot < R) s.occ[MAX_BACKOFF + c][slot] = (int)e;
-      }
+    for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
+      long long e[4];
+      int l[4];
+      hit_ends(r, s, lo, p0, hi, e, l);
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        for (int c = 0; c < nc; ++c) {
+          const int m = s.mode[c];
+          if (m == 0 || l[q] < s.len[MAX_BACKOFF + c] || (m == 2 && e[q] < s.pref[c])) continue;
+          const int slot = atomicAdd(&s.cnt[MAX_BACKOFF + c], 1);
+          if (slot < R) s.occ[MAX_BACKOFF + c][slot] = (int)e[q];
+        }
     }
     __syncthreads();
     if (tid < nc) s.cnt[MAX_BACKOFF + tid] = min(R, s.cnt[MAX_BACKOFF + tid]);  // (exactly room or fewer)
