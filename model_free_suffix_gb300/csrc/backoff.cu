@@ -32,6 +32,7 @@ constexpr int BO_THREADS = 512;
 constexpr int BO_WARPS = BO_THREADS / 32;
 constexpr int BO_CANDS = 2 * MAX_BACKOFF;  // row candidates, then corpus candidates
 constexpr int BO_LCACHE = 16384;           // interval hits whose length is kept on chip
+static_assert(BO_LCACHE % (4 * BO_THREADS) == 0, "hit_ends: four hits on one side of the cache end");
 
 struct BoShared {
   int tail[MAX_D];
@@ -82,15 +83,6 @@ __device__ __forceinline__ int self_len(const BoRow &r, int j) {
   const int lim = min(r.dl, j + 1);
   int l = 0;
   while (l < lim && __ldg(r.row + j - l) == r.tail[l]) ++l;
-  return l;
-}
-
-// Snapshot end e known to match two tokens, extended (0 without a continuation).
-__device__ __forceinline__ int snap_len(const BoRow &r, long long e) {
-  if (e + 1 >= r.N || __ldg(r.X + e + 1) == r.Z) return 0;
-  const long long lim = min((long long)r.dl, e + 1);
-  int l = 2;
-  while (l < lim && __ldg(r.X + e - l) == r.tail[l]) ++l;
   return l;
 }
 
@@ -282,10 +274,16 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
 }
 
 // Ends and lengths of interval hits p0 + q * BO_THREADS (q < 4; l = -1 past
-// hi): the suffix-array entries read together, the lengths from the on-chip
-// cache, else evaluated again.
+// hi): the suffix-array entries read together and the lengths from the
+// on-chip cache, or beyond it both evaluated again as in the first pass (the
+// four hits of a call lie on one side of the cache's end: p0 - lo is
+// tid + a multiple of 4 * BO_THREADS, and the cache size is a multiple of it).
 __device__ __forceinline__ void hit_ends(const BoRow &r, const BoShared &s, long long lo, long long p0,
                                          long long hi, long long e[4], int l[4]) {
+  if (p0 - lo >= BO_LCACHE) {
+    hit_lens(r, p0, hi, l, e);
+    return;
+  }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const long long p = p0 + (long long)q * BO_THREADS;
@@ -294,7 +292,7 @@ __device__ __forceinline__ void hit_ends(const BoRow &r, const BoShared &s, long
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const long long p = p0 + (long long)q * BO_THREADS;
-    l[q] = p >= hi ? -1 : (p - lo < BO_LCACHE ? (int)s.u.lc[p - lo] : snap_len(r, e[q]));
+    l[q] = p >= hi ? -1 : (int)s.u.lc[p - lo];
   }
 }
 
