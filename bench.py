@@ -516,9 +516,10 @@ def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state,
                 dr.build_sa(side)
                 state["pending"] = True
                 state["ingested"] = 0
-            st, _ = dr.poll(wait=False)
-            if st == 1:
-                state["pending"] = False
+            if state["pending"]:  # (nothing to swap in otherwise)
+                st, _ = dr.poll(wait=False)
+                if st == 1:
+                    state["pending"] = False
         stream.synchronize()
         times.append(time.perf_counter() - t0)
         bi = (BT + 3 * m) * 4
