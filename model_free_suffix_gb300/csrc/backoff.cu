@@ -22,7 +22,7 @@
 // and thread 0 picks the winner with exact integer comparisons.
 #include <climits>
 
-#include "sgd_internal.h"
+#include "delta_sig.cuh"
 
 namespace sgd {
 
@@ -57,9 +57,28 @@ struct BoShared {
   int dcnt[BO_CANDS][MAX_K];           // and their vote counts
   int dlen[BO_CANDS];
   long long dsum[BO_CANDS];
+  int wl[BO_THREADS];                   // delta windows that can hold an end (one batch)
   long long lo, hi, ds;
   int n, dv, ns, nc, stop, win;
 };
+
+// Ordered compaction over the CTA: the values of the threads whose pred holds,
+// in thread order, into out; returns their number.  wbuf: BO_WARPS words.
+__device__ __forceinline__ int block_compact(bool pred, int val, int *out, unsigned *wbuf, int warp,
+                                             int lane) {
+  const unsigned bal = __ballot_sync(FULL, pred);
+  if (lane == 0) wbuf[warp] = bal;
+  __syncthreads();
+  int base = 0, total = 0;
+  for (int w = 0; w < BO_WARPS; ++w) {
+    const int c = __popc(wbuf[w]);
+    if (w < warp) base += c;
+    total += c;
+  }
+  if (pred) out[base + __popc(bal & ((1u << lane) - 1u))] = val;
+  __syncthreads();
+  return total;
+}
 
 struct BoRow {
   const int32_t *row;  // the row's tokens
@@ -414,29 +433,39 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
         atomicAdd(&s.hs[l], 1);
       }
   }
-  if (delta)
-    for (long long u0 = tid; u0 <= r.dv - 2; u0 += 4 * BO_THREADS) {
-      int x[4], c[4];
+  // The delta in 128-token windows of the ring (window w holds Y indices
+  // [w * WIN - off, w * WIN - off + WIN)); an end matching >= 2 tokens ends
+  // the row's last pair, whose bucket is then set in its window's gram
+  // signature, so the windows without it are skipped (exactly).
+  const int d_off = (int)(r.ds % WIN);
+  const int d_nw = delta ? (d_off + r.dv - 1) / WIN + 1 : 0;
+  const int d_nrw = (int)(r.C / WIN);
+  const unsigned d_b2 = delta ? sig_bucket(2, s.tail[0], s.tail[1], 0, 0) : 0u;
+  auto d_cand = [&](int w) {  // window w may hold an end matching >= 2 tokens
+    const int rw = (int)((r.ds / WIN + w) % d_nrw);
+    return ((__ldg(a.sig + (size_t)(d_b2 >> 5) * d_nrw + rw) >> (d_b2 & 31)) & 1u) != 0;
+  };
+  for (int wb = 0; wb < d_nw; wb += BO_THREADS) {
+    const int w = wb + tid;
+    const int nl = block_compact(w < d_nw && d_cand(w), w, s.wl, s.wb[0], warp, lane);
+    for (int i = warp; i < nl; i += BO_WARPS) {  // a warp per listed window, 4 tokens per lane
+      const int wi = s.wl[i];
+      const long long rw = (r.ds / WIN + wi) % d_nrw;
+      const int4 v = __ldg(reinterpret_cast<const int4 *>(r.ring + rw * WIN) + lane);
+      const int tok[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const long long u = u0 + (long long)q * BO_THREADS;
-        x[q] = -1;
-        c[q] = r.Z;
-        if (u <= r.dv - 2) {
-          x[q] = y_at(r, u);
-          c[q] = y_at(r, u + 1);
+      for (int c = 0; c < 4; ++c) {
+        const long long u = (long long)wi * WIN - d_off + 4 * lane + c;
+        if (u < 0 || u > r.dv - 2 || tok[c] != s.tail[0]) continue;
+        const int l = delta_len(r, u);
+        if (l >= 2) {
+          atomicAdd(&s.hc[l], 1);
+          atomicAdd(&s.hd[l], 1);
         }
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q)
-        if (x[q] == s.tail[0] && c[q] != r.Z) {
-          const int l = delta_len(r, u0 + (long long)q * BO_THREADS);
-          if (l >= 2) {
-            atomicAdd(&s.hc[l], 1);
-            atomicAdd(&s.hd[l], 1);
-          }
-        }
     }
+    __syncthreads();
+  }
   __syncthreads();
   const long long lo = s.lo, hi = s.hi;
   for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
@@ -483,13 +512,22 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
       s.stop = none;
     }
     __syncthreads();
-    if (!s.stop)
-      for (long long base = r.dv - 2; base >= 0; base -= BO_THREADS) {
-        const long long u = base - tid;
-        bo_collect(s, MAX_BACKOFF, nc, s.dtot + MAX_BACKOFF, u >= 0 ? delta_len(r, u) : 0,
+    // listed windows newest first, four per chunk: thread tid takes position
+    // WIN - 1 - tid % WIN of the chunk's window tid / WIN (recency falls with tid)
+    for (int wb = 0; wb < d_nw && !s.stop; wb += BO_THREADS) {
+      const int w = d_nw - 1 - wb - tid;
+      const int nl = block_compact(w >= 0 && d_cand(w), w, s.wl, s.wb[0], warp, lane);
+      for (int c0 = 0; c0 < nl; c0 += BO_THREADS / WIN) {
+        const int li = c0 + tid / WIN;
+        long long u = -1;
+        if (li < nl) u = (long long)s.wl[li] * WIN - d_off + (WIN - 1 - tid % WIN);
+        const bool ok = u >= 0 && u <= r.dv - 2;
+        bo_collect(s, MAX_BACKOFF, nc, s.dtot + MAX_BACKOFF, ok ? delta_len(r, u) : 0,
                    (int)(-(u + 1)), R, tid, warp, lane);
         if (s.stop) break;
       }
+      __syncthreads();  // (the list is rewritten by the next batch)
+    }
   }
   if (nc > 0 && snap && hi > lo) {
     if (tid < nc) {
