@@ -167,18 +167,20 @@ def test_step_wait_injection_skips_docs_and_recovers(delta):
     dr.close()
 
 
+@pytest.mark.parametrize("nb", [1, 4], ids=["longest", "backoff4"])
 @pytest.mark.parametrize("pinned", [True, False], ids=["pinned-in-place", "pageable-staged"])
-def test_step_host_matches_device_step(pinned):
+def test_step_host_matches_device_step(pinned, nb):
     """sgd_step_host gives exactly what sgd_step gives on device buffers, step
-    after step: with page-locked host buffers the kernel reads and writes them
-    in place, with pageable ones the library stages copies."""
+    after step: with page-locked host buffers the kernels read and write them
+    in place, with pageable ones the library stages copies; also with
+    multi-length backoff (update, backoff and ingest launches)."""
     W, O, H = _mods()
     from model_free_suffix_gb300 import SuffixDrafter
     pin = (lambda t: t.pin_memory()) if pinned else (lambda t: t)
     V, S, B, T, k = 97, 256, 24, 5, 8
     rng = np.random.default_rng(21)
     kw = dict(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=16, max_occurrences=16,
-              max_sampled=T, corpus_capacity=2048, max_docs=256)
+              max_sampled=T, corpus_capacity=2048, max_docs=256, num_backoff=nb)
     A, Bd = SuffixDrafter(**kw), SuffixDrafter(**kw)
     tok = np.zeros((B, S), dtype=np.int32)
     n = rng.integers(40, 120, size=B).astype(np.int32)
