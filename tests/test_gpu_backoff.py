@@ -227,3 +227,19 @@ def test_backoff_edges(V, C, delta, R, k, D, nb):
     H.compare(out, O.propose(p, tok, n, X=Xd, active=active, threads=H.THREADS))
     assert dr.get_error() == 0
     dr.close()
+
+
+def test_backoff_full_serving_size_sampled_rows():
+    """The serving workload at its full size (B = 256, S = 4096, 1M-token
+    corpus, rebuilds), num_backoff = 8 through the step as the benchmark runs
+    it: 48 sampled rows per step against the oracle."""
+    W, O, H = _mods()
+    cfg = dataclasses.replace(W.CONFIGS["c3"], rebuild_tokens=8192)
+    ls = H.Lockstep(cfg, seed=3, steps=6, fused=True, drafter_over=dict(num_backoff=8),
+                    param_over=dict(num_backoff=8))
+    ls.prefill(seed=3)
+    rng = np.random.default_rng(3)
+    for _ in range(6):
+        ls.step(check_rows=np.sort(rng.choice(cfg.B, size=48, replace=False)), check_state=True)
+    assert ls.dr.get_error() == 0
+    ls.close()
