@@ -11,15 +11,17 @@
 //     step 3 (each candidate expanded by majority vote and scored; the best
 //     wins per path and the two winners compete by the same score).
 //
-// One CTA of 256 threads per row.  Match lengths are exact: every end of the
+// One CTA of 512 threads per row.  Match lengths are exact: every end of the
 // row is measured against the tail, and so is every end of the corpus that
 // can match >= 2 tokens -- the hits of the suffix-array interval of the last
-// two tokens, and every position of the delta.  A histogram of the lengths
-// gives the candidate lengths (thresholds 1..nb); one more pass per path
-// collects, for each candidate, its R most recent ends (the row's and the
-// delta's by a backward scan, the snapshot's by a radix selection on the end
-// position over the interval's hits).  Each warp then votes one candidate,
-// and thread 0 picks the winner with exact integer comparisons.
+// two tokens, and every delta position in a ring window whose gram signature
+// holds the last two tokens (no other window can hold such an end).  A
+// histogram of the lengths gives the candidate lengths (thresholds 1..nb);
+// one more pass per path collects, for each candidate, its R most recent ends
+// (the row's and the delta's by a backward scan, the snapshot's by a radix
+// selection on the end position over the interval's hits).  Each warp then
+// votes one candidate, and thread 0 picks the winner with exact integer
+// comparisons.
 #include <climits>
 
 #include "delta_sig.cuh"
