@@ -181,20 +181,21 @@ def test_backoff_worked_example():
         dr.close()
 
 
-@pytest.mark.parametrize("V,C,delta,R,k,D,nb", [
-    (2, 1 << 16, 0, 8, 6, 12, 8),
-    (2, 1 << 16, 1 << 15, 16, 8, 16, 5),
-    (3, 1 << 14, 1 << 12, 1, 1, 2, 2),
-    (5, 1 << 14, 1 << 14, 128, 16, 128, 8),
-], ids=["wide-interval", "wide+delta", "R1-k1-D2", "R128-D128"])
-def test_backoff_edges(V, C, delta, R, k, D, nb):
+@pytest.mark.parametrize("V,C,delta,R,k,D,nb,S", [
+    (2, 1 << 16, 0, 8, 6, 12, 8, 512),
+    (2, 1 << 16, 1 << 15, 16, 8, 16, 5, 512),
+    (3, 1 << 14, 1 << 12, 1, 1, 2, 2, 512),
+    (5, 1 << 14, 1 << 14, 128, 16, 128, 8, 512),
+    (7, 1 << 16, 1 << 14, 64, 64, 32, 8, 8192),
+], ids=["wide-interval", "wide+delta", "R1-k1-D2", "R128-D128", "k64-S8192"])
+def test_backoff_edges(V, C, delta, R, k, D, nb, S):
     """Few ids, so the interval of the last two tokens holds thousands of hits
     (more than the on-chip length cache: lengths evaluated again, ends chosen
     by the radix selection); the extreme knobs; rows that are empty, one or
     two tokens long, full, or inactive; docs both indexed and in the delta."""
     W, O, H = _mods()
     from model_free_suffix_gb300 import SuffixDrafter
-    S, B = 512, 40
+    B = 40
     rng = np.random.default_rng(V * 1000 + R)
     dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=D,
                        max_occurrences=R, min_token_prob=(1, 4), max_spec_offset=2,
