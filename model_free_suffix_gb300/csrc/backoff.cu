@@ -53,7 +53,10 @@ struct BoShared {
   int mode[MAX_BACKOFF];               // snapshot ends: 0 none, 1 every qualifying end, 2 the need most recent
   union {
     unsigned char lc[BO_LCACHE];       // interval hit lengths (0: no continuation), until the votes
-    int vv[BO_WARPS][MAX_R];           // per-warp vote scratch
+    struct {
+      int key[MAX_R];                  // a warp's vote: open-addressing count table
+      int cnt[MAX_R];
+    } ht[BO_WARPS];
   } u;
   int dtok[BO_CANDS][MAX_K];           // each candidate's voted tokens
   int dcnt[BO_CANDS][MAX_K];           // and their vote counts
@@ -232,7 +235,8 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
                         int lane) {
   const int c0 = s.cnt[ci], M = s.len[ci];
   const int cap = bo_cap(a, M, r.n);
-  int *vv = s.u.vv[warp];
+  int *hkey = s.u.ht[warp].key;
+  int *hcnt = s.u.ht[warp].cnt;
   bool alive[MAX_R / 32];
   int v[MAX_R / 32];
 #pragma unroll
@@ -253,22 +257,41 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
     bool any = false;
 #pragma unroll
     for (int u = 0; u < MAX_R / 32; ++u) {
-      const int i = lane + 32 * u;
       v[u] = -1;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         if ((d & 3) == q && alive[u]) v[u] = ahead[u][q];
-      if (i < c0) vv[i] = v[u];
       any |= v[u] >= 0;
     }
-    __syncwarp();
     if (!__any_sync(FULL, any)) break;
+    // count each continuation token in a table of MAX_R slots (>= the distinct
+    // tokens, at most c0 <= MAX_R, so an insert always finds its slot)
+#pragma unroll
+    for (int u = 0; u < MAX_R / 32; ++u) {
+      hkey[lane + 32 * u] = -1;
+      hcnt[lane + 32 * u] = 0;
+    }
+    __syncwarp();
+    int hs[MAX_R / 32];
+#pragma unroll
+    for (int u = 0; u < MAX_R / 32; ++u) {
+      hs[u] = -1;
+      if (v[u] < 0) continue;
+      static_assert(MAX_R == 128, "the slot hash takes 7 bits");
+      unsigned h = ((unsigned)v[u] * 2654435761u) >> 25;
+      for (;;) {
+        const int prev = atomicCAS(&hkey[h], -1, v[u]);
+        if (prev == -1 || prev == v[u]) break;
+        h = (h + 1) & (MAX_R - 1);
+      }
+      atomicAdd(&hcnt[h], 1);
+      hs[u] = (int)h;
+    }
+    __syncwarp();
     int best = 0, cu[MAX_R / 32];
 #pragma unroll
     for (int u = 0; u < MAX_R / 32; ++u) {
-      cu[u] = 0;
-      if (v[u] < 0) continue;
-      for (int i = 0; i < c0; ++i) cu[u] += vv[i] == v[u];
+      cu[u] = hs[u] >= 0 ? hcnt[hs[u]] : 0;
       best = max(best, cu[u]);
     }
     const int bc = (int)__reduce_max_sync(FULL, (unsigned)best);
@@ -277,7 +300,7 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
     for (int u = 0; u < MAX_R / 32; ++u)
       if (v[u] >= 0 && cu[u] == bc) mine = min(mine, (unsigned)v[u]);
     const int bt = (int)__reduce_min_sync(FULL, mine);
-    __syncwarp();  // every lane done reading vv before the next depth writes it
+    __syncwarp();  // every lane done reading the table before the next depth clears it
     if (!a.fixed && (long long)bc * a.pD < a.pN * (long long)c0) break;
     if (lane == 0) {
       s.dtok[ci][d] = bt;
