@@ -508,19 +508,18 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
   __syncthreads();
 
   // ---- candidate lengths: thresholds 1..nb of each path ----
-  if (tid == 0) {
-    s.ns = pick_lengths(s.hs, dl, 1, nb, s.len, s.tot);
-    s.nc = pick_lengths(s.hc, dl, 2, nb, s.len + MAX_BACKOFF, s.tot + MAX_BACKOFF);
-    for (int c = 0; c < BO_CANDS; ++c) s.cnt[c] = 0;
-    for (int c = 0; c < s.nc; ++c) {
-      int t = 0;
-      for (int m = s.len[MAX_BACKOFF + c]; m <= dl; ++m) t += s.hd[m];
-      s.dtot[MAX_BACKOFF + c] = t;
-    }
-    s.stop = 0;
-  }
+  if (tid == 0) s.ns = pick_lengths(s.hs, dl, 1, nb, s.len, s.tot);
+  if (tid == 32) s.nc = pick_lengths(s.hc, dl, 2, nb, s.len + MAX_BACKOFF, s.tot + MAX_BACKOFF);
+  if (tid < BO_CANDS) s.cnt[tid] = 0;
+  if (tid == 64) s.stop = 0;
   __syncthreads();
   const int ns = s.ns, nc = s.nc;
+  if (tid < nc) {  // the delta's ends reaching each corpus length
+    int t = 0;
+    for (int m = s.len[MAX_BACKOFF + tid]; m <= dl; ++m) t += s.hd[m];
+    s.dtot[MAX_BACKOFF + tid] = t;
+  }
+  __syncthreads();
 
   // ---- the row's candidates: their R most recent ends, by a backward scan ----
   if (ns > 0)
@@ -582,16 +581,36 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
                 atomicAdd(&s.hist[c][(e[q] >> sh) & 255], 1);
         }
         __syncthreads();
-        if (tid < nc && s.mode[tid] == 2) {
-          int cum = 0;
-          for (int d = 255; d >= 0; --d) {
-            const int h = s.hist[tid][d];
-            if (cum + h >= s.need[tid]) {
-              s.pref[tid] |= (long long)d << sh;
-              s.need[tid] -= cum;
-              break;
+        if (warp < nc && s.mode[warp] == 2) {
+          // warp c picks candidate c's digit: lane L sums bins 255 - 8L .. 248 - 8L,
+          // a scan over the lanes finds the lane where the count from the top
+          // reaches `need`, and that lane walks its eight bins
+          const int c = warp;
+          int hb[8], loc = 0;
+#pragma unroll
+          for (int q = 0; q < 8; ++q) {
+            hb[q] = s.hist[c][255 - 8 * lane - q];
+            loc += hb[q];
+          }
+          int incl = loc;
+#pragma unroll
+          for (int o = 1; o < 32; o <<= 1) {
+            const int y = __shfl_up_sync(FULL, incl, o);
+            if (lane >= o) incl += y;
+          }
+          const int need = s.need[c];
+          const int excl = incl - loc;
+          if (excl < need && incl >= need) {  // exactly one lane
+            int cum = excl;
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+              if (cum + hb[q] >= need) {
+                s.pref[c] |= (long long)(255 - 8 * lane - q) << sh;
+                s.need[c] = need - cum;
+                break;
+              }
+              cum += hb[q];
             }
-            cum += h;
           }
         }
         __syncthreads();
