@@ -64,7 +64,7 @@ struct BoShared {
   long long dsum[BO_CANDS];
   int wl[BO_THREADS];                   // delta windows that can hold an end (one batch)
   long long lo, hi, ds;
-  int n, dv, ns, nc, stop, win;
+  int n, dv, ns, nc, win;
 };
 
 // Ordered compaction over the CTA: the values of the threads whose pred holds,
@@ -343,8 +343,9 @@ __device__ __forceinline__ void hit_ends(const BoRow &r, const BoShared &s, long
 // One chunk of a backward scan: thread tid holds end `val` with length l
 // (ends in descending recency by tid).  Each candidate c < ncand of list
 // `off` (length s.len[off + c]) appends the chunk's ends reaching its length,
-// in order, up to R; s.stop is set once every list holds min(R, target[c]).
-__device__ void bo_collect(BoShared &s, int off, int ncand, const int *target, int l, int val, int R,
+// in order, up to R.  Returns, in every thread, whether every list now holds
+// min(R, target[c]) ends.
+__device__ bool bo_collect(BoShared &s, int off, int ncand, const int *target, int l, int val, int R,
                            int tid, int warp, int lane) {
   for (int c = 0; c < ncand; ++c) {
     const unsigned bal = __ballot_sync(FULL, l >= s.len[off + c]);
@@ -359,17 +360,15 @@ __device__ void bo_collect(BoShared &s, int off, int ncand, const int *target, i
     if (slot < R) s.occ[off + c][slot] = val;
   }
   __syncthreads();
-  if (tid == 0) {
-    bool full = true;
-    for (int c = 0; c < ncand; ++c) {
-      int t = 0;
-      for (int w = 0; w < BO_WARPS; ++w) t += __popc(s.wb[c][w]);
-      s.cnt[off + c] = min(R, s.cnt[off + c] + t);
-      full &= s.cnt[off + c] >= min(R, target[c]);
-    }
-    s.stop = full;
+  bool full = true;
+  if (tid < ncand) {  // thread c: candidate c's count
+    int t = 0;
+    for (int w = 0; w < BO_WARPS; ++w) t += __popc(s.wb[tid][w]);
+    const int cn = min(R, s.cnt[off + tid] + t);
+    s.cnt[off + tid] = cn;
+    full = cn >= min(R, target[tid]);
   }
-  __syncthreads();
+  return __syncthreads_and(full) != 0;
 }
 
 __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a) {
@@ -395,7 +394,6 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     }
     s.lo = 0;
     s.hi = 0;
-    s.stop = 0;
     s.win = -1;
   }
   for (int i = tid; i <= MAX_D; i += BO_THREADS) {
@@ -511,7 +509,6 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
   if (tid == 0) s.ns = pick_lengths(s.hs, dl, 1, nb, s.len, s.tot);
   if (tid == 32) s.nc = pick_lengths(s.hc, dl, 2, nb, s.len + MAX_BACKOFF, s.tot + MAX_BACKOFF);
   if (tid < BO_CANDS) s.cnt[tid] = 0;
-  if (tid == 64) s.stop = 0;
   __syncthreads();
   const int ns = s.ns, nc = s.nc;
   if (tid < nc) {  // the delta's ends reaching each corpus length
@@ -525,20 +522,15 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
   if (ns > 0)
     for (int base = n - 2; base >= 0; base -= BO_THREADS) {
       const int j = base - tid;
-      bo_collect(s, 0, ns, s.tot, j >= 0 ? self_len(r, j) : 0, j, R, tid, warp, lane);
-      if (s.stop) break;
+      if (bo_collect(s, 0, ns, s.tot, j >= 0 ? self_len(r, j) : 0, j, R, tid, warp, lane)) break;
     }
   // ---- the corpus's: the delta's ends first (the most recent), then the snapshot's ----
   if (nc > 0 && delta) {
-    if (tid == 0) {
-      bool none = true;
-      for (int c = 0; c < nc; ++c) none &= s.dtot[MAX_BACKOFF + c] == 0;
-      s.stop = none;
-    }
-    __syncthreads();
+    bool stop = true;  // (no delta end reaches any corpus length)
+    for (int c = 0; c < nc; ++c) stop &= s.dtot[MAX_BACKOFF + c] == 0;
     // listed windows newest first, four per chunk: thread tid takes position
     // WIN - 1 - tid % WIN of the chunk's window tid / WIN (recency falls with tid)
-    for (int wb = 0; wb < d_nw && !s.stop; wb += BO_THREADS) {
+    for (int wb = 0; wb < d_nw && !stop; wb += BO_THREADS) {
       const int w = d_nw - 1 - wb - tid;
       const int nl = block_compact(w >= 0 && d_cand(w), w, s.wl, s.wb[0], warp, lane);
       for (int c0 = 0; c0 < nl; c0 += BO_THREADS / WIN) {
@@ -546,9 +538,9 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
         long long u = -1;
         if (li < nl) u = (long long)s.wl[li] * WIN - d_off + (WIN - 1 - tid % WIN);
         const bool ok = u >= 0 && u <= r.dv - 2;
-        bo_collect(s, MAX_BACKOFF, nc, s.dtot + MAX_BACKOFF, ok ? delta_len(r, u) : 0,
-                   (int)(-(u + 1)), R, tid, warp, lane);
-        if (s.stop) break;
+        stop = bo_collect(s, MAX_BACKOFF, nc, s.dtot + MAX_BACKOFF, ok ? delta_len(r, u) : 0,
+                          (int)(-(u + 1)), R, tid, warp, lane);
+        if (stop) break;
       }
       __syncthreads();  // (the list is rewritten by the next batch)
     }
