@@ -34,6 +34,7 @@ constexpr int BO_THREADS = 512;
 constexpr int BO_WARPS = BO_THREADS / 32;
 constexpr int BO_CANDS = 2 * MAX_BACKOFF;  // row candidates, then corpus candidates
 constexpr int BO_LCACHE = 16384;           // interval hits whose length is kept on chip
+constexpr int BO_TOPC = 5;                 // length classes of the first radix digit
 static_assert(BO_LCACHE % (4 * BO_THREADS) == 0, "hit_ends: four hits on one side of the cache end");
 
 struct BoShared {
@@ -58,8 +59,14 @@ struct BoShared {
       int cnt[MAX_R];
     } ht[BO_WARPS];
   } u;
-  int dtok[BO_CANDS][MAX_K];           // each candidate's voted tokens
-  int dcnt[BO_CANDS][MAX_K];           // and their vote counts
+  union {
+    struct {
+      int tok[BO_CANDS][MAX_K];        // each candidate's voted tokens
+      int cnt[BO_CANDS][MAX_K];        // and their vote counts
+    } d;
+    int top[BO_TOPC][256];             // until the votes: valid interval hits by length
+                                       // class (2, 3, 4, 5, >= 6) and top digit of the end
+  } v;
   int dlen[BO_CANDS];
   long long dsum[BO_CANDS];
   int wl[BO_THREADS];                   // delta windows that can hold an end (one batch)
@@ -303,8 +310,8 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
     __syncwarp();  // every lane done reading the table before the next depth clears it
     if (!a.fixed && (long long)bc * a.pD < a.pN * (long long)c0) break;
     if (lane == 0) {
-      s.dtok[ci][d] = bt;
-      s.dcnt[ci][d] = bc;
+      s.v.d.tok[ci][d] = bt;
+      s.v.d.cnt[ci][d] = bc;
     }
     sum += bc;
     ++len;
@@ -401,6 +408,7 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     s.hc[i] = 0;
     s.hd[i] = 0;
   }
+  for (int i = tid; i < BO_TOPC * 256; i += BO_THREADS) s.v.top[i >> 8][i & 255] = 0;
   __syncthreads();
   const int n = s.n;
   int32_t *dr = a.drafts + (size_t)b * k;
@@ -491,6 +499,9 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
   }
   __syncthreads();
   const long long lo = s.lo, hi = s.hi;
+  // the radix selection's first digit (end bits sh_top and up) is counted here
+  // too, per length class, so that its first pass needs no walk of the interval
+  const int sh_top = snap ? ((64 - __clzll(r.N - 1) + 7) / 8 - 1) * 8 : 0;
   for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
     int l[4];
     long long e[4];
@@ -500,7 +511,10 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
       const long long p = p0 + (long long)j * BO_THREADS;
       if (l[j] < 0) continue;
       if (p - lo < BO_LCACHE) s.u.lc[p - lo] = (unsigned char)l[j];
-      if (l[j] > 0) atomicAdd(&s.hc[l[j]], 1);
+      if (l[j] > 0) {
+        atomicAdd(&s.hc[l[j]], 1);
+        atomicAdd(&s.v.top[min(l[j], 6) - 2][(e[j] >> sh_top) & 255], 1);
+      }
     }
   }
   __syncthreads();
@@ -556,23 +570,35 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     __syncthreads();
     bool radix = false;
     for (int c = 0; c < nc; ++c) radix |= s.mode[c] == 2;
+    bool classed = true;  // every selecting candidate's length within the counted classes
+    for (int c = 0; c < nc; ++c) classed &= s.mode[c] != 2 || s.len[MAX_BACKOFF + c] <= 6;
     if (radix) {  // the need most recent qualifying ends: MSB-first radix selection on e
-      const int nbits = 64 - __clzll(r.N - 1);
-      for (int sh = ((nbits + 7) / 8 - 1) * 8; sh >= 0; sh -= 8) {
-        for (int i = tid; i < nc * 256; i += BO_THREADS) s.hist[i >> 8][i & 255] = 0;
-        __syncthreads();
-        for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
-          long long e[4];
-          int l[4];
-          hit_ends(r, s, lo, p0, hi, e, l);
+      for (int sh = sh_top; sh >= 0; sh -= 8) {
+        if (sh == sh_top && classed) {  // the first digit from the length pass's counts
+          for (int i = tid; i < nc * 256; i += BO_THREADS) {
+            const int c = i >> 8, d = i & 255;
+            int t = 0;
+            if (s.mode[c] == 2)
+              for (int k = s.len[MAX_BACKOFF + c] - 2; k < BO_TOPC; ++k) t += s.v.top[k][d];
+            s.hist[c][d] = t;
+          }
+          __syncthreads();
+        } else {
+          for (int i = tid; i < nc * 256; i += BO_THREADS) s.hist[i >> 8][i & 255] = 0;
+          __syncthreads();
+          for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
+            long long e[4];
+            int l[4];
+            hit_ends(r, s, lo, p0, hi, e, l);
 #pragma unroll
-          for (int q = 0; q < 4; ++q)
-            for (int c = 0; c < nc; ++c)
-              if (s.mode[c] == 2 && l[q] >= s.len[MAX_BACKOFF + c] &&
-                  (e[q] >> (sh + 8)) == (s.pref[c] >> (sh + 8)))
-                atomicAdd(&s.hist[c][(e[q] >> sh) & 255], 1);
+            for (int q = 0; q < 4; ++q)
+              for (int c = 0; c < nc; ++c)
+                if (s.mode[c] == 2 && l[q] >= s.len[MAX_BACKOFF + c] &&
+                    (e[q] >> (sh + 8)) == (s.pref[c] >> (sh + 8)))
+                  atomicAdd(&s.hist[c][(e[q] >> sh) & 255], 1);
+          }
+          __syncthreads();
         }
-        __syncthreads();
         if (warp < nc && s.mode[warp] == 2) {
           // warp c picks candidate c's digit: lane L sums bins 255 - 8L .. 248 - 8L,
           // a scan over the lanes finds the lane where the count from the top
@@ -650,8 +676,8 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
   const int len = w >= 0 ? s.dlen[w] : 0;
   const int fill = a.fixed ? s.tail[0] : -1;
   for (int d = tid; d < k; d += BO_THREADS) {
-    dr[d] = d < len ? s.dtok[w][d] : fill;
-    if (pr) pr[d] = d < len ? (float)((double)s.dcnt[w][d] / (double)s.cnt[w]) : 0.f;
+    dr[d] = d < len ? s.v.d.tok[w][d] : fill;
+    if (pr) pr[d] = d < len ? (float)((double)s.v.d.cnt[w][d] / (double)s.cnt[w]) : 0.f;
   }
   if (tid == 0) {
     a.num_valid[b] = a.fixed ? k : len;
