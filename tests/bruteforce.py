@@ -148,6 +148,67 @@ def brute_propose(t: Sequence[int], n: int, k: int, D: int, R: Optional[int], S:
     return res
 
 
+def brute_backoff(t: Sequence[int], n: int, k: int, D: int, R: int, S: int,
+                  factor: Tuple[int, int], offset: int, min_prob: Tuple[int, int],
+                  nb: int, X: Optional[Sequence[int]] = None, Z: int = -1) -> Result:
+    """Multi-length backoff read literally: for support threshold t the
+    candidate length is the largest l whose last-l-token string occurs (with a
+    continuation) at least t times, found by counting substring occurrences
+    for every l; each candidate votes with the R most recent occurrences of
+    its string; the best score wins, then the longer length, then the row."""
+    t = list(t[:n])
+    best: Optional[Result] = None
+    if n == 0:
+        return Result()
+    paths = [(1, t, 1, min(D, n - 1))]
+    if X is not None and len(X) > 0 and D >= 2 and n >= 2:
+        paths.append((2, list(X), 2, min(D, n)))
+    for src, text, lmin, lmax in paths:
+        def valid(e):
+            if src == 1:
+                return e <= n - 2
+            return e + 1 < len(text) and text[e + 1] != Z
+
+        occ_of = {l: sorted((e for e in ends_of(text, t[n - l:]) if valid(e)), reverse=True)
+                  for l in range(lmin, lmax + 1)}
+        lengths = []
+        for th in range(1, nb + 1):
+            ok = [l for l in occ_of if len(occ_of[l]) >= th]
+            if ok and max(ok) not in lengths:
+                lengths.append(max(ok))
+        for l in lengths:
+            occ = occ_of[l][:R]
+            res = Result()
+            res.M, res.source, res.c0 = l, src, len(occ)
+            cap = min(k, (factor[0] * l) // factor[1] + offset, max(0, S - n - 1))
+            alive = list(occ)
+            for d in range(max(cap, 0)):
+                vals = []
+                for e in alive:
+                    q = e + 1 + d
+                    if src == 1:
+                        v = t[q] if q <= n - 1 else None
+                    else:
+                        v = text[q] if q < len(text) and text[q] != Z else None
+                    if v is not None:
+                        vals.append((e, v))
+                if not vals:
+                    break
+                counts = {}
+                for _, v in vals:
+                    counts[v] = counts.get(v, 0) + 1
+                top = max(counts.values())
+                tau = min(v for v, c in counts.items() if c == top)
+                if top * min_prob[1] < min_prob[0] * res.c0:
+                    break
+                res.drafts.append(tau)
+                res.probs.append(Fraction(top, res.c0))
+                alive = [e for e, v in vals if v == tau]
+            if best is None or res.score > best.score or (res.score == best.score and l > best.M):
+                best = res
+    return best if best is not None else Result()
+
+
 def brute_suffix_array(X: Sequence[int]) -> List[int]:
     """Python's list order is lexicographic with a proper prefix first."""
     X = list(X)

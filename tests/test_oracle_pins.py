@@ -743,3 +743,38 @@ def test_backoff_never_scores_below_fewer_candidates(orc):
                 seen_shorter += int(M != cands[0])
             prev = cur
     assert seen_shorter > 10  # shorter lengths do win
+
+
+def test_backoff_matches_substring_count_brute_force(orc):
+    """The oracle's backoff (per-end match lengths, their t-th largest values)
+    against a literal reading of the pages (for each threshold t the largest
+    length whose string occurs at least t times, by counting substring
+    occurrences), on tiny random rows and corpora."""
+    from bruteforce import brute_backoff
+    rng = np.random.default_rng(77)
+    checked = shorter = 0
+    for trial in range(300):
+        V = int(rng.integers(2, 5))
+        n = int(rng.integers(0, 28))
+        t = [int(x) for x in rng.integers(0, V, n)]
+        X = None
+        if rng.random() < 0.7:
+            X = _doc_text([rng.integers(0, V, rng.integers(1, 9)) for _ in range(int(rng.integers(1, 5)))], V)
+        kw = dict(S=40, V=V, k=int(rng.integers(1, 6)), D=int(rng.integers(1, 8)),
+                  R=int(rng.integers(1, 6)), factor=(int(rng.integers(1, 3)), 1),
+                  offset=int(rng.integers(0, 3)), min_prob=(int(rng.integers(1, 3)), 4))
+        nb = int(rng.integers(2, 9))
+        r = _row(orc, orc.Params(**kw, num_backoff=nb), t, X=X) if n > 0 else None
+        b = brute_backoff(t, n, kw["k"], kw["D"], kw["R"], kw["S"], kw["factor"], kw["offset"],
+                          kw["min_prob"], nb, X=None if X is None else X.tolist(), Z=V)
+        if r is None:
+            continue
+        L = len(b.drafts)
+        assert r.match_info[0].tolist() == [b.M, b.source], (trial, t, X)
+        assert int(r.num_valid[0]) == L and r.drafts[0, :L].tolist() == b.drafts
+        assert np.float32(r.score[0]) == np.float32(b.score)
+        assert [np.float32(x) for x in r.probs[0, :L]] == [np.float32(x) for x in b.probs]
+        checked += 1
+        one = _row(orc, orc.Params(**kw, select_by_score=True), t, X=X)
+        shorter += int(one.match_info[0].tolist() != [b.M, b.source])
+    assert checked > 200 and shorter > 10
