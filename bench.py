@@ -324,7 +324,7 @@ def run_ours(args, rank, world, delta=0, backoff=1):
                                                      "launches of the step)",
                              "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
                              "frac": round(ach / peak, 4), "bytes_per_launch": int(byts),
-                             "peak_kind": peak_kind},
+                             "traffic": kernel_traffic("backoff_kernel"), "peak_kind": peak_kind},
                 "builds_in_timed_region": builds_in_region, "clocks": clocks}
     if delta:
         peak, peak_kind = peaks()
