@@ -49,7 +49,16 @@ class Proposal:
 
 
 class SuffixDrafter:
-    """One libsgd context on one GPU."""
+    """One libsgd context on one GPU.
+
+    The knobs are those of sgd_config in include/sgd.h, where each is
+    documented; the ones that change what is drafted: max_spec_factor,
+    max_spec_offset, min_token_prob, depth_sum_cap, delta_capacity (docs not
+    yet indexed are matched too), draft_mode (1: Model Runner V2 fixed-length
+    drafts), select_by_score (1: the better score wins between the row's and
+    the corpus's candidates) and num_backoff (2..8: multi-length backoff).
+    The others choose between equivalent forms of the same computation.
+    """
 
     def __init__(self, max_batch: int, seq_capacity: int, vocab_size: int, k: int = 16,
                  max_tree_depth: int = 24, max_occurrences: int = 64, max_sampled: Optional[int] = None,
