@@ -349,7 +349,8 @@ def run_ours(args, rank, world, delta=0, backoff=1):
                                "p90": round(1e3 * float(np.percentile(prop_ms, 90)), 2)},
                 "roofline": {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 2),
                              "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-                             "bytes_per_launch": int(byts), "peak_kind": peak_kind},
+                             "bytes_per_launch": int(byts),
+                             "traffic": kernel_traffic("propose_kernel_delta"), "peak_kind": peak_kind},
                 "builds_in_timed_region": builds_in_region, "clocks": clocks}
     # e2e: host buffers through the public API, copies inside the timed region
     if state["pending"]:
