@@ -320,11 +320,13 @@ int sgd_suffix_array(sgd_ctx *ctx, const int32_t *text, int64_t n, int32_t *sa, 
  * SGD_NOALLOC_MAX_TOKENS tokens (about 2.5 MB, held on every GPU that loads the
  * library until the process exits); longer texts return SGD_ETOOLARGE.  The
  * first call on a device (with that device current) looks the array up on
- * that device; make that first call before any stream capture.  All calls
- * share the array and it keeps the previous call's contents: calls whose GPU
- * work overlaps (two streams, two threads, two processes' graphs) race;
- * host threads are serialised inside the call.  Blocks the host until the
- * array is written.  SGD_EBUILD if the sort reported a failure. */
+ * that device; make that first call before any stream capture.  `stream`
+ * must belong to the current device (SGD_EINVAL otherwise).  All calls in a
+ * process share the array and find the previous call's contents in it: two
+ * calls whose GPU work overlapped would race on it.  The call prevents that
+ * itself: callers on different host threads are serialised, and each call
+ * waits for its own GPU work (blocking the host) before it returns.
+ * SGD_EBUILD if the sort reported a failure. */
 #define SGD_NOALLOC_MAX_TOKENS 65536
 int sgd_suffix_array_noalloc(const int32_t *text, int64_t n, int32_t *sa, void *stream);
 

@@ -47,6 +47,15 @@ extern "C" int sgd_suffix_array_noalloc(const int32_t *text, int64_t n, int32_t 
   std::lock_guard<std::mutex> lock(g_mu);
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return SGD_ECUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // the array's address is resolved for the current device; a stream of
+  // another device would run the sort against that device's memory
+  int sdev = -1;
+  if (cudaStreamGetDevice(st, &sdev) != cudaSuccess) {
+    cudaGetLastError();
+    return SGD_EINVAL;
+  }
+  if (sdev != dev) return SGD_EINVAL;
   if (g_base[dev] == nullptr) {
     // first call on this device (with it current): resolve the array's address
     void *p = nullptr;
@@ -63,7 +72,6 @@ extern "C" int sgd_suffix_array_noalloc(const int32_t *text, int64_t n, int32_t 
   s.h_pinned = g_h_count;
   s.h_hist = g_h_hist;
   uint32_t *err = reinterpret_cast<uint32_t *>(g_base[dev] + used);
-  cudaStream_t st = static_cast<cudaStream_t>(stream);
   // the array keeps the previous call's contents: the error word must start
   // at zero (the sort clears its own histograms and look-back words per pass)
   if (cudaMemsetAsync(err, 0, 4, st) != cudaSuccess) return SGD_ECUDA;

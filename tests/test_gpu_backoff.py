@@ -5,7 +5,7 @@ The oracle computes every match length by brute force and ranks the
 candidates; the GPU measures lengths exactly too (row ends, the hits of the
 last two tokens' suffix-array interval, every delta position) and selects the
 R most recent ends per candidate.  Drafts, counts and match info bit-exact,
-scores and probabilities within 1e-6 relative.
+scores and probabilities bit-equal as float32 words.
 """
 import dataclasses
 

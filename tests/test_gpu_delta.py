@@ -4,7 +4,7 @@ a brute-force scan before the next rebuild indexes them.
 The oracle's corpus is the snapshot followed by the delta's text (oracle
 Ring.delta, cut at the capacity); the GPU reads the delta in place from the
 ring.  Drafts, counts and match info bit-exact, scores and probabilities
-within 1e-6 relative, through every path: one fused launch per step (the
+bit-equal as float32 words, through every path: one fused launch per step (the
 ingest CTA appending while the rows scan), the two-launch mode, the plain
 propose, a ring that wraps and evicts, a delta larger than its capacity.
 """

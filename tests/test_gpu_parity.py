@@ -1,8 +1,9 @@
 """CUDA library vs CPU oracle, element by element, on the same seeded inputs.
 
 Drafts, valid counts, match info, token buffers and suffix arrays must be
-bit-exact; scores and per-slot probabilities within 1e-6 relative (both sides
-round float(integer / c0) from double, so they are expected to be identical).
+bit-exact; scores and per-slot probabilities bit-equal as float32 words (both
+sides round the same integer quotient over c0 to float32, which lands on the
+same float: tests/test_arith.py).
 """
 import dataclasses
 import json
@@ -53,20 +54,28 @@ def _ingest_text(dr, X, V, S):
 
 
 # ---------------------------------------------------------------------------
+# Every parameter a worked example may set, and the drafter argument it becomes.
+# A key missing here fails the test instead of being dropped silently.
+GOLDEN_KNOBS = {"S": "seq_capacity", "V": "vocab_size", "k": "k", "D": "max_tree_depth",
+                "R": "max_occurrences", "factor": "max_spec_factor", "offset": "max_spec_offset",
+                "min_prob": "min_token_prob", "depth_sum_cap": "depth_sum_cap",
+                "num_backoff": "num_backoff"}
+
+
 @pytest.mark.parametrize("case", GOLDEN["cases"], ids=lambda c: c["name"])
 def test_golden_case(case):
     SuffixDrafter, W, O, H = _mods()
     pr = dict(S=1000, V=100, k=8, D=24, R=64, factor=(1, 1), offset=0, min_prob=(1, 10),
-              depth_sum_cap=False)
+              depth_sum_cap=False, num_backoff=1)
+    unknown = set(case.get("params", {})) - set(GOLDEN_KNOBS)
+    assert not unknown, "golden parameters with no drafter argument: %s" % sorted(unknown)
     for key, val in case.get("params", {}).items():
         pr[key] = tuple(val) if isinstance(val, list) else val
     if pr["S"] % 4:
         pytest.skip("row capacity must be a multiple of 4 on the GPU (oracle-only case)")
     X = case.get("X")
-    dr = SuffixDrafter(max_batch=1, seq_capacity=pr["S"], vocab_size=pr["V"], k=pr["k"],
-                       max_tree_depth=pr["D"], max_occurrences=pr["R"], max_spec_factor=pr["factor"],
-                       max_spec_offset=pr["offset"], min_token_prob=pr["min_prob"],
-                       depth_sum_cap=pr["depth_sum_cap"], corpus_capacity=64 if X else 0)
+    dr = SuffixDrafter(max_batch=1, corpus_capacity=64 if X else 0,
+                       **{GOLDEN_KNOBS[key]: val for key, val in pr.items()})
     t = case["t"]
     row = np.full((1, pr["S"]), -1, dtype=np.int32)
     row[0, :len(t)] = t
