@@ -12,11 +12,24 @@ GB/s of the dominant kernel against the measured copy bandwidth.
 Under torchrun every rank runs an independent replica of the workload on its
 own GPU (rows shard across GPUs; there is no data-path collective); rank 0
 prints one JSON line.  `--impl reference` times the CPU oracle instead.
+
+Secondary lines in the same JSON object (each its own workload, named in it):
+  warm / latency_floor  the headline step without the L2 flush, and one graph
+                        of one minimal kernel between the same events;
+  delta, backoff        the headline loop with the delta scan / multi-length
+                        backoff drafting;
+  long_context          the long-context serving loop (B=1024, S=32768, 4M
+                        corpus, 64 steps, 5% of rows finishing per step);
+  sa_build              standalone suffix-array builds (1M, 16M tokens);
+  sa_concurrent         drafting steps with and without a suffix-array build
+                        running on a side stream, the build's wall time and
+                        the swap cost;
+  cpu_baseline          the CPU oracle on the host's cores and on one core,
+                        and the naive comparison-sort suffix array.
 """
 from __future__ import annotations
 
 import argparse
-import dataclasses
 import json
 import os
 import statistics
@@ -32,11 +45,30 @@ if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
 METRIC = "propose steps/s & µs/step at B=256,S=4096; SA build Mtok/s; HBM GB/s"
-WORKLOAD = ("c3 serving loop: B=256 rows, S=4096 int32, vocab 151936 (Zipf 1.1 fresh tokens, "
-            "p=0.5 repeats from 256 spans of 16-128), num_tokens U[1024,4096], k=16, "
-            "max_tree_depth=24, max_occurrences=64, T=17 sampled ids (U[1,17] accepted), "
-            "1M-token corpus ring prefilled with 64-512-token responses; per step 5% of rows "
-            "finish and are ingested, a side-stream rebuild starts once 2^16 tokens arrived")
+WORKLOADS = {
+    "c1": ("self-match loop: B=4 rows, S=2048 int32, vocab 32000 (uniform fresh tokens, p=0.7 "
+           "repeats from 64 spans of 8-64), num_tokens U[512,2048], k=8, max_tree_depth=24, "
+           "T=9 sampled ids, no corpus"),
+    "c2": ("self-match loop: B=64 rows, S=8192 int32, vocab 151936 (Zipf 1.1 fresh tokens, "
+           "p=0.5 repeats from 256 spans of 16-128), num_tokens U[1024,8192], k=16, "
+           "max_tree_depth=24, T=17 sampled ids, no corpus"),
+    "c3": ("serving loop: B=256 rows, S=4096 int32, vocab 151936 (Zipf 1.1 fresh tokens, "
+           "p=0.5 repeats from 256 spans of 16-128), num_tokens U[1024,4096], k=16, "
+           "max_tree_depth=24, max_occurrences=64, T=17 sampled ids (U[1,17] accepted), "
+           "1M-token corpus ring prefilled with 64-512-token responses; per step 5% of rows "
+           "finish and are ingested, a side-stream rebuild starts once 2^16 tokens arrived"),
+    "c5": ("long-context serving loop: B=1024 rows, S=32768 int32, vocab 151936 (Zipf 1.1 "
+           "fresh tokens, p=0.8 repeats from 1024 spans of 32-512), num_tokens U[8192,32768], "
+           "k=32, max_tree_depth=32, max_occurrences=64, T=33 sampled ids, 4M-token corpus "
+           "ring prefilled; per step 5% of rows (51) finish and are ingested, a side-stream "
+           "rebuild starts once 2^16 tokens arrived and none is in flight"),
+}
+TIMING_NOTE = {
+    "l2": "flushed before every timed step (a write of twice the L2 size, outside the events)",
+    "launch": "each step replays one CUDA graph (the fused sgd_step launch: update + propose + "
+              "ingest, or the separate calls where the step cannot fuse) on a highest-priority "
+              "stream; rebuilds run on a lowest-priority side stream",
+}
 
 
 def kernel_traffic(kernel, items=None):
@@ -120,6 +152,12 @@ class Clocks:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
+def _us(ms_list):
+    return {"mean": round(1e3 * float(np.mean(ms_list)), 2),
+            "median": round(1e3 * float(np.median(ms_list)), 2),
+            "p90": round(1e3 * float(np.percentile(ms_list, 90)), 2)}
+
+
 # ---------------------------------------------------------------------------
 def make_steps(cfg, seed, n_steps):
     from model_free_suffix_gb300 import workload as W
@@ -130,38 +168,90 @@ def make_steps(cfg, seed, n_steps):
 
 
 def algorithmic_bytes_propose(sum_n, B, T, k, N, ingest_tokens=0):
-    """Bytes one step launch must touch (lower bound): every valid token of
-    every row once, the sampled ids, the outputs, the sectors of two
-    suffix-array binary searches per row, and the ingested docs (read once,
-    written once into the ring)."""
+    """Bytes one step launch must touch, the data-independent lower bound:
+    every valid token of every row once, the sampled ids, the outputs, the
+    sectors of two suffix-array binary searches per row, and the ingested
+    docs (read once, written once into the ring)."""
     probe = 0 if N <= 0 else B * 2 * int(np.ceil(np.log2(N + 1))) * 2 * 32
     return 4 * sum_n + 4 * B * T + B * (8 * k + 16) + probe + 8 * ingest_tokens
 
 
+class RowStats:
+    """Per-row statistics the drafting kernel writes (sgd_set_row_stats),
+    summed over the timed steps: the suffix-array hits each row's probe
+    scanned and the continuation gathers of rows drafted from the corpus.
+    Each scanned hit costs an SA entry and a text sector (4 + 32 bytes); each
+    corpus occurrence that votes reads ceil(4 cap / 32) sectors."""
+
+    def __init__(self, dr, B, dev):
+        import torch
+        self.buf = torch.zeros(dr.cfg.max_batch * 4, dtype=torch.int32, device=dev)
+        self.acc = torch.zeros(3, dtype=torch.int64, device=dev)
+        self.steps = 0
+        self.B = B
+        dr.set_row_stats(self.buf)
+
+    def add(self):
+        import torch
+        st = self.buf[:4 * self.B].view(self.B, 4).to(torch.int64)
+        corpus = (st[:, 3] == 2).to(torch.int64)
+        gather = st[:, 1] * ((4 * st[:, 2] + 31) // 32 * 32) * corpus
+        self.acc += torch.stack([st[:, 0].sum(), gather.sum(), (st[:, 3] == 2).sum()])
+        self.steps += 1
+
+    def per_step(self):
+        a = self.acc.cpu().numpy().astype(np.float64) / max(1, self.steps)
+        return {"hits_scanned": round(float(a[0]), 1), "gather_bytes": round(float(a[1]), 1),
+                "corpus_rows": round(float(a[2]), 2)}
+
+
 def workload_config(cfg, world):
     """The workload both arms run, by what it is and its sizes."""
-    return {"workload": WORKLOAD, "B": cfg.B, "S": cfg.S, "k": cfg.k, "D": cfg.D, "R": cfg.R,
-            "T": cfg.T, "corpus_tokens": cfg.corpus_tokens, "rebuild_tokens": cfg.rebuild_tokens,
+    return {"workload": WORKLOADS[cfg.name], "B": cfg.B, "S": cfg.S, "k": cfg.k, "D": cfg.D,
+            "R": cfg.R, "T": cfg.T, "corpus_tokens": cfg.corpus_tokens,
+            "rebuild_tokens": cfg.rebuild_tokens,
             "parallelism": "replicas" if world > 1 else "single"}
 
 
-def run_ours(args, rank, world, delta=0, backoff=1):
-    """The serving loop.  delta > 0: the same loop with the docs ingested since
-    the current snapshot also matched (brute-force scan of up to `delta`
-    tokens); backoff > 1: the same loop drafting with multi-length backoff.
-    Either is timed as a secondary line (no end-to-end or build legs)."""
+def _prefill(dr, cfg, tr, dev, side, rank, chunk=2048):
+    """Corpus prefill (setup, untimed): docs until the ring is full, then the
+    first snapshot, built and swapped in."""
+    import torch
+    from model_free_suffix_gb300 import workload as W
+    docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
+    for s0 in range(0, docs.shape[0], chunk):
+        d = docs[s0:s0 + chunk]
+        m = d.shape[0]
+        buf = torch.full((m, cfg.S), -1, dtype=torch.int32, device=dev)
+        buf[:, :d.shape[1]] = torch.from_numpy(d).to(dev)
+        dr.ingest(buf, torch.arange(m, dtype=torch.int32, device=dev),
+                  torch.zeros(m, dtype=torch.int32, device=dev),
+                  torch.from_numpy(np.ascontiguousarray(lens[s0:s0 + chunk])).to(dev))
+        del buf
+    dr.build_sa(side)
+    assert dr.poll(wait=True)[0] == 1
+
+
+def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=None,
+               headline=False):
+    """The serving loop of `cfg_name`: per step the update, propose and ingest
+    of the rows that finish (one captured graph), then the host's rebuild
+    policy and swap poll.  delta > 0: the docs ingested since the current
+    snapshot are matched too; backoff > 1: multi-length backoff drafting.
+    headline: also the warm and latency-floor timings, the end-to-end leg
+    through host buffers and the standalone suffix-array builds."""
     import torch
     from model_free_suffix_gb300 import SuffixDrafter
     from model_free_suffix_gb300 import workload as W
 
     dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
     torch.cuda.set_device(dev)
-    cfg = W.CONFIGS[args.config]
-    secondary = bool(delta) or backoff > 1
-    K = args.delta_steps if delta else (args.backoff_steps if backoff > 1 else args.steps)
-    Wm = args.warmup
-    K_e2e = 0 if secondary else min(K, args.e2e_steps)
-    tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=Wm + K + K_e2e)
+    cfg = W.CONFIGS[cfg_name]
+    K = args.steps if K is None else K
+    Wm = args.warmup if Wm is None else Wm
+    K_warm = min(K, args.warm_steps) if headline else 0
+    K_e2e = min(K, args.e2e_steps) if headline else 0
+    tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=Wm + K + K_warm + K_e2e)
     dr = SuffixDrafter(max_batch=cfg.B, seq_capacity=cfg.S, vocab_size=cfg.V, k=cfg.k,
                        max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
                        max_spec_factor=cfg.factor, max_spec_offset=cfg.offset,
@@ -172,46 +262,38 @@ def run_ours(args, rank, world, delta=0, backoff=1):
     stream = torch.cuda.Stream(device=dev, priority=greatest)
     side = torch.cuda.Stream(device=dev, priority=least)
     torch.cuda.set_stream(stream)
-    # corpus prefill (setup, untimed)
     if cfg.corpus_tokens:
-        docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
-        for s0 in range(0, docs.shape[0], 2048):
-            d = docs[s0:s0 + 2048]
-            m = d.shape[0]
-            buf = torch.full((m, cfg.S), -1, dtype=torch.int32, device=dev)
-            buf[:, :d.shape[1]] = torch.from_numpy(d).to(dev)
-            dr.ingest(buf, torch.arange(m, dtype=torch.int32, device=dev),
-                      torch.zeros(m, dtype=torch.int32, device=dev),
-                      torch.from_numpy(np.ascontiguousarray(lens[s0:s0 + 2048])).to(dev))
-        dr.build_sa(side)
-        assert dr.poll(wait=True)[0] == 1
+        _prefill(dr, cfg, tr, dev, side, rank, chunk=2048 if cfg.S <= 8192 else 256)
 
     g_tok = torch.from_numpy(tok).to(dev)
     g_n = torch.from_numpy(n).to(dev)
     out = dr.new_outputs(cfg.B)
+    stats = RowStats(dr, cfg.B, dev) if backoff == 1 else None
     m_fin = int(np.floor(cfg.finish_frac * cfg.B))
     # fixed device inputs of one step; each step's values are staged into them
     d_samp = torch.full((cfg.B, cfg.T), -1, dtype=torch.int32, device=dev)
     d_rows = torch.zeros(max(1, m_fin), dtype=torch.int32, device=dev)
     d_st = torch.zeros(max(1, m_fin), dtype=torch.int32, device=dev)
     d_ln = torch.zeros(max(1, m_fin), dtype=torch.int32, device=dev)
-    samp = [torch.from_numpy(s.sampled).to(dev) for s in steps]
+    n_dev_steps = Wm + K + K_warm
+    samp = [torch.from_numpy(s.sampled).to(dev) for s in steps[:n_dev_steps]]
     fin = [(torch.from_numpy(s.finished).to(dev), torch.from_numpy(s.ingest_starts).to(dev),
             torch.from_numpy(s.ingest_lengths).to(dev), int(s.ingest_lengths.sum()),
             torch.from_numpy(s.finished.astype(np.int64)).to(dev),
             None if s.reset_tokens is None else torch.from_numpy(s.reset_tokens).to(dev),
-            torch.from_numpy(s.reset_n).to(dev)) for s in steps]
+            torch.from_numpy(s.reset_n).to(dev)) for s in steps[:n_dev_steps]]
     # the step, captured once: update + propose + ingest of the finished rows
-    # (one fused launch; the two calls when there is nothing to ingest)
-    fused = bool(m_fin and cfg.corpus_tokens)
+    ingest = bool(m_fin and cfg.corpus_tokens)
     g_step = torch.cuda.CUDAGraph()
     dr.propose_with_update(g_tok, g_n, d_samp, out=out)  # warm the launch path
     torch.cuda.synchronize()
+    l_cap = dr.launch_count()
     with torch.cuda.graph(g_step, stream=stream):
-        if fused:
+        if ingest:
             dr.step(g_tok, g_n, d_samp, d_rows, d_st, d_ln, out=out, stream=stream)
         else:
             dr.propose_with_update(g_tok, g_n, d_samp, out=out, stream=stream)
+    graph_kernels = dr.launch_count() - l_cap   # library kernels one replay runs
     g_tok.copy_(torch.from_numpy(tok))   # undo the warm-up update
     g_n.copy_(torch.from_numpy(n))
     props = torch.cuda.get_device_properties(dev)
@@ -223,10 +305,10 @@ def run_ours(args, rank, world, delta=0, backoff=1):
              # ring tokens placed since the current / the pending snapshot was linearised
              "since_front": 0, "since_pending": 0, "delta_tok": []}
 
-    def stage(i):
+    def stage(i, cold=True):
         """Outside the timed region: the previous step's finished rows restart
         (workload bookkeeping), this step's inputs land in the fixed buffers,
-        and L2 is flushed."""
+        and (cold) L2 is flushed."""
         if i > 0:
             _, _, _, _, idx, rt, rn = fin[i - 1]
             if idx.numel():
@@ -238,7 +320,8 @@ def run_ours(args, rank, world, delta=0, backoff=1):
             d_rows.copy_(rows)
             d_st.copy_(st_)
             d_ln.copy_(ln)
-        flush.fill_(i)
+        if cold:
+            flush.fill_(i)
 
     def policy(i):
         """Host side of the step: rebuild policy and the swap poll."""
@@ -260,8 +343,8 @@ def run_ours(args, rank, world, delta=0, backoff=1):
                 state["since_front"] = state["since_pending"]
                 state["build_stats"].append(dr.build_stats())
 
-    def one_step(i, ev=None):
-        stage(i)
+    def one_step(i, ev=None, cold=True, collect=False):
+        stage(i, cold)
         if ev:
             ev[0].record(stream)
         g_step.replay()
@@ -270,6 +353,8 @@ def run_ours(args, rank, world, delta=0, backoff=1):
         policy(i)
         if ev:
             ev[2].record(stream)
+        if collect and stats is not None:
+            stats.add()   # (after the events: device work of the statistics is not timed)
 
     for i in range(Wm):
         one_step(i)
@@ -285,13 +370,12 @@ def run_ours(args, rank, world, delta=0, backoff=1):
     b0 = state["builds"]
     t_wall = time.perf_counter()
     for j in range(K):
-        one_step(Wm + j, evs[j])
+        one_step(Wm + j, evs[j], collect=True)
     torch.cuda.synchronize()
     t_wall = time.perf_counter() - t_wall
     clocks = clk.stop()
     barrier(world)
     torch.cuda.synchronize()
-    graph_kernels = 1
     launches = dr.launch_count() - l0 + graph_kernels * K
     step_ms = [e[0].elapsed_time(e[2]) for e in evs]
     prop_ms = [e[0].elapsed_time(e[1]) for e in evs]
@@ -300,177 +384,108 @@ def run_ours(args, rank, world, delta=0, backoff=1):
     builds_in_region = state["builds"] - b0
     region_builds = state["build_stats"][nb0:]
     n_sum = int(g_n.sum().item())
+    peak, peak_kind = peaks()
+    ing_tok = float(np.mean([fin[Wm + j][3] for j in range(K)])) if ingest else 0.0
+    lower = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens, ing_tok)
+    prop_avg_s = float(np.mean(prop_ms)) / 1e3
+    row = stats.per_step() if stats is not None else None
+    full = None if row is None else int(lower + 36 * row["hits_scanned"] + row["gather_bytes"])
+    dev_bytes, pinned_bytes = dr.memory()
+    caller_bytes = (g_tok.numel() + g_n.numel() + d_samp.numel() + 3 * d_rows.numel()) * 4 + sum(
+        t.numel() * t.element_size() for t in (out.drafts, out.num_valid, out.score, out.probs,
+                                               out.match_info))
+    memory = {"context_device_bytes": int(dev_bytes), "context_pinned_bytes": int(pinned_bytes),
+              "caller_device_bytes": int(caller_bytes)}
+
+    def roofline(kernel, byts, traffic_key):
+        ach = byts / prop_avg_s / 1e9
+        return {"bound": "hbm", "kernel": kernel, "achieved": round(ach, 2), "peak": peak,
+                "unit": "GB/s", "frac": round(ach / peak, 4), "bytes_per_launch": int(byts),
+                "traffic": kernel_traffic(traffic_key), "avg_launch_us": round(prop_avg_s * 1e6, 2),
+                "peak_kind": peak_kind}
+
+    res = {"steps": K, "us_per_step": round(1e3 * total_ms_max / K, 2),
+           "steps_per_s": round(world * K / (total_ms_max / 1e3), 2),
+           "graph_us": _us(prop_ms), "kernels_per_step": int(graph_kernels),
+           "builds_in_timed_region": builds_in_region, "swaps_in_timed_region": len(region_builds),
+           "memory": memory, "clocks": clocks}
+    if row is not None:
+        res["row_stats"] = row
+        res["bytes_per_step"] = {"lower_bound": int(lower), "with_scans_and_gathers": full}
     if backoff > 1:
-        peak, peak_kind = peaks()
-        ing_tok = float(np.mean([fin[Wm + j][3] for j in range(K)])) if fused else 0.0
-        byts = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens, ing_tok)
-        prop_avg_s = float(np.mean(prop_ms)) / 1e3
-        ach = byts / prop_avg_s / 1e9
-        if state["pending"]:
-            dr.poll(wait=True, stream=stream)
-        dr.close()
-        return {"workload": "the serving loop above with num_backoff=%d: for support thresholds "
-                            "1..%d the t-th largest match length of each path is a candidate, "
-                            "every candidate voted, the best score wins (the update, the "
-                            "backoff kernel and the ingest as separate launches in the graph)"
-                            % (backoff, backoff),
-                "num_backoff": backoff, "steps": K,
-                "us_per_step": round(1e3 * total_ms_max / K, 2),
-                "steps_per_s": round(world * K / (total_ms_max / 1e3), 2),
-                "graph_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
-                             "median": round(1e3 * float(np.median(prop_ms)), 2),
-                             "p90": round(1e3 * float(np.percentile(prop_ms, 90)), 2)},
-                "roofline": {"bound": "hbm", "kernel": "backoff_kernel (with the update and ingest "
-                                                     "launches of the step)",
-                             "achieved": round(ach, 2), "peak": peak, "unit": "GB/s",
-                             "frac": round(ach / peak, 4), "bytes_per_launch": int(byts),
-                             "traffic": kernel_traffic("backoff_kernel"), "peak_kind": peak_kind},
-                "builds_in_timed_region": builds_in_region, "clocks": clocks}
-    if delta:
-        peak, peak_kind = peaks()
-        ing_tok = float(np.mean([fin[Wm + j][3] for j in range(K)])) if fused else 0.0
+        res["roofline"] = roofline("backoff_kernel (with the update and ingest launches of the "
+                                   "step)", lower, "backoff_kernel")
+    elif delta:
         dv = float(np.mean(state["delta_tok"][Wm:Wm + K]))
+        res["mean_delta_tokens"] = round(dv, 1)
         # the delta is read from HBM once per step (every row then finds it in L2)
-        byts = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens, ing_tok) + 4 * dv
-        prop_avg_s = float(np.mean(prop_ms)) / 1e3
-        ach = byts / prop_avg_s / 1e9
+        res["roofline"] = roofline("propose_kernel", full + 4 * dv, "propose_kernel_delta")
+    else:
+        res["roofline"] = roofline("propose_kernel", full,
+                                   "propose_kernel" if cfg_name == "c3" else "propose_kernel_c5")
+        res["roofline"]["bytes_lower_bound"] = int(lower)
+    if not headline:
         if state["pending"]:
             dr.poll(wait=True, stream=stream)
         dr.close()
-        return {"workload": "the serving loop above with delta_capacity=%d: the docs ingested "
-                            "since the current snapshot was linearised are matched too (every "
-                            "delta position accounted for; each row reads the ring windows "
-                            "whose gram signature can hold an end that matters)" % delta,
-                "delta_capacity": delta, "steps": K, "mean_delta_tokens": round(dv, 1),
-                "us_per_step": round(1e3 * total_ms_max / K, 2),
-                "steps_per_s": round(world * K / (total_ms_max / 1e3), 2),
-                "propose_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
-                               "median": round(1e3 * float(np.median(prop_ms)), 2),
-                               "p90": round(1e3 * float(np.percentile(prop_ms, 90)), 2)},
-                "roofline": {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 2),
-                             "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-                             "bytes_per_launch": int(byts),
-                             "traffic": kernel_traffic("propose_kernel_delta"), "peak_kind": peak_kind},
-                "builds_in_timed_region": builds_in_region, "clocks": clocks}
+        return res
+
+    # warm: the same step back to back, no flush between steps
+    evw = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K_warm)]
+    for j in range(K_warm):
+        one_step(Wm + K + j, evw[j], cold=False)
+    torch.cuda.synchronize()
+    warm_ms = [e[0].elapsed_time(e[2]) for e in evw]
+    res["warm"] = {"steps": K_warm, "us_per_step": round(1e3 * float(np.mean(warm_ms)), 2),
+                   "graph_us": _us([e[0].elapsed_time(e[1]) for e in evw]),
+                   "l2": "not flushed: steps back to back"}
+    # latency floor: one graph holding one minimal kernel, between the same events
+    tiny = torch.zeros(1, dtype=torch.int32, device=dev)
+    g_tiny = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_tiny, stream=stream):
+        tiny.fill_(1)
+    floor = {}
+    for mode in ("cold", "warm"):
+        ms = []
+        for j in range(64):
+            if mode == "cold":
+                flush.fill_(j)
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g_tiny.replay()
+            e1.record(stream)
+            torch.cuda.synchronize()
+            ms.append(e0.elapsed_time(e1))
+        floor[mode] = _us(ms)
+    res["latency_floor_us"] = {"what": "one CUDA graph of one minimal kernel replayed between "
+                                       "the step's CUDA events", **floor}
     # e2e: host buffers through the public API, copies inside the timed region
     if state["pending"]:
         dr.poll(wait=True, stream=stream)
         state["pending"] = False
-    e2e = e2e_leg(args, dr, cfg, steps, Wm + K, K_e2e, g_tok, g_n, out, flush, side, state, dev,
-                  stream)
-    dr.close()
-    # suffix-array builds, standalone (the suffix-array workload)
-    sa = sa_build_leg(args, dev)
-    peak, peak_kind = peaks()
-    ing_tok = float(np.mean([fin[Wm + j][3] for j in range(K)])) if fused else 0.0
-    byts = algorithmic_bytes_propose(n_sum, cfg.B, cfg.T, cfg.k, cfg.corpus_tokens, ing_tok)
-    prop_avg_s = float(np.mean(prop_ms)) / 1e3
-    ach = byts / prop_avg_s / 1e9
-    rl_prop = {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 2),
-               "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-               "traffic": kernel_traffic("propose_kernel"),
-               "bytes_per_launch": int(byts), "avg_launch_us": round(prop_avg_s * 1e6, 2),
-               "peak_kind": peak_kind}
-    # GPU time of the background builds that finished inside the region
+    res["e2e"] = e2e_leg(dr, cfg, steps, Wm + K + K_warm, K_e2e, g_tok, g_n, flush, side, state,
+                         dev, stream)
     pass_ms = float(sum(b["pass_ms"] for b in region_builds))
     pass_elems = int(sum(b["pass_elems"] for b in region_builds))
     n_passes = int(sum(b["passes"] for b in region_builds))
-    kernels = {"propose_kernel": {"launches": K, "total_ms": round(float(np.sum(prop_ms)), 3)},
-               "k_onesweep (side stream)": {"launches": n_passes, "total_ms": round(pass_ms, 3)}}
-    rl = rl_prop
+    res["kernels"] = {"propose_kernel": {"launches": K, "total_ms": round(float(np.sum(prop_ms)), 3)},
+                      "k_onesweep (side stream)": {"launches": n_passes, "total_ms": round(pass_ms, 3)}}
+    res["gpu_launches"] = int(launches)
+    res["wall_s_timed_region"] = round(t_wall, 4)
+    res["roofline_propose"] = res["roofline"]
     if pass_ms > float(np.sum(prop_ms)) and n_passes:
         ach_p = 24.0 * pass_elems / (pass_ms / 1e3) / 1e9
-        rl = {"bound": "hbm", "kernel": "k_onesweep", "achieved": round(ach_p, 2), "peak": peak,
-              "unit": "GB/s", "frac": round(ach_p / peak, 4),
-              "traffic": kernel_traffic("k_onesweep", pass_elems / n_passes),
-              "bytes_per_launch": int(24 * pass_elems / n_passes),
-              "avg_launch_us": round(1e3 * pass_ms / n_passes, 2), "peak_kind": peak_kind}
-    value = world * K / (total_ms_max / 1e3)
-    res = {
-        "metric": METRIC, "value": round(value, 2), "unit": "steps/s", "n_gpus": world,
-        "steps": K, "warmup": Wm, "ms_per_step": round(total_ms_max / K, 5),
-        "us_per_step": round(1e3 * total_ms_max / K, 2),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
-        "data": "synthetic",
-        "config": dict(workload_config(cfg, world),
-                   l2="flushed before every timed step (%d MiB write)" % (flush.numel() * 4 >> 20),
-                   launch="each step replays one CUDA graph: the fused sgd_step launch "
-                          "(update + propose + ingest) on a highest-priority stream; "
-                          "rebuilds on a lowest-priority side stream"),
-        "roofline": rl, "roofline_propose": rl_prop, "kernels": kernels,
-        "propose_us": {"mean": round(1e3 * float(np.mean(prop_ms)), 2),
-                       "median": round(1e3 * float(np.median(prop_ms)), 2),
-                       "p90": round(1e3 * float(np.percentile(prop_ms, 90)), 2)},
-        "builds_in_timed_region": builds_in_region,
-        "wall_s_timed_region": round(t_wall, 4),
-        "e2e": e2e, "gpu_launches": int(launches), "clocks": clocks, "sa_build": sa,
-    }
+        res["roofline"] = {"bound": "hbm", "kernel": "k_onesweep", "achieved": round(ach_p, 2),
+                           "peak": peak, "unit": "GB/s", "frac": round(ach_p / peak, 4),
+                           "traffic": kernel_traffic("k_onesweep", pass_elems / n_passes),
+                           "bytes_per_launch": int(24 * pass_elems / n_passes),
+                           "avg_launch_us": round(1e3 * pass_ms / n_passes, 2),
+                           "peak_kind": peak_kind}
+    dr.close()
     return res
 
 
-def long_context_leg(args, rank):
-    """Propose steps of the long-context workload (B=1024, S=32768, 4M-token
-    corpus, k=32, D=32): the per-row scans dominate, so this is where the
-    propose kernel meets the HBM roofline.  Each step: L2 flush (untimed),
-    propose_with_update timed with CUDA events."""
-    import torch
-    from model_free_suffix_gb300 import SuffixDrafter
-    from model_free_suffix_gb300 import workload as W
-    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-    cfg = W.CONFIGS["c5"]
-    K, Wm = args.long_context_steps, 3
-    tr = W.ServingTrace(cfg, seed=rank, steps=K + Wm, finish_frac=0.0)
-    tok, n = tr.initial()
-    steps = [tr.next_step() for _ in range(K + Wm)]
-    dr = SuffixDrafter(max_batch=cfg.B, seq_capacity=cfg.S, vocab_size=cfg.V, k=cfg.k,
-                       max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
-                       corpus_capacity=cfg.corpus_tokens, device=dev.index)
-    docs, lens = W.corpus_docs(cfg, seed=rank, capacity=cfg.corpus_tokens, pool=tr.pool)
-    chunk = 512
-    for s0 in range(0, docs.shape[0], chunk):
-        d = docs[s0:s0 + chunk]
-        m = d.shape[0]
-        buf = torch.full((m, cfg.S), -1, dtype=torch.int32, device=dev)
-        buf[:, :d.shape[1]] = torch.from_numpy(d).to(dev)
-        dr.ingest(buf, torch.arange(m, dtype=torch.int32, device=dev),
-                  torch.zeros(m, dtype=torch.int32, device=dev),
-                  torch.from_numpy(np.ascontiguousarray(lens[s0:s0 + chunk])).to(dev))
-        del buf
-    side = torch.cuda.Stream(device=dev)
-    dr.build_sa(side)
-    assert dr.poll(wait=True)[0] == 1
-    g_tok = torch.from_numpy(tok).to(dev)
-    g_n = torch.from_numpy(n).to(dev)
-    out = dr.new_outputs(cfg.B)
-    samp = [torch.from_numpy(s.sampled).to(dev) for s in steps]
-    flush = torch.empty(256 << 20 >> 2, dtype=torch.int32, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    ms, sum_n = [], []
-    for i in range(K + Wm):
-        flush.fill_(i)
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        dr.propose_with_update(g_tok, g_n, samp[i], out=out)
-        e1.record(stream)
-        torch.cuda.synchronize()
-        if i >= Wm:
-            ms.append(e0.elapsed_time(e1))
-            sum_n.append(int(g_n.sum().item()))
-    dr.close()
-    peak, peak_kind = peaks()
-    byts = algorithmic_bytes_propose(int(np.mean(sum_n)), cfg.B, cfg.T, cfg.k, cfg.corpus_tokens)
-    avg = float(np.mean(ms)) / 1e3
-    ach = byts / avg / 1e9
-    return {"workload": "c5: B=1024, S=32768, num_tokens U[8192,32768], Zipf(1.1) over 151936, "
-                        "p=0.8 repeats of 1024 spans 32-512, k=32, D=32, R=64, T=33, 4M-token corpus",
-            "steps": K, "propose_us": round(avg * 1e6, 2), "steps_per_s": round(1.0 / avg, 2),
-            "roofline": {"bound": "hbm", "kernel": "propose_kernel", "achieved": round(ach, 1),
-                         "peak": peak, "unit": "GB/s", "frac": round(ach / peak, 4),
-                         "bytes_per_launch": int(byts), "peak_kind": peak_kind},
-            "l2": "flushed before every timed step"}
-
-
-def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state, dev, stream):
+def e2e_leg(dr, cfg, steps, first, K, g_tok, g_n, flush, side, state, dev, stream):
     """Same steps through the public API with pinned host buffers
     (SuffixDrafter.step_host): each step copies its sampled ids and ingest
     arguments host->device and reads the drafts and valid counts back, all
@@ -497,7 +512,6 @@ def e2e_leg(args, dr, cfg, steps, first, K, g_tok, g_n, out, flush, side, state,
     times = []
     bi = bo = 0
     for j in range(K):
-        s = steps[first + j]
         if first + j > 0:
             p = steps[first + j - 1]
             if p.finished.shape[0]:
@@ -559,9 +573,13 @@ def sa_build_leg(args, dev, sizes=None):
         r_pass = pass_bytes / (best["pass_ms"] / 1e3) / 1e9 if best["pass_ms"] > 0 else None
         r_all = best["model_bytes"] / (best["ms"] / 1e3) / 1e9
         out["%dM" % (N >> 20)] = {
+            "workload": "suffix-array workload: %d int32 tokens, docs of 64-512 Zipf(1.1) tokens "
+                        "over 151936 each followed by the sentinel, 30%% repeats of 512 spans "
+                        "of 32-256" % N,
             "n": N, "ms": round(best["ms"], 3), "mtok_s": round(N / best["ms"] / 1e3, 1),
             "rounds": best["rounds"], "passes": best["passes"],
             "sorted_elems": best["sorted_elems"],
+            "model_bytes": int(best["model_bytes"]),
             "model_gbs": round(r_all, 1), "model_frac": round(r_all / peak, 4),
             "radix_pass": {"bound": "hbm", "achieved": None if r_pass is None else round(r_pass, 1),
                            "peak": peak, "unit": "GB/s",
@@ -577,14 +595,125 @@ def sa_build_leg(args, dev, sizes=None):
     return out
 
 
+def sa_concurrent_leg(args, dev, N):
+    """Drafting steps while a suffix-array build runs on a side stream.
+
+    A context over the N-token suffix-array workload (its docs ingested, the
+    first snapshot built) drafts the serving rows (B=256, S=4096, k=16) with
+    one captured graph per step.  Timed per step (L2 flushed before each):
+    steps with no build in flight; then a build started on a lowest-priority
+    side stream and steps back to back, each followed by a non-blocking poll,
+    until the poll swaps the new snapshot in.  Reported: step us without and
+    with the build, the build's wall time from the call to the swap, its own
+    GPU time, and the swap (the poll that swaps: host us and the GPU time of
+    its descriptor write on the drafting stream).  The graph was captured
+    before the swap and keeps running after it (the descriptor's address does
+    not change)."""
+    import torch
+    from model_free_suffix_gb300 import SuffixDrafter
+    from model_free_suffix_gb300 import workload as W
+    cfg = W.CONFIGS["c3"]
+    X = W.sa_corpus(N, seed=0)
+    docs, lens = W.docs_from_text(X, cfg.V)
+    dr = SuffixDrafter(max_batch=cfg.B, seq_capacity=cfg.S, vocab_size=cfg.V, k=cfg.k,
+                       max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
+                       corpus_capacity=N, device=dev.index)
+    least, greatest = torch.cuda.Stream.priority_range()
+    stream = torch.cuda.Stream(device=dev, priority=greatest)
+    side = torch.cuda.Stream(device=dev, priority=least)
+    torch.cuda.set_stream(stream)
+    chunk = 2048
+    for s0 in range(0, docs.shape[0], chunk):
+        d = docs[s0:s0 + chunk]
+        m = d.shape[0]
+        buf = torch.full((m, cfg.S), -1, dtype=torch.int32, device=dev)
+        buf[:, :d.shape[1]] = torch.from_numpy(d).to(dev)
+        dr.ingest(buf, torch.arange(m, dtype=torch.int32, device=dev),
+                  torch.zeros(m, dtype=torch.int32, device=dev),
+                  torch.from_numpy(np.ascontiguousarray(lens[s0:s0 + chunk])).to(dev))
+        del buf
+    dr.build_sa(side, stream=stream)
+    assert dr.poll(wait=True, stream=stream)[0] == 1
+    # the rows are not updated: every step drafts the same batch, so the steps
+    # before, during and after the build do identical work
+    tr = W.ServingTrace(cfg, seed=0, steps=1)
+    tok, n = tr.initial()
+    g_tok, g_n = torch.from_numpy(tok).to(dev), torch.from_numpy(n).to(dev)
+    out = dr.new_outputs(cfg.B)
+    dr.propose(g_tok, g_n, out=out)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        dr.propose(g_tok, g_n, out=out, stream=stream)
+    flush = torch.empty(256 << 20 >> 2, dtype=torch.int32, device=dev)
+    counter = [0]
+
+    def step():
+        counter[0] += 1
+        flush.fill_(counter[0])
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        return e0, e1
+
+    for _ in range(3):
+        step()
+    torch.cuda.synchronize()
+    idle = [step() for _ in range(args.concurrent_steps)]
+    torch.cuda.synchronize()
+    idle_ms = [a.elapsed_time(b) for a, b in idle]
+    gen0 = dr.poll(wait=False, stream=stream)[1]
+    # the build, and steps until its swap
+    busy, swap = [], None
+    t0 = time.perf_counter()
+    dr.build_sa(side, stream=stream)
+    for _ in range(args.concurrent_max_steps):
+        busy.append(step())
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ea.record(stream)
+        h0 = time.perf_counter()
+        st, gen = dr.poll(wait=False, stream=stream)
+        h1 = time.perf_counter()
+        eb.record(stream)
+        if st == 1:
+            swap = (h1 - t0, h1 - h0, ea, eb, gen)
+            break
+    torch.cuda.synchronize()
+    busy_ms = [a.elapsed_time(b) for a, b in busy]
+    after = [step() for _ in range(32)]
+    torch.cuda.synchronize()
+    after_ms = [a.elapsed_time(b) for a, b in after]
+    bs = dr.build_stats()
+    if swap is None:
+        dr.poll(wait=True, stream=stream)
+    res = {"workload": "serving rows (B=256, S=4096, k=16, D=24, R=64) drafting over the "
+                       "suffix-array workload's %d-token corpus; one captured propose graph "
+                       "per step (the same rows every step), L2 flushed before each" % N,
+           "n": N, "step_us_no_build": _us(idle_ms),
+           "step_us_during_build": _us(busy_ms) if busy_ms else None,
+           "steps_during_build": len(busy_ms),
+           "step_us_after_swap": _us(after_ms) if after_ms else None,
+           "build_gpu_ms": round(bs["ms"], 3)}
+    if swap is not None:
+        res["build_wall_ms"] = round(1e3 * swap[0], 3)
+        res["swap"] = {"poll_host_us": round(1e6 * swap[1], 2),
+                       "poll_gpu_us": round(1e3 * swap[2].elapsed_time(swap[3]), 2),
+                       "generation": [int(gen0), int(swap[4])]}
+    dr.close()
+    del flush
+    torch.cuda.empty_cache()
+    return res
+
+
 # ---------------------------------------------------------------------------
-def cpu_oracle_leg(cfg, seconds, rank=0):
-    """The CPU oracle as it stands, on the same workload, rows spread over all
-    host cores; a bounded sample of steps."""
+def cpu_oracle_leg(cfg, seconds, rank=0, threads=None):
+    """The CPU oracle as it stands, on the same workload, rows spread over
+    `threads` host threads (all cores by default); a bounded sample of steps."""
     from oracle import oracle as O
     from model_free_suffix_gb300 import workload as W
     O.build()
-    threads = os.cpu_count() or 1
+    threads = threads or os.cpu_count() or 1
     tr, tok, n, steps = make_steps(cfg, seed=rank, n_steps=400)
     ring, X = None, None
     if cfg.corpus_tokens:
@@ -613,8 +742,26 @@ def cpu_oracle_leg(cfg, seconds, rank=0):
             break
     el = time.perf_counter() - t0
     return {"value": round(done / el, 3), "unit": "steps/s", "cores": threads, "kind": "oracle",
+            "us_per_step": round(1e6 * el / done, 1),
             "sample": "%d steps of the same workload (update + propose of all %d rows + ingest; "
                       "no suffix-array rebuild in the sample), %.1f s" % (done, cfg.B, el)}
+
+
+def cpu_sa_leg(sizes):
+    """The oracle's naive suffix array (a comparison sort of every suffix, one
+    thread) on the suffix-array workload."""
+    from oracle import oracle as O
+    from model_free_suffix_gb300 import workload as W
+    O.build()
+    out = {}
+    for N in sizes:
+        X = W.sa_corpus(N, seed=0)
+        t0 = time.perf_counter()
+        O.suffix_array(X)
+        el = time.perf_counter() - t0
+        out["%dM" % (N >> 20)] = {"n": N, "s": round(el, 3), "mtok_s": round(N / el / 1e6, 3),
+                                  "cores": 1, "kind": "oracle naive comparison sort"}
+    return out
 
 
 # ---------------------------------------------------------------------------
@@ -640,22 +787,27 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=512)
     ap.add_argument("--e2e-steps", type=int, default=256)
+    ap.add_argument("--warm-steps", type=int, default=128)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", default="c3")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--cpu-single-seconds", type=float, default=6.0)
     ap.add_argument("--no-sa16m", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--long-context-steps", type=int, default=16,
-                    help="steps of the long-context workload timed as a secondary line (0: skip)")
+    ap.add_argument("--long-context-steps", type=int, default=64,
+                    help="steps of the long-context serving loop, a secondary line (0: skip)")
     ap.add_argument("--sa-only", type=int, default=0,
                     help="only time suffix-array builds of this many tokens and print them")
     ap.add_argument("--backoff-steps", type=int, default=64,
                     help="steps of the serving loop with num_backoff=8, a secondary line (0: skip)")
     ap.add_argument("--delta-steps", type=int, default=256,
                     help="steps of the serving loop with the delta scan on, a secondary line (0: skip)")
+    ap.add_argument("--concurrent-steps", type=int, default=64,
+                    help="steps timed with no build in flight in the concurrent-build line (0: skip)")
+    ap.add_argument("--concurrent-max-steps", type=int, default=4096)
     ap.add_argument("--long-only", action="store_true",
-                    help="only time the long-context workload and print its line")
+                    help="only time the long-context serving loop and print its line")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -685,27 +837,56 @@ def main():
         return
     from __graft_entry__ import build
     build()
+    import torch
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
     if args.sa_only:
-        import torch
-        dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
-        torch.cuda.set_device(dev)
         if rank == 0:
             print(json.dumps(sa_build_leg(args, dev, sizes=[args.sa_only])), flush=True)
         return
     if args.long_only:
+        r = serve_loop(args, rank, world, "c5", K=args.long_context_steps, Wm=3)
         if rank == 0:
-            print(json.dumps(long_context_leg(args, rank)), flush=True)
+            print(json.dumps(r), flush=True)
         return
-    res = run_ours(args, rank, world)
-    if args.delta_steps > 0 and args.config == "c3":
-        res["delta"] = run_ours(args, rank, world, delta=cfg.rebuild_tokens)
-    if args.backoff_steps > 0 and args.config == "c3":
-        res["backoff"] = run_ours(args, rank, world, backoff=8)
-    if args.long_context_steps > 0 and args.config == "c3":
-        res["long_context"] = long_context_leg(args, rank)
+    h = serve_loop(args, rank, world, args.config, headline=True)
+    K = args.steps
+    res = {
+        "metric": METRIC, "value": h["steps_per_s"], "unit": "steps/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round(h["us_per_step"] / 1e3, 5),
+        "us_per_step": h["us_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int32",
+        "data": "synthetic", "config": workload_config(cfg, world), "timing": TIMING_NOTE,
+    }
+    res.update({k: v for k, v in h.items() if k not in ("steps", "us_per_step", "steps_per_s")})
+    if args.config == "c3":
+        if args.delta_steps > 0:
+            res["delta"] = dict(workload="the serving loop above with delta_capacity=%d: the docs "
+                                         "ingested since the current snapshot was linearised are "
+                                         "matched too" % cfg.rebuild_tokens,
+                                **serve_loop(args, rank, world, "c3", delta=cfg.rebuild_tokens,
+                                             K=args.delta_steps))
+        if args.backoff_steps > 0:
+            res["backoff"] = dict(workload="the serving loop above with num_backoff=8: for support "
+                                           "thresholds 1..8 the t-th largest match length of each "
+                                           "path is a candidate, every candidate voted, the best "
+                                           "score wins",
+                                  **serve_loop(args, rank, world, "c3", backoff=8,
+                                               K=args.backoff_steps))
+        if args.long_context_steps > 0:
+            res["long_context"] = dict(workload=WORKLOADS["c5"],
+                                       **serve_loop(args, rank, world, "c5",
+                                                    K=args.long_context_steps, Wm=3))
+    res["sa_build"] = sa_build_leg(args, dev)
+    if args.concurrent_steps > 0:
+        res["sa_concurrent"] = {("%dM" % (N >> 20)): sa_concurrent_leg(args, dev, N)
+                                for N in ([1 << 20] + ([] if args.no_sa16m else [1 << 24]))}
     if rank == 0:
         if not args.no_cpu_baseline:
-            res["cpu_baseline"] = cpu_oracle_leg(cfg, args.cpu_seconds)
+            cb = cpu_oracle_leg(cfg, args.cpu_seconds)
+            cb["single_thread"] = cpu_oracle_leg(cfg, args.cpu_single_seconds, threads=1)
+            cb["naive_suffix_array"] = cpu_sa_leg([1 << 20] + ([] if args.no_sa16m else [1 << 24]))
+            res["cpu_baseline"] = cb
         print(json.dumps(res), flush=True)
     if world > 1:
         import torch.distributed as dist

@@ -395,6 +395,23 @@ int sgd_debug_inject(sgd_ctx *ctx, int what);
 /* Kernel launches the context made since creation (every library kernel). */
 int sgd_launch_count(sgd_ctx *ctx, uint64_t *count);
 
+/* Per-row statistics of the drafting launches made after this call, for
+ * measuring the bytes a step touched (SuffixGPU (PyPI), How it works, steps
+ * 2-3: the suffix-array hits scanned and the continuations gathered).
+ *   row_stats: caller-owned DEVICE int32 [max_batch, 4], 16-byte aligned, or
+ *   null to stop.  Each launch of the default drafting kernel (num_backoff =
+ *   1) writes, for every row b < B: [4b] the suffix-array hits the corpus
+ *   probe scanned (every level evaluated), [4b+1] the occurrences that voted
+ *   (c0), [4b+2] the draft cap, [4b+3] the source (0 none, 1 row, 2 corpus).
+ * The pointer is read when a call is made, so a CUDA graph captured after
+ * this call keeps writing to it.  SGD_EINVAL for an unaligned buffer. */
+int sgd_set_row_stats(sgd_ctx *ctx, int32_t *row_stats);
+
+/* Memory the context allocated at sgd_create (it allocates nothing later):
+ * device bytes (ring, both snapshots with their indexes, sort scratch,
+ * staging) and page-locked host bytes.  Either pointer may be null. */
+int sgd_memory(sgd_ctx *ctx, int64_t *device_bytes, int64_t *pinned_bytes);
+
 const char *sgd_strerror(int status);
 int sgd_version(void); /* major * 10000 + minor * 100 + patch */
 

@@ -127,6 +127,8 @@ def load() -> ctypes.CDLL:
         "sgd_build_stats": (ctypes.c_int, [P, ctypes.POINTER(SgdBuildInfo)]),
         "sgd_debug_inject": (ctypes.c_int, [P, ctypes.c_int]),
         "sgd_launch_count": (ctypes.c_int, [P, u64p]),
+        "sgd_set_row_stats": (ctypes.c_int, [P, P]),
+        "sgd_memory": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(L, name)

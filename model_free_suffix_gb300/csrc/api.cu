@@ -44,6 +44,9 @@ struct sgd_ctx {
   int32_t *d_hin = nullptr;         // sgd_step_host inputs: sampled, rows, starts, lengths
   int32_t *d_hout = nullptr;        // sgd_step_host outputs: drafts, num_valid, score, probs, match_info
   int32_t *d_self_res = nullptr;    // two-launch propose: per-row self results
+  int32_t *d_row_stats = nullptr;   // caller's [max_batch, 4] statistics buffer, or null
+  int64_t dev_bytes = 0;            // device memory the context allocated
+  int64_t pinned_bytes = 0;         // page-locked host memory the context allocated
   // sgd_step_host: the last set of host buffers checked for in-place access
   const void *zc_key[9] = {};
   void *zc_dev[9] = {};
@@ -336,6 +339,7 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
   cudaError_t e = cudaSuccess;
   auto al = [&](void **p, size_t bytes) {
     if (e == cudaSuccess) e = cudaMalloc(p, bytes);
+    if (e == cudaSuccess) x->dev_bytes += (int64_t)bytes;
   };
   al((void **)&x->d_err, 4);
   al((void **)&x->d_build_err, 4);
@@ -392,6 +396,10 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
       if (e == cudaSuccess) e = cudaMemset(x->d_sig, 0, (size_t)(C / WIN) * SIG_WORDS * 4);
     }
     if (e == cudaSuccess) e = sa_scratch_alloc(&x->sa, C);
+    if (e == cudaSuccess) {
+      x->dev_bytes += (int64_t)sa_scratch_bytes(C);
+      x->pinned_bytes += 64 + 8 * 256 * 4 + 8 + 4;  // the sort's read-back words, h_n, h_err
+    }
     if (e == cudaSuccess) e = cudaMemset(x->d_rs, 0, sizeof(RingState));
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_start, 0, (size_t)cfg->max_docs * 8);
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_len, 0, (size_t)cfg->max_docs * 4);
@@ -468,6 +476,7 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.self_res = x->d_self_res;
   a.by_score = c.select_by_score;
   a.nb = c.num_backoff;
+  a.row_stats = x->d_row_stats;
   if (c.draft_mode == 1) {  // no probability floor: the vote runs while an occurrence continues
     a.fixed = 1;
     a.pN = 0;
@@ -1052,6 +1061,20 @@ int sgd_debug_inject(sgd_ctx *x, int what) {
     x->bstate = B_DONE;
     x->cv.notify_all();
   }
+  return SGD_OK;
+}
+
+int sgd_set_row_stats(sgd_ctx *x, int32_t *row_stats) {
+  if (!x) return SGD_EINVAL;
+  if (row_stats && !aligned16(row_stats)) return SGD_EINVAL;
+  x->d_row_stats = row_stats;
+  return SGD_OK;
+}
+
+int sgd_memory(sgd_ctx *x, int64_t *device_bytes, int64_t *pinned_bytes) {
+  if (!x) return SGD_EINVAL;
+  if (device_bytes) *device_bytes = x->dev_bytes;
+  if (pinned_bytes) *pinned_bytes = x->pinned_bytes;
   return SGD_OK;
 }
 

@@ -1227,6 +1227,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ int s_dstate[MAX_SELF_WARPS];  // per self warp: its delta (length << 16 | ends)
   __shared__ int s_dcB, s_dcN, s_dmore;     // the CTA's delta list: length, ends; another round
   __shared__ uint32_t s_ep;
+  __shared__ int s_scan;  // suffix-array hits the probe warps scanned (row statistics)
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
   const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
@@ -1328,6 +1329,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_cpf = 0;
       s_ckey = 0;
       s_ep = e0;
+      s_scan = 0;
       s_best_delta = 0;
       for (int w = 0; w < MAX_SELF_WARPS; ++w) s_dstate[w] = 0;
       s_dcB = 0;
@@ -1365,6 +1367,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         a.num_valid[b] = 0;
         if (a.score) a.score[b] = 0.f;
         if (a.match_info) { a.match_info[2 * b] = 0; a.match_info[2 * b + 1] = 0; }
+        if (a.row_stats) *reinterpret_cast<int4 *>(a.row_stats + 4 * (size_t)b) = make_int4(0, 0, 0, 0);
       }
     }
     return;
@@ -1608,6 +1611,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       if (D >= 4 && n >= 4 && s_bound[1] > s_bound[0] && pms < dl) {
         for (int i = ptid; i <= MAX_D; i += pthr) s_lhist[i] = 0;
         probe_sync();
+        if (ptid == 0) s_scan += (int)min(s_bound[1] - s_bound[0], (long long)INT_MAX);
         p4ctx = p4_ctx_fits(s_bound[1] - s_bound[0], cp.Rec ? cp.rs.ri : k + dl - 4);
         if (p4ctx)
           scan_p4_ctx(cp, Z, s_bound[0], s_bound[1], s_tail, n, D, k, s_L, s_e4, s_ctx, s_lhist,
@@ -1638,7 +1642,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
           if (pms >= lv) break;
         }
         probe_sync();  // s_q from an earlier level has been read
-        if (ptid == 0) s_q = 0;
+        if (ptid == 0) {
+          s_q = 0;
+          s_scan = (int)min((long long)s_scan + (h0 - l0), (long long)INT_MAX);
+        }
         probe_sync();
         // one pass: count the valid hits and keep their ends on chip (while
         // they fit); a warp takes its slots with one shared atomic per batch
@@ -1966,6 +1973,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     a.num_valid[b] = a.fixed ? k : len;
     if (a.score) a.score[b] = cw > 0 ? (float)sum / (float)cw : 0.f;
     if (a.match_info) { a.match_info[2 * b] = M; a.match_info[2 * b + 1] = src; }
+    if (a.row_stats)
+      *reinterpret_cast<int4 *>(a.row_stats + 4 * (size_t)b) =
+          make_int4(s_scan, cw, src == 1 && both ? cap_s : cap, src);
   }
 }
 

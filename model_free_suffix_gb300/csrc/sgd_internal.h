@@ -161,6 +161,9 @@ struct ProposeArgs {
   int by_score;
   // multi-length backoff: candidate lengths per path (> 1: backoff.cu)
   int nb;
+  // [B, 4] or null: per row, the suffix-array hits the corpus probe scanned,
+  // the occurrences that voted (c0), the draft cap and the source (0/1/2)
+  int32_t *row_stats;
 };
 
 __host__ __device__ constexpr int self_res_ints(int R) { return 2 * R + 10; }

@@ -326,6 +326,25 @@ class SuffixDrafter:
     def debug_inject(self, what: int) -> None:
         self._check(self._lib.sgd_debug_inject(self._h, int(what)), "sgd_debug_inject")
 
+    def set_row_stats(self, row_stats: Optional[torch.Tensor]) -> None:
+        """Per-row statistics of later drafting launches into `row_stats`
+        (int32 [max_batch, 4] on the device: hits scanned, c0, cap, source),
+        or None to stop.  The tensor must outlive the launches (and graphs)
+        that write it."""
+        if row_stats is not None:
+            assert row_stats.dtype == torch.int32 and row_stats.is_cuda and row_stats.is_contiguous()
+            assert row_stats.numel() >= 4 * self.cfg.max_batch
+        self._row_stats = row_stats
+        self._check(self._lib.sgd_set_row_stats(
+            self._h, ctypes.c_void_p(row_stats.data_ptr() if row_stats is not None else 0)),
+            "sgd_set_row_stats")
+
+    def memory(self) -> Tuple[int, int]:
+        """(device bytes, page-locked host bytes) the context allocated."""
+        d, h = ctypes.c_int64(), ctypes.c_int64()
+        self._check(self._lib.sgd_memory(self._h, ctypes.byref(d), ctypes.byref(h)), "sgd_memory")
+        return int(d.value), int(h.value)
+
     def launch_count(self) -> int:
         c = ctypes.c_uint64()
         self._check(self._lib.sgd_launch_count(self._h, ctypes.byref(c)), "sgd_launch_count")
