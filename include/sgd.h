@@ -157,6 +157,24 @@ typedef struct {
                                   tokens, every delta position), so this mode costs one
                                   more launch per step and a scan of the whole
                                   suffix-array interval of the row's last two tokens. */
+  int32_t  row_index;          /* 0 (default): each step scans every row's valid tokens
+                                  for its own match.  1: each row also keeps a bigram
+                                  position index on the device (the per-request
+                                  structure of the [RFC] Summary), kept current by every
+                                  update, so that a step reads only the earlier
+                                  positions of the row's last two tokens, extended
+                                  backwards, instead of the whole row; a row whose
+                                  last bigram occurs more than 12 times, or not at all
+                                  when the corpus has no match of 2 or more, is still
+                                  scanned.  Drafts are the same either way.  The
+                                  caller must call sgd_reset_rows for every row it
+                                  writes other than through this library's updates
+                                  (a new request in a row, rows written before the
+                                  first step); a row whose length changed unseen is
+                                  scanned until it is reset.  Requires propose_mode 0,
+                                  delta_capacity 0, select_by_score 0, num_backoff 1
+                                  and vocab_size <= 2^24; 64 * next_pow2(2 S) bytes
+                                  per row (max_batch rows). */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)
@@ -402,10 +420,27 @@ int sgd_launch_count(sgd_ctx *ctx, uint64_t *count);
  *   null to stop.  Each launch of the default drafting kernel (num_backoff =
  *   1) writes, for every row b < B: [4b] the suffix-array hits the corpus
  *   probe scanned (every level evaluated), [4b+1] the occurrences that voted
- *   (c0), [4b+2] the draft cap, [4b+3] the source (0 none, 1 row, 2 corpus).
+ *   (c0), [4b+2] the draft cap, [4b+3] the source (0 none, 1 row, 2 corpus)
+ *   plus 256 times how the row's own match was found: 0 by a scan of the
+ *   row, 1 from its bigram index (row_index), 2 not needed (row_index: the
+ *   row's last bigram occurs nowhere earlier and the corpus matched >= 2).
  * The pointer is read when a call is made, so a CUDA graph captured after
  * this call keeps writing to it.  SGD_EINVAL for an unaligned buffer. */
 int sgd_set_row_stats(sgd_ctx *ctx, int32_t *row_stats);
+
+/* Starts the bigram position indexes of rows[0, m) over from the rows'
+ * current contents (row_index = 1; no-op otherwise).  Call it after writing a
+ * row other than through sgd_update_state / sgd_propose_with_update /
+ * sgd_step: a new request placed in a row, and every row before its first
+ * step.  Until then such a row is scanned, and a row rewritten with the same
+ * length as before would be matched against stale positions.
+ *   token_ids DEVICE int32 [>= max row + 1, S], num_tokens DEVICE int32 (the
+ *   rows' lengths), rows DEVICE int32 [m], row indices (a row listed twice is
+ *   reset once; indices outside [0, max_batch) are skipped); async on stream.
+ * Cost: one pass over each listed row (an atomic insert per position).
+ * SGD_EINVAL for m < 0 or m > 2^20. */
+int sgd_reset_rows(sgd_ctx *ctx, const int32_t *token_ids, const int32_t *num_tokens,
+                   const int32_t *rows, int32_t m, void *stream);
 
 /* Memory the context allocated at sgd_create (it allocates nothing later):
  * device bytes (ring, both snapshots with their indexes, sort scratch,

@@ -64,6 +64,7 @@ class SgdConfig(ctypes.Structure):
         ("draft_mode", ctypes.c_int32),
         ("select_by_score", ctypes.c_int32),
         ("num_backoff", ctypes.c_int32),
+        ("row_index", ctypes.c_int32),
     ]
 
 
@@ -128,6 +129,7 @@ def load() -> ctypes.CDLL:
         "sgd_debug_inject": (ctypes.c_int, [P, ctypes.c_int]),
         "sgd_launch_count": (ctypes.c_int, [P, u64p]),
         "sgd_set_row_stats": (ctypes.c_int, [P, P]),
+        "sgd_reset_rows": (ctypes.c_int, [P, P, P, P, i32, P]),
         "sgd_memory": (ctypes.c_int, [P, ctypes.POINTER(ctypes.c_int64), ctypes.POINTER(ctypes.c_int64)]),
     }
     for name, (res, args) in sig.items():

@@ -20,6 +20,7 @@
 #include <vector>
 
 #include "delta_sig.cuh"
+#include "row_index.cuh"
 #include "sgd_internal.h"
 
 using namespace sgd;
@@ -47,6 +48,9 @@ struct sgd_ctx {
   int32_t *d_row_stats = nullptr;   // caller's [max_batch, 4] statistics buffer, or null
   int64_t dev_bytes = 0;            // device memory the context allocated
   int64_t pinned_bytes = 0;         // page-locked host memory the context allocated
+  RowIndexArgs ri{};                // per-row bigram position indexes (row_index = 1)
+  unsigned long long *d_ri_claim = nullptr;  // sgd_reset_rows: the listing that resets a row
+  unsigned long long ri_epoch = 0;
   // sgd_step_host: the last set of host buffers checked for in-place access
   const void *zc_key[9] = {};
   void *zc_dev[9] = {};
@@ -123,6 +127,10 @@ int validate(const sgd_config &c) {
   if (c.draft_mode != 0 && c.draft_mode != 1) return SGD_EINVAL;
   if (c.select_by_score != 0 && c.select_by_score != 1) return SGD_EINVAL;
   if (c.num_backoff < 1 || c.num_backoff > MAX_BACKOFF) return SGD_EINVAL;
+  if (c.row_index != 0 && c.row_index != 1) return SGD_EINVAL;
+  if (c.row_index && (c.propose_mode == 2 || c.delta_capacity > 0 || c.select_by_score ||
+                      c.num_backoff > 1 || c.vocab_size > RI_MAX_TOKEN + 1))
+    return SGD_EINVAL;
   return SGD_OK;
 }
 
@@ -137,6 +145,9 @@ int choose_self_warps(const sgd_config &c) {
 
 void free_ctx(sgd_ctx *x) {
   cudaFree(x->d_err);
+  cudaFree(x->ri.tab);
+  cudaFree(x->ri.meta);
+  cudaFree(x->d_ri_claim);
   cudaFree(x->d_step_ready);
   cudaFree(x->d_hin);
   cudaFree(x->d_self_res);
@@ -293,6 +304,7 @@ int sgd_config_default(sgd_config *c) {
   c->select_by_score = 0;
   c->num_backoff = 1;
   c->self_warps = 0;
+  c->row_index = 0;
   return SGD_OK;
 }
 
@@ -352,6 +364,21 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
   }
   if (e == cudaSuccess) e = cudaMemset(x->d_err, 0, 4);
   if (e == cudaSuccess) e = cudaMemset(x->d_build_err, 0, 4);
+  if (cfg->row_index) {
+    // every entry empty (generation 0); every row invalid until it is reset
+    const size_t Bm = (size_t)cfg->max_batch;
+    x->ri.H = ri_entries(cfg->seq_capacity);
+    al((void **)&x->ri.tab, Bm * (size_t)x->ri.H * RI_ENTRY * 4);
+    al((void **)&x->ri.meta, Bm * 2 * 4);
+    al((void **)&x->d_ri_claim, Bm * 8);
+    if (e == cudaSuccess) e = cudaMemset(x->ri.tab, 0, Bm * (size_t)x->ri.H * RI_ENTRY * 4);
+    if (e == cudaSuccess) e = cudaMemset(x->d_ri_claim, 0, Bm * 8);
+    if (e == cudaSuccess) {
+      std::vector<int32_t> m0(2 * Bm);
+      for (size_t i = 0; i < Bm; ++i) { m0[2 * i] = -1; m0[2 * i + 1] = 0; }
+      e = cudaMemcpy(x->ri.meta, m0.data(), m0.size() * 4, cudaMemcpyHostToDevice);
+    }
+  }
   if (x->corpus) {
     const int64_t C = cfg->corpus_capacity;
     al((void **)&x->d_ring, (size_t)C * 4);
@@ -477,6 +504,7 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.by_score = c.select_by_score;
   a.nb = c.num_backoff;
   a.row_stats = x->d_row_stats;
+  a.ri = x->ri;
   if (c.draft_mode == 1) {  // no probability floor: the vote runs while an occurrence continues
     a.fixed = 1;
     a.pN = 0;
@@ -501,7 +529,7 @@ int sgd_update_state(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const 
   if (!aligned16(token_ids)) return SGD_EINVAL;
   x->launches++;
   return check_cuda(launch_update(token_ids, num_tokens, sampled, B, T, x->cfg.seq_capacity,
-                                  x->cfg.vocab_size, x->d_err, (cudaStream_t)stream));
+                                  x->cfg.vocab_size, x->d_err, x->ri, (cudaStream_t)stream));
 }
 
 static int propose_impl(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, const int32_t *sampled,
@@ -531,7 +559,7 @@ static int propose_impl(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, con
       x->launches++;
       const int r = check_cuda(launch_update(token_ids, num_tokens, sampled, B, T,
                                              x->cfg.seq_capacity, x->cfg.vocab_size, x->d_err,
-                                             (cudaStream_t)stream));
+                                             x->ri, (cudaStream_t)stream));
       if (r != SGD_OK) return r;
     }
     x->launches++;
@@ -1062,6 +1090,17 @@ int sgd_debug_inject(sgd_ctx *x, int what) {
     x->cv.notify_all();
   }
   return SGD_OK;
+}
+
+int sgd_reset_rows(sgd_ctx *x, const int32_t *token_ids, const int32_t *num_tokens,
+                   const int32_t *rows, int32_t m, void *stream) {
+  if (!x || m < 0 || m > (1 << 20)) return SGD_EINVAL;
+  if (m == 0 || x->ri.tab == nullptr) return SGD_OK;
+  if (!token_ids || !num_tokens || !rows) return SGD_EINVAL;
+  x->launches += 2;
+  return check_cuda(launch_row_index_reset(x->ri, token_ids, num_tokens, x->cfg.seq_capacity, rows,
+                                           m, x->cfg.max_batch, x->d_ri_claim, ++x->ri_epoch,
+                                           (cudaStream_t)stream));
 }
 
 int sgd_set_row_stats(sgd_ctx *x, int32_t *row_stats) {

@@ -27,6 +27,7 @@
 #include <climits>
 
 #include "ingest_cta.cuh"
+#include "row_index.cuh"
 
 namespace sgd {
 
@@ -324,6 +325,124 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
     }
   }
   asm volatile("cp.async.wait_all;" ::: "memory");  // nothing of the ring left in flight
+}
+
+// The self result from the self warps' lists (warps hold ascending ranges):
+// the longest length over the warps and its R most recent ends; when no end
+// matches two tokens, the R most recent positions of the last token (L = 1).
+// One warp.
+__device__ __forceinline__ void merge_self_lists(int nself, int R, const int *s_wM, const int *s_wcnt,
+                                                 const int *s_wcnt1, const int *s_wlist,
+                                                 const int *s_wlist1, int *s_occ, int lane, int &Ms,
+                                                 int &c) {
+  Ms = 0;
+  for (int w = 0; w < nself; ++w) Ms = max(Ms, s_wM[w]);
+  c = 0;
+  if (Ms > 0) {
+    for (int w = nself - 1; w >= 0 && c < R; --w) {
+      if (s_wM[w] != Ms) continue;
+      const int mm = min(s_wcnt[w], R - c);
+      for (int i = lane; i < mm; i += 32) s_occ[c + i] = s_wlist[w * R + i];
+      c += mm;
+    }
+  } else {  // no end matches two tokens: the ends are the t0 positions (L = 1)
+    for (int w = nself - 1; w >= 0 && c < R; --w) {
+      const int mm = min(s_wcnt1[w], R - c);
+      for (int i = lane; i < mm; i += 32) s_occ[c + i] = s_wlist1[w * R + i];
+      c += mm;
+    }
+    if (c > 0) Ms = 1;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// The row's self match from its bigram index, run by the self warps after the
+// barrier that follows the lookup (icnt, pos: the bigram's count and listed
+// positions, all below n_old).  The ends with L >= 2 are the positions
+// j <= n - 2 holding the tail's last bigram (t1, t0): the listed ones and the
+// appended positions [max(1, n_old), n - 2] that hold it.  Each is extended
+// backwards against the tail (every (end, depth) comparison loaded in one
+// batch), and the R most recent ends of the longest length are kept.
+// Returns 1 when the match was found this way (s_Ms, s_cs, s_occ written and
+// published through s_ms_ready); 2 when no end matches two tokens (the match
+// is at most 1; published as 1 with no ends -- the caller scans the row if
+// the corpus does not decide the row); 0 when the row must be scanned (the
+// list is incomplete, or the ends do not fit in `cap`).  Every self warp
+// returns the same value.
+__device__ int index_self(const int32_t *row, int n, int n_old, int D, int R, int nself, int warp,
+                          int lane, int t1, int t0, int icnt, const int *pos, const int *s_tail,
+                          int *cand, int *candL, int cap, int *s_nc, int *s_occ, int *s_Ms,
+                          int *s_cs, int *s_ms_ready) {
+  if (icnt < 0 || icnt > RI_K) return 0;
+  if (warp == 0) {
+    const bool keep = lane < icnt && pos[lane] <= n - 2;
+    const unsigned mk = __ballot_sync(FULL, keep);
+    const unsigned lt = (1u << lane) - 1u;
+    if (keep && __popc(mk & lt) < cap) cand[__popc(mk & lt)] = pos[lane];
+    int c = __popc(mk);
+    for (int base = max(1, n_old); base <= n - 2; base += 32) {
+      const int p = base + lane;
+      const bool hit = p <= n - 2 && row[p - 1] == t1 && row[p] == t0;
+      const unsigned mh = __ballot_sync(FULL, hit);
+      const int slot = c + __popc(mh & lt);
+      if (hit && slot < cap) cand[slot] = p;
+      c += __popc(mh);
+    }
+    for (int i = lane; i < min(c, cap); i += 32) candL[i] = min(D, cand[i] + 1);
+    if (lane == 0) *s_nc = c;
+  }
+  self_sync(nself);
+  const int nc = *s_nc;
+  if (nc > cap) return 0;
+  if (nc == 0) {
+    if (warp == 0 && lane == 0) {
+      *s_Ms = 1;
+      *s_cs = 0;
+      __threadfence_block();
+      *(volatile int *)s_ms_ready = 1;
+    }
+    return 2;
+  }
+  // every (end, depth >= 2) pair: the first depth that differs bounds the end
+  const int W = D - 2, tot = nc * W, st = 32 * nself;
+  for (int f0 = 32 * warp + lane; f0 < tot; f0 += 4 * st) {
+    int v[4], cidx[4], dep[4];
+    bool in[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const int f = f0 + u * st;
+      cidx[u] = f < tot ? f / W : 0;
+      dep[u] = f < tot ? 2 + f % W : D;
+      // (depths past the text start are excluded by candL's initial bound)
+      in[u] = f < tot && dep[u] <= cand[cidx[u]];
+      v[u] = in[u] ? row[cand[cidx[u]] - dep[u]] : 0;
+    }
+#pragma unroll
+    for (int u = 0; u < 4; ++u)
+      if (in[u] && v[u] != s_tail[dep[u]]) atomicMin(&candL[cidx[u]], dep[u]);
+  }
+  self_sync(nself);
+  if (warp == 0) {
+    int M = 0;
+    for (int i = lane; i < nc; i += 32) M = max(M, candL[i]);
+    M = (int)__reduce_max_sync(FULL, (unsigned)M);
+    int cnt = 0;
+    for (int i = lane; i < nc; i += 32) {
+      if (candL[i] != M) continue;
+      ++cnt;
+      int rank = 0;  // the more recent ends of length M
+      for (int q = 0; q < nc; ++q) rank += candL[q] == M && cand[q] > cand[i];
+      if (rank < R) s_occ[rank] = cand[i];
+    }
+    cnt = (int)__reduce_add_sync(FULL, (unsigned)cnt);
+    if (lane == 0) {
+      *s_Ms = M;
+      *s_cs = min(cnt, R);
+      __threadfence_block();
+      *(volatile int *)s_ms_ready = 1;
+    }
+  }
+  return 1;
 }
 
 // ---------------------------------------------------------------------------
@@ -940,19 +1059,86 @@ __device__ int update_row_warp(int32_t *row, int n, const int32_t *sp, int T, in
 }
 
 __global__ void __launch_bounds__(128) update_kernel(int32_t *tok, int32_t *ntok, const int32_t *sampled,
-                                                     int B, int T, int S, int V, uint32_t *err) {
+                                                     int B, int T, int S, int V, uint32_t *err,
+                                                     const RowIndexArgs ri) {
   const int b = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (b >= B) return;
-  int n = ntok[b];
+  const int n_in = ntok[b];
+  const int covered = ri.tab ? ri.meta[2 * (size_t)b] : -1;
+  int n = n_in;
   uint32_t fl = 0;
   if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
   if (n > S) { n = S; fl |= SGD_ERR_NUM_TOKENS; }
-  n = update_row_warp(tok + (size_t)b * S, n, sampled + (size_t)b * T, T, S, V, lane, fl);
+  const int n_old = n;
+  int32_t *row = tok + (size_t)b * S;
+  n = update_row_warp(row, n, sampled + (size_t)b * T, T, S, V, lane, fl);
   if (lane == 0) {
     ntok[b] = n;
     if (fl) atomicOr(err, fl);
   }
+  if (ri.tab) {
+    __syncwarp();  // the appended ids visible to every lane
+    ri_after_update(ri, b, row, n_old, n, covered == n_in && covered == n_old, lane);
+  }
+}
+
+// sgd_reset_rows, first launch: each listed row is claimed by its last listing
+// (the largest index i), so that a row listed twice is rebuilt once.
+__global__ void __launch_bounds__(256) ri_claim_kernel(const int32_t *rows, int m, int max_batch,
+                                                       unsigned long long *claim,
+                                                       unsigned long long epoch) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= m) return;
+  const int r = rows[i];
+  if (r < 0 || r >= max_batch) return;
+  atomicMax(claim + r, (epoch << 24) | (unsigned long long)i);
+}
+
+// Second launch, one CTA per listing: the claimed row takes the next
+// generation (every older entry reads as empty; after generation 255 the
+// table is cleared and generation 1 is used again) and every position p >= 1
+// of its current contents is inserted.  Ids outside [0, 2^24) or a full table
+// leave the row invalid (scanned) until its next reset.
+__global__ void __launch_bounds__(1024) ri_reset_kernel(const RowIndexArgs ri, const int32_t *tok,
+                                                        const int32_t *ntok, int S,
+                                                        const int32_t *rows, int max_batch,
+                                                        const unsigned long long *claim,
+                                                        unsigned long long epoch) {
+  __shared__ int s_gen, s_wrap, s_ok;
+  const int i = blockIdx.x;
+  const int r = rows[i];
+  if (r < 0 || r >= max_batch) return;
+  if (claim[r] != ((epoch << 24) | (unsigned long long)i)) return;  // listed again later
+  int n = ntok[r];
+  n = n < 0 ? 0 : (n > S ? S : n);
+  int32_t *meta = ri.meta + 2 * (size_t)r;
+  int32_t *tab = ri.tab + (size_t)r * ri.H * RI_ENTRY;
+  if (threadIdx.x == 0) {
+    const int g = meta[1];
+    s_wrap = g >= 255;
+    s_gen = g >= 255 || g < 1 ? 1 : g + 1;
+    s_ok = 1;
+    meta[0] = -1;
+    meta[1] = s_gen;
+  }
+  __syncthreads();
+  if (s_wrap) {
+    for (long long e = threadIdx.x; e < ri.H; e += blockDim.x)
+      *reinterpret_cast<unsigned long long *>(tab + e * RI_ENTRY) = 0ull;
+    __syncthreads();
+  }
+  const int gen = s_gen;
+  const int32_t *row = tok + (size_t)r * S;
+  bool ok = true;
+  for (int p = 1 + threadIdx.x; p < n; p += blockDim.x) {
+    const int t1 = row[p - 1], t0 = row[p];
+    if (t1 < 0 || t1 > RI_MAX_TOKEN || t0 < 0 || t0 > RI_MAX_TOKEN) ok = false;
+    else ok &= ri_insert(tab, ri.H, gen, t1, t0, p);
+  }
+  if (!ok) s_ok = 0;
+  __syncthreads();
+  if (threadIdx.x == 0) meta[0] = s_ok ? n : -1;
 }
 
 // ---------------------------------------------------------------------------
@@ -1228,10 +1414,19 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ int s_dcB, s_dcN, s_dmore;     // the CTA's delta list: length, ends; another round
   __shared__ uint32_t s_ep;
   __shared__ int s_scan;  // suffix-array hits the probe warps scanned (row statistics)
+  // the row's bigram index: its entries cover the row (maintenance), the self
+  // match may come from it, the row length before the update, the last two
+  // tokens after it, the looked-up count and positions, self match deferred
+  __shared__ int s_iok, s_iuse, s_nold, s_il0, s_il1, s_icnt, s_idefer, s_igen, s_inc;
+  __shared__ int s_imode;  // how the row's own match was found (row statistics)
+  __shared__ int s_ipos[RI_K];
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nthr = blockDim.x;
   const int S = a.S, R = a.R, k = a.k, D = a.D, Z = a.V;
   int32_t *row = a.tok + (size_t)b * S;
+  // the row index is used by the one-launch kernel without a delta or
+  // score-ranked selection (the host enables it only there)
+  constexpr bool IDX = MODE == 0 && !EXT;
   const int big = SELF_ONLY ? 0 : max(a.cand_cap, R * ((k + 3) & ~3));
   int *s_tail = dsm;                   // MAX_D
   int *s_wlist = s_tail + MAX_D;       // nself * R: per warp, ends matching >= 2 tokens
@@ -1276,13 +1471,36 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_ds = 0;
       s_dv = 0;
     }
-    int n = a.ntok[b];
+    const int n_in = a.ntok[b];
+    const int covered = IDX && a.ri.tab ? a.ri.meta[2 * (size_t)b] : -1;
+    const int igen = IDX && a.ri.tab ? a.ri.meta[2 * (size_t)b + 1] : 0;
+    int n = n_in;
     uint32_t fl = 0;
     if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
     if (n > S) { n = S; fl |= SGD_ERR_NUM_TOKENS; }
     const int n_old = n;
+    // (the row's last two tokens before the update, read with the sampled ids)
+    const int o1 = IDX && a.ri.tab && n_old >= 1 ? row[n_old - 1] : 0;
+    const int o2 = IDX && a.ri.tab && n_old >= 2 ? row[n_old - 2] : 0;
     if (a.do_update) n = update_row_warp(row, n, a.sampled + (size_t)b * a.T, a.T, S, a.V, lane, fl);
     if (lane == 0 && a.do_update) a.ntok[b] = n;
+    if (IDX && lane == 0) {
+      const bool iok = a.ri.tab != nullptr && covered == n_in && covered == n_old;
+      // the last two tokens after the update: appended ids, else the old ones
+      auto last = [&](int pos) {
+        return pos >= n_old ? a.sampled[(size_t)b * a.T + (pos - n_old)]
+                            : (pos == n_old - 1 ? o1 : o2);
+      };
+      s_iok = iok;
+      s_iuse = iok && n >= 2 && D >= 2;
+      s_nold = n_old;
+      s_il0 = n >= 1 ? last(n - 1) : 0;
+      s_il1 = n >= 2 ? last(n - 2) : 0;
+      s_icnt = -1;
+      s_idefer = 0;
+      s_igen = igen;
+      s_imode = 0;
+    }
     // When the update appended >= 4 ids, the last four tokens are those ids:
     // the probe warps can look the n-grams up before the tail is read back.
     bool early = a.do_update && n - n_old >= 4;
@@ -1358,6 +1576,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const bool done_signal = EXT && MODE == 0 && a.dcap > 0 && a.ing_m > 0 && a.step_ready != nullptr;
   if (!((a.active == nullptr || a.active[b] != 0) && n > 0)) {
     if (done_signal && tid == 0) step_done(a.step_sync, s_ep);
+    // (the update applies to inactive rows too: their index follows it)
+    if (IDX && a.ri.tab && warp == 0) ri_after_update(a.ri, b, row, s_nold, n, s_iok, lane);
     if constexpr (!SELF_ONLY) {  // (the self-only launch leaves the outputs to the second)
       for (int d = tid; d < k; d += nthr) {
         dr[d] = -1;
@@ -1383,9 +1603,18 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   if (early_bounds && warp >= a.nself)
     pattern_bounds(cp, s_early, 4 - (warp - a.nself), D, n, lane, &s_bound[2 * (warp - a.nself)]);
   SelfScan sc;
+  // With a usable row index, warp 0 looks the row's last bigram up while the
+  // tail is read, and the self warps fetch no window before they know whether
+  // the row must be scanned at all.
+  const bool use_idx = IDX && s_iuse;
+  if (use_idx && warp == 0) {
+    const int c = ri_lookup(a.ri.tab + (size_t)b * a.ri.H * RI_ENTRY, a.ri.H, s_igen, s_il1, s_il0,
+                            lane, s_ipos);
+    if (lane == 0) s_icnt = c;
+  }
   // staged keys landed (no-op without any); a self warp's window groups,
   // committed after them, stay in flight
-  if (!FROM_RES && warp < a.nself &&
+  if (!FROM_RES && warp < a.nself && !use_idx &&
       self_prefetch(row, n, S, warp, a.nself, lane, s_ring + warp * (SR * 32), sc))
     asm volatile("cp.async.wait_group %0;" ::"n"(SPF + 1) : "memory");
   else
@@ -1412,160 +1641,156 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       *(volatile int *)&s_ms_ready = 1;
     }
   } else if (!FROM_RES && warp < a.nself) {
-    int Mw, cnt, cnt1;
-    self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, s_wlist1 + warp * R, lane, sc, Mw, cnt,
-                 cnt1);
-    if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; s_wcnt1[warp] = cnt1; }
-    // The self result: the longest length over the warps and its most recent
-    // ends (warps hold ascending ranges); published to the probe warps.
-    auto merge_self = [&]() {
-      __threadfence_block();
-      int Ms = 0;
-      for (int w = 0; w < a.nself; ++w) Ms = max(Ms, s_wM[w]);
-      int c = 0;
-      if (Ms > 0) {
-        for (int w = a.nself - 1; w >= 0 && c < R; --w) {
-          if (s_wM[w] != Ms) continue;
-          const int mm = min(s_wcnt[w], R - c);
-          for (int i = lane; i < mm; i += 32) s_occ[c + i] = s_wlist[w * R + i];
-          c += mm;
-        }
-      } else {  // no end matches two tokens: the ends are the t0 positions (L = 1)
-        for (int w = a.nself - 1; w >= 0 && c < R; --w) {
-          const int mm = min(s_wcnt1[w], R - c);
-          for (int i = lane; i < mm; i += 32) s_occ[c + i] = s_wlist1[w * R + i];
-          c += mm;
-        }
-        if (c > 0) Ms = 1;
-      }
-      if (lane == 0) {
-        s_Ms = Ms;
-        s_cs = c;
+    // 0: scan the row; 1: the row index gave the match; 2: no end matches two
+    // tokens (decided after the corpus, see below)
+    int imode = 0;
+    if (use_idx) {
+      imode = index_self(row, n, s_nold, D, R, a.nself, warp, lane, s_il1, s_il0, s_icnt, s_ipos, s_tail,
+                         s_wlist, s_wlist1, a.nself * R, &s_inc, s_occ, &s_Ms, &s_cs, &s_ms_ready);
+      if (imode == 2 && warp == 0 && lane == 0) s_idefer = 1;
+      if (warp == 0 && lane == 0) s_imode = imode;
+      if (imode == 0) self_prefetch(row, n, S, warp, a.nself, lane, s_ring + warp * (SR * 32), sc);
+    }
+    if (imode == 0) {
+      int Mw, cnt, cnt1;
+      self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, s_wlist1 + warp * R, lane, sc, Mw, cnt,
+                   cnt1);
+      if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; s_wcnt1[warp] = cnt1; }
+      // The self result: the longest length over the warps and its most recent
+      // ends (warps hold ascending ranges); published to the probe warps.
+      auto merge_self = [&]() {
         __threadfence_block();
-        *(volatile int *)&s_ms_ready = 1;
-      }
-      if (SELF_ONLY) {  // the row's self result for the second launch
-        __syncwarp();
-        int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
-        for (int i = lane; i < c; i += 32) res[6 + i] = s_occ[i];
-        if (lane < 4) res[2 + lane] = lane < dl ? s_tail[lane] : 0;
+        int Ms, c;
+        merge_self_lists(a.nself, R, s_wM, s_wcnt, s_wcnt1, s_wlist, s_wlist1, s_occ, lane, Ms, c);
         if (lane == 0) {
-          res[0] = Ms;
-          res[1] = c;
+          s_Ms = Ms;
+          s_cs = c;
+          __threadfence_block();
+          *(volatile int *)&s_ms_ready = 1;
         }
-      }
-    };
-    if (EXT && s_dv > 0 && D >= 2 && n >= 2) {
-      // The delta, after the row.  Its first windows are requested before the
-      // self merge (each warp's ring is free again); the per-warp lists are
-      // reused once warp 0 has merged the row's.
-      int4 *sring = s_ring + warp * (SR * 32);
-      DeltaScan dsc;
-      delta_windows(a.C, s_ds, s_dv, dsc);
-      const int G = DNB * a.nself;  // windows per round
-      const int dlim = min(D, n);
-      const int t2 = dlim >= 3 ? s_tail[2] : 0, t3 = dlim >= 4 ? s_tail[3] : 0;
-      const DeltaGrams grams{sig_bucket(2, s_tail[0], s_tail[1], 0, 0),
-                             dlim >= 3 ? sig_bucket(3, s_tail[0], s_tail[1], t2, 0) : 0u,
-                             dlim >= 4 ? sig_bucket(4, s_tail[0], s_tail[1], t2, t3) : 0u};
-      // the signature words of each round's block are read one round ahead
-      // (round 0's while the row's result is merged)
-      SigAhead ahead = sig_ahead(a.sig, dsc, grams, dsc.nw - 1 - DNB * (a.nself - 1 - warp), dlim, lane);
-      self_sync(a.nself);
-      if (warp == 0) merge_self();
-      self_sync(a.nself);
-      // (the row's per-warp lists are free now: s_wlist holds each warp's
-      // ends of a block or range, s_wlist1[0, R) the CTA's list)
-      int *wl = s_wlist + warp * R;
-      int covered = 0;
-      for (int t = 0;; ++t) {
-        const int hi = dsc.nw - 1 - t * G - DNB * (a.nself - 1 - warp);
-        const SigAhead cur = ahead;
-        ahead = sig_ahead(a.sig, dsc, grams, hi - G, dlim, lane);  // the next round's
-        int M = 0, c = 0;
-        delta_process(a.ring, a.sig, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, max(0, hi - DNB + 1),
-                      hi, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp, a.nself, grams, &cur, M, c);
-        if (lane == 0) s_dstate[warp] = M << 16 | c;
-        self_sync(a.nself);
-        covered = min(dsc.nw, covered + G);
-        if (warp == 0) {  // the round's ends join the CTA's list (blocks newest first)
-          const int st = lane < a.nself ? s_dstate[lane] : 0;
-          const int Bn = max(s_dcB, (int)__reduce_max_sync(FULL, (unsigned)(st >> 16)));
-          int N = Bn > s_dcB ? 0 : s_dcN;
-          const int N0 = N;
-          if (Bn >= 2)
-            for (int w = a.nself - 1; w >= 0 && N < R; --w) {
-              const int sw = s_dstate[w];
-              if ((sw >> 16) != Bn) continue;
-              const int mm = min(sw & 0xffff, R - N);
-              for (int i = lane; i < mm; i += 32) s_wlist1[N + i] = s_wlist[w * R + i];
-              N += mm;
-            }
-          __syncwarp();
-          if (lane < a.nself) s_dstate[lane] = 0;
-          if (lane == 0) {
-            s_dcB = Bn;
-            s_dcN = N;
-            // another round if windows remain, the list is not full and this
-            // round was dense
-            s_dmore = covered < dsc.nw && N < R && 4 * (N - N0) >= R;
-          }
-        }
-        self_sync(a.nself);
-        if (!s_dmore) break;
-      }
-      // the ranges below the rounds
-      const int rest = dsc.nw - covered;
-      const int per = (rest + a.nself - 1) / a.nself;
-      int dM = 0, dcnt = 0;
-      delta_process(a.ring, a.sig, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, warp * per,
-                    min(rest, (warp + 1) * per) - 1, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp,
-                    a.nself, grams, nullptr, dM, dcnt);
-      if (lane == 0) s_dstate[warp] = dM << 16 | dcnt;
-      self_sync(a.nself);
-      if (warp == 0) {
-        // longest delta match; its ends, most recent first: the CTA's list
-        // (when of that length), then the ranges from the newest warp down
-        const int st = lane < a.nself ? s_dstate[lane] : 0;
-        const int Md = max(s_dcB, (int)__reduce_max_sync(FULL, (unsigned)(st >> 16)));
-        int c = Md >= 2 && s_dcB == Md ? s_dcN : 0;
-        if (Md >= 2)
-          for (int w = a.nself - 1; w >= 0 && c < R; --w) {
-            const int sw = s_dstate[w];
-            if ((sw >> 16) != Md) continue;
-            const int mm = min(sw & 0xffff, R - c);
-            for (int i = lane; i < mm; i += 32) s_wlist1[c + i] = s_wlist[w * R + i];
-            c += mm;
-          }
-        if (lane == 0) {
-          s_Md = Md >= 2 ? Md : 0;
-          s_cd = Md >= 2 ? c : 0;
-        }
-        if (SELF_ONLY) {
+        if (SELF_ONLY) {  // the row's self result for the second launch
           __syncwarp();
           int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
-          for (int i = lane; i < c; i += 32) res[R + 10 + i] = s_wlist1[i];
+          for (int i = lane; i < c; i += 32) res[6 + i] = s_occ[i];
+          if (lane < 4) res[2 + lane] = lane < dl ? s_tail[lane] : 0;
           if (lane == 0) {
-            res[R + 6] = Md >= 2 ? Md : 0;
-            res[R + 7] = Md >= 2 ? c : 0;
-            res[R + 8] = (int)s_ds;
-            res[R + 9] = s_dv;
+            res[0] = Ms;
+            res[1] = c;
           }
         }
-      }
-    } else {
-      __threadfence_block();
-      __syncwarp();
-      int last = 0;
-      if (lane == 0) last = atomicAdd(&s_self_done, 1) == a.nself - 1;
-      last = __shfl_sync(FULL, last, 0);
-      if (last) merge_self();  // the last self warp to finish
-      if (EXT && SELF_ONLY && warp == 0 && lane == 0) {  // no delta for this row
-        int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
-        res[R + 6] = 0;
-        res[R + 7] = 0;
-        res[R + 8] = (int)s_ds;
-        res[R + 9] = 0;
+      };
+      if (EXT && s_dv > 0 && D >= 2 && n >= 2) {
+        // The delta, after the row.  Its first windows are requested before the
+        // self merge (each warp's ring is free again); the per-warp lists are
+        // reused once warp 0 has merged the row's.
+        int4 *sring = s_ring + warp * (SR * 32);
+        DeltaScan dsc;
+        delta_windows(a.C, s_ds, s_dv, dsc);
+        const int G = DNB * a.nself;  // windows per round
+        const int dlim = min(D, n);
+        const int t2 = dlim >= 3 ? s_tail[2] : 0, t3 = dlim >= 4 ? s_tail[3] : 0;
+        const DeltaGrams grams{sig_bucket(2, s_tail[0], s_tail[1], 0, 0),
+                               dlim >= 3 ? sig_bucket(3, s_tail[0], s_tail[1], t2, 0) : 0u,
+                               dlim >= 4 ? sig_bucket(4, s_tail[0], s_tail[1], t2, t3) : 0u};
+        // the signature words of each round's block are read one round ahead
+        // (round 0's while the row's result is merged)
+        SigAhead ahead = sig_ahead(a.sig, dsc, grams, dsc.nw - 1 - DNB * (a.nself - 1 - warp), dlim, lane);
+        self_sync(a.nself);
+        if (warp == 0) merge_self();
+        self_sync(a.nself);
+        // (the row's per-warp lists are free now: s_wlist holds each warp's
+        // ends of a block or range, s_wlist1[0, R) the CTA's list)
+        int *wl = s_wlist + warp * R;
+        int covered = 0;
+        for (int t = 0;; ++t) {
+          const int hi = dsc.nw - 1 - t * G - DNB * (a.nself - 1 - warp);
+          const SigAhead cur = ahead;
+          ahead = sig_ahead(a.sig, dsc, grams, hi - G, dlim, lane);  // the next round's
+          int M = 0, c = 0;
+          delta_process(a.ring, a.sig, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, max(0, hi - DNB + 1),
+                        hi, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp, a.nself, grams, &cur, M, c);
+          if (lane == 0) s_dstate[warp] = M << 16 | c;
+          self_sync(a.nself);
+          covered = min(dsc.nw, covered + G);
+          if (warp == 0) {  // the round's ends join the CTA's list (blocks newest first)
+            const int st = lane < a.nself ? s_dstate[lane] : 0;
+            const int Bn = max(s_dcB, (int)__reduce_max_sync(FULL, (unsigned)(st >> 16)));
+            int N = Bn > s_dcB ? 0 : s_dcN;
+            const int N0 = N;
+            if (Bn >= 2)
+              for (int w = a.nself - 1; w >= 0 && N < R; --w) {
+                const int sw = s_dstate[w];
+                if ((sw >> 16) != Bn) continue;
+                const int mm = min(sw & 0xffff, R - N);
+                for (int i = lane; i < mm; i += 32) s_wlist1[N + i] = s_wlist[w * R + i];
+                N += mm;
+              }
+            __syncwarp();
+            if (lane < a.nself) s_dstate[lane] = 0;
+            if (lane == 0) {
+              s_dcB = Bn;
+              s_dcN = N;
+              // another round if windows remain, the list is not full and this
+              // round was dense
+              s_dmore = covered < dsc.nw && N < R && 4 * (N - N0) >= R;
+            }
+          }
+          self_sync(a.nself);
+          if (!s_dmore) break;
+        }
+        // the ranges below the rounds
+        const int rest = dsc.nw - covered;
+        const int per = (rest + a.nself - 1) / a.nself;
+        int dM = 0, dcnt = 0;
+        delta_process(a.ring, a.sig, s_dv, Z, D, n, R, s_tail, lane, sring, dsc, warp * per,
+                      min(rest, (warp + 1) * per) - 1, wl, &s_best_delta, s_dstate, s_dcB, s_dcN, warp,
+                      a.nself, grams, nullptr, dM, dcnt);
+        if (lane == 0) s_dstate[warp] = dM << 16 | dcnt;
+        self_sync(a.nself);
+        if (warp == 0) {
+          // longest delta match; its ends, most recent first: the CTA's list
+          // (when of that length), then the ranges from the newest warp down
+          const int st = lane < a.nself ? s_dstate[lane] : 0;
+          const int Md = max(s_dcB, (int)__reduce_max_sync(FULL, (unsigned)(st >> 16)));
+          int c = Md >= 2 && s_dcB == Md ? s_dcN : 0;
+          if (Md >= 2)
+            for (int w = a.nself - 1; w >= 0 && c < R; --w) {
+              const int sw = s_dstate[w];
+              if ((sw >> 16) != Md) continue;
+              const int mm = min(sw & 0xffff, R - c);
+              for (int i = lane; i < mm; i += 32) s_wlist1[c + i] = s_wlist[w * R + i];
+              c += mm;
+            }
+          if (lane == 0) {
+            s_Md = Md >= 2 ? Md : 0;
+            s_cd = Md >= 2 ? c : 0;
+          }
+          if (SELF_ONLY) {
+            __syncwarp();
+            int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
+            for (int i = lane; i < c; i += 32) res[R + 10 + i] = s_wlist1[i];
+            if (lane == 0) {
+              res[R + 6] = Md >= 2 ? Md : 0;
+              res[R + 7] = Md >= 2 ? c : 0;
+              res[R + 8] = (int)s_ds;
+              res[R + 9] = s_dv;
+            }
+          }
+        }
+      } else {
+        __threadfence_block();
+        __syncwarp();
+        int last = 0;
+        if (lane == 0) last = atomicAdd(&s_self_done, 1) == a.nself - 1;
+        last = __shfl_sync(FULL, last, 0);
+        if (last) merge_self();  // the last self warp to finish
+        if (EXT && SELF_ONLY && warp == 0 && lane == 0) {  // no delta for this row
+          int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
+          res[R + 6] = 0;
+          res[R + 7] = 0;
+          res[R + 8] = (int)s_ds;
+          res[R + 9] = 0;
+        }
       }
     }
   } else if (corpus_ok) {
@@ -1841,6 +2066,31 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   if (SELF_ONLY) return;
   __syncthreads();
 
+  if (IDX && s_idefer && (corpus_ok ? s_Mc : 0) < 2) {
+    // No earlier end holds the row's last bigram, so its match is at most 1,
+    // and the corpus has no match of 2 or more: the row's own result decides
+    // after all, from a scan of the row.
+    if (warp < a.nself) {
+      SelfScan sd;
+      self_prefetch(row, n, S, warp, a.nself, lane, s_ring + warp * (SR * 32), sd);
+      int Mw, cnt, cnt1;
+      self_process(row, n, S, D, R, s_tail, s_wlist + warp * R, s_wlist1 + warp * R, lane, sd, Mw, cnt,
+                   cnt1);
+      if (lane == 0) { s_wM[warp] = Mw; s_wcnt[warp] = cnt; s_wcnt1[warp] = cnt1; }
+      self_sync(a.nself);
+      if (warp == 0) {
+        int Ms, c;
+        merge_self_lists(a.nself, R, s_wM, s_wcnt, s_wcnt1, s_wlist, s_wlist1, s_occ, lane, Ms, c);
+        if (lane == 0) {
+          s_Ms = Ms;
+          s_cs = c;
+          s_imode = 0;
+        }
+      }
+    }
+    __syncthreads();
+  }
+
   // ---- the longer match wins (equal lengths: the row itself) ----
   // The corpus is the snapshot followed by the delta: its longest match is
   // the longer of the two, and at equal lengths the delta's ends are the more
@@ -1931,6 +2181,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     __syncthreads();
   }
   if (done_signal && tid == 0) step_done(a.step_sync, s_ep);  // the row's ring reads are over
+  // the row index follows this step's update (for the next step), off the
+  // vote's path: warp 1 when there is one
+  const int iwarp = nthr > 32 ? 1 : 0;
+  if (IDX && a.ri.tab && warp == iwarp && iwarp != 0) ri_after_update(a.ri, b, row, s_nold, n, s_iok, lane);
   if (warp != 0) return;
 
   // ---- depth-wise majority vote (one warp) ----
@@ -1969,13 +2223,14 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     dr[d] = fill;
     if (pr) pr[d] = 0.f;
   }
+  if (IDX && a.ri.tab && iwarp == 0) ri_after_update(a.ri, b, row, s_nold, n, s_iok, lane);
   if (lane == 0) {
     a.num_valid[b] = a.fixed ? k : len;
     if (a.score) a.score[b] = cw > 0 ? (float)sum / (float)cw : 0.f;
     if (a.match_info) { a.match_info[2 * b] = M; a.match_info[2 * b + 1] = src; }
     if (a.row_stats)
       *reinterpret_cast<int4 *>(a.row_stats + 4 * (size_t)b) =
-          make_int4(s_scan, cw, src == 1 && both ? cap_s : cap, src);
+          make_int4(s_scan, cw, src == 1 && both ? cap_s : cap, src | (IDX ? s_imode << 8 : 0));
   }
 }
 
@@ -2059,9 +2314,21 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
 }
 
 cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, int B, int T, int S,
-                          int V, uint32_t *err, cudaStream_t st) {
+                          int V, uint32_t *err, const RowIndexArgs &ri, cudaStream_t st) {
   if (B <= 0) return cudaSuccess;
-  update_kernel<<<(B + 3) / 4, 128, 0, st>>>(tok, ntok, sampled, B, T, S, V, err);
+  update_kernel<<<(B + 3) / 4, 128, 0, st>>>(tok, ntok, sampled, B, T, S, V, err, ri);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_row_index_reset(const RowIndexArgs &ri, const int32_t *tok, const int32_t *ntok,
+                                   int S, const int32_t *rows, int m, int max_batch,
+                                   unsigned long long *claim, unsigned long long epoch,
+                                   cudaStream_t st) {
+  if (m <= 0 || ri.tab == nullptr) return cudaSuccess;
+  ri_claim_kernel<<<(m + 255) / 256, 256, 0, st>>>(rows, m, max_batch, claim, epoch);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  ri_reset_kernel<<<m, 1024, 0, st>>>(ri, tok, ntok, S, rows, max_batch, claim, epoch);
   return cudaGetLastError();
 }
 

@@ -106,6 +106,13 @@ __host__ __device__ inline DeltaView delta_view(const RingState &r, long long si
   return v;
 }
 
+// Per-row bigram position index (row_index.cuh), or tab == null.
+struct RowIndexArgs {
+  int32_t *tab;    // [max_batch][H][16] entries
+  int32_t *meta;   // [max_batch][2]: row length the entries cover (-1: invalid), generation
+  long long H;     // entries per row
+};
+
 struct ProposeArgs {
   int32_t *tok;            // [B, S]
   int32_t *ntok;           // [B]
@@ -164,6 +171,9 @@ struct ProposeArgs {
   // [B, 4] or null: per row, the suffix-array hits the corpus probe scanned,
   // the occurrences that voted (c0), the draft cap and the source (0/1/2)
   int32_t *row_stats;
+  // the rows' bigram position indexes: the self match from them when complete
+  // (one fused kernel per step, no delta, no score-ranked selection)
+  RowIndexArgs ri;
 };
 
 __host__ __device__ constexpr int self_res_ints(int R) { return 2 * R + 10; }
@@ -173,7 +183,15 @@ size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap);  // 
 int propose_step_max_docs();  // largest doc count a fused step ingests in-kernel
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st);
 cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, int B,
-                          int T, int S, int V, uint32_t *err, cudaStream_t st);
+                          int T, int S, int V, uint32_t *err, const RowIndexArgs &ri,
+                          cudaStream_t st);
+// Starts the indexes of rows[0, m) over from their current contents (distinct
+// rows; a row listed twice is reset once).  claim: [max_batch] u64 words,
+// epoch: a number the context never passed before.
+cudaError_t launch_row_index_reset(const RowIndexArgs &ri, const int32_t *tok, const int32_t *ntok,
+                                   int S, const int32_t *rows, int m, int max_batch,
+                                   unsigned long long *claim, unsigned long long epoch,
+                                   cudaStream_t st);
 cudaError_t propose_set_smem_limit(size_t bytes);
 
 // backoff.cu: multi-length backoff drafting of rows [0, B), one CTA per row

@@ -68,7 +68,7 @@ class SuffixDrafter:
                  corpus_cand_cap: int = 2048, self_warps: int = 0, corpus_records: int = 1,
                  corpus_gram_index: int = 1, propose_mode: int = 0, delta_capacity: int = 0,
                  draft_mode: int = 0, select_by_score: int = 0, num_backoff: int = 1,
-                 device: int = 0):
+                 row_index: int = 0, device: int = 0):
         self._lib = L.load()
         cfg = L.SgdConfig()
         self._check(self._lib.sgd_config_default(ctypes.byref(cfg)), "sgd_config_default")
@@ -95,6 +95,7 @@ class SuffixDrafter:
         cfg.draft_mode = draft_mode
         cfg.select_by_score = select_by_score
         cfg.num_backoff = num_backoff
+        cfg.row_index = row_index
         self.cfg = cfg
         self.device = torch.device("cuda", device)
         torch.cuda.init()
@@ -325,6 +326,16 @@ class SuffixDrafter:
 
     def debug_inject(self, what: int) -> None:
         self._check(self._lib.sgd_debug_inject(self._h, int(what)), "sgd_debug_inject")
+
+    def reset_rows(self, token_ids: torch.Tensor, num_tokens: torch.Tensor, rows: torch.Tensor,
+                   stream=None) -> None:
+        """Rebuilds the bigram position index of the listed rows from their
+        current contents (row_index=1; no-op otherwise).  Call it for every
+        row written other than through the library's updates."""
+        self._check(self._lib.sgd_reset_rows(self._h, self._t(token_ids), self._t(num_tokens),
+                                             self._t(rows, name="rows"), rows.shape[0],
+                                             _stream_handle(stream)),
+                    "sgd_reset_rows")
 
     def set_row_stats(self, row_stats: Optional[torch.Tensor]) -> None:
         """Per-row statistics of later drafting launches into `row_stats`

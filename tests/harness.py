@@ -126,6 +126,10 @@ class Lockstep:
         dev = self.dr.device
         self.tok = torch.from_numpy(tok).to(dev)
         self.n = torch.from_numpy(n).to(dev)
+        # rows written by the caller: their bigram indexes start from them
+        self.row_index = bool(over.get("row_index"))
+        if self.row_index:
+            self.dr.reset_rows(self.tok, self.n, torch.arange(self.B, dtype=torch.int32, device=dev))
         self.out = self.dr.new_outputs(self.B)
         self.X = None            # oracle's current snapshot
         self.X_pending = None
@@ -226,6 +230,8 @@ class Lockstep:
             idx = torch.from_numpy(sd.finished.astype(np.int64)).to(dev)
             self.tok[idx] = torch.from_numpy(sd.reset_tokens).to(dev)
             self.n[idx] = torch.from_numpy(sd.reset_n).to(dev)
+            if self.row_index:  # new requests in these rows
+                self.dr.reset_rows(self.tok, self.n, idx.to(torch.int32))
             if (self.ring is not None and not self.build_pending
                     and self.ingested_since_build >= self.cfg.rebuild_tokens):
                 self.start_build()

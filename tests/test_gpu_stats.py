@@ -42,7 +42,8 @@ def test_row_stats_agree_with_the_drafts(mode):
         mi = H.to_np(ls.out.match_info)
         nv = H.to_np(ls.out.num_valid)
         sc = H.to_np(ls.out.score).astype(np.float64)
-        scanned, c0, cap, src = st[:, 0], st[:, 1], st[:, 2], st[:, 3]
+        scanned, c0, cap, src = st[:, 0], st[:, 1], st[:, 2], st[:, 3] & 255
+        assert (st[:, 3] >> 8 == 0).all()  # (no row index: every row scanned)
         assert np.array_equal(src, mi[:, 1])
         assert (nv <= cap).all() and (scanned >= 0).all()
         assert ((c0 >= 1) & (c0 <= cfg.R))[src > 0].all() and (c0[src == 0] == 0).all()
