@@ -234,11 +234,13 @@ def _prefill(dr, cfg, tr, dev, side, rank, chunk=2048):
 
 
 def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=None,
-               headline=False):
+               headline=False, row_index=0):
     """The serving loop of `cfg_name`: per step the update, propose and ingest
     of the rows that finish (one captured graph), then the host's rebuild
     policy and swap poll.  delta > 0: the docs ingested since the current
-    snapshot are matched too; backoff > 1: multi-length backoff drafting.
+    snapshot are matched too; backoff > 1: multi-length backoff drafting;
+    row_index: each row's own match from its bigram position index (the rows
+    a step restarts are reset outside the timed region, like their contents).
     headline: also the warm and latency-floor timings, the end-to-end leg
     through host buffers and the standalone suffix-array builds."""
     import torch
@@ -257,7 +259,8 @@ def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=
                        max_tree_depth=cfg.D, max_occurrences=cfg.R, max_sampled=cfg.T,
                        max_spec_factor=cfg.factor, max_spec_offset=cfg.offset,
                        min_token_prob=cfg.min_prob, corpus_capacity=cfg.corpus_tokens,
-                       delta_capacity=delta, num_backoff=backoff, device=dev.index)
+                       delta_capacity=delta, num_backoff=backoff, row_index=row_index,
+                       device=dev.index)
     # drafting at the device's highest stream priority, snapshot builds at the lowest
     least, greatest = torch.cuda.Stream.priority_range()
     stream = torch.cuda.Stream(device=dev, priority=greatest)
@@ -268,6 +271,8 @@ def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=
 
     g_tok = torch.from_numpy(tok).to(dev)
     g_n = torch.from_numpy(n).to(dev)
+    if row_index:
+        dr.reset_rows(g_tok, g_n, torch.arange(cfg.B, dtype=torch.int32, device=dev))
     out = dr.new_outputs(cfg.B)
     stats = RowStats(dr, cfg.B, dev) if backoff == 1 else None
     m_fin = int(np.floor(cfg.finish_frac * cfg.B))
@@ -311,10 +316,12 @@ def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=
         (workload bookkeeping), this step's inputs land in the fixed buffers,
         and (cold) L2 is flushed."""
         if i > 0:
-            _, _, _, _, idx, rt, rn = fin[i - 1]
+            rows0, _, _, _, idx, rt, rn = fin[i - 1]
             if idx.numel():
                 g_tok[idx] = rt
                 g_n[idx] = rn
+                if row_index:
+                    dr.reset_rows(g_tok, g_n, rows0)
         d_samp.copy_(samp[i])
         rows, st_, ln, _, _, _, _ = fin[i]
         if rows.numel():
@@ -465,7 +472,7 @@ def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=
         dr.poll(wait=True, stream=stream)
         state["pending"] = False
     res["e2e"] = e2e_leg(dr, cfg, steps, Wm + K + K_warm, K_e2e, g_tok, g_n, flush, side, state,
-                         dev, stream)
+                         dev, stream, row_index)
     pass_ms = float(sum(b["pass_ms"] for b in region_builds))
     pass_elems = int(sum(b["pass_elems"] for b in region_builds))
     n_passes = int(sum(b["passes"] for b in region_builds))
@@ -486,7 +493,7 @@ def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=
     return res
 
 
-def e2e_leg(dr, cfg, steps, first, K, g_tok, g_n, flush, side, state, dev, stream):
+def e2e_leg(dr, cfg, steps, first, K, g_tok, g_n, flush, side, state, dev, stream, row_index=0):
     """Same steps through the public API with pinned host buffers
     (SuffixDrafter.step_host): each step copies its sampled ids and ingest
     arguments host->device and reads the drafts and valid counts back, all
@@ -519,6 +526,8 @@ def e2e_leg(dr, cfg, steps, first, K, g_tok, g_n, flush, side, state, dev, strea
                 idx = torch.from_numpy(p.finished.astype(np.int64)).to(dev)
                 g_tok[idx] = torch.from_numpy(p.reset_tokens).to(dev)
                 g_n[idx] = torch.from_numpy(p.reset_n).to(dev)
+                if row_index:
+                    dr.reset_rows(g_tok, g_n, idx.to(torch.int32))
         flush.fill_(j)
         h_in_np[:] = blocks[j]       # this step's inputs land in pinned host memory
         torch.cuda.synchronize()
@@ -807,8 +816,12 @@ def main():
     ap.add_argument("--concurrent-steps", type=int, default=64,
                     help="steps timed with no build in flight in the concurrent-build line (0: skip)")
     ap.add_argument("--concurrent-max-steps", type=int, default=4096)
+    ap.add_argument("--row-index-steps", type=int, default=256,
+                    help="steps of the serving loop with row_index=1, a secondary line (0: skip)")
     ap.add_argument("--long-only", action="store_true",
                     help="only time the long-context serving loop and print its line")
+    ap.add_argument("--long-row-index", type=int, default=0,
+                    help="with --long-only: row_index of the long-context loop")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -846,7 +859,8 @@ def main():
             print(json.dumps(sa_build_leg(args, dev, sizes=[args.sa_only])), flush=True)
         return
     if args.long_only:
-        r = serve_loop(args, rank, world, "c5", K=args.long_context_steps, Wm=3)
+        r = serve_loop(args, rank, world, "c5", K=args.long_context_steps, Wm=3,
+                       row_index=args.long_row_index)
         if rank == 0:
             print(json.dumps(r), flush=True)
         return
@@ -874,10 +888,19 @@ def main():
                                            "score wins",
                                   **serve_loop(args, rank, world, "c3", backoff=8,
                                                K=args.backoff_steps))
+        if args.row_index_steps > 0:
+            res["row_index"] = dict(workload="the serving loop above with row_index=1: each row's "
+                                             "own match from its bigram position index",
+                                    **serve_loop(args, rank, world, "c3", K=args.row_index_steps,
+                                                 row_index=1))
         if args.long_context_steps > 0:
             res["long_context"] = dict(workload=WORKLOADS["c5"],
                                        **serve_loop(args, rank, world, "c5",
                                                     K=args.long_context_steps, Wm=3))
+            res["long_context_row_index"] = dict(
+                workload=WORKLOADS["c5"] + "; row_index=1: each row's own match from its bigram "
+                                           "position index",
+                **serve_loop(args, rank, world, "c5", K=args.long_context_steps, Wm=3, row_index=1))
     res["sa_build"] = sa_build_leg(args, dev)
     if args.concurrent_steps > 0:
         res["sa_concurrent"] = {("%dM" % (N >> 20)): sa_concurrent_leg(args, dev, N)

@@ -248,7 +248,7 @@ int sgd_propose_with_update(sgd_ctx *ctx, int32_t *token_ids, int32_t *num_token
  * read from the rows after their update ([PYPI] Quickstart: the serving loop
  * calls propose_with_update and harvest_finished every step).  Results equal
  * those of the two calls made in that order on `stream` (num_tokens, after
- * the update, bounds the docs).  With 1 <= n_docs <= 32 everything runs in
+ * the update, bounds the docs).  With 1 <= n_docs <= 64 everything runs in
  * ONE kernel launch: one extra CTA appends the docs while the row CTAs
  * draft, after waiting (bounded, ~0.1 s) for each doc's row to be updated; a
  * wait that runs out skips that doc and sets SGD_ERR_INGEST_WAIT.  Larger

@@ -20,7 +20,7 @@ namespace sgd {
 namespace {
 
 constexpr int PLAN_WINDOW = 1024;  // oldest FIFO lengths staged for evictions
-constexpr int SMALL_DOCS = 32;     // calls up to this size run in one CTA
+constexpr int SMALL_DOCS = 64;     // calls up to this size run in one CTA (of > 64 threads)
 constexpr int SMALL_BATCH = 4;     // loads each thread has in flight per sweep
 constexpr unsigned STEP_SPIN_LIMIT = 1u << 17;  // ~0.1 s of polling; a normal wait is microseconds
 
@@ -70,15 +70,19 @@ __device__ inline void place_doc(PlanWalk &w, int i, int L, long long C, const i
   w.placed += s;
 }
 
-// Warp 0: inclusive prefix sums of c over the 32 lanes into s_cum[1..32].
-__device__ __forceinline__ void small_cum(int c, int *s_cum) {
+// Warp 0: inclusive prefix sums of c[0 .. SMALL_DOCS) (two per lane) into
+// s_cum[1 .. SMALL_DOCS].
+__device__ __forceinline__ void small_cum(const int *c, int *s_cum) {
   const int lane = threadIdx.x & 31;
+  const int c0 = c[2 * lane], c1 = c[2 * lane + 1];
+  int x = c0 + c1;
 #pragma unroll
   for (int off = 1; off < 32; off <<= 1) {
-    const int y = __shfl_up_sync(FULL, c, off);
-    if (lane >= off) c += y;
+    const int y = __shfl_up_sync(FULL, x, off);
+    if (lane >= off) x += y;
   }
-  s_cum[lane + 1] = c;
+  s_cum[2 * lane + 1] = x - c1;
+  s_cum[2 * lane + 2] = x;
   if (lane == 0) s_cum[0] = 0;
 }
 
@@ -87,7 +91,7 @@ __device__ __forceinline__ void small_cum(int c, int *s_cum) {
 __device__ __forceinline__ int small_doc(const int *s_cum, int m, int g) {
   int d = 0;
 #pragma unroll
-  for (int step = 16; step; step >>= 1)
+  for (int step = SMALL_DOCS / 2; step; step >>= 1)
     if (d + step < m && s_cum[d + step] <= g) d += step;
   return d;
 }
@@ -102,6 +106,7 @@ struct SmallIngestSmem {
   int64_t dest[SMALL_DOCS];
   int row[SMALL_DOCS], st[SMALL_DOCS], ln[SMALL_DOCS], first[SMALL_DOCS], order[SMALL_DOCS];
   int cum[SMALL_DOCS + 1];
+  int cnt[SMALL_DOCS];  // per doc: the tokens to scan / to copy
   int dl[PLAN_WINDOW];
   RingState rs;
   int stop;  // a wait gave up: no doc of the call is placed
@@ -144,7 +149,8 @@ __device__ inline bool wait_flag(const uint32_t *f, uint32_t expect) {
   return true;
 }
 
-// The whole call in one CTA (any block size that is a multiple of 32).  Each
+// The whole call in one CTA (a block of more than SMALL_DOCS threads, a
+// multiple of 32).  Each
 // phase issues all of its loads at once over the docs' tokens laid end to
 // end: (1) the arguments and the ring state; [the bounded wait for the
 // rows' updates;] (2) the num_tokens bounds, the oldest FIFO lengths and
@@ -153,7 +159,7 @@ __device__ inline bool wait_flag(const uint32_t *f, uint32_t expect) {
 __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int m = g.m;
-  if (tid < 32) {
+  if (tid < SMALL_DOCS) {
     int ln = 0;
     bool ok = false;
     if (tid < m) {
@@ -166,11 +172,13 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
       s.ln[tid] = ok ? ln : -1;
       s.first[tid] = ln;
     }
-    small_cum(ok ? ln : 0, s.cum);
-  } else if (tid == 32) {
+    s.cnt[tid] = ok ? ln : 0;
+  } else if (tid == SMALL_DOCS) {
     s.rs = *g.rs;
     s.stop = 0;
   }
+  __syncthreads();
+  if (tid < 32) small_cum(s.cnt, s.cum);
   __syncthreads();
   const bool delta = g.ready != nullptr && g.sync != nullptr && g.dcap > 0;
   if (g.ready != nullptr) {
@@ -179,7 +187,7 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
       if (!wait_flag(g.ready + s.row[tid], g.expect)) s.ln[tid] = -2;
       __threadfence();
     }
-    if (delta && tid == 32 && !wait_flag(g.sync, g.expect)) s.stop = 1;  // every row CTA counted in
+    if (delta && tid == SMALL_DOCS && !wait_flag(g.sync, g.expect)) s.stop = 1;  // every row CTA counted in
     __syncthreads();
   }
   const RingState r0 = s.rs;
@@ -187,7 +195,7 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
   for (int j = tid; j < win; j += nthr) s.dl[j] = g.doc_len[(r0.head + j) % g.max_docs];
   long long ntv = LLONG_MAX;
   if (tid < m && g.ntok != nullptr && s.ln[tid] >= 0) ntv = g.ntok[s.row[tid]];
-  const int total = s.cum[32];
+  const int total = s.cum[SMALL_DOCS];
   for (int g0 = 0; g0 < total; g0 += nthr * SMALL_BATCH) {
     int v[SMALL_BATCH], dd[SMALL_BATCH], uu[SMALL_BATCH];
 #pragma unroll
@@ -243,9 +251,11 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
     if (w.fl) atomicOr(g.err, w.fl);
   }
   __syncthreads();
-  if (tid < 32) small_cum(tid < m && s.dest[tid] >= 0 ? s.first[tid] + 1 : 0, s.cum);
+  if (tid < SMALL_DOCS) s.cnt[tid] = tid < m && s.dest[tid] >= 0 ? s.first[tid] + 1 : 0;
   __syncthreads();
-  const int total2 = s.cum[32];
+  if (tid < 32) small_cum(s.cnt, s.cum);
+  __syncthreads();
+  const int total2 = s.cum[SMALL_DOCS];
   for (int g0 = 0; g0 < total2; g0 += nthr * SMALL_BATCH) {
     int v[SMALL_BATCH];
     long long pos[SMALL_BATCH];

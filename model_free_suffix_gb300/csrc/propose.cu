@@ -243,9 +243,8 @@ __device__ __forceinline__ void window_ends(int L0, int L1, int L2, int L3, int 
 // bytes of the ring slot), so a window without t0 costs one load, four
 // compares and a vote.  Otherwise the R most recent t0 positions are kept
 // (list1: the answer when no end matches two tokens) and every (t1, t0)
-// position, most recent first, is extended by the whole warp (pair_extend)
-// into (Mw, list).  The row's ends are few per window, so this serial form
-// has the shortest latency per window (the probe warps may wait for it).
+// position's depth is taken from the lanes' registers up to 4 tokens;
+// deeper ends are extended (window_ends) into (Mw, list).
 __device__ void self_process(const int32_t *row, int n, int S, int D, int R, const int *s_tail,
                              int *list, int *list1, int lane, SelfScan &sc, int &Mw, int &cnt,
                              int &cnt1) {
@@ -257,6 +256,7 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
   const int t0 = s_tail[0];
   const bool two = D >= 2 && n >= 2;
   const int t1 = two ? s_tail[1] : 0;
+  const int t2 = D >= 3 && n >= 3 ? s_tail[2] : 0, t3 = D >= 4 && n >= 4 ? s_tail[3] : 0;
   const int tail1 = lane + 1 < min(D, n) ? s_tail[1 + lane] : 0;
   for (int wi = sc.whi, q = 0; wi >= sc.wlo; --wi, ++q) {
     // keep SPF windows in flight; then windows q and q + 1 must have landed
@@ -284,42 +284,30 @@ __device__ void self_process(const int32_t *row, int n, int S, int D, int R, con
         if (a0) { if (slot < R) list1[slot] = p0; }
         cnt1 = min(R, cnt1 + total);
       }
-      // (t1, t0) positions: the token before position p0 is the previous
-      // lane's last one, or the last token of the window below for lane 0
+      // (t1, t0) positions.  The three tokens before a lane's first are the
+      // previous lane's last three, or the window below's for lane 0.  Depths
+      // 2..4 come from these registers; only ends matching at least four
+      // tokens are extended (window_ends: by their own lane, deeper ones by the
+      // whole warp), so a bigram occurring hundreds of times in the row costs
+      // no serial extension per occurrence.
       const int4 prv = sc.ring[((q + 1) % SR) * 32 + lane];
-      const int up = __shfl_up_sync(FULL, cur.w, 1);
-      const int below = __shfl_sync(FULL, prv.w, 31);
-      const int before0 = lane == 0 ? below : up;
-      unsigned m0 = __ballot_sync(FULL, a0 && two && p0 >= 1 && before0 == t1);
-      unsigned m1 = __ballot_sync(FULL, a1 && two && cur.x == t1);
-      unsigned m2 = __ballot_sync(FULL, a2 && two && cur.y == t1);
-      unsigned m3 = __ballot_sync(FULL, a3 && two && cur.z == t1);
-      if (m0 | m1 | m2 | m3) {
+      int py = __shfl_up_sync(FULL, cur.y, 1), pz = __shfl_up_sync(FULL, cur.z, 1);
+      int pv = __shfl_up_sync(FULL, cur.w, 1);
+      const int by = __shfl_sync(FULL, prv.y, 31), bz = __shfl_sync(FULL, prv.z, 31);
+      const int bw = __shfl_sync(FULL, prv.w, 31);
+      if (lane == 0) { py = by; pz = bz; pv = bw; }
+      const bool c0 = a0 && two && pv == t1, c1 = a1 && two && cur.x == t1;
+      const bool c2 = a2 && two && cur.y == t1, c3 = a3 && two && cur.z == t1;
+      if (__any_sync(FULL, c0 | c1 | c2 | c3)) {
         __syncwarp();  // every lane's copies visible to the warp (the extension reads across lanes)
         const int *cw = reinterpret_cast<const int *>(sc.ring + (q % SR) * 32);
         const int *pw = reinterpret_cast<const int *>(sc.ring + ((q + 1) % SR) * 32);
-        for (;;) {  // candidates in descending position 4 * lane + c
-          int best = -1;
-          if (m0) best = 4 * (31 - __clz(m0));
-          if (m1) best = max(best, 4 * (31 - __clz(m1)) + 1);
-          if (m2) best = max(best, 4 * (31 - __clz(m2)) + 2);
-          if (m3) best = max(best, 4 * (31 - __clz(m3)) + 3);
-          if (best < 0) break;
-          const unsigned keep = ~(1u << (best >> 2));
-          const int bc = best & 3;
-          m0 = bc == 0 ? m0 & keep : m0;
-          m1 = bc == 1 ? m1 & keep : m1;
-          m2 = bc == 2 ? m2 & keep : m2;
-          m3 = bc == 3 ? m3 & keep : m3;
-          const int jj = base + best;
-          // the row's text starts at position 0: pair index WIN - base
-          const int L = pair_extend(WIN + best, WIN - base, cw, pw, D, s_tail, tail1, lane);
-          if (L > Mw) { Mw = L; cnt = 0; }
-          if (L == Mw && cnt < R) {
-            if (lane == 0) list[cnt] = jj;
-            ++cnt;
-          }
-        }
+        // (the row's text starts at position 0: pair index WIN - base)
+        const int lo = WIN - base;
+        int L0, L1, L2, L3;
+        window_depths(cur, pv, pz, py, t0, t1, t2, t3, D, 2, lo, lane, c0, c1, c2, c3, L0, L1, L2, L3);
+        window_ends(L0, L1, L2, L3, base + 4 * lane, lo, cw, pw, D, s_tail, tail1, lane, R, list, Mw,
+                    cnt);
         __syncwarp();  // cross-lane reads of the slot done before it is refilled
       }
     }
@@ -1035,13 +1023,21 @@ __device__ __forceinline__ int draft_cap(const ProposeArgs &a, int M, int n) {
   return c < 0 ? 0 : (int)c;
 }
 
+// Appends the leading run of ids in [0, V) of sp[0, T) to row at n (ids past
+// S dropped) and returns the new length.  The first 64 ids are read once
+// (`sp` may be page-locked host memory read in place).  With tail != null the
+// appended ids also go to tail[0 .. min(appended, dtail)), newest first
+// (tail[i] = the token at new length - 1 - i).  Whole warp.
 __device__ int update_row_warp(int32_t *row, int n, const int32_t *sp, int T, int S, int V, int lane,
-                               uint32_t &fl) {
+                               uint32_t &fl, int *tail = nullptr, int dtail = 0) {
   int c = T;
   bool bad = false;
+  int keep0 = 0, keep1 = 0;  // sp[lane], sp[32 + lane]
   for (int base = 0; base < T; base += 32) {
     const int i = base + lane;
     const int v = i < T ? sp[i] : 0;
+    if (base == 0) keep0 = v;
+    else if (base == 32) keep1 = v;
     const bool term = i < T && (v < 0 || v >= V);
     const unsigned m = __ballot_sync(FULL, term);
     if (m) {
@@ -1052,10 +1048,14 @@ __device__ int update_row_warp(int32_t *row, int n, const int32_t *sp, int T, in
       break;
     }
   }
-  for (int i = lane; i < c; i += 32)
-    if ((long long)n + i < S) row[n + i] = sp[i];
+  const int ca = (int)min((long long)c, (long long)S - n);  // ids that fit
+  for (int i = lane; i < ca; i += 32) {
+    const int v = i < 32 ? keep0 : (i < 64 ? keep1 : sp[i]);
+    row[n + i] = v;
+    if (tail != nullptr && ca - 1 - i < dtail) tail[ca - 1 - i] = v;
+  }
   if (bad) fl |= SGD_ERR_SAMPLED_TOKEN;
-  return (int)min((long long)S, (long long)n + c);
+  return n + max(ca, 0);
 }
 
 __global__ void __launch_bounds__(128) update_kernel(int32_t *tok, int32_t *ntok, const int32_t *sampled,
@@ -1403,7 +1403,6 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ long long s_bound[2 * NPROBE3];
   __shared__ int s_n, s_Ms, s_cs, s_q, s_sel, s_need, s_have_corpus;
   __shared__ int s_self_done, s_ms_ready, s_pms, s_Mc, s_c0c, s_cpf;
-  __shared__ int s_early[4], s_early_ok;  // last four tokens, known from the update
   __shared__ int s_ckey;  // short level whose continuation comes from keys and records, or 0
   // the delta: ring start, visible tokens, longest match and its ends (their
   // list is in s_wlist1 once merged); the fused step's epoch
@@ -1415,9 +1414,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ uint32_t s_ep;
   __shared__ int s_scan;  // suffix-array hits the probe warps scanned (row statistics)
   // the row's bigram index: its entries cover the row (maintenance), the self
-  // match may come from it, the row length before the update, the last two
-  // tokens after it, the looked-up count and positions, self match deferred
-  __shared__ int s_iok, s_iuse, s_nold, s_il0, s_il1, s_icnt, s_idefer, s_igen, s_inc;
+  // match may come from it, the row length before the update, the looked-up
+  // count and positions, self match deferred
+  __shared__ int s_iok, s_iuse, s_nold, s_icnt, s_idefer, s_igen, s_inc;
   __shared__ int s_imode;  // how the row's own match was found (row statistics)
   __shared__ int s_ipos[RI_K];
 
@@ -1479,38 +1478,41 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
     if (n > S) { n = S; fl |= SGD_ERR_NUM_TOKENS; }
     const int n_old = n;
-    // (the row's last two tokens before the update, read with the sampled ids)
-    const int o1 = IDX && a.ri.tab && n_old >= 1 ? row[n_old - 1] : 0;
-    const int o2 = IDX && a.ri.tab && n_old >= 2 ? row[n_old - 2] : 0;
-    if (a.do_update) n = update_row_warp(row, n, a.sampled + (size_t)b * a.T, a.T, S, a.V, lane, fl);
+    // The row's last D tokens before the update, read with the sampled ids: the
+    // tail after the update is the appended ids (newest first) followed by
+    // them, so it never has to be read back from the row.
+    const int dl0 = min(D, n_old);
+    int ot[MAX_D / 32];
+#pragma unroll
+    for (int u = 0; u < MAX_D / 32; ++u) {
+      const int i = lane + 32 * u;
+      ot[u] = i < dl0 ? row[n_old - 1 - i] : 0;
+    }
+    if (a.do_update)
+      n = update_row_warp(row, n, a.sampled + (size_t)b * a.T, a.T, S, a.V, lane, fl, s_tail, D);
     if (lane == 0 && a.do_update) a.ntok[b] = n;
+    {
+      const int ca = n - n_old, dl1 = min(D, n);
+#pragma unroll
+      for (int u = 0; u < MAX_D / 32; ++u) {
+        const int i = lane + 32 * u;
+        if (i < dl0 && i + ca < dl1) s_tail[i + ca] = ot[u];
+      }
+    }
     if (IDX && lane == 0) {
       const bool iok = a.ri.tab != nullptr && covered == n_in && covered == n_old;
       // the last two tokens after the update: appended ids, else the old ones
-      auto last = [&](int pos) {
-        return pos >= n_old ? a.sampled[(size_t)b * a.T + (pos - n_old)]
-                            : (pos == n_old - 1 ? o1 : o2);
-      };
       s_iok = iok;
       s_iuse = iok && n >= 2 && D >= 2;
       s_nold = n_old;
-      s_il0 = n >= 1 ? last(n - 1) : 0;
-      s_il1 = n >= 2 ? last(n - 2) : 0;
       s_icnt = -1;
       s_idefer = 0;
       s_igen = igen;
       s_imode = 0;
     }
-    // When the update appended >= 4 ids, the last four tokens are those ids:
-    // the probe warps can look the n-grams up before the tail is read back.
-    bool early = a.do_update && n - n_old >= 4;
-    // (plain loads: `sampled` may be page-locked host memory read in place)
-    if (early && lane < 4) s_early[lane] = a.sampled[(size_t)b * a.T + (n - n_old) - 1 - lane];
     if (FROM_RES) {  // the first launch's result: Ms, cs, the last four tokens; the delta's
       const int32_t *res = a.self_res + (size_t)b * self_res_ints(R);
       const int v = lane < 6 ? __ldg(res + lane) : (EXT && lane < 10 ? __ldg(res + R + lane) : 0);
-      if (lane >= 2 && lane < 6) s_early[lane - 2] = v;
-      early = n >= 4;
       const int Ms = __shfl_sync(FULL, v, 0), cs = __shfl_sync(FULL, v, 1);
       const int Md = __shfl_sync(FULL, v, 6), cd = __shfl_sync(FULL, v, 7);
       const int ds = __shfl_sync(FULL, v, 8), dv = __shfl_sync(FULL, v, 9);
@@ -1533,7 +1535,6 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     }
     if (lane == 0) {
       if (fl) atomicOr(a.err, fl);
-      s_early_ok = early;
       s_n = n;
       s_have_corpus = a.desc != nullptr && cp.N >= 2;
       s_self_done = 0;
@@ -1594,21 +1595,20 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   }
   const bool corpus_ok = s_have_corpus && D >= 2 && n >= 2;
 
-  // ---- phase 1: tail[i] = t[n-1-i]; self warps prefetch their first windows ----
+  // ---- phase 1: (tail[i] = t[n-1-i] is in shared memory already) the self
+  // warps prefetch their first windows; with an n-gram table the probe warps
+  // find their intervals ----
   const int dl = min(D, n);
-  for (int i = tid; i < dl; i += nthr) s_tail[i] = row[n - 1 - i];
-  // with the last four tokens known from the update and an n-gram table, the
-  // probe warps find their intervals now, while the tail is being read
-  const bool early_bounds = corpus_ok && s_early_ok && cp.GT != nullptr;
+  const bool early_bounds = corpus_ok && cp.GT != nullptr;
   if (early_bounds && warp >= a.nself)
-    pattern_bounds(cp, s_early, 4 - (warp - a.nself), D, n, lane, &s_bound[2 * (warp - a.nself)]);
+    pattern_bounds(cp, s_tail, 4 - (warp - a.nself), D, n, lane, &s_bound[2 * (warp - a.nself)]);
   SelfScan sc;
   // With a usable row index, warp 0 looks the row's last bigram up while the
   // tail is read, and the self warps fetch no window before they know whether
   // the row must be scanned at all.
   const bool use_idx = IDX && s_iuse;
   if (use_idx && warp == 0) {
-    const int c = ri_lookup(a.ri.tab + (size_t)b * a.ri.H * RI_ENTRY, a.ri.H, s_igen, s_il1, s_il0,
+    const int c = ri_lookup(a.ri.tab + (size_t)b * a.ri.H * RI_ENTRY, a.ri.H, s_igen, s_tail[1], s_tail[0],
                             lane, s_ipos);
     if (lane == 0) s_icnt = c;
   }
@@ -1645,7 +1645,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     // tokens (decided after the corpus, see below)
     int imode = 0;
     if (use_idx) {
-      imode = index_self(row, n, s_nold, D, R, a.nself, warp, lane, s_il1, s_il0, s_icnt, s_ipos, s_tail,
+      imode = index_self(row, n, s_nold, D, R, a.nself, warp, lane, s_tail[1], s_tail[0], s_icnt, s_ipos, s_tail,
                          s_wlist, s_wlist1, a.nself * R, &s_inc, s_occ, &s_Ms, &s_cs, &s_ms_ready);
       if (imode == 2 && warp == 0 && lane == 0) s_idefer = 1;
       if (warp == 0 && lane == 0) s_imode = imode;
@@ -2132,7 +2132,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     const int tot = (src == 2 && s_cpf && nd == 0) ? 0 : c0 * cap;
     const int ck = src == 2 && nd == 0 ? s_ckey : 0;
     const int *occp = reinterpret_cast<const int *>(s_L) + a.cand_cap;
-    for (int idx = tid; idx < tot; idx += nthr) {
+    auto item = [&](int idx) {
       const int o = idx / cap, d = idx - o * cap;
       const long long pos = (long long)occ[o] + 1 + d;
       int v;
@@ -2151,7 +2151,22 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       } else {
         v = pos < cp.N ? __ldg(cp.X + pos) : Z;
       }
-      cont[o * capp + d] = v;
+      return v;
+    };
+    // four loads in flight per thread: the continuations are independent reads
+    constexpr int GB = 4;
+    for (int i0 = tid; i0 < tot; i0 += GB * nthr) {
+      int v[GB];
+#pragma unroll
+      for (int u = 0; u < GB; ++u) v[u] = i0 + u * nthr < tot ? item(i0 + u * nthr) : 0;
+#pragma unroll
+      for (int u = 0; u < GB; ++u) {
+        const int idx = i0 + u * nthr;
+        if (idx < tot) {
+          const int o = idx / cap;
+          cont[o * capp + (idx - o * cap)] = v[u];
+        }
+      }
     }
     __syncthreads();
     for (int o = tid; o < c0; o += nthr) {

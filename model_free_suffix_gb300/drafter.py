@@ -183,7 +183,7 @@ class SuffixDrafter:
              active: Optional[torch.Tensor] = None, out: Optional[Proposal] = None,
              stream=None) -> Proposal:
         """propose_with_update, then ingest of the docs (rows, starts, lengths)
-        read after the update: one kernel launch for up to 32 docs."""
+        read after the update: one kernel launch for up to 64 docs."""
         B, T = sampled.shape
         m = rows.shape[0]
         out = out or self.new_outputs(B)

@@ -1,7 +1,7 @@
 """The fused decoding step (sgd_step) against the oracle.
 
 sgd_step is sgd_propose_with_update followed by sgd_ingest of the step's
-finished docs; up to 32 docs run inside the same kernel launch (one extra CTA
+finished docs; up to 64 docs run inside the same kernel launch (one extra CTA
 appends them once their rows are updated).  Drafts, the updated rows, the
 ring and every snapshot built from it must equal the oracle's, step after
 step, whether the step runs as one launch or as the two calls.
@@ -32,12 +32,14 @@ def _ring_matches(ls):
 
 
 @pytest.mark.parametrize("mode", [1, 2], ids=["one-launch", "two-launch"])
-@pytest.mark.parametrize("finish_frac", [0.1, 0.6])
-def test_fused_step_matches_oracle(finish_frac, mode):
-    """0.1: a few docs per step (in-kernel ingest); 0.6: more than 32 docs (two calls)."""
+@pytest.mark.parametrize("finish_frac,B", [(0.1, 64), (0.45, 128), (0.6, 128)],
+                         ids=["6-docs", "57-docs", "76-docs"])
+def test_fused_step_matches_oracle(finish_frac, B, mode):
+    """A few docs per step and 33-64 docs (in-kernel ingest); more than 64
+    docs (two calls)."""
     W, O, H = _mods()
     cfg = dataclasses.replace(W.CONFIGS["c3"], rebuild_tokens=2048)
-    ls = H.Lockstep(cfg, seed=3, B=64, steps=14, finish_frac=finish_frac, corpus=1 << 16, fused=True,
+    ls = H.Lockstep(cfg, seed=3, B=B, steps=14, finish_frac=finish_frac, corpus=1 << 16, fused=True,
                     drafter_over=dict(propose_mode=mode))
     ls.prefill(seed=3)
     docs = 0
@@ -46,6 +48,8 @@ def test_fused_step_matches_oracle(finish_frac, mode):
         docs += sd.finished.shape[0]
         _ring_matches(ls)
     assert docs > 0 and ls.generation >= 2
+    if ls.build_pending:  # (a rebuild the last steps started)
+        ls.swap()
     ls.build_and_swap()
     text, sa, _ = ls.dr.export_snapshot()
     assert text.cpu().numpy().tolist() == ls.X.tolist()
