@@ -21,7 +21,8 @@ namespace {
 
 constexpr int PLAN_WINDOW = 1024;  // oldest FIFO lengths staged for evictions
 constexpr int SMALL_DOCS = 64;     // calls up to this size run in one CTA (of > 64 threads)
-constexpr int SMALL_BATCH = 4;     // loads each thread has in flight per sweep
+constexpr int SMALL_BATCH = 8;     // loads each thread has in flight per sweep
+constexpr int STAGE_TOKENS = 8192; // validated doc tokens kept on chip for the copy
 constexpr unsigned STEP_SPIN_LIMIT = 1u << 17;  // ~0.1 s of polling; a normal wait is microseconds
 
 // Sequential placement, in call order: evict the oldest docs while the new
@@ -106,13 +107,25 @@ struct SmallIngestSmem {
   int64_t dest[SMALL_DOCS];
   int row[SMALL_DOCS], st[SMALL_DOCS], ln[SMALL_DOCS], first[SMALL_DOCS], order[SMALL_DOCS];
   int cum[SMALL_DOCS + 1];
+  int vcum[SMALL_DOCS + 1];  // the scan's prefix sums (where a doc's staged tokens start)
   int cnt[SMALL_DOCS];  // per doc: the tokens to scan / to copy
+  int pcum[SMALL_DOCS + 1], kcum[SMALL_DOCS + 1];  // placement: ring tokens, docs before each
+  int ev[SMALL_DOCS];   // placement: oldest docs evicted before each doc is placed
+  int ntv[SMALL_DOCS];  // the num_tokens bound of each doc's row
   int dl[PLAN_WINDOW];
+  int esum[PLAN_WINDOW + 1];  // ring tokens of the oldest docs, prefix sums
   RingState rs;
-  int stop;  // a wait gave up: no doc of the call is placed
+  int stop;    // a wait gave up: no doc of the call is placed
+  int serial;  // the parallel placement does not apply: one thread walks the docs
   long long placed;
-  SigBatchSmem sig;
+  union {
+    SigBatchSmem sig;             // (after the copy)
+    int32_t tok[STAGE_TOKENS];    // the first STAGE_TOKENS doc tokens, as scanned
+  } u;
 };
+
+// (a static shared-memory array in the standalone ingest kernel)
+static_assert(sizeof(SmallIngestSmem) <= 48 * 1024, "SmallIngestSmem exceeds static shared memory");
 
 struct SmallIngest {
   const int32_t *tok;   // [B, S]
@@ -150,12 +163,12 @@ __device__ inline bool wait_flag(const uint32_t *f, uint32_t expect) {
 }
 
 // The whole call in one CTA (a block of more than SMALL_DOCS threads, a
-// multiple of 32).  Each
-// phase issues all of its loads at once over the docs' tokens laid end to
-// end: (1) the arguments and the ring state; [the bounded wait for the
-// rows' updates;] (2) the num_tokens bounds, the oldest FIFO lengths and
-// every token (first id outside [0, V) per doc); thread 0 then places the
-// docs from shared memory; (3) the copy into the ring.
+// multiple of 32): (1) the arguments and the ring state; (2) per doc, by the
+// warps in turn, [the bounded wait for its row's update,] its tokens read
+// once (the first id outside [0, V) ends it) and staged on chip, and its
+// row's num_tokens bound; the oldest FIFO lengths; (3) the placement (in
+// parallel from prefix sums; one thread when evictions reach past the staged
+// FIFO lengths); (4) the copy into the ring from the staged tokens.
 __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s) {
   const int tid = threadIdx.x, nthr = blockDim.x;
   const int m = g.m;
@@ -181,37 +194,54 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
   if (tid < 32) small_cum(s.cnt, s.cum);
   __syncthreads();
   const bool delta = g.ready != nullptr && g.sync != nullptr && g.dcap > 0;
-  if (g.ready != nullptr) {
-    if (tid < m && s.ln[tid] >= 0) {
-      // give the doc up rather than read a row mid-update
-      if (!wait_flag(g.ready + s.row[tid], g.expect)) s.ln[tid] = -2;
-      __threadfence();
-    }
-    if (delta && tid == SMALL_DOCS && !wait_flag(g.sync, g.expect)) s.stop = 1;  // every row CTA counted in
-    __syncthreads();
-  }
+  if (delta && tid == SMALL_DOCS && !wait_flag(g.sync, g.expect)) s.stop = 1;  // every row CTA counted in
   const RingState r0 = s.rs;
   const int win = min(r0.ndocs, PLAN_WINDOW);
   for (int j = tid; j < win; j += nthr) s.dl[j] = g.doc_len[(r0.head + j) % g.max_docs];
-  long long ntv = LLONG_MAX;
-  if (tid < m && g.ntok != nullptr && s.ln[tid] >= 0) ntv = g.ntok[s.row[tid]];
-  const int total = s.cum[SMALL_DOCS];
-  for (int g0 = 0; g0 < total; g0 += nthr * SMALL_BATCH) {
-    int v[SMALL_BATCH], dd[SMALL_BATCH], uu[SMALL_BATCH];
-#pragma unroll
-    for (int b = 0; b < SMALL_BATCH; ++b) {
-      const int gi = g0 + b * nthr + tid;
-      dd[b] = -1;
-      if (gi < total) {
-        const int d = small_doc(s.cum, m, gi);
-        dd[b] = d;
-        uu[b] = gi - s.cum[d];
-        v[b] = g.tok[(size_t)s.row[d] * g.S + s.st[d] + uu[b]];
+  if (tid <= SMALL_DOCS) s.vcum[tid] = s.cum[tid];
+  // Each warp takes docs w, w + warps, ...: waits (bounded) for the doc's row
+  // to be updated, then reads the doc's tokens once -- the first id outside
+  // [0, V) ends it -- staging them on chip for the copy.  Docs of rows that
+  // were updated early are read while later rows are still being drafted.
+  const int warp = tid >> 5, lane = tid & 31, nwarps = nthr >> 5;
+  for (int d = warp; d < m; d += nwarps) {
+    if (s.ln[d] < 0) continue;  // bad arguments
+    if (g.ready != nullptr) {
+      // give the doc up rather than read a row mid-update
+      bool ok = true;
+      if (lane == 0) ok = wait_flag(g.ready + s.row[d], g.expect);
+      ok = __shfl_sync(FULL, ok, 0);
+      __threadfence();
+      if (!ok) {
+        if (lane == 0) s.ln[d] = -2;
+        continue;
       }
     }
+    const int ln = s.ln[d];
+    const int32_t *src = g.tok + (size_t)s.row[d] * g.S + s.st[d];
+    int bad = ln;  // first id outside [0, V)
+    for (int u0 = 0; u0 < ln; u0 += 32 * SMALL_BATCH) {
+      int v[SMALL_BATCH];
 #pragma unroll
-    for (int b = 0; b < SMALL_BATCH; ++b)
-      if (dd[b] >= 0 && (v[b] < 0 || v[b] >= g.V)) atomicMin(&s.first[dd[b]], uu[b]);
+      for (int b = 0; b < SMALL_BATCH; ++b) {
+        const int u = u0 + 32 * b + lane;
+        v[b] = u < ln ? src[u] : 0;
+      }
+#pragma unroll
+      for (int b = 0; b < SMALL_BATCH; ++b) {
+        const int u = u0 + 32 * b + lane;
+        if (u < ln) {
+          if (v[b] < 0 || v[b] >= g.V) bad = min(bad, u);
+          const int sg = s.cum[d] + u;  // (s.vcum is copied from s.cum meanwhile)
+          if (sg < STAGE_TOKENS) s.u.tok[sg] = v[b];
+        }
+      }
+    }
+    bad = __reduce_min_sync(FULL, (unsigned)bad);
+    if (lane == 0) {
+      s.first[d] = bad;
+      s.ntv[d] = g.ntok != nullptr ? g.ntok[s.row[d]] : INT_MAX;
+    }
   }
   __syncthreads();
   if (tid < m) {
@@ -219,7 +249,7 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
     if (ln == -2) {
       s.first[tid] = -1;
       atomicOr(g.err, SGD_ERR_INGEST_WAIT);
-    } else if (ln < 0 || (long long)s.st[tid] + ln > ntv) {
+    } else if (ln < 0 || (long long)s.st[tid] + ln > s.ntv[tid]) {
       s.first[tid] = -1;
       atomicOr(g.err, SGD_ERR_DOC_ARGS);
     } else if (s.first[tid] < ln) {
@@ -243,12 +273,110 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
         atomicOr(g.err, SGD_ERR_INGEST_WAIT);
       }
     }
-    PlanWalk w{r0, r0.ndocs, win, 0, 0, 0, 0u, 0};
-    for (int i = 0; i < m; ++i)
-      place_doc(w, i, s.first[i], g.C, s.dl, g.doc_start, g.doc_len, g.max_docs, s.dest, s.order);
-    *g.rs = w.r;
-    s.placed = w.placed;
-    if (w.fl) atomicOr(g.err, w.fl);
+  }
+  __syncthreads();
+  // Placement.  Docs go to the write offset in call order, each after
+  // evicting the oldest docs while it would not fit (or the FIFO is full).
+  // Doc i's place follows from the ring sizes of the docs before it (pcum),
+  // and the evictions before it from the prefix sums of the oldest docs'
+  // sizes (esum): the fewest oldest docs whose removal makes room, a count
+  // that can only grow with i.  This holds while those docs are among the
+  // staged oldest ones and no doc of this call has to go; otherwise thread 0
+  // walks the docs one by one.
+  if (tid < SMALL_DOCS) {
+    const int L = tid < m ? s.first[tid] : -1;
+    const bool too_long = L > 0 && (long long)L + 1 > g.C;
+    if (too_long) atomicOr(g.err, SGD_ERR_DOC_TOO_LONG);
+    s.cnt[tid] = L > 0 && !too_long ? L + 1 : 0;
+  } else if (tid == SMALL_DOCS) {
+    s.serial = 0;
+  }
+  __syncthreads();
+  if (tid < 32) {
+    small_cum(s.cnt, s.pcum);
+    // the oldest docs' ring sizes, prefix sums over the staged window
+    int run = 0;
+    if (tid == 0) s.esum[0] = 0;
+    for (int j0 = 0; j0 < win; j0 += 32) {
+      const int j = j0 + tid;
+      int x = j < win ? s.dl[j] + 1 : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(FULL, x, off);
+        if (tid >= off) x += y;
+      }
+      if (j < win) s.esum[j + 1] = run + x;
+      run += __shfl_sync(FULL, x, 31);
+    }
+  } else if (tid >= 32 && tid < 64) {
+    // docs placed before each: the same scan over 0/1
+    int c[2];
+    const int l = tid - 32;
+    c[0] = s.cnt[2 * l] > 0;
+    c[1] = s.cnt[2 * l + 1] > 0;
+    int x = c[0] + c[1];
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(FULL, x, off);
+      if (l >= off) x += y;
+    }
+    s.kcum[2 * l + 1] = x - c[1];
+    s.kcum[2 * l + 2] = x;
+    if (l == 0) s.kcum[0] = 0;
+  }
+  __syncthreads();
+  if (tid < m && s.cnt[tid] > 0) {
+    // the fewest oldest docs e with live - esum[e] + pcum[tid + 1] <= C and
+    // ndocs - e + kcum[tid + 1] <= max_docs
+    const long long need = r0.live + s.pcum[tid + 1] - g.C;
+    int lo = 0, hi = win + 1;  // esum[e] >= need for the smallest e in [lo, hi)
+    if (need > 0) {
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (s.esum[mid] >= need) hi = mid;
+        else lo = mid + 1;
+      }
+    }
+    const int e = max(lo, r0.ndocs + s.kcum[tid + 1] - g.max_docs);
+    if (e > win || e > r0.ndocs) s.serial = 1;
+    s.ev[tid] = e;
+  }
+  __syncthreads();
+  if (s.serial) {
+    if (tid == 0) {
+      PlanWalk w{r0, r0.ndocs, win, 0, 0, 0, 0u, 0};
+      for (int i = 0; i < m; ++i)
+        place_doc(w, i, s.first[i], g.C, s.dl, g.doc_start, g.doc_len, g.max_docs, s.dest, s.order);
+      *g.rs = w.r;
+      s.placed = w.placed;
+    }
+  } else {
+    if (tid < m) {
+      if (s.cnt[tid] > 0) {
+        const long long d = (r0.wp + s.pcum[tid]) % g.C;
+        const int slot = (int)(((long long)r0.head + r0.ndocs + s.kcum[tid]) % g.max_docs);
+        g.doc_start[slot] = d;
+        g.doc_len[slot] = s.first[tid];
+        s.dest[tid] = d;
+        s.order[s.kcum[tid]] = tid;
+      } else {
+        s.dest[tid] = -1;
+      }
+    }
+    if (tid == 0) {
+      const int K = s.kcum[m], P = s.pcum[m];
+      int e = 0;  // evictions by the last doc placed
+      for (int i = m - 1; i >= 0; --i)
+        if (s.cnt[i] > 0) { e = s.ev[i]; break; }
+      RingState r = r0;
+      r.live = r0.live - s.esum[e] + P;
+      r.head = (int)(((long long)r0.head + e) % g.max_docs);
+      r.ndocs = r0.ndocs - e + K;
+      r.wp = (r0.wp + P) % g.C;
+      r.pushed = r0.pushed + K;
+      *g.rs = r;
+      s.placed = P;
+    }
   }
   __syncthreads();
   if (tid < SMALL_DOCS) s.cnt[tid] = tid < m && s.dest[tid] >= 0 ? s.first[tid] + 1 : 0;
@@ -266,7 +394,9 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
       if (gi < total2) {
         const int d = small_doc(s.cum, m, gi);
         const int u = gi - s.cum[d];
-        v[b] = u < s.first[d] ? g.tok[(size_t)s.row[d] * g.S + s.st[d] + u] : g.V;
+        const int sg = s.vcum[d] + u;  // where the scan staged it
+        v[b] = u < s.first[d] ? (sg < STAGE_TOKENS ? s.u.tok[sg] : g.tok[(size_t)s.row[d] * g.S + s.st[d] + u])
+                              : g.V;
         long long p = s.dest[d] + u;
         if (p >= g.C) p -= g.C;
         pos[b] = p;
@@ -278,7 +408,7 @@ __device__ inline void ingest_small_cta(const SmallIngest &g, SmallIngestSmem &s
   }
   if (g.sig != nullptr && s.placed > 0) {
     __syncthreads();  // the docs are in the ring
-    sig_update_cta(SigBuild{g.ring, g.C, g.V, g.sig, g.C / WIN}, r0.wp, s.placed, s.sig);
+    sig_update_cta(SigBuild{g.ring, g.C, g.V, g.sig, g.C / WIN}, r0.wp, s.placed, s.u.sig);
   }
 }
 
