@@ -56,6 +56,7 @@ struct sgd_ctx {
   void *zc_dev[9] = {};
   bool zc_ok = false;
   int split = 0;
+  int stage_keys = 0;               // the probe descends the key array (no n-gram tables)
   int32_t *d_ring = nullptr;
   RingState *d_rs = nullptr;
   int64_t *d_doc_start = nullptr;
@@ -343,10 +344,19 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
   x->corpus = cfg->corpus_capacity > 0;
   x->split = cfg->propose_mode == 2;
   {
-    const int R = cfg->max_occurrences, k = cfg->k, cc = cfg->corpus_cand_cap;
-    x->smem = x->split ? std::max(propose_smem_bytes(1, x->nself, R, k, cc),
-                                  propose_smem_bytes(2, 1, R, k, cc))
-                       : propose_smem_bytes(0, x->nself, R, k, cc);
+    // with n-gram tables the probe never descends the key array, so its top
+    // levels are not staged in shared memory
+    bool gt_on = false;
+    if (x->corpus) {
+      unsigned long long nb = 1;
+      while (nb < (unsigned long long)cfg->corpus_capacity) nb <<= 1;
+      gt_on = cfg->corpus_gram_index && 2ull * nb * GT_BUCKET * GT_ENTRY * 4ull <= SGD_RECORD_BUDGET;
+    }
+    x->stage_keys = x->corpus && !gt_on;
+    const int R = cfg->max_occurrences, k = cfg->k, cc = cfg->corpus_cand_cap, sk = x->stage_keys;
+    x->smem = x->split ? std::max(propose_smem_bytes(1, x->nself, R, k, cc, sk),
+                                  propose_smem_bytes(2, 1, R, k, cc, sk))
+                       : propose_smem_bytes(0, x->nself, R, k, cc, sk);
   }
   cudaError_t e = cudaSuccess;
   auto al = [&](void **p, size_t bytes) {
@@ -505,6 +515,7 @@ static ProposeArgs base_args(sgd_ctx *x) {
   a.nb = c.num_backoff;
   a.row_stats = x->d_row_stats;
   a.ri = x->ri;
+  a.stage_keys = x->stage_keys;
   if (c.draft_mode == 1) {  // no probability floor: the vote runs while an occurrence continues
     a.fixed = 1;
     a.pN = 0;

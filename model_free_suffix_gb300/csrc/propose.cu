@@ -686,8 +686,8 @@ struct Corpus {
 };
 
 __device__ __forceinline__ int4 key_at(const Corpus &c, int l, long long q) {
-  if (l == c.Lmax) return c.s_top[q >> (5 * l)];
-  if (l == c.Lmax - 1) return c.s_mid[q >> (5 * l)];
+  if (c.s_top != nullptr && l == c.Lmax) return c.s_top[q >> (5 * l)];
+  if (c.s_mid != nullptr && l == c.Lmax - 1) return c.s_mid[q >> (5 * l)];
   return __ldg(c.K + q);
 }
 
@@ -1413,6 +1413,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ int s_dcB, s_dcN, s_dmore;     // the CTA's delta list: length, ends; another round
   __shared__ uint32_t s_ep;
   __shared__ int s_scan;  // suffix-array hits the probe warps scanned (row statistics)
+  // the last four tokens known from the sampled ids (probe warps, phase 0)
+  __shared__ int s_l4[4], s_pre, s_pre_n;
   // the row's bigram index: its entries cover the row (maintenance), the self
   // match may come from it, the row length before the update, the looked-up
   // count and positions, self match deferred
@@ -1437,11 +1439,15 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int boff = (MAX_D + 2 * a.nself * R + 3 * R + 3) & ~3;
   int *s_big = dsm + boff;             // max(cand_cap, R * roundup4(k))
   const int koff = (boff + big + 3) & ~3;
-  int4 *s_top = reinterpret_cast<int4 *>(dsm + koff);                  // TOP_KEYS
-  int4 *s_mid = s_top + TOP_KEYS;                                      // MID_KEYS
-  unsigned char *s_L = reinterpret_cast<unsigned char *>(s_mid + MID_KEYS);  // LCAP
+  // the top two levels of the key array, staged only for a descent (a
+  // context without n-gram tables)
+  int4 *s_keys = reinterpret_cast<int4 *>(dsm + koff);
+  int4 *s_top = a.stage_keys ? s_keys : nullptr;                       // TOP_KEYS
+  int4 *s_mid = a.stage_keys ? s_keys + TOP_KEYS : nullptr;            // MID_KEYS
+  unsigned char *s_L =
+      reinterpret_cast<unsigned char *>(s_keys + (a.stage_keys ? TOP_KEYS + MID_KEYS : 0));  // LCAP
   // nself * SR windows; the self-only launch has no corpus areas before them
-  int4 *s_ring = SELF_ONLY ? s_top : reinterpret_cast<int4 *>(s_L + LCAP);
+  int4 *s_ring = SELF_ONLY ? s_keys : reinterpret_cast<int4 *>(s_L + LCAP);
 
   // ---- phase 0: warp 0 updates the row; the others fetch the snapshot
   // descriptor and stage the top two levels of its key array ----
@@ -1558,7 +1564,50 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         s_cd = 0;
       }
     }
-  } else if (!SELF_ONLY && a.desc != nullptr && cp.N >= 2 && cp.GT == nullptr) {
+  } else if (!SELF_ONLY && !FROM_RES && a.do_update && cp.GT != nullptr && cp.N >= 2 && D >= 2 &&
+             warp >= a.nself) {
+    // When the update appends >= 4 ids, the last four tokens are those ids:
+    // the probe warps look their n-grams up now, beside warp 0's update,
+    // instead of after the tail is assembled.  Probe warp 0 reads the row's
+    // length and the sampled ids itself (the same leading run of ids in
+    // [0, V) the update accepts).
+    const int pw = warp - a.nself;
+    if (pw == 0) {
+      int n0 = a.ntok[b];
+      n0 = n0 < 0 ? 0 : (n0 > S ? S : n0);
+      const int32_t *sp = a.sampled + (size_t)b * a.T;
+      int c = a.T, kp0 = 0, kp1 = 0;
+      for (int base = 0; base < a.T; base += 32) {
+        const int i = base + lane;
+        const int v = i < a.T ? sp[i] : 0;  // (plain loads: `sampled` may be host memory)
+        if (base == 0) kp0 = v;
+        else if (base == 32) kp1 = v;
+        const unsigned m = __ballot_sync(FULL, i < a.T && (v < 0 || v >= a.V));
+        if (m) {
+          c = base + __ffs(m) - 1;
+          break;
+        }
+      }
+      const int ca = min(c, S - n0);
+      const bool pre = ca >= 4 && ca <= 64;
+      if (pre) {
+        int l4 = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int j = ca - 1 - i;  // tail[i] is appended id j
+          const int v0 = __shfl_sync(FULL, kp0, j & 31), v1 = __shfl_sync(FULL, kp1, j & 31);
+          if (lane == i) l4 = j < 32 ? v0 : v1;
+        }
+        if (lane < 4) s_l4[lane] = l4;
+      }
+      if (lane == 0) {
+        s_pre = pre;
+        s_pre_n = n0 + max(ca, 0);
+      }
+    }
+    probe_sync();
+    if (s_pre) pattern_bounds(cp, s_l4, 4 - pw, D, s_pre_n, lane, &s_bound[2 * pw]);
+  } else if (!SELF_ONLY && a.stage_keys && a.desc != nullptr && cp.N >= 2 && cp.GT == nullptr) {
     const int sh = 5 * cp.Lmax;
     const long long ntop = (cp.N + (1LL << sh) - 1) >> sh;
     const long long nmid = cp.Lmax > 0 ? (cp.N + (1LL << (sh - 5)) - 1) >> (sh - 5) : 0;
@@ -1600,7 +1649,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // find their intervals ----
   const int dl = min(D, n);
   const bool early_bounds = corpus_ok && cp.GT != nullptr;
-  if (early_bounds && warp >= a.nself)
+  const bool pre_bounds = !SELF_ONLY && !FROM_RES && a.do_update && cp.GT != nullptr && cp.N >= 2 &&
+                          D >= 2 && s_pre;
+  if (early_bounds && warp >= a.nself && !pre_bounds)
     pattern_bounds(cp, s_tail, 4 - (warp - a.nself), D, n, lane, &s_bound[2 * (warp - a.nself)]);
   SelfScan sc;
   // With a usable row index, warp 0 looks the row's last bigram up while the
@@ -2276,14 +2327,14 @@ void launch_kernel(bool ext, int grid, int threads, size_t smem, cudaStream_t st
 
 }  // namespace
 
-size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap) {
+size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap, int stage_keys) {
   const size_t big = mode == 1 ? 0 : (size_t)max(cand_cap, R * ((k + 3) & ~3));
   const size_t boff = ((size_t)MAX_D + 2 * (size_t)nself * R + 3 * (size_t)R + 3) & ~(size_t)3;
   const size_t ints = (boff + big + 3) & ~(size_t)3;
   const size_t ring = (size_t)nself * SR * 32 * sizeof(int4);
   size_t bytes = sizeof(int) * ints;
   if (mode == 1) return bytes + ring;
-  bytes += sizeof(int4) * (TOP_KEYS + MID_KEYS) + LCAP + (mode == 0 ? ring : 0);
+  bytes += sizeof(int4) * (stage_keys ? TOP_KEYS + MID_KEYS : 0) + LCAP + (mode == 0 ? ring : 0);
   return bytes > sizeof(SmallIngestSmem) ? bytes : sizeof(SmallIngestSmem);
 }
 
@@ -2295,7 +2346,7 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   const bool ext = a.dcap > 0 || a.by_score;
   if (!a.split) {
     const int warps = a.nself + probe;
-    const size_t smem = propose_smem_bytes(0, a.nself, a.R, a.k, a.cand_cap);
+    const size_t smem = propose_smem_bytes(0, a.nself, a.R, a.k, a.cand_cap, a.stage_keys);
     const int grid = a.B + (a.ing_m > 0 ? 1 : 0);
     if (warps <= 12)
       launch_kernel<384, 2, 0>(ext, grid, 32 * warps, smem, st, a);
@@ -2308,7 +2359,7 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   ProposeArgs a1 = a;
   if (a.dcap == 0) a1.desc = nullptr;
   a1.ing_m = 0;
-  const size_t smem1 = propose_smem_bytes(1, a.nself, a.R, a.k, a.cand_cap);
+  const size_t smem1 = propose_smem_bytes(1, a.nself, a.R, a.k, a.cand_cap, a.stage_keys);
   if (a.nself <= 8)
     launch_kernel<256, 3, 1>(ext, a.B, 32 * a.nself, smem1, st, a1);
   else
@@ -2322,7 +2373,7 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
   a2.nself = 1;
   a2.step_ready = nullptr;
   a2.step_sync = nullptr;
-  const size_t smem2 = propose_smem_bytes(2, 1, a.R, a.k, a.cand_cap);
+  const size_t smem2 = propose_smem_bytes(2, 1, a.R, a.k, a.cand_cap, a.stage_keys);
   const int grid2 = a.B + (a.ing_m > 0 ? 1 : 0);
   launch_kernel<128, 3, 2>(ext, grid2, 32 * (1 + probe), smem2, st, a2);
   return cudaGetLastError();

@@ -174,12 +174,16 @@ struct ProposeArgs {
   // the rows' bigram position indexes: the self match from them when complete
   // (one fused kernel per step, no delta, no score-ranked selection)
   RowIndexArgs ri;
+  // 1: the snapshots have no n-gram tables, so the probe descends the key
+  // array and its top two levels are staged in shared memory
+  int stage_keys;
 };
 
 __host__ __device__ constexpr int self_res_ints(int R) { return 2 * R + 10; }
 
 // propose.cu
-size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap);  // mode as the kernel's
+// mode as the kernel's; stage_keys: the top key-array levels are staged (no n-gram tables)
+size_t propose_smem_bytes(int mode, int nself, int R, int k, int cand_cap, int stage_keys);
 int propose_step_max_docs();  // largest doc count a fused step ingests in-kernel
 cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st);
 cudaError_t launch_update(int32_t *tok, int32_t *ntok, const int32_t *sampled, int B,
