@@ -186,7 +186,7 @@ class RowStats:
     def __init__(self, dr, B, dev):
         import torch
         self.buf = torch.zeros(dr.cfg.max_batch * 4, dtype=torch.int32, device=dev)
-        self.acc = torch.zeros(4, dtype=torch.int64, device=dev)
+        self.acc = torch.zeros(5, dtype=torch.int64, device=dev)
         self.steps = 0
         self.B = B
         dr.set_row_stats(self.buf)
@@ -194,16 +194,20 @@ class RowStats:
     def add(self):
         import torch
         st = self.buf[:4 * self.B].view(self.B, 4).to(torch.int64)
-        src, how = st[:, 3] & 255, st[:, 3] >> 8
+        src, how = st[:, 3] & 255, (st[:, 3] >> 8) & 15
         corpus = (src == 2).to(torch.int64)
         gather = st[:, 1] * ((4 * st[:, 2] + 31) // 32 * 32) * corpus
-        self.acc += torch.stack([st[:, 0].sum(), gather.sum(), corpus.sum(), (how == 0).sum()])
+        # (a corpus draft read from a gram draft gathers nothing)
+        gather = gather * (1 - ((st[:, 3] >> 12) & 1))
+        self.acc += torch.stack([st[:, 0].sum(), gather.sum(), corpus.sum(), (how == 0).sum(),
+                                 ((st[:, 3] >> 12) & 1).sum()])
         self.steps += 1
 
     def per_step(self):
         a = self.acc.cpu().numpy().astype(np.float64) / max(1, self.steps)
         return {"hits_scanned": round(float(a[0]), 1), "gather_bytes": round(float(a[1]), 1),
-                "corpus_rows": round(float(a[2]), 2), "rows_scanned": round(float(a[3]), 2)}
+                "corpus_rows": round(float(a[2]), 2), "rows_scanned": round(float(a[3]), 2),
+                "gram_draft_rows": round(float(a[4]), 2)}
 
 
 def workload_config(cfg, world):

@@ -175,6 +175,16 @@ typedef struct {
                                   delta_capacity 0, select_by_score 0, num_backoff 1
                                   and vocab_size <= 2^24; 64 * next_pow2(2 S) bytes
                                   per row (max_batch rows). */
+  int32_t  gram_drafts;        /* 1 (default, with corpus_gram_index): each snapshot also
+                                  holds, for every 2- and 3-token gram whose suffix-array
+                                  interval has 8 or more hits, the R most recent of its
+                                  ends that continue and their vote to depth k, so that a
+                                  row whose corpus match is such a gram reads its draft
+                                  (cut at the row's cap) instead of evaluating the
+                                  interval and voting; up to corpus_capacity / 4 grams,
+                                  (16 + 8 roundup4(k)) bytes each, per snapshot, used only
+                                  while both snapshots' blocks fit in SGD_RECORD_BUDGET.
+                                  0: off.  Drafts are the same either way. */
 } sgd_config;
 
 #define SGD_RECORD_BUDGET (8ull << 30)
@@ -423,7 +433,8 @@ int sgd_launch_count(sgd_ctx *ctx, uint64_t *count);
  *   (c0), [4b+2] the draft cap, [4b+3] the source (0 none, 1 row, 2 corpus)
  *   plus 256 times how the row's own match was found: 0 by a scan of the
  *   row, 1 from its bigram index (row_index), 2 not needed (row_index: the
- *   row's last bigram occurs nowhere earlier and the corpus matched >= 2).
+ *   row's last bigram occurs nowhere earlier and the corpus matched >= 2),
+ *   plus 4096 when the corpus draft came from a gram draft (gram_drafts).
  * The pointer is read when a call is made, so a CUDA graph captured after
  * this call keeps writing to it.  SGD_EINVAL for an unaligned buffer. */
 int sgd_set_row_stats(sgd_ctx *ctx, int32_t *row_stats);

@@ -65,6 +65,7 @@ class SgdConfig(ctypes.Structure):
         ("select_by_score", ctypes.c_int32),
         ("num_backoff", ctypes.c_int32),
         ("row_index", ctypes.c_int32),
+        ("gram_drafts", ctypes.c_int32),
     ]
 
 

@@ -67,6 +67,10 @@ struct sgd_ctx {
   int32_t *d_rec[2] = {nullptr, nullptr};  // per-position records, or null (off / over budget)
   RecShape rsh{};
   int32_t *d_gt[2] = {nullptr, nullptr};   // n-gram tables, or null (off / over budget)
+  int32_t *d_gd[2] = {nullptr, nullptr};   // gram drafts, or null (off / over budget)
+  int32_t *d_gd_count = nullptr, *d_gd_owner = nullptr;  // their build's counter, block owners
+  int gd_cap = 0;                          // blocks per snapshot
+  int32_t *h_gd_count = nullptr;           // pinned: the blocks a build assigned
   uint64_t gt_mask = 0;
   CorpusDesc *d_desc = nullptr;
   IngestScratch ing{};
@@ -129,6 +133,7 @@ int validate(const sgd_config &c) {
   if (c.select_by_score != 0 && c.select_by_score != 1) return SGD_EINVAL;
   if (c.num_backoff < 1 || c.num_backoff > MAX_BACKOFF) return SGD_EINVAL;
   if (c.row_index != 0 && c.row_index != 1) return SGD_EINVAL;
+  if (c.gram_drafts != 0 && c.gram_drafts != 1) return SGD_EINVAL;
   if (c.row_index && (c.propose_mode == 2 || c.delta_capacity > 0 || c.select_by_score ||
                       c.num_backoff > 1 || c.vocab_size > RI_MAX_TOKEN + 1))
     return SGD_EINVAL;
@@ -147,6 +152,9 @@ int choose_self_warps(const sgd_config &c) {
 void free_ctx(sgd_ctx *x) {
   cudaFree(x->d_err);
   cudaFree(x->ri.tab);
+  for (int i = 0; i < 2; ++i) cudaFree(x->d_gd[i]);
+  cudaFree(x->d_gd_count);
+  cudaFree(x->d_gd_owner);
   cudaFree(x->ri.meta);
   cudaFree(x->d_ri_claim);
   cudaFree(x->d_step_ready);
@@ -177,6 +185,7 @@ void free_ctx(sgd_ctx *x) {
   if (x->sa.keyA) sa_scratch_free(&x->sa);
   if (x->h_n) cudaFreeHost(x->h_n);
   if (x->h_err) cudaFreeHost(x->h_err);
+  if (x->h_gd_count) cudaFreeHost(x->h_gd_count);
   if (x->ev_lin) cudaEventDestroy(x->ev_lin);
   if (x->ev_b0) cudaEventDestroy(x->ev_b0);
   if (x->ev_b1) cudaEventDestroy(x->ev_b1);
@@ -219,6 +228,17 @@ void worker_main(sgd_ctx *x) {
         if (launch_gram_table(x->d_keys[back], n, x->d_gt[back], x->gt_mask, side) != cudaSuccess)
           status = SGD_EBUILD;
         launches += 2;
+        if (x->d_gd[back] != nullptr) {
+          // (the drafting vote's stop rule: no probability floor for fixed-length drafts)
+          const long long pN = x->cfg.draft_mode == 1 ? 0 : x->cfg.min_prob_num;
+          const long long pD = x->cfg.draft_mode == 1 ? 1 : x->cfg.min_prob_den;
+          if (launch_gram_drafts(x->d_gt[back], x->gt_mask, x->d_keys[back], x->d_sa[back],
+                                 x->d_text[back], n, x->cfg.vocab_size, x->cfg.k,
+                                 x->cfg.max_occurrences, pN, pD, x->d_gd[back], x->gd_cap,
+                                 x->d_gd_count, x->d_gd_owner, x->h_gd_count, side) != cudaSuccess)
+            status = SGD_EBUILD;
+          launches += 2;
+        }
       }
       if (r == 0 && x->d_rec[back] != nullptr) {
         if (launch_records(x->d_text[back], x->d_sa[back], n, x->rsh, x->cfg.vocab_size,
@@ -306,6 +326,7 @@ int sgd_config_default(sgd_config *c) {
   c->num_backoff = 1;
   c->self_warps = 0;
   c->row_index = 0;
+  c->gram_drafts = 1;
   return SGD_OK;
 }
 
@@ -417,6 +438,16 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
         al((void **)&x->d_gt[0], (size_t)bytes);
         al((void **)&x->d_gt[1], (size_t)bytes);
         if (e == cudaSuccess) e = cudaMemset(x->d_gt[0], 0, (size_t)bytes);
+        // gram drafts: a block for up to C / 4 grams per snapshot
+        const long long cap = std::max(1024LL, (long long)(C / 4));
+        const unsigned long long gbytes = (unsigned long long)cap * gd_ints(cfg->k) * 4ull;
+        if (cfg->gram_drafts && 2ull * gbytes <= SGD_RECORD_BUDGET && cap < (1LL << 31)) {
+          x->gd_cap = (int)cap;
+          al((void **)&x->d_gd[0], (size_t)gbytes);
+          al((void **)&x->d_gd[1], (size_t)gbytes);
+          al((void **)&x->d_gd_count, 4);
+          al((void **)&x->d_gd_owner, (size_t)cap * 4);
+        }
       }
     }
     al((void **)&x->d_step_ready, (size_t)cfg->max_batch * 4);
@@ -435,17 +466,19 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
     if (e == cudaSuccess) e = sa_scratch_alloc(&x->sa, C);
     if (e == cudaSuccess) {
       x->dev_bytes += (int64_t)sa_scratch_bytes(C);
-      x->pinned_bytes += 64 + 8 * 256 * 4 + 8 + 4;  // the sort's read-back words, h_n, h_err
+      x->pinned_bytes += 64 + 8 * 256 * 4 + 8 + 4 + 4;  // the sort's read-back words, h_n, h_err, h_gd_count
     }
     if (e == cudaSuccess) e = cudaMemset(x->d_rs, 0, sizeof(RingState));
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_start, 0, (size_t)cfg->max_docs * 8);
     if (e == cudaSuccess) e = cudaMemset(x->d_doc_len, 0, (size_t)cfg->max_docs * 4);
     if (e == cudaSuccess) {
-      CorpusDesc d0{x->d_text[0], x->d_sa[0], x->d_keys[0], 0, 0, x->d_rec[0], x->d_gt[0], x->gt_mask};
+      CorpusDesc d0{x->d_text[0], x->d_sa[0], x->d_keys[0], 0, 0, x->d_rec[0], x->d_gt[0], x->gt_mask,
+                    0, 0, x->d_gd[0]};
       e = cudaMemcpy(x->d_desc, &d0, sizeof(d0), cudaMemcpyHostToDevice);
     }
     if (e == cudaSuccess) e = cudaMallocHost((void **)&x->h_n, 8);
     if (e == cudaSuccess) e = cudaMallocHost((void **)&x->h_err, 4);
+    if (e == cudaSuccess) e = cudaMallocHost((void **)&x->h_gd_count, 4);
     if (e == cudaSuccess) e = cudaEventCreateWithFlags(&x->ev_lin, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventCreate(&x->ev_b0);
     if (e == cudaSuccess) e = cudaEventCreate(&x->ev_b1);
@@ -820,8 +853,8 @@ int sgd_poll(sgd_ctx *x, int wait, int64_t timeout_us, void *stream, uint64_t *g
   }
   const int back = 1 - x->front;
   const cudaError_t e = launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->d_keys[back],
-                                    x->d_rec[back], x->d_gt[back], x->gt_mask, x->built_n, x->gen + 1,
-                                    x->d_rs, (cudaStream_t)stream);
+                                    x->d_rec[back], x->d_gt[back], x->gt_mask, x->d_gd[back],
+                                    x->built_n, x->gen + 1, x->d_rs, (cudaStream_t)stream);
   if (e != cudaSuccess) return SGD_ECUDA;
   x->launches++;
   x->front = back;
@@ -1047,7 +1080,7 @@ int sgd_load(sgd_ctx *x, const char *path, void *stream) {
   if (launch_sig_all(x->d_ring, C, V, x->d_sig, st) != cudaSuccess) return SGD_ECUDA;
   if (h.snap_n == 0) {  // no snapshot: an empty one, the delta from the saved point
     if (launch_swap(x->d_desc, x->d_text[back], x->d_sa[back], x->d_keys[back], x->d_rec[back],
-                    x->d_gt[back], x->gt_mask, 0, x->gen + 1, x->d_rs, st) != cudaSuccess ||
+                    x->d_gt[back], x->gt_mask, x->d_gd[back], 0, x->gen + 1, x->d_rs, st) != cudaSuccess ||
         cudaStreamSynchronize(st) != cudaSuccess)
       return SGD_ECUDA;
     std::unique_lock<std::mutex> lk(x->mu);

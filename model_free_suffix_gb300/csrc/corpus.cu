@@ -142,7 +142,9 @@ __global__ void __launch_bounds__(256) linearize_kernel(const int32_t *ring, lon
 // no other starts while a build is outstanding).
 __global__ void swap_kernel(CorpusDesc *desc, const int32_t *text, const int32_t *sa,
                             const int4 *keys, const int32_t *rec, const int32_t *gt,
-                            uint64_t gt_mask, long long n, uint64_t gen, const RingState *rs) {
+                            uint64_t gt_mask, const int32_t *gd, long long n, uint64_t gen,
+                            const RingState *rs) {
+  desc->gd = gd;
   desc->lin_pushed = rs->snap_pushed;
   desc->lin_wp = rs->snap_wp;
   desc->text = text;
@@ -311,9 +313,9 @@ cudaError_t launch_linearize(const int32_t *ring, int64_t C, RingState *rs, cons
 }
 
 cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
-                        const int32_t *rec, const int32_t *gt, uint64_t gt_mask, int64_t n,
-                        uint64_t gen, const RingState *rs, cudaStream_t st) {
-  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, rec, gt, gt_mask, n, gen, rs);
+                        const int32_t *rec, const int32_t *gt, uint64_t gt_mask, const int32_t *gd,
+                        int64_t n, uint64_t gen, const RingState *rs, cudaStream_t st) {
+  swap_kernel<<<1, 1, 0, st>>>(desc, text, sa, keys, rec, gt, gt_mask, gd, n, gen, rs);
   return cudaGetLastError();
 }
 

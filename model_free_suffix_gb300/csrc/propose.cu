@@ -679,6 +679,7 @@ struct Corpus {
   RecShape rs;
   const int32_t *GT;   // n-gram table, or null
   uint64_t gtm;        // its buckets - 1
+  const int32_t *GD;   // gram drafts, or null
   long long N;
   int Lmax;
   const int4 *s_top;  // K[j * 32^Lmax]
@@ -733,10 +734,11 @@ __device__ void probe_bounds(const Corpus &c, const int4 &P, int m, int lane, lo
 // ballots find the matching entry; a bucket with an empty entry ends the
 // search (the gram does not begin any suffix).
 __device__ void gram_bounds(const Corpus &c, const int4 &P, int m, int lane, long long &lo,
-                            long long &hi) {
+                            long long &hi, int &slot7) {
   const int4 g = make_int4(P.x, m >= 2 ? P.y : KEY_END, m >= 3 ? P.z : KEY_END, m >= 4 ? P.w : KEY_END);
   uint64_t b = gram_hash(m, g.x, g.y, g.z, g.w) & c.gtm;
   lo = hi = 0;
+  slot7 = -2;
   for (uint64_t step = 0; step <= c.gtm; ++step, b = (b + 1) & c.gtm) {
     int4 v = make_int4(0, 0, 0, 0);
     if (lane < 2 * GT_BUCKET)
@@ -747,9 +749,10 @@ __device__ void gram_bounds(const Corpus &c, const int4 &P, int m, int lane, lon
     const unsigned e1 = __ballot_sync(FULL, odd && v.x == g.w);
     const unsigned match = e0 & (e1 >> 1);  // bit 2e: entry e holds the gram
     if (match) {
-      const int src = __ffs(match);          // lane 2e + 1: (t3, lo, hi, -)
+      const int src = __ffs(match);          // lane 2e + 1: (t3, lo, hi, [7])
       lo = __shfl_sync(FULL, v.y, src);
       hi = __shfl_sync(FULL, v.z, src);
+      slot7 = __shfl_sync(FULL, v.w, src);
       return;
     }
     if (__ballot_sync(FULL, even && v.x == 0)) return;
@@ -759,20 +762,26 @@ __device__ void gram_bounds(const Corpus &c, const int4 &P, int m, int lane, lon
 // The interval of the last m tokens (t[i] = the i-th token from the end),
 // written to bound[0..1] by lane 0; empty when the row is shorter, m > D or
 // the pattern holds KEY_END (corpus tokens are in [0, V], so it cannot occur).
+// *blk: the gram's draft block (m = 2, 3 with gram drafts), else -2.
 __device__ void pattern_bounds(const Corpus &c, const int *t, int m, int D, int n, int lane,
-                               long long *bound) {
+                               long long *bound, int *blk) {
   long long plo = 0, phi = 0;
+  int slot7 = -2;
   if (D >= m && n >= m) {
     const int4 P = make_int4(t[m - 1], m >= 2 ? t[m - 2] : 0, m >= 3 ? t[m - 3] : 0,
                              m >= 4 ? t[m - 4] : 0);
     const bool endless = P.x != KEY_END && (m < 2 || P.y != KEY_END) &&
                          (m < 3 || P.z != KEY_END) && (m < 4 || P.w != KEY_END);
     if (endless) {
-      if (c.GT != nullptr) gram_bounds(c, P, m, lane, plo, phi);
+      if (c.GT != nullptr) gram_bounds(c, P, m, lane, plo, phi, slot7);
       else probe_bounds(c, P, m, lane, plo, phi);
     }
   }
-  if (lane == 0) { bound[0] = plo; bound[1] = phi; }
+  if (lane == 0) {
+    bound[0] = plo;
+    bound[1] = phi;
+    *blk = c.GD != nullptr && m <= 3 ? slot7 : -2;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -1392,6 +1401,178 @@ __device__ void vote_warp(const ProposeArgs &a, const int *cont, int capp, const
 // the update and the self scan only; the row's self result is written to
 // a.self_res.  MODE 2 (second launch): one warp reads that result back in
 // place of the scan, the probe warps and the vote run as in MODE 0.
+// ---------------------------------------------------------------------------
+// Gram drafts (built with each snapshot).  For a row whose corpus match is a
+// 2- or 3-gram G (no hit of its last four tokens has a continuation, resp. no
+// hit of its last three), the corpus candidate is the R most recent valid ends
+// of G in the snapshot and their vote, which depend on G alone: the row only
+// truncates the vote at its cap (the vote at depth d depends only on the
+// occurrences still agreeing at d, never on where it will stop).  So each
+// snapshot holds, for every 2-/3-gram whose interval has GD_MIN_HITS or more
+// hits (where a row's own evaluation would select among them), a
+// block: [0] c0, [1] the tokens the vote emits up to depth k, [2] Q (its
+// valid ends), [4, 4 + k) the tokens, [4 + k4, 4 + k4 + k) the count agreeing
+// at each depth (k4 = k rounded up to 4); its index sits in the gram's
+// table entry ([7]; -2: no block, the row evaluates the interval itself).
+
+constexpr int GD_MIN_HITS = 8;  // smaller intervals are evaluated by the row (one short pass)
+
+// Pass 1: every 2-/3-gram entry with >= GD_MIN_HITS hits takes a block (while
+// there are blocks); the others get -2.
+__global__ void __launch_bounds__(256) gd_assign_kernel(int32_t *gt, unsigned long long entries,
+                                                        int32_t *count, int cap, int32_t *owner) {
+  const unsigned long long stride = (unsigned long long)gridDim.x * blockDim.x;
+  for (unsigned long long e = (unsigned long long)blockIdx.x * blockDim.x + threadIdx.x; e < entries;
+       e += stride) {
+    int32_t *en = gt + e * GT_ENTRY;
+    const int m = en[0];
+    if (m != 2 && m != 3) continue;
+    int idx = -2;
+    if (en[6] - en[5] >= GD_MIN_HITS) {
+      const int c = atomicAdd(count, 1);
+      if (c < cap) {
+        idx = c;
+        owner[c] = (int32_t)e;
+      }
+    }
+    en[7] = idx;
+  }
+}
+
+constexpr int GD_THREADS = 128;
+constexpr int GD_CAND = 1024;  // candidate ends kept on chip
+constexpr int GD_LOADS = 4;    // interval hits each thread has in flight
+
+// The R largest of s_cand[0, *cnt) (distinct values) kept in s_cand[0, R),
+// *cnt = R; returns the smallest kept.  A radix select from the top byte.
+__device__ unsigned gd_keep_top(int *s_cand, int *cnt, int R, int *s_hist, int *s_sel, int *s_need,
+                                int *s_tmp) {
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int c = *cnt;
+  unsigned thr = 0, mk = 0;
+  int need = R;
+  for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256; i += GD_THREADS) s_hist[i] = 0;
+    __syncthreads();
+    for (int i = tid; i < c; i += GD_THREADS) {
+      const unsigned e = (unsigned)s_cand[i];
+      if ((e & mk) == thr) atomicAdd(&s_hist[(e >> shift) & 255u], 1);
+    }
+    __syncthreads();
+    if (warp == 0) pick_bin(s_hist, need, lane, s_sel, s_need);
+    __syncthreads();
+    thr |= (unsigned)*s_sel << shift;
+    mk |= 255u << shift;
+    need = *s_need;
+    __syncthreads();
+  }
+  // compact the kept ones to the front (through s_tmp, R entries)
+  if (tid == 0) *s_sel = 0;
+  __syncthreads();
+  for (int i = tid; i < c; i += GD_THREADS)
+    if ((unsigned)s_cand[i] >= thr) s_tmp[atomicAdd(s_sel, 1)] = s_cand[i];
+  __syncthreads();
+  for (int i = tid; i < R; i += GD_THREADS) s_cand[i] = s_tmp[i];
+  if (tid == 0) *cnt = R;
+  __syncthreads();
+  return thr;
+}
+
+// Pass 2: one CTA per block.  The gram's valid ends in one pass over its
+// interval, keeping the R most recent: ends above the current R-th largest
+// join a candidate buffer, which is cut back to its R largest when it fills
+// (end positions are distinct).  Then their continuations up to k tokens and
+// the vote (vote_warp, the drafting vote, to depth k).
+__global__ void __launch_bounds__(GD_THREADS) gd_build_kernel(const int32_t *gt, const int32_t *owner,
+                                                             const int4 *K, const int32_t *SA,
+                                                             const int32_t *X, long long N, int Z,
+                                                             int k, int R, long long pN, long long pD,
+                                                             int32_t *gd) {
+  // dynamic: GD_CAND candidates, then R continuation rows of roundup4(k) ints
+  extern __shared__ __align__(16) int gd_dsm[];
+  int *s_cand = gd_dsm;
+  int *s_cont = gd_dsm + GD_CAND;
+  __shared__ int s_run[MAX_R], s_vv[MAX_R], s_tmp[MAX_R];
+  __shared__ int s_hist[256];
+  __shared__ __align__(16) unsigned char s_hash[256 * 12];
+  __shared__ int s_tok[MAX_K];
+  __shared__ float s_prob[MAX_K];
+  __shared__ int s_q, s_cnt, s_sel, s_need;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int bi = blockIdx.x;
+  const int k4 = (k + 3) & ~3;
+  const int32_t *en = gt + (size_t)owner[bi] * GT_ENTRY;
+  const int m = en[0];
+  const long long lo = en[5], hi = en[6];
+  if (tid == 0) {
+    s_q = 0;
+    s_cnt = 0;
+  }
+  __syncthreads();
+  unsigned thr = 0;  // ends below it cannot be among the R largest
+  for (long long p0 = lo; p0 < hi; p0 += (long long)GD_THREADS * GD_LOADS) {
+    int e[GD_LOADS];
+    bool v[GD_LOADS];
+#pragma unroll
+    for (int u = 0; u < GD_LOADS; ++u) {
+      const long long p = p0 + u * GD_THREADS + tid;
+      v[u] = false;
+      e[u] = 0;
+      if (p < hi) {
+        const int4 kk = __ldg(K + p);
+        const int t = m == 2 ? kk.z : kk.w;  // the token after the gram
+        v[u] = t != Z && t != KEY_END;
+        e[u] = __ldg(SA + p) + m - 1;
+      }
+    }
+    int nv = 0;
+#pragma unroll
+    for (int u = 0; u < GD_LOADS; ++u) {
+      nv += v[u];
+      if (v[u] && (unsigned)e[u] >= thr) s_cand[atomicAdd(&s_cnt, 1)] = e[u];
+    }
+    if (nv) atomicAdd(&s_q, nv);
+    __syncthreads();
+    if (s_cnt > GD_CAND - GD_THREADS * GD_LOADS) thr = gd_keep_top(s_cand, &s_cnt, R, s_hist, &s_sel, &s_need, s_tmp);
+  }
+  __syncthreads();
+  if (s_cnt > R) gd_keep_top(s_cand, &s_cnt, R, s_hist, &s_sel, &s_need, s_tmp);
+  const int Q = s_q, c0 = s_cnt;  // c0 = min(Q, R)
+  // continuations: X[e + 1 ..], up to k tokens, stopping at the sentinel
+  for (int idx = tid; idx < c0 * k; idx += GD_THREADS) {
+    const int o = idx / k, d = idx - o * k;
+    const long long pos = (long long)s_cand[o] + 1 + d;
+    s_cont[o * k4 + d] = pos < N ? __ldg(X + pos) : Z;
+  }
+  __syncthreads();
+  for (int o = tid; o < c0; o += GD_THREADS) {
+    int r = 0;
+    while (r < k && s_cont[o * k4 + r] != Z) ++r;
+    s_run[o] = r;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    ProposeArgs va{};
+    va.pN = pN;
+    va.pD = pD;
+    int len = 0;
+    long long sum = 0;
+    if (c0 > 0) vote_warp(va, s_cont, k4, s_run, c0, k, s_hist, s_vv, s_hash, s_tok, s_prob, len, sum);
+    __syncwarp();
+    int32_t *blk = gd + (size_t)bi * gd_ints(k);
+    for (int d = lane; d < k; d += 32) {
+      blk[4 + d] = d < len ? s_tok[d] : -1;
+      blk[4 + k4 + d] = d < len ? __float2int_rn(s_prob[d] * (float)c0) : 0;
+    }
+    if (lane == 0) {
+      blk[0] = c0;
+      blk[1] = len;
+      blk[2] = Q;
+      blk[3] = 0;
+    }
+  }
+}
+
 template <int MODE, bool EXT>
 __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) {
   constexpr bool SELF_ONLY = MODE == 1, FROM_RES = MODE == 2;
@@ -1415,6 +1596,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   __shared__ int s_scan;  // suffix-array hits the probe warps scanned (row statistics)
   // the last four tokens known from the sampled ids (probe warps, phase 0)
   __shared__ int s_l4[4], s_pre, s_pre_n;
+  // gram drafts: each probe level's block (-2: none); the block the corpus
+  // candidate comes from, or -1
+  __shared__ int s_bidx[NPROBE3], s_blk;
   // the row's bigram index: its entries cover the row (maintenance), the self
   // match may come from it, the row length before the update, the looked-up
   // count and positions, self match deferred
@@ -1451,7 +1635,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
 
   // ---- phase 0: warp 0 updates the row; the others fetch the snapshot
   // descriptor and stage the top two levels of its key array ----
-  Corpus cp{nullptr, nullptr, nullptr, nullptr, a.rsh, nullptr, 0, 0, 0, s_top, s_mid};
+  Corpus cp{nullptr, nullptr, nullptr, nullptr, a.rsh, nullptr, 0, nullptr, 0, 0, s_top, s_mid};
   if (!SELF_ONLY && a.desc != nullptr) {
     cp.X = a.desc->text;
     cp.SA = a.desc->sa;
@@ -1459,6 +1643,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     cp.Rec = a.desc->rec;
     cp.GT = a.desc->gt;
     cp.gtm = a.desc->gt_mask;
+    // gram drafts: used by the one-launch kernel without a delta or
+    // score-ranked selection (the corpus candidate is then the gram's alone)
+    cp.GD = MODE == 0 && !EXT ? a.desc->gd : nullptr;
     cp.N = a.desc->n;
     cp.Lmax = cp.N >= 2 ? top_level(cp.N) : 0;
   }
@@ -1555,6 +1742,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       s_ckey = 0;
       s_ep = e0;
       s_scan = 0;
+      s_blk = -1;
       s_best_delta = 0;
       for (int w = 0; w < MAX_SELF_WARPS; ++w) s_dstate[w] = 0;
       s_dcB = 0;
@@ -1606,7 +1794,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
       }
     }
     probe_sync();
-    if (s_pre) pattern_bounds(cp, s_l4, 4 - pw, D, s_pre_n, lane, &s_bound[2 * pw]);
+    if (s_pre) pattern_bounds(cp, s_l4, 4 - pw, D, s_pre_n, lane, &s_bound[2 * pw], &s_bidx[pw]);
   } else if (!SELF_ONLY && a.stage_keys && a.desc != nullptr && cp.N >= 2 && cp.GT == nullptr) {
     const int sh = 5 * cp.Lmax;
     const long long ntop = (cp.N + (1LL << sh) - 1) >> sh;
@@ -1652,7 +1840,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const bool pre_bounds = !SELF_ONLY && !FROM_RES && a.do_update && cp.GT != nullptr && cp.N >= 2 &&
                           D >= 2 && s_pre;
   if (early_bounds && warp >= a.nself && !pre_bounds)
-    pattern_bounds(cp, s_tail, 4 - (warp - a.nself), D, n, lane, &s_bound[2 * (warp - a.nself)]);
+    pattern_bounds(cp, s_tail, 4 - (warp - a.nself), D, n, lane, &s_bound[2 * (warp - a.nself)],
+                   &s_bidx[warp - a.nself]);
   SelfScan sc;
   // With a usable row index, warp 0 looks the row's last bigram up while the
   // tail is read, and the self warps fetch no window before they know whether
@@ -1847,7 +2036,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   } else if (corpus_ok) {
     const int pw = warp - a.nself;  // 0: last 4 tokens, 1: last 3, 2: last 2
     const int ptid = tid - 32 * a.nself, pthr = 32 * NPROBE3;
-    if (!early_bounds) pattern_bounds(cp, s_tail, 4 - pw, D, n, lane, &s_bound[2 * pw]);
+    if (!early_bounds) pattern_bounds(cp, s_tail, 4 - pw, D, n, lane, &s_bound[2 * pw], &s_bidx[pw]);
     probe_sync();
     // The row's own match length, -1 while the self warps still scan.  Before
     // a large piece of work the probe warps wait for it (bounded; on time-out
@@ -1868,6 +2057,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     };
     int pms = self_len(false);
     int Mc = 0, lvl = 0, Q = 0;
+    int blk = -1;  // the gram draft block the candidate comes from
     bool p4ctx = false;   // the P4 interval was evaluated on chip (scan_p4_ctx)
     bool oncand = false;  // a short level's ends are all in s_big already
     // A short level's candidates also keep their suffix-array positions (in the
@@ -1913,6 +2103,23 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         if (pms >= lv) break;  // neither this level nor the next can win
         const long long l0 = s_bound[2 * (4 - lv)], h0 = s_bound[2 * (4 - lv) + 1];
         if (h0 <= l0) continue;
+        const int bi = s_bidx[4 - lv];
+        if (bi >= 0) {
+          // the gram's draft block: its valid ends are counted there (every
+          // end matching lv tokens matches exactly lv when the longer level
+          // has none that continues), and its candidate is decided
+          const int qb = __ldg(cp.GD + (size_t)bi * gd_ints(k) + 2);
+          if (qb > 0) {
+            Mc = lv;
+            lvl = lv;
+            lo = l0;
+            hi = h0;
+            Q = qb;
+            blk = bi;
+            decided = true;
+          }
+          continue;
+        }
         if (pms < 0 && h0 - l0 > BIG_INTERVAL) {
           pms = self_len(true);
           if (pms >= lv) break;
@@ -1960,8 +2167,17 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
         }
       }
     }
-    if (Mc > 0 && pms < 0 && Q > R) pms = self_len(true);
-    if (Mc > 0 && Mc > pms && lvl == 4 && p4ctx) {
+    if (Mc > 0 && blk < 0 && pms < 0 && Q > R) pms = self_len(true);
+    if (blk >= 0 && Mc > pms) {
+      // a gram draft: nothing to select, gather or vote
+      if (ptid == 0) {
+        s_Mc = Mc;
+        s_c0c = min(Q, R);
+        s_cpf = 0;
+        s_ckey = 0;
+        s_blk = blk;
+      }
+    } else if (Mc > 0 && Mc > pms && lvl == 4 && p4ctx) {
       // A small P4 interval: ends, lengths and continuations are on chip.
       // The R largest ends of length Mc (a radix select over the ends when
       // there are more), their continuations copied for the vote.
@@ -2158,6 +2374,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   const int ns = src == 2 && Mcs == Mc ? min(s_c0c, R - nd) : 0;  // snapshot ends voting
   const int cap = M > 0 ? draft_cap(a, M, n) : 0;
   const int c0 = src == 2 ? nd + ns : s_cs;
+  // the corpus candidate is a gram draft: its tokens and counts are read, cut at the cap
+  const int dblk = src == 2 && nd == 0 ? s_blk : -1;
   const int *occ = src == 2 ? s_occc : s_occ;
   if (nd > 0) {
     // occurrences: the delta's ends, then the ns most recent of the snapshot's
@@ -2178,7 +2396,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   }
   int *cont = s_big;                  // cont[o * capp + d]: rows 16-byte aligned
   const int capp = (cap + 3) & ~3;
-  if (cap > 0 && c0 > 0) {
+  if (cap > 0 && c0 > 0 && dblk < 0) {
     // (prefetched by the probe warps when only the snapshot's ends vote)
     const int tot = (src == 2 && s_cpf && nd == 0) ? 0 : c0 * cap;
     const int ck = src == 2 && nd == 0 ? s_ckey : 0;
@@ -2256,7 +2474,21 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   // ---- depth-wise majority vote (one warp) ----
   int len = 0;
   long long sum = 0;
-  vote_warp(a, cont, capp, s_run, c0, cap, s_hist, s_vv, s_L, dr, pr, len, sum);
+  if (dblk >= 0) {
+    const int k4 = (k + 3) & ~3;
+    const int32_t *gb = cp.GD + (size_t)dblk * gd_ints(k);
+    len = min(__ldg(gb + 1), cap);
+    int part = 0;
+    for (int d = lane; d < len; d += 32) {
+      const int cnt = __ldg(gb + 4 + k4 + d);
+      dr[d] = __ldg(gb + 4 + d);
+      if (pr) pr[d] = (float)cnt / (float)c0;
+      part += cnt;
+    }
+    sum = (long long)__reduce_add_sync(FULL, (unsigned)part);
+  } else {
+    vote_warp(a, cont, capp, s_run, c0, cap, s_hist, s_vv, s_L, dr, pr, len, sum);
+  }
   int cw = c0;  // the winner's occurrences
   if (both) {
     // the row's draft, staged; it wins unless the corpus's score (sum / c0) is
@@ -2296,7 +2528,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     if (a.match_info) { a.match_info[2 * b] = M; a.match_info[2 * b + 1] = src; }
     if (a.row_stats)
       *reinterpret_cast<int4 *>(a.row_stats + 4 * (size_t)b) =
-          make_int4(s_scan, cw, src == 1 && both ? cap_s : cap, src | (IDX ? s_imode << 8 : 0));
+          make_int4(s_scan, cw, src == 1 && both ? cap_s : cap,
+                    src | (IDX ? s_imode << 8 : 0) | (src == 2 && dblk >= 0 ? 1 << 12 : 0));
   }
 }
 
@@ -2395,6 +2628,30 @@ cudaError_t launch_row_index_reset(const RowIndexArgs &ri, const int32_t *tok, c
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   ri_reset_kernel<<<m, 1024, 0, st>>>(ri, tok, ntok, S, rows, max_batch, claim, epoch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gram_drafts(int32_t *gt, uint64_t gt_mask, const int4 *keys, const int32_t *sa,
+                               const int32_t *text, int64_t n, int Z, int k, int R, long long pN,
+                               long long pD, int32_t *gd, int cap, int32_t *count, int32_t *owner,
+                               int32_t *h_count, cudaStream_t st) {
+  if (gt == nullptr || gd == nullptr || n <= 0) return cudaSuccess;
+  cudaError_t e = cudaMemsetAsync(count, 0, 4, st);
+  if (e != cudaSuccess) return e;
+  const unsigned long long entries = (gt_mask + 1) * GT_BUCKET;
+  gd_assign_kernel<<<152 * 8, 256, 0, st>>>(gt, entries, count, cap, owner);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  // one short CTA per block, so that a drafting launch finds SMs between them
+  // (the caller is the build's host thread: it may wait for the count)
+  int32_t blocks = 0;
+  e = cudaMemcpyAsync(h_count, count, 4, cudaMemcpyDeviceToHost, st);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(st);
+  if (e != cudaSuccess) return e;
+  blocks = *h_count < cap ? *h_count : cap;
+  const size_t dyn = (size_t)(GD_CAND + R * ((k + 3) & ~3)) * 4;
+  if (blocks > 0)
+    gd_build_kernel<<<blocks, GD_THREADS, dyn, st>>>(gt, owner, keys, sa, text, n, Z, k, R, pN, pD, gd);
   return cudaGetLastError();
 }
 

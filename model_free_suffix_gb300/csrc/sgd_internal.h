@@ -31,12 +31,14 @@ struct CorpusDesc {
   uint64_t gt_mask;     // buckets - 1
   int64_t lin_pushed;   // the ring's docs placed when X was linearised
   int64_t lin_wp;       // the ring's write offset then (where the next doc went)
+  const int32_t *gd;    // gram drafts (blocks of 4 + 2 roundup4(k) ints), or null
 };
 
 // n-gram table: for every distinct m-gram (m = 2, 3, 4) that begins a suffix
 // of the snapshot, its suffix-array interval [lo, hi).  Open addressing over
 // buckets of GT_BUCKET entries of GT_ENTRY ints: [0] m (0: empty), [1..4] the
-// tokens (KEY_END past m), [5] lo, [6] hi, [7] unused.  A bucket is 128 bytes.
+// tokens (KEY_END past m), [5] lo, [6] hi, [7] for m = 2, 3 with gram drafts:
+// the gram's draft block, or -2.  A bucket is 128 bytes.
 constexpr int GT_BUCKET = 4;
 constexpr int GT_ENTRY = 8;
 __host__ __device__ inline uint64_t gram_hash(int m, int t0, int t1, int t2, int t3) {
@@ -223,8 +225,16 @@ cudaError_t launch_records(const int32_t *text, const int32_t *sa, int64_t n, Re
 cudaError_t launch_gram_table(const int4 *keys, int64_t n, int32_t *gt, uint64_t mask,
                               cudaStream_t st);
 cudaError_t launch_swap(CorpusDesc *desc, const int32_t *text, const int32_t *sa, const int4 *keys,
-                        const int32_t *rec, const int32_t *gt, uint64_t gt_mask,
+                        const int32_t *rec, const int32_t *gt, uint64_t gt_mask, const int32_t *gd,
                         int64_t n, uint64_t gen, const RingState *rs, cudaStream_t st);
+// gram drafts of a snapshot (propose.cu): blocks for its 2-/3-grams' votes
+// (cap blocks of 4 + 2 roundup4(k) ints), their indexes in the n-gram table.
+// Waits once for the stream (the number of blocks, read into pinned h_count).
+cudaError_t launch_gram_drafts(int32_t *gt, uint64_t gt_mask, const int4 *keys, const int32_t *sa,
+                               const int32_t *text, int64_t n, int Z, int k, int R, long long pN,
+                               long long pD, int32_t *gd, int cap, int32_t *count, int32_t *owner,
+                               int32_t *h_count, cudaStream_t st);
+__host__ __device__ inline int gd_ints(int k) { return 4 + 2 * ((k + 3) & ~3); }
 // keys[p] = text[sa[p] .. sa[p]+3] (KEY_END past n), on `st`
 cudaError_t launch_suffix_keys(const int32_t *text, const int32_t *sa, int64_t n, int4 *keys,
                                cudaStream_t st);

@@ -68,7 +68,7 @@ class SuffixDrafter:
                  corpus_cand_cap: int = 2048, self_warps: int = 0, corpus_records: int = 1,
                  corpus_gram_index: int = 1, propose_mode: int = 0, delta_capacity: int = 0,
                  draft_mode: int = 0, select_by_score: int = 0, num_backoff: int = 1,
-                 row_index: int = 0, device: int = 0):
+                 row_index: int = 0, gram_drafts: int = 1, device: int = 0):
         self._lib = L.load()
         cfg = L.SgdConfig()
         self._check(self._lib.sgd_config_default(ctypes.byref(cfg)), "sgd_config_default")
@@ -96,6 +96,7 @@ class SuffixDrafter:
         cfg.select_by_score = select_by_score
         cfg.num_backoff = num_backoff
         cfg.row_index = row_index
+        cfg.gram_drafts = gram_drafts
         self.cfg = cfg
         self.device = torch.device("cuda", device)
         torch.cuda.init()

@@ -31,11 +31,11 @@ def _mods():
 def test_row_stats_agree_with_the_drafts(mode):
     W, O, H = _mods()
     cfg = dataclasses.replace(W.CONFIGS["c3"], rebuild_tokens=4096)
-    ls = H.Lockstep(cfg, seed=5, B=96, steps=6, corpus=1 << 16, drafter_over=dict(propose_mode=mode))
+    ls = H.Lockstep(cfg, seed=5, B=96, steps=6, corpus=1 << 18, drafter_over=dict(propose_mode=mode))
     ls.prefill(seed=5)
     stats = torch.full((96 * 4,), -9, dtype=torch.int32, device=ls.dr.device)
     ls.dr.set_row_stats(stats)
-    seen_corpus = 0
+    seen_corpus = seen_gd = 0
     for _ in range(6):
         ls.step()  # (compares the drafts with the oracle's)
         st = stats.view(96, 4).cpu().numpy()
@@ -43,15 +43,19 @@ def test_row_stats_agree_with_the_drafts(mode):
         nv = H.to_np(ls.out.num_valid)
         sc = H.to_np(ls.out.score).astype(np.float64)
         scanned, c0, cap, src = st[:, 0], st[:, 1], st[:, 2], st[:, 3] & 255
-        assert (st[:, 3] >> 8 == 0).all()  # (no row index: every row scanned)
+        gd = (st[:, 3] >> 12) & 1  # the corpus draft came from a gram draft (nothing scanned)
+        assert ((st[:, 3] >> 8) & 15 == 0).all()  # (no row index: every row scanned)
+        assert (gd[src != 2] == 0).all()
         assert np.array_equal(src, mi[:, 1])
         assert (nv <= cap).all() and (scanned >= 0).all()
         assert ((c0 >= 1) & (c0 <= cfg.R))[src > 0].all() and (c0[src == 0] == 0).all()
-        assert (scanned >= c0)[src == 2].all()
+        assert (scanned >= c0)[(src == 2) & (gd == 0)].all()
+        seen_gd += int(gd.sum())
         prod = sc * c0
         assert (np.abs(prod - np.round(prod)) < 1e-3).all()
         seen_corpus += int((src == 2).sum())
     assert seen_corpus > 0
+    assert seen_gd > 0 or mode == 2  # (gram drafts serve the one-launch kernel)
     ls.dr.set_row_stats(None)
     ls.close()
 
