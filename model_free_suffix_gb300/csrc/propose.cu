@@ -1611,7 +1611,8 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
   int32_t *row = a.tok + (size_t)b * S;
   // the row index is used by the one-launch kernel without a delta or
   // score-ranked selection (the host enables it only there)
-  constexpr bool IDX = MODE == 0 && !EXT;
+  // (MODE 3: the one-launch kernel of a context with row indexes)
+  constexpr bool IDX = MODE == 3 && !EXT;
   const int big = SELF_ONLY ? 0 : max(a.cand_cap, R * ((k + 3) & ~3));
   int *s_tail = dsm;                   // MAX_D
   int *s_wlist = s_tail + MAX_D;       // nself * R: per warp, ends matching >= 2 tokens
@@ -1645,7 +1646,7 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
     cp.gtm = a.desc->gt_mask;
     // gram drafts: used by the one-launch kernel without a delta or
     // score-ranked selection (the corpus candidate is then the gram's alone)
-    cp.GD = MODE == 0 && !EXT ? a.desc->gd : nullptr;
+    cp.GD = (MODE == 0 || MODE == 3) && !EXT ? a.desc->gd : nullptr;
     cp.N = a.desc->n;
     cp.Lmax = cp.N >= 2 ? top_level(cp.N) : 0;
   }
@@ -2539,7 +2540,9 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
 // the corpus chain and vote (one warp + the probe warps).
 // EXT: the kernel also handles the delta and score-ranked selection; the
 // instantiations without them are what a context with neither runs (the
-// extra code costs registers and latency even when unused).
+// extra code costs registers and latency even when unused).  MODE 3 is the
+// one-launch kernel of a context with row indexes (their lookup, the
+// candidates' extension and the deferred scan are compiled only there).
 template <int MAXT, int MINB, int MODE, bool EXT>
 __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a) {
   if (MODE != 1 && a.ing_m > 0) {
@@ -2581,10 +2584,16 @@ cudaError_t launch_propose(const ProposeArgs &a, cudaStream_t st) {
     const int warps = a.nself + probe;
     const size_t smem = propose_smem_bytes(0, a.nself, a.R, a.k, a.cand_cap, a.stage_keys);
     const int grid = a.B + (a.ing_m > 0 ? 1 : 0);
-    if (warps <= 12)
+    if (a.ri.tab != nullptr) {  // row indexes (never with the delta or score-ranked selection)
+      if (warps <= 12)
+        propose_kernel<384, 2, 3, false><<<grid, 32 * warps, smem, st>>>(a);
+      else
+        propose_kernel<640, 1, 3, false><<<grid, 32 * warps, smem, st>>>(a);
+    } else if (warps <= 12) {
       launch_kernel<384, 2, 0>(ext, grid, 32 * warps, smem, st, a);
-    else
+    } else {
       launch_kernel<640, 1, 0>(ext, grid, 32 * warps, smem, st, a);
+    }
     return cudaGetLastError();
   }
   // first launch: update + self scan of every row, and of the delta (no
@@ -2659,6 +2668,7 @@ cudaError_t propose_set_smem_limit(size_t bytes) {
   // every instantiation may be launched with up to `bytes` of dynamic shared memory
   const void *fns[] = {
       (const void *)propose_kernel<384, 2, 0, false>, (const void *)propose_kernel<640, 1, 0, false>,
+      (const void *)propose_kernel<384, 2, 3, false>, (const void *)propose_kernel<640, 1, 3, false>,
       (const void *)propose_kernel<256, 3, 1, false>, (const void *)propose_kernel<512, 1, 1, false>,
       (const void *)propose_kernel<128, 3, 2, false>, (const void *)propose_kernel<384, 2, 0, true>,
       (const void *)propose_kernel<640, 1, 0, true>,  (const void *)propose_kernel<256, 3, 1, true>,
