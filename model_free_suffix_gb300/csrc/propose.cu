@@ -2545,12 +2545,10 @@ __device__ __forceinline__ void propose_body(const ProposeArgs &a, const int b) 
 // candidates' extension and the deferred scan are compiled only there).
 template <int MAXT, int MINB, int MODE, bool EXT>
 __global__ void __launch_bounds__(MAXT, MINB) propose_kernel(const ProposeArgs a) {
-  if (MODE != 1 && a.ing_m > 0) {
-    if (blockIdx.x == 0) step_ingest(a, EXT ? a.dcap : 0);
-    else propose_body<MODE, EXT>(a, blockIdx.x - 1);
-  } else {
-    propose_body<MODE, EXT>(a, blockIdx.x);
-  }
+  // (one call site of the body: its code is inlined once)
+  const int b = MODE != 1 && a.ing_m > 0 ? (int)blockIdx.x - 1 : (int)blockIdx.x;
+  if (b < 0) step_ingest(a, EXT ? a.dcap : 0);
+  else propose_body<MODE, EXT>(a, b);
 }
 
 template <int MAXT, int MINB, int MODE>
