@@ -22,9 +22,19 @@
 // selection on the end position over the interval's hits).  Each warp then
 // votes one candidate, and thread 0 picks the winner with exact integer
 // comparisons.
+//
+// With the snapshot's n-gram table and gram drafts, and no delta ends, the
+// interval walked is that of the shortest of the last 2-, 3- and 4-gram
+// without a draft block.  An end matching m or more tokens ends the last
+// m-gram, so the ends reaching length m are the valid hits of its interval;
+// a block holds their number and the vote of the R most recent of them
+// (built with the snapshot), which is exactly the corpus candidate of length
+// m.  So the lengths below the walked gram's are counted from the blocks, and
+// their candidates come from them, without reading their (largest) intervals.
 #include <climits>
 
 #include "delta_sig.cuh"
+#include "gram_lookup.cuh"
 
 namespace sgd {
 
@@ -71,6 +81,8 @@ struct BoShared {
   long long dsum[BO_CANDS];
   int wl[BO_THREADS];                   // delta windows that can hold an end (one batch)
   long long lo, hi, ds;
+  long long glo[3], ghi[3];             // the last 2-, 3-, 4-gram's interval (n-gram table)
+  int gblk[3];                          // the last 2-, 3-gram's draft block, or -2
   int n, dv, ns, nc, win;
 };
 
@@ -117,39 +129,48 @@ __device__ __forceinline__ int self_len(const BoRow &r, int j) {
   return l;
 }
 
-// The lengths of interval hits p0 + j * BO_THREADS (j < 4; l[j] = -1 past hi),
-// their loads issued together: the key gives the continuation X[e+1] (its
-// third token; KEY_END past the text), then the token before the pair for
-// the valid hits; the rare longer matches are extended one token at a time.
-__device__ __forceinline__ void hit_lens(const BoRow &r, long long p0, long long hi, int l[4],
+// The lengths of hits p0 + j * BO_THREADS (j < 4; l[j] = -1 past hi) of the
+// interval of the last m-gram (2 <= m <= 4; end e = SA[p] + m - 1), their
+// loads issued together: the continuation X[e+1] (from the key for m <= 3:
+// its token m, KEY_END past the text), then the token before the gram for the
+// valid hits; the rare longer matches are extended one token at a time.
+__device__ __forceinline__ void hit_lens(const BoRow &r, int m, long long p0, long long hi, int l[4],
                                          long long e[4]) {
-  int4 kk[4];
-  int ii[4];
+  int cn[4], ii[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
     const long long p = p0 + (long long)j * BO_THREADS;
-    kk[j] = make_int4(0, 0, KEY_END, 0);
+    cn[j] = KEY_END;
     ii[j] = 0;
     if (p < hi) {
-      kk[j] = __ldg(r.K + p);
+      if (m <= 3) {
+        const int4 kk = __ldg(r.K + p);
+        cn[j] = m == 2 ? kk.z : kk.w;
+      }
       ii[j] = __ldg(r.SA + p);
     }
   }
   int xb[4];
-  bool three[4];
+  bool more[4];
 #pragma unroll
   for (int j = 0; j < 4; ++j) {
-    const bool valid = kk[j].z != KEY_END && kk[j].z != r.Z;
-    three[j] = valid && r.dl >= 3 && ii[j] >= 1;
-    xb[j] = three[j] ? __ldg(r.X + ii[j] - 1) : 0;
-    e[j] = (long long)ii[j] + 1;
-    l[j] = p0 + (long long)j * BO_THREADS < hi ? (valid ? 2 : 0) : -1;
+    const bool in = p0 + (long long)j * BO_THREADS < hi;
+    if (m == 4 && in) cn[j] = (long long)ii[j] + 4 < r.N ? __ldg(r.X + ii[j] + 4) : KEY_END;
+    more[j] = in && r.dl > m && ii[j] >= 1;
+    xb[j] = more[j] ? __ldg(r.X + ii[j] - 1) : 0;
+  }
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const bool valid = cn[j] != KEY_END && cn[j] != r.Z;
+    more[j] = more[j] && valid;
+    e[j] = (long long)ii[j] + m - 1;
+    l[j] = p0 + (long long)j * BO_THREADS < hi ? (valid ? m : 0) : -1;
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    if (three[j] && xb[j] == r.tail[2]) {
+    if (more[j] && xb[j] == r.tail[m]) {
       const long long lim = min((long long)r.dl, e[j] + 1);
-      int L = 3;
+      int L = m + 1;
       while (L < lim && __ldg(r.X + e[j] - L) == r.tail[L]) ++L;
       l[j] = L;
     }
@@ -329,16 +350,16 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
 // on-chip cache, or beyond it both evaluated again as in the first pass (the
 // four hits of a call lie on one side of the cache's end: p0 - lo is
 // tid + a multiple of 4 * BO_THREADS, and the cache size is a multiple of it).
-__device__ __forceinline__ void hit_ends(const BoRow &r, const BoShared &s, long long lo, long long p0,
-                                         long long hi, long long e[4], int l[4]) {
+__device__ __forceinline__ void hit_ends(const BoRow &r, const BoShared &s, int m, long long lo,
+                                         long long p0, long long hi, long long e[4], int l[4]) {
   if (p0 - lo >= BO_LCACHE) {
-    hit_lens(r, p0, hi, l, e);
+    hit_lens(r, m, p0, hi, l, e);
     return;
   }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
     const long long p = p0 + (long long)q * BO_THREADS;
-    e[q] = p < hi ? (long long)__ldg(r.SA + p) + 1 : -1;
+    e[q] = p < hi ? (long long)__ldg(r.SA + p) + m - 1 : -1;
   }
 #pragma unroll
   for (int q = 0; q < 4; ++q) {
@@ -446,7 +467,24 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
   __syncthreads();
 
   // ---- match lengths: the row's ends, the interval of the last two tokens, the delta ----
-  if (snap && warp < 2) {
+  const bool grams = snap && !delta && cd->gt != nullptr;
+  if (grams && warp < 3) {  // the last 2-, 3-, 4-gram (warp 0, 1, 2)
+    const int m = 2 + warp;
+    long long glo = 0, ghi = 0;
+    int blk = -2;
+    bool endless = dl >= m;  // (no suffix holds KEY_END: a pattern with it has no hit)
+    for (int i = 0; i < m && endless; ++i) endless = s.tail[i] != KEY_END;
+    if (endless) {
+      const int4 P = make_int4(s.tail[m - 1], s.tail[m - 2], m >= 3 ? s.tail[m - 3] : 0,
+                               m >= 4 ? s.tail[m - 4] : 0);
+      gt_lookup(cd->gt, cd->gt_mask, P, m, lane, glo, ghi, blk);
+    }
+    if (lane == 0) {
+      s.glo[warp] = glo;
+      s.ghi[warp] = ghi;
+      if (warp < 2) s.gblk[warp] = cd->gd != nullptr ? blk : -2;
+    }
+  } else if (snap && !grams && warp < 2) {
     const long long q = pair_bound(r.K, r.N, s.tail[1], s.tail[0], warp == 1, lane);
     if (lane == 0) (warp == 0 ? s.lo : s.hi) = q;
   }
@@ -498,14 +536,19 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     __syncthreads();
   }
   __syncthreads();
-  const long long lo = s.lo, hi = s.hi;
+  // the walked gram: the shortest without a draft block (lengths below it
+  // come from the blocks)
+  int wm = 2;
+  if (grams && s.gblk[0] >= 0) wm = s.gblk[1] >= 0 ? 4 : 3;
+  const long long lo = grams ? (wm <= dl ? s.glo[wm - 2] : 0) : s.lo;
+  const long long hi = grams ? (wm <= dl ? s.ghi[wm - 2] : 0) : s.hi;
   // the radix selection's first digit (end bits sh_top and up) is counted here
   // too, per length class, so that its first pass needs no walk of the interval
   const int sh_top = snap ? ((64 - __clzll(r.N - 1) + 7) / 8 - 1) * 8 : 0;
   for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
     int l[4];
     long long e[4];
-    hit_lens(r, p0, hi, l, e);
+    hit_lens(r, wm, p0, hi, l, e);
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const long long p = p0 + (long long)j * BO_THREADS;
@@ -515,6 +558,24 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
         atomicAdd(&s.hc[l[j]], 1);
         atomicAdd(&s.v.top[min(l[j], 6) - 2][(e[j] >> sh_top) & 255], 1);
       }
+    }
+  }
+  __syncthreads();
+
+  const int k4 = (k + 3) & ~3;
+  auto gblock = [&](int m) { return cd->gd + (size_t)s.gblk[m - 2] * gd_ints(k); };
+  if (wm > 2 && tid == 0) {
+    // ends of exactly m < wm tokens: the valid ends of the m-gram less those
+    // of the (m + 1)-gram (counted by the walk for m + 1 = wm)
+    int walked = 0;
+    for (int L = wm; L <= dl; ++L) walked += s.hc[L];
+    const int q2 = __ldg(gblock(2) + 2);
+    if (wm == 3) {
+      s.hc[2] = q2 - walked;
+    } else {
+      const int q3 = __ldg(gblock(3) + 2);
+      s.hc[2] = q2 - q3;
+      s.hc[3] = q3 - walked;
     }
   }
   __syncthreads();
@@ -563,7 +624,8 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     if (tid < nc) {
       const int c = MAX_BACKOFF + tid;
       const int room = R - s.cnt[c], xq = s.tot[c] - s.dtot[c];
-      s.mode[tid] = room <= 0 || xq <= 0 ? 0 : (xq <= room ? 1 : 2);
+      // (a length below the walked gram's: its candidate is the gram's block)
+      s.mode[tid] = room <= 0 || xq <= 0 || s.len[c] < wm ? 0 : (xq <= room ? 1 : 2);
       s.need[tid] = min(room, xq);
       s.pref[tid] = 0;
     }
@@ -589,7 +651,7 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
           for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
             long long e[4];
             int l[4];
-            hit_ends(r, s, lo, p0, hi, e, l);
+            hit_ends(r, s, wm, lo, p0, hi, e, l);
 #pragma unroll
             for (int q = 0; q < 4; ++q)
               for (int c = 0; c < nc; ++c)
@@ -637,7 +699,7 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     for (long long p0 = lo + tid; p0 < hi; p0 += 4LL * BO_THREADS) {
       long long e[4];
       int l[4];
-      hit_ends(r, s, lo, p0, hi, e, l);
+      hit_ends(r, s, wm, lo, p0, hi, e, l);
 #pragma unroll
       for (int q = 0; q < 4; ++q)
         for (int c = 0; c < nc; ++c) {
@@ -651,10 +713,32 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
     if (tid < nc) s.cnt[MAX_BACKOFF + tid] = min(R, s.cnt[MAX_BACKOFF + tid]);  // (exactly room or fewer)
     __syncthreads();
   }
+  if (wm > 2 && tid < nc && s.len[MAX_BACKOFF + tid] < wm)  // a block's candidate: its c0 = min(Q, R)
+    s.cnt[MAX_BACKOFF + tid] = __ldg(gblock(s.len[MAX_BACKOFF + tid]));
+  __syncthreads();
 
   // ---- every candidate voted (one warp each), the best score wins ----
   for (int q = warp; q < ns + nc; q += BO_WARPS) {
     const int ci = q < ns ? q : MAX_BACKOFF + (q - ns);
+    if (q >= ns && s.len[ci] < wm) {
+      // the gram's block: its vote to depth k, cut at this candidate's cap
+      // (the vote at a depth never depends on where it will stop)
+      const int32_t *gb = gblock(s.len[ci]);
+      const int len = min(__ldg(gb + 1), bo_cap(a, s.len[ci], n));
+      unsigned part = 0;
+      for (int d = lane; d < len; d += 32) {
+        const int cnt = __ldg(gb + 4 + k4 + d);
+        s.v.d.tok[ci][d] = __ldg(gb + 4 + d);
+        s.v.d.cnt[ci][d] = cnt;
+        part += (unsigned)cnt;
+      }
+      const unsigned sum = __reduce_add_sync(FULL, part);
+      if (lane == 0) {
+        s.dlen[ci] = len;
+        s.dsum[ci] = sum;
+      }
+      continue;
+    }
     bo_vote(a, r, s, ci, q < ns ? 1 : 2, warp, lane);
   }
   __syncthreads();

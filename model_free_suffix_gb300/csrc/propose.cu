@@ -26,6 +26,7 @@
 // match, which leaves the chosen source and its occurrences unchanged.
 #include <climits>
 
+#include "gram_lookup.cuh"
 #include "ingest_cta.cuh"
 #include "row_index.cuh"
 
@@ -729,34 +730,10 @@ __device__ void probe_bounds(const Corpus &c, const int4 &P, int m, int lane, lo
   hi = bU;
 }
 
-// [lo, hi) for the m-gram P from the snapshot's n-gram table, by one warp:
-// lanes 0..7 read a 128-byte bucket (lane 2e and 2e + 1 hold entry e), two
-// ballots find the matching entry; a bucket with an empty entry ends the
-// search (the gram does not begin any suffix).
-__device__ void gram_bounds(const Corpus &c, const int4 &P, int m, int lane, long long &lo,
-                            long long &hi, int &slot7) {
-  const int4 g = make_int4(P.x, m >= 2 ? P.y : KEY_END, m >= 3 ? P.z : KEY_END, m >= 4 ? P.w : KEY_END);
-  uint64_t b = gram_hash(m, g.x, g.y, g.z, g.w) & c.gtm;
-  lo = hi = 0;
-  slot7 = -2;
-  for (uint64_t step = 0; step <= c.gtm; ++step, b = (b + 1) & c.gtm) {
-    int4 v = make_int4(0, 0, 0, 0);
-    if (lane < 2 * GT_BUCKET)
-      v = __ldg(reinterpret_cast<const int4 *>(c.GT + (size_t)b * GT_BUCKET * GT_ENTRY) + lane);
-    const bool even = (lane & 1) == 0 && lane < 2 * GT_BUCKET;
-    const bool odd = (lane & 1) == 1 && lane < 2 * GT_BUCKET;
-    const unsigned e0 = __ballot_sync(FULL, even && v.x == m && v.y == g.x && v.z == g.y && v.w == g.z);
-    const unsigned e1 = __ballot_sync(FULL, odd && v.x == g.w);
-    const unsigned match = e0 & (e1 >> 1);  // bit 2e: entry e holds the gram
-    if (match) {
-      const int src = __ffs(match);          // lane 2e + 1: (t3, lo, hi, [7])
-      lo = __shfl_sync(FULL, v.y, src);
-      hi = __shfl_sync(FULL, v.z, src);
-      slot7 = __shfl_sync(FULL, v.w, src);
-      return;
-    }
-    if (__ballot_sync(FULL, even && v.x == 0)) return;
-  }
+// [lo, hi) for the m-gram P from the snapshot's n-gram table, by one warp.
+__device__ __forceinline__ void gram_bounds(const Corpus &c, const int4 &P, int m, int lane, long long &lo,
+                                            long long &hi, int &slot7) {
+  gt_lookup(c.GT, c.gtm, P, m, lane, lo, hi, slot7);
 }
 
 // The interval of the last m tokens (t[i] = the i-th token from the end),
@@ -1295,19 +1272,18 @@ __device__ void vote_warp(const ProposeArgs &a, const int *cont, int capp, const
       const unsigned bad2 = __ballot_sync(FULL, x2 < cap && !ok2);
       const int F = bad1 ? d + __ffs(bad1) - 1 : (bad2 ? d + 32 + __ffs(bad2) - 1 : cap);
       // emit depths [d, F): the reference's tokens
-      long long part_sum = 0;
+      unsigned part_sum = 0;  // (at most 64 depths of at most 128 each)
       if (x1 < F) {
         dr[x1] = cont[ref * capp + x1];
         if (pr) pr[x1] = (float)c1 / (float)c0;
-        part_sum += c1;
+        part_sum += (unsigned)c1;
       }
       if (x2 < F) {
         dr[x2] = cont[ref * capp + x2];
         if (pr) pr[x2] = (float)c2 / (float)c0;
-        part_sum += c2;
+        part_sum += (unsigned)c2;
       }
-      for (int off = 16; off > 0; off >>= 1) part_sum += __shfl_xor_sync(FULL, part_sum, off);
-      sum += part_sum;
+      sum += (long long)__reduce_add_sync(FULL, part_sum);
       len += F - d;
       if (F >= cap) break;
       // depth F: stop if the reference's majority only missed the threshold

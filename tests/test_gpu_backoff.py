@@ -230,6 +230,54 @@ def test_backoff_edges(V, C, delta, R, k, D, nb, S):
     dr.close()
 
 
+@pytest.mark.parametrize("V,D,nb", [(40, 12, 8), (6, 12, 8), (6, 3, 4), (6, 2, 2), (40, 4, 3), (3, 24, 8)],
+                         ids=["2gram-blocks", "2-3gram-blocks", "blocks-D3", "blocks-D2",
+                              "2gram-blocks-D4", "V3"])
+@pytest.mark.parametrize("gd", [1, 0], ids=["gram-drafts", "no-gram-drafts"])
+def test_backoff_gram_blocks(V, D, nb, gd):
+    """The corpus side from the snapshot's gram draft blocks: with V = 40 the
+    last 2-gram has a block and the 3-gram's interval is walked; with V = 6
+    both have blocks and only the 4-gram's interval is walked (D = 3, 2: no
+    walk at all).  The same rows with blocks off walk the 2-gram's interval;
+    both against the oracle."""
+    W, O, H = _mods()
+    from model_free_suffix_gb300 import SuffixDrafter
+    B, S, C, R, k = 48, 1024, 1 << 16, 16, 8
+    rng = np.random.default_rng(V * 100 + D)
+    dr = SuffixDrafter(max_batch=B, seq_capacity=S, vocab_size=V, k=k, max_tree_depth=D,
+                       max_occurrences=R, min_token_prob=(1, 3), max_spec_offset=1,
+                       corpus_capacity=C, num_backoff=nb, gram_drafts=gd)
+    p = O.Params(S=S, V=V, k=k, D=D, R=R, min_prob=(1, 3), offset=1, num_backoff=nb)
+    ring = O.Ring(C, 65536, V)
+    while ring.live < 3 * C // 4:
+        m = 32
+        lens = rng.integers(20, 400, size=m).astype(np.int32)
+        buf = rng.integers(0, V, size=(m, S)).astype(np.int32)
+        # repeated spans, so that longer matches and their continuations agree
+        for i in range(m):
+            if lens[i] > 60:
+                at = int(rng.integers(0, lens[i] - 40))
+                buf[i, at:at + 24] = buf[(i + 1) % m, 10:34]
+        rows = torch.arange(m, dtype=torch.int32, device="cuda")
+        dr.ingest(torch.from_numpy(buf).cuda(), rows, torch.zeros_like(rows), torch.from_numpy(lens).cuda())
+        ring.ingest(buf, np.arange(m), np.zeros(m), lens)
+    dr.build_sa(torch.cuda.Stream())
+    assert dr.poll(wait=True)[0] == 1
+    X = ring.snapshot()
+    tok = rng.integers(0, V, size=(B, S)).astype(np.int32)
+    n = rng.integers(3, S - 16, size=B).astype(np.int32)
+    n[:3] = [1, 2, 3]
+    for b in range(3, B, 2):  # rows ending in a corpus span
+        d = X[int(rng.integers(0, X.shape[0] - 40)):][:32]
+        if n[b] >= 32 and (d < V).all():
+            tok[b, n[b] - 32:n[b]] = d
+    out = dr.propose(torch.from_numpy(tok).cuda(), torch.from_numpy(n).cuda())
+    torch.cuda.synchronize()
+    H.compare(out, O.propose(p, tok, n, X=X, threads=H.THREADS))
+    assert dr.get_error() == 0
+    dr.close()
+
+
 def test_backoff_full_serving_size_sampled_rows():
     """The serving workload at its full size (B = 256, S = 4096, 1M-token
     corpus, rebuilds), num_backoff = 8 through the step as the benchmark runs
