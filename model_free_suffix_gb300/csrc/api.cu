@@ -484,6 +484,7 @@ int sgd_create(const sgd_config *cfg, int device, sgd_ctx **out) {
     if (e == cudaSuccess) e = cudaEventCreate(&x->ev_b1);
   }
   if (e == cudaSuccess && x->smem > 48 * 1024) e = propose_set_smem_limit(x->smem);
+  if (e == cudaSuccess && cfg->num_backoff > 1) e = backoff_set_smem_limit();
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     const bool oom = e == cudaErrorMemoryAllocation;

@@ -45,6 +45,7 @@ constexpr int BO_WARPS = BO_THREADS / 32;
 constexpr int BO_CANDS = 2 * MAX_BACKOFF;  // row candidates, then corpus candidates
 constexpr int BO_LCACHE = 16384;           // interval hits whose length is kept on chip
 constexpr int BO_TOPC = 5;                 // length classes of the first radix digit
+constexpr int BO_RLCAP = 16384;            // row ends whose match length is kept on chip (dynamic)
 static_assert(BO_LCACHE % (4 * BO_THREADS) == 0, "hit_ends: four hits on one side of the cache end");
 
 struct BoShared {
@@ -121,12 +122,32 @@ __device__ __forceinline__ int y_at(const BoRow &r, long long i) {
   return __ldg(r.ring + (r.ds + i) % r.C);
 }
 
+// The largest L in [l0, lim] with at(j - i) == tail[i] for every i in
+// [l0, L) (at(j - i) is read only for i < lim): eight tokens per round trip,
+// their loads issued together.
+template <class At>
+__device__ __forceinline__ int match_back(const At &at, long long j, int l0, int lim, const int *tail) {
+  int L = l0;
+  while (L < lim) {
+    const int cn = min(8, lim - L);
+    int v[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) v[q] = q < cn ? at(j - L - q) : 0;
+    int f = cn;  // first mismatch in the chunk
+#pragma unroll
+    for (int q = 7; q >= 0; --q)
+      if (q < cn && v[q] != tail[L + q]) f = q;
+    L += f;
+    if (f < cn) break;
+  }
+  return L;
+}
+
 // Row end j (j <= n-2): the longest l <= min(D, j+1) with t[j-i] == t[n-1-i], i < l.
 __device__ __forceinline__ int self_len(const BoRow &r, int j) {
   const int lim = min(r.dl, j + 1);
-  int l = 0;
-  while (l < lim && __ldg(r.row + j - l) == r.tail[l]) ++l;
-  return l;
+  if (lim <= 0 || __ldg(r.row + j) != r.tail[0]) return 0;  // (most ends: one load)
+  return match_back([&](long long p) { return __ldg(r.row + p); }, j, 1, lim, r.tail);
 }
 
 // The lengths of hits p0 + j * BO_THREADS (j < 4; l[j] = -1 past hi) of the
@@ -168,22 +189,17 @@ __device__ __forceinline__ void hit_lens(const BoRow &r, int m, long long p0, lo
   }
 #pragma unroll
   for (int j = 0; j < 4; ++j)
-    if (more[j] && xb[j] == r.tail[m]) {
-      const long long lim = min((long long)r.dl, e[j] + 1);
-      int L = m + 1;
-      while (L < lim && __ldg(r.X + e[j] - L) == r.tail[L]) ++L;
-      l[j] = L;
-    }
+    if (more[j] && xb[j] == r.tail[m])
+      l[j] = match_back([&](long long p) { return __ldg(r.X + p); }, e[j], m + 1,
+                        (int)min((long long)r.dl, e[j] + 1), r.tail);
 }
 
 // Delta end u (u <= dv-2): 0 without a continuation, else its match length
 // within the delta (its first token follows the snapshot's final sentinel).
 __device__ __forceinline__ int delta_len(const BoRow &r, long long u) {
   if (y_at(r, u + 1) == r.Z) return 0;
-  const long long lim = min((long long)r.dl, u + 1);
-  int l = 0;
-  while (l < lim && y_at(r, u - l) == r.tail[l]) ++l;
-  return l;
+  return match_back([&](long long p) { return y_at(r, p); }, u, 0, (int)min((long long)r.dl, u + 1),
+                    r.tail);
 }
 
 // First suffix-array index whose key's first two tokens are >= (upper: >) P,
@@ -292,43 +308,62 @@ __device__ void bo_vote(const ProposeArgs &a, const BoRow &r, BoShared &s, int c
       any |= v[u] >= 0;
     }
     if (!__any_sync(FULL, any)) break;
-    // count each continuation token in a table of MAX_R slots (>= the distinct
-    // tokens, at most c0 <= MAX_R, so an insert always finds its slot)
+    // The first continuing end's token: when more than half of the continuing
+    // ends share it, it is the most frequent (and no other ties it).
+    int np = 0, ref = -1;
 #pragma unroll
     for (int u = 0; u < MAX_R / 32; ++u) {
-      hkey[lane + 32 * u] = -1;
-      hcnt[lane + 32 * u] = 0;
+      const unsigned m = __ballot_sync(FULL, v[u] >= 0);
+      np += __popc(m);
+      const int t = __shfl_sync(FULL, v[u], m ? __ffs(m) - 1 : 0);
+      if (ref < 0 && m) ref = t;
     }
-    __syncwarp();
-    int hs[MAX_R / 32];
+    int nref = 0;
 #pragma unroll
-    for (int u = 0; u < MAX_R / 32; ++u) {
-      hs[u] = -1;
-      if (v[u] < 0) continue;
-      static_assert(MAX_R == 128, "the slot hash takes 7 bits");
-      unsigned h = ((unsigned)v[u] * 2654435761u) >> 25;
-      for (;;) {
-        const int prev = atomicCAS(&hkey[h], -1, v[u]);
-        if (prev == -1 || prev == v[u]) break;
-        h = (h + 1) & (MAX_R - 1);
+    for (int u = 0; u < MAX_R / 32; ++u) nref += __popc(__ballot_sync(FULL, v[u] == ref));
+    int bc, bt;
+    if (2 * nref > np) {
+      bc = nref;
+      bt = ref;
+    } else {
+      // count each continuation token in a table of MAX_R slots (>= the
+      // distinct tokens, at most c0 <= MAX_R, so an insert always finds its slot)
+#pragma unroll
+      for (int u = 0; u < MAX_R / 32; ++u) {
+        hkey[lane + 32 * u] = -1;
+        hcnt[lane + 32 * u] = 0;
       }
-      atomicAdd(&hcnt[h], 1);
-      hs[u] = (int)h;
-    }
-    __syncwarp();
-    int best = 0, cu[MAX_R / 32];
+      __syncwarp();
+      int hs[MAX_R / 32];
 #pragma unroll
-    for (int u = 0; u < MAX_R / 32; ++u) {
-      cu[u] = hs[u] >= 0 ? hcnt[hs[u]] : 0;
-      best = max(best, cu[u]);
-    }
-    const int bc = (int)__reduce_max_sync(FULL, (unsigned)best);
-    unsigned mine = UINT_MAX;
+      for (int u = 0; u < MAX_R / 32; ++u) {
+        hs[u] = -1;
+        if (v[u] < 0) continue;
+        static_assert(MAX_R == 128, "the slot hash takes 7 bits");
+        unsigned h = ((unsigned)v[u] * 2654435761u) >> 25;
+        for (;;) {
+          const int prev = atomicCAS(&hkey[h], -1, v[u]);
+          if (prev == -1 || prev == v[u]) break;
+          h = (h + 1) & (MAX_R - 1);
+        }
+        atomicAdd(&hcnt[h], 1);
+        hs[u] = (int)h;
+      }
+      __syncwarp();
+      int best = 0, cu[MAX_R / 32];
 #pragma unroll
-    for (int u = 0; u < MAX_R / 32; ++u)
-      if (v[u] >= 0 && cu[u] == bc) mine = min(mine, (unsigned)v[u]);
-    const int bt = (int)__reduce_min_sync(FULL, mine);
-    __syncwarp();  // every lane done reading the table before the next depth clears it
+      for (int u = 0; u < MAX_R / 32; ++u) {
+        cu[u] = hs[u] >= 0 ? hcnt[hs[u]] : 0;
+        best = max(best, cu[u]);
+      }
+      bc = (int)__reduce_max_sync(FULL, (unsigned)best);
+      unsigned mine = UINT_MAX;
+#pragma unroll
+      for (int u = 0; u < MAX_R / 32; ++u)
+        if (v[u] >= 0 && cu[u] == bc) mine = min(mine, (unsigned)v[u]);
+      bt = (int)__reduce_min_sync(FULL, mine);
+      __syncwarp();  // every lane done reading the table before the next depth clears it
+    }
     if (!a.fixed && (long long)bc * a.pD < a.pN * (long long)c0) break;
     if (lane == 0) {
       s.v.d.tok[ci][d] = bt;
@@ -399,11 +434,15 @@ __device__ bool bo_collect(BoShared &s, int off, int ncand, const int *target, i
   return __syncthreads_and(full) != 0;
 }
 
-__global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a) {
+__global__ void __launch_bounds__(BO_THREADS, 2) backoff_kernel(const ProposeArgs a) {
   __shared__ BoShared s;
+  // the match lengths of row ends j < rlc (byte j), from the length pass, for
+  // the backward scan that collects the row's candidates
+  extern __shared__ unsigned char s_rl[];
   const int b = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.S, D = a.D, R = a.R, k = a.k, nb = a.nb;
+  const int rlc = min(S, BO_RLCAP);
   const int32_t *row = a.tok + (size_t)b * S;
   const CorpusDesc *cd = a.desc;
   if (tid == 0) {
@@ -496,11 +535,15 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
       x[q] = j <= n - 2 ? __ldg(row + j) : -1;
     }
 #pragma unroll
-    for (int q = 0; q < 4; ++q)
+    for (int q = 0; q < 4; ++q) {
+      const int j = j0 + q * BO_THREADS;
+      int l = 0;
       if (x[q] == s.tail[0]) {
-        const int l = self_len(r, j0 + q * BO_THREADS);
+        l = self_len(r, j);
         atomicAdd(&s.hs[l], 1);
       }
+      if (j <= n - 2 && j < rlc) s_rl[j] = (unsigned char)l;
+    }
   }
   // The delta in 128-token windows of the ring (window w holds Y indices
   // [w * WIN - off, w * WIN - off + WIN)); an end matching >= 2 tokens ends
@@ -597,7 +640,8 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
   if (ns > 0)
     for (int base = n - 2; base >= 0; base -= BO_THREADS) {
       const int j = base - tid;
-      if (bo_collect(s, 0, ns, s.tot, j >= 0 ? self_len(r, j) : 0, j, R, tid, warp, lane)) break;
+      const int l = j < 0 ? 0 : (j < rlc ? (int)s_rl[j] : self_len(r, j));
+      if (bo_collect(s, 0, ns, s.tot, l, j, R, tid, warp, lane)) break;
     }
   // ---- the corpus's: the delta's ends first (the most recent), then the snapshot's ----
   if (nc > 0 && delta) {
@@ -775,9 +819,21 @@ __global__ void __launch_bounds__(BO_THREADS) backoff_kernel(const ProposeArgs a
 
 }  // namespace
 
+cudaError_t backoff_set_smem_limit() {
+  // (and the largest shared memory carveout: two CTAs per SM, one launch for
+  // every row of a batch of up to two per SM)
+  cudaError_t e = cudaFuncSetAttribute((const void *)backoff_kernel,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, BO_RLCAP);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute((const void *)backoff_kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
+  return e;
+}
+
 cudaError_t launch_backoff(const ProposeArgs &a, cudaStream_t st) {
   if (a.B <= 0) return cudaSuccess;
-  backoff_kernel<<<a.B, BO_THREADS, 0, st>>>(a);
+  const size_t dyn = (size_t)((min(a.S, BO_RLCAP) + 15) & ~15);
+  backoff_kernel<<<a.B, BO_THREADS, dyn, st>>>(a);
   return cudaGetLastError();
 }
 

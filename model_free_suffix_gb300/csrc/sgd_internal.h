@@ -203,6 +203,7 @@ cudaError_t propose_set_smem_limit(size_t bytes);
 // backoff.cu: multi-length backoff drafting of rows [0, B), one CTA per row
 // (no update: the caller launches it first)
 cudaError_t launch_backoff(const ProposeArgs &a, cudaStream_t st);
+cudaError_t backoff_set_smem_limit();  // the backoff kernel's dynamic shared memory (its row-length cache)
 
 // corpus.cu
 struct IngestScratch {
