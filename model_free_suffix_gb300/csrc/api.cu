@@ -599,14 +599,7 @@ static int propose_impl(sgd_ctx *x, int32_t *token_ids, int32_t *num_tokens, con
   a.score = score;
   a.probs = probs;
   a.match_info = match_info;
-  if (a.nb > 1) {  // multi-length backoff: the update, then the backoff kernel
-    if (a.do_update) {
-      x->launches++;
-      const int r = check_cuda(launch_update(token_ids, num_tokens, sampled, B, T,
-                                             x->cfg.seq_capacity, x->cfg.vocab_size, x->d_err,
-                                             x->ri, (cudaStream_t)stream));
-      if (r != SGD_OK) return r;
-    }
+  if (a.nb > 1) {  // multi-length backoff: one kernel, the update included
     x->launches++;
     return check_cuda(launch_backoff(a, (cudaStream_t)stream));
   }

@@ -35,6 +35,7 @@
 
 #include "delta_sig.cuh"
 #include "gram_lookup.cuh"
+#include "update_row.cuh"
 
 namespace sgd {
 
@@ -144,10 +145,11 @@ __device__ __forceinline__ int match_back(const At &at, long long j, int l0, int
 }
 
 // Row end j (j <= n-2): the longest l <= min(D, j+1) with t[j-i] == t[n-1-i], i < l.
+// (The row is read with ordinary loads: this kernel appends the step's ids.)
 __device__ __forceinline__ int self_len(const BoRow &r, int j) {
   const int lim = min(r.dl, j + 1);
-  if (lim <= 0 || __ldg(r.row + j) != r.tail[0]) return 0;  // (most ends: one load)
-  return match_back([&](long long p) { return __ldg(r.row + p); }, j, 1, lim, r.tail);
+  if (lim <= 0 || r.row[j] != r.tail[0]) return 0;  // (most ends: one load)
+  return match_back([&](long long p) { return r.row[p]; }, j, 1, lim, r.tail);
 }
 
 // The lengths of hits p0 + j * BO_THREADS (j < 4; l[j] = -1 past hi) of the
@@ -257,7 +259,7 @@ __device__ int pick_lengths(const int *h, int top, int minlen, int nb, int *len,
 __device__ __forceinline__ int bo_cont(const BoRow &r, int src, int o, int d) {
   if (src == 1) {
     const int q = o + 1 + d;
-    return q <= r.n - 1 ? __ldg(r.row + q) : -1;
+    return q <= r.n - 1 ? r.row[q] : -1;
   }
   if (o >= 0) {
     const long long q = (long long)o + 1 + d;
@@ -443,25 +445,45 @@ __global__ void __launch_bounds__(BO_THREADS, 2) backoff_kernel(const ProposeArg
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int S = a.S, D = a.D, R = a.R, k = a.k, nb = a.nb;
   const int rlc = min(S, BO_RLCAP);
-  const int32_t *row = a.tok + (size_t)b * S;
+  int32_t *row = a.tok + (size_t)b * S;
   const CorpusDesc *cd = a.desc;
-  if (tid == 0) {
+  if (warp == 0) {
+    // the step's update (with sampled ids): the accepted ids appended to the
+    // row; the tail (the last D tokens, newest first) is the appended ids
+    // followed by the row's old last tokens, read before the update
     int n = a.ntok[b];
     uint32_t fl = 0;
     if (n < 0) { n = 0; fl |= SGD_ERR_NUM_TOKENS; }
     if (n > S) { n = S; fl |= SGD_ERR_NUM_TOKENS; }
-    if (fl) atomicOr(a.err, fl);
-    s.n = n;
-    s.ds = 0;
-    s.dv = 0;
-    if (a.dcap > 0 && cd != nullptr) {  // the docs placed since the snapshot was linearised
-      const DeltaView v = delta_view(*a.rs, cd->lin_pushed, cd->lin_wp, a.C, a.doc_start);
-      s.ds = v.start;
-      s.dv = (int)min(v.len, a.dcap);
+    const int n_old = n, dl0 = min(D, n_old);
+    int ot[MAX_D / 32];
+#pragma unroll
+    for (int u = 0; u < MAX_D / 32; ++u) {
+      const int i = lane + 32 * u;
+      ot[u] = i < dl0 ? row[n_old - 1 - i] : 0;
     }
-    s.lo = 0;
-    s.hi = 0;
-    s.win = -1;
+    if (a.do_update) n = update_row_warp(row, n, a.sampled + (size_t)b * a.T, a.T, S, a.V, lane, fl, s.tail, D);
+    const int ca = n - n_old, dl1 = min(D, n);
+#pragma unroll
+    for (int u = 0; u < MAX_D / 32; ++u) {
+      const int i = lane + 32 * u;
+      if (i < dl0 && i + ca < dl1) s.tail[i + ca] = ot[u];
+    }
+    if (lane == 0) {
+      if (a.do_update) a.ntok[b] = n;
+      if (fl) atomicOr(a.err, fl);
+      s.n = n;
+      s.ds = 0;
+      s.dv = 0;
+      if (a.dcap > 0 && cd != nullptr) {  // the docs placed since the snapshot was linearised
+        const DeltaView v = delta_view(*a.rs, cd->lin_pushed, cd->lin_wp, a.C, a.doc_start);
+        s.ds = v.start;
+        s.dv = (int)min(v.len, a.dcap);
+      }
+      s.lo = 0;
+      s.hi = 0;
+      s.win = -1;
+    }
   }
   for (int i = tid; i <= MAX_D; i += BO_THREADS) {
     s.hs[i] = 0;
@@ -486,7 +508,6 @@ __global__ void __launch_bounds__(BO_THREADS, 2) backoff_kernel(const ProposeArg
     return;
   }
   const int dl = min(D, n);
-  for (int i = tid; i < dl; i += BO_THREADS) s.tail[i] = __ldg(row + n - 1 - i);
   BoRow r;
   r.row = row;
   r.n = n;
@@ -532,7 +553,7 @@ __global__ void __launch_bounds__(BO_THREADS, 2) backoff_kernel(const ProposeArg
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
       const int j = j0 + q * BO_THREADS;
-      x[q] = j <= n - 2 ? __ldg(row + j) : -1;
+      x[q] = j <= n - 2 ? row[j] : -1;
     }
 #pragma unroll
     for (int q = 0; q < 4; ++q) {
