@@ -425,8 +425,8 @@ def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=
         res["row_stats"] = row
         res["bytes_per_step"] = {"lower_bound": int(lower), "with_scans_and_gathers": full}
     if backoff > 1:
-        res["roofline"] = roofline("backoff_kernel (with the update and ingest launches of the "
-                                   "step)", lower, "backoff_kernel")
+        res["roofline"] = roofline("backoff_kernel (the update included; with the ingest launch of "
+                                   "the step)", lower, "backoff_kernel")
     elif delta:
         dv = float(np.mean(state["delta_tok"][Wm:Wm + K]))
         res["mean_delta_tokens"] = round(dv, 1)
