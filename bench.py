@@ -335,12 +335,17 @@ def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=
         if cold:
             flush.fill_(i)
 
-    def policy(i):
-        """Host side of the step: rebuild policy and the swap poll."""
+    def account(i):
+        """The trace's bookkeeping for step i (host only, before its events):
+        the docs it ingests count toward the rebuild policy."""
         state["delta_tok"].append(min(delta, state["since_front"]))  # what this step's rows scanned
         state["ingested"] += fin[i][3]
         state["since_front"] += ring_tok[i]
         state["since_pending"] += ring_tok[i]
+
+    def policy(i):
+        """The step's library calls after its launch: the rebuild policy and the
+        swap poll (a swap launches on the step's stream, inside its events)."""
         if cfg.corpus_tokens:
             if not state["pending"] and state["ingested"] >= cfg.rebuild_tokens:
                 dr.build_sa(side, stream=stream)
@@ -348,15 +353,17 @@ def serve_loop(args, rank, world, cfg_name="c3", delta=0, backoff=1, K=None, Wm=
                 state["ingested"] = 0
                 state["since_pending"] = 0
                 state["builds"] += 1
-            st, _ = dr.poll(wait=False, stream=stream)
-            if st == 1:
-                state["pending"] = False
-                state["swaps"] += 1
-                state["since_front"] = state["since_pending"]
-                state["build_stats"].append(dr.build_stats())
+            if state["pending"]:  # (nothing to poll for otherwise)
+                st, _ = dr.poll(wait=False, stream=stream)
+                if st == 1:
+                    state["pending"] = False
+                    state["swaps"] += 1
+                    state["since_front"] = state["since_pending"]
+                    state["build_stats"].append(dr.build_stats())
 
     def one_step(i, ev=None, cold=True, collect=False):
         stage(i, cold)
+        account(i)
         if ev:
             ev[0].record(stream)
         g_step.replay()
