@@ -154,9 +154,13 @@ typedef struct {
                                   scores: the longer length, then the row), whatever
                                   select_by_score says.  The match lengths are exact
                                   (every row end, every corpus end matching the last two
-                                  tokens, every delta position), so this mode costs one
-                                  more launch per step and a scan of the whole
-                                  suffix-array interval of the row's last two tokens. */
+                                  tokens, every delta position): this mode runs its own
+                                  kernel (the update included, one launch like the
+                                  default; a step's ingest is a second launch), which
+                                  scans the row and the suffix-array interval of the
+                                  shortest of the row's last 2-, 3-, 4-gram that has no
+                                  gram draft block (gram_drafts; without them, or with
+                                  delta ends, that of the last two tokens). */
   int32_t  row_index;          /* 0 (default): each step scans every row's valid tokens
                                   for its own match.  1: each row also keeps a bigram
                                   position index on the device (the per-request
