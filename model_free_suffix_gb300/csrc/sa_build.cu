@@ -161,7 +161,7 @@ __global__ void __launch_bounds__(256) k_round_keys(const int32_t *act, const ui
 // its items in shared memory in digit order so that consecutive threads
 // write consecutive outputs.  Look-back words: epoch (bits 63..34, the
 // build's pass number), flag (33..32: 1 aggregate, 2 inclusive), count.
-__global__ void __launch_bounds__(OS_THREADS) k_onesweep(const uint64_t *kin, const int32_t *vin,
+__global__ void __launch_bounds__(OS_THREADS, 4) k_onesweep(const uint64_t *kin, const int32_t *vin,
                                                          uint64_t *kout, int32_t *vout, long long n,
                                                          int shift, const uint32_t *hist_d,
                                                          unsigned long long *status, uint32_t *ticket,
@@ -480,6 +480,11 @@ cudaError_t sa_scratch_alloc(SaScratch *s, int64_t cap) {
   s->owned = base;
   e = cudaMallocHost((void **)&s->h_pinned, 64);
   if (e == cudaSuccess) e = cudaMallocHost((void **)&s->h_hist, 8 * RADIX * 4);
+  // four radix-pass CTAs per SM (64 registers, 36 KB of shared memory each):
+  // the largest shared-memory carveout
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute((const void *)k_onesweep, cudaFuncAttributePreferredSharedMemoryCarveout,
+                             (int)cudaSharedmemCarveoutMaxShared);
   if (e != cudaSuccess) sa_scratch_free(s);
   return e;
 }
