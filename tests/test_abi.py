@@ -34,6 +34,8 @@ def test_config_defaults(lib):
     assert c.delta_capacity == 0  # newly ingested docs wait for the next swap
     assert c.draft_mode == 0      # drafts stop at the probability floor and the factor cap
     assert c.num_backoff == 1     # one candidate length per path: the longest match
+    assert c.row_index == 0       # rows scanned each step unless the caller opts in
+    assert c.gram_drafts == 1     # frequent 2/3-gram votes built with each snapshot
 
 
 def test_config_set_float_rationals(lib):
@@ -64,13 +66,25 @@ def test_create_rejects_bad_knobs_before_touching_the_gpu(lib):
     bad = [("seq_capacity", 4098), ("k", 0), ("k", 65), ("max_tree_depth", 129),
            ("max_occurrences", 0), ("corpus_cand_cap", 100), ("corpus_cand_cap", 32),
            ("min_prob_den", 0), ("self_warps", 17), ("draft_mode", 2), ("draft_mode", -1),
-           ("select_by_score", 2), ("num_backoff", 0), ("num_backoff", 9)]
+           ("select_by_score", 2), ("num_backoff", 0), ("num_backoff", 9), ("row_index", 2),
+           ("row_index", -1), ("gram_drafts", 2), ("gram_drafts", -1)]
     for field, val in bad:
         c = lib.SgdConfig()
         L.sgd_config_default(ctypes.byref(c))
         setattr(c, field, val)
         h = ctypes.c_void_p()
         assert L.sgd_create(ctypes.byref(c), 0, ctypes.byref(h)) == lib.SGD_EINVAL, field
+    # row indexes: not with the two-launch mode, a delta, score-ranked selection,
+    # backoff (they need every end's length) or ids of 2^24 and more
+    for over in [dict(propose_mode=2), dict(delta_capacity=1024), dict(select_by_score=1),
+                 dict(num_backoff=2), dict(vocab_size=(1 << 24) + 1)]:
+        c = lib.SgdConfig()
+        L.sgd_config_default(ctypes.byref(c))
+        c.row_index = 1
+        for f, v in over.items():
+            setattr(c, f, v)
+        h = ctypes.c_void_p()
+        assert L.sgd_create(ctypes.byref(c), 0, ctypes.byref(h)) == lib.SGD_EINVAL, over
     # the delta: within the ring, and the ring a whole number of 128-token windows
     for cap, dcap in [(1 << 20, -1), (1 << 20, (1 << 20) + 1), (1000, 64), (0, 128)]:
         c = lib.SgdConfig()
