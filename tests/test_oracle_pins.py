@@ -373,6 +373,36 @@ def test_invariants_random_rows(orc):
             assert ("," + ",".join(map(str, W)) + ",") in s
 
 
+def test_vote_is_a_prefix_whatever_the_cap(orc):
+    """The vote at a depth never depends on where it will stop: with the cap
+    set by the offset alone (factor 0), a smaller cap gives a prefix of a
+    larger cap's draft with the same probabilities, and num_valid =
+    min(cap, the larger cap's num_valid).  (This is what lets a precomputed
+    depth-k vote of a gram serve every row whose candidate it is, cut at the
+    row's own cap.)"""
+    rng = np.random.default_rng(23)
+    for _ in range(150):
+        V = int(rng.integers(2, 6))
+        n = int(rng.integers(2, 60))
+        t = rng.integers(0, V, size=n).astype(np.int32)
+        X = None
+        if rng.random() < 0.6:
+            X = rng.integers(0, V + 1, size=int(rng.integers(10, 120))).astype(np.int32)
+            X[-1] = V
+        k = int(rng.integers(2, 12))
+        kw = dict(S=n + 40, V=V, k=k, D=int(rng.integers(2, 10)), R=int(rng.integers(1, 9)),
+                  factor=(0, 1), min_prob=(1, int(rng.integers(2, 6))))
+        full = orc.propose_row(orc.Params(offset=k, **kw), t, n, X=X)
+        for cap in range(k + 1):
+            r = orc.propose_row(orc.Params(offset=cap, **kw), t, n, X=X)
+            L = r.num_valid
+            assert L == min(cap, full.num_valid), (cap, L, full.num_valid)
+            assert r.drafts[:L].tolist() == full.drafts[:L].tolist()
+            assert np.array_equal(r.probs[:L].view(np.uint32), full.probs[:L].view(np.uint32))
+            if L:
+                assert r.match_info.tolist() == full.match_info.tolist()
+
+
 # --------------------------------------------------------------------------
 # delta (docs placed after the snapshot was taken, not yet indexed)
 
